@@ -1,0 +1,175 @@
+"""Plain float64 CPU oracle for the speculative-decoding verify step.
+
+TEST INFRASTRUCTURE ONLY.  The test suite, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline / reference arm may import this package; the product
+path (the CUDA library and its binding) never does, and shares no code with it.
+
+The arithmetic lives in ``oracle.c`` (plain C, float64, OpenMP over sequences);
+this module only builds it with gcc and marshals numpy arrays through ctypes.
+``enumerate_exact`` (in ``exact.py``) adds the exact-enumeration checks.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from dataclasses import dataclass
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = os.path.join(HERE, "oracle.c")
+LIB = os.path.join(HERE, "liboracle.so")
+
+SAMPLE, GREEDY, SAMPLE_BUGGY = 0, 1, 2
+F_BAD, F_DEGENERATE, F_OVERFLOW = 1, 2, 4
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``liboracle.so`` next to its source (gcc, -O2, OpenMP, no FMA contraction)."""
+    if (not force and os.path.exists(LIB)
+            and os.path.getmtime(LIB) >= max(os.path.getmtime(SRC),
+                                             os.path.getmtime(os.path.join(HERE, "oracle.h")))):
+        return LIB
+    tmp = LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
+           "-fno-fast-math", "-Wall", "-o", tmp, SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, LIB)
+    return LIB
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    build()
+    lib = ctypes.CDLL(LIB)
+    P = ctypes.c_void_p
+    lib.orc_row_stats.argtypes = [P, ctypes.c_double, ctypes.c_int, P, P, P]
+    lib.orc_row_stats.restype = ctypes.c_int
+    lib.orc_draw_cdf.argtypes = [P, P, ctypes.c_double, ctypes.c_int, P]
+    lib.orc_draw_cdf.restype = ctypes.c_int
+    lib.orc_verify_seq.argtypes = [ctypes.c_int, P, P, P, P, ctypes.c_double, ctypes.c_double,
+                                   ctypes.c_int, ctypes.c_int, P, P, P, P, P, P]
+    lib.orc_verify_seq.restype = None
+    lib.orc_verify_batch.argtypes = [ctypes.c_int, P, ctypes.c_int, P, P, P, P, ctypes.c_float,
+                                     ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P,
+                                     P, P, P, P, P, P, P, P, P, ctypes.c_int]
+    lib.orc_verify_batch.restype = ctypes.c_int
+    lib.orc_max_threads.argtypes = []
+    lib.orc_max_threads.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def max_threads() -> int:
+    return int(_load().orc_max_threads())
+
+
+def row_stats(l, T: float = 1.0):
+    """(m, S, argmax, bad) of one float64 row."""
+    l = np.ascontiguousarray(l, dtype=np.float64)
+    m = np.zeros(1)
+    S = np.zeros(1)
+    am = np.zeros(1, dtype=np.int32)
+    bad = _load().orc_row_stats(_ptr(l), float(T), l.size, _ptr(m), _ptr(S), _ptr(am))
+    return float(m[0]), float(S[0]), int(am[0]), bool(bad)
+
+
+def draw_cdf(l, q=None, T: float = 1.0):
+    """Normalised cumulative boundaries C_j / C_{V-1} of the draw weights of one row."""
+    l = np.ascontiguousarray(l, dtype=np.float64)
+    qq = None if q is None else np.ascontiguousarray(q, dtype=np.float64)
+    cdf = np.zeros(l.size)
+    rc = _load().orc_draw_cdf(_ptr(l), _ptr(qq), float(T), l.size, _ptr(cdf))
+    return None if rc else cdf
+
+
+@dataclass
+class SeqResult:
+    out: np.ndarray
+    n: int
+    thr: np.ndarray
+    draw_lo: float
+    draw_hi: float
+    flags: int
+
+
+def verify_seq(mode, logits, q, x, ua, ur, T) -> SeqResult:
+    """One sequence with float64 inputs: logits [k+1,V], q [k,V], x [k], ua [k], ur."""
+    logits = np.ascontiguousarray(logits, dtype=np.float64)
+    k1, V = logits.shape
+    k = k1 - 1
+    x = np.ascontiguousarray(x, dtype=np.int32)
+    qq = None if q is None else np.ascontiguousarray(q, dtype=np.float64)
+    uu = None if ua is None else np.ascontiguousarray(ua, dtype=np.float64)
+    out = np.zeros(k + 1, dtype=np.int32)
+    n = np.zeros(1, dtype=np.int32)
+    thr = np.zeros(k)
+    lo = np.zeros(1)
+    hi = np.zeros(1)
+    fl = np.zeros(1, dtype=np.int32)
+    _load().orc_verify_seq(int(mode), _ptr(logits), _ptr(qq), _ptr(x), _ptr(uu),
+                           float(0.0 if ur is None else ur), float(T), k, V, _ptr(out),
+                           _ptr(n), _ptr(thr), _ptr(lo), _ptr(hi), _ptr(fl))
+    return SeqResult(out, int(n[0]), thr, float(lo[0]), float(hi[0]), int(fl[0]))
+
+
+@dataclass
+class BatchResult:
+    out: np.ndarray        # [B, k+1] int32
+    n: np.ndarray          # [B] int32
+    row_m: np.ndarray      # [B, k+1] max_j l_j / T
+    row_S: np.ndarray      # [B, k+1] sum_j exp(l_j/T - m)
+    row_argmax: np.ndarray  # [B, k+1]
+    row_px: np.ndarray     # [B, k+1] p_i(x_i) (NaN on row k)
+    row_qx: np.ndarray     # [B, k+1] q_i(x_i) (NaN on row k)
+    thr: np.ndarray        # [B, k] min(1, P/Q) at judged positions, NaN elsewhere
+    draw_lo: np.ndarray    # [B]
+    draw_hi: np.ndarray    # [B]
+    flags: np.ndarray      # [B]
+
+
+def verify_batch(mode, logits, dtype: str, q, x, ua, ur, T, nthreads: int = 0) -> BatchResult:
+    """Batch verify over inputs in the device layouts.
+
+    logits: [B, k+1, V] uint16 bf16 bit patterns (dtype "bf16") or float32 ("f32");
+    q: [B, k, V] float32 or None (greedy); x: [B, k] int32; ua: [B, k] float32;
+    ur: [B] float32.
+    """
+    B, k1, V = logits.shape
+    k = k1 - 1
+    if dtype == "bf16":
+        logits = np.ascontiguousarray(logits, dtype=np.uint16)
+        dt = 0
+    elif dtype == "f32":
+        logits = np.ascontiguousarray(logits, dtype=np.float32)
+        dt = 1
+    else:
+        raise ValueError(dtype)
+    greedy = mode == GREEDY
+    qq = None if greedy else np.ascontiguousarray(q, dtype=np.float32)
+    x = np.ascontiguousarray(x, dtype=np.int32)
+    uu = None if greedy else np.ascontiguousarray(ua, dtype=np.float32)
+    rr = None if greedy else np.ascontiguousarray(ur, dtype=np.float32)
+    r = BatchResult(
+        out=np.zeros((B, k + 1), np.int32), n=np.zeros(B, np.int32),
+        row_m=np.zeros((B, k + 1)), row_S=np.zeros((B, k + 1)),
+        row_argmax=np.zeros((B, k + 1), np.int32), row_px=np.zeros((B, k + 1)),
+        row_qx=np.zeros((B, k + 1)), thr=np.zeros((B, k)), draw_lo=np.zeros(B),
+        draw_hi=np.zeros(B), flags=np.zeros(B, np.int32))
+    rc = _load().orc_verify_batch(
+        int(mode), _ptr(logits), dt, _ptr(qq), _ptr(x), _ptr(uu), _ptr(rr), float(T), B, k, V,
+        _ptr(r.out), _ptr(r.n), _ptr(r.row_m), _ptr(r.row_S), _ptr(r.row_argmax),
+        _ptr(r.row_px), _ptr(r.row_qx), _ptr(r.thr), _ptr(r.draw_lo), _ptr(r.draw_hi),
+        _ptr(r.flags), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    return r

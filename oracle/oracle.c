@@ -1,0 +1,332 @@
+/*
+ * Plain float64 CPU oracle for the speculative-decoding verify step.
+ *
+ * TEST INFRASTRUCTURE ONLY: used by the test suite, the smoke check and the
+ * benchmark's CPU-baseline / reference arm, never by the product path.  It is
+ * written straight from the method's definition, one step at a time, with no
+ * blocking, fusion or reordering, so that it can be checked by eye:
+ *
+ *   1. p_i = softmax(l_i / T) for every one of the k+1 target rows
+ *      ([DEE] §"O ciclo de rascunho e verificação"; [SD15] §"Why the result is
+ *      exactly the target model", the accept_sampled signature).
+ *   2. Judge the drafts left to right; accept x_i with probability
+ *      min(1, p_i(x_i) / q_i(x_i)), i.e. accept iff p >= q or u < p/q
+ *      ([DEE] §"A regra de amostragem por rejeição", rule 1; [SDF] §"El mecanismo
+ *      desnudo", paso 3).  Stop at the first rejection.
+ *   3. At a rejection draw from norm(max(0, p - q)); if all k survive draw a bonus
+ *      token from p_k ([DEE] same section, rules 2 and 3; [SDF] paso 3).
+ *   4. The categorical draw takes the first j whose running sum C_j exceeds
+ *      u * C_{V-1} ([DEE] §"Amostragem especulativa em numpy, com prova": the
+ *      sampler is a right-sided search of the cumulative sum).
+ *   5. Greedy: accept while the draft equals argmax p, emit argmax at the first
+ *      mismatch or for the bonus ([DEE] §"A regra de amostragem por rejeição",
+ *      greedy paragraph; [SD15] §"Why the result is exactly the target model").
+ *   6. num_accepted = n is the KV-cache length to keep ([DEE] §"O ciclo de
+ *      rascunho e verificação", bookkeeping paragraph).
+ *
+ * Readings where the pages are silent (each also listed in the design notes):
+ *   - an exact tie u == p/q rejects (strict "<", as in the page's sampler);
+ *   - p >= q always accepts, which also covers q(x) == 0;
+ *   - one uniform u_resample per sequence serves whichever single draw happens;
+ *   - a rejected row whose residual has zero total mass draws from p instead;
+ *   - a draw that runs past the last bin clamps to the last positive bin;
+ *   - argmax ties go to the lowest index; positions after the draw are -1;
+ *   - invalid data on a row or token the scan reaches marks the sequence invalid
+ *     (num_accepted = -1, out all -1).
+ *
+ * Built with -ffp-contract=off so no multiply-add is fused and x86 / Arm builds
+ * round identically.
+ */
+#include "oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+int orc_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* Step 1: row statistics.  m = max_j l_j/T, S = sum_j exp(l_j/T - m), summed in
+ * index order with Neumaier's compensation. */
+int orc_row_stats(const double* l, double T, int V, double* m_out, double* S_out,
+                  int32_t* argmax_out) {
+    int bad = 0;
+    int amax = -1;
+    double lmax = -INFINITY;
+    for (int j = 0; j < V; ++j) {
+        double v = l[j];
+        if (isnan(v) || v == INFINITY) bad = 1;
+        if (v > lmax) { /* strict: the first (lowest) index of the maximum wins */
+            lmax = v;
+            amax = j;
+        }
+    }
+    if (amax < 0) bad = 1; /* every entry -inf (or V == 0) */
+    if (argmax_out) *argmax_out = amax < 0 ? 0 : amax;
+    double m = lmax / T;
+    double s = 0.0, c = 0.0;
+    if (!bad) {
+        for (int j = 0; j < V; ++j) {
+            double e = exp(l[j] / T - m);
+            double t = s + e;
+            if (fabs(s) >= fabs(e)) c += (s - t) + e;
+            else c += (e - t) + s;
+            s = t;
+        }
+    }
+    if (m_out) *m_out = m;
+    if (S_out) *S_out = s + c;
+    return bad;
+}
+
+/* p_j of a row from its statistics. */
+static double row_p(const double* l, double T, double m, double S, int j) {
+    return exp(l[j] / T - m) / S;
+}
+
+/* Weights of the draw at one row: the residual max(0, p - q) or p itself. */
+static void draw_weights(const double* l, const double* q, double T, double m, double S,
+                         int V, double* w) {
+    for (int j = 0; j < V; ++j) {
+        double p = row_p(l, T, m, S, j);
+        if (q) w[j] = (p > q[j]) ? p - q[j] : 0.0;
+        else w[j] = p;
+    }
+}
+
+/* Step 4: first j with C_j > u * C_{V-1}, C_j the running sum in index order. */
+static int categorical(const double* w, int V, double u, double* lo, double* hi,
+                       int* overflow) {
+    double C = 0.0;
+    for (int j = 0; j < V; ++j) C += w[j];
+    double Ctot = C;
+    double tau = u * Ctot;
+    double prev = 0.0;
+    C = 0.0;
+    for (int j = 0; j < V; ++j) {
+        C += w[j];
+        if (C > tau) {
+            *lo = prev / Ctot;
+            *hi = C / Ctot;
+            *overflow = 0;
+            return j;
+        }
+        prev = C;
+    }
+    /* Rounding pushed tau past the last boundary: clamp to the last positive bin. */
+    *overflow = 1;
+    int last = V - 1;
+    while (last > 0 && !(w[last] > 0.0)) --last;
+    C = 0.0;
+    prev = 0.0;
+    for (int j = 0; j <= last; ++j) {
+        prev = C;
+        C += w[j];
+    }
+    *lo = prev / Ctot;
+    *hi = C / Ctot;
+    return last;
+}
+
+int orc_draw_cdf(const double* l, const double* q, double T, int V, double* cdf) {
+    double m, S;
+    int32_t am;
+    if (orc_row_stats(l, T, V, &m, &S, &am)) return 1;
+    double* w = (double*)malloc(sizeof(double) * (size_t)V);
+    draw_weights(l, q, T, m, S, V, w);
+    double C = 0.0;
+    for (int j = 0; j < V; ++j) C += w[j];
+    double Ctot = C;
+    if (!(Ctot > 0.0)) {
+        free(w);
+        return 1;
+    }
+    C = 0.0;
+    for (int j = 0; j < V; ++j) {
+        C += w[j];
+        cdf[j] = C / Ctot;
+    }
+    free(w);
+    return 0;
+}
+
+static void mark_invalid(int k, int32_t* out, int32_t* n_acc, int32_t* flags) {
+    for (int i = 0; i <= k; ++i) out[i] = -1;
+    *n_acc = -1;
+    if (flags) *flags |= ORC_F_BAD;
+}
+
+void orc_verify_seq(int mode, const double* logits, const double* q, const int32_t* x,
+                    const double* ua, double ur, double T, int k, int V,
+                    int32_t* out, int32_t* n_acc, double* thr, double* draw_lo,
+                    double* draw_hi, int32_t* flags) {
+    const int greedy = (mode == ORC_GREEDY);
+    const double Tr = greedy ? 1.0 : T;
+    if (flags) *flags = 0;
+    if (thr)
+        for (int i = 0; i < k; ++i) thr[i] = NAN;
+    if (draw_lo) *draw_lo = NAN;
+    if (draw_hi) *draw_hi = NAN;
+
+    /* Step 2 (and 5): the left-to-right scan. */
+    int n = k;
+    for (int i = 0; i < k; ++i) {
+        const double* li = logits + (size_t)i * V;
+        double m, S;
+        int32_t am;
+        if (orc_row_stats(li, Tr, V, &m, &S, &am)) {
+            mark_invalid(k, out, n_acc, flags);
+            return;
+        }
+        int xi = x[i];
+        if (xi < 0 || xi >= V) {
+            mark_invalid(k, out, n_acc, flags);
+            return;
+        }
+        int accept;
+        if (greedy) {
+            accept = (xi == am);
+        } else {
+            double u = ua[i];
+            double Q = q[(size_t)i * V + xi];
+            if (!(u >= 0.0 && u < 1.0) || isnan(Q) || Q < 0.0) {
+                mark_invalid(k, out, n_acc, flags);
+                return;
+            }
+            double P = row_p(li, Tr, m, S, xi);
+            if (thr) thr[i] = (P >= Q) ? 1.0 : P / Q;
+            accept = (P >= Q) || (u < P / Q);
+        }
+        if (!accept) {
+            n = i;
+            break;
+        }
+    }
+
+    /* Step 3 (and 5): the correction at the first rejection, or the bonus. */
+    const double* ln = logits + (size_t)n * V;
+    double m, S;
+    int32_t am;
+    if (orc_row_stats(ln, Tr, V, &m, &S, &am)) {
+        mark_invalid(k, out, n_acc, flags);
+        return;
+    }
+    int token;
+    if (greedy) {
+        token = am;
+    } else {
+        if (!(ur >= 0.0 && ur < 1.0)) {
+            mark_invalid(k, out, n_acc, flags);
+            return;
+        }
+        double* w = (double*)malloc(sizeof(double) * (size_t)V);
+        const double* qn = (n < k && mode == ORC_SAMPLE) ? q + (size_t)n * V : NULL;
+        draw_weights(ln, qn, Tr, m, S, V, w);
+        if (qn) {
+            double tot = 0.0;
+            for (int j = 0; j < V; ++j) tot += w[j];
+            if (!(tot > 0.0)) { /* zero residual mass: draw from p */
+                draw_weights(ln, NULL, Tr, m, S, V, w);
+                if (flags) *flags |= ORC_F_DEGENERATE;
+            }
+        }
+        double lo, hi;
+        int ovf;
+        token = categorical(w, V, ur, &lo, &hi, &ovf);
+        if (ovf && flags) *flags |= ORC_F_OVERFLOW;
+        if (draw_lo) *draw_lo = lo;
+        if (draw_hi) *draw_hi = hi;
+        free(w);
+    }
+
+    /* Step 6: outputs. */
+    for (int i = 0; i < n; ++i) out[i] = x[i];
+    out[n] = token;
+    for (int i = n + 1; i <= k; ++i) out[i] = -1;
+    *n_acc = n;
+}
+
+static double bf16_to_double(uint16_t h) {
+    uint32_t bits = ((uint32_t)h) << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+int orc_verify_batch(int mode, const void* logits, int dtype, const float* q,
+                     const int32_t* x, const float* ua, const float* ur, float T,
+                     int B, int k, int V, int32_t* out, int32_t* n_acc,
+                     double* row_m, double* row_S, int32_t* row_argmax,
+                     double* row_px, double* row_qx, double* thr,
+                     double* draw_lo, double* draw_hi, int32_t* flags, int nthreads) {
+    if (B < 0 || k < 1 || V < 1 || !logits || !x || !out || !n_acc) return -1;
+    if (dtype != 0 && dtype != 1) return -1;
+    const int greedy = (mode == ORC_GREEDY);
+    if (!greedy && (!q || !ua || !ur)) return -1;
+    const double Td = greedy ? 1.0 : (double)T;
+    const size_t rowsz = (size_t)V;
+    const size_t seqsz = (size_t)(k + 1) * rowsz;
+    int nt = nthreads > 0 ? nthreads : orc_max_threads();
+    (void)nt;
+
+#pragma omp parallel num_threads(nt)
+    {
+        double* L = (double*)malloc(sizeof(double) * seqsz);
+        double* Qd = greedy ? NULL : (double*)malloc(sizeof(double) * (size_t)k * rowsz);
+        double* ua_d = (double*)malloc(sizeof(double) * (size_t)k);
+#pragma omp for schedule(dynamic, 1)
+        for (int b = 0; b < B; ++b) {
+            /* Step 0: exact conversion of the inputs to double. */
+            if (dtype == 0) {
+                const uint16_t* src = (const uint16_t*)logits + (size_t)b * seqsz;
+                for (size_t j = 0; j < seqsz; ++j) L[j] = bf16_to_double(src[j]);
+            } else {
+                const float* src = (const float*)logits + (size_t)b * seqsz;
+                for (size_t j = 0; j < seqsz; ++j) L[j] = (double)src[j];
+            }
+            if (!greedy) {
+                const float* qs = q + (size_t)b * k * rowsz;
+                for (size_t j = 0; j < (size_t)k * rowsz; ++j) Qd[j] = (double)qs[j];
+                for (int i = 0; i < k; ++i) ua_d[i] = (double)ua[(size_t)b * k + i];
+            }
+            /* Per-row statistics of every row, for parity of the stats. */
+            for (int i = 0; i <= k; ++i) {
+                size_t r = (size_t)b * (k + 1) + i;
+                double m, S;
+                int32_t am;
+                int bad = orc_row_stats(L + (size_t)i * rowsz, Td, V, &m, &S, &am);
+                if (row_m) row_m[r] = m;
+                if (row_S) row_S[r] = bad ? NAN : S;
+                if (row_argmax) row_argmax[r] = am;
+                double px = NAN, qx = NAN;
+                if (i < k) {
+                    int xi = x[(size_t)b * k + i];
+                    if (xi >= 0 && xi < V) {
+                        if (!bad) px = row_p(L + (size_t)i * rowsz, Td, m, S, xi);
+                        if (!greedy) qx = Qd[(size_t)i * rowsz + xi];
+                    }
+                }
+                if (row_px) row_px[r] = px;
+                if (row_qx) row_qx[r] = qx;
+            }
+            int32_t fl = 0;
+            orc_verify_seq(mode, L, Qd, x + (size_t)b * k, ua_d, greedy ? 0.0 : (double)ur[b],
+                           Td, k, V, out + (size_t)b * (k + 1), n_acc + b,
+                           thr ? thr + (size_t)b * k : NULL, draw_lo ? draw_lo + b : NULL,
+                           draw_hi ? draw_hi + b : NULL, &fl);
+            if (flags) flags[b] = fl;
+        }
+        free(L);
+        free(Qd);
+        free(ua_d);
+    }
+    return 0;
+}

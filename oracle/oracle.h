@@ -1,0 +1,87 @@
+/*
+ * Plain float64 CPU oracle for the speculative-decoding verify step.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may include, link,
+ * load or call this code: only the test suite, the smoke check and the
+ * benchmark's CPU-baseline / reference arm use it.  It shares no code, header,
+ * table or constant with the CUDA library.
+ *
+ * Sources (cited by page title and section):
+ *   [DEE] "Decodificação especulativa explicada: rascunhe barato, verifique numa
+ *         passada" (gsantana.dev)
+ *   [SD15] "Speculative Decoding", ch15 of "LLM serving from scratch"
+ *         (snowch.github.io)
+ *   [SDF] "Speculative decoding: el secretario que adelanta lo que va a decir el
+ *         jefe — fundamentos, matemáticas y estado mayo 2026" (blog.lo0.es)
+ */
+#ifndef SV_ORACLE_H
+#define SV_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Verify modes. */
+enum {
+    ORC_SAMPLE = 0,       /* rejection sampling, [DEE] §"A regra de amostragem por rejeição" */
+    ORC_GREEDY = 1,       /* accept while draft == argmax, [DEE] same section, last paragraph */
+    ORC_SAMPLE_BUGGY = 2  /* negative control: resample from p instead of the residual,
+                             [DEE] §"A regra de amostragem por rejeição" (the "Júnior" aside),
+                             [SD15] §"Why the result is exactly the target model" */
+};
+
+/* Per-sequence flag bits written by the oracle. */
+enum {
+    ORC_F_BAD = 1,         /* a row / token / uniform the scan needed was invalid */
+    ORC_F_DEGENERATE = 2,  /* rejected but the residual had zero mass: drew from p instead */
+    ORC_F_OVERFLOW = 4     /* the draw ran past the last bin: clamped to the last positive bin */
+};
+
+/* Row statistics of one logits row (float64 input).
+ * m = max_j l_j / T, S = sum_j exp(l_j/T - m) (Neumaier-compensated),
+ * argmax = lowest j holding the largest raw l_j.
+ * Returns 1 if the row is invalid (a NaN, a +inf, or every entry -inf), else 0. */
+int orc_row_stats(const double* l, double T, int V, double* m, double* S, int32_t* argmax);
+
+/* Normalised cumulative boundaries cdf[j] = C_j / C_{V-1} of the weights the draw
+ * uses for one row: w_j = max(0, p_j - q_j) when q != NULL, else w_j = p_j.
+ * Returns 0, or 1 when the total weight is zero (cdf left untouched). */
+int orc_draw_cdf(const double* l, const double* q, double T, int V, double* cdf);
+
+/* One sequence, all inputs already float64.
+ *   logits [k+1][V], q [k][V] (unused in greedy), x [k], ua [k] (unused in greedy),
+ *   ur (unused in greedy), T > 0 (greedy ignores it).
+ * Outputs: out [k+1] (drafts 0..n-1, the drawn token at n, -1 after),
+ *   *n_acc = n in [0,k] (-1 if the sequence is invalid),
+ *   thr [k] (may be NULL): min(1, P/Q) at every judged sampled position, NaN elsewhere,
+ *   *draw_lo / *draw_hi (may be NULL): C_{t-1}/C_tot and C_t/C_tot of the drawn bin
+ *   (NaN in greedy mode), *flags (may be NULL): ORC_F_* bits. */
+void orc_verify_seq(int mode, const double* logits, const double* q, const int32_t* x,
+                    const double* ua, double ur, double T, int k, int V,
+                    int32_t* out, int32_t* n_acc, double* thr, double* draw_lo,
+                    double* draw_hi, int32_t* flags);
+
+/* Batch form over B independent sequences, inputs in the device layouts:
+ *   logits [B][k+1][V] as bf16 bit patterns (dtype 0, uint16) or float32 (dtype 1),
+ *   q [B][k][V] float32, x [B][k] int32, ua [B][k] float32, ur [B] float32.
+ * Every per-row / per-sequence output pointer may be NULL.
+ *   row_m, row_S, row_px, row_qx: [B][k+1] float64 (px, qx are NaN on row k and for
+ *   out-of-range draft tokens); row_argmax [B][k+1]; thr [B][k];
+ *   draw_lo, draw_hi, flags [B].
+ * nthreads <= 0 uses the OpenMP default.  Returns 0, or -1 on bad arguments. */
+int orc_verify_batch(int mode, const void* logits, int dtype, const float* q,
+                     const int32_t* x, const float* ua, const float* ur, float T,
+                     int B, int k, int V, int32_t* out, int32_t* n_acc,
+                     double* row_m, double* row_S, int32_t* row_argmax,
+                     double* row_px, double* row_qx, double* thr,
+                     double* draw_lo, double* draw_hi, int32_t* flags, int nthreads);
+
+/* Number of OpenMP threads a batch call with nthreads <= 0 would use. */
+int orc_max_threads(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,209 @@
+"""Seeded synthetic inputs for the verify step.
+
+This module only makes inputs: target logits, the draft's distributions q, the
+drafted tokens and the uniforms.  It holds none of the verify arithmetic (no
+acceptance test, no residual, no categorical draw of the verifier); drafted
+tokens are drawn with numpy's own ``Generator.choice``.  Both the CUDA path and
+the CPU oracle are fed from here.
+
+Workloads (sizes, value distributions and seeds):
+
+  c1  sampled, B=1,   k=4, V=32,     fp32, T=1.0: target logits i.i.d. N(0, 2^2);
+      draft logits = target + N(0, 0.5^2), q = softmax(draft logits).
+  c2  greedy,  B=64,  k=4, V=32000,  bf16: Zipf-shaped rows (slope 1.1, N(0,1)
+      noise) under a random vocabulary permutation; the draft token is the row's
+      argmax with probability 0.8, else a uniform random id.
+  c3  sampled, B=32,  k=5, V=128256, bf16, T=0.8: Zipf rows (1.1, N(0,1));
+      q = softmax((logits + N(0, 0.7^2)) / 0.8).
+  c4  sampled, B=256, k=8, V=151936, fp32, T=1.0: Zipf rows (1.0, N(0, 1.5^2));
+      q = softmax(logits + N(0, 1)).
+  c5  sampled, B=1,   k=8, V=256000, bf16, T=0.7: Zipf rows (1.1, N(0,1));
+      q = softmax((logits + N(0, 0.5^2)) / 0.7).
+
+A Zipf-shaped row puts -s*ln(r) + eps_r at the position pi(r-1) of a fresh random
+permutation pi, r = 1..V.  Drafted tokens are sampled from the float32 q rows;
+uniforms are float32 in [0, 1).  Every stream (logits, draft noise,
+permutations, draft sampling, u_accept, u_resample) has its own child seed.
+"""
+from __future__ import annotations
+
+import os
+from concurrent.futures import ThreadPoolExecutor
+from dataclasses import dataclass, field
+
+import numpy as np
+
+WORKLOADS = {
+    "c1": dict(mode="sample", B=1, k=4, V=32, dtype="f32", T=1.0, kind="gauss",
+               scale=2.0, draft_sigma=0.5, draft_T=1.0, seed=0),
+    "c2": dict(mode="greedy", B=64, k=4, V=32000, dtype="bf16", T=1.0, kind="zipf",
+               slope=1.1, noise=1.0, p_argmax=0.8, seed=1),
+    "c3": dict(mode="sample", B=32, k=5, V=128256, dtype="bf16", T=0.8, kind="zipf",
+               slope=1.1, noise=1.0, draft_sigma=0.7, draft_T=0.8, seed=2),
+    "c4": dict(mode="sample", B=256, k=8, V=151936, dtype="f32", T=1.0, kind="zipf",
+               slope=1.0, noise=1.5, draft_sigma=1.0, draft_T=1.0, seed=3),
+    "c5": dict(mode="sample", B=1, k=8, V=256000, dtype="bf16", T=0.7, kind="zipf",
+               slope=1.1, noise=1.0, draft_sigma=0.5, draft_T=0.7, seed=4),
+}
+
+WORKLOAD_NAMES = {
+    "c1": "sampled B=1 k=4 V=32 fp32 T=1.0 (gaussian logits)",
+    "c2": "greedy B=64 k=4 V=32000 bf16 (zipf logits)",
+    "c3": "sampled B=32 k=5 V=128256 bf16 T=0.8 (zipf logits)",
+    "c4": "sampled B=256 k=8 V=151936 fp32 T=1.0 (zipf logits)",
+    "c5": "sampled B=1 k=8 V=256000 bf16 T=0.7 (zipf logits)",
+}
+
+
+@dataclass
+class VerifyInputs:
+    mode: str                 # "sample" or "greedy"
+    dtype: str                # "bf16" or "f32"
+    B: int
+    k: int
+    V: int
+    T: float
+    logits: np.ndarray        # [B, k+1, V] uint16 bf16 bit patterns or float32
+    q: np.ndarray | None      # [B, k, V] float32 (sampled) or None
+    x: np.ndarray             # [B, k] int32 drafted tokens
+    ua: np.ndarray | None     # [B, k] float32 u_accept
+    ur: np.ndarray | None     # [B] float32 u_resample
+    meta: dict = field(default_factory=dict)
+
+    def logits_f32(self) -> np.ndarray:
+        """The logits as float32 values (exact widening of bf16)."""
+        if self.dtype == "bf16":
+            return (self.logits.astype(np.uint32) << 16).view(np.float32)
+        return self.logits
+
+    @property
+    def nbytes_logits(self) -> int:
+        return int(self.logits.nbytes)
+
+
+def bf16_bits(a: np.ndarray) -> np.ndarray:
+    """Round float32 values to bf16 (round to nearest, ties to even); uint16 bit patterns."""
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    u = a.view(np.uint32).astype(np.uint64)
+    bias = ((u >> 16) & 1) + 0x7FFF
+    return ((u + bias) >> 16).astype(np.uint16)
+
+
+def _streams(seed: int):
+    ss = np.random.SeedSequence(seed)
+    names = ("logits", "draft_noise", "perm", "draft_sample", "u_accept", "u_resample")
+    return dict(zip(names, ss.spawn(len(names))))
+
+
+_CHUNK = 64
+
+
+def _chunked(n_rows, seq: np.random.SeedSequence, fn):
+    """Run fn(rng, r0, r1) over fixed 64-row chunks, each with its own child seed,
+    on a thread pool (numpy releases the GIL); the result does not depend on the
+    thread count."""
+    starts = list(range(0, n_rows, _CHUNK))
+    kids = seq.spawn(len(starts))
+    workers = max(1, min(len(starts), os.cpu_count() or 1))
+
+    def run(i):
+        r0 = starts[i]
+        fn(np.random.default_rng(kids[i]), r0, min(n_rows, r0 + _CHUNK))
+
+    if workers == 1:
+        for i in range(len(starts)):
+            run(i)
+    else:
+        with ThreadPoolExecutor(workers) as ex:
+            list(ex.map(run, range(len(starts))))
+
+
+def _zipf_rows(s_val, s_perm, n_rows, V, slope, noise):
+    base = -slope * np.log(np.arange(1, V + 1, dtype=np.float64))
+    out = np.empty((n_rows, V), dtype=np.float32)
+    perm_kids = s_perm.spawn(-(-n_rows // _CHUNK))
+
+    def fill(g, r0, r1):
+        gp = np.random.default_rng(perm_kids[r0 // _CHUNK])
+        vals = base[None, :] + noise * g.standard_normal((r1 - r0, V))
+        perm = gp.permuted(np.tile(np.arange(V), (r1 - r0, 1)), axis=1)
+        rows = np.empty((r1 - r0, V), dtype=np.float64)
+        np.put_along_axis(rows, perm, vals, axis=1)
+        out[r0:r1] = rows.astype(np.float32)
+
+    _chunked(n_rows, s_val, fill)
+    return out
+
+
+def _draft_q(base_rows, s_noise, sigma, T):
+    """q = softmax((target + N(0, sigma^2)) / T), rows in float64, stored float32."""
+    n, V = base_rows.shape
+    q = np.empty((n, V), dtype=np.float32)
+
+    def fill(g, r0, r1):
+        z = (base_rows[r0:r1].astype(np.float64) + sigma * g.standard_normal((r1 - r0, V))) / T
+        z -= z.max(axis=1, keepdims=True)
+        e = np.exp(z)
+        q[r0:r1] = (e / e.sum(axis=1, keepdims=True)).astype(np.float32)
+
+    _chunked(n, s_noise, fill)
+    return q
+
+
+def make_inputs(mode="sample", B=1, k=4, V=32, dtype="f32", T=1.0, kind="zipf",
+                slope=1.1, noise=1.0, scale=2.0, draft_sigma=0.5, draft_T=None,
+                p_argmax=0.8, seed=0) -> VerifyInputs:
+    """Build one seeded batch.  ``kind`` is "zipf" (Zipf-shaped rows) or "gauss"
+    (i.i.d. N(0, scale^2) logits)."""
+    if draft_T is None:
+        draft_T = T
+    s = _streams(seed)
+    R = B * (k + 1)
+    if kind == "zipf":
+        rows = _zipf_rows(s["logits"], s["perm"], R, V, slope, noise)
+    elif kind == "gauss":
+        rows = (scale * np.random.default_rng(s["logits"]).standard_normal((R, V))).astype(
+            np.float32)
+    else:
+        raise ValueError(kind)
+    if dtype == "bf16":
+        bits = bf16_bits(rows)
+        logits = bits.reshape(B, k + 1, V)
+        vals = (bits.astype(np.uint32) << 16).view(np.float32).reshape(B, k + 1, V)
+    elif dtype == "f32":
+        logits = rows.reshape(B, k + 1, V)
+        vals = logits
+    else:
+        raise ValueError(dtype)
+
+    if mode == "greedy":
+        am = np.argmax(vals[:, :k, :], axis=2)
+        gd = np.random.default_rng(s["draft_sample"])
+        rnd = gd.integers(0, V, size=(B, k))
+        keep = gd.random((B, k)) < p_argmax
+        x = np.where(keep, am, rnd).astype(np.int32)
+        return VerifyInputs(mode, dtype, B, k, V, float(T), logits, None, x, None, None,
+                            meta=dict(kind=kind, seed=seed))
+
+    q = _draft_q(vals[:, :k, :].reshape(B * k, V), s["draft_noise"], draft_sigma,
+                 draft_T).reshape(B, k, V)
+    x = np.empty((B, k), dtype=np.int32)
+    gs = np.random.default_rng(s["draft_sample"])
+    for b in range(B):
+        for i in range(k):
+            p = q[b, i].astype(np.float64)
+            x[b, i] = gs.choice(V, p=p / p.sum())
+    ua = np.random.default_rng(s["u_accept"]).random((B, k), dtype=np.float32)
+    ur = np.random.default_rng(s["u_resample"]).random(B, dtype=np.float32)
+    return VerifyInputs(mode, dtype, B, k, V, float(T), logits, q, x, ua, ur,
+                        meta=dict(kind=kind, seed=seed))
+
+
+def workload(name: str, seed: int | None = None) -> VerifyInputs:
+    """One of the five named workloads (c1..c5), optionally with another seed."""
+    cfg = dict(WORKLOADS[name])
+    if seed is not None:
+        cfg["seed"] = seed
+    inp = make_inputs(**cfg)
+    inp.meta["workload"] = name
+    return inp
