@@ -1,0 +1,442 @@
+#!/usr/bin/env python3
+"""Benchmark of the batched speculative-decoding verify step on GB300.
+
+One step = one verify of one batch of the named workload (default c2: greedy,
+B=64, k=4, V=32000, bf16 logits): the row stream, the accept scan and the draw.
+Metric: verify rows per second, rows = B*(k+1) per step, summed over GPUs.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c1..c5]
+                  [--impl ours|reference]
+
+Timing: inputs are resident in HBM and rotated over enough copies to exceed the
+129 MB L2 between reuses; K steps are replayed from CUDA graphs (one graph of
+`copies` consecutive verifies) and timed with CUDA events on the launching
+stream, bracketed by a barrier and a device synchronisation, max over ranks.
+The row-stream kernel is also timed alone with events around each launch for
+the roofline figure.  `e2e` repeats the measurement through the same C ABI with
+the inputs in pinned HOST memory: every step copies its inputs host-to-device,
+verifies and copies the outputs back.  `cpu_baseline` times the float64 oracle
+on a bounded sample on this host's cores.  With --impl reference the oracle is
+the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from speculative_decoding_verification_18_gb300 import inputs as I  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=0, help="timed steps (0: about 2 s worth)")
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="c2", choices=sorted(I.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("specverify.cu", "ff.cuh"):
+        with open(os.path.join(ROOT, "speculative_decoding_verification_18_gb300", "csrc", f),
+                  "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def ncu_traffic(workload, kernel):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if it was
+    captured from the current kernel source; else None."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    e = d.get(workload, {}).get(kernel)
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid):
+        self.uuid = uuid
+        self.proc = None
+
+    def __enter__(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        if self.uuid:
+            cmd += ["-i", self.uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def algorithmic_bytes_rows(inp):
+    """Bytes the row stream must move per launch: every logits row once, the draft
+    tokens, the gathered l(x) / q(x) (one 32-byte sector each), the row records."""
+    R = inp.B * (inp.k + 1)
+    esz = 2 if inp.dtype == "bf16" else 4
+    b = R * inp.V * esz + inp.B * inp.k * 4 + R * 32
+    b += inp.B * inp.k * 32 * (2 if inp.mode == "sample" else 1)
+    return b
+
+
+def oracle_time(inp, seqs, nthreads, min_seconds=3.0, min_reps=2):
+    """Seconds per call of the oracle on the first `seqs` sequences."""
+    import oracle
+    oracle.build()
+    sl = slice(0, seqs)
+    args = (oracle.GREEDY if inp.mode == "greedy" else oracle.SAMPLE, inp.logits[sl], inp.dtype,
+            None if inp.q is None else inp.q[sl], inp.x[sl],
+            None if inp.ua is None else inp.ua[sl], None if inp.ur is None else inp.ur[sl],
+            inp.T if inp.mode == "sample" else 1.0)
+    reps, t0 = 0, time.perf_counter()
+    while reps < min_reps or time.perf_counter() - t0 < min_seconds:
+        oracle.verify_batch(*args, nthreads=nthreads)
+        reps += 1
+    return (time.perf_counter() - t0) / reps
+
+
+def cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, world, rank):
+    """The reference arm: the float64 oracle on this host's cores, same workload."""
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    inp = I.workload(args.workload)
+    nt = cores()
+    steps = args.steps if args.steps > 0 else 5
+    per_seq = oracle_time(inp, 1, nt, min_seconds=0.5, min_reps=1)
+    budget = 120.0 / max(1, steps + args.warmup)
+    seqs = int(max(1, min(inp.B, budget / max(per_seq, 1e-9))))
+    sl = slice(0, seqs)
+    call = lambda: oracle.verify_batch(
+        oracle.GREEDY if inp.mode == "greedy" else oracle.SAMPLE, inp.logits[sl], inp.dtype,
+        None if inp.q is None else inp.q[sl], inp.x[sl], None if inp.ua is None else inp.ua[sl],
+        None if inp.ur is None else inp.ur[sl], inp.T if inp.mode == "sample" else 1.0,
+        nthreads=nt)
+    for _ in range(args.warmup):
+        call()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        call()
+    dt = time.perf_counter() - t0
+    rows = seqs * (inp.k + 1) * steps
+    value = rows / dt
+    sample = f"first {seqs} of {inp.B} sequences per step ({seqs * (inp.k + 1)} rows)"
+    line = {
+        "impl": "reference", "metric": "verify rows/s", "value": value, "unit": "rows/s",
+        "n_gpus": args.gpus, "steps": steps, "warmup": args.warmup,
+        "ms_per_step": dt / steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {I.WORKLOAD_NAMES[args.workload]}",
+                   "B": inp.B, "k": inp.k, "V": inp.V, "logits_dtype": inp.dtype,
+                   "mode": inp.mode},
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": nt, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        if world > 1:
+            # Rank 0 alone runs the CPU reference; the others exit without work.
+            run_reference(args, world, rank)
+            return
+        run_reference(args, world, rank)
+        return
+
+    import torch
+    from speculative_decoding_verification_18_gb300 import build as libbuild
+    from speculative_decoding_verification_18_gb300 import specverify as sv
+
+    libbuild.build()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    inp = I.workload(args.workload)
+    B, k, V = inp.B, inp.k, inp.V
+    rows_per_step = B * (k + 1)
+    set_bytes = inp.logits.nbytes + (0 if inp.q is None else inp.q.nbytes)
+    copies = int(min(16, max(1, -(-2 * L2_BYTES // set_bytes))))
+
+    # Device-resident inputs, rotated over `copies` distinct buffers.
+    def dev_set():
+        if inp.dtype == "bf16":
+            lg = torch.from_numpy(inp.logits.view(np.int16)).view(torch.bfloat16).to(dev)
+        else:
+            lg = torch.from_numpy(inp.logits).to(dev)
+        d = {"logits": lg, "x": torch.from_numpy(inp.x).to(dev)}
+        if inp.mode == "sample":
+            d["q"] = torch.from_numpy(inp.q).to(dev)
+            d["ua"] = torch.from_numpy(inp.ua).to(dev)
+            d["ur"] = torch.from_numpy(inp.ur).to(dev)
+        return d
+
+    sets = [dev_set() for _ in range(copies)]
+    ws = [sv.workspace(B, k, V, sets[0]["logits"].dtype, dev) for _ in range(copies)]
+    outs = [torch.empty((B, k + 1), dtype=torch.int32, device=dev) for _ in range(copies)]
+    ns = [torch.empty(B, dtype=torch.int32, device=dev) for _ in range(copies)]
+
+    def verify(i, stream=None):
+        s = sets[i]
+        if inp.mode == "greedy":
+            sv.spec_verify_greedy(s["logits"], s["x"], outs[i], ns[i], ws[i], stream)
+        else:
+            sv.spec_verify_sample(s["logits"], s["q"], s["x"], s["ua"], s["ur"], inp.T, outs[i],
+                                  ns[i], ws[i], stream)
+
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for i in range(copies):
+            verify(i)  # device set-up outside capture
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            for i in range(copies):
+                verify(i)
+    torch.cuda.synchronize(dev)
+
+    # Warm-up (at least 3 steps), then pick K if not given (about 2 s of steps).
+    warm_reps = max(1, -(-max(3, args.warmup) // copies))
+    t0 = time.perf_counter()
+    for _ in range(warm_reps):
+        graph.replay()
+    torch.cuda.synchronize(dev)
+    est = (time.perf_counter() - t0) / (warm_reps * copies)
+    K = args.steps if args.steps > 0 else int(min(200000, max(copies, 2.0 / max(est, 1e-7))))
+    reps = -(-K // copies)
+    K = reps * copies
+
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid).replace("GPU-", "")
+    except Exception:
+        pass
+
+    # ---- timed region
+    sampler = ClockSampler(uuid)
+    with sampler:
+        time.sleep(0.3)
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(reps):
+                graph.replay()
+            ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        if dist:
+            dist.barrier()
+        ms = ev0.elapsed_time(ev1)
+
+        # Row-stream kernel alone, events around every launch (same stream, rotated inputs).
+        n_k1 = max(copies, min(2000, K))
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n_k1)]
+        mode = sv.SV_MODE_GREEDY if inp.mode == "greedy" else sv.SV_MODE_SAMPLE
+        with torch.cuda.stream(stream):
+            for j in range(n_k1):
+                i = j % copies
+                s = sets[i]
+                evs[j][0].record(stream)
+                sv.spec_verify_rows(mode, s["logits"], s.get("q"), s["x"], inp.T, ws[i])
+                evs[j][1].record(stream)
+        torch.cuda.synchronize(dev)
+        k1_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    clocks = sampler.summary()
+
+    ms_t = torch.tensor([ms], device=dev)
+    if dist:
+        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
+    ms = float(ms_t.item())
+    value = rows_per_step * K * world / (ms / 1e3)
+
+    # ---- end to end through the C ABI with host buffers
+    pin = lambda a: torch.from_numpy(a).pin_memory()
+    h_logits = pin(inp.logits.view(np.int16) if inp.dtype == "bf16" else inp.logits)
+    h = {"logits": h_logits, "x": pin(inp.x)}
+    if inp.mode == "sample":
+        h.update(q=pin(inp.q), ua=pin(inp.ua), ur=pin(inp.ur))
+    h_out = torch.empty((B, k + 1), dtype=torch.int32).pin_memory()
+    h_n = torch.empty(B, dtype=torch.int32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in h.values())
+    d2h = h_out.numel() * 4 + h_n.numel() * 4
+    e2e_steps = int(max(3, min(K, 2.0 / max(est * 4 + h2d / 200e9, 1e-7))))
+
+    def e2e_step():
+        s = sets[0]
+        if inp.dtype == "bf16":
+            s["logits"].view(torch.int16).copy_(h["logits"], non_blocking=True)
+        else:
+            s["logits"].copy_(h["logits"], non_blocking=True)
+        for key in h:
+            if key != "logits":
+                s[key].copy_(h[key], non_blocking=True)
+        verify(0)
+        h_out.copy_(outs[0], non_blocking=True)
+        h_n.copy_(ns[0], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        if dist:
+            dist.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1)
+    et = torch.tensor([e2e_ms], device=dev)
+    if dist:
+        dist.all_reduce(et, op=dist.ReduceOp.MAX)
+    e2e_value = rows_per_step * e2e_steps * world / (float(et.item()) / 1e3)
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+
+    # ---- roofline of the row-stream kernel
+    peak, peak_src = measured_peaks()
+    alg = algorithmic_bytes_rows(inp)
+    achieved = alg / (k1_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4),
+                "traffic": ncu_traffic(args.workload, "sv_rows_kernel"),
+                "kernel": "sv_rows_kernel", "kernel_ms": round(k1_ms, 5),
+                "algorithmic_bytes": alg, "peak_source": peak_src}
+
+    # ---- CPU baseline: the oracle on a bounded sample
+    nt = cores()
+    per_call = oracle_time(inp, min(B, 1), nt, min_seconds=0.2, min_reps=1)
+    seqs = int(max(1, min(B, 5.0 / max(per_call, 1e-9))))
+    t_cpu = oracle_time(inp, seqs, nt, min_seconds=5.0, min_reps=2)
+    cpu_value = seqs * (k + 1) / t_cpu
+
+    line = {
+        "metric": "verify rows/s", "value": value, "unit": "rows/s", "n_gpus": world,
+        "steps": K, "warmup": warm_reps * copies, "ms_per_step": ms / K,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {I.WORKLOAD_NAMES[args.workload]}",
+                   "B": B, "k": k, "V": V, "logits_dtype": inp.dtype, "mode": inp.mode,
+                   "T": inp.T, "rows_per_step": rows_per_step,
+                   "l2": f"inputs rotated over {copies} device copies "
+                         f"({copies * set_bytes / 2**20:.0f} MiB > 129 MB L2)",
+                   "timing": f"{reps} replays of a CUDA graph of {copies} verifies",
+                   "parallelism": f"replicas x{world}"},
+        "clocks": clocks,
+        "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": 2 * K,
+        "roofline": roofline,
+        "cpu_baseline": {"value": cpu_value, "unit": "rows/s", "cores": nt, "kind": "oracle",
+                         "sample": f"first {seqs} of {B} sequences ({seqs * (k + 1)} rows), "
+                                   f"repeated for >= 5 s"},
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

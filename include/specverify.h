@@ -1,0 +1,168 @@
+/*
+ * specverify — the batched draft-verify step of speculative decoding on one
+ * GB300 (sm_103a), behind a plain C ABI.
+ *
+ * What it computes.  For each of B independent sequences the target scored the
+ * prefix plus k drafted tokens in one pass, giving k+1 rows of logits l_0..l_k
+ * over a vocabulary of V tokens; row i judges draft x_i and row k is the bonus
+ * row ("Decodificação especulativa explicada: rascunhe barato, verifique numa
+ * passada", §"O ciclo de rascunho e verificação"; "Speculative decoding: el
+ * secretario que adelanta lo que va a decir el jefe", §"El mecanismo desnudo",
+ * paso 2).
+ *
+ *   p_i = softmax(l_i / T).
+ *   Sampled mode: judge x_0, x_1, ... left to right and accept x_i when
+ *     p_i(x_i) >= q_i(x_i) or u_accept[i] < p_i(x_i) / q_i(x_i), i.e. with
+ *     probability min(1, p/q); stop at the first rejection n and draw the
+ *     replacement from norm(max(0, p_n - q_n)); if all k survive, draw a bonus
+ *     token from p_k ("Decodificação especulativa explicada", §"A regra de
+ *     amostragem por rejeição", rules 1-3; "Speculative Decoding" (ch15, LLM
+ *     serving from scratch), §"Why the result is exactly the target model").
+ *   Greedy mode: accept while x_i == argmax p_i; emit argmax p_n at the first
+ *     mismatch, or argmax p_k as the bonus (same sections, greedy case).
+ *   A draw from weights w takes the first j whose running sum C_j exceeds
+ *     u_resample * C_{V-1} ("Decodificação especulativa explicada",
+ *     §"Amostragem especulativa em numpy, com prova", the sampler), so a
+ *     zero-weight token is never drawn.
+ *   num_accepted[b] = n is also the number of drafted positions whose KV-cache
+ *     entries the caller keeps (§"O ciclo de rascunho e verificação",
+ *     bookkeeping paragraph); the round emits n + 1 tokens.
+ *
+ * Readings where the pages are silent: a tie u == p/q rejects; p >= q always
+ * accepts (so q(x) == 0 accepts); one uniform per sequence serves the single
+ * draw that happens; argmax ties go to the lowest token id; a rejection whose
+ * residual has zero mass (possible only through rounding or an unnormalised q)
+ * draws from p instead and is counted; output positions after the drawn token
+ * are -1.
+ *
+ * Conventions shared by every entry point.
+ *  - All tensor pointers are DEVICE pointers owned by the caller, contiguous,
+ *    row-major, 16-byte aligned.  Any V >= 1 is accepted.
+ *  - The library allocates nothing.  Scratch lives in the caller's workspace
+ *    (ws, ws_bytes >= spec_verify_workspace_size(...)), 16-byte aligned; it
+ *    needs no initialisation and may be reused by later calls on the same
+ *    stream.  Calls sharing one workspace must not overlap in time.
+ *  - Launches are asynchronous on `stream`; nothing synchronises except
+ *    spec_verify_read_status and spec_verify_row_stats.
+ *  - Argument errors return an error code synchronously and launch nothing.
+ *  - Bad data found on the device (a NaN or +inf logit, an all -inf row, a draft
+ *    token outside [0,V), a uniform outside [0,1), a NaN or negative q(x)) on a
+ *    row or token that the scan reaches marks that sequence invalid: its
+ *    num_accepted is -1 and its out_tokens row is all -1, and a bit is set in
+ *    the workspace status word (spec_verify_read_status).
+ *  - Limits: 1 <= k <= 64, 1 <= V <= 2^21, B >= 0, B*(k+1)*V < 2^40,
+ *    B*(k+1) < 2^27.  B == 0 launches nothing (the workspace is left as it was).
+ */
+#ifndef SPECVERIFY_H
+#define SPECVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SV_OK = 0,
+    SV_ERR_INVALID_ARG = 1,  /* null pointer, bad size, bad T, misaligned pointer */
+    SV_ERR_WORKSPACE = 2,    /* workspace missing or smaller than required */
+    SV_ERR_UNSUPPORTED = 3,  /* sizes beyond the limits above, or no sm_103a device */
+    SV_ERR_CUDA = 4,         /* a CUDA runtime call failed (launch, copy) */
+    SV_ERR_DATA = 5,         /* device-detected bad data (spec_verify_read_status) */
+    SV_ERR_TIMEOUT = 6       /* reserved: a bounded device-side wait gave up */
+} sv_status;
+
+typedef enum { SV_BF16 = 0, SV_F32 = 1 } sv_dtype;
+
+typedef enum { SV_MODE_SAMPLE = 0, SV_MODE_GREEDY = 1 } sv_mode;
+
+/* Bits of the device status word. */
+#define SV_DEV_BAD_ROW 0x1u      /* a reached row held a NaN / +inf, or was all -inf */
+#define SV_DEV_BAD_TOKEN 0x2u    /* a reached draft token outside [0, V) */
+#define SV_DEV_BAD_UNIFORM 0x4u  /* a used uniform outside [0, 1) (or NaN) */
+#define SV_DEV_BAD_Q 0x8u        /* q_i(x_i) NaN or negative at a reached position */
+#define SV_DEV_DEGENERATE 0x10u  /* informational: a zero-mass residual drew from p */
+
+/* Bytes of workspace the calls below need for these sizes (0 for invalid sizes). */
+size_t spec_verify_workspace_size(int B, int k, int V, sv_dtype dtype);
+
+/* Greedy verify.
+ *   logits       [B, k+1, V] bf16 or fp32 (dtype), the target's logits.
+ *   draft_tokens [B, k] int32.
+ *   out_tokens   [B, k+1] int32 (written): argmax-accepted drafts 0..n-1, the
+ *                argmax token at n, -1 after.
+ *   num_accepted [B] int32 (written): n in [0, k], or -1 for an invalid sequence.
+ * Temperature plays no part in greedy verify. */
+sv_status spec_verify_greedy(const void* logits, sv_dtype dtype,
+                             const int32_t* draft_tokens, int B, int k, int V,
+                             int32_t* out_tokens, int32_t* num_accepted,
+                             void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Sampled verify (rejection sampling).
+ *   logits       [B, k+1, V] bf16 or fp32, the target's logits; p = softmax(l/T).
+ *   draft_probs  [B, k, V] fp32, the draft's distributions q recorded while
+ *                drafting (used as given, no temperature applied).
+ *   draft_tokens [B, k] int32.
+ *   u_accept     [B, k] fp32 in [0, 1): uniform for the accept test at i.
+ *   u_resample   [B] fp32 in [0, 1): uniform for the one draw per sequence.
+ *   T            temperature, finite and > 0.
+ *   out_tokens   [B, k+1] int32 (written): accepted drafts 0..n-1, the drawn
+ *                token at n, -1 after.
+ *   num_accepted [B] int32 (written): n in [0, k], or -1 for an invalid sequence.
+ * The acceptance ratios are formed in double from fp32 row statistics; the
+ * draw's exponentials, normaliser and running sums are computed to about 48
+ * bits (float-float arithmetic, integer prefix sums) so that its token matches
+ * an exact-arithmetic draw except when u_resample lies within ~1e-12 of a bin
+ * boundary. */
+sv_status spec_verify_sample(const void* logits, sv_dtype dtype, const float* draft_probs,
+                             const int32_t* draft_tokens, const float* u_accept,
+                             const float* u_resample, float T, int B, int k, int V,
+                             int32_t* out_tokens, int32_t* num_accepted,
+                             void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* The same work as the two calls above, split at its one internal dependency so
+ * that each half can be timed or overlapped separately.  spec_verify_rows
+ * streams every logits row once and leaves per-row statistics (max, normaliser,
+ * argmax, gathered l(x), q(x), p(x)) in ws; spec_verify_finish then runs the
+ * accept scan and the draws from ws and writes the outputs.  Calling rows then
+ * finish on one stream with the same arguments is exactly spec_verify_greedy
+ * (mode SV_MODE_GREEDY; draft_probs, u_accept, u_resample may be NULL, T is
+ * ignored) or spec_verify_sample (mode SV_MODE_SAMPLE). */
+sv_status spec_verify_rows(sv_mode mode, const void* logits, sv_dtype dtype,
+                           const float* draft_probs, const int32_t* draft_tokens,
+                           float T, int B, int k, int V, void* ws, size_t ws_bytes,
+                           cudaStream_t stream);
+sv_status spec_verify_finish(sv_mode mode, const void* logits, sv_dtype dtype,
+                             const float* draft_probs, const int32_t* draft_tokens,
+                             const float* u_accept, const float* u_resample, float T,
+                             int B, int k, int V, int32_t* out_tokens,
+                             int32_t* num_accepted, void* ws, size_t ws_bytes,
+                             cudaStream_t stream);
+
+/* Synchronises `stream`, then copies the device status word of the last call
+ * that used `ws` into *device_status (SV_DEV_* bits).  Returns SV_ERR_DATA if
+ * any error bit (all but SV_DEV_DEGENERATE) is set, else SV_OK.
+ * *n_degenerate (may be NULL) receives the number of zero-mass residual draws. */
+sv_status spec_verify_read_status(const void* ws, cudaStream_t stream,
+                                  uint32_t* device_status, uint32_t* n_degenerate);
+
+/* Debug / test: synchronises `stream` and copies the per-row statistics of the
+ * last call that used `ws` to HOST arrays of B*(k+1) entries each (any may be
+ * NULL): m = max_j l_j (the largest raw logit; max_j l_j/T = m/T),
+ * S = sum_j exp((l_j - m)/T), argmax (lowest index of the largest raw logit),
+ * px = p_i(x_i) and qx = q_i(x_i) (NaN on row k; px and S are 0 in greedy
+ * mode, which does not form them). */
+sv_status spec_verify_row_stats(const void* ws, cudaStream_t stream, int B, int k,
+                                float* m, float* S, int32_t* argmax, float* px,
+                                float* qx);
+
+/* Static description of a status code. */
+const char* spec_verify_status_string(sv_status status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPECVERIFY_H */

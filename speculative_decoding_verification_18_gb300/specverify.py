@@ -1,0 +1,215 @@
+"""Thin ctypes binding of ``libspecverify.so`` (declared in include/specverify.h).
+
+Argument marshalling only: every step of the verify path runs in the CUDA
+library.  Functions take torch CUDA tensors (contiguous, on the current device)
+and launch on the current torch stream unless ``stream`` is given.  There is no
+CPU fallback: if the library is missing this module raises on first use.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB = os.path.join(HERE, "libspecverify.so")
+
+SV_OK, SV_ERR_INVALID_ARG, SV_ERR_WORKSPACE, SV_ERR_UNSUPPORTED, SV_ERR_CUDA, SV_ERR_DATA, \
+    SV_ERR_TIMEOUT = range(7)
+SV_BF16, SV_F32 = 0, 1
+SV_MODE_SAMPLE, SV_MODE_GREEDY = 0, 1
+SV_DEV_BAD_ROW, SV_DEV_BAD_TOKEN, SV_DEV_BAD_UNIFORM, SV_DEV_BAD_Q, SV_DEV_DEGENERATE = (
+    0x1, 0x2, 0x4, 0x8, 0x10)
+
+EXPORTS = ("spec_verify_workspace_size", "spec_verify_greedy", "spec_verify_sample",
+           "spec_verify_rows", "spec_verify_finish", "spec_verify_read_status",
+           "spec_verify_row_stats", "spec_verify_status_string")
+
+_lib = None
+
+
+class SpecVerifyError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+        self.status = status
+
+
+def load():
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB):
+        raise ImportError(f"libspecverify.so is not built ({LIB}); run "
+                          "speculative_decoding_verification_18_gb300.build.build() first")
+    lib = ctypes.CDLL(LIB)
+    P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.spec_verify_workspace_size.argtypes = [I, I, I, I]
+    lib.spec_verify_workspace_size.restype = Z
+    lib.spec_verify_greedy.argtypes = [P, I, P, I, I, I, P, P, P, Z, P]
+    lib.spec_verify_greedy.restype = I
+    lib.spec_verify_sample.argtypes = [P, I, P, P, P, P, F, I, I, I, P, P, P, Z, P]
+    lib.spec_verify_sample.restype = I
+    lib.spec_verify_rows.argtypes = [I, P, I, P, P, F, I, I, I, P, Z, P]
+    lib.spec_verify_rows.restype = I
+    lib.spec_verify_finish.argtypes = [I, P, I, P, P, P, P, F, I, I, I, P, P, P, Z, P]
+    lib.spec_verify_finish.restype = I
+    lib.spec_verify_read_status.argtypes = [P, P, P, P]
+    lib.spec_verify_read_status.restype = I
+    lib.spec_verify_row_stats.argtypes = [P, P, I, I, P, P, P, P, P]
+    lib.spec_verify_row_stats.restype = I
+    lib.spec_verify_status_string.argtypes = [I]
+    lib.spec_verify_status_string.restype = ctypes.c_char_p
+    lib.spec_verify_debug_ffexp.argtypes = [P, F, F, I, P, P]
+    lib.spec_verify_debug_ffexp.restype = I
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().spec_verify_status_string(int(status)).decode()
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _dtype(logits):
+    if logits.dtype == torch.bfloat16:
+        return SV_BF16
+    if logits.dtype == torch.float32:
+        return SV_F32
+    raise TypeError(f"logits must be bfloat16 or float32, not {logits.dtype}")
+
+
+def _check(st, where):
+    if st != SV_OK:
+        raise SpecVerifyError(st, where)
+
+
+def spec_verify_workspace_size(B: int, k: int, V: int, dtype=SV_BF16) -> int:
+    return int(load().spec_verify_workspace_size(B, k, V, dtype))
+
+
+def spec_verify_greedy(logits, draft_tokens, out_tokens, num_accepted, ws, stream=None):
+    """logits [B,k+1,V] bf16/fp32, draft_tokens [B,k] int32 -> out_tokens [B,k+1], num_accepted [B]."""
+    B, k1, V = logits.shape
+    st = load().spec_verify_greedy(_ptr(logits), _dtype(logits), _ptr(draft_tokens), B, k1 - 1, V,
+                                   _ptr(out_tokens), _ptr(num_accepted), _ptr(ws), ws.numel(),
+                                   _stream(stream))
+    _check(st, "spec_verify_greedy")
+
+
+def spec_verify_sample(logits, draft_probs, draft_tokens, u_accept, u_resample, T, out_tokens,
+                       num_accepted, ws, stream=None):
+    B, k1, V = logits.shape
+    st = load().spec_verify_sample(_ptr(logits), _dtype(logits), _ptr(draft_probs),
+                                   _ptr(draft_tokens), _ptr(u_accept), _ptr(u_resample), float(T),
+                                   B, k1 - 1, V, _ptr(out_tokens), _ptr(num_accepted), _ptr(ws),
+                                   ws.numel(), _stream(stream))
+    _check(st, "spec_verify_sample")
+
+
+def spec_verify_rows(mode, logits, draft_probs, draft_tokens, T, ws, stream=None):
+    B, k1, V = logits.shape
+    st = load().spec_verify_rows(int(mode), _ptr(logits), _dtype(logits), _ptr(draft_probs),
+                                 _ptr(draft_tokens), float(T), B, k1 - 1, V, _ptr(ws), ws.numel(),
+                                 _stream(stream))
+    _check(st, "spec_verify_rows")
+
+
+def spec_verify_finish(mode, logits, draft_probs, draft_tokens, u_accept, u_resample, T,
+                       out_tokens, num_accepted, ws, stream=None):
+    B, k1, V = logits.shape
+    st = load().spec_verify_finish(int(mode), _ptr(logits), _dtype(logits), _ptr(draft_probs),
+                                   _ptr(draft_tokens), _ptr(u_accept), _ptr(u_resample), float(T),
+                                   B, k1 - 1, V, _ptr(out_tokens), _ptr(num_accepted), _ptr(ws),
+                                   ws.numel(), _stream(stream))
+    _check(st, "spec_verify_finish")
+
+
+def spec_verify_read_status(ws, stream=None):
+    """(status code, device status bits, number of zero-mass residual draws); syncs the stream."""
+    bits = ctypes.c_uint32(0)
+    ndeg = ctypes.c_uint32(0)
+    st = load().spec_verify_read_status(_ptr(ws), _stream(stream), ctypes.byref(bits),
+                                        ctypes.byref(ndeg))
+    if st not in (SV_OK, SV_ERR_DATA):
+        raise SpecVerifyError(st, "spec_verify_read_status")
+    return st, int(bits.value), int(ndeg.value)
+
+
+def spec_verify_row_stats(ws, B, k, stream=None):
+    """Per-row statistics of the last call on ``ws`` as numpy arrays [B, k+1]."""
+    import numpy as np
+    R = B * (k + 1)
+    m = np.zeros(R, np.float32)
+    S = np.zeros(R, np.float32)
+    am = np.zeros(R, np.int32)
+    px = np.zeros(R, np.float32)
+    qx = np.zeros(R, np.float32)
+    c = lambda a: a.ctypes.data_as(ctypes.c_void_p)
+    st = load().spec_verify_row_stats(_ptr(ws), _stream(stream), B, k, c(m), c(S), c(am), c(px),
+                                      c(qx))
+    _check(st, "spec_verify_row_stats")
+    sh = (B, k + 1)
+    return dict(m=m.reshape(sh), S=S.reshape(sh), argmax=am.reshape(sh), px=px.reshape(sh),
+                qx=qx.reshape(sh))
+
+
+def spec_verify_status_string(status: int) -> str:
+    return status_string(status)
+
+
+def debug_ffexp(l, m: float, T: float, stream=None):
+    """exp((l - m)/T) by the draw's float-float exponential (test hook), as float64."""
+    out = torch.empty(l.numel(), dtype=torch.float64, device=l.device)
+    st = load().spec_verify_debug_ffexp(_ptr(l), float(m), float(T), l.numel(), _ptr(out),
+                                        _stream(stream))
+    _check(st, "spec_verify_debug_ffexp")
+    return out
+
+
+# ---------------------------------------------------------------- convenience
+
+def workspace(B, k, V, dtype=torch.bfloat16, device=None):
+    """A workspace tensor of the required size (bytes, uint8)."""
+    n = spec_verify_workspace_size(B, k, V, SV_BF16 if dtype == torch.bfloat16 else SV_F32)
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device or "cuda")
+
+
+def verify_greedy(logits, draft_tokens, ws=None, stream=None):
+    B, k1, V = logits.shape
+    out = torch.empty((B, k1), dtype=torch.int32, device=logits.device)
+    n = torch.empty(B, dtype=torch.int32, device=logits.device)
+    if ws is None:
+        ws = workspace(B, k1 - 1, V, logits.dtype, logits.device)
+    spec_verify_greedy(logits, draft_tokens, out, n, ws, stream)
+    return out, n
+
+
+def verify_sample(logits, draft_probs, draft_tokens, u_accept, u_resample, T, ws=None,
+                  stream=None):
+    B, k1, V = logits.shape
+    out = torch.empty((B, k1), dtype=torch.int32, device=logits.device)
+    n = torch.empty(B, dtype=torch.int32, device=logits.device)
+    if ws is None:
+        ws = workspace(B, k1 - 1, V, logits.dtype, logits.device)
+    spec_verify_sample(logits, draft_probs, draft_tokens, u_accept, u_resample, T, out, n, ws,
+                       stream)
+    return out, n

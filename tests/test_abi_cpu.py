@@ -1,0 +1,93 @@
+"""The C ABI without a GPU: the library loads, exports every declared symbol,
+and rejects bad arguments synchronously, before touching the CUDA runtime."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+HEADERS = [os.path.join(ROOT, "include", h) for h in ("specverify.h", "specverify_debug.h")]
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from speculative_decoding_verification_18_gb300 import build
+    build.build()
+    from speculative_decoding_verification_18_gb300 import specverify
+    return specverify.load()
+
+
+def declared():
+    names = []
+    for h in HEADERS:
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"\b(spec_verify_\w+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_workspace_size(lib):
+    from speculative_decoding_verification_18_gb300 import specverify as sv
+    assert sv.spec_verify_workspace_size(64, 4, 32000) == 256 + 64 * 5 * 32
+    assert sv.spec_verify_workspace_size(1, 1, 1) == 512
+    assert sv.spec_verify_workspace_size(0, 4, 10) == 256
+    assert sv.spec_verify_workspace_size(1, 0, 10) == 0
+    assert sv.spec_verify_workspace_size(1, 65, 10) == 0
+    assert sv.spec_verify_workspace_size(1, 4, (1 << 21) + 1) == 0
+    assert sv.spec_verify_workspace_size(1, 4, 10, 7) == 0
+
+
+def test_argument_errors_without_gpu(lib):
+    from speculative_decoding_verification_18_gb300 import specverify as sv
+    P = 4096  # a 16-byte-aligned fake address: never dereferenced on these paths
+    ws = sv.spec_verify_workspace_size(2, 3, 100)
+    args = lambda **kw: dict(dict(l=P, dt=sv.SV_F32, q=P, x=P, ua=P, ur=P, T=1.0, B=2, k=3,
+                                  V=100, out=P, n=P, ws=P, wsb=ws), **kw)
+
+    def sample(**kw):
+        a = args(**kw)
+        return lib.spec_verify_sample(a["l"], a["dt"], a["q"], a["x"], a["ua"], a["ur"], a["T"],
+                                      a["B"], a["k"], a["V"], a["out"], a["n"], a["ws"], a["wsb"],
+                                      None)
+
+    assert sample(l=None) == sv.SV_ERR_INVALID_ARG
+    assert sample(q=None) == sv.SV_ERR_INVALID_ARG
+    assert sample(T=0.0) == sv.SV_ERR_INVALID_ARG
+    assert sample(T=float("nan")) == sv.SV_ERR_INVALID_ARG
+    assert sample(T=float("inf")) == sv.SV_ERR_INVALID_ARG
+    assert sample(l=P + 2) == sv.SV_ERR_INVALID_ARG           # misaligned
+    assert sample(ws=None) == sv.SV_ERR_WORKSPACE
+    assert sample(wsb=ws - 1) == sv.SV_ERR_WORKSPACE
+    assert sample(k=65, wsb=1 << 20) == sv.SV_ERR_UNSUPPORTED
+    assert sample(V=0) == sv.SV_ERR_INVALID_ARG
+    assert sample(B=-1) == sv.SV_ERR_INVALID_ARG
+    assert sample(dt=9) == sv.SV_ERR_INVALID_ARG
+    assert lib.spec_verify_greedy(None, 0, P, 2, 3, 100, P, P, P, ws, None) == sv.SV_ERR_INVALID_ARG
+    assert lib.spec_verify_greedy(P, 0, P, 2, 3, 100, None, P, P, ws, None) == sv.SV_ERR_INVALID_ARG
+    assert lib.spec_verify_rows(7, P, 0, P, P, 1.0, 2, 3, 100, P, ws, None) == sv.SV_ERR_INVALID_ARG
+    assert lib.spec_verify_read_status(None, None, None, None) == sv.SV_ERR_INVALID_ARG
+    assert lib.spec_verify_debug_ffexp(None, 0.0, 1.0, 5, None, None) == sv.SV_ERR_INVALID_ARG
+
+
+def test_status_strings(lib):
+    from speculative_decoding_verification_18_gb300 import specverify as sv
+    seen = {sv.status_string(s) for s in range(7)}
+    assert len(seen) == 7 and "ok" in seen
+    assert sv.status_string(99) == "unknown status"
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    from speculative_decoding_verification_18_gb300 import specverify as sv
+    monkeypatch.setattr(sv, "_lib", None)
+    monkeypatch.setattr(sv, "LIB", str(tmp_path / "missing.so"))
+    with pytest.raises(ImportError):
+        sv.load()
