@@ -142,6 +142,35 @@ sv_status spec_verify_finish(sv_mode mode, const void* logits, sv_dtype dtype,
                              int32_t* num_accepted, void* ws, size_t ws_bytes,
                              cudaStream_t stream);
 
+/* Sampled verify for callers that cannot allocate device memory.  Some callers
+ * are handed only their input and output tensors and have no way to allocate a
+ * workspace: operator plug-ins inside an inference engine that owns all device
+ * memory, or serving loops that forbid device allocation once they have started
+ * (an allocation can synchronise the device and stall every stream).  This entry
+ * point takes the same arguments as spec_verify_sample minus the workspace, and
+ * keeps its scratch in a fixed array inside this library instead.  (The pages
+ * describe no such variant; it is an interface convenience.)
+ *   - Limit: B*(k+1) <= SV_NOALLOC_MAX_ROWS rows; larger batches return
+ *     SV_ERR_WORKSPACE and launch nothing.  The array is SV_NOALLOC_SCRATCH_BYTES
+ *     of device memory, held by every GPU that loads the library until exit.
+ *   - The first call made with a given device current looks up the array's
+ *     device address (cudaGetSymbolAddress) and caches it; make that first call
+ *     before any stream capture begins on that device.
+ *   - Every call shares the one array and leaves its contents behind; nothing in
+ *     it needs to start at zero, because each call writes every header field and
+ *     row record before reading it.  Calls that overlap on the GPU (for example
+ *     on two streams at once) race on the array and must be avoided.
+ *   - It allocates nothing and calls no allocating routine; the result and the
+ *     device-detected data errors (num_accepted = -1) are as for
+ *     spec_verify_sample. */
+#define SV_NOALLOC_SCRATCH_BYTES 1048576
+#define SV_NOALLOC_MAX_ROWS 32760
+sv_status spec_verify_sample_noalloc(const void* logits, sv_dtype dtype,
+                                     const float* draft_probs, const int32_t* draft_tokens,
+                                     const float* u_accept, const float* u_resample, float T,
+                                     int B, int k, int V, int32_t* out_tokens,
+                                     int32_t* num_accepted, cudaStream_t stream);
+
 /* Synchronises `stream`, then copies the device status word of the last call
  * that used `ws` into *device_status (SV_DEV_* bits).  Returns SV_ERR_DATA if
  * any error bit (all but SV_DEV_DEGENERATE) is set, else SV_OK.

@@ -1145,3 +1145,56 @@ sv_status spec_verify_debug_ffexp(const float* l, float m, float T, int n, doubl
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------ entry point without allocation
+//
+// spec_verify_sample with its scratch in a fixed device array of this library
+// instead of a caller-provided workspace.  The array's name is only a host-side
+// handle; its device address is looked up once per device with
+// cudaGetSymbolAddress and then passed to the kernels like any workspace.
+namespace sv {
+
+constexpr size_t kNoAllocScratchBytes = SV_NOALLOC_SCRATCH_BYTES;
+static_assert(kNoAllocScratchBytes >= 256 + 32 * (size_t)SV_NOALLOC_MAX_ROWS, "scratch size");
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+static std::mutex g_noalloc_mu;
+static void* g_noalloc_addr[64];
+
+// Device address of the scratch array on the current device (looked up on the
+// first call made with that device current, then cached).
+static sv_status noalloc_scratch(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SV_ERR_CUDA;
+    if (dev < 0 || dev >= 64) return SV_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+            return SV_ERR_CUDA;
+        g_noalloc_addr[dev] = p;
+    }
+    *out = g_noalloc_addr[dev];
+    return SV_OK;
+}
+
+}  // namespace sv
+
+extern "C" sv_status spec_verify_sample_noalloc(const void* logits, sv_dtype dtype,
+                                                const float* draft_probs,
+                                                const int32_t* draft_tokens,
+                                                const float* u_accept, const float* u_resample,
+                                                float T, int B, int k, int V,
+                                                int32_t* out_tokens, int32_t* num_accepted,
+                                                cudaStream_t stream) {
+    if (B < 0 || k < 1 || V < 1) return SV_ERR_INVALID_ARG;
+    if (k > sv::kMaxK || V > sv::kMaxV) return SV_ERR_UNSUPPORTED;
+    if ((long long)B * (k + 1) > SV_NOALLOC_MAX_ROWS) return SV_ERR_WORKSPACE;
+    void* ws = nullptr;
+    sv_status st = sv::noalloc_scratch(&ws);
+    if (st != SV_OK) return st;
+    return spec_verify_sample(logits, dtype, draft_probs, draft_tokens, u_accept, u_resample, T,
+                              B, k, V, out_tokens, num_accepted, ws, sv::kNoAllocScratchBytes,
+                              stream);
+}

@@ -24,7 +24,9 @@ SV_DEV_BAD_ROW, SV_DEV_BAD_TOKEN, SV_DEV_BAD_UNIFORM, SV_DEV_BAD_Q, SV_DEV_DEGEN
 
 EXPORTS = ("spec_verify_workspace_size", "spec_verify_greedy", "spec_verify_sample",
            "spec_verify_rows", "spec_verify_finish", "spec_verify_read_status",
-           "spec_verify_row_stats", "spec_verify_status_string")
+           "spec_verify_row_stats", "spec_verify_status_string", "spec_verify_sample_noalloc")
+SV_NOALLOC_SCRATCH_BYTES = 1048576
+SV_NOALLOC_MAX_ROWS = 32760
 
 _lib = None
 
@@ -61,6 +63,8 @@ def load():
     lib.spec_verify_row_stats.restype = I
     lib.spec_verify_status_string.argtypes = [I]
     lib.spec_verify_status_string.restype = ctypes.c_char_p
+    lib.spec_verify_sample_noalloc.argtypes = [P, I, P, P, P, P, F, I, I, I, P, P, P]
+    lib.spec_verify_sample_noalloc.restype = I
     lib.spec_verify_debug_ffexp.argtypes = [P, F, F, I, P, P]
     lib.spec_verify_debug_ffexp.restype = I
     _lib = lib
@@ -123,6 +127,18 @@ def spec_verify_sample(logits, draft_probs, draft_tokens, u_accept, u_resample, 
                                    B, k1 - 1, V, _ptr(out_tokens), _ptr(num_accepted), _ptr(ws),
                                    ws.numel(), _stream(stream))
     _check(st, "spec_verify_sample")
+
+
+def spec_verify_sample_noalloc(logits, draft_probs, draft_tokens, u_accept, u_resample, T,
+                               out_tokens, num_accepted, stream=None):
+    """spec_verify_sample without a workspace: scratch lives in a fixed device array
+    of the library (B*(k+1) <= SV_NOALLOC_MAX_ROWS)."""
+    B, k1, V = logits.shape
+    st = load().spec_verify_sample_noalloc(_ptr(logits), _dtype(logits), _ptr(draft_probs),
+                                           _ptr(draft_tokens), _ptr(u_accept), _ptr(u_resample),
+                                           float(T), B, k1 - 1, V, _ptr(out_tokens),
+                                           _ptr(num_accepted), _stream(stream))
+    _check(st, "spec_verify_sample_noalloc")
 
 
 def spec_verify_rows(mode, logits, draft_probs, draft_tokens, T, ws, stream=None):
