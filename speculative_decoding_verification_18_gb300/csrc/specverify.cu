@@ -1,33 +1,39 @@
 // specverify: batched speculative-decoding verify on GB300 (sm_103a).
 //
-// Three kernels, launched back to back on the caller's stream:
+// The one-call entry points run ONE kernel, sv_verify_kernel: a thread-block
+// cluster of G CTAs per sequence (distributed shared memory, hardware cluster
+// barriers; no global-memory handshakes) does the whole verify of that
+// sequence:
 //
-//  1. sv_rows_kernel — the only pass over the whole logits tensor.  One CTA (or
-//     one thread-block cluster of G CTAs splitting the vocabulary when there are
-//     too few rows to fill the 152 SMs) streams each row once with 16-byte
-//     coalesced loads and keeps an online max / sum-of-exponentials per thread
-//     (one ex2 per element, rescaled only when the running max moves), plus the
-//     first index of the maximum.  Threads merge with warp shuffles, warps through
-//     shared memory, and the CTAs of a cluster through distributed shared memory
-//     (DSMEM) into rank 0, which gathers l(x) and q(x) for the row's draft token
-//     and writes one 32-byte record per row to the workspace.
-//     Softmax statistics: "Speculative Decoding" (ch15, LLM serving from
-//     scratch), §"Why the result is exactly the target model" (accept_sampled
-//     takes the target logits); p = softmax(l/T).
-//  2. sv_scan_greedy_kernel (greedy) — one thread per sequence: accept while the
-//     draft equals the row's argmax, emit argmax at the first mismatch or the
-//     bonus ("Decodificação especulativa explicada: rascunhe barato, verifique
-//     numa passada", §"A regra de amostragem por rejeição", greedy case).
-//  3. sv_draw_kernel (sampled) — one cluster per sequence: the accept scan on
-//     the row records (min(1, p/q) in double, §"A regra de amostragem por
-//     rejeição", rule 1), then the draw from the one decision row: the residual
-//     norm(max(0, p - q)) at a rejection (rule 2) or p itself for the bonus
-//     (rule 3).  The draw recomputes that row's exponentials in float-float,
-//     sums them exactly enough (~2^-47) for the normaliser, turns every weight
-//     into a 62-bit fixed-point integer so that all prefix sums are exact and
-//     order-independent, and locates the first j with C_j > u * C_{V-1} (the
-//     right-sided search of §"Amostragem especulativa em numpy, com prova")
-//     with a cluster-wide exclusive scan through DSMEM.
+//  1. Row statistics ("Speculative Decoding" (ch15, LLM serving from scratch),
+//     §"Why the result is exactly the target model": the target's logits in,
+//     p = softmax(l/T)): every CTA streams its vocabulary slice of the rows
+//     with 16-byte coalesced loads and keeps an online max / sum-of-exponentials
+//     (one ex2 per element) and the first index of the maximum.  Rows are
+//     taken in waves: all k+1 at once when the batch is too small to fill the
+//     GPU, one at a time (stopping at the first rejection, so later rows are
+//     never read) when other sequences keep the HBM busy.  Warp shuffles,
+//     shared memory and DSMEM merge the partials; every CTA then holds the same
+//     row statistics.
+//  2. The accept scan ("Decodificação especulativa explicada: rascunhe barato,
+//     verifique numa passada", §"A regra de amostragem por rejeição": accept x
+//     with probability min(1, p(x)/q(x)), stop at the first rejection; greedy:
+//     accept while x == argmax p), computed redundantly by every CTA.
+//  3. The draw (same section, rules 2 and 3: the residual norm(max(0, p - q))
+//     at a rejection, p itself for the bonus; the categorical draw is the first
+//     j with C_j > u * C_{V-1}, the right-sided search of §"Amostragem
+//     especulativa em numpy, com prova").  The decision row's exponentials are
+//     recomputed in float-float (~48 bits), the normaliser summed to ~2^-47,
+//     and the weights turned into 60-bit fixed-point integers per 8-element
+//     chunk, so every prefix sum is exact and order-independent; a DSMEM scan
+//     over the cluster finds the CTA, a block scan the chunk, and one thread
+//     the token.
+//
+// The two-stage entry points (spec_verify_rows / spec_verify_finish) run the
+// same work as two kernels with the per-row statistics in the workspace:
+// sv_rows_kernel (one CTA or cluster per row) and sv_finish_greedy_kernel /
+// sv_finish_sample_kernel (one cluster per sequence), sharing the device code
+// above.
 //
 // Nothing here allocates memory, synchronises the host, or waits on another
 // CTA outside hardware cluster barriers.
@@ -39,6 +45,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <new>
 
 #include "../../include/specverify.h"
 #include "ff.cuh"
@@ -49,23 +56,22 @@ namespace sv {
 
 // ------------------------------------------------------------------ workspace
 
-constexpr uint32_t kMagic = 0x53564631u;  // "SVF1"
+constexpr uint32_t kMagic = 0x53564632u;  // "SVF2"
 constexpr int kMaxK = 64;
 constexpr int kMaxV = 1 << 21;
 
 struct alignas(16) Header {
-    uint32_t status;
-    uint32_t n_degenerate;
-    uint32_t B, k, V, mode, magic;
-    uint32_t pad[57];
+    uint32_t magic;
+    uint32_t B, k, V, mode;
+    uint32_t pad[59];
 };
 static_assert(sizeof(Header) == 256, "header size");
 
 // One record per logits row.
 struct alignas(16) RowRec {
-    float mraw;       // max_j l_j (raw logits)
-    float S;          // sum_j 2^((l_j - mraw) * log2(e)/T)  (sampled mode)
-    double px;        // p(x) = exp((l_x - mraw)/T) / S in double (sampled, rows < k)
+    float mraw;       // max_j l_j (raw logits); NaN for a row the scan never reached
+    float S;          // sum_j exp((l_j - mraw)/T)  (sampled mode)
+    double px;        // p(x) (sampled, rows < k)
     float lx;         // l[x]
     float qx;         // q[x]
     int32_t argmax;   // lowest index of the maximum raw logit
@@ -73,10 +79,15 @@ struct alignas(16) RowRec {
 };
 static_assert(sizeof(RowRec) == 32, "row record size");
 
-constexpr uint32_t kRowBad = 1u, kRowTokenBad = 2u, kRowQBad = 4u;
+constexpr uint32_t kRowBad = 1u, kRowTokenBad = 2u, kRowQBad = 4u, kRowSkipped = 8u;
 
-__host__ __device__ inline size_t ws_bytes_for(long long R) {
-    size_t b = sizeof(Header) + (size_t)R * sizeof(RowRec);
+// Layout: header | B*(k+1) row records | B per-sequence status words.
+__host__ __device__ inline size_t ws_rows_offset() { return sizeof(Header); }
+__host__ __device__ inline size_t ws_seq_offset(long long B, int k) {
+    return sizeof(Header) + (size_t)B * (k + 1) * sizeof(RowRec);
+}
+__host__ __device__ inline size_t ws_bytes_for(long long B, int k) {
+    size_t b = ws_seq_offset(B, k) + (size_t)B * sizeof(uint32_t);
     return (b + 255) & ~(size_t)255;
 }
 
@@ -128,97 +139,57 @@ __device__ __forceinline__ uint4 ld_stream16(const uint4* p) {
     return v;
 }
 
-// Online softmax partial of one thread: running max m, sum s of 2^((l-m)c),
-// index of the first maximum (or the first index of the 16-byte vector holding
-// it, resolved at the end), and a NaN flag (greedy mode, which forms no sum).
+// ------------------------------------------------------------------ online softmax partials
+
+// Running max m (raw logits), sum s of 2^((l - m) c), index of the first maximum,
+// and a NaN flag (greedy mode, which forms no sum that would carry the NaN).
 struct Partial {
     float m, s;
     int idx;
-    int vec;   // 1 if idx is the start of an unresolved vector
     int nan;
 };
 
-// Merge b into a (a holds lower-or-equal indices on ties only by the explicit
-// index comparison, so the merge order does not matter).
+__device__ __forceinline__ Partial empty_partial() { return Partial{-INFINITY, 0.0f, -1, 0}; }
+
 template <bool SAMPLED>
-__device__ __forceinline__ void merge(Partial& a, float bm, float bs, int bidx, int bnan,
-                                      float c) {
-    float mn = fmaxf(a.m, bm);
+__device__ __forceinline__ void merge(Partial& a, const Partial& b, float c) {
+    float mn = fmaxf(a.m, b.m);
     if (SAMPLED) {
         float fa = (a.m == mn) ? 1.0f : ex2_approx((a.m - mn) * c);
-        float fb = (bm == mn) ? 1.0f : ex2_approx((bm - mn) * c);
-        a.s = a.s * fa + bs * fb;
+        float fb = (b.m == mn) ? 1.0f : ex2_approx((b.m - mn) * c);
+        a.s = a.s * fa + b.s * fb;
     }
-    if (bm > a.m || (bm == a.m && (unsigned)bidx < (unsigned)a.idx)) a.idx = bidx;
+    if (b.m > a.m || (b.m == a.m && (unsigned)b.idx < (unsigned)a.idx)) a.idx = b.idx;
     a.m = mn;
-    a.nan |= bnan;
+    a.nan |= b.nan;
 }
 
-// ------------------------------------------------------------------ kernel 1: row stream
+template <bool SAMPLED>
+__device__ __forceinline__ Partial warp_merge(Partial p, float c) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        Partial o;
+        o.m = __shfl_xor_sync(0xffffffffu, p.m, off);
+        o.s = __shfl_xor_sync(0xffffffffu, p.s, off);
+        o.idx = __shfl_xor_sync(0xffffffffu, p.idx, off);
+        o.nan = __shfl_xor_sync(0xffffffffu, p.nan, off);
+        merge<SAMPLED>(p, o, c);
+    }
+    return p;
+}
 
-struct RowsArgs {
-    const void* logits;
-    const float* q;
-    const int32_t* x;
-    Header* hdr;
-    RowRec* rows;
-    int B, k, V, G, mode;
-    float c;        // log2(e) / T
-    double T;
-};
-
-template <typename DT, bool SAMPLED, int kThreads>
-__global__ void __launch_bounds__(kThreads) sv_rows_kernel(RowsArgs a) {
+// One thread's share of a vocabulary slice of one row: vectors [vb, ve) of the
+// row's aligned body handled by threads tg = 0..ng-1 (stride ng), plus the
+// unaligned head (if `head_here`) and tail (if `tail_here`) as scalars.
+template <typename DT, bool SAMPLED, int U>
+__device__ __forceinline__ Partial stream_slice(const DT* __restrict__ rowp, int V, long long vb,
+                                                long long ve, int head, long long tail0,
+                                                bool head_here, bool tail_here, int tg, int ng,
+                                                float c) {
     using E = Elt<DT>;
     constexpr int VW = E::kVec;
-    constexpr int kWarps = kThreads / 32;
-    const int tid = threadIdx.x;
-    const int G = a.G;
-    const long long row = blockIdx.x / G;
-    const int rank = blockIdx.x % G;  // == cluster rank: clusters are (G,1,1) along x
-    const int V = a.V;
-    const DT* rowp = static_cast<const DT*>(a.logits) + row * (long long)V;
-
-    if (blockIdx.x == 0 && tid == 0) {
-        a.hdr->status = 0;
-        a.hdr->n_degenerate = 0;
-        a.hdr->B = a.B;
-        a.hdr->k = a.k;
-        a.hdr->V = V;
-        a.hdr->mode = a.mode;
-        a.hdr->magic = kMagic;
-    }
-
-    // Gather of the draft token's logit and q (rank 0, last thread: issued early,
-    // consumed at the end).
-    const int b = (int)(row / (a.k + 1));
-    const int i = (int)(row % (a.k + 1));
-    int xi = -1;
-    float lx = NAN, qx = NAN;
-    uint32_t gflags = 0;
-    if (rank == 0 && tid == kThreads - 1 && i < a.k) {
-        xi = a.x[(long long)b * a.k + i];
-        if (xi < 0 || xi >= V) {
-            gflags |= kRowTokenBad;
-        } else {
-            lx = E::load1(rowp + xi);
-            if (SAMPLED) qx = a.q[((long long)b * a.k + i) * V + xi];
-        }
-    }
-
-    // Row layout: [0, head) unaligned scalars, then nvec 16-byte vectors, then a
-    // scalar tail.  The vectors are split evenly over the G ranks.
-    const uintptr_t addr = reinterpret_cast<uintptr_t>(rowp);
-    int head = (int)(((16 - (addr & 15)) & 15) / sizeof(DT));
-    if (head > V) head = V;
-    const long long nvec = (V - head) / VW;
-    const long long tail0 = head + nvec * VW;
-    const long long vb = nvec * rank / G, ve = nvec * (rank + 1) / G;
-    const uint4* vp = reinterpret_cast<const uint4*>(rowp + head);
-
-    Partial p{-INFINITY, 0.0f, -1, 0, 0};
-    const float c = a.c;
-
+    Partial p = empty_partial();
+    int best_vec = 0;  // p.idx names the first element of a vector to resolve at the end
     auto scalar = [&](long long j) {
         float v = E::load1(rowp + j);
         if (!SAMPLED) p.nan |= (v != v);
@@ -226,7 +197,7 @@ __global__ void __launch_bounds__(kThreads) sv_rows_kernel(RowsArgs a) {
             if (SAMPLED) p.s *= ex2_approx((p.m - v) * c);
             p.m = v;
             p.idx = (int)j;
-            p.vec = 0;
+            best_vec = 0;
         }
         if (SAMPLED) p.s += ex2_approx((v - p.m) * c);
     };
@@ -241,7 +212,7 @@ __global__ void __launch_bounds__(kThreads) sv_rows_kernel(RowsArgs a) {
             if (SAMPLED) p.s *= ex2_approx((p.m - vmax) * c);
             p.m = vmax;
             p.idx = (int)j0;
-            p.vec = 1;
+            best_vec = 1;
         }
         if (SAMPLED) {
             float acc = 0.0f;
@@ -250,197 +221,56 @@ __global__ void __launch_bounds__(kThreads) sv_rows_kernel(RowsArgs a) {
             p.s += acc;
         }
     };
-
-    if (rank == 0)
-        for (long long j = tid; j < head; j += kThreads) scalar(j);
-    constexpr int U = 4;
-    long long v = vb + tid;
-    for (; v + (U - 1) * kThreads < ve; v += U * kThreads) {
+    if (head_here)
+        for (long long j = tg; j < head; j += ng) scalar(j);
+    const uint4* vp = reinterpret_cast<const uint4*>(rowp + head);
+    long long v = vb + tg;
+    for (; v + (long long)(U - 1) * ng < ve; v += (long long)U * ng) {
         uint4 buf[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) buf[u] = ld_stream16(vp + v + u * kThreads);
+        for (int u = 0; u < U; ++u) buf[u] = ld_stream16(vp + v + (long long)u * ng);
 #pragma unroll
-        for (int u = 0; u < U; ++u) vector(buf[u], head + (v + u * kThreads) * VW);
+        for (int u = 0; u < U; ++u) vector(buf[u], head + (v + (long long)u * ng) * VW);
     }
-    for (; v < ve; v += kThreads) vector(ld_stream16(vp + v), head + v * VW);
-    if (rank == G - 1)
-        for (long long j = tail0 + tid; j < V; j += kThreads) scalar(j);
-
-    // Resolve the index of the first maximum inside its vector.
-    if (p.vec) {
+    for (; v < ve; v += ng) vector(ld_stream16(vp + v), head + v * VW);
+    if (tail_here)
+        for (long long j = tail0 + tg; j < V; j += ng) scalar(j);
+    if (best_vec) {  // first element equal to the maximum inside its vector
         float f[VW];
         E::unpack(*reinterpret_cast<const uint4*>(rowp + p.idx), f);
         int e = 0;
         while (e < VW - 1 && !(f[e] == p.m)) ++e;
         p.idx += e;
-        p.vec = 0;
     }
+    return p;
+}
 
-    // Warp, then CTA reduction.
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        float om = __shfl_xor_sync(0xffffffffu, p.m, off);
-        float os = __shfl_xor_sync(0xffffffffu, p.s, off);
-        int oi = __shfl_xor_sync(0xffffffffu, p.idx, off);
-        int on = __shfl_xor_sync(0xffffffffu, p.nan, off);
-        merge<SAMPLED>(p, om, os, oi, on, c);
-    }
-    __shared__ float sm_m[kWarps], sm_s[kWarps];
-    __shared__ int sm_i[kWarps], sm_n[kWarps];
-    __shared__ Partial cta_part;  // read by cluster rank 0 through DSMEM
-    const int warp = tid >> 5, lane = tid & 31;
-    if (lane == 0) {
-        sm_m[warp] = p.m;
-        sm_s[warp] = p.s;
-        sm_i[warp] = p.idx;
-        sm_n[warp] = p.nan;
-    }
-    __syncthreads();
-    if (warp == 0) {
-        Partial w{-INFINITY, 0.0f, -1, 0, 0};
-        if (lane < kWarps) w = Partial{sm_m[lane], sm_s[lane], sm_i[lane], 0, sm_n[lane]};
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            float om = __shfl_xor_sync(0xffffffffu, w.m, off);
-            float os = __shfl_xor_sync(0xffffffffu, w.s, off);
-            int oi = __shfl_xor_sync(0xffffffffu, w.idx, off);
-            int on = __shfl_xor_sync(0xffffffffu, w.nan, off);
-            merge<SAMPLED>(w, om, os, oi, on, c);
-        }
-        p = w;
-        if (lane == 0) cta_part = w;
-    }
+// Aligned body of a row: `head` unaligned leading elements, `nvec` 16-byte
+// vectors, scalars from `tail0`.
+template <typename DT>
+__device__ __forceinline__ void row_layout(const DT* rowp, int V, int& head, long long& nvec,
+                                           long long& tail0) {
+    const uintptr_t addr = reinterpret_cast<uintptr_t>(rowp);
+    head = (int)(((16 - (addr & 15)) & 15) / sizeof(DT));
+    if (head > V) head = V;
+    nvec = (V - head) / Elt<DT>::kVec;
+    tail0 = head + nvec * Elt<DT>::kVec;
+}
 
-    if (G > 1) {
-        cg::cluster_group cluster = cg::this_cluster();
-        cluster.sync();
-        if (rank == 0 && warp == 0) {
-            Partial w{-INFINITY, 0.0f, -1, 0, 0};
-            if (lane < G) w = *cluster.map_shared_rank(&cta_part, lane);
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                float om = __shfl_xor_sync(0xffffffffu, w.m, off);
-                float os = __shfl_xor_sync(0xffffffffu, w.s, off);
-                int oi = __shfl_xor_sync(0xffffffffu, w.idx, off);
-                int on = __shfl_xor_sync(0xffffffffu, w.nan, off);
-                merge<SAMPLED>(w, om, os, oi, on, c);
-            }
-            p = w;
-        }
-        cluster.sync();  // keep every CTA's shared memory alive until rank 0 has read it
-    }
-
-    if (rank != 0) return;
-    // The gather lives in the last thread; hand it to thread 0 through shared memory.
-    __shared__ int g_x;
-    __shared__ float g_lx, g_qx;
-    __shared__ uint32_t g_fl;
-    if (tid == kThreads - 1) {
-        g_x = xi;
-        g_lx = lx;
-        g_qx = qx;
-        g_fl = gflags;
-    }
-    __syncthreads();
-    if (tid != 0) return;
-    RowRec rec;
-    rec.mraw = p.m;
-    rec.S = SAMPLED ? p.s : 0.0f;
-    rec.argmax = p.idx < 0 ? 0 : p.idx;
-    rec.lx = g_lx;
-    rec.qx = g_qx;
-    rec.px = 0.0;
-    uint32_t fl = (i < a.k) ? g_fl : 0u;
+// kRowBad when the merged statistics show a NaN, a +inf, or an all -inf row.
+template <bool SAMPLED>
+__device__ __forceinline__ uint32_t row_flags(const Partial& p) {
     bool bad = !(p.m > -INFINITY) || p.m == INFINITY || p.nan;
     if (SAMPLED) bad = bad || !(p.s > 0.0f) || !(p.s < INFINITY);
-    if (bad) fl |= kRowBad;
-    if (SAMPLED && i < a.k && !(fl & (kRowBad | kRowTokenBad))) {
-        if (!(rec.qx >= 0.0f)) fl |= kRowQBad;  // NaN or negative
-        rec.px = exp(((double)rec.lx - (double)p.m) / a.T) / (double)p.s;
-    }
-    if (i == a.k) {
-        rec.lx = NAN;
-        rec.qx = NAN;
-        rec.px = NAN;
-    }
-    rec.flags = fl;
-    a.rows[row] = rec;
+    return bad ? kRowBad : 0u;
 }
 
-// ------------------------------------------------------------------ kernel 2: greedy scan
+// ------------------------------------------------------------------ draw phase
 
-__global__ void sv_scan_greedy_kernel(const int32_t* __restrict__ x, const RowRec* __restrict__ rows,
-                                      Header* hdr, int B, int k, int32_t* __restrict__ out,
-                                      int32_t* __restrict__ nacc) {
-    const int b = blockIdx.x * blockDim.x + threadIdx.x;
-    if (b >= B) return;
-    const RowRec* r = rows + (long long)b * (k + 1);
-    int32_t* o = out + (long long)b * (k + 1);
-    uint32_t bits = 0;
-    int n = k;
-    for (int i = 0; i < k; ++i) {
-        uint32_t fl = r[i].flags;
-        if (fl & kRowBad) { bits |= SV_DEV_BAD_ROW; break; }
-        if (fl & kRowTokenBad) { bits |= SV_DEV_BAD_TOKEN; break; }
-        if (x[(long long)b * k + i] != r[i].argmax) { n = i; break; }
-    }
-    if (!bits && (r[n].flags & kRowBad)) bits |= SV_DEV_BAD_ROW;
-    if (bits) {
-        for (int i = 0; i <= k; ++i) o[i] = -1;
-        nacc[b] = -1;
-        atomicOr(&hdr->status, bits);
-        return;
-    }
-    for (int i = 0; i < n; ++i) o[i] = x[(long long)b * k + i];
-    o[n] = r[n].argmax;
-    for (int i = n + 1; i <= k; ++i) o[i] = -1;
-    nacc[b] = n;
-}
-
-// ------------------------------------------------------------------ kernel 3: sampled scan + draw
-
-constexpr int kDrawThreads = 512;
-constexpr int kChunk = 8;           // contiguous elements per work item
-constexpr int kSegMax = 16384;      // elements of one CTA's segment kept in shared memory
-
-struct DrawArgs {
-    const void* logits;
-    const float* q;
-    const int32_t* x;
-    const float* ua;
-    const float* ur;
-    Header* hdr;
-    const RowRec* rows;
-    int32_t* out;
-    int32_t* nacc;
-    int B, k, V, G;
-    ff rT;          // 1/T in float-float
-    FFExpConst fc;
-};
-
-// uint64 fixed point: a weight w in [0, 1] becomes round(w * 2^62).
-__device__ __forceinline__ unsigned long long quantize(ff w) {
-    const float s = 4611686018427387904.0f;  // 2^62
-    long long h = __float2ll_rn(__fmul_rn(w.hi, s));
-    long long l = __float2ll_rn(__fmul_rn(w.lo, s));
-    return (unsigned long long)(h + l);
-}
-
-// floor(u * C) for u in [0, 1) given as a float, C < 2^64, exactly.
-__device__ __forceinline__ unsigned long long scale_floor(float u, unsigned long long C) {
-    uint32_t bits = __float_as_uint(u);
-    int ex = (int)((bits >> 23) & 0xFF);
-    unsigned long long mant = bits & 0x7FFFFF;
-    if (ex == 0) ex = 1;
-    else mant |= 0x800000;
-    if (mant == 0) return 0ull;
-    int sh = 150 - ex;  // u = mant * 2^-sh, sh >= 24 for u < 1
-    unsigned long long lo = mant * C;
-    unsigned long long hi = __umul64hi(mant, C);
-    if (sh >= 128) return 0ull;
-    if (sh >= 64) return hi >> (sh - 64);
-    return (lo >> sh) | (sh == 0 ? 0ull : (hi << (64 - sh)));
-}
+constexpr int kThreads = 512;       // threads per CTA of the per-sequence kernels
+constexpr int kWarps = kThreads / 32;
+constexpr int kChunk = 8;           // contiguous elements per draw work item
+constexpr int kSegStore = 10240;    // largest slice whose exponentials stay in shared memory
 
 template <typename DT>
 __device__ __forceinline__ void load_chunk(const DT* __restrict__ rowp, long long j0, int V,
@@ -475,17 +305,11 @@ __device__ __forceinline__ void load_q_chunk(const float* __restrict__ qrow, lon
     }
 }
 
-// e_j = exp((l_j - m)/T) in float-float; 0 below exp(-44) (such a weight is
-// below the 2^-62 resolution of the fixed-point sums once divided by S >= 1).
-__device__ __forceinline__ ff exp_elem(float l, float m, ff rT, const float* thi,
-                                       const float* tlo, const FFExpConst& fc) {
-    ff d = two_sum(l, -m);
-    ff y = ff_mul(d, rT);
-    if (!(y.hi >= -44.0f)) return ff{0.0f, 0.0f};  // also -inf logits
-    return ff_exp_neg(y, thi, tlo, fc.c1, fc.c2, fc.c3, fc.inv_l);
-}
-
-__device__ __forceinline__ ff weight(ff e, ff inv, float qv, bool residual) {
+// Weight of one element for the draw: p = e/S (bonus) or max(0, p - q)
+// (residual).  Elements with e*inv < q(1 - 2^-20) have p < q for certain and
+// weigh exactly 0 without the float-float work.
+__device__ __forceinline__ ff draw_weight(ff e, ff inv, float qv, bool residual) {
+    if (residual && __fmul_rn(e.hi, inv.hi) < __fmul_rn(qv, 0.99999905f)) return ff{0.0f, 0.0f};
     ff p = ff_mul(e, inv);
     if (!residual) return p;
     ff s = two_sum(p.hi, -qv);
@@ -511,160 +335,166 @@ __device__ __forceinline__ ff warp_sum_ff(ff v) {
     return v;
 }
 
+// floor(u * C) for u in [0, 1) given as a float, C < 2^64, exactly.
+__device__ __forceinline__ unsigned long long scale_floor(float u, unsigned long long C) {
+    uint32_t bits = __float_as_uint(u);
+    int ex = (int)((bits >> 23) & 0xFF);
+    unsigned long long mant = bits & 0x7FFFFF;
+    if (ex == 0) ex = 1;
+    else mant |= 0x800000;
+    if (mant == 0) return 0ull;
+    int sh = 150 - ex;  // u = mant * 2^-sh, sh >= 24 for u < 1
+    unsigned long long lo = mant * C;
+    unsigned long long hi = __umul64hi(mant, C);
+    if (sh >= 128) return 0ull;
+    if (sh >= 64) return hi >> (sh - 64);
+    return (lo >> sh) | (hi << (64 - sh));
+}
+
+// Shared memory the draw phase needs besides its dynamic arrays.
+struct DrawShared {
+    float thi[kExpTable], tlo[kExpTable];
+    ff red_ff[kWarps];
+    unsigned long long red_u[kWarps];
+    unsigned long long woff[kWarps];
+    ff slot_S;                     // this CTA's partial normaliser (read through DSMEM)
+    unsigned long long slot_W[2];  // this CTA's weight totals (read through DSMEM)
+    ff S_tot;
+    unsigned long long prefix, total;
+};
+
+__device__ const Exp2Table g_exp2_table = make_exp2_table();
+
+__device__ __forceinline__ void load_exp_table(DrawShared& sh) {
+    for (int i = threadIdx.x; i < kExpTable; i += blockDim.x) {
+        sh.thi[i] = g_exp2_table.hi[i];
+        sh.tlo[i] = g_exp2_table.lo[i];
+    }
+}
+
+// Chunk-level weight of the chunk starting at element j0: the float-float sum of
+// its eight weights, quantised.  Element-level cumulative values inside the
+// chunk are quantisations of the partial sums in the same order, so the last
+// one equals the chunk value exactly.  With `token` set, the first element
+// whose cumulative value exceeds `want` is stored there.
 template <typename DT, bool STORE>
-__global__ void __launch_bounds__(kDrawThreads) sv_draw_kernel(DrawArgs a) {
-    constexpr int kWarps = kDrawThreads / 32;
-    extern __shared__ __align__(16) unsigned char dyn[];
-    __shared__ RowRec recs[kMaxK + 1];
-    __shared__ float s_ua[kMaxK];
-    __shared__ float thi[64], tlo[64];
-    __shared__ int s_n, s_valid;
-    __shared__ uint32_t s_bits;
-    __shared__ ff red_ff[kWarps];
-    __shared__ unsigned long long red_u[kWarps];
-    __shared__ ff slot_S;                      // this CTA's partial normaliser (DSMEM)
-    __shared__ unsigned long long slot_W[2];   // this CTA's residual / fallback totals (DSMEM)
-    __shared__ unsigned long long s_scan[kDrawThreads];
+__device__ __forceinline__ unsigned long long chunk_weight(
+    const DT* __restrict__ rowp, const float* __restrict__ qrow, long long j0, int V, bool al_l,
+    bool al_q, bool residual, float m, ff c, ff inv, const float* ehi, const float* elo,
+    int cidx, int nchs, const DrawShared& sh, unsigned long long want, int* token) {
+    float lf[kChunk], qf[kChunk];
+    if (!STORE) load_chunk<DT>(rowp, j0, V, al_l, lf);
+    if (residual) load_q_chunk(qrow, j0, V, al_q, qf);
+    ff acc{0.0f, 0.0f};
+#pragma unroll
+    for (int e = 0; e < kChunk; ++e) {
+        ff ev = STORE ? ff{ehi[e * nchs + cidx], elo[e * nchs + cidx]}
+                      : exp_rel(lf[e], m, c, sh.thi, sh.tlo);
+        ff w = draw_weight(ev, inv, residual ? qf[e] : 0.0f, residual);
+        ff_accumulate(acc, w);
+        if (token && *token < 0 && w.hi > 0.0f && to_fixed(ff_normalize(acc)) > want)
+            *token = (int)(j0 + e);
+    }
+    return to_fixed(ff_normalize(acc));
+}
 
+// The draw on one row by the G CTAs of a cluster (every CTA calls it; rank r
+// owns chunks [nch*r/G, nch*(r+1)/G)).  The token is written to *token_out by
+// the owning thread only; `degenerate` is set in all threads.
+template <typename DT, bool STORE>
+__device__ void draw_phase(cg::cluster_group& cluster, DrawShared& sh, unsigned char* dyn,
+                           const DT* __restrict__ rowp, const float* __restrict__ qrow,
+                           bool residual, int V, float m, ff c, float u, int rank, int G,
+                           int32_t* token_out, bool& degenerate) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int G = a.G;
-    const int b = blockIdx.x / G;
-    const int rank = blockIdx.x % G;
-    const int k = a.k, V = a.V;
-
-    if (tid < 64) {
-        thi[tid] = a.fc.tbl_hi[tid];
-        tlo[tid] = a.fc.tbl_lo[tid];
-    }
-    for (int i = tid; i <= k; i += kDrawThreads) recs[i] = a.rows[(long long)b * (k + 1) + i];
-    for (int i = tid; i < k; i += kDrawThreads) s_ua[i] = a.ua[(long long)b * k + i];
-    __syncthreads();
-
-    // ---- accept scan (every CTA of the cluster computes the same result)
-    if (tid == 0) {
-        uint32_t bits = 0;
-        int n = k;
-        for (int i = 0; i < k; ++i) {
-            const RowRec& r = recs[i];
-            if (r.flags & kRowBad) { bits |= SV_DEV_BAD_ROW; break; }
-            if (r.flags & kRowTokenBad) { bits |= SV_DEV_BAD_TOKEN; break; }
-            float u = s_ua[i];
-            if (!(u >= 0.0f && u < 1.0f)) { bits |= SV_DEV_BAD_UNIFORM; break; }
-            if (r.flags & kRowQBad) { bits |= SV_DEV_BAD_Q; break; }
-            double P = r.px, Q = (double)r.qx;
-            bool accept = (P >= Q) || ((double)u < P / Q);
-            if (!accept) { n = i; break; }
-        }
-        if (!bits && (recs[n].flags & kRowBad)) bits |= SV_DEV_BAD_ROW;
-        if (!bits) {
-            float u = a.ur[b];
-            if (!(u >= 0.0f && u < 1.0f)) bits |= SV_DEV_BAD_UNIFORM;
-        }
-        s_n = n;
-        s_bits = bits;
-        s_valid = bits == 0;
-    }
-    __syncthreads();
-    const int n = s_n;
-    if (!s_valid) {
-        if (rank == 0) {
-            int32_t* o = a.out + (long long)b * (k + 1);
-            for (int i = tid; i <= k; i += kDrawThreads) o[i] = -1;
-            if (tid == 0) {
-                a.nacc[b] = -1;
-                atomicOr(&a.hdr->status, s_bits);
-            }
-        }
-        return;  // every CTA of the cluster takes this branch together
-    }
-
-    // ---- the draw on row n
-    cg::cluster_group cluster = cg::this_cluster();
-    const long long rowid = (long long)b * (k + 1) + n;
-    const DT* rowp = static_cast<const DT*>(a.logits) + rowid * V;
-    const bool residual = n < k;
-    const float* qrow = residual ? a.q + ((long long)b * k + n) * V : nullptr;
-    const float m = recs[n].mraw;
-    const float u = a.ur[b];
     const bool al_l = (reinterpret_cast<uintptr_t>(rowp) & 15) == 0;
     const bool al_q = residual && (reinterpret_cast<uintptr_t>(qrow) & 15) == 0;
-
     const long long nch = (V + kChunk - 1) / kChunk;
     const long long c0 = nch * rank / G, c1 = nch * (rank + 1) / G;
     const int mych = (int)(c1 - c0);
     float* ehi = reinterpret_cast<float*>(dyn);
-    float* elo = ehi + (STORE ? kSegMax : 0);
-    unsigned long long* csum =
-        reinterpret_cast<unsigned long long*>(dyn + (STORE ? 2 * kSegMax * sizeof(float) : 0));
+    float* elo = ehi + (STORE ? kSegStore : 0);
+    unsigned long long* csum = reinterpret_cast<unsigned long long*>(
+        dyn + (STORE ? 2 * kSegStore * sizeof(float) : 0));
+    const int nchs = STORE ? kSegStore / kChunk : 0;  // stride of the element-major e layout
 
-    // Pass A: e_j and the normaliser S = sum_j e_j.
+    // Pass A: e_j = exp((l_j - m)/T) and the normaliser S = sum_j e_j.
     ff acc{0.0f, 0.0f};
-    for (int c = tid; c < mych; c += kDrawThreads) {
-        const long long j0 = (c0 + c) * kChunk;
+    for (int ci = tid; ci < mych; ci += kThreads) {
+        const long long j0 = (c0 + ci) * kChunk;
         float f[kChunk];
         load_chunk<DT>(rowp, j0, V, al_l, f);
 #pragma unroll
         for (int e = 0; e < kChunk; ++e) {
-            ff ev = exp_elem(f[e], m, a.rT, thi, tlo, a.fc);
+            ff ev = exp_rel(f[e], m, c, sh.thi, sh.tlo);
             if (STORE) {
-                ehi[c * kChunk + e] = ev.hi;
-                elo[c * kChunk + e] = ev.lo;
+                ehi[e * nchs + ci] = ev.hi;
+                elo[e * nchs + ci] = ev.lo;
             }
-            acc = ff_add(acc, ev);
+            ff_accumulate(acc, ev);
         }
     }
-    acc = warp_sum_ff(acc);
-    if (lane == 0) red_ff[warp] = acc;
+    acc = warp_sum_ff(ff_normalize(acc));
+    if (lane == 0) sh.red_ff[warp] = acc;
     __syncthreads();
     if (warp == 0) {
-        ff w = lane < kWarps ? red_ff[lane] : ff{0.0f, 0.0f};
+        ff w = lane < kWarps ? sh.red_ff[lane] : ff{0.0f, 0.0f};
         w = warp_sum_ff(w);
-        if (lane == 0) slot_S = w;
+        if (lane == 0) sh.slot_S = w;
     }
     cluster.sync();
-    ff S{0.0f, 0.0f};
-    for (int r = 0; r < G; ++r) S = ff_add(S, *cluster.map_shared_rank(&slot_S, r));
-    const ff inv = ff_recip(S);
+    if (warp == 0) {
+        ff w = lane < G ? *cluster.map_shared_rank(&sh.slot_S, lane) : ff{0.0f, 0.0f};
+        w = warp_sum_ff(w);  // same tree in every CTA: identical S everywhere
+        if (lane == 0) sh.S_tot = w;
+    }
+    __syncthreads();
+    const ff inv = ff_recip(sh.S_tot);
 
-    // Pass B: fixed-point weights, per-chunk sums, CTA total; cluster prefix.
-    // A second round draws from p when the residual has no mass.
-    unsigned long long prefix = 0, total = 0, mytot = 0;
+    // Pass B: chunk weights, CTA total, cluster prefix; a second round draws
+    // from p when the residual has no mass.
     bool use_res = residual;
-    bool degenerate = false;
+    degenerate = false;
+    unsigned long long prefix = 0, total = 0, mytot = 0;
     for (int round = 0; round < 2; ++round) {
         unsigned long long tacc = 0;
-        for (int c = tid; c < mych; c += kDrawThreads) {
-            const long long j0 = (c0 + c) * kChunk;
-            float lf[kChunk], qf[kChunk];
-            if (!STORE) load_chunk<DT>(rowp, j0, V, al_l, lf);
-            if (use_res) load_q_chunk(qrow, j0, V, al_q, qf);
-            unsigned long long cs = 0;
-#pragma unroll
-            for (int e = 0; e < kChunk; ++e) {
-                ff ev = STORE ? ff{ehi[c * kChunk + e], elo[c * kChunk + e]}
-                              : exp_elem(lf[e], m, a.rT, thi, tlo, a.fc);
-                cs += quantize(weight(ev, inv, use_res ? qf[e] : 0.0f, use_res));
-            }
-            csum[c] = cs;
+        for (int ci = tid; ci < mych; ci += kThreads) {
+            const long long j0 = (c0 + ci) * kChunk;
+            unsigned long long cs = chunk_weight<DT, STORE>(rowp, qrow, j0, V, al_l, al_q,
+                                                            use_res, m, c, inv, ehi, elo, ci,
+                                                            nchs, sh, 0ull, nullptr);
+            csum[ci] = cs;
             tacc += cs;
         }
         tacc = warp_sum(tacc);
-        if (lane == 0) red_u[warp] = tacc;
+        if (lane == 0) sh.red_u[warp] = tacc;
         __syncthreads();
         if (warp == 0) {
-            unsigned long long w = lane < kWarps ? red_u[lane] : 0ull;
+            unsigned long long w = lane < kWarps ? sh.red_u[lane] : 0ull;
             w = warp_sum(w);
-            if (lane == 0) slot_W[round] = w;
+            if (lane == 0) sh.slot_W[round] = w;
         }
         cluster.sync();
-        prefix = 0;
-        total = 0;
-        for (int r = 0; r < G; ++r) {
-            unsigned long long t = cluster.map_shared_rank(slot_W, r)[round];
-            if (r < rank) prefix += t;
-            total += t;
+        if (warp == 0) {
+            unsigned long long t =
+                lane < G ? cluster.map_shared_rank(sh.slot_W, lane)[round] : 0ull;
+            unsigned long long incl = t;  // inclusive prefix over ranks
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                unsigned long long o = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += o;
+            }
+            unsigned long long tot = __shfl_sync(0xffffffffu, incl, 31);
+            unsigned long long pre = __shfl_sync(0xffffffffu, incl - t, rank);
+            if (lane == 0) {
+                sh.prefix = pre;
+                sh.total = tot;
+            }
         }
-        mytot = slot_W[round];
+        __syncthreads();
+        prefix = sh.prefix;
+        total = sh.total;
+        mytot = sh.slot_W[round];
         if (total > 0 || !use_res) break;
         use_res = false;  // zero residual mass: draw from p (counted)
         degenerate = true;
@@ -673,23 +503,33 @@ __global__ void __launch_bounds__(kDrawThreads) sv_draw_kernel(DrawArgs a) {
     const unsigned long long tau = scale_floor(u, total);
     const bool owner = mytot > 0 && prefix <= tau && tau - prefix < mytot;
     if (owner) {
-        // Exclusive scan of the per-chunk sums in index order: thread t owns the
+        // Exclusive scan of the chunk weights in index order: thread t owns the
         // contiguous chunk range [t*L, (t+1)*L).
         const unsigned long long want = tau - prefix;
-        const int L = (mych + kDrawThreads - 1) / kDrawThreads;
+        const int L = (mych + kThreads - 1) / kThreads;
         const int cb = tid * L, ce = min(mych, cb + L);
         unsigned long long mine = 0;
-        for (int c = cb; c < ce; ++c) mine += csum[c];
-        // inclusive block scan through shared memory (Hillis-Steele)
-        s_scan[tid] = mine;
-        __syncthreads();
-        for (int off = 1; off < kDrawThreads; off <<= 1) {
-            unsigned long long add = tid >= off ? s_scan[tid - off] : 0ull;
-            __syncthreads();
-            s_scan[tid] += add;
-            __syncthreads();
+        for (int ci = cb; ci < ce; ++ci) mine += csum[ci];
+        unsigned long long incl = mine;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            unsigned long long o = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += o;
         }
-        const unsigned long long excl = s_scan[tid] - mine;
+        if (lane == 31) sh.red_u[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            unsigned long long wv = lane < kWarps ? sh.red_u[lane] : 0ull;
+            unsigned long long wi = wv;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                unsigned long long o = __shfl_up_sync(0xffffffffu, wi, off);
+                if (lane >= off) wi += o;
+            }
+            if (lane < kWarps) sh.woff[lane] = wi - wv;  // exclusive warp offsets
+        }
+        __syncthreads();
+        const unsigned long long excl = sh.woff[warp] + incl - mine;
         if (mine > 0 && excl <= want && want - excl < mine) {
             unsigned long long run = excl;
             int cstar = cb;
@@ -697,86 +537,483 @@ __global__ void __launch_bounds__(kDrawThreads) sv_draw_kernel(DrawArgs a) {
                 if (want - run < csum[cstar]) break;
                 run += csum[cstar];
             }
-            if (cstar >= ce) cstar = ce - 1;  // unreachable: mine covers `want`
-            const long long j0 = (c0 + cstar) * kChunk;
-            float lf[kChunk], qf[kChunk];
-            if (!STORE) load_chunk<DT>(rowp, j0, V, al_l, lf);
-            if (use_res) load_q_chunk(qrow, j0, V, al_q, qf);
+            if (cstar >= ce) cstar = ce - 1;  // unreachable: `mine` covers `want`
             int tok = -1;
-#pragma unroll
-            for (int e = 0; e < kChunk; ++e) {
-                ff ev = STORE ? ff{ehi[cstar * kChunk + e], elo[cstar * kChunk + e]}
-                              : exp_elem(lf[e], m, a.rT, thi, tlo, a.fc);
-                unsigned long long w = quantize(weight(ev, inv, use_res ? qf[e] : 0.0f, use_res));
-                if (tok < 0 && w > 0 && want - run < w) tok = (int)(j0 + e);
-                if (tok < 0) run += w;
-            }
-            a.out[(long long)b * (k + 1) + n] = tok;
+            chunk_weight<DT, STORE>(rowp, qrow, (c0 + cstar) * kChunk, V, al_l, al_q, use_res, m,
+                                    c, inv, ehi, elo, cstar, nchs, sh, want - run, &tok);
+            *token_out = tok;
         }
     }
-    if (rank == 0) {
-        int32_t* o = a.out + (long long)b * (k + 1);
-        const int32_t* xs = a.x + (long long)b * k;
-        for (int i = tid; i <= k; i += kDrawThreads) {
-            if (i < n) o[i] = xs[i];
-            else if (i > n) o[i] = -1;
+}
+
+// ------------------------------------------------------------------ the fused kernel
+
+struct VerifyArgs {
+    const void* logits;
+    const float* q;
+    const int32_t* x;
+    const float* ua;
+    const float* ur;
+    Header* hdr;
+    RowRec* rows;
+    uint32_t* seqstat;
+    int32_t* out;
+    int32_t* nacc;
+    int B, k, V, G, W;
+    float c;     // log2(e)/T (float, for the row statistics)
+    ff c2;       // log2(e)/T in float-float (p(x) and the draw)
+};
+
+struct FusedShared {
+    Partial wpart[kWarps];
+    Partial part[2][kWarps];   // this CTA's per-row partials of a wave (read through DSMEM)
+    Partial rowstat[kWarps];   // merged statistics of the wave's rows
+    float lx[kMaxK], qx[kMaxK], ua[kMaxK];
+    int xs[kMaxK];
+    uint32_t gfl[kMaxK];
+    float px[kWarps];
+    int n, bits;
+};
+
+template <typename DT, bool SAMPLED, bool STORE>
+__global__ void __launch_bounds__(kThreads) sv_verify_kernel(VerifyArgs a) {
+    using E = Elt<DT>;
+    extern __shared__ __align__(16) unsigned char dyn[];
+    __shared__ FusedShared fs;
+    __shared__ DrawShared ds;
+
+    cg::cluster_group cluster = cg::this_cluster();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int G = a.G;
+    const int b = blockIdx.x / G;
+    const int rank = blockIdx.x % G;  // == cluster rank: clusters are (G,1,1) along x
+    const int k = a.k, V = a.V;
+    const DT* seq_logits = static_cast<const DT*>(a.logits) + (long long)b * (k + 1) * V;
+
+    if (blockIdx.x == 0 && tid == 0) {
+        a.hdr->magic = kMagic;
+        a.hdr->B = a.B;
+        a.hdr->k = k;
+        a.hdr->V = V;
+        a.hdr->mode = SAMPLED ? SV_MODE_SAMPLE : SV_MODE_GREEDY;
+    }
+    // Draft tokens, their logits and q values, and the uniforms of this sequence.
+    for (int i = tid; i < k; i += kThreads) {
+        const int xi = a.x[(long long)b * k + i];
+        fs.xs[i] = xi;
+        uint32_t fl = 0;
+        float lx = NAN, qx = NAN;
+        if (xi < 0 || xi >= V) {
+            fl = kRowTokenBad;
+        } else {
+            lx = E::load1(seq_logits + (long long)i * V + xi);
+            if (SAMPLED) {
+                qx = a.q[((long long)b * k + i) * V + xi];
+                if (!(qx >= 0.0f)) fl = kRowQBad;
+            }
         }
+        fs.lx[i] = lx;
+        fs.qx[i] = qx;
+        fs.gfl[i] = fl;
+        fs.ua[i] = SAMPLED ? a.ua[(long long)b * k + i] : 0.0f;
+    }
+    if (SAMPLED) load_exp_table(ds);
+    if (tid == 0) {
+        fs.n = -1;
+        fs.bits = 0;
+    }
+    __syncthreads();
+
+    // ---- row statistics and the accept scan, wave by wave
+    const float c = a.c;
+    int buf = 0;
+    int last_wave_end = 0, wave_row0 = 0;
+    for (int i0 = 0; i0 <= k; i0 += a.W) {
+        const int Wc = min(a.W, k + 1 - i0);
+        // warps [g0, g1) stream row i0 + w, w = warp * Wc / kWarps
+        const int w = warp * Wc / kWarps;
+        const int g0 = (w * kWarps + Wc - 1) / Wc, g1 = ((w + 1) * kWarps + Wc - 1) / Wc;
+        const int tg = tid - g0 * 32, ng = (g1 - g0) * 32;
+        const DT* rowp = seq_logits + (long long)(i0 + w) * V;
+        int head;
+        long long nvec, tail0;
+        row_layout<DT>(rowp, V, head, nvec, tail0);
+        const long long vb = nvec * rank / G, ve = nvec * (rank + 1) / G;
+        Partial p = stream_slice<DT, SAMPLED, 4>(rowp, V, vb, ve, head, tail0, rank == 0,
+                                                 rank == G - 1, tg, ng, c);
+        p = warp_merge<SAMPLED>(p, c);
+        if (lane == 0) fs.wpart[warp] = p;
+        __syncthreads();
+        if (tid < Wc) {  // CTA partial of row i0 + tid from its warp group
+            const int h0 = (tid * kWarps + Wc - 1) / Wc, h1 = ((tid + 1) * kWarps + Wc - 1) / Wc;
+            Partial r = fs.wpart[h0];
+            for (int h = h0 + 1; h < h1; ++h) merge<SAMPLED>(r, fs.wpart[h], c);
+            fs.part[buf][tid] = r;
+        }
+        if (G > 1) {
+            cluster.sync();
+            if (warp < Wc) {  // merge over ranks: lane r holds rank r's partial
+                Partial r = lane < G ? *cluster.map_shared_rank(&fs.part[buf][warp], lane)
+                                     : empty_partial();
+                r = warp_merge<SAMPLED>(r, c);
+                if (lane == 0) fs.rowstat[warp] = r;
+            }
+        } else {
+            __syncthreads();
+            if (tid < Wc) fs.rowstat[tid] = fs.part[buf][tid];
+        }
+        __syncthreads();
+        if (tid == 0) {  // the scan over this wave's rows
+            int n = -1, bits = 0;
+            for (int ww = 0; ww < Wc; ++ww) {
+                const int i = i0 + ww;
+                const Partial& r = fs.rowstat[ww];
+                if (row_flags<SAMPLED>(r) & kRowBad) { bits = SV_DEV_BAD_ROW; break; }
+                if (i == k) { n = k; break; }
+                if (fs.gfl[i] & kRowTokenBad) { bits = SV_DEV_BAD_TOKEN; break; }
+                bool accept;
+                if (SAMPLED) {
+                    const float u = fs.ua[i];
+                    if (!(u >= 0.0f && u < 1.0f)) { bits = SV_DEV_BAD_UNIFORM; break; }
+                    if (fs.gfl[i] & kRowQBad) { bits = SV_DEV_BAD_Q; break; }
+                    ff ex = exp_rel(fs.lx[i], r.m, a.c2, ds.thi, ds.tlo);
+                    const float P = __fdiv_rn(ex.hi, r.s);
+                    const float Q = fs.qx[i];
+                    fs.px[ww] = P;
+                    accept = (P >= Q) || (u < __fdiv_rn(P, Q));
+                } else {
+                    accept = fs.xs[i] == r.idx;
+                }
+                if (!accept) { n = i; break; }
+            }
+            fs.n = n;
+            fs.bits = bits;
+        }
+        __syncthreads();
+        if (rank == 0 && tid < Wc) {  // row records for the statistics read-back
+            const int i = i0 + tid;
+            const Partial& r = fs.rowstat[tid];
+            RowRec rec;
+            rec.mraw = r.m;
+            rec.S = SAMPLED ? r.s : 0.0f;
+            rec.argmax = r.idx < 0 ? 0 : r.idx;
+            uint32_t fl = row_flags<SAMPLED>(r);
+            if (i < k) {
+                fl |= fs.gfl[i];
+                rec.lx = fs.lx[i];
+                rec.qx = fs.qx[i];
+                // p(x) was formed by the scan only up to the decision row
+                rec.px = (SAMPLED && (fs.n < 0 || i <= fs.n)) ? (double)fs.px[tid] : 0.0;
+            } else {
+                rec.lx = NAN;
+                rec.qx = NAN;
+                rec.px = NAN;
+            }
+            rec.flags = fl;
+            a.rows[(long long)b * (k + 1) + i] = rec;
+        }
+        wave_row0 = i0;
+        last_wave_end = i0 + Wc;
+        buf ^= 1;
+        if (fs.n >= 0 || fs.bits) break;
+    }
+    // Rows past the last wave were never read.
+    if (rank == 0)
+        for (int i = last_wave_end + tid; i <= k; i += kThreads) {
+            RowRec rec;
+            rec.mraw = NAN;
+            rec.S = NAN;
+            rec.px = NAN;
+            rec.lx = NAN;
+            rec.qx = NAN;
+            rec.argmax = -1;
+            rec.flags = kRowSkipped;
+            a.rows[(long long)b * (k + 1) + i] = rec;
+        }
+
+    const int n = fs.n;
+    const int bits = fs.bits;
+    int32_t* o = a.out + (long long)b * (k + 1);
+    if (bits || !SAMPLED) {
+        if (rank == 0) {
+            for (int i = tid; i <= k; i += kThreads)
+                o[i] = bits ? -1 : (i < n ? fs.xs[i] : (i == n ? fs.rowstat[n - wave_row0].idx : -1));
+            if (tid == 0) {
+                a.nacc[b] = bits ? -1 : n;
+                a.seqstat[b] = (uint32_t)bits;
+            }
+        }
+        if (G > 1) cluster.sync();  // partial slots may still be read by other ranks
+        return;
+    }
+
+    // ---- the draw on row n, then the outputs
+    const float u = a.ur[b];
+    if (!(u >= 0.0f && u < 1.0f)) {  // every CTA sees the same uniform
+        if (rank == 0) {
+            for (int i = tid; i <= k; i += kThreads) o[i] = -1;
+            if (tid == 0) {
+                a.nacc[b] = -1;
+                a.seqstat[b] = SV_DEV_BAD_UNIFORM;
+            }
+        }
+        if (G > 1) cluster.sync();
+        return;
+    }
+    const DT* drow = seq_logits + (long long)n * V;
+    const float* qrow = n < k ? a.q + ((long long)b * k + n) * V : nullptr;
+    const float m = fs.rowstat[n - wave_row0].m;
+    bool degenerate = false;
+    draw_phase<DT, STORE>(cluster, ds, dyn, drow, qrow, n < k, V, m, a.c2, u, rank, G, o + n,
+                          degenerate);
+    if (rank == 0) {
+        for (int i = tid; i <= k; i += kThreads)
+            if (i != n) o[i] = i < n ? fs.xs[i] : -1;
         if (tid == 0) {
             a.nacc[b] = n;
-            if (degenerate) {
-                atomicOr(&a.hdr->status, SV_DEV_DEGENERATE);
-                atomicAdd(&a.hdr->n_degenerate, 1u);
-            }
+            a.seqstat[b] = degenerate ? SV_DEV_DEGENERATE : 0u;
         }
     }
     cluster.sync();  // no CTA leaves while another may still read its slots
 }
 
+// ------------------------------------------------------------------ two-stage kernels
+
+struct RowsArgs {
+    const void* logits;
+    const float* q;
+    const int32_t* x;
+    Header* hdr;
+    RowRec* rows;
+    int B, k, V, G, mode;
+    float c;        // log2(e) / T
+    ff c2;          // log2(e) / T in float-float (p(x))
+};
+
+// One CTA (or a cluster of G CTAs splitting the vocabulary) per row.
+template <typename DT, bool SAMPLED, int NT>
+__global__ void __launch_bounds__(NT) sv_rows_kernel(RowsArgs a) {
+    using E = Elt<DT>;
+    constexpr int NW = NT / 32;
+    __shared__ Partial wpart[NW];
+    __shared__ Partial cta_part;  // read by cluster rank 0 through DSMEM
+    __shared__ float thi[SAMPLED ? kExpTable : 1], tlo[SAMPLED ? kExpTable : 1];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int G = a.G;
+    const long long row = blockIdx.x / G;
+    const int rank = blockIdx.x % G;
+    const int V = a.V;
+    const DT* rowp = static_cast<const DT*>(a.logits) + row * (long long)V;
+    const int b = (int)(row / (a.k + 1));
+    const int i = (int)(row % (a.k + 1));
+    if (blockIdx.x == 0 && tid == 0) {
+        a.hdr->magic = kMagic;
+        a.hdr->B = a.B;
+        a.hdr->k = a.k;
+        a.hdr->V = V;
+        a.hdr->mode = a.mode;
+    }
+    int head;
+    long long nvec, tail0;
+    row_layout<DT>(rowp, V, head, nvec, tail0);
+    const long long vb = nvec * rank / G, ve = nvec * (rank + 1) / G;
+    Partial p = stream_slice<DT, SAMPLED, 4>(rowp, V, vb, ve, head, tail0, rank == 0,
+                                             rank == G - 1, tid, NT, a.c);
+    p = warp_merge<SAMPLED>(p, a.c);
+    if (lane == 0) wpart[warp] = p;
+    __syncthreads();
+    if (warp == 0) {
+        Partial w = lane < NW ? wpart[lane] : empty_partial();
+        w = warp_merge<SAMPLED>(w, a.c);
+        p = w;
+        if (lane == 0) cta_part = w;
+    }
+    if (G > 1) {
+        cg::cluster_group cluster = cg::this_cluster();
+        cluster.sync();
+        if (rank == 0 && warp == 0) {
+            Partial w = lane < G ? *cluster.map_shared_rank(&cta_part, lane) : empty_partial();
+            p = warp_merge<SAMPLED>(w, a.c);
+        }
+        cluster.sync();
+    }
+    if (rank != 0) return;
+    if (SAMPLED && i < a.k) {
+        for (int t = tid; t < kExpTable; t += NT) {
+            thi[t] = g_exp2_table.hi[t];
+            tlo[t] = g_exp2_table.lo[t];
+        }
+        __syncthreads();
+    }
+    if (tid != 0) return;
+    RowRec rec;
+    rec.mraw = p.m;
+    rec.S = SAMPLED ? p.s : 0.0f;
+    rec.argmax = p.idx < 0 ? 0 : p.idx;
+    rec.px = 0.0;
+    rec.lx = NAN;
+    rec.qx = NAN;
+    uint32_t fl = row_flags<SAMPLED>(p);
+    if (i < a.k) {
+        const int xi = a.x[(long long)b * a.k + i];
+        if (xi < 0 || xi >= V) {
+            fl |= kRowTokenBad;
+        } else {
+            rec.lx = E::load1(rowp + xi);
+            if (SAMPLED) {
+                rec.qx = a.q[((long long)b * a.k + i) * V + xi];
+                if (!(rec.qx >= 0.0f)) fl |= kRowQBad;
+                if (!(fl & kRowBad)) {
+                    ff ex = exp_rel(rec.lx, p.m, a.c2, thi, tlo);
+                    rec.px = (double)__fdiv_rn(ex.hi, p.s);
+                }
+            }
+        }
+    } else {
+        rec.px = NAN;
+    }
+    rec.flags = fl;
+    a.rows[row] = rec;
+}
+
+// One warp per sequence: the lanes load the records in parallel, lane 0 scans.
+__global__ void sv_finish_greedy_kernel(const int32_t* __restrict__ x,
+                                        const RowRec* __restrict__ rows,
+                                        uint32_t* __restrict__ seqstat, int B, int k,
+                                        int32_t* __restrict__ out, int32_t* __restrict__ nacc) {
+    __shared__ RowRec recs[4][kMaxK + 1];
+    __shared__ int xs[4][kMaxK];
+    const int wi = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = blockIdx.x * 4 + wi;
+    if (b >= B) return;
+    RowRec* rr = recs[wi];
+    int* xx = xs[wi];
+    for (int i = lane; i <= k; i += 32) rr[i] = rows[(long long)b * (k + 1) + i];
+    for (int i = lane; i < k; i += 32) xx[i] = x[(long long)b * k + i];
+    __syncwarp();
+    if (lane != 0) return;
+    int32_t* o = out + (long long)b * (k + 1);
+    uint32_t bits = 0;
+    int n = k;
+    for (int i = 0; i < k; ++i) {
+        if (rr[i].flags & kRowBad) { bits = SV_DEV_BAD_ROW; break; }
+        if (rr[i].flags & kRowTokenBad) { bits = SV_DEV_BAD_TOKEN; break; }
+        if (xx[i] != rr[i].argmax) { n = i; break; }
+    }
+    if (!bits && (rr[n].flags & kRowBad)) bits = SV_DEV_BAD_ROW;
+    seqstat[b] = bits;
+    if (bits) {
+        for (int i = 0; i <= k; ++i) o[i] = -1;
+        nacc[b] = -1;
+        return;
+    }
+    for (int i = 0; i < n; ++i) o[i] = xx[i];
+    o[n] = rr[n].argmax;
+    for (int i = n + 1; i <= k; ++i) o[i] = -1;
+    nacc[b] = n;
+}
+
+struct FinishArgs {
+    const void* logits;
+    const float* q;
+    const int32_t* x;
+    const float* ua;
+    const float* ur;
+    const RowRec* rows;
+    uint32_t* seqstat;
+    int32_t* out;
+    int32_t* nacc;
+    int B, k, V, G;
+    ff c2;
+};
+
+template <typename DT, bool STORE>
+__global__ void __launch_bounds__(kThreads) sv_finish_sample_kernel(FinishArgs a) {
+    extern __shared__ __align__(16) unsigned char dyn[];
+    __shared__ DrawShared ds;
+    __shared__ RowRec recs[kMaxK + 1];
+    __shared__ float uas[kMaxK];
+    __shared__ int s_n, s_bits;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int tid = threadIdx.x;
+    const int G = a.G;
+    const int b = blockIdx.x / G;
+    const int rank = blockIdx.x % G;
+    const int k = a.k, V = a.V;
+    load_exp_table(ds);
+    for (int i = tid; i <= k; i += kThreads) recs[i] = a.rows[(long long)b * (k + 1) + i];
+    for (int i = tid; i < k; i += kThreads) uas[i] = a.ua[(long long)b * k + i];
+    __syncthreads();
+    if (tid == 0) {
+        int bits = 0, n = k;
+        for (int i = 0; i < k; ++i) {
+            const RowRec& r = recs[i];
+            if (r.flags & kRowBad) { bits = SV_DEV_BAD_ROW; break; }
+            if (r.flags & kRowTokenBad) { bits = SV_DEV_BAD_TOKEN; break; }
+            const float u = uas[i];
+            if (!(u >= 0.0f && u < 1.0f)) { bits = SV_DEV_BAD_UNIFORM; break; }
+            if (r.flags & kRowQBad) { bits = SV_DEV_BAD_Q; break; }
+            const float P = (float)r.px, Q = r.qx;
+            if (!((P >= Q) || (u < __fdiv_rn(P, Q)))) { n = i; break; }
+        }
+        if (!bits && (recs[n].flags & kRowBad)) bits = SV_DEV_BAD_ROW;
+        if (!bits) {
+            const float u = a.ur[b];
+            if (!(u >= 0.0f && u < 1.0f)) bits = SV_DEV_BAD_UNIFORM;
+        }
+        s_n = n;
+        s_bits = bits;
+    }
+    __syncthreads();
+    const int n = s_n;
+    int32_t* o = a.out + (long long)b * (k + 1);
+    if (s_bits) {
+        if (rank == 0) {
+            for (int i = tid; i <= k; i += kThreads) o[i] = -1;
+            if (tid == 0) {
+                a.nacc[b] = -1;
+                a.seqstat[b] = (uint32_t)s_bits;
+            }
+        }
+        return;  // every CTA of the cluster takes this branch together
+    }
+    const DT* drow = static_cast<const DT*>(a.logits) + ((long long)b * (k + 1) + n) * V;
+    const float* qrow = n < k ? a.q + ((long long)b * k + n) * V : nullptr;
+    bool degenerate = false;
+    draw_phase<DT, STORE>(cluster, ds, dyn, drow, qrow, n < k, V, recs[n].mraw, a.c2, a.ur[b],
+                          rank, G, o + n, degenerate);
+    if (rank == 0) {
+        for (int i = tid; i <= k; i += kThreads)
+            if (i != n) o[i] = i < n ? a.x[(long long)b * k + i] : -1;
+        if (tid == 0) {
+            a.nacc[b] = n;
+            a.seqstat[b] = degenerate ? SV_DEV_DEGENERATE : 0u;
+        }
+    }
+    cluster.sync();
+}
+
 // ------------------------------------------------------------------ debug kernel
 
-__global__ void sv_debug_ffexp_kernel(const float* l, float m, int n, ff rT, FFExpConst fc,
-                                      double* out) {
-    __shared__ float thi[64], tlo[64];
-    if (threadIdx.x < 64) {
-        thi[threadIdx.x] = fc.tbl_hi[threadIdx.x];
-        tlo[threadIdx.x] = fc.tbl_lo[threadIdx.x];
+__global__ void sv_debug_ffexp_kernel(const float* l, float m, int n, ff c2, double* out) {
+    __shared__ float thi[kExpTable], tlo[kExpTable];
+    for (int t = threadIdx.x; t < kExpTable; t += blockDim.x) {
+        thi[t] = g_exp2_table.hi[t];
+        tlo[t] = g_exp2_table.lo[t];
     }
     __syncthreads();
     int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n) return;
-    ff e = exp_elem(l[i], m, rT, thi, tlo, fc);
+    ff e = exp_rel(l[i], m, c2, thi, tlo);
     out[i] = (double)e.hi + (double)e.lo;
 }
 
 // ------------------------------------------------------------------ host side
 
-static FFExpConst make_exp_const() {
-    FFExpConst c;
-    for (int i = 0; i < 64; ++i) {
-        double v = std::exp2((double)i / 64.0);
-        c.tbl_hi[i] = (float)v;
-        c.tbl_lo[i] = (float)(v - (double)c.tbl_hi[i]);
-    }
-    const double L = std::log(2.0) / 64.0;
-    int e;
-    double f = std::frexp(L, &e);                      // L = f * 2^e, f in [0.5, 1)
-    double c1 = std::ldexp(std::nearbyint(std::ldexp(f, 12)), e - 12);  // 12 significant bits
-    c.c1 = (float)c1;
-    c.c2 = (float)(L - c1);
-    c.c3 = (float)(L - c1 - (double)c.c2);
-    c.inv_l = (float)(64.0 / std::log(2.0));
-    return c;
-}
-
-static const FFExpConst& exp_const() {
-    static const FFExpConst c = make_exp_const();
-    return c;
-}
-
-static ff make_rT(float T) {
-    double r = 1.0 / (double)T;
-    float hi = (float)r;
-    return ff{hi, (float)(r - (double)hi)};
+static ff log2e_over(float T) {
+    const double v = 1.4426950408889634074 / (double)T;
+    const float hi = (float)v;
+    return ff{hi, (float)(v - (double)hi)};
 }
 
 struct DeviceInfo {
@@ -787,16 +1024,15 @@ struct DeviceInfo {
 static std::mutex g_mu;
 static DeviceInfo g_dev[64];
 
-template <typename DT, bool SAMPLED, int NT> static cudaError_t set_rows_attr() {
-    return cudaFuncSetAttribute(sv_rows_kernel<DT, SAMPLED, NT>,
-                                cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-}
-template <typename DT, bool STORE> static cudaError_t set_draw_attr() {
-    cudaError_t e = cudaFuncSetAttribute(sv_draw_kernel<DT, STORE>,
-                                         cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(sv_draw_kernel<DT, STORE>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+constexpr size_t kDynSmemMax = 160 * 1024;
+
+template <typename K> static cudaError_t cluster_attrs(K kernel, bool dyn) {
+    cudaError_t e =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e == cudaSuccess && dyn)
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kDynSmemMax);
+    return e;
 }
 
 static sv_status device_setup(int* sms) {
@@ -815,22 +1051,28 @@ static sv_status device_setup(int* sms) {
         if (d.ok) {
             cudaError_t e = cudaSuccess;
 #define SV_TRY(x) if (e == cudaSuccess) e = (x)
-            SV_TRY((set_rows_attr<__nv_bfloat16, true, 128>()));
-            SV_TRY((set_rows_attr<__nv_bfloat16, true, 256>()));
-            SV_TRY((set_rows_attr<__nv_bfloat16, true, 512>()));
-            SV_TRY((set_rows_attr<__nv_bfloat16, false, 128>()));
-            SV_TRY((set_rows_attr<__nv_bfloat16, false, 256>()));
-            SV_TRY((set_rows_attr<__nv_bfloat16, false, 512>()));
-            SV_TRY((set_rows_attr<float, true, 128>()));
-            SV_TRY((set_rows_attr<float, true, 256>()));
-            SV_TRY((set_rows_attr<float, true, 512>()));
-            SV_TRY((set_rows_attr<float, false, 128>()));
-            SV_TRY((set_rows_attr<float, false, 256>()));
-            SV_TRY((set_rows_attr<float, false, 512>()));
-            SV_TRY((set_draw_attr<__nv_bfloat16, true>()));
-            SV_TRY((set_draw_attr<__nv_bfloat16, false>()));
-            SV_TRY((set_draw_attr<float, true>()));
-            SV_TRY((set_draw_attr<float, false>()));
+            SV_TRY(cluster_attrs(sv_verify_kernel<__nv_bfloat16, true, true>, true));
+            SV_TRY(cluster_attrs(sv_verify_kernel<__nv_bfloat16, true, false>, true));
+            SV_TRY(cluster_attrs(sv_verify_kernel<float, true, true>, true));
+            SV_TRY(cluster_attrs(sv_verify_kernel<float, true, false>, true));
+            SV_TRY(cluster_attrs(sv_verify_kernel<__nv_bfloat16, false, false>, false));
+            SV_TRY(cluster_attrs(sv_verify_kernel<float, false, false>, false));
+            SV_TRY(cluster_attrs(sv_finish_sample_kernel<__nv_bfloat16, true>, true));
+            SV_TRY(cluster_attrs(sv_finish_sample_kernel<__nv_bfloat16, false>, true));
+            SV_TRY(cluster_attrs(sv_finish_sample_kernel<float, true>, true));
+            SV_TRY(cluster_attrs(sv_finish_sample_kernel<float, false>, true));
+            SV_TRY(cluster_attrs(sv_rows_kernel<__nv_bfloat16, true, 128>, false));
+            SV_TRY(cluster_attrs(sv_rows_kernel<__nv_bfloat16, true, 256>, false));
+            SV_TRY(cluster_attrs(sv_rows_kernel<__nv_bfloat16, true, 512>, false));
+            SV_TRY(cluster_attrs(sv_rows_kernel<__nv_bfloat16, false, 128>, false));
+            SV_TRY(cluster_attrs(sv_rows_kernel<__nv_bfloat16, false, 256>, false));
+            SV_TRY(cluster_attrs(sv_rows_kernel<__nv_bfloat16, false, 512>, false));
+            SV_TRY(cluster_attrs(sv_rows_kernel<float, true, 128>, false));
+            SV_TRY(cluster_attrs(sv_rows_kernel<float, true, 256>, false));
+            SV_TRY(cluster_attrs(sv_rows_kernel<float, true, 512>, false));
+            SV_TRY(cluster_attrs(sv_rows_kernel<float, false, 128>, false));
+            SV_TRY(cluster_attrs(sv_rows_kernel<float, false, 256>, false));
+            SV_TRY(cluster_attrs(sv_rows_kernel<float, false, 512>, false));
 #undef SV_TRY
             if (e != cudaSuccess) return SV_ERR_CUDA;
         }
@@ -854,12 +1096,112 @@ static sv_status check_common(const void* logits, sv_dtype dt, const int32_t* x,
     if (B > 0 && (!aligned16(logits) || !aligned16(x))) return SV_ERR_INVALID_ARG;
     if (!ws) return SV_ERR_WORKSPACE;
     if (!aligned16(ws)) return SV_ERR_INVALID_ARG;
-    if (ws_bytes < ws_bytes_for((long long)B * (k + 1))) return SV_ERR_WORKSPACE;
+    if (ws_bytes < ws_bytes_for(B, k)) return SV_ERR_WORKSPACE;
     return SV_OK;
 }
 
-// Vocabulary split of the row stream: enough CTAs to give every SM about four,
-// while keeping each CTA's slice at 512 16-byte vectors (8 KiB) or more.
+static sv_status check_outputs(const int32_t* out, const int32_t* nacc, int B) {
+    if (B > 0 && (!out || !nacc)) return SV_ERR_INVALID_ARG;
+    if (B > 0 && (!aligned16(out) || !aligned16(nacc))) return SV_ERR_INVALID_ARG;
+    return SV_OK;
+}
+
+static sv_status check_sample(const float* q, const float* ua, const float* ur, float T, int B) {
+    if (!(T > 0.0f) || !std::isfinite(T)) return SV_ERR_INVALID_ARG;
+    if (B > 0 && (!q || !ua || !ur)) return SV_ERR_INVALID_ARG;
+    if (B > 0 && (!aligned16(q) || !aligned16(ua) || !aligned16(ur))) return SV_ERR_INVALID_ARG;
+    return SV_OK;
+}
+
+static cudaLaunchAttribute cluster_attr(int G) {
+    cudaLaunchAttribute at;
+    at.id = cudaLaunchAttributeClusterDimension;
+    at.val.clusterDim.x = G;
+    at.val.clusterDim.y = 1;
+    at.val.clusterDim.z = 1;
+    return at;
+}
+
+// Cluster size of the per-sequence kernels.  Sampled: the smallest split whose
+// slice keeps its exponentials in shared memory (V <= 16 * 10240), widened while
+// the batch leaves SMs idle.  Greedy: enough CTAs to give each SM four, with at
+// least 4 KiB of every row per CTA.
+static int seq_split(bool sampled, int B, int V, int esz, int sms) {
+    int G = 1;
+    if (sampled) {
+        while (G < 16 && (V + G - 1) / G > kSegStore) G *= 2;
+        while (G < 16 && (long long)B * G < 2LL * sms && V / (2 * G) >= 2048) G *= 2;
+    } else {
+        while (G < 16 && (long long)B * G < 4LL * sms && (long long)V * esz / (2LL * G) >= 4096)
+            G *= 2;
+    }
+    return G;
+}
+
+// Rows per wave of the fused kernel: all k+1 rows at once while the batch
+// cannot keep every SM busy (nothing else would use the bandwidth), else one
+// row at a time so that rows after the first rejection are never read.
+static int wave_rows(int B, int k, int G, int sms) {
+    const long long ctas = (long long)B * G;
+    const int W = ctas >= 2LL * sms ? 1 : k + 1;
+    return W > kWarps ? kWarps : W;
+}
+
+static sv_status launch_fused(bool sampled, const void* logits, sv_dtype dt, const float* q,
+                              const int32_t* x, const float* ua, const float* ur, float T, int B,
+                              int k, int V, int32_t* out, int32_t* nacc, void* ws,
+                              cudaStream_t stream, int sms) {
+    VerifyArgs a;
+    a.logits = logits;
+    a.q = q;
+    a.x = x;
+    a.ua = ua;
+    a.ur = ur;
+    a.hdr = static_cast<Header*>(ws);
+    a.rows = reinterpret_cast<RowRec*>(static_cast<char*>(ws) + ws_rows_offset());
+    a.seqstat = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + ws_seq_offset(B, k));
+    a.out = out;
+    a.nacc = nacc;
+    a.B = B;
+    a.k = k;
+    a.V = V;
+    const int esz = dt == SV_BF16 ? 2 : 4;
+    a.G = seq_split(sampled, B, V, esz, sms);
+    a.W = wave_rows(B, k, a.G, sms);
+    a.c2 = log2e_over(sampled ? T : 1.0f);
+    a.c = a.c2.hi;
+    size_t smem = 0;
+    bool store = false;
+    if (sampled) {
+        const long long nch = (V + kChunk - 1) / kChunk;
+        const long long mych_max = (nch + a.G - 1) / a.G;
+        store = mych_max * kChunk <= kSegStore;
+        smem = (store ? 2 * kSegStore * sizeof(float) : 0) + (size_t)mych_max * 8;
+        if (smem > kDynSmemMax) return SV_ERR_UNSUPPORTED;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((long long)B * a.G), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1] = {cluster_attr(a.G)};
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e;
+    if (dt == SV_BF16) {
+        if (!sampled) e = cudaLaunchKernelEx(&cfg, sv_verify_kernel<__nv_bfloat16, false, false>, a);
+        else if (store) e = cudaLaunchKernelEx(&cfg, sv_verify_kernel<__nv_bfloat16, true, true>, a);
+        else e = cudaLaunchKernelEx(&cfg, sv_verify_kernel<__nv_bfloat16, true, false>, a);
+    } else {
+        if (!sampled) e = cudaLaunchKernelEx(&cfg, sv_verify_kernel<float, false, false>, a);
+        else if (store) e = cudaLaunchKernelEx(&cfg, sv_verify_kernel<float, true, true>, a);
+        else e = cudaLaunchKernelEx(&cfg, sv_verify_kernel<float, true, false>, a);
+    }
+    return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+// Vocabulary split of the per-row kernel: enough CTAs to give every SM about
+// four, while keeping each CTA's slice at 512 16-byte vectors (8 KiB) or more.
 static int rows_split(long long R, long long nvec_row, int sms) {
     int G = 1;
     while (G < 16 && R * G < 4LL * sms && nvec_row / (2LL * G) >= 512) G *= 2;
@@ -883,28 +1225,22 @@ static sv_status launch_rows(bool sampled, const void* logits, sv_dtype dt, cons
     a.q = q;
     a.x = x;
     a.hdr = static_cast<Header*>(ws);
-    a.rows = reinterpret_cast<RowRec*>(static_cast<char*>(ws) + sizeof(Header));
+    a.rows = reinterpret_cast<RowRec*>(static_cast<char*>(ws) + ws_rows_offset());
     a.B = B;
     a.k = k;
     a.V = V;
     a.mode = sampled ? SV_MODE_SAMPLE : SV_MODE_GREEDY;
-    a.T = sampled ? (double)T : 1.0;
-    a.c = sampled ? (float)(1.4426950408889634 / (double)T) : 1.0f;
+    a.c2 = log2e_over(sampled ? T : 1.0f);
+    a.c = a.c2.hi;
     const int esz = dt == SV_BF16 ? 2 : 4;
     const long long nvec_row = ((long long)V * esz + 15) / 16;
     a.G = rows_split(R, nvec_row, sms);
     const int nt = rows_threads(R * a.G, nvec_row / a.G, sms);
-
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(R * a.G), 1, 1);
     cfg.blockDim = dim3(nt, 1, 1);
-    cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = a.G;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[1] = {cluster_attr(a.G)};
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cudaError_t e;
@@ -923,76 +1259,54 @@ static sv_status launch_rows(bool sampled, const void* logits, sv_dtype dt, cons
     return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
-// Cluster size of the draw: each CTA's slice of the decision row fits in shared
-// memory when possible (V <= 16 * 16384), and small batches spread wider.
-static int draw_split(int B, int V, int sms) {
-    int G = 1;
-    while (G < 16 && (V + G - 1) / G > kSegMax) G *= 2;
-    while (G < 16 && (long long)B * G < 2LL * sms && V / (2 * G) >= 2048) G *= 2;
-    return G;
-}
-
 static sv_status launch_finish(bool sampled, const void* logits, sv_dtype dt, const float* q,
                                const int32_t* x, const float* ua, const float* ur, float T,
                                int B, int k, int V, int32_t* out, int32_t* nacc, void* ws,
                                cudaStream_t stream, int sms) {
-    Header* hdr = static_cast<Header*>(ws);
-    const RowRec* rows = reinterpret_cast<const RowRec*>(static_cast<char*>(ws) + sizeof(Header));
+    const RowRec* rows =
+        reinterpret_cast<const RowRec*>(static_cast<char*>(ws) + ws_rows_offset());
+    uint32_t* seqstat = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + ws_seq_offset(B, k));
     cudaError_t e;
     if (!sampled) {
-        const int nt = 128;
-        sv_scan_greedy_kernel<<<(B + nt - 1) / nt, nt, 0, stream>>>(x, rows, hdr, B, k, out, nacc);
+        sv_finish_greedy_kernel<<<(B + 3) / 4, 128, 0, stream>>>(x, rows, seqstat, B, k, out, nacc);
         e = cudaGetLastError();
         return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
     }
-    DrawArgs a;
+    FinishArgs a;
     a.logits = logits;
     a.q = q;
     a.x = x;
     a.ua = ua;
     a.ur = ur;
-    a.hdr = hdr;
     a.rows = rows;
+    a.seqstat = seqstat;
     a.out = out;
     a.nacc = nacc;
     a.B = B;
     a.k = k;
     a.V = V;
-    a.G = draw_split(B, V, sms);
-    a.rT = make_rT(T);
-    a.fc = exp_const();
-    const long long seg = ((long long)(V + kChunk - 1) / kChunk + a.G - 1) / a.G * kChunk;
-    const bool store = seg <= kSegMax;
-    const size_t nchunk_max = (size_t)(seg / kChunk + 1);
-    const size_t smem = (store ? 2 * kSegMax * sizeof(float) : 0) + nchunk_max * 8;
-    if (smem > 200 * 1024) return SV_ERR_UNSUPPORTED;
-
+    a.G = seq_split(true, B, V, dt == SV_BF16 ? 2 : 4, sms);
+    a.c2 = log2e_over(T);
+    const long long nch = (V + kChunk - 1) / kChunk;
+    const long long mych_max = (nch + a.G - 1) / a.G;
+    const bool store = mych_max * kChunk <= kSegStore;
+    const size_t smem = (store ? 2 * kSegStore * sizeof(float) : 0) + (size_t)mych_max * 8;
+    if (smem > kDynSmemMax) return SV_ERR_UNSUPPORTED;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((long long)B * a.G), 1, 1);
-    cfg.blockDim = dim3(kDrawThreads, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = a.G;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[1] = {cluster_attr(a.G)};
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (dt == SV_BF16)
-        e = store ? cudaLaunchKernelEx(&cfg, sv_draw_kernel<__nv_bfloat16, true>, a)
-                  : cudaLaunchKernelEx(&cfg, sv_draw_kernel<__nv_bfloat16, false>, a);
+        e = store ? cudaLaunchKernelEx(&cfg, sv_finish_sample_kernel<__nv_bfloat16, true>, a)
+                  : cudaLaunchKernelEx(&cfg, sv_finish_sample_kernel<__nv_bfloat16, false>, a);
     else
-        e = store ? cudaLaunchKernelEx(&cfg, sv_draw_kernel<float, true>, a)
-                  : cudaLaunchKernelEx(&cfg, sv_draw_kernel<float, false>, a);
+        e = store ? cudaLaunchKernelEx(&cfg, sv_finish_sample_kernel<float, true>, a)
+                  : cudaLaunchKernelEx(&cfg, sv_finish_sample_kernel<float, false>, a);
     return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
-}
-
-static sv_status check_sample(const float* q, const float* ua, const float* ur, float T, int B) {
-    if (!(T > 0.0f) || !std::isfinite(T)) return SV_ERR_INVALID_ARG;
-    if (B > 0 && (!q || !ua || !ur)) return SV_ERR_INVALID_ARG;
-    if (B > 0 && (!aligned16(q) || !aligned16(ua) || !aligned16(ur))) return SV_ERR_INVALID_ARG;
-    return SV_OK;
 }
 
 }  // namespace sv
@@ -1004,7 +1318,7 @@ extern "C" {
 size_t spec_verify_workspace_size(int B, int k, int V, sv_dtype dtype) {
     if (B < 0 || k < 1 || V < 1 || k > kMaxK || V > kMaxV) return 0;
     if (dtype != SV_BF16 && dtype != SV_F32) return 0;
-    return ws_bytes_for((long long)B * (k + 1));
+    return ws_bytes_for(B, k);
 }
 
 sv_status spec_verify_rows(sv_mode mode, const void* logits, sv_dtype dtype,
@@ -1033,8 +1347,7 @@ sv_status spec_verify_finish(sv_mode mode, const void* logits, sv_dtype dtype,
     if (mode != SV_MODE_SAMPLE && mode != SV_MODE_GREEDY) return SV_ERR_INVALID_ARG;
     sv_status st = check_common(logits, dtype, draft_tokens, B, k, V, ws, ws_bytes);
     if (st != SV_OK) return st;
-    if (B > 0 && (!out_tokens || !num_accepted)) return SV_ERR_INVALID_ARG;
-    if (B > 0 && (!aligned16(out_tokens) || !aligned16(num_accepted))) return SV_ERR_INVALID_ARG;
+    if ((st = check_outputs(out_tokens, num_accepted, B)) != SV_OK) return st;
     const bool sampled = mode == SV_MODE_SAMPLE;
     if (sampled && (st = check_sample(draft_probs, u_accept, u_resample, T, B)) != SV_OK) return st;
     int sms = 0;
@@ -1049,15 +1362,12 @@ sv_status spec_verify_greedy(const void* logits, sv_dtype dtype, const int32_t* 
                              void* ws, size_t ws_bytes, cudaStream_t stream) {
     sv_status st = check_common(logits, dtype, draft_tokens, B, k, V, ws, ws_bytes);
     if (st != SV_OK) return st;
-    if (B > 0 && (!out_tokens || !num_accepted)) return SV_ERR_INVALID_ARG;
-    if (B > 0 && (!aligned16(out_tokens) || !aligned16(num_accepted))) return SV_ERR_INVALID_ARG;
+    if ((st = check_outputs(out_tokens, num_accepted, B)) != SV_OK) return st;
     int sms = 0;
     if ((st = device_setup(&sms)) != SV_OK) return st;
     if (B == 0) return SV_OK;
-    st = launch_rows(false, logits, dtype, nullptr, draft_tokens, 1.0f, B, k, V, ws, stream, sms);
-    if (st != SV_OK) return st;
-    return launch_finish(false, logits, dtype, nullptr, draft_tokens, nullptr, nullptr, 1.0f, B, k,
-                         V, out_tokens, num_accepted, ws, stream, sms);
+    return launch_fused(false, logits, dtype, nullptr, draft_tokens, nullptr, nullptr, 1.0f, B, k,
+                        V, out_tokens, num_accepted, ws, stream, sms);
 }
 
 sv_status spec_verify_sample(const void* logits, sv_dtype dtype, const float* draft_probs,
@@ -1067,16 +1377,13 @@ sv_status spec_verify_sample(const void* logits, sv_dtype dtype, const float* dr
                              size_t ws_bytes, cudaStream_t stream) {
     sv_status st = check_common(logits, dtype, draft_tokens, B, k, V, ws, ws_bytes);
     if (st != SV_OK) return st;
-    if (B > 0 && (!out_tokens || !num_accepted)) return SV_ERR_INVALID_ARG;
-    if (B > 0 && (!aligned16(out_tokens) || !aligned16(num_accepted))) return SV_ERR_INVALID_ARG;
+    if ((st = check_outputs(out_tokens, num_accepted, B)) != SV_OK) return st;
     if ((st = check_sample(draft_probs, u_accept, u_resample, T, B)) != SV_OK) return st;
     int sms = 0;
     if ((st = device_setup(&sms)) != SV_OK) return st;
     if (B == 0) return SV_OK;
-    st = launch_rows(true, logits, dtype, draft_probs, draft_tokens, T, B, k, V, ws, stream, sms);
-    if (st != SV_OK) return st;
-    return launch_finish(true, logits, dtype, draft_probs, draft_tokens, u_accept, u_resample, T,
-                         B, k, V, out_tokens, num_accepted, ws, stream, sms);
+    return launch_fused(true, logits, dtype, draft_probs, draft_tokens, u_accept, u_resample, T, B,
+                        k, V, out_tokens, num_accepted, ws, stream, sms);
 }
 
 sv_status spec_verify_read_status(const void* ws, cudaStream_t stream, uint32_t* device_status,
@@ -1086,9 +1393,24 @@ sv_status spec_verify_read_status(const void* ws, cudaStream_t stream, uint32_t*
     Header h;
     if (cudaMemcpy(&h, ws, sizeof(Header), cudaMemcpyDeviceToHost) != cudaSuccess)
         return SV_ERR_CUDA;
-    *device_status = h.status;
-    if (n_degenerate) *n_degenerate = h.n_degenerate;
-    return (h.status & ~SV_DEV_DEGENERATE) ? SV_ERR_DATA : SV_OK;
+    if (h.magic != kMagic || h.k < 1 || h.k > (uint32_t)kMaxK) return SV_ERR_INVALID_ARG;
+    uint32_t* st = new (std::nothrow) uint32_t[h.B > 0 ? h.B : 1];
+    if (!st) return SV_ERR_INVALID_ARG;
+    cudaError_t e = cudaMemcpy(st, static_cast<const char*>(ws) + ws_seq_offset(h.B, (int)h.k),
+                               (size_t)h.B * sizeof(uint32_t), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) {
+        delete[] st;
+        return SV_ERR_CUDA;
+    }
+    uint32_t bits = 0, ndeg = 0;
+    for (uint32_t b = 0; b < h.B; ++b) {
+        bits |= st[b];
+        ndeg += (st[b] & SV_DEV_DEGENERATE) ? 1u : 0u;
+    }
+    delete[] st;
+    *device_status = bits;
+    if (n_degenerate) *n_degenerate = ndeg;
+    return (bits & ~SV_DEV_DEGENERATE) ? SV_ERR_DATA : SV_OK;
 }
 
 sv_status spec_verify_row_stats(const void* ws, cudaStream_t stream, int B, int k, float* m,
@@ -1102,14 +1424,12 @@ sv_status spec_verify_row_stats(const void* ws, cudaStream_t stream, int B, int 
     const long long R = (long long)B * (k + 1);
     RowRec* host = new (std::nothrow) RowRec[R > 0 ? R : 1];
     if (!host) return SV_ERR_INVALID_ARG;
-    cudaError_t e = cudaMemcpy(host, static_cast<const char*>(ws) + sizeof(Header),
+    cudaError_t e = cudaMemcpy(host, static_cast<const char*>(ws) + ws_rows_offset(),
                                R * sizeof(RowRec), cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) {
         delete[] host;
         return SV_ERR_CUDA;
     }
-    // A temperature is not kept in the workspace; m is reported as stored scaled
-    // back with the T of the records' px (greedy: T = 1).
     for (long long r = 0; r < R; ++r) {
         if (m) m[r] = host[r].mraw;
         if (S) S[r] = host[r].S;
@@ -1140,7 +1460,7 @@ sv_status spec_verify_debug_ffexp(const float* l, float m, float T, int n, doubl
                                   cudaStream_t stream) {
     if (n < 0 || (n > 0 && (!l || !out)) || !(T > 0.0f)) return SV_ERR_INVALID_ARG;
     if (n == 0) return SV_OK;
-    sv_debug_ffexp_kernel<<<(n + 255) / 256, 256, 0, stream>>>(l, m, n, make_rT(T), exp_const(), out);
+    sv_debug_ffexp_kernel<<<(n + 255) / 256, 256, 0, stream>>>(l, m, n, log2e_over(T), out);
     return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
@@ -1155,7 +1475,9 @@ sv_status spec_verify_debug_ffexp(const float* l, float m, float T, int n, doubl
 namespace sv {
 
 constexpr size_t kNoAllocScratchBytes = SV_NOALLOC_SCRATCH_BYTES;
-static_assert(kNoAllocScratchBytes >= 256 + 32 * (size_t)SV_NOALLOC_MAX_ROWS, "scratch size");
+static_assert(kNoAllocScratchBytes >= 256 + 32 * (size_t)SV_NOALLOC_MAX_ROWS +
+                                          4 * (size_t)(SV_NOALLOC_MAX_ROWS / 2) + 255,
+              "scratch size");
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 

@@ -57,7 +57,7 @@ def test_sampled_small(B, k, V, dtype, T, kind):
     assert rep.hard == 0, rep.hard_detail
     assert rep.near_threshold <= 1
     assert st == 0 and bits == 0
-    compare_stats(inp, stats, ref)
+    compare_stats(inp, stats, ref, n)
 
 
 @pytest.mark.parametrize("B,k,V,dtype,T,kind", SMALL)
@@ -68,7 +68,7 @@ def test_greedy_small(B, k, V, dtype, T, kind):
     ref = run_oracle(inp)
     assert np.array_equal(n, ref.n) and np.array_equal(out, ref.out)
     assert st == 0 and bits == 0
-    compare_stats(inp, stats, ref)
+    compare_stats(inp, stats, ref, n)
 
 
 def test_two_stage_equals_one_call():
@@ -94,7 +94,7 @@ def test_workload_full_size(name):
         assert rep.hard == 0, rep.hard_detail
         assert rep.near_threshold <= max(1, rep.rows // 100000)
     assert st == 0 and bits == 0
-    compare_stats(inp, stats, ref)
+    compare_stats(inp, stats, ref, n)
 
 
 def test_config1_shape_many_sequences():
@@ -106,7 +106,7 @@ def test_config1_shape_many_sequences():
     rep = compare_outputs(inp, out, n, ref)
     assert rep.hard == 0, rep.hard_detail
     assert rep.near_threshold <= 2
-    compare_stats(inp, stats, ref)
+    compare_stats(inp, stats, ref, n)
 
 
 def test_mismatch_rate_two_hundred_thousand_rows():
