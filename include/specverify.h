@@ -72,7 +72,7 @@ typedef enum {
     SV_ERR_UNSUPPORTED = 3,  /* sizes beyond the limits above, or no sm_103a device */
     SV_ERR_CUDA = 4,         /* a CUDA runtime call failed (launch, copy) */
     SV_ERR_DATA = 5,         /* device-detected bad data (spec_verify_read_status) */
-    SV_ERR_TIMEOUT = 6       /* reserved: a bounded device-side wait gave up */
+    SV_ERR_TIMEOUT = 6       /* reserved: no device-side wait exists in this version */
 } sv_status;
 
 typedef enum { SV_BF16 = 0, SV_F32 = 1 } sv_dtype;
@@ -85,6 +85,7 @@ typedef enum { SV_MODE_SAMPLE = 0, SV_MODE_GREEDY = 1 } sv_mode;
 #define SV_DEV_BAD_UNIFORM 0x4u  /* a used uniform outside [0, 1) (or NaN) */
 #define SV_DEV_BAD_Q 0x8u        /* q_i(x_i) NaN or negative at a reached position */
 #define SV_DEV_DEGENERATE 0x10u  /* informational: a zero-mass residual drew from p */
+#define SV_DEV_PRECISE 0x20u     /* informational: a draw needed the float-float pass */
 
 /* Bytes of workspace the calls below need for these sizes (0 for invalid sizes). */
 size_t spec_verify_workspace_size(int B, int k, int V, sv_dtype dtype);
@@ -112,10 +113,13 @@ sv_status spec_verify_greedy(const void* logits, sv_dtype dtype,
  *   out_tokens   [B, k+1] int32 (written): accepted drafts 0..n-1, the drawn
  *                token at n, -1 after.
  *   num_accepted [B] int32 (written): n in [0, k], or -1 for an invalid sequence.
- * The acceptance ratios are formed in double from fp32 row statistics; the
- * draw's exponentials, normaliser and running sums are computed to about 48
- * bits (float-float arithmetic, integer prefix sums) so that its token matches
- * an exact-arithmetic draw except when u_resample lies within ~1e-12 of a bin
+ * The acceptance ratios are formed from fp32 row statistics (relative error
+ * ~1e-7..1e-6).  The draw is exact up to ~1e-12: a first fp32 pass with exact
+ * integer prefix sums carries a rigorous error bound D and keeps its token when
+ * u_resample * C lies farther than 2D from both edges of the chosen bin;
+ * otherwise (a few percent of draws, flagged SV_DEV_PRECISE) a second pass
+ * recomputes the row in float-float (~48 bits), so the token matches an
+ * exact-arithmetic draw except when u_resample lies within ~1e-12 of a bin
  * boundary. */
 sv_status spec_verify_sample(const void* logits, sv_dtype dtype, const float* draft_probs,
                              const int32_t* draft_tokens, const float* u_accept,
@@ -171,10 +175,11 @@ sv_status spec_verify_sample_noalloc(const void* logits, sv_dtype dtype,
                                      int B, int k, int V, int32_t* out_tokens,
                                      int32_t* num_accepted, cudaStream_t stream);
 
-/* Synchronises `stream`, then copies the device status word of the last call
- * that used `ws` into *device_status (SV_DEV_* bits).  Returns SV_ERR_DATA if
- * any error bit (all but SV_DEV_DEGENERATE) is set, else SV_OK.
- * *n_degenerate (may be NULL) receives the number of zero-mass residual draws. */
+/* Synchronises `stream`, then ORs the per-sequence status words of the last
+ * call that used `ws` into *device_status (SV_DEV_* bits).  Returns SV_ERR_DATA
+ * if any error bit (all but SV_DEV_DEGENERATE and SV_DEV_PRECISE) is set, else
+ * SV_OK.  *n_degenerate (may be NULL) receives the number of zero-mass residual
+ * draws. */
 sv_status spec_verify_read_status(const void* ws, cudaStream_t stream,
                                   uint32_t* device_status, uint32_t* n_degenerate);
 

@@ -149,6 +149,8 @@ __device__ __forceinline__ ff exp2_ff(float ah, float al, const float* __restric
 
 // e = exp((l - m)/T) = 2^((l - m) * log2(e)/T) for l <= m, with c = log2(e)/T
 // as float-float; 0 when the exponent is below kExp2Min (and for l = -inf).
+// Branch-free: out-of-range arguments are evaluated at 0 and the result masked,
+// so the lanes of a warp never diverge here.
 __device__ __forceinline__ ff exp_rel(float l, float m, ff c, const float* __restrict__ thi,
                                       const float* __restrict__ tlo) {
     ff d = two_sum(l, -m);  // l - m exactly
@@ -156,8 +158,9 @@ __device__ __forceinline__ ff exp_rel(float l, float m, ff c, const float* __res
     float al = __fmaf_rn(d.hi, c.hi, -ah);
     al = __fmaf_rn(d.hi, c.lo, al);
     al = __fmaf_rn(d.lo, c.hi, al);
-    if (!(ah >= kExp2Min)) return ff{0.0f, 0.0f};
-    return exp2_ff(ah, al, thi, tlo);
+    const bool ok = ah >= kExp2Min;  // false for NaN and -inf too
+    ff e = exp2_ff(ok ? ah : 0.0f, ok ? al : 0.0f, thi, tlo);
+    return ff{ok ? e.hi : 0.0f, ok ? e.lo : 0.0f};
 }
 
 // ------------------------------------------------------------------ fixed point
@@ -168,16 +171,16 @@ __device__ __forceinline__ ff exp_rel(float l, float m, ff c, const float* __res
 
 constexpr int kFixBits = 60;
 
-// round-toward-zero of |x| * 2^60 for |x| < 16.
+// round-toward-zero of |x| * 2^60 for |x| < 16, branch-free.
 __device__ __forceinline__ unsigned long long fix_mag(float x) {
     const uint32_t b = __float_as_uint(x) & 0x7FFFFFFFu;
     const int ex = (int)(b >> 23);
-    if (ex == 0) return 0ull;  // zero or subnormal: below the resolution
     const unsigned long long mant = (unsigned long long)((b & 0x7FFFFFu) | 0x800000u);
-    const int sh = ex - 127 - 23 + kFixBits;
-    if (sh >= 0) return mant << sh;
-    if (sh <= -24) return 0ull;
-    return mant >> (-sh);
+    const int sh = ex - 127 - 23 + kFixBits;  // <= 40 for |x| < 16
+    const unsigned long long left = mant << (sh > 0 ? sh : 0);
+    const unsigned long long right = mant >> (sh < 0 ? (sh > -63 ? -sh : 63) : 0);
+    const unsigned long long v = sh >= 0 ? left : right;
+    return ex == 0 ? 0ull : v;  // zero or subnormal: below the resolution
 }
 
 // Fixed-point value of a non-negative float-float (hi >= 0, |lo| <= ulp(hi)).

@@ -44,6 +44,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <new>
 
@@ -270,7 +271,21 @@ __device__ __forceinline__ uint32_t row_flags(const Partial& p) {
 constexpr int kThreads = 512;       // threads per CTA of the per-sequence kernels
 constexpr int kWarps = kThreads / 32;
 constexpr int kChunk = 8;           // contiguous elements per draw work item
-constexpr int kSegStore = 10240;    // largest slice whose exponentials stay in shared memory
+constexpr int kSliceMax = 163840;   // largest slice of a row one CTA draws from (chunk sums in smem)
+
+// Error model of the fast fp32 draw.  ex2.approx.ftz.f32 is taken to be within
+// kEx2RelErr of 2^a (relative) on [-126, 0]; a test measures its worst case
+// exhaustively on that range and checks it is at least 2x below this bound.
+constexpr float kEx2RelErr = 4.76837158e-07f;  // 2^-21
+// Relative error bound of p = ex2(a)/S per element, apart from the argument
+// term: ex2 itself, the normaliser's ex2 errors, and the roundings of 1/S
+// (with S carried to 2^-47), of e * (1/S) and of p - q.
+constexpr float kFastE0 = 2.0f * kEx2RelErr + 4.0f * 5.96046448e-08f;
+// The fp32 argument a = fl(fl(l - m) * fl(log2(e)/T)) is off by at most
+// 3 * 2^-24 * |a|, i.e. 2^a by a relative 3 * 2^-24 * ln2 * |a|.
+constexpr float kFastKappa = 3.0f * 5.96046448e-08f * 0.693147181f;
+// Elements with p < q (1 - kRelSlack) for sure weigh exactly 0 in both passes.
+constexpr float kRelSlack = 4.0e-5f;
 
 template <typename DT>
 __device__ __forceinline__ void load_chunk(const DT* __restrict__ rowp, long long j0, int V,
@@ -305,18 +320,16 @@ __device__ __forceinline__ void load_q_chunk(const float* __restrict__ qrow, lon
     }
 }
 
-// Weight of one element for the draw: p = e/S (bonus) or max(0, p - q)
-// (residual).  Elements with e*inv < q(1 - 2^-20) have p < q for certain and
-// weigh exactly 0 without the float-float work.
+// Weight of one element for the precise draw: p = e/S (bonus) or max(0, p - q)
+// (residual), branch-free.
 __device__ __forceinline__ ff draw_weight(ff e, ff inv, float qv, bool residual) {
-    if (residual && __fmul_rn(e.hi, inv.hi) < __fmul_rn(qv, 0.99999905f)) return ff{0.0f, 0.0f};
     ff p = ff_mul(e, inv);
-    if (!residual) return p;
+    if (!residual) return p;  // uniform across the CTA
     ff s = two_sum(p.hi, -qv);
     ff w = fast_two_sum(s.hi, __fadd_rn(s.lo, p.lo));
-    if (!(w.hi > 0.0f)) return ff{0.0f, 0.0f};
-    if (w.hi > 1.0f) return ff{1.0f, 0.0f};  // only reachable with a negative q entry
-    return w;
+    const bool pos = w.hi > 0.0f;
+    const bool big = w.hi > 1.0f;  // only reachable with a negative q entry
+    return ff{pos ? (big ? 1.0f : w.hi) : 0.0f, (pos && !big) ? w.lo : 0.0f};
 }
 
 template <typename T>
@@ -351,16 +364,25 @@ __device__ __forceinline__ unsigned long long scale_floor(float u, unsigned long
     return (lo >> sh) | (hi << (64 - sh));
 }
 
-// Shared memory the draw phase needs besides its dynamic arrays.
+// Shared memory of the draw besides its dynamic chunk-sum array.
 struct DrawShared {
     float thi[kExpTable], tlo[kExpTable];
     ff red_ff[kWarps];
+    float red_f[kWarps];
     unsigned long long red_u[kWarps];
     unsigned long long woff[kWarps];
-    ff slot_S;                     // this CTA's partial normaliser (read through DSMEM)
-    unsigned long long slot_W[2];  // this CTA's weight totals (read through DSMEM)
+    // per-CTA values read by the other CTAs of the cluster through DSMEM
+    ff slot_S;
+    float slot_A;
+    unsigned long long slot_W[3];
+    float slot_D;
+    int slot_cert;
+    // cluster-wide values, identical in every CTA
     ff S_tot;
+    float A_tot, D_tot;
     unsigned long long prefix, total;
+    int cert_all;
+    int token;
 };
 
 __device__ const Exp2Table g_exp2_table = make_exp2_table();
@@ -372,70 +394,13 @@ __device__ __forceinline__ void load_exp_table(DrawShared& sh) {
     }
 }
 
-// Chunk-level weight of the chunk starting at element j0: the float-float sum of
-// its eight weights, quantised.  Element-level cumulative values inside the
-// chunk are quantisations of the partial sums in the same order, so the last
-// one equals the chunk value exactly.  With `token` set, the first element
-// whose cumulative value exceeds `want` is stored there.
-template <typename DT, bool STORE>
-__device__ __forceinline__ unsigned long long chunk_weight(
-    const DT* __restrict__ rowp, const float* __restrict__ qrow, long long j0, int V, bool al_l,
-    bool al_q, bool residual, float m, ff c, ff inv, const float* ehi, const float* elo,
-    int cidx, int nchs, const DrawShared& sh, unsigned long long want, int* token) {
-    float lf[kChunk], qf[kChunk];
-    if (!STORE) load_chunk<DT>(rowp, j0, V, al_l, lf);
-    if (residual) load_q_chunk(qrow, j0, V, al_q, qf);
-    ff acc{0.0f, 0.0f};
-#pragma unroll
-    for (int e = 0; e < kChunk; ++e) {
-        ff ev = STORE ? ff{ehi[e * nchs + cidx], elo[e * nchs + cidx]}
-                      : exp_rel(lf[e], m, c, sh.thi, sh.tlo);
-        ff w = draw_weight(ev, inv, residual ? qf[e] : 0.0f, residual);
-        ff_accumulate(acc, w);
-        if (token && *token < 0 && w.hi > 0.0f && to_fixed(ff_normalize(acc)) > want)
-            *token = (int)(j0 + e);
-    }
-    return to_fixed(ff_normalize(acc));
-}
-
-// The draw on one row by the G CTAs of a cluster (every CTA calls it; rank r
-// owns chunks [nch*r/G, nch*(r+1)/G)).  The token is written to *token_out by
-// the owning thread only; `degenerate` is set in all threads.
-template <typename DT, bool STORE>
-__device__ void draw_phase(cg::cluster_group& cluster, DrawShared& sh, unsigned char* dyn,
-                           const DT* __restrict__ rowp, const float* __restrict__ qrow,
-                           bool residual, int V, float m, ff c, float u, int rank, int G,
-                           int32_t* token_out, bool& degenerate) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const bool al_l = (reinterpret_cast<uintptr_t>(rowp) & 15) == 0;
-    const bool al_q = residual && (reinterpret_cast<uintptr_t>(qrow) & 15) == 0;
-    const long long nch = (V + kChunk - 1) / kChunk;
-    const long long c0 = nch * rank / G, c1 = nch * (rank + 1) / G;
-    const int mych = (int)(c1 - c0);
-    float* ehi = reinterpret_cast<float*>(dyn);
-    float* elo = ehi + (STORE ? kSegStore : 0);
-    unsigned long long* csum = reinterpret_cast<unsigned long long*>(
-        dyn + (STORE ? 2 * kSegStore * sizeof(float) : 0));
-    const int nchs = STORE ? kSegStore / kChunk : 0;  // stride of the element-major e layout
-
-    // Pass A: e_j = exp((l_j - m)/T) and the normaliser S = sum_j e_j.
-    ff acc{0.0f, 0.0f};
-    for (int ci = tid; ci < mych; ci += kThreads) {
-        const long long j0 = (c0 + ci) * kChunk;
-        float f[kChunk];
-        load_chunk<DT>(rowp, j0, V, al_l, f);
-#pragma unroll
-        for (int e = 0; e < kChunk; ++e) {
-            ff ev = exp_rel(f[e], m, c, sh.thi, sh.tlo);
-            if (STORE) {
-                ehi[e * nchs + ci] = ev.hi;
-                elo[e * nchs + ci] = ev.lo;
-            }
-            ff_accumulate(acc, ev);
-        }
-    }
-    acc = warp_sum_ff(ff_normalize(acc));
-    if (lane == 0) sh.red_ff[warp] = acc;
+// Block sum of a float-float value, then the cluster sum over ranks 0..G-1 in a
+// fixed order (the same tree in every CTA, so every CTA gets the same value).
+__device__ __forceinline__ ff cluster_sum_ff(cg::cluster_group& cluster, DrawShared& sh, ff v,
+                                             int G) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    v = warp_sum_ff(ff_normalize(v));
+    if (lane == 0) sh.red_ff[warp] = v;
     __syncthreads();
     if (warp == 0) {
         ff w = lane < kWarps ? sh.red_ff[lane] : ff{0.0f, 0.0f};
@@ -445,11 +410,272 @@ __device__ void draw_phase(cg::cluster_group& cluster, DrawShared& sh, unsigned 
     cluster.sync();
     if (warp == 0) {
         ff w = lane < G ? *cluster.map_shared_rank(&sh.slot_S, lane) : ff{0.0f, 0.0f};
-        w = warp_sum_ff(w);  // same tree in every CTA: identical S everywhere
+        w = warp_sum_ff(w);
         if (lane == 0) sh.S_tot = w;
     }
     __syncthreads();
-    const ff inv = ff_recip(sh.S_tot);
+    return sh.S_tot;
+}
+
+// Block sum of the chunk-weight totals, then the exclusive prefix of this rank
+// and the grand total over the cluster (sh.prefix, sh.total); `slot` selects
+// which of the three DSMEM slots carries this round.  Also sums one float over
+// the cluster into sh.D_tot (pass 0.0f when unused).
+__device__ __forceinline__ void cluster_prefix(cg::cluster_group& cluster, DrawShared& sh,
+                                               unsigned long long t, float d, int slot, int rank,
+                                               int G) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    t = warp_sum(t);
+    d = warp_sum(d);
+    if (lane == 0) {
+        sh.red_u[warp] = t;
+        sh.red_f[warp] = d;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        unsigned long long w = lane < kWarps ? sh.red_u[lane] : 0ull;
+        float f = lane < kWarps ? sh.red_f[lane] : 0.0f;
+        w = warp_sum(w);
+        f = warp_sum(f);
+        if (lane == 0) {
+            sh.slot_W[slot] = w;
+            sh.slot_D = f;
+        }
+    }
+    cluster.sync();
+    if (warp == 0) {
+        unsigned long long v = lane < G ? cluster.map_shared_rank(sh.slot_W, lane)[slot] : 0ull;
+        float f = lane < G ? *cluster.map_shared_rank(&sh.slot_D, lane) : 0.0f;
+        unsigned long long incl = v;  // inclusive prefix over ranks
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            unsigned long long o = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += o;
+        }
+        f = warp_sum(f);
+        unsigned long long tot = __shfl_sync(0xffffffffu, incl, 31);
+        unsigned long long pre = __shfl_sync(0xffffffffu, incl - v, rank);
+        if (lane == 0) {
+            sh.prefix = pre;
+            sh.total = tot;
+            sh.D_tot = f;
+        }
+    }
+    __syncthreads();
+}
+
+// Inside the CTA that owns `want` (0 <= want < sum of csum[0..mych)), the
+// thread whose contiguous chunk range holds it returns true with the chunk
+// index and the cumulative weight before that chunk; other threads return false.
+__device__ __forceinline__ bool find_chunk(DrawShared& sh, const unsigned long long* csum,
+                                           int mych, unsigned long long want, int* cstar,
+                                           unsigned long long* before) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int L = (mych + kThreads - 1) / kThreads;
+    const int cb = tid * L, ce = min(mych, cb + L);
+    unsigned long long mine = 0;
+    for (int ci = cb; ci < ce; ++ci) mine += csum[ci];
+    unsigned long long incl = mine;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        unsigned long long o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+    }
+    if (lane == 31) sh.red_u[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        unsigned long long wv = lane < kWarps ? sh.red_u[lane] : 0ull;
+        unsigned long long wi = wv;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            unsigned long long o = __shfl_up_sync(0xffffffffu, wi, off);
+            if (lane >= off) wi += o;
+        }
+        if (lane < kWarps) sh.woff[lane] = wi - wv;  // exclusive warp offsets
+    }
+    __syncthreads();
+    const unsigned long long excl = sh.woff[warp] + incl - mine;
+    if (!(mine > 0 && excl <= want && want - excl < mine)) return false;
+    unsigned long long run = excl;
+    int c = cb;
+    for (; c < ce; ++c) {
+        if (want - run < csum[c]) break;
+        run += csum[c];
+    }
+    if (c >= ce) c = ce - 1;  // unreachable: `mine` covers `want`
+    *cstar = c;
+    *before = run;
+    return true;
+}
+
+// ---- fast pass: fp32 exponentials, exact integer prefix sums, error bound
+
+// Fixed-point weights of one chunk from fp32 arithmetic, with the error-bound
+// contribution of its elements.  With `want` < ~0ull, also the first element
+// whose cumulative weight exceeds `want` and the cumulative weights around it.
+template <typename DT>
+__device__ __forceinline__ unsigned long long fast_chunk(
+    const DT* __restrict__ rowp, const float* __restrict__ qrow, long long j0, int V, bool al_l,
+    bool al_q, bool residual, float m, float c, float inv, float* bound, unsigned long long want,
+    int* token, unsigned long long* lo_out, unsigned long long* hi_out) {
+    float lf[kChunk], qf[kChunk];
+    load_chunk<DT>(rowp, j0, V, al_l, lf);
+    if (residual) load_q_chunk(qrow, j0, V, al_q, qf);
+    unsigned long long cs = 0;
+    float bd = 0.0f;
+#pragma unroll
+    for (int e = 0; e < kChunk; ++e) {
+        const float a = (lf[e] - m) * c;
+        const float p = ex2_approx(a) * inv;
+        const float w = residual ? fmaxf(p - qf[e], 0.0f) : p;
+        const bool rel = !residual || p >= qf[e] * (1.0f - kRelSlack);
+        bd += rel ? p * (kFastE0 + kFastKappa * fabsf(a)) : 0.0f;
+        const unsigned long long W = fix_mag(w);
+        if (token && *token < 0 && W > 0 && cs + W > want) {
+            *token = (int)(j0 + e);
+            *lo_out = cs;
+            *hi_out = cs + W;
+        }
+        cs += W;
+    }
+    *bound += bd;
+    return cs;
+}
+
+// The fast draw by the G CTAs of a cluster.  Returns true (in every thread of
+// every CTA) when the token is certified, i.e. u*C lies farther than twice the
+// accumulated error bound from both edges of the chosen bin, so the exact
+// draw picks the same bin; the owner CTA then holds it in sh.token.
+template <typename DT>
+__device__ bool draw_fast(cg::cluster_group& cluster, DrawShared& sh, unsigned long long* csum,
+                          const DT* __restrict__ rowp, const float* __restrict__ qrow,
+                          bool residual, int V, float m, float c, float u, int rank, int G) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const bool al_l = (reinterpret_cast<uintptr_t>(rowp) & 15) == 0;
+    const bool al_q = residual && (reinterpret_cast<uintptr_t>(qrow) & 15) == 0;
+    const long long nch = (V + kChunk - 1) / kChunk;
+    const long long c0 = nch * rank / G, c1 = nch * (rank + 1) / G;
+    const int mych = (int)(c1 - c0);
+
+    // Pass A: S = sum_j ex2(a_j), carried in float-float.
+    ff accS{0.0f, 0.0f};
+    for (int ci = tid; ci < mych; ci += kThreads) {
+        float f[kChunk];
+        load_chunk<DT>(rowp, (c0 + ci) * kChunk, V, al_l, f);
+#pragma unroll
+        for (int e = 0; e < kChunk; ++e) {
+            ff s = two_sum(accS.hi, ex2_approx((f[e] - m) * c));
+            accS.hi = s.hi;
+            accS.lo = __fadd_rn(accS.lo, s.lo);
+        }
+    }
+    const ff S = cluster_sum_ff(cluster, sh, accS, G);
+    const float inv = __frcp_rn(S.hi);
+
+    // Pass B: fixed-point weights, chunk sums, the error bound, cluster prefix.
+    unsigned long long tacc = 0;
+    float bound = 0.0f;
+    for (int ci = tid; ci < mych; ci += kThreads) {
+        unsigned long long cs = fast_chunk<DT>(rowp, qrow, (c0 + ci) * kChunk, V, al_l, al_q,
+                                               residual, m, c, inv, &bound, 0ull, nullptr,
+                                               nullptr, nullptr);
+        csum[ci] = cs;
+        tacc += cs;
+    }
+    cluster_prefix(cluster, sh, tacc, bound, 0, rank, G);
+    const unsigned long long prefix = sh.prefix, total = sh.total, mytot = sh.slot_W[0];
+    // Bound in fixed-point units: the element bounds (with margin for their own
+    // fp32 summation), the rounding of p - q (2^-24 of the total), and one unit
+    // of truncation per element.
+    const float dunits = sh.D_tot * 1.0009765625f * 1.152921504606847e18f +
+                         (float)total * 5.96046448e-08f + (float)V + 2.0f;
+    const unsigned long long D = (unsigned long long)dunits + 1ull;
+
+    const unsigned long long tau = scale_floor(u, total);
+    const bool owner = total > 0 && mytot > 0 && prefix <= tau && tau - prefix < mytot;
+    if (tid == 0) {
+        sh.token = -1;
+        sh.slot_cert = owner ? 0 : 1;
+    }
+    __syncthreads();
+    if (owner) {
+        const unsigned long long want = tau - prefix;
+        int cstar;
+        unsigned long long before;
+        if (find_chunk(sh, csum, mych, want, &cstar, &before)) {
+            float unused = 0.0f;
+            int tok = -1;
+            unsigned long long lo = 0, hi = 0;
+            fast_chunk<DT>(rowp, qrow, (c0 + cstar) * kChunk, V, al_l, al_q, residual, m, c, inv,
+                           &unused, want - before, &tok, &lo, &hi);
+            // bin edges relative to `want`: want - (before + lo) >= 2D and
+            // (before + hi) - want > 2D + 1 certify the bin
+            const unsigned long long below = want - before - lo, above = before + hi - want;
+            sh.token = tok;
+            sh.slot_cert = (tok >= 0 && below >= 2 * D && above > 2 * D + 1) ? 1 : 0;
+        }
+    }
+    cluster.sync();
+    if (warp == 0) {
+        int ok = lane < G ? *cluster.map_shared_rank(&sh.slot_cert, lane) : 1;
+        ok = __all_sync(0xffffffffu, ok);
+        if (lane == 0) sh.cert_all = ok && total > 0;
+    }
+    __syncthreads();
+    return sh.cert_all != 0;
+}
+
+// ---- precise pass: float-float exponentials, exact integer prefix sums
+
+// Chunk-level weight of the chunk starting at element j0: the float-float sum of
+// its eight weights, quantised.  Element-level cumulative values inside the
+// chunk are quantisations of the partial sums in the same order, so the last
+// one equals the chunk value exactly.  With `token` set, the first element
+// whose cumulative value exceeds `want` is stored there.
+template <typename DT>
+__device__ __forceinline__ unsigned long long chunk_weight(
+    const DT* __restrict__ rowp, const float* __restrict__ qrow, long long j0, int V, bool al_l,
+    bool al_q, bool residual, float m, ff c, ff inv, const DrawShared& sh,
+    unsigned long long want, int* token) {
+    float lf[kChunk], qf[kChunk];
+    load_chunk<DT>(rowp, j0, V, al_l, lf);
+    if (residual) load_q_chunk(qrow, j0, V, al_q, qf);
+    ff acc{0.0f, 0.0f};
+#pragma unroll
+    for (int e = 0; e < kChunk; ++e) {
+        ff ev = exp_rel(lf[e], m, c, sh.thi, sh.tlo);
+        ff w = draw_weight(ev, inv, residual ? qf[e] : 0.0f, residual);
+        ff_accumulate(acc, w);
+        if (token && *token < 0 && w.hi > 0.0f && to_fixed(ff_normalize(acc)) > want)
+            *token = (int)(j0 + e);
+    }
+    return to_fixed(ff_normalize(acc));
+}
+
+// The precise draw on one row by the G CTAs of a cluster (rank r owns chunks
+// [nch*r/G, nch*(r+1)/G)).  The owner CTA holds the token in sh.token;
+// `degenerate` is set in all threads.
+template <typename DT>
+__device__ void draw_precise(cg::cluster_group& cluster, DrawShared& sh,
+                             unsigned long long* csum, const DT* __restrict__ rowp,
+                             const float* __restrict__ qrow, bool residual, int V, float m, ff c,
+                             float u, int rank, int G, bool& degenerate) {
+    const int tid = threadIdx.x;
+    const bool al_l = (reinterpret_cast<uintptr_t>(rowp) & 15) == 0;
+    const bool al_q = residual && (reinterpret_cast<uintptr_t>(qrow) & 15) == 0;
+    const long long nch = (V + kChunk - 1) / kChunk;
+    const long long c0 = nch * rank / G, c1 = nch * (rank + 1) / G;
+    const int mych = (int)(c1 - c0);
+
+    // Pass A: e_j = exp((l_j - m)/T) and the normaliser S = sum_j e_j.
+    ff acc{0.0f, 0.0f};
+    for (int ci = tid; ci < mych; ci += kThreads) {
+        float f[kChunk];
+        load_chunk<DT>(rowp, (c0 + ci) * kChunk, V, al_l, f);
+#pragma unroll
+        for (int e = 0; e < kChunk; ++e) ff_accumulate(acc, exp_rel(f[e], m, c, sh.thi, sh.tlo));
+    }
+    const ff inv = ff_recip(cluster_sum_ff(cluster, sh, acc, G));
 
     // Pass B: chunk weights, CTA total, cluster prefix; a second round draws
     // from p when the residual has no mass.
@@ -459,42 +685,15 @@ __device__ void draw_phase(cg::cluster_group& cluster, DrawShared& sh, unsigned 
     for (int round = 0; round < 2; ++round) {
         unsigned long long tacc = 0;
         for (int ci = tid; ci < mych; ci += kThreads) {
-            const long long j0 = (c0 + ci) * kChunk;
-            unsigned long long cs = chunk_weight<DT, STORE>(rowp, qrow, j0, V, al_l, al_q,
-                                                            use_res, m, c, inv, ehi, elo, ci,
-                                                            nchs, sh, 0ull, nullptr);
+            unsigned long long cs = chunk_weight<DT>(rowp, qrow, (c0 + ci) * kChunk, V, al_l,
+                                                     al_q, use_res, m, c, inv, sh, 0ull, nullptr);
             csum[ci] = cs;
             tacc += cs;
         }
-        tacc = warp_sum(tacc);
-        if (lane == 0) sh.red_u[warp] = tacc;
-        __syncthreads();
-        if (warp == 0) {
-            unsigned long long w = lane < kWarps ? sh.red_u[lane] : 0ull;
-            w = warp_sum(w);
-            if (lane == 0) sh.slot_W[round] = w;
-        }
-        cluster.sync();
-        if (warp == 0) {
-            unsigned long long t =
-                lane < G ? cluster.map_shared_rank(sh.slot_W, lane)[round] : 0ull;
-            unsigned long long incl = t;  // inclusive prefix over ranks
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                unsigned long long o = __shfl_up_sync(0xffffffffu, incl, off);
-                if (lane >= off) incl += o;
-            }
-            unsigned long long tot = __shfl_sync(0xffffffffu, incl, 31);
-            unsigned long long pre = __shfl_sync(0xffffffffu, incl - t, rank);
-            if (lane == 0) {
-                sh.prefix = pre;
-                sh.total = tot;
-            }
-        }
-        __syncthreads();
+        cluster_prefix(cluster, sh, tacc, 0.0f, 1 + round, rank, G);
         prefix = sh.prefix;
         total = sh.total;
-        mytot = sh.slot_W[round];
+        mytot = sh.slot_W[1 + round];
         if (total > 0 || !use_res) break;
         use_res = false;  // zero residual mass: draw from p (counted)
         degenerate = true;
@@ -503,47 +702,40 @@ __device__ void draw_phase(cg::cluster_group& cluster, DrawShared& sh, unsigned 
     const unsigned long long tau = scale_floor(u, total);
     const bool owner = mytot > 0 && prefix <= tau && tau - prefix < mytot;
     if (owner) {
-        // Exclusive scan of the chunk weights in index order: thread t owns the
-        // contiguous chunk range [t*L, (t+1)*L).
         const unsigned long long want = tau - prefix;
-        const int L = (mych + kThreads - 1) / kThreads;
-        const int cb = tid * L, ce = min(mych, cb + L);
-        unsigned long long mine = 0;
-        for (int ci = cb; ci < ce; ++ci) mine += csum[ci];
-        unsigned long long incl = mine;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            unsigned long long o = __shfl_up_sync(0xffffffffu, incl, off);
-            if (lane >= off) incl += o;
-        }
-        if (lane == 31) sh.red_u[warp] = incl;
-        __syncthreads();
-        if (warp == 0) {
-            unsigned long long wv = lane < kWarps ? sh.red_u[lane] : 0ull;
-            unsigned long long wi = wv;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                unsigned long long o = __shfl_up_sync(0xffffffffu, wi, off);
-                if (lane >= off) wi += o;
-            }
-            if (lane < kWarps) sh.woff[lane] = wi - wv;  // exclusive warp offsets
-        }
-        __syncthreads();
-        const unsigned long long excl = sh.woff[warp] + incl - mine;
-        if (mine > 0 && excl <= want && want - excl < mine) {
-            unsigned long long run = excl;
-            int cstar = cb;
-            for (; cstar < ce; ++cstar) {
-                if (want - run < csum[cstar]) break;
-                run += csum[cstar];
-            }
-            if (cstar >= ce) cstar = ce - 1;  // unreachable: `mine` covers `want`
+        int cstar;
+        unsigned long long before;
+        if (find_chunk(sh, csum, mych, want, &cstar, &before)) {
             int tok = -1;
-            chunk_weight<DT, STORE>(rowp, qrow, (c0 + cstar) * kChunk, V, al_l, al_q, use_res, m,
-                                    c, inv, ehi, elo, cstar, nchs, sh, want - run, &tok);
-            *token_out = tok;
+            chunk_weight<DT>(rowp, qrow, (c0 + cstar) * kChunk, V, al_l, al_q, use_res, m, c,
+                             inv, sh, want - before, &tok);
+            sh.token = tok;
         }
     }
+}
+
+// The draw: the certified fast pass, and the precise pass when the fast one
+// cannot certify its bin (or when `force_precise`).  Every CTA calls it; the
+// owner CTA's thread 0 writes the token to *token_out.  Sets `degenerate` and
+// `fallback` in all threads.
+template <typename DT>
+__device__ void draw(cg::cluster_group& cluster, DrawShared& sh, unsigned long long* csum,
+                     const DT* __restrict__ rowp, const float* __restrict__ qrow, bool residual,
+                     int V, float m, float c, ff c2, float u, int rank, int G, bool force_precise,
+                     int32_t* token_out, bool& degenerate, bool& fallback) {
+    degenerate = false;
+    fallback = true;
+    if (!force_precise && draw_fast<DT>(cluster, sh, csum, rowp, qrow, residual, V, m, c, u, rank,
+                                        G)) {
+        fallback = false;
+        if (threadIdx.x == 0 && sh.token >= 0) *token_out = sh.token;
+        return;
+    }
+    if (threadIdx.x == 0) sh.token = -1;
+    __syncthreads();
+    draw_precise<DT>(cluster, sh, csum, rowp, qrow, residual, V, m, c2, u, rank, G, degenerate);
+    __syncthreads();
+    if (threadIdx.x == 0 && sh.token >= 0) *token_out = sh.token;
 }
 
 // ------------------------------------------------------------------ the fused kernel
@@ -560,8 +752,9 @@ struct VerifyArgs {
     int32_t* out;
     int32_t* nacc;
     int B, k, V, G, W;
-    float c;     // log2(e)/T (float, for the row statistics)
-    ff c2;       // log2(e)/T in float-float (p(x) and the draw)
+    int force_precise;  // test hook: skip the fast draw
+    float c;     // log2(e)/T (float, for the row statistics and the fast draw)
+    ff c2;       // log2(e)/T in float-float (p(x) and the precise draw)
 };
 
 struct FusedShared {
@@ -575,7 +768,7 @@ struct FusedShared {
     int n, bits;
 };
 
-template <typename DT, bool SAMPLED, bool STORE>
+template <typename DT, bool SAMPLED>
 __global__ void __launch_bounds__(kThreads) sv_verify_kernel(VerifyArgs a) {
     using E = Elt<DT>;
     extern __shared__ __align__(16) unsigned char dyn[];
@@ -659,7 +852,6 @@ __global__ void __launch_bounds__(kThreads) sv_verify_kernel(VerifyArgs a) {
                 if (lane == 0) fs.rowstat[warp] = r;
             }
         } else {
-            __syncthreads();
             if (tid < Wc) fs.rowstat[tid] = fs.part[buf][tid];
         }
         __syncthreads();
@@ -763,15 +955,15 @@ __global__ void __launch_bounds__(kThreads) sv_verify_kernel(VerifyArgs a) {
     const DT* drow = seq_logits + (long long)n * V;
     const float* qrow = n < k ? a.q + ((long long)b * k + n) * V : nullptr;
     const float m = fs.rowstat[n - wave_row0].m;
-    bool degenerate = false;
-    draw_phase<DT, STORE>(cluster, ds, dyn, drow, qrow, n < k, V, m, a.c2, u, rank, G, o + n,
-                          degenerate);
+    bool degenerate = false, fallback = false;
+    draw<DT>(cluster, ds, reinterpret_cast<unsigned long long*>(dyn), drow, qrow, n < k, V, m, a.c,
+             a.c2, u, rank, G, a.force_precise != 0, o + n, degenerate, fallback);
     if (rank == 0) {
         for (int i = tid; i <= k; i += kThreads)
             if (i != n) o[i] = i < n ? fs.xs[i] : -1;
         if (tid == 0) {
             a.nacc[b] = n;
-            a.seqstat[b] = degenerate ? SV_DEV_DEGENERATE : 0u;
+            a.seqstat[b] = (degenerate ? SV_DEV_DEGENERATE : 0u) | (fallback ? SV_DEV_PRECISE : 0u);
         }
     }
     cluster.sync();  // no CTA leaves while another may still read its slots
@@ -806,6 +998,9 @@ __global__ void __launch_bounds__(NT) sv_rows_kernel(RowsArgs a) {
     const DT* rowp = static_cast<const DT*>(a.logits) + row * (long long)V;
     const int b = (int)(row / (a.k + 1));
     const int i = (int)(row % (a.k + 1));
+    // The finish kernel is launched as a programmatic dependent: let it start
+    // its launch now; it waits (griddepcontrol.wait) for this grid's results.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (blockIdx.x == 0 && tid == 0) {
         a.hdr->magic = kMagic;
         a.hdr->B = a.B;
@@ -885,6 +1080,7 @@ __global__ void sv_finish_greedy_kernel(const int32_t* __restrict__ x,
     __shared__ int xs[4][kMaxK];
     const int wi = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.x * 4 + wi;
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the row records are complete
     if (b >= B) return;
     RowRec* rr = recs[wi];
     int* xx = xs[wi];
@@ -924,10 +1120,12 @@ struct FinishArgs {
     int32_t* out;
     int32_t* nacc;
     int B, k, V, G;
+    int force_precise;
+    float c;
     ff c2;
 };
 
-template <typename DT, bool STORE>
+template <typename DT>
 __global__ void __launch_bounds__(kThreads) sv_finish_sample_kernel(FinishArgs a) {
     extern __shared__ __align__(16) unsigned char dyn[];
     __shared__ DrawShared ds;
@@ -941,6 +1139,7 @@ __global__ void __launch_bounds__(kThreads) sv_finish_sample_kernel(FinishArgs a
     const int rank = blockIdx.x % G;
     const int k = a.k, V = a.V;
     load_exp_table(ds);
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the row records are complete
     for (int i = tid; i <= k; i += kThreads) recs[i] = a.rows[(long long)b * (k + 1) + i];
     for (int i = tid; i < k; i += kThreads) uas[i] = a.ua[(long long)b * k + i];
     __syncthreads();
@@ -979,15 +1178,16 @@ __global__ void __launch_bounds__(kThreads) sv_finish_sample_kernel(FinishArgs a
     }
     const DT* drow = static_cast<const DT*>(a.logits) + ((long long)b * (k + 1) + n) * V;
     const float* qrow = n < k ? a.q + ((long long)b * k + n) * V : nullptr;
-    bool degenerate = false;
-    draw_phase<DT, STORE>(cluster, ds, dyn, drow, qrow, n < k, V, recs[n].mraw, a.c2, a.ur[b],
-                          rank, G, o + n, degenerate);
+    bool degenerate = false, fallback = false;
+    draw<DT>(cluster, ds, reinterpret_cast<unsigned long long*>(dyn), drow, qrow, n < k, V,
+             recs[n].mraw, a.c, a.c2, a.ur[b], rank, G, a.force_precise != 0, o + n, degenerate,
+             fallback);
     if (rank == 0) {
         for (int i = tid; i <= k; i += kThreads)
             if (i != n) o[i] = i < n ? a.x[(long long)b * k + i] : -1;
         if (tid == 0) {
             a.nacc[b] = n;
-            a.seqstat[b] = degenerate ? SV_DEV_DEGENERATE : 0u;
+            a.seqstat[b] = (degenerate ? SV_DEV_DEGENERATE : 0u) | (fallback ? SV_DEV_PRECISE : 0u);
         }
     }
     cluster.sync();
@@ -1008,6 +1208,37 @@ __global__ void sv_debug_ffexp_kernel(const float* l, float m, int n, ff c2, dou
     out[i] = (double)e.hi + (double)e.lo;
 }
 
+// Worst relative error of ex2.approx over n consecutive negative-float bit
+// patterns starting at b_lo, against the float-float exponential.
+__global__ void sv_debug_ex2_kernel(uint32_t b_lo, unsigned long long n, float* out) {
+    __shared__ float thi[kExpTable], tlo[kExpTable];
+    for (int t = threadIdx.x; t < kExpTable; t += blockDim.x) {
+        thi[t] = g_exp2_table.hi[t];
+        tlo[t] = g_exp2_table.lo[t];
+    }
+    __syncthreads();
+    float worst = 0.0f;
+    const unsigned long long stride = (unsigned long long)gridDim.x * blockDim.x;
+    for (unsigned long long i = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += stride) {
+        const float a = __uint_as_float(b_lo + (uint32_t)i);
+        const float y = ex2_approx(a);
+        ff r = a >= kExp2Min ? exp2_ff(a, 0.0f, thi, tlo) : ff{0.0f, 0.0f};
+        if (a < kExp2Min) {  // 2^a = 2^-64 * 2^(a + 64), both factors exact or in range
+            ff t = exp2_ff(a + 64.0f, 0.0f, thi, tlo);
+            r = ff{t.hi * 5.42101086e-20f, t.lo * 5.42101086e-20f};
+        }
+        const float err = fabsf((y - r.hi) - r.lo) / r.hi;
+        worst = fmaxf(worst, err);
+    }
+    worst = fmaxf(worst, __shfl_xor_sync(0xffffffffu, worst, 16));
+    worst = fmaxf(worst, __shfl_xor_sync(0xffffffffu, worst, 8));
+    worst = fmaxf(worst, __shfl_xor_sync(0xffffffffu, worst, 4));
+    worst = fmaxf(worst, __shfl_xor_sync(0xffffffffu, worst, 2));
+    worst = fmaxf(worst, __shfl_xor_sync(0xffffffffu, worst, 1));
+    if ((threadIdx.x & 31) == 0) atomicMax(reinterpret_cast<int*>(out), __float_as_int(worst));
+}
+
 // ------------------------------------------------------------------ host side
 
 static ff log2e_over(float T) {
@@ -1015,6 +1246,10 @@ static ff log2e_over(float T) {
     const float hi = (float)v;
     return ff{hi, (float)(v - (double)hi)};
 }
+
+// Test hook (spec_verify_debug_force_precise): every draw takes the precise pass.
+static std::atomic<int> g_force_precise{0};
+
 
 struct DeviceInfo {
     int sms = 0;
@@ -1024,7 +1259,7 @@ struct DeviceInfo {
 static std::mutex g_mu;
 static DeviceInfo g_dev[64];
 
-constexpr size_t kDynSmemMax = 160 * 1024;
+constexpr size_t kDynSmemMax = 160 * 1024;  // chunk sums: up to kSliceMax bytes
 
 template <typename K> static cudaError_t cluster_attrs(K kernel, bool dyn) {
     cudaError_t e =
@@ -1051,16 +1286,12 @@ static sv_status device_setup(int* sms) {
         if (d.ok) {
             cudaError_t e = cudaSuccess;
 #define SV_TRY(x) if (e == cudaSuccess) e = (x)
-            SV_TRY(cluster_attrs(sv_verify_kernel<__nv_bfloat16, true, true>, true));
-            SV_TRY(cluster_attrs(sv_verify_kernel<__nv_bfloat16, true, false>, true));
-            SV_TRY(cluster_attrs(sv_verify_kernel<float, true, true>, true));
-            SV_TRY(cluster_attrs(sv_verify_kernel<float, true, false>, true));
-            SV_TRY(cluster_attrs(sv_verify_kernel<__nv_bfloat16, false, false>, false));
-            SV_TRY(cluster_attrs(sv_verify_kernel<float, false, false>, false));
-            SV_TRY(cluster_attrs(sv_finish_sample_kernel<__nv_bfloat16, true>, true));
-            SV_TRY(cluster_attrs(sv_finish_sample_kernel<__nv_bfloat16, false>, true));
-            SV_TRY(cluster_attrs(sv_finish_sample_kernel<float, true>, true));
-            SV_TRY(cluster_attrs(sv_finish_sample_kernel<float, false>, true));
+            SV_TRY(cluster_attrs(sv_verify_kernel<__nv_bfloat16, true>, true));
+            SV_TRY(cluster_attrs(sv_verify_kernel<float, true>, true));
+            SV_TRY(cluster_attrs(sv_verify_kernel<__nv_bfloat16, false>, false));
+            SV_TRY(cluster_attrs(sv_verify_kernel<float, false>, false));
+            SV_TRY(cluster_attrs(sv_finish_sample_kernel<__nv_bfloat16>, true));
+            SV_TRY(cluster_attrs(sv_finish_sample_kernel<float>, true));
             SV_TRY(cluster_attrs(sv_rows_kernel<__nv_bfloat16, true, 128>, false));
             SV_TRY(cluster_attrs(sv_rows_kernel<__nv_bfloat16, true, 256>, false));
             SV_TRY(cluster_attrs(sv_rows_kernel<__nv_bfloat16, true, 512>, false));
@@ -1122,15 +1353,16 @@ static cudaLaunchAttribute cluster_attr(int G) {
     return at;
 }
 
-// Cluster size of the per-sequence kernels.  Sampled: the smallest split whose
-// slice keeps its exponentials in shared memory (V <= 16 * 10240), widened while
-// the batch leaves SMs idle.  Greedy: enough CTAs to give each SM four, with at
-// least 4 KiB of every row per CTA.
+// Cluster size of the per-sequence kernels.  Sampled: about four CTAs per SM
+// over the whole batch (a 512-thread CTA of these kernels needs little shared
+// memory, so four fit on an SM), but no CTA draws from more than kSliceMax
+// elements of a row and none from fewer than 2048.  Greedy: enough CTAs to give
+// each SM four, with at least 4 KiB of every row per CTA.
 static int seq_split(bool sampled, int B, int V, int esz, int sms) {
     int G = 1;
     if (sampled) {
-        while (G < 16 && (V + G - 1) / G > kSegStore) G *= 2;
-        while (G < 16 && (long long)B * G < 2LL * sms && V / (2 * G) >= 2048) G *= 2;
+        while (G < 16 && (V + G - 1) / G > kSliceMax) G *= 2;
+        while (G < 16 && (long long)B * G * 2 <= 4LL * sms && V / (2 * G) >= 2048) G *= 2;
     } else {
         while (G < 16 && (long long)B * G < 4LL * sms && (long long)V * esz / (2LL * G) >= 4096)
             G *= 2;
@@ -1138,12 +1370,15 @@ static int seq_split(bool sampled, int B, int V, int esz, int sms) {
     return G;
 }
 
-// Rows per wave of the fused kernel: all k+1 rows at once while the batch
-// cannot keep every SM busy (nothing else would use the bandwidth), else one
-// row at a time so that rows after the first rejection are never read.
-static int wave_rows(int B, int k, int G, int sms) {
-    const long long ctas = (long long)B * G;
-    const int W = ctas >= 2LL * sms ? 1 : k + 1;
+// Rows per wave of the fused kernel.  One wave costs about one HBM round trip
+// whatever its size, so a wave should carry enough bytes across the batch to
+// cover the bandwidth-latency product (taken as 32 MiB); beyond that, waves of
+// one row stop at the first rejection and never read the later rows.
+static int wave_rows(int B, int k, int V, int esz) {
+    const double wave_bytes = (double)B * V * esz;
+    int W = (int)std::ceil((32.0 * 1024 * 1024) / (wave_bytes > 1.0 ? wave_bytes : 1.0));
+    if (W < 1) W = 1;
+    if (W > k + 1) W = k + 1;
     return W > kWarps ? kWarps : W;
 }
 
@@ -1167,16 +1402,14 @@ static sv_status launch_fused(bool sampled, const void* logits, sv_dtype dt, con
     a.V = V;
     const int esz = dt == SV_BF16 ? 2 : 4;
     a.G = seq_split(sampled, B, V, esz, sms);
-    a.W = wave_rows(B, k, a.G, sms);
+    a.W = wave_rows(B, k, V, esz);
     a.c2 = log2e_over(sampled ? T : 1.0f);
     a.c = a.c2.hi;
+    a.force_precise = g_force_precise.load();
     size_t smem = 0;
-    bool store = false;
     if (sampled) {
         const long long nch = (V + kChunk - 1) / kChunk;
-        const long long mych_max = (nch + a.G - 1) / a.G;
-        store = mych_max * kChunk <= kSegStore;
-        smem = (store ? 2 * kSegStore * sizeof(float) : 0) + (size_t)mych_max * 8;
+        smem = (size_t)((nch + a.G - 1) / a.G) * 8;  // chunk sums of this CTA's slice
         if (smem > kDynSmemMax) return SV_ERR_UNSUPPORTED;
     }
     cudaLaunchConfig_t cfg = {};
@@ -1188,15 +1421,12 @@ static sv_status launch_fused(bool sampled, const void* logits, sv_dtype dt, con
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cudaError_t e;
-    if (dt == SV_BF16) {
-        if (!sampled) e = cudaLaunchKernelEx(&cfg, sv_verify_kernel<__nv_bfloat16, false, false>, a);
-        else if (store) e = cudaLaunchKernelEx(&cfg, sv_verify_kernel<__nv_bfloat16, true, true>, a);
-        else e = cudaLaunchKernelEx(&cfg, sv_verify_kernel<__nv_bfloat16, true, false>, a);
-    } else {
-        if (!sampled) e = cudaLaunchKernelEx(&cfg, sv_verify_kernel<float, false, false>, a);
-        else if (store) e = cudaLaunchKernelEx(&cfg, sv_verify_kernel<float, true, true>, a);
-        else e = cudaLaunchKernelEx(&cfg, sv_verify_kernel<float, true, false>, a);
-    }
+    if (dt == SV_BF16)
+        e = sampled ? cudaLaunchKernelEx(&cfg, sv_verify_kernel<__nv_bfloat16, true>, a)
+                    : cudaLaunchKernelEx(&cfg, sv_verify_kernel<__nv_bfloat16, false>, a);
+    else
+        e = sampled ? cudaLaunchKernelEx(&cfg, sv_verify_kernel<float, true>, a)
+                    : cudaLaunchKernelEx(&cfg, sv_verify_kernel<float, false>, a);
     return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
@@ -1267,9 +1497,17 @@ static sv_status launch_finish(bool sampled, const void* logits, sv_dtype dt, co
         reinterpret_cast<const RowRec*>(static_cast<char*>(ws) + ws_rows_offset());
     uint32_t* seqstat = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + ws_seq_offset(B, k));
     cudaError_t e;
+    cudaLaunchAttribute pdl;
+    pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl.val.programmaticStreamSerializationAllowed = 1;
     if (!sampled) {
-        sv_finish_greedy_kernel<<<(B + 3) / 4, 128, 0, stream>>>(x, rows, seqstat, B, k, out, nacc);
-        e = cudaGetLastError();
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)((B + 3) / 4), 1, 1);
+        cfg.blockDim = dim3(128, 1, 1);
+        cfg.stream = stream;
+        cfg.attrs = &pdl;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, sv_finish_greedy_kernel, x, rows, seqstat, B, k, out, nacc);
         return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
     }
     FinishArgs a;
@@ -1287,26 +1525,33 @@ static sv_status launch_finish(bool sampled, const void* logits, sv_dtype dt, co
     a.V = V;
     a.G = seq_split(true, B, V, dt == SV_BF16 ? 2 : 4, sms);
     a.c2 = log2e_over(T);
+    a.c = a.c2.hi;
+    a.force_precise = g_force_precise.load();
     const long long nch = (V + kChunk - 1) / kChunk;
-    const long long mych_max = (nch + a.G - 1) / a.G;
-    const bool store = mych_max * kChunk <= kSegStore;
-    const size_t smem = (store ? 2 * kSegStore * sizeof(float) : 0) + (size_t)mych_max * 8;
+    const size_t smem = (size_t)((nch + a.G - 1) / a.G) * 8;
     if (smem > kDynSmemMax) return SV_ERR_UNSUPPORTED;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((long long)B * a.G), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1] = {cluster_attr(a.G)};
+    cudaLaunchAttribute attr[2] = {cluster_attr(a.G), pdl};
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (dt == SV_BF16)
-        e = store ? cudaLaunchKernelEx(&cfg, sv_finish_sample_kernel<__nv_bfloat16, true>, a)
-                  : cudaLaunchKernelEx(&cfg, sv_finish_sample_kernel<__nv_bfloat16, false>, a);
-    else
-        e = store ? cudaLaunchKernelEx(&cfg, sv_finish_sample_kernel<float, true>, a)
-                  : cudaLaunchKernelEx(&cfg, sv_finish_sample_kernel<float, false>, a);
+    cfg.numAttrs = 2;
+    e = dt == SV_BF16 ? cudaLaunchKernelEx(&cfg, sv_finish_sample_kernel<__nv_bfloat16>, a)
+                      : cudaLaunchKernelEx(&cfg, sv_finish_sample_kernel<float>, a);
     return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+// The one-call entry points run the fused per-sequence kernel (rows read in
+// waves, early exit) when the batch alone has a sequence for every SM; smaller
+// batches take the two-kernel path, whose row stream spreads every row over
+// all SMs.
+// Test hook (spec_verify_debug_force_path): 0 automatic, 1 two-kernel, 2 fused.
+static std::atomic<int> g_force_path{0};
+static bool prefer_fused(int B, int sms) {
+    const int f = g_force_path.load();
+    return f == 2 || (f == 0 && B >= sms);
 }
 
 }  // namespace sv
@@ -1366,8 +1611,13 @@ sv_status spec_verify_greedy(const void* logits, sv_dtype dtype, const int32_t* 
     int sms = 0;
     if ((st = device_setup(&sms)) != SV_OK) return st;
     if (B == 0) return SV_OK;
-    return launch_fused(false, logits, dtype, nullptr, draft_tokens, nullptr, nullptr, 1.0f, B, k,
-                        V, out_tokens, num_accepted, ws, stream, sms);
+    if (prefer_fused(B, sms))
+        return launch_fused(false, logits, dtype, nullptr, draft_tokens, nullptr, nullptr, 1.0f, B,
+                            k, V, out_tokens, num_accepted, ws, stream, sms);
+    st = launch_rows(false, logits, dtype, nullptr, draft_tokens, 1.0f, B, k, V, ws, stream, sms);
+    if (st != SV_OK) return st;
+    return launch_finish(false, logits, dtype, nullptr, draft_tokens, nullptr, nullptr, 1.0f, B, k,
+                         V, out_tokens, num_accepted, ws, stream, sms);
 }
 
 sv_status spec_verify_sample(const void* logits, sv_dtype dtype, const float* draft_probs,
@@ -1382,8 +1632,13 @@ sv_status spec_verify_sample(const void* logits, sv_dtype dtype, const float* dr
     int sms = 0;
     if ((st = device_setup(&sms)) != SV_OK) return st;
     if (B == 0) return SV_OK;
-    return launch_fused(true, logits, dtype, draft_probs, draft_tokens, u_accept, u_resample, T, B,
-                        k, V, out_tokens, num_accepted, ws, stream, sms);
+    if (prefer_fused(B, sms))
+        return launch_fused(true, logits, dtype, draft_probs, draft_tokens, u_accept, u_resample,
+                            T, B, k, V, out_tokens, num_accepted, ws, stream, sms);
+    st = launch_rows(true, logits, dtype, draft_probs, draft_tokens, T, B, k, V, ws, stream, sms);
+    if (st != SV_OK) return st;
+    return launch_finish(true, logits, dtype, draft_probs, draft_tokens, u_accept, u_resample, T,
+                         B, k, V, out_tokens, num_accepted, ws, stream, sms);
 }
 
 sv_status spec_verify_read_status(const void* ws, cudaStream_t stream, uint32_t* device_status,
@@ -1410,7 +1665,7 @@ sv_status spec_verify_read_status(const void* ws, cudaStream_t stream, uint32_t*
     delete[] st;
     *device_status = bits;
     if (n_degenerate) *n_degenerate = ndeg;
-    return (bits & ~SV_DEV_DEGENERATE) ? SV_ERR_DATA : SV_OK;
+    return (bits & ~(SV_DEV_DEGENERATE | SV_DEV_PRECISE)) ? SV_ERR_DATA : SV_OK;
 }
 
 sv_status spec_verify_row_stats(const void* ws, cudaStream_t stream, int B, int k, float* m,
@@ -1462,6 +1717,38 @@ sv_status spec_verify_debug_ffexp(const float* l, float m, float T, int n, doubl
     if (n == 0) return SV_OK;
     sv_debug_ffexp_kernel<<<(n + 255) / 256, 256, 0, stream>>>(l, m, n, log2e_over(T), out);
     return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+// Test hook (declared in include/specverify_debug.h): route every sampled draw
+// through the precise float-float pass (on != 0) or back to the certified fast
+// pass with fallback (on == 0).  Affects launches made after the call.
+void spec_verify_debug_force_precise(int on) { g_force_precise.store(on != 0 ? 1 : 0); }
+
+// Test hook (declared in include/specverify_debug.h): choose the one-call path.
+void spec_verify_debug_force_path(int path) { g_force_path.store(path >= 0 && path <= 2 ? path : 0); }
+
+// Introspection (declared in include/specverify_debug.h): 1 if the one-call
+// entry points run the fused per-sequence kernel for a batch of B sequences on
+// the current device, 0 for the two-kernel path, -1 on error.
+int spec_verify_debug_uses_fused(int B) {
+    int sms = 0;
+    if (device_setup(&sms) != SV_OK) return -1;
+    return prefer_fused(B, sms) ? 1 : 0;
+}
+
+// Test hook: the largest relative error of ex2.approx.ftz.f32 against the
+// float-float 2^a over every float a in [a0, a1] (a0 <= a1 <= 0, a0 >= -126),
+// written to *out (a DEVICE float).  Synchronous.
+sv_status spec_verify_debug_ex2_error(float a0, float a1, float* out, cudaStream_t stream) {
+    if (!out || !(a0 <= a1) || !(a1 <= 0.0f) || !(a0 >= -126.0f)) return SV_ERR_INVALID_ARG;
+    if (cudaMemsetAsync(out, 0, sizeof(float), stream) != cudaSuccess) return SV_ERR_CUDA;
+    // floats in [a0, a1] are the bit patterns from bits(a1) up to bits(a0) (negative)
+    const uint32_t b_hi = __builtin_bit_cast(uint32_t, a0);
+    const uint32_t b_lo = __builtin_bit_cast(uint32_t, a1 == 0.0f ? -0.0f : a1);
+    const unsigned long long n = (unsigned long long)(b_hi - b_lo) + 1ull;
+    sv_debug_ex2_kernel<<<1216, 256, 0, stream>>>(b_lo, n, out);
+    if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+    return cudaStreamSynchronize(stream) == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -21,6 +21,7 @@ SV_BF16, SV_F32 = 0, 1
 SV_MODE_SAMPLE, SV_MODE_GREEDY = 0, 1
 SV_DEV_BAD_ROW, SV_DEV_BAD_TOKEN, SV_DEV_BAD_UNIFORM, SV_DEV_BAD_Q, SV_DEV_DEGENERATE = (
     0x1, 0x2, 0x4, 0x8, 0x10)
+SV_DEV_PRECISE = 0x20
 
 EXPORTS = ("spec_verify_workspace_size", "spec_verify_greedy", "spec_verify_sample",
            "spec_verify_rows", "spec_verify_finish", "spec_verify_read_status",
@@ -67,6 +68,14 @@ def load():
     lib.spec_verify_sample_noalloc.restype = I
     lib.spec_verify_debug_ffexp.argtypes = [P, F, F, I, P, P]
     lib.spec_verify_debug_ffexp.restype = I
+    lib.spec_verify_debug_force_precise.argtypes = [I]
+    lib.spec_verify_debug_force_precise.restype = None
+    lib.spec_verify_debug_force_path.argtypes = [I]
+    lib.spec_verify_debug_force_path.restype = None
+    lib.spec_verify_debug_uses_fused.argtypes = [I]
+    lib.spec_verify_debug_uses_fused.restype = I
+    lib.spec_verify_debug_ex2_error.argtypes = [F, F, P, P]
+    lib.spec_verify_debug_ex2_error.restype = I
     _lib = lib
     return lib
 
@@ -199,6 +208,32 @@ def debug_ffexp(l, m: float, T: float, stream=None):
                                         _stream(stream))
     _check(st, "spec_verify_debug_ffexp")
     return out
+
+
+def debug_force_precise(on: bool):
+    """Test hook: every sampled draw takes the precise float-float pass."""
+    load().spec_verify_debug_force_precise(1 if on else 0)
+
+
+def debug_force_path(path: int):
+    """Test hook: 0 automatic, 1 two-kernel path, 2 fused kernel."""
+    load().spec_verify_debug_force_path(int(path))
+
+
+def uses_fused(B: int) -> bool:
+    """Whether the one-call entry points run the fused kernel for B sequences."""
+    r = load().spec_verify_debug_uses_fused(int(B))
+    if r < 0:
+        raise SpecVerifyError(SV_ERR_CUDA, "spec_verify_debug_uses_fused")
+    return bool(r)
+
+
+def debug_ex2_error(a0: float, a1: float, stream=None) -> float:
+    """Test hook: worst relative error of ex2.approx.ftz.f32 over every float in [a0, a1]."""
+    out = torch.zeros(1, dtype=torch.float32, device="cuda")
+    st = load().spec_verify_debug_ex2_error(float(a0), float(a1), _ptr(out), _stream(stream))
+    _check(st, "spec_verify_debug_ex2_error")
+    return float(out.item())
 
 
 # ---------------------------------------------------------------- convenience
