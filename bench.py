@@ -12,9 +12,10 @@ Timing: inputs are resident in HBM and rotated over enough copies to exceed the
 129 MB L2 between reuses; K steps are replayed from CUDA graphs (one graph of
 `copies` consecutive verifies) and timed with CUDA events on the launching
 stream, bracketed by a barrier and a device synchronisation, max over ranks.
-The dominant kernel of the path the one-call API takes is timed the same way
-for the roofline figure (the fused kernel is the whole verify; on the two-kernel
-path the row stream is replayed alone).  `e2e` repeats the measurement through the same C ABI with
+Each kernel of the path the one-call API takes is timed the same way for the
+roofline figure (the fused kernel is the whole verify; on the two-stage paths
+the row stream and the draw kernel are replayed alone), and the slower one is
+reported.  `e2e` repeats the measurement through the same C ABI with
 the inputs in pinned HOST memory: every step copies its inputs host-to-device,
 verifies and copies the outputs back.  `cpu_baseline` times the float64 oracle
 on a bounded sample on this host's cores.  With --impl reference the oracle is
@@ -171,6 +172,31 @@ def algorithmic_bytes_fused(inp, n):
     return b
 
 
+def algorithmic_bytes_rows_needed(inp, n):
+    """Bytes the row stream must move when it reads only the rows the scan needs
+    (0..n_b of every sequence), with their gathers, and writes every record."""
+    esz = 2 if inp.dtype == "bf16" else 4
+    n = np.asarray(n, dtype=np.int64)
+    rows = int(np.sum(np.clip(n, 0, inp.k) + 1))
+    b = rows * inp.V * esz + inp.B * (inp.k + 1) * 32
+    b += inp.B * inp.k * 4 + inp.B * inp.k * 32 * (2 if inp.mode == "sample" else 1)
+    if inp.mode == "sample":
+        b += inp.B * inp.k * 4
+    return b
+
+
+def algorithmic_bytes_draw(inp, n):
+    """Bytes the draw kernel must move: the records of each sequence and, in
+    sampled mode, its decision row once and the q row of a rejection, the
+    uniforms, the outputs."""
+    esz = 2 if inp.dtype == "bf16" else 4
+    n = np.asarray(n, dtype=np.int64)
+    b = inp.B * (inp.k + 1) * 32 + inp.B * inp.k * 4 + inp.B * (inp.k + 2) * 4
+    if inp.mode == "sample":
+        b += inp.B * inp.V * esz + int(np.sum(n < inp.k)) * inp.V * 4 + inp.B * (inp.k + 1) * 4
+    return b
+
+
 def full_tensor_bytes(inp):
     """logits + draft_probs + small inputs (the convention of the headline metric)."""
     b = inp.logits.nbytes + inp.x.nbytes
@@ -288,7 +314,9 @@ def main():
         return d
 
     sets = [dev_set() for _ in range(copies)]
-    fused = sv.uses_fused(B)
+    path = sv.debug_path(sv.SV_MODE_GREEDY if inp.mode == "greedy" else sv.SV_MODE_SAMPLE, B, V,
+                         inp.dtype)
+    fused = path == sv.PATH_FUSED
     ws = [sv.workspace(B, k, V, sets[0]["logits"].dtype, dev) for _ in range(copies)]
     outs = [torch.empty((B, k + 1), dtype=torch.int32, device=dev) for _ in range(copies)]
     ns = [torch.empty(B, dtype=torch.int32, device=dev) for _ in range(copies)]
@@ -349,30 +377,50 @@ def main():
             dist.barrier()
         ms = ev0.elapsed_time(ev1)
 
-        # The dominant kernel of the one-call path, timed alone: the fused kernel
-        # is the whole verify (the loop above); the two-kernel path's row stream
-        # is replayed from a graph of its own over the same rotated inputs.
-        if fused:
-            k1_ms = ms / K
-        else:
-            mode = sv.SV_MODE_GREEDY if inp.mode == "greedy" else sv.SV_MODE_SAMPLE
-            g1 = torch.cuda.CUDAGraph()
+        # Each kernel of the one-call path timed alone: the fused kernel is the
+        # whole verify (the loop above); the two-stage paths' row stream and draw
+        # kernel are replayed from graphs of their own over the same rotated inputs
+        # (the draw graph reads the row records the row-stream graph left).
+        mode = sv.SV_MODE_GREEDY if inp.mode == "greedy" else sv.SV_MODE_SAMPLE
+
+        def stage_ms(fn):
+            g = torch.cuda.CUDAGraph()
             with torch.cuda.stream(stream):
-                with torch.cuda.graph(g1, stream=stream):
+                with torch.cuda.graph(g, stream=stream):
                     for i in range(copies):
-                        s = sets[i]
-                        sv.spec_verify_rows(mode, s["logits"], s.get("q"), s["x"], inp.T, ws[i])
-                g1.replay()
+                        fn(i)
+                g.replay()
                 torch.cuda.synchronize(dev)
                 r1 = max(1, reps // 2)
                 a0 = torch.cuda.Event(enable_timing=True)
                 a1 = torch.cuda.Event(enable_timing=True)
                 a0.record(stream)
                 for _ in range(r1):
-                    g1.replay()
+                    g.replay()
                 a1.record(stream)
             torch.cuda.synchronize(dev)
-            k1_ms = a0.elapsed_time(a1) / (r1 * copies)
+            return a0.elapsed_time(a1) / (r1 * copies)
+
+        def rows_stage(i):
+            s = sets[i]
+            if path == sv.PATH_SKIP:
+                sv.debug_rows_skip(mode, s["logits"], s.get("q"), s["x"], s.get("ua"), inp.T,
+                                   ws[i])
+            else:
+                sv.spec_verify_rows(mode, s["logits"], s.get("q"), s["x"], inp.T, ws[i])
+
+        def finish_stage(i):
+            s = sets[i]
+            sv.spec_verify_finish(mode, s["logits"], s.get("q"), s["x"], s.get("ua"), s.get("ur"),
+                                  inp.T, outs[i], ns[i], ws[i])
+
+        if fused:
+            stage_times = {"sv_verify_kernel": ms / K}
+        else:
+            fin_name = ("sv_finish_greedy_kernel" if inp.mode == "greedy"
+                        else "sv_finish_sample_kernel")
+            stage_times = {"sv_rows_kernel": stage_ms(rows_stage),
+                           fin_name: stage_ms(finish_stage)}
     clocks = sampler.summary()
 
     ms_t = torch.tensor([ms], device=dev)
@@ -432,18 +480,40 @@ def main():
 
     # ---- roofline of the dominant kernel
     peak, peak_src = measured_peaks()
-    kname = "sv_verify_kernel" if fused else "sv_rows_kernel"
-    if fused:
-        alg = int(np.mean([algorithmic_bytes_fused(inp, nn.cpu().numpy()) for nn in ns]))
-    else:
-        alg = algorithmic_bytes_rows(inp)
+    n_all = [nn.cpu().numpy() for nn in ns]
+    rows_read = None
+    if path == sv.PATH_SKIP:  # rows the position-major stream actually read (copy 0)
+        st0 = sv.spec_verify_row_stats(ws[0], B, k)
+        rows_read = int((st0["argmax"] >= 0).sum())
+
+    def alg_bytes(kname):
+        if kname == "sv_verify_kernel":
+            return int(np.mean([algorithmic_bytes_fused(inp, nn) for nn in n_all]))
+        if kname == "sv_rows_kernel":
+            if path == sv.PATH_SKIP:
+                return int(np.mean([algorithmic_bytes_rows_needed(inp, nn) for nn in n_all]))
+            return algorithmic_bytes_rows(inp)
+        return int(np.mean([algorithmic_bytes_draw(inp, nn) for nn in n_all]))
+
+    stages = {}
+    for kname, kms in stage_times.items():
+        alg = alg_bytes(kname)
+        stages[kname] = {"ms": round(kms, 5), "algorithmic_bytes": alg,
+                         "achieved_gbs": round(alg / (kms / 1e3) / 1e9, 1)}
+    kname = max(stage_times, key=stage_times.get)
+    k1_ms = stage_times[kname]
+    alg = stages[kname]["algorithmic_bytes"]
     achieved = alg / (k1_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4),
                 "traffic": ncu_traffic(args.workload, kname),
                 "kernel": kname, "kernel_ms": round(k1_ms, 5),
                 "algorithmic_bytes": alg, "peak_source": peak_src + " (copy bandwidth)",
+                "stages": stages,
                 "full_tensor_gbs": round(full_tensor_bytes(inp) / (ms / K / 1e3) / 1e9, 1)}
+    if rows_read is not None:
+        roofline["rows_read"] = rows_read
+        roofline["rows_needed"] = int(np.mean([np.sum(np.clip(nn, 0, k) + 1) for nn in n_all]))
 
     # ---- CPU baseline: the oracle on a bounded sample
     nt = cores()
@@ -463,7 +533,9 @@ def main():
                    "l2": f"inputs rotated over {copies} device copies "
                          f"({copies * set_bytes / 2**20:.0f} MiB > 129 MB L2)",
                    "timing": f"{reps} replays of a CUDA graph of {copies} verifies",
-                   "path": "fused per-sequence kernel" if fused else "row stream + draw kernels",
+                   "path": {sv.PATH_FUSED: "fused per-sequence kernel",
+                            sv.PATH_SKIP: "position-major row stream with row skipping + draw kernel",
+                            sv.PATH_TWO_KERNEL: "row stream + draw kernels"}[path],
                    "parallelism": f"replicas x{world}"},
         "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": h2d,

@@ -168,7 +168,7 @@ sv_status spec_verify_finish(sv_mode mode, const void* logits, sv_dtype dtype,
  *     device-detected data errors (num_accepted = -1) are as for
  *     spec_verify_sample. */
 #define SV_NOALLOC_SCRATCH_BYTES 1048576
-#define SV_NOALLOC_MAX_ROWS 30720
+#define SV_NOALLOC_MAX_ROWS 27000
 sv_status spec_verify_sample_noalloc(const void* logits, sv_dtype dtype,
                                      const float* draft_probs, const int32_t* draft_tokens,
                                      const float* u_accept, const float* u_resample, float T,

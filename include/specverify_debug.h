@@ -24,14 +24,40 @@ sv_status spec_verify_debug_ffexp(const float* l, float m, float T, int n, doubl
 void spec_verify_debug_force_precise(int on);
 
 /* Choose the path of spec_verify_greedy / spec_verify_sample: 0 automatic
- * (the default: the fused per-sequence kernel when B is at least the SM count,
- * else the two-kernel path), 1 always the two-kernel path, 2 always the fused
- * kernel.  A process-wide setting read at launch time, for tests. */
+ * (the default: the row-skipping path when B is at least the SM count; else,
+ * in sampled mode, the fused per-sequence kernel when its clusters cover every
+ * SM; else the two-kernel path), 1 always the two-kernel path, 2 always the
+ * fused per-sequence kernel, 3 always the row-skipping path.  A process-wide
+ * setting read at launch time, for tests. */
 void spec_verify_debug_force_path(int path);
 
-/* 1 if the one-call entry points would run the fused kernel for a batch of B
- * sequences on the current device, 0 for the two-kernel path, -1 on error. */
-int spec_verify_debug_uses_fused(int B);
+/* The path (1, 2 or 3 as above) the one-call entry points would take for these
+ * sizes on the current device, -1 on error or bad sizes. */
+int spec_verify_debug_path(sv_mode mode, int B, int V, sv_dtype dtype);
+
+/* Fix the cluster size of the sampled draw kernel (spec_verify_finish and the
+ * two-stage paths' second kernel) to G in {1, 2, 4, 8, 16}; 0 restores the
+ * automatic choice; other values are ignored.  A process-wide setting read at
+ * launch time, for tuning and tests. */
+void spec_verify_debug_draw_split(int G);
+
+/* Tuning of the fused per-sequence kernel: defer_mode 0 (default) hands the
+ * draws that need the precise pass to a separate kernel when B is at least the
+ * SM count, 1 always, 2 never; pad_kib > 0 gives every CTA at least that much
+ * dynamic shared memory (KiB, up to 160), limiting how many share an SM.  Out
+ * of range values are ignored.  A process-wide setting read at launch time. */
+void spec_verify_debug_fused_tuning(int defer_mode, int pad_kib);
+
+/* The first stage of the row-skipping path alone: resets the per-sequence stop
+ * rows in `ws` and runs the position-major row stream, leaving the row records
+ * that spec_verify_finish reads (as spec_verify_rows does for the two-kernel
+ * path; rows past a sequence's first stop may be left unread).  Arguments as
+ * for spec_verify_rows, plus u_accept [B, k] fp32 (sampled mode, DEVICE).  For
+ * timing the stages separately. */
+sv_status spec_verify_debug_rows_skip(sv_mode mode, const void* logits, sv_dtype dtype,
+                                      const float* draft_probs, const int32_t* draft_tokens,
+                                      const float* u_accept, float T, int B, int k, int V,
+                                      void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* Writes to *out (a DEVICE float) the largest relative error of the
  * ex2.approx.ftz.f32 instruction against the float-float 2^a over every float a

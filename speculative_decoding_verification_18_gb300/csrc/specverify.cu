@@ -44,6 +44,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 #include <new>
@@ -82,13 +83,21 @@ static_assert(sizeof(RowRec) == 32, "row record size");
 
 constexpr uint32_t kRowBad = 1u, kRowTokenBad = 2u, kRowQBad = 4u, kRowSkipped = 8u;
 
-// Layout: header | B*(k+1) row records | B per-sequence status words.
+// Layout: header | B*(k+1) row records | B per-sequence status words | B
+// per-sequence stop rows (the row-skipping path) | a 16-byte counter and B
+// entries of the list of draws left to the precise kernel (large batches).
 __host__ __device__ inline size_t ws_rows_offset() { return sizeof(Header); }
 __host__ __device__ inline size_t ws_seq_offset(long long B, int k) {
     return sizeof(Header) + (size_t)B * (k + 1) * sizeof(RowRec);
 }
+__host__ __device__ inline size_t ws_stop_offset(long long B, int k) {
+    return ws_seq_offset(B, k) + (size_t)B * sizeof(uint32_t);
+}
+__host__ __device__ inline size_t ws_plist_offset(long long B, int k) {
+    return (ws_stop_offset(B, k) + (size_t)B * sizeof(uint32_t) + 15) & ~(size_t)15;
+}
 __host__ __device__ inline size_t ws_bytes_for(long long B, int k) {
-    size_t b = ws_seq_offset(B, k) + (size_t)B * sizeof(uint32_t);
+    size_t b = ws_plist_offset(B, k) + 16 + (size_t)B * sizeof(uint32_t);
     return (b + 255) & ~(size_t)255;
 }
 
@@ -225,15 +234,18 @@ __device__ __forceinline__ Partial stream_slice(const DT* __restrict__ rowp, int
     if (head_here)
         for (long long j = tg; j < head; j += ng) scalar(j);
     const uint4* vp = reinterpret_cast<const uint4*>(rowp + head);
-    long long v = vb + tg;
-    for (; v + (long long)(U - 1) * ng < ve; v += (long long)U * ng) {
+    // Batches of U vectors per thread, the loads of a batch issued together (the
+    // last batch predicated), so a thread with up to U*n vectors waits for n
+    // round trips.
+    for (long long v = vb + tg; v < ve; v += (long long)U * ng) {
         uint4 buf[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) buf[u] = ld_stream16(vp + v + (long long)u * ng);
+        for (int u = 0; u < U; ++u)
+            if (v + (long long)u * ng < ve) buf[u] = ld_stream16(vp + v + (long long)u * ng);
 #pragma unroll
-        for (int u = 0; u < U; ++u) vector(buf[u], head + (v + (long long)u * ng) * VW);
+        for (int u = 0; u < U; ++u)
+            if (v + (long long)u * ng < ve) vector(buf[u], head + (v + (long long)u * ng) * VW);
     }
-    for (; v < ve; v += ng) vector(ld_stream16(vp + v), head + v * VW);
     if (tail_here)
         for (long long j = tail0 + tg; j < V; j += ng) scalar(j);
     if (best_vec) {  // first element equal to the maximum inside its vector
@@ -271,16 +283,18 @@ __device__ __forceinline__ uint32_t row_flags(const Partial& p) {
 constexpr int kThreads = 512;       // threads per CTA of the per-sequence kernels
 constexpr int kWarps = kThreads / 32;
 constexpr int kChunk = 8;           // contiguous elements per draw work item
-constexpr int kSliceMax = 163840;   // largest slice of a row one CTA draws from (chunk sums in smem)
+constexpr int kSliceMax = 163840;   // largest slice of a row one CTA draws from
 
 // Error model of the fast fp32 draw.  ex2.approx.ftz.f32 is taken to be within
 // kEx2RelErr of 2^a (relative) on [-126, 0]; a test measures its worst case
 // exhaustively on that range and checks it is at least 2x below this bound.
 constexpr float kEx2RelErr = 4.76837158e-07f;  // 2^-21
 // Relative error bound of p = ex2(a)/S per element, apart from the argument
-// term: ex2 itself, the normaliser's ex2 errors, and the roundings of 1/S
-// (with S carried to 2^-47), of e * (1/S) and of p - q.
-constexpr float kFastE0 = 2.0f * kEx2RelErr + 4.0f * 5.96046448e-08f;
+// term: ex2 itself; the normaliser's ex2 errors and the three roundings deep
+// pairwise sums of its chunks (the chunk sums are then carried to 2^-47); the
+// roundings of 1/S (two: the reciprocal and the dropped low part) and of
+// e * (1/S).
+constexpr float kFastE0 = 2.0f * kEx2RelErr + 6.0f * 5.96046448e-08f;
 // The fp32 argument a = fl(fl(l - m) * fl(log2(e)/T)) is off by at most
 // 3 * 2^-24 * |a|, i.e. 2^a by a relative 3 * 2^-24 * ln2 * |a|.
 constexpr float kFastKappa = 3.0f * 5.96046448e-08f * 0.693147181f;
@@ -364,66 +378,109 @@ __device__ __forceinline__ unsigned long long scale_floor(float u, unsigned long
     return (lo >> sh) | (hi << (64 - sh));
 }
 
-// Shared memory of the draw besides its dynamic chunk-sum array.
+// Shared memory of the draw besides its dynamic arrays.  Values exchanged
+// between the CTAs of a cluster are pushed: each CTA writes its total into slot
+// [rank] of every CTA of the cluster (DSMEM stores), then one cluster barrier;
+// afterwards every CTA reads only its own copies, in the same order, so every
+// CTA computes the same totals, and no CTA touches another's shared memory
+// after the last barrier it passes.  Every slot array is written once per draw.
+constexpr int kMaxG = 16;
 struct DrawShared {
-    float thi[kExpTable], tlo[kExpTable];
     ff red_ff[kWarps];
     float red_f[kWarps];
     unsigned long long red_u[kWarps];
     unsigned long long woff[kWarps];
-    // per-CTA values read by the other CTAs of the cluster through DSMEM
-    ff slot_S;
-    float slot_A;
-    unsigned long long slot_W[3];
-    float slot_D;
-    int slot_cert;
-    // cluster-wide values, identical in every CTA
+    ff xS[2][kMaxG];                  // normaliser totals: fast, precise
+    float xA[kMaxG];                  // sum of e * |a| totals (fast)
+    unsigned long long xW[3][kMaxG];  // weight totals: fast, precise, fallback round
+    float xD[kMaxG];                  // error-bound totals (fast)
+    int xC[kMaxG];                    // certificate flags (fast)
     ff S_tot;
-    float A_tot, D_tot;
-    unsigned long long prefix, total;
-    int cert_all;
+    float A_tot;
+    unsigned long long prefix, total, mytot;
+    unsigned long long before;  // find_block's result
+    float D_tot;
+    int blk;
+    int cert, cert_all;
     int token;
 };
 
 __device__ const Exp2Table g_exp2_table = make_exp2_table();
 
-__device__ __forceinline__ void load_exp_table(DrawShared& sh) {
-    for (int i = threadIdx.x; i < kExpTable; i += blockDim.x) {
-        sh.thi[i] = g_exp2_table.hi[i];
-        sh.tlo[i] = g_exp2_table.lo[i];
+// Cluster barrier, or a CTA barrier for a cluster of one.
+__device__ __forceinline__ void xsync(cg::cluster_group& cluster, int G) {
+    if (G > 1) cluster.sync();
+    else __syncthreads();
+}
+
+// Prefetches a CTA's slice (chunks [c0, c0 + mych) of a row) into L2 with bulk
+// prefetches of at most 32 KiB; the part before the first 16-byte boundary and
+// the ragged end are left to the ordinary loads.
+template <typename T>
+__device__ __forceinline__ void prefetch_slice_l2(const T* row, long long c0, int mych, int V) {
+    const long long j0 = c0 * kChunk;
+    const long long n = min((long long)mych * kChunk, (long long)V - j0);
+    if (n <= 0) return;
+    const char* p = reinterpret_cast<const char*>(row + j0);
+    long long bytes = n * (long long)sizeof(T);
+    const long long skip = (long long)((16 - (reinterpret_cast<uintptr_t>(p) & 15)) & 15);
+    p += skip;
+    bytes = (bytes - skip) & ~15ll;
+    for (long long off = 0; off < bytes; off += 32768) {
+        const uint32_t sz = (uint32_t)min(32768ll, bytes - off);
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p + off), "r"(sz)
+                     : "memory");
     }
 }
 
-// Block sum of a float-float value, then the cluster sum over ranks 0..G-1 in a
-// fixed order (the same tree in every CTA, so every CTA gets the same value).
-__device__ __forceinline__ ff cluster_sum_ff(cg::cluster_group& cluster, DrawShared& sh, ff v,
-                                             int G) {
+// Cluster sum of a float-float value (and, with `xa`, of one float into
+// sh.A_tot): a block reduction, the CTA total pushed to slot [rank] of every
+// CTA of the cluster, then each CTA adds the G totals in one fixed order.
+__device__ __forceinline__ ff cluster_sum_ff(cg::cluster_group& cluster, DrawShared& sh,
+                                             ff* xslot, ff v, int rank, int G,
+                                             float* xa = nullptr, float va = 0.0f) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     v = warp_sum_ff(ff_normalize(v));
-    if (lane == 0) sh.red_ff[warp] = v;
+    if (xa) va = warp_sum(va);
+    if (lane == 0) {
+        sh.red_ff[warp] = v;
+        sh.red_f[warp] = va;
+    }
     __syncthreads();
     if (warp == 0) {
         ff w = lane < kWarps ? sh.red_ff[lane] : ff{0.0f, 0.0f};
+        float f = (xa && lane < kWarps) ? sh.red_f[lane] : 0.0f;
         w = warp_sum_ff(w);
-        if (lane == 0) sh.slot_S = w;
+        w = ff{__shfl_sync(0xffffffffu, w.hi, 0), __shfl_sync(0xffffffffu, w.lo, 0)};
+        if (xa) f = __shfl_sync(0xffffffffu, warp_sum(f), 0);
+        if (lane < G) {
+            *cluster.map_shared_rank(&xslot[rank], lane) = w;
+            if (xa) *cluster.map_shared_rank(&xa[rank], lane) = f;
+        }
     }
-    cluster.sync();
+    xsync(cluster, G);
     if (warp == 0) {
-        ff w = lane < G ? *cluster.map_shared_rank(&sh.slot_S, lane) : ff{0.0f, 0.0f};
+        ff w = lane < G ? xslot[lane] : ff{0.0f, 0.0f};
+        float f = (xa && lane < G) ? xa[lane] : 0.0f;
         w = warp_sum_ff(w);
-        if (lane == 0) sh.S_tot = w;
+        if (xa) f = warp_sum(f);
+        if (lane == 0) {
+            sh.S_tot = w;
+            sh.A_tot = f;
+        }
     }
     __syncthreads();
     return sh.S_tot;
 }
 
-// Block sum of the chunk-weight totals, then the exclusive prefix of this rank
-// and the grand total over the cluster (sh.prefix, sh.total); `slot` selects
-// which of the three DSMEM slots carries this round.  Also sums one float over
-// the cluster into sh.D_tot (pass 0.0f when unused).
+// Cluster prefix of the chunk-weight totals: a block reduction (and of one
+// float), the CTA totals pushed to slot [rank] of every CTA; then this rank's
+// exclusive prefix, its own total and the grand total (sh.prefix, sh.mytot,
+// sh.total) and the float's cluster sum (sh.D_tot).  `xw` is the slot array of
+// this round; `xd` may be null.
 __device__ __forceinline__ void cluster_prefix(cg::cluster_group& cluster, DrawShared& sh,
-                                               unsigned long long t, float d, int slot, int rank,
-                                               int G) {
+                                               unsigned long long* xw, float* xd,
+                                               unsigned long long t, float d, int rank, int G) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     t = warp_sum(t);
     d = warp_sum(d);
@@ -435,17 +492,17 @@ __device__ __forceinline__ void cluster_prefix(cg::cluster_group& cluster, DrawS
     if (warp == 0) {
         unsigned long long w = lane < kWarps ? sh.red_u[lane] : 0ull;
         float f = lane < kWarps ? sh.red_f[lane] : 0.0f;
-        w = warp_sum(w);
-        f = warp_sum(f);
-        if (lane == 0) {
-            sh.slot_W[slot] = w;
-            sh.slot_D = f;
+        w = __shfl_sync(0xffffffffu, warp_sum(w), 0);
+        f = __shfl_sync(0xffffffffu, warp_sum(f), 0);
+        if (lane < G) {
+            *cluster.map_shared_rank(&xw[rank], lane) = w;
+            if (xd) *cluster.map_shared_rank(&xd[rank], lane) = f;
         }
     }
-    cluster.sync();
+    xsync(cluster, G);
     if (warp == 0) {
-        unsigned long long v = lane < G ? cluster.map_shared_rank(sh.slot_W, lane)[slot] : 0ull;
-        float f = lane < G ? *cluster.map_shared_rank(&sh.slot_D, lane) : 0.0f;
+        const unsigned long long v = lane < G ? xw[lane] : 0ull;  // lane r: rank r's total
+        float f = (xd && lane < G) ? xd[lane] : 0.0f;
         unsigned long long incl = v;  // inclusive prefix over ranks
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
@@ -453,28 +510,196 @@ __device__ __forceinline__ void cluster_prefix(cg::cluster_group& cluster, DrawS
             if (lane >= off) incl += o;
         }
         f = warp_sum(f);
-        unsigned long long tot = __shfl_sync(0xffffffffu, incl, 31);
-        unsigned long long pre = __shfl_sync(0xffffffffu, incl - v, rank);
+        const unsigned long long tot = __shfl_sync(0xffffffffu, incl, 31);
+        const unsigned long long pre = __shfl_sync(0xffffffffu, incl - v, rank);
+        const unsigned long long mine = __shfl_sync(0xffffffffu, v, rank);
         if (lane == 0) {
             sh.prefix = pre;
             sh.total = tot;
+            sh.mytot = mine;
             sh.D_tot = f;
         }
     }
     __syncthreads();
 }
 
-// Inside the CTA that owns `want` (0 <= want < sum of csum[0..mych)), the
-// thread whose contiguous chunk range holds it returns true with the chunk
-// index and the cumulative weight before that chunk; other threads return false.
-__device__ __forceinline__ bool find_chunk(DrawShared& sh, const unsigned long long* csum,
-                                           int mych, unsigned long long want, int* cstar,
+// ---- work layout of a draw
+//
+// The CTA of rank r owns chunks [c0, c0 + mych) of the row (nch chunks of 8
+// elements split evenly over the G ranks).  Thread t takes chunks t, t + kThreads,
+// ...; a warp's 32 lanes thus cover 32 consecutive chunks per iteration, a
+// "block" of 256 elements whose fixed-point weight total the warp keeps in
+// bsum[block].  Locating the drawn token needs only the block totals: the
+// owning block is recomputed by one warp, the owning chunk by one lane.
+constexpr int kBlockChunks = 32;
+
+template <typename DT>
+struct DrawCtx {
+    const DT* rowp;
+    const float* qrow;
+    int V;
+    bool residual;
+    float m, c;     // row max (raw logit), log2(e)/T in float
+    ff c2;          // log2(e)/T in float-float
+    float u;
+    long long c0;
+    int mych, nblk;
+    bool al_l, al_q;
+    int rank, G;
+    bool prefetch;             // bulk-prefetch the slices into L2 first
+    unsigned long long* bsum;  // [nblk]
+    float* acache;             // [mych * 8] fast-pass exponents, or null
+    ff* ecache;                // [mych * 8] precise exponentials, or null
+    float* thi;                // [kExpTable] each; loaded by the precise pass
+    float* tlo;
+};
+
+template <typename DT>
+__device__ __forceinline__ void load_l(const DrawCtx<DT>& d, int ci, float* f) {
+    load_chunk<DT>(d.rowp, (d.c0 + ci) * kChunk, d.V, d.al_l, f);
+}
+template <typename DT>
+__device__ __forceinline__ void load_q(const DrawCtx<DT>& d, int ci, bool use, float* f) {
+    if (use) {
+        load_q_chunk(d.qrow, (d.c0 + ci) * kChunk, d.V, d.al_q, f);
+    } else {
+#pragma unroll
+        for (int e = 0; e < kChunk; ++e) f[e] = 0.0f;
+    }
+}
+
+__device__ __forceinline__ void store8(float* p, const float* v) {
+    float4* q = reinterpret_cast<float4*>(p);
+    q[0] = make_float4(v[0], v[1], v[2], v[3]);
+    q[1] = make_float4(v[4], v[5], v[6], v[7]);
+}
+__device__ __forceinline__ void load8(const float* p, float* v) {
+    const float4* q = reinterpret_cast<const float4*>(p);
+    const float4 x = q[0], y = q[1];
+    v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+    v[4] = y.x; v[5] = y.y; v[6] = y.z; v[7] = y.w;
+}
+
+// Raw bits of one chunk, so that a thread can hold several chunks in flight in
+// few registers: 8 logits (one or two 16-byte vectors) or 8 q values.  Elements
+// past V read as -inf (logits) or 0 (q), the fill of the scalar loads.
+template <typename DT> struct RawL;
+template <> struct RawL<__nv_bfloat16> { uint4 v[1]; };
+template <> struct RawL<float> { uint4 v[2]; };
+struct RawQ { uint4 v[2]; };
+
+template <typename DT>
+__device__ __forceinline__ void raw_load_l(const DrawCtx<DT>& d, int ci, RawL<DT>& r) {
+    const long long j0 = (d.c0 + ci) * kChunk;
+    constexpr int NV = (int)(sizeof(RawL<DT>) / 16);
+    if (d.al_l && j0 + kChunk <= d.V) {
+#pragma unroll
+        for (int w = 0; w < NV; ++w) r.v[w] = reinterpret_cast<const uint4*>(d.rowp + j0)[w];
+    } else {
+        float f[kChunk];
+        load_chunk<DT>(d.rowp, j0, d.V, d.al_l, f);
+        if constexpr (sizeof(DT) == 2) {  // back to bf16 bits (exact: they came from bf16)
+            uint32_t h[kChunk];
+#pragma unroll
+            for (int e = 0; e < kChunk; ++e) h[e] = __float_as_uint(f[e]) >> 16;
+            r.v[0] = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
+                                h[6] | (h[7] << 16));
+        } else {
+            r.v[0] = make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]),
+                                __float_as_uint(f[2]), __float_as_uint(f[3]));
+            r.v[1] = make_uint4(__float_as_uint(f[4]), __float_as_uint(f[5]),
+                                __float_as_uint(f[6]), __float_as_uint(f[7]));
+        }
+    }
+}
+template <typename DT>
+__device__ __forceinline__ void raw_unpack(const RawL<DT>& r, float* f) {
+    if constexpr (sizeof(DT) == 2) {
+        Elt<__nv_bfloat16>::unpack(r.v[0], f);
+    } else {
+        Elt<float>::unpack(r.v[0], f);
+        Elt<float>::unpack(r.v[1], f + 4);
+    }
+}
+template <typename DT>
+__device__ __forceinline__ void raw_load_q(const DrawCtx<DT>& d, int ci, RawQ& r) {
+    const long long j0 = (d.c0 + ci) * kChunk;
+    if (d.al_q && j0 + kChunk <= d.V) {
+        r.v[0] = reinterpret_cast<const uint4*>(d.qrow + j0)[0];
+        r.v[1] = reinterpret_cast<const uint4*>(d.qrow + j0)[1];
+    } else {
+        float f[kChunk];
+        load_q_chunk(d.qrow, j0, d.V, d.al_q, f);
+        r.v[0] = make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                            __float_as_uint(f[3]));
+        r.v[1] = make_uint4(__float_as_uint(f[4]), __float_as_uint(f[5]), __float_as_uint(f[6]),
+                            __float_as_uint(f[7]));
+    }
+}
+__device__ __forceinline__ void raw_unpack_q(const RawQ& r, float* f) {
+    Elt<float>::unpack(r.v[0], f);
+    Elt<float>::unpack(r.v[1], f + 4);
+}
+
+// Exponents a = (l - m) * log2(e)/T of one chunk, rounded the same way
+// wherever they are formed.
+__device__ __forceinline__ void fast_exponents(const float* l, float m, float c, float* a) {
+#pragma unroll
+    for (int e = 0; e < kChunk; ++e) a[e] = __fmul_rn(__fsub_rn(l[e], m), c);
+}
+
+// The exponents of chunk ci: from the cache when there is one, else formed
+// from the logits (identical values either way).
+template <typename DT>
+__device__ __forceinline__ void chunk_exponents(const DrawCtx<DT>& d, int ci, const float* l,
+                                                float* a) {
+    if (d.acache) {
+        load8(d.acache + (size_t)ci * kChunk, a);
+    } else {
+        fast_exponents(l, d.m, d.c, a);
+    }
+}
+
+// Weights of one chunk in fp32 (p = ex2(a) / S, or max(0, p - q) when RES)
+// with their error-bound contribution added to *bd.
+template <bool RES>
+__device__ __forceinline__ void fast_weights(const float* a, const float* q, float inv, float* w,
+                                             float* bd) {
+    float b = 0.0f;
+#pragma unroll
+    for (int e = 0; e < kChunk; ++e) {
+        const float p = __fmul_rn(ex2_approx(a[e]), inv);
+        w[e] = RES ? fmaxf(__fsub_rn(p, q[e]), 0.0f) : p;
+        const bool rel = !RES || p >= q[e] * (1.0f - kRelSlack);
+        b = fmaf(rel ? p : 0.0f, fmaf(kFastKappa, fabsf(a[e]), kFastE0), b);
+    }
+    *bd += b;
+}
+
+// Fixed-point value of a chunk: its weights summed left to right in fp32, the
+// sum quantised.  The same partial sums quantised give the element-level
+// cumulative values, so the last of them equals the chunk value.
+__device__ __forceinline__ unsigned long long fast_chunk_value(const float* w) {
+    float cs = 0.0f;
+#pragma unroll
+    for (int e = 0; e < kChunk; ++e) cs = __fadd_rn(cs, w[e]);
+    return fix_mag(cs);
+}
+
+// Inside the CTA: the block holding `want` (0 <= want < the CTA's total) and
+// the total of the blocks before it.  Every thread returns the same values.
+__device__ __forceinline__ void find_block(DrawShared& sh, const unsigned long long* bsum,
+                                           int nblk, unsigned long long want, int* blk,
                                            unsigned long long* before) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int L = (mych + kThreads - 1) / kThreads;
-    const int cb = tid * L, ce = min(mych, cb + L);
+    const int L = (nblk + kThreads - 1) / kThreads;
+    const int cb = min(nblk, tid * L), ce = min(nblk, cb + L);
+    if (tid == 0) {  // replaced by the one thread whose range holds `want`
+        sh.blk = 0;
+        sh.before = 0;
+    }
     unsigned long long mine = 0;
-    for (int ci = cb; ci < ce; ++ci) mine += csum[ci];
+    for (int i = cb; i < ce; ++i) mine += bsum[i];
     unsigned long long incl = mine;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -495,129 +720,202 @@ __device__ __forceinline__ bool find_chunk(DrawShared& sh, const unsigned long l
     }
     __syncthreads();
     const unsigned long long excl = sh.woff[warp] + incl - mine;
-    if (!(mine > 0 && excl <= want && want - excl < mine)) return false;
-    unsigned long long run = excl;
-    int c = cb;
-    for (; c < ce; ++c) {
-        if (want - run < csum[c]) break;
-        run += csum[c];
+    if (mine > 0 && excl <= want && want - excl < mine) {  // exactly one thread
+        unsigned long long run = excl;
+        int i = cb;
+        for (; i < ce - 1; ++i) {
+            if (want - run < bsum[i]) break;
+            run += bsum[i];
+        }
+        sh.blk = i;
+        sh.before = run;
     }
-    if (c >= ce) c = ce - 1;  // unreachable: `mine` covers `want`
-    *cstar = c;
-    *before = run;
-    return true;
+    __syncthreads();
+    *blk = min(max(sh.blk, 0), max(nblk - 1, 0));
+    *before = sh.before;
+}
+
+// Inside warp 0: lane values v (chunk weights of a block, in chunk order); the
+// lane whose chunk holds `want` (relative to the block) returns true with the
+// weight before its chunk.
+__device__ __forceinline__ bool find_lane(unsigned long long v, unsigned long long want,
+                                          unsigned long long* before) {
+    const int lane = threadIdx.x & 31;
+    unsigned long long incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        unsigned long long o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+    }
+    const unsigned long long excl = incl - v;
+    *before = excl;
+    return v > 0 && excl <= want && want - excl < v;
 }
 
 // ---- fast pass: fp32 exponentials, exact integer prefix sums, error bound
 
-// Fixed-point weights of one chunk from fp32 arithmetic, with the error-bound
-// contribution of its elements.  With `want` < ~0ull, also the first element
-// whose cumulative weight exceeds `want` and the cumulative weights around it.
-template <typename DT>
-__device__ __forceinline__ unsigned long long fast_chunk(
-    const DT* __restrict__ rowp, const float* __restrict__ qrow, long long j0, int V, bool al_l,
-    bool al_q, bool residual, float m, float c, float inv, float* bound, unsigned long long want,
-    int* token, unsigned long long* lo_out, unsigned long long* hi_out) {
-    float lf[kChunk], qf[kChunk];
-    load_chunk<DT>(rowp, j0, V, al_l, lf);
-    if (residual) load_q_chunk(qrow, j0, V, al_q, qf);
-    unsigned long long cs = 0;
-    float bd = 0.0f;
-#pragma unroll
-    for (int e = 0; e < kChunk; ++e) {
-        const float a = (lf[e] - m) * c;
-        const float p = ex2_approx(a) * inv;
-        const float w = residual ? fmaxf(p - qf[e], 0.0f) : p;
-        const bool rel = !residual || p >= qf[e] * (1.0f - kRelSlack);
-        bd += rel ? p * (kFastE0 + kFastKappa * fabsf(a)) : 0.0f;
-        const unsigned long long W = fix_mag(w);
-        if (token && *token < 0 && W > 0 && cs + W > want) {
-            *token = (int)(j0 + e);
-            *lo_out = cs;
-            *hi_out = cs + W;
-        }
-        cs += W;
-    }
-    *bound += bd;
-    return cs;
-}
-
-// The fast draw by the G CTAs of a cluster.  Returns true (in every thread of
-// every CTA) when the token is certified, i.e. u*C lies farther than twice the
-// accumulated error bound from both edges of the chosen bin, so the exact
-// draw picks the same bin; the owner CTA then holds it in sh.token.
-template <typename DT>
-__device__ bool draw_fast(cg::cluster_group& cluster, DrawShared& sh, unsigned long long* csum,
-                          const DT* __restrict__ rowp, const float* __restrict__ qrow,
-                          bool residual, int V, float m, float c, float u, int rank, int G) {
+// The fast draw by the G CTAs of a cluster (RES: the residual max(0, p - q),
+// else p).  Returns true (in every thread of every CTA) when the token is
+// certified: u * C lies farther than twice the accumulated error bound from
+// both edges of the chosen bin, so the exact draw picks the same bin.  The owner
+// CTA then holds the token in sh.token.
+template <typename DT, bool RES>
+__device__ bool draw_fast(cg::cluster_group& cluster, DrawShared& sh, const DrawCtx<DT>& d) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const bool al_l = (reinterpret_cast<uintptr_t>(rowp) & 15) == 0;
-    const bool al_q = residual && (reinterpret_cast<uintptr_t>(qrow) & 15) == 0;
-    const long long nch = (V + kChunk - 1) / kChunk;
-    const long long c0 = nch * rank / G, c1 = nch * (rank + 1) / G;
-    const int mych = (int)(c1 - c0);
-
-    // Pass A: S = sum_j ex2(a_j), carried in float-float.
-    ff accS{0.0f, 0.0f};
-    for (int ci = tid; ci < mych; ci += kThreads) {
-        float f[kChunk];
-        load_chunk<DT>(rowp, (c0 + ci) * kChunk, V, al_l, f);
-#pragma unroll
-        for (int e = 0; e < kChunk; ++e) {
-            ff s = two_sum(accS.hi, ex2_approx((f[e] - m) * c));
-            accS.hi = s.hi;
-            accS.lo = __fadd_rn(accS.lo, s.lo);
-        }
-    }
-    const ff S = cluster_sum_ff(cluster, sh, accS, G);
-    const float inv = __frcp_rn(S.hi);
-
-    // Pass B: fixed-point weights, chunk sums, the error bound, cluster prefix.
-    unsigned long long tacc = 0;
-    float bound = 0.0f;
-    for (int ci = tid; ci < mych; ci += kThreads) {
-        unsigned long long cs = fast_chunk<DT>(rowp, qrow, (c0 + ci) * kChunk, V, al_l, al_q,
-                                               residual, m, c, inv, &bound, 0ull, nullptr,
-                                               nullptr, nullptr);
-        csum[ci] = cs;
-        tacc += cs;
-    }
-    cluster_prefix(cluster, sh, tacc, bound, 0, rank, G);
-    const unsigned long long prefix = sh.prefix, total = sh.total, mytot = sh.slot_W[0];
-    // Bound in fixed-point units: the element bounds (with margin for their own
-    // fp32 summation), the rounding of p - q (2^-24 of the total), and one unit
-    // of truncation per element.
-    const float dunits = sh.D_tot * 1.0009765625f * 1.152921504606847e18f +
-                         (float)total * 5.96046448e-08f + (float)V + 2.0f;
-    const unsigned long long D = (unsigned long long)dunits + 1ull;
-
-    const unsigned long long tau = scale_floor(u, total);
-    const bool owner = total > 0 && mytot > 0 && prefix <= tau && tau - prefix < mytot;
     if (tid == 0) {
         sh.token = -1;
-        sh.slot_cert = owner ? 0 : 1;
+        sh.cert = 0;
     }
-    __syncthreads();
-    if (owner) {
-        const unsigned long long want = tau - prefix;
-        int cstar;
-        unsigned long long before;
-        if (find_chunk(sh, csum, mych, want, &cstar, &before)) {
-            float unused = 0.0f;
-            int tok = -1;
-            unsigned long long lo = 0, hi = 0;
-            fast_chunk<DT>(rowp, qrow, (c0 + cstar) * kChunk, V, al_l, al_q, residual, m, c, inv,
-                           &unused, want - before, &tok, &lo, &hi);
-            // bin edges relative to `want`: want - (before + lo) >= 2D and
-            // (before + hi) - want > 2D + 1 certify the bin
-            const unsigned long long below = want - before - lo, above = before + hi - want;
-            sh.token = tok;
-            sh.slot_cert = (tok >= 0 && below >= 2 * D && above > 2 * D + 1) ? 1 : 0;
+
+    // Pass A: S = sum_j ex2(a_j); each chunk summed pairwise in fp32 (3 roundings
+    // deep), the chunk sums accumulated in float-float.  Also A = sum_j ex2(a_j)|a_j|
+    // for the argument-rounding part of S's error.
+    ff accS{0.0f, 0.0f};
+    float accA = 0.0f;
+    // UA chunks per thread in flight (16 registers of raw logits).
+    constexpr int UA = sizeof(DT) == 2 ? 4 : 2;
+    for (int base = tid; base < d.mych; base += UA * kThreads) {
+        RawL<DT> raw[UA];
+#pragma unroll
+        for (int u = 0; u < UA; ++u)
+            if (base + u * kThreads < d.mych) raw_load_l(d, base + u * kThreads, raw[u]);
+#pragma unroll
+        for (int u = 0; u < UA; ++u) {
+            const int ci = base + u * kThreads;
+            if (ci >= d.mych) break;
+            float l[kChunk], a[kChunk];
+            raw_unpack(raw[u], l);
+            fast_exponents(l, d.m, d.c, a);
+            if (d.acache) store8(d.acache + (size_t)ci * kChunk, a);
+            float y[kChunk];
+#pragma unroll
+            for (int e = 0; e < kChunk; ++e) {
+                y[e] = ex2_approx(a[e]);
+                accA = fmaf(y[e], fabsf(a[e]), accA);
+            }
+            const float s = __fadd_rn(__fadd_rn(__fadd_rn(y[0], y[1]), __fadd_rn(y[2], y[3])),
+                                      __fadd_rn(__fadd_rn(y[4], y[5]), __fadd_rn(y[6], y[7])));
+            const ff t = two_sum(accS.hi, s);
+            accS.hi = t.hi;
+            accS.lo = __fadd_rn(accS.lo, t.lo);
         }
     }
-    cluster.sync();
+    const ff S = cluster_sum_ff(cluster, sh, sh.xS[0], accS, d.rank, d.G, sh.xA, accA);
+    const float inv = __frcp_rn(S.hi);
+
+    // Pass B: fixed-point chunk values, block totals, the error bound.
+    unsigned long long tacc = 0;
+    float bound = 0.0f;
+    // Two blocks per warp in flight: the q chunks, and the logits when they
+    // are not cached.
+    constexpr int UB = 2;
+    for (int base0 = warp * kBlockChunks; base0 < d.mych; base0 += UB * kThreads) {
+        RawQ rq[UB];
+        RawL<DT> rl[UB];
+#pragma unroll
+        for (int u = 0; u < UB; ++u) {
+            const int ci = base0 + u * kThreads + lane;
+            if (ci < d.mych) {
+                if (RES) raw_load_q(d, ci, rq[u]);
+                if (!d.acache) raw_load_l(d, ci, rl[u]);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < UB; ++u) {
+            const int base = base0 + u * kThreads;
+            if (base >= d.mych) break;  // uniform across the warp
+            const int ci = base + lane;
+            unsigned long long W = 0;
+            if (ci < d.mych) {
+                float q[kChunk] = {}, l[kChunk] = {}, a[kChunk], w[kChunk];
+                if (RES) raw_unpack_q(rq[u], q);
+                if (!d.acache) raw_unpack(rl[u], l);
+                chunk_exponents(d, ci, l, a);
+                fast_weights<RES>(a, q, inv, w, &bound);
+                W = fast_chunk_value(w);
+                // the cache now keeps the weights, for the owner's search
+                if (d.acache) store8(d.acache + (size_t)ci * kChunk, w);
+            }
+            const unsigned long long bw = warp_sum(W);
+            if (lane == 0) {
+                d.bsum[base / kBlockChunks] = bw;
+                tacc += bw;
+            }
+        }
+    }
+    cluster_prefix(cluster, sh, sh.xW[0], sh.xD, tacc, bound, d.rank, d.G);
+    const unsigned long long prefix = sh.prefix, total = sh.total, mytot = sh.mytot;
+    // Bound in fixed-point units: the element bounds; for the residual, the
+    // argument roundings inside S (kappa * sum_j p_j |a_j|, times the mass of
+    // the counted elements, at most about 1; a common factor of all p, so
+    // irrelevant to the draw from p), both with a margin for their own fp32
+    // sums; the roundings of p - q and of the sequential chunk sums (8 units of
+    // 2^-24 of the total); one unit of truncation per chunk value plus two for
+    // the bin edges.
+    const long long nch = ((long long)d.V + kChunk - 1) / kChunk;
+    const float sarg = RES ? kFastKappa * sh.A_tot * inv * 1.0009765625f : 0.0f;
+    float dunits = (sh.D_tot + sarg) * 1.0009765625f * 1.152921504606847e18f +
+                   (float)total * (8.0f * 5.96046448e-08f) + (float)nch + 4.0f;
+    dunits = fminf(dunits, 1.0e18f);  // beyond any total: certifies nothing
+    const unsigned long long D = (unsigned long long)dunits + 1ull;
+
+    const unsigned long long tau = scale_floor(d.u, total);
+    const bool owner = total > 0 && mytot > 0 && prefix <= tau && tau - prefix < mytot;
+    int cert = 1;
+    if (owner) {  // uniform across the CTA
+        const unsigned long long want = tau - prefix;
+        int blk;
+        unsigned long long bbefore;
+        find_block(sh, d.bsum, d.nblk, want, &blk, &bbefore);
+        if (warp == 0) {
+            const int ci = blk * kBlockChunks + lane;
+            float w[kChunk] = {};
+            unsigned long long W = 0;
+            if (ci < d.mych) {
+                if (d.acache) {
+                    load8(d.acache + (size_t)ci * kChunk, w);
+                } else {
+                    float l[kChunk], q[kChunk], a[kChunk], unused = 0.0f;
+                    load_l(d, ci, l);
+                    load_q(d, ci, RES, q);
+                    fast_exponents(l, d.m, d.c, a);
+                    fast_weights<RES>(a, q, inv, w, &unused);
+                }
+                W = fast_chunk_value(w);
+            }
+            const unsigned long long wb = want - bbefore;
+            unsigned long long cb;
+            if (find_lane(W, wb, &cb)) {
+                const unsigned long long wc = wb - cb;  // `want` inside the chunk
+                float cs = 0.0f;
+                int tok = -1;
+                unsigned long long lo = 0, hi = 0;
+#pragma unroll
+                for (int e = 0; e < kChunk; ++e) {
+                    const float prev = cs;
+                    cs = __fadd_rn(cs, w[e]);
+                    const unsigned long long h = fix_mag(cs);
+                    if (tok < 0 && h > wc) {
+                        tok = e;
+                        lo = fix_mag(prev);
+                        hi = h;
+                    }
+                }
+                // bin edges relative to `want`: want - lo >= 2D and hi - want > 2D + 1
+                // certify the bin
+                if (tok >= 0) {
+                    sh.token = (int)((d.c0 + ci) * kChunk + tok);
+                    sh.cert = (wc - lo >= 2 * D && hi - wc > 2 * D + 1) ? 1 : 0;
+                }
+            }
+        }
+        __syncthreads();
+        cert = sh.cert;
+    }
+    if (tid < d.G) *cluster.map_shared_rank(&sh.xC[d.rank], tid) = cert;
+    xsync(cluster, d.G);
     if (warp == 0) {
-        int ok = lane < G ? *cluster.map_shared_rank(&sh.slot_cert, lane) : 1;
+        int ok = lane < d.G ? sh.xC[lane] : 1;
         ok = __all_sync(0xffffffffu, ok);
         if (lane == 0) sh.cert_all = ok && total > 0;
     }
@@ -627,115 +925,276 @@ __device__ bool draw_fast(cg::cluster_group& cluster, DrawShared& sh, unsigned l
 
 // ---- precise pass: float-float exponentials, exact integer prefix sums
 
-// Chunk-level weight of the chunk starting at element j0: the float-float sum of
-// its eight weights, quantised.  Element-level cumulative values inside the
-// chunk are quantisations of the partial sums in the same order, so the last
-// one equals the chunk value exactly.  With `token` set, the first element
-// whose cumulative value exceeds `want` is stored there.
-template <typename DT>
-__device__ __forceinline__ unsigned long long chunk_weight(
-    const DT* __restrict__ rowp, const float* __restrict__ qrow, long long j0, int V, bool al_l,
-    bool al_q, bool residual, float m, ff c, ff inv, const DrawShared& sh,
-    unsigned long long want, int* token) {
-    float lf[kChunk], qf[kChunk];
-    load_chunk<DT>(rowp, j0, V, al_l, lf);
-    if (residual) load_q_chunk(qrow, j0, V, al_q, qf);
+// Fixed-point value of chunk ci for the precise draw: the float-float sum of its
+// eight weights, quantised.  Element-level cumulative values inside the chunk
+// are quantisations of the partial sums in the same order, so the last one
+// equals the chunk value.  With `token` set, the first element (0..7) whose
+// cumulative value exceeds `want` is stored there.  The exponentials come from
+// the cache (`e_cached`) or are recomputed from the logits l; with `wstore`
+// the weights are stored there (over the cached exponentials they came from).
+template <typename DT, bool RES, bool ECACHED, bool WSTORE>
+__device__ __forceinline__ unsigned long long precise_chunk(const DrawCtx<DT>& d, int ci,
+                                                            const float* l, const float* q,
+                                                            ff inv, unsigned long long want,
+                                                            int* token) {
     ff acc{0.0f, 0.0f};
+    ff* wstore = WSTORE ? d.ecache + (size_t)ci * kChunk : nullptr;
 #pragma unroll
     for (int e = 0; e < kChunk; ++e) {
-        ff ev = exp_rel(lf[e], m, c, sh.thi, sh.tlo);
-        ff w = draw_weight(ev, inv, residual ? qf[e] : 0.0f, residual);
+        const ff ev = ECACHED ? d.ecache[(size_t)ci * kChunk + e]
+                              : exp_rel(l[e], d.m, d.c2, d.thi, d.tlo);
+        const ff w = draw_weight(ev, inv, RES ? q[e] : 0.0f, RES);
+        if (WSTORE) wstore[e] = w;
         ff_accumulate(acc, w);
-        if (token && *token < 0 && w.hi > 0.0f && to_fixed(ff_normalize(acc)) > want)
-            *token = (int)(j0 + e);
+        if (token && *token < 0 && w.hi > 0.0f && to_fixed(ff_normalize(acc)) > want) *token = e;
     }
     return to_fixed(ff_normalize(acc));
 }
 
-// The precise draw on one row by the G CTAs of a cluster (rank r owns chunks
-// [nch*r/G, nch*(r+1)/G)).  The owner CTA holds the token in sh.token;
-// `degenerate` is set in all threads.
-template <typename DT>
-__device__ void draw_precise(cg::cluster_group& cluster, DrawShared& sh,
-                             unsigned long long* csum, const DT* __restrict__ rowp,
-                             const float* __restrict__ qrow, bool residual, int V, float m, ff c,
-                             float u, int rank, int G, bool& degenerate) {
+// One round of the precise pass B over the CTA's slice: chunk values into the
+// block totals; returns this thread's share of the CTA total.
+template <typename DT, bool RES, bool ECACHED, bool WSTORE>
+__device__ __forceinline__ unsigned long long precise_pass_b(const DrawCtx<DT>& d, ff inv) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    unsigned long long tacc = 0;
+    float nq[kChunk] = {}, nl[kChunk] = {};
+    int ci = warp * kBlockChunks + lane;
+    if (ci < d.mych) {
+        load_q(d, ci, RES, nq);
+        if (!ECACHED) load_l(d, ci, nl);
+    }
+    for (int base = warp * kBlockChunks; base < d.mych; base += kThreads) {
+        ci = base + lane;
+        float q[kChunk], l[kChunk];
+#pragma unroll
+        for (int e = 0; e < kChunk; ++e) {
+            q[e] = nq[e];
+            l[e] = nl[e];
+        }
+        if (ci + kThreads < d.mych) {
+            load_q(d, ci + kThreads, RES, nq);
+            if (!ECACHED) load_l(d, ci + kThreads, nl);
+        }
+        const unsigned long long W =
+            ci < d.mych ? precise_chunk<DT, RES, ECACHED, WSTORE>(d, ci, l, q, inv, 0ull, nullptr)
+                        : 0ull;
+        const unsigned long long bw = warp_sum(W);
+        if (lane == 0) {
+            d.bsum[base / kBlockChunks] = bw;
+            tacc += bw;
+        }
+    }
+    return tacc;
+}
+
+// The same value (and token search) from stored weights.
+__device__ __forceinline__ unsigned long long stored_chunk(const ff* w, unsigned long long want,
+                                                           int* token) {
+    ff acc{0.0f, 0.0f};
+#pragma unroll
+    for (int e = 0; e < kChunk; ++e) {
+        const ff we = w[e];
+        ff_accumulate(acc, we);
+        if (token && *token < 0 && we.hi > 0.0f && to_fixed(ff_normalize(acc)) > want) *token = e;
+    }
+    return to_fixed(ff_normalize(acc));
+}
+
+// Precise pass A over the CTA's slice: this thread's float-float share of
+// S = sum_j exp((l_j - m)/T), the exponentials kept in the cache when ECACHE.
+template <typename DT, bool ECACHE>
+__device__ __forceinline__ ff precise_pass_a(const DrawCtx<DT>& d) {
     const int tid = threadIdx.x;
-    const bool al_l = (reinterpret_cast<uintptr_t>(rowp) & 15) == 0;
-    const bool al_q = residual && (reinterpret_cast<uintptr_t>(qrow) & 15) == 0;
-    const long long nch = (V + kChunk - 1) / kChunk;
-    const long long c0 = nch * rank / G, c1 = nch * (rank + 1) / G;
-    const int mych = (int)(c1 - c0);
+    ff acc{0.0f, 0.0f};
+    float nf[kChunk] = {};
+    if (tid < d.mych) load_l(d, tid, nf);
+    for (int ci = tid; ci < d.mych; ci += kThreads) {
+        float f[kChunk];
+#pragma unroll
+        for (int e = 0; e < kChunk; ++e) f[e] = nf[e];
+        if (ci + kThreads < d.mych) load_l(d, ci + kThreads, nf);
+#pragma unroll
+        for (int e = 0; e < kChunk; ++e) {
+            const ff ev = exp_rel(f[e], d.m, d.c2, d.thi, d.tlo);
+            if (ECACHE) d.ecache[(size_t)ci * kChunk + e] = ev;
+            ff_accumulate(acc, ev);
+        }
+    }
+    return acc;
+}
+
+// The precise draw on one row by the G CTAs of a cluster.  The owner CTA holds
+// the token in sh.token; `degenerate` is set in all threads.
+template <typename DT>
+__device__ void draw_precise(cg::cluster_group& cluster, DrawShared& sh, const DrawCtx<DT>& d,
+                             bool& degenerate) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int i = tid; i < kExpTable; i += kThreads) {
+        d.thi[i] = g_exp2_table.hi[i];
+        d.tlo[i] = g_exp2_table.lo[i];
+    }
+    __syncthreads();
 
     // Pass A: e_j = exp((l_j - m)/T) and the normaliser S = sum_j e_j.
-    ff acc{0.0f, 0.0f};
-    for (int ci = tid; ci < mych; ci += kThreads) {
-        float f[kChunk];
-        load_chunk<DT>(rowp, (c0 + ci) * kChunk, V, al_l, f);
-#pragma unroll
-        for (int e = 0; e < kChunk; ++e) ff_accumulate(acc, exp_rel(f[e], m, c, sh.thi, sh.tlo));
-    }
-    const ff inv = ff_recip(cluster_sum_ff(cluster, sh, acc, G));
+    const ff acc = d.ecache ? precise_pass_a<DT, true>(d) : precise_pass_a<DT, false>(d);
+    const ff inv = ff_recip(cluster_sum_ff(cluster, sh, sh.xS[1], acc, d.rank, d.G));
 
-    // Pass B: chunk weights, CTA total, cluster prefix; a second round draws
+    // Pass B: chunk values, block totals, cluster prefix; a second round draws
     // from p when the residual has no mass.
-    bool use_res = residual;
+    bool use_res = d.residual;
     degenerate = false;
     unsigned long long prefix = 0, total = 0, mytot = 0;
     for (int round = 0; round < 2; ++round) {
-        unsigned long long tacc = 0;
-        for (int ci = tid; ci < mych; ci += kThreads) {
-            unsigned long long cs = chunk_weight<DT>(rowp, qrow, (c0 + ci) * kChunk, V, al_l,
-                                                     al_q, use_res, m, c, inv, sh, 0ull, nullptr);
-            csum[ci] = cs;
-            tacc += cs;
-        }
-        cluster_prefix(cluster, sh, tacc, 0.0f, 1 + round, rank, G);
+        // The first round reads the cached exponentials and leaves the weights
+        // in their place; a second round recomputes the exponentials.
+        unsigned long long tacc;
+        if (round == 0 && d.ecache)
+            tacc = use_res ? precise_pass_b<DT, true, true, true>(d, inv)
+                           : precise_pass_b<DT, false, true, true>(d, inv);
+        else if (d.ecache)
+            tacc = precise_pass_b<DT, false, false, true>(d, inv);  // round 1: from p
+        else
+            tacc = use_res ? precise_pass_b<DT, true, false, false>(d, inv)
+                           : precise_pass_b<DT, false, false, false>(d, inv);
+        cluster_prefix(cluster, sh, sh.xW[1 + round], nullptr, tacc, 0.0f, d.rank, d.G);
         prefix = sh.prefix;
         total = sh.total;
-        mytot = sh.slot_W[1 + round];
+        mytot = sh.mytot;
         if (total > 0 || !use_res) break;
         use_res = false;  // zero residual mass: draw from p (counted)
         degenerate = true;
     }
 
-    const unsigned long long tau = scale_floor(u, total);
+    const unsigned long long tau = scale_floor(d.u, total);
     const bool owner = mytot > 0 && prefix <= tau && tau - prefix < mytot;
-    if (owner) {
+    if (owner) {  // uniform across the CTA
         const unsigned long long want = tau - prefix;
-        int cstar;
-        unsigned long long before;
-        if (find_chunk(sh, csum, mych, want, &cstar, &before)) {
-            int tok = -1;
-            chunk_weight<DT>(rowp, qrow, (c0 + cstar) * kChunk, V, al_l, al_q, use_res, m, c,
-                             inv, sh, want - before, &tok);
-            sh.token = tok;
+        int blk;
+        unsigned long long bbefore;
+        find_block(sh, d.bsum, d.nblk, want, &blk, &bbefore);
+        if (warp == 0) {
+            const int ci = blk * kBlockChunks + lane;
+            float l[kChunk] = {}, q[kChunk] = {};
+            const ff* wc = d.ecache ? d.ecache + (size_t)ci * kChunk : nullptr;
+            unsigned long long W = 0;
+            if (ci < d.mych) {
+                if (wc) {
+                    W = stored_chunk(wc, 0ull, nullptr);
+                } else {
+                    load_l(d, ci, l);
+                    load_q(d, ci, use_res, q);
+                    W = use_res ? precise_chunk<DT, true, false, false>(d, ci, l, q, inv, 0ull, nullptr)
+                                : precise_chunk<DT, false, false, false>(d, ci, l, q, inv, 0ull,
+                                                                          nullptr);
+                }
+            }
+            const unsigned long long wb = want - bbefore;
+            unsigned long long cb;
+            if (find_lane(W, wb, &cb)) {
+                int tok = -1;
+                if (wc)
+                    stored_chunk(wc, wb - cb, &tok);
+                else if (use_res)
+                    precise_chunk<DT, true, false, false>(d, ci, l, q, inv, wb - cb, &tok);
+                else
+                    precise_chunk<DT, false, false, false>(d, ci, l, q, inv, wb - cb, &tok);
+                if (tok >= 0) sh.token = (int)((d.c0 + ci) * kChunk + tok);
+            }
         }
     }
+}
+
+// Dynamic shared memory of a draw: block totals, the 2^(i/1024) table, and a
+// cache of the CTA's slice (level 1: fp32 exponents for the fast pass; level 2:
+// also room for the float-float exponentials of the precise pass).
+// log2 of a cluster size (a power of two, at most 16): slices are cut with
+// shifts, not 64-bit divisions.
+__host__ __device__ inline int log2_pow2(int G) {
+    int lg = 0;
+    while ((1 << lg) < G && lg < 4) ++lg;
+    return lg;
+}
+__host__ __device__ inline long long draw_slice_chunks(int V, int G) {
+    const long long nch = ((long long)V + kChunk - 1) / kChunk;
+    return (nch + G - 1) >> log2_pow2(G);
+}
+__host__ __device__ inline size_t draw_bsum_bytes(int V, int G) {
+    const long long nblk = (draw_slice_chunks(V, G) + kBlockChunks - 1) / kBlockChunks;
+    return ((size_t)nblk * 8 + 15) & ~(size_t)15;
+}
+__host__ __device__ inline size_t draw_smem_bytes(int V, int G, int level) {
+    const size_t slice = (size_t)draw_slice_chunks(V, G) * kChunk;
+    return draw_bsum_bytes(V, G) + 2 * kExpTable * sizeof(float) +
+           (level >= 2 ? slice * sizeof(ff) : level == 1 ? slice * sizeof(float) : 0);
+}
+
+template <typename DT>
+__device__ __forceinline__ DrawCtx<DT> make_draw_ctx(unsigned char* dyn, int level, bool prefetch,
+                                                    const DT* rowp, const float* qrow,
+                                                    bool residual, int V, float m, float c,
+                                                    ff c2, float u, int rank, int G) {
+    DrawCtx<DT> d;
+    d.prefetch = prefetch;
+    d.rowp = rowp;
+    d.qrow = qrow;
+    d.V = V;
+    d.residual = residual;
+    d.m = m;
+    d.c = c;
+    d.c2 = c2;
+    d.u = u;
+    const long long nch = ((long long)V + kChunk - 1) / kChunk;
+    const int lg = log2_pow2(G);
+    d.c0 = (nch * rank) >> lg;
+    d.mych = (int)(((nch * (rank + 1)) >> lg) - d.c0);
+    d.nblk = (d.mych + kBlockChunks - 1) / kBlockChunks;
+    d.al_l = (reinterpret_cast<uintptr_t>(rowp) & 15) == 0;
+    d.al_q = residual && (reinterpret_cast<uintptr_t>(qrow) & 15) == 0;
+    d.rank = rank;
+    d.G = G;
+    const size_t bb = draw_bsum_bytes(V, G);
+    d.bsum = reinterpret_cast<unsigned long long*>(dyn);
+    d.thi = reinterpret_cast<float*>(dyn + bb);
+    d.tlo = d.thi + kExpTable;
+    unsigned char* cache = dyn + bb + 2 * kExpTable * sizeof(float);
+    d.acache = level >= 1 ? reinterpret_cast<float*>(cache) : nullptr;
+    d.ecache = level >= 2 ? reinterpret_cast<ff*>(cache) : nullptr;
+    return d;
 }
 
 // The draw: the certified fast pass, and the precise pass when the fast one
 // cannot certify its bin (or when `force_precise`).  Every CTA calls it; the
 // owner CTA's thread 0 writes the token to *token_out.  Sets `degenerate` and
-// `fallback` in all threads.
+// `fallback` in all threads.  The CTA's slices of the decision row and of the
+// q row are first prefetched into L2 in bulk when the launch's draws fit in L2
+// together (d.prefetch).  With `defer_precise` a draw that
+// needs the precise pass returns true at once (in every thread) and writes no
+// token: the caller hands it to the precise kernel.
 template <typename DT>
-__device__ void draw(cg::cluster_group& cluster, DrawShared& sh, unsigned long long* csum,
-                     const DT* __restrict__ rowp, const float* __restrict__ qrow, bool residual,
-                     int V, float m, float c, ff c2, float u, int rank, int G, bool force_precise,
-                     int32_t* token_out, bool& degenerate, bool& fallback) {
+__device__ bool draw(cg::cluster_group& cluster, DrawShared& sh, const DrawCtx<DT>& d,
+                     bool force_precise, bool defer_precise, int32_t* token_out,
+                     bool& degenerate, bool& fallback) {
+    if (d.prefetch && threadIdx.x == 0) {
+        prefetch_slice_l2(d.rowp, d.c0, d.mych, d.V);
+        if (d.residual) prefetch_slice_l2(d.qrow, d.c0, d.mych, d.V);
+    }
     degenerate = false;
     fallback = true;
-    if (!force_precise && draw_fast<DT>(cluster, sh, csum, rowp, qrow, residual, V, m, c, u, rank,
-                                        G)) {
+    const bool certified =
+        !force_precise && (d.residual ? draw_fast<DT, true>(cluster, sh, d)
+                                      : draw_fast<DT, false>(cluster, sh, d));
+    if (certified) {
         fallback = false;
         if (threadIdx.x == 0 && sh.token >= 0) *token_out = sh.token;
-        return;
+        return false;
     }
+    if (defer_precise) return true;
     if (threadIdx.x == 0) sh.token = -1;
     __syncthreads();
-    draw_precise<DT>(cluster, sh, csum, rowp, qrow, residual, V, m, c2, u, rank, G, degenerate);
+    draw_precise<DT>(cluster, sh, d, degenerate);
     __syncthreads();
     if (threadIdx.x == 0 && sh.token >= 0) *token_out = sh.token;
+    return false;
 }
 
 // ------------------------------------------------------------------ the fused kernel
@@ -751,11 +1210,18 @@ struct VerifyArgs {
     uint32_t* seqstat;
     int32_t* out;
     int32_t* nacc;
+    uint32_t* plist_count;  // with plist: draws needing the precise pass are
+    uint32_t* plist;        // appended here for sv_precise_kernel (else run here)
     int B, k, V, G, W;
+    int draw_level;     // shared-memory cache level of the draw
+    int prefetch;       // the draws bulk-prefetch their slices into L2
     int force_precise;  // test hook: skip the fast draw
     float c;     // log2(e)/T (float, for the row statistics and the fast draw)
     ff c2;       // log2(e)/T in float-float (p(x) and the precise draw)
 };
+
+// Outcome of one row's test: accept, reject, the bonus row, or an error bit.
+constexpr uint32_t kCodeAccept = 0u, kCodeReject = 1u, kCodeBonus = 2u, kCodeError = 0x100u;
 
 struct FusedShared {
     Partial wpart[kWarps];
@@ -765,11 +1231,13 @@ struct FusedShared {
     int xs[kMaxK];
     uint32_t gfl[kMaxK];
     float px[kWarps];
+    uint32_t code[kWarps];
+    float ur;
     int n, bits;
 };
 
 template <typename DT, bool SAMPLED>
-__global__ void __launch_bounds__(kThreads) sv_verify_kernel(VerifyArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(VerifyArgs a) {
     using E = Elt<DT>;
     extern __shared__ __align__(16) unsigned char dyn[];
     __shared__ FusedShared fs;
@@ -810,10 +1278,10 @@ __global__ void __launch_bounds__(kThreads) sv_verify_kernel(VerifyArgs a) {
         fs.gfl[i] = fl;
         fs.ua[i] = SAMPLED ? a.ua[(long long)b * k + i] : 0.0f;
     }
-    if (SAMPLED) load_exp_table(ds);
     if (tid == 0) {
         fs.n = -1;
         fs.bits = 0;
+        if (SAMPLED) fs.ur = a.ur[b];
     }
     __syncthreads();
 
@@ -831,7 +1299,8 @@ __global__ void __launch_bounds__(kThreads) sv_verify_kernel(VerifyArgs a) {
         int head;
         long long nvec, tail0;
         row_layout<DT>(rowp, V, head, nvec, tail0);
-        const long long vb = nvec * rank / G, ve = nvec * (rank + 1) / G;
+        const int lgG = log2_pow2(G);
+    const long long vb = (nvec * rank) >> lgG, ve = (nvec * (rank + 1)) >> lgG;
         Partial p = stream_slice<DT, SAMPLED, 4>(rowp, V, vb, ve, head, tail0, rank == 0,
                                                  rank == G - 1, tg, ng, c);
         p = warp_merge<SAMPLED>(p, c);
@@ -855,28 +1324,43 @@ __global__ void __launch_bounds__(kThreads) sv_verify_kernel(VerifyArgs a) {
             if (tid < Wc) fs.rowstat[tid] = fs.part[buf][tid];
         }
         __syncthreads();
-        if (tid == 0) {  // the scan over this wave's rows
-            int n = -1, bits = 0;
-            for (int ww = 0; ww < Wc; ++ww) {
-                const int i = i0 + ww;
-                const Partial& r = fs.rowstat[ww];
-                if (row_flags<SAMPLED>(r) & kRowBad) { bits = SV_DEV_BAD_ROW; break; }
-                if (i == k) { n = k; break; }
-                if (fs.gfl[i] & kRowTokenBad) { bits = SV_DEV_BAD_TOKEN; break; }
-                bool accept;
-                if (SAMPLED) {
-                    const float u = fs.ua[i];
-                    if (!(u >= 0.0f && u < 1.0f)) { bits = SV_DEV_BAD_UNIFORM; break; }
-                    if (fs.gfl[i] & kRowQBad) { bits = SV_DEV_BAD_Q; break; }
-                    ff ex = exp_rel(fs.lx[i], r.m, a.c2, ds.thi, ds.tlo);
+        if (tid < Wc) {  // each row's test, in parallel (kCode* values)
+            const int i = i0 + tid;
+            const Partial& r = fs.rowstat[tid];
+            uint32_t c;
+            if (row_flags<SAMPLED>(r) & kRowBad) {
+                c = kCodeError | SV_DEV_BAD_ROW;
+            } else if (i == k) {
+                c = kCodeBonus;
+            } else if (fs.gfl[i] & kRowTokenBad) {
+                c = kCodeError | SV_DEV_BAD_TOKEN;
+            } else if (SAMPLED) {
+                const float u = fs.ua[i];
+                if (!(u >= 0.0f && u < 1.0f)) {
+                    c = kCodeError | SV_DEV_BAD_UNIFORM;
+                } else if (fs.gfl[i] & kRowQBad) {
+                    c = kCodeError | SV_DEV_BAD_Q;
+                } else {
+                    ff ex = exp_rel(fs.lx[i], r.m, a.c2, g_exp2_table.hi, g_exp2_table.lo);
                     const float P = __fdiv_rn(ex.hi, r.s);
                     const float Q = fs.qx[i];
-                    fs.px[ww] = P;
-                    accept = (P >= Q) || (u < __fdiv_rn(P, Q));
-                } else {
-                    accept = fs.xs[i] == r.idx;
+                    fs.px[tid] = P;
+                    c = ((P >= Q) || (u < __fdiv_rn(P, Q))) ? kCodeAccept : kCodeReject;
                 }
-                if (!accept) { n = i; break; }
+            } else {
+                c = fs.xs[i] == r.idx ? kCodeAccept : kCodeReject;
+            }
+            fs.code[tid] = c;
+        }
+        __syncthreads();
+        if (tid == 0) {  // the scan over this wave's rows: the first row that stops it
+            int n = -1, bits = 0;
+            for (int ww = 0; ww < Wc; ++ww) {
+                const uint32_t c = fs.code[ww];
+                if (c == kCodeAccept) continue;
+                if (c & kCodeError) bits = (int)(c & ~kCodeError);
+                else n = c == kCodeBonus ? k : i0 + ww;
+                break;
             }
             fs.n = n;
             fs.bits = bits;
@@ -940,7 +1424,7 @@ __global__ void __launch_bounds__(kThreads) sv_verify_kernel(VerifyArgs a) {
     }
 
     // ---- the draw on row n, then the outputs
-    const float u = a.ur[b];
+    const float u = fs.ur;
     if (!(u >= 0.0f && u < 1.0f)) {  // every CTA sees the same uniform
         if (rank == 0) {
             for (int i = tid; i <= k; i += kThreads) o[i] = -1;
@@ -956,17 +1440,25 @@ __global__ void __launch_bounds__(kThreads) sv_verify_kernel(VerifyArgs a) {
     const float* qrow = n < k ? a.q + ((long long)b * k + n) * V : nullptr;
     const float m = fs.rowstat[n - wave_row0].m;
     bool degenerate = false, fallback = false;
-    draw<DT>(cluster, ds, reinterpret_cast<unsigned long long*>(dyn), drow, qrow, n < k, V, m, a.c,
-             a.c2, u, rank, G, a.force_precise != 0, o + n, degenerate, fallback);
+    const DrawCtx<DT> dc =
+        make_draw_ctx<DT>(dyn, a.draw_level, a.prefetch != 0, drow, qrow, n < k, V, m, a.c, a.c2,
+                          u, rank, G);
+    const bool deferred = draw<DT>(cluster, ds, dc, a.force_precise != 0, a.plist != nullptr,
+                                   o + n, degenerate, fallback);
     if (rank == 0) {
         for (int i = tid; i <= k; i += kThreads)
             if (i != n) o[i] = i < n ? fs.xs[i] : -1;
         if (tid == 0) {
             a.nacc[b] = n;
             a.seqstat[b] = (degenerate ? SV_DEV_DEGENERATE : 0u) | (fallback ? SV_DEV_PRECISE : 0u);
+            if (deferred) {
+                const uint32_t j = atomicAdd(a.plist_count, 1u);
+                if (j < (uint32_t)a.B) a.plist[j] = (uint32_t)b;  // at most B entries
+            }
         }
     }
-    cluster.sync();  // no CTA leaves while another may still read its slots
+    // No final cluster barrier: the draw's exchanges are pushed before its last
+    // barrier, and the row partials were read before its first.
 }
 
 // ------------------------------------------------------------------ two-stage kernels
@@ -975,43 +1467,90 @@ struct RowsArgs {
     const void* logits;
     const float* q;
     const int32_t* x;
+    const float* ua;   // u_accept (sampled, with `skip`)
     Header* hdr;
     RowRec* rows;
+    uint32_t* stop;    // [B] lowest row known to end its sequence's scan (with `skip`)
     int B, k, V, G, mode;
+    int skip;          // rows in position-major order; rows past a known stop are skipped
     float c;        // log2(e) / T
     ff c2;          // log2(e) / T in float-float (p(x))
 };
 
 // One CTA (or a cluster of G CTAs splitting the vocabulary) per row.
+//
+// With `skip` (only for G == 1) the grid enumerates rows position-major (row 0
+// of every sequence, then row 1, ...), each CTA decides its own row's test
+// (every test depends on its row alone) and lowers stop[b] to its row index
+// when the scan would end there; a CTA whose row lies past stop[b] when it
+// starts reads nothing and marks the row skipped.  The scan ends at its first
+// stopping row n, and no row at or before n can be skipped (that would need a
+// stopping row below n), so the finish kernel reads only rows this kernel
+// computed.  stop[] must hold 0xFFFFFFFF when the grid starts.
 template <typename DT, bool SAMPLED, int NT>
 __global__ void __launch_bounds__(NT) sv_rows_kernel(RowsArgs a) {
     using E = Elt<DT>;
     constexpr int NW = NT / 32;
     __shared__ Partial wpart[NW];
     __shared__ Partial cta_part;  // read by cluster rank 0 through DSMEM
-    __shared__ float thi[SAMPLED ? kExpTable : 1], tlo[SAMPLED ? kExpTable : 1];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int G = a.G;
-    const long long row = blockIdx.x / G;
+    const long long r0 = blockIdx.x / G;
     const int rank = blockIdx.x % G;
-    const int V = a.V;
+    const int V = a.V, k = a.k;
+    const int b = a.skip ? (int)(r0 % a.B) : (int)(r0 / (k + 1));
+    const int i = a.skip ? (int)(r0 / a.B) : (int)(r0 % (k + 1));
+    const long long row = (long long)b * (k + 1) + i;
     const DT* rowp = static_cast<const DT*>(a.logits) + row * (long long)V;
-    const int b = (int)(row / (a.k + 1));
-    const int i = (int)(row % (a.k + 1));
     // The finish kernel is launched as a programmatic dependent: let it start
     // its launch now; it waits (griddepcontrol.wait) for this grid's results.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (blockIdx.x == 0 && tid == 0) {
         a.hdr->magic = kMagic;
         a.hdr->B = a.B;
-        a.hdr->k = a.k;
+        a.hdr->k = k;
         a.hdr->V = V;
         a.hdr->mode = a.mode;
+    }
+    if (a.skip && i > 0) {
+        // One thread reads the stop row and the CTA follows its decision (the
+        // value may change under concurrent CTAs, so each thread reading it
+        // could decide differently).  G == 1: no other CTA shares the row.
+        __shared__ int s_skip;
+        if (tid == 0)
+            s_skip = *reinterpret_cast<volatile const uint32_t*>(a.stop + b) < (uint32_t)i;
+        __syncthreads();
+        if (s_skip) {
+            if (tid == 0) {
+                RowRec rec;
+                rec.mraw = NAN;
+                rec.S = NAN;
+                rec.px = NAN;
+                rec.lx = NAN;
+                rec.qx = NAN;
+                rec.argmax = -1;
+                rec.flags = kRowSkipped;
+                a.rows[row] = rec;
+            }
+            return;
+        }
+    }
+    // The gathers of this row, issued now and used after the stream.
+    int xi = -1;
+    float lx = NAN, qx = NAN, ua = 0.0f;
+    if (rank == 0 && tid == 0 && i < k) {
+        xi = a.x[(long long)b * k + i];
+        if (xi >= 0 && xi < V) {
+            lx = E::load1(rowp + xi);
+            if (SAMPLED) qx = a.q[((long long)b * k + i) * V + xi];
+        }
+        if (SAMPLED && a.skip) ua = a.ua[(long long)b * k + i];
     }
     int head;
     long long nvec, tail0;
     row_layout<DT>(rowp, V, head, nvec, tail0);
-    const long long vb = nvec * rank / G, ve = nvec * (rank + 1) / G;
+    const int lgG = log2_pow2(G);
+    const long long vb = (nvec * rank) >> lgG, ve = (nvec * (rank + 1)) >> lgG;
     Partial p = stream_slice<DT, SAMPLED, 4>(rowp, V, vb, ve, head, tail0, rank == 0,
                                              rank == G - 1, tid, NT, a.c);
     p = warp_merge<SAMPLED>(p, a.c);
@@ -1032,15 +1571,7 @@ __global__ void __launch_bounds__(NT) sv_rows_kernel(RowsArgs a) {
         }
         cluster.sync();
     }
-    if (rank != 0) return;
-    if (SAMPLED && i < a.k) {
-        for (int t = tid; t < kExpTable; t += NT) {
-            thi[t] = g_exp2_table.hi[t];
-            tlo[t] = g_exp2_table.lo[t];
-        }
-        __syncthreads();
-    }
-    if (tid != 0) return;
+    if (rank != 0 || tid != 0) return;
     RowRec rec;
     rec.mraw = p.m;
     rec.S = SAMPLED ? p.s : 0.0f;
@@ -1049,19 +1580,30 @@ __global__ void __launch_bounds__(NT) sv_rows_kernel(RowsArgs a) {
     rec.lx = NAN;
     rec.qx = NAN;
     uint32_t fl = row_flags<SAMPLED>(p);
-    if (i < a.k) {
-        const int xi = a.x[(long long)b * a.k + i];
+    bool ends = false;  // the scan stops at this row (sequences with `skip`)
+    if (i < k) {
         if (xi < 0 || xi >= V) {
             fl |= kRowTokenBad;
         } else {
-            rec.lx = E::load1(rowp + xi);
+            rec.lx = lx;
             if (SAMPLED) {
-                rec.qx = a.q[((long long)b * a.k + i) * V + xi];
-                if (!(rec.qx >= 0.0f)) fl |= kRowQBad;
+                rec.qx = qx;
+                if (!(qx >= 0.0f)) fl |= kRowQBad;
                 if (!(fl & kRowBad)) {
-                    ff ex = exp_rel(rec.lx, p.m, a.c2, thi, tlo);
+                    ff ex = exp_rel(lx, p.m, a.c2, g_exp2_table.hi, g_exp2_table.lo);
                     rec.px = (double)__fdiv_rn(ex.hi, p.s);
                 }
+            }
+        }
+        if (a.skip) {
+            // The same tests, in the same arithmetic, as the finish kernels' scans.
+            if (fl & (kRowBad | kRowTokenBad | kRowQBad)) {
+                ends = true;
+            } else if (SAMPLED) {
+                const float P = (float)rec.px, Q = rec.qx;
+                ends = !(ua >= 0.0f && ua < 1.0f) || !((P >= Q) || (ua < __fdiv_rn(P, Q)));
+            } else {
+                ends = xi != rec.argmax;
             }
         }
     } else {
@@ -1069,6 +1611,7 @@ __global__ void __launch_bounds__(NT) sv_rows_kernel(RowsArgs a) {
     }
     rec.flags = fl;
     a.rows[row] = rec;
+    if (ends) atomicMin(a.stop + b, (uint32_t)i);
 }
 
 // One warp per sequence: the lanes load the records in parallel, lane 0 scans.
@@ -1092,11 +1635,11 @@ __global__ void sv_finish_greedy_kernel(const int32_t* __restrict__ x,
     uint32_t bits = 0;
     int n = k;
     for (int i = 0; i < k; ++i) {
-        if (rr[i].flags & kRowBad) { bits = SV_DEV_BAD_ROW; break; }
+        if (rr[i].flags & (kRowBad | kRowSkipped)) { bits = SV_DEV_BAD_ROW; break; }
         if (rr[i].flags & kRowTokenBad) { bits = SV_DEV_BAD_TOKEN; break; }
         if (xx[i] != rr[i].argmax) { n = i; break; }
     }
-    if (!bits && (rr[n].flags & kRowBad)) bits = SV_DEV_BAD_ROW;
+    if (!bits && (rr[n].flags & (kRowBad | kRowSkipped))) bits = SV_DEV_BAD_ROW;
     seqstat[b] = bits;
     if (bits) {
         for (int i = 0; i <= k; ++i) o[i] = -1;
@@ -1119,18 +1662,24 @@ struct FinishArgs {
     uint32_t* seqstat;
     int32_t* out;
     int32_t* nacc;
+    uint32_t* plist_count;  // with plist: draws needing the precise pass are
+    uint32_t* plist;        // appended here for sv_precise_kernel (else run here)
     int B, k, V, G;
+    int draw_level;
+    int prefetch;  // the draws bulk-prefetch their slices into L2
     int force_precise;
     float c;
     ff c2;
 };
 
 template <typename DT>
-__global__ void __launch_bounds__(kThreads) sv_finish_sample_kernel(FinishArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) sv_finish_sample_kernel(FinishArgs a) {
     extern __shared__ __align__(16) unsigned char dyn[];
     __shared__ DrawShared ds;
     __shared__ RowRec recs[kMaxK + 1];
     __shared__ float uas[kMaxK];
+    __shared__ uint32_t codes[kMaxK];
+    __shared__ float s_ur;
     __shared__ int s_n, s_bits;
     cg::cluster_group cluster = cg::this_cluster();
     const int tid = threadIdx.x;
@@ -1138,28 +1687,41 @@ __global__ void __launch_bounds__(kThreads) sv_finish_sample_kernel(FinishArgs a
     const int b = blockIdx.x / G;
     const int rank = blockIdx.x % G;
     const int k = a.k, V = a.V;
-    load_exp_table(ds);
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the row records are complete
     for (int i = tid; i <= k; i += kThreads) recs[i] = a.rows[(long long)b * (k + 1) + i];
     for (int i = tid; i < k; i += kThreads) uas[i] = a.ua[(long long)b * k + i];
+    if (tid == kThreads - 1) s_ur = a.ur[b];
     __syncthreads();
-    if (tid == 0) {
+    for (int i = tid; i < k; i += kThreads) {  // each row's test, in parallel
+        const RowRec& r = recs[i];
+        const float u = uas[i];
+        uint32_t c;
+        if (r.flags & (kRowBad | kRowSkipped)) {  // a skipped row is never reached
+            c = kCodeError | SV_DEV_BAD_ROW;
+        } else if (r.flags & kRowTokenBad) {
+            c = kCodeError | SV_DEV_BAD_TOKEN;
+        } else if (!(u >= 0.0f && u < 1.0f)) {
+            c = kCodeError | SV_DEV_BAD_UNIFORM;
+        } else if (r.flags & kRowQBad) {
+            c = kCodeError | SV_DEV_BAD_Q;
+        } else {
+            const float P = (float)r.px, Q = r.qx;
+            c = ((P >= Q) || (u < __fdiv_rn(P, Q))) ? kCodeAccept : kCodeReject;
+        }
+        codes[i] = c;
+    }
+    __syncthreads();
+    if (tid == 0) {  // the first row that stops the scan
         int bits = 0, n = k;
         for (int i = 0; i < k; ++i) {
-            const RowRec& r = recs[i];
-            if (r.flags & kRowBad) { bits = SV_DEV_BAD_ROW; break; }
-            if (r.flags & kRowTokenBad) { bits = SV_DEV_BAD_TOKEN; break; }
-            const float u = uas[i];
-            if (!(u >= 0.0f && u < 1.0f)) { bits = SV_DEV_BAD_UNIFORM; break; }
-            if (r.flags & kRowQBad) { bits = SV_DEV_BAD_Q; break; }
-            const float P = (float)r.px, Q = r.qx;
-            if (!((P >= Q) || (u < __fdiv_rn(P, Q)))) { n = i; break; }
+            const uint32_t c = codes[i];
+            if (c == kCodeAccept) continue;
+            if (c & kCodeError) bits = (int)(c & ~kCodeError);
+            else n = i;
+            break;
         }
-        if (!bits && (recs[n].flags & kRowBad)) bits = SV_DEV_BAD_ROW;
-        if (!bits) {
-            const float u = a.ur[b];
-            if (!(u >= 0.0f && u < 1.0f)) bits = SV_DEV_BAD_UNIFORM;
-        }
+        if (!bits && (recs[n].flags & (kRowBad | kRowSkipped))) bits = SV_DEV_BAD_ROW;
+        if (!bits && !(s_ur >= 0.0f && s_ur < 1.0f)) bits = SV_DEV_BAD_UNIFORM;
         s_n = n;
         s_bits = bits;
     }
@@ -1179,18 +1741,73 @@ __global__ void __launch_bounds__(kThreads) sv_finish_sample_kernel(FinishArgs a
     const DT* drow = static_cast<const DT*>(a.logits) + ((long long)b * (k + 1) + n) * V;
     const float* qrow = n < k ? a.q + ((long long)b * k + n) * V : nullptr;
     bool degenerate = false, fallback = false;
-    draw<DT>(cluster, ds, reinterpret_cast<unsigned long long*>(dyn), drow, qrow, n < k, V,
-             recs[n].mraw, a.c, a.c2, a.ur[b], rank, G, a.force_precise != 0, o + n, degenerate,
-             fallback);
+    const DrawCtx<DT> dc = make_draw_ctx<DT>(dyn, a.draw_level, a.prefetch != 0, drow, qrow, n < k,
+                                             V, recs[n].mraw, a.c, a.c2, s_ur, rank, G);
+    const bool deferred = draw<DT>(cluster, ds, dc, a.force_precise != 0, a.plist != nullptr,
+                                   o + n, degenerate, fallback);
     if (rank == 0) {
         for (int i = tid; i <= k; i += kThreads)
             if (i != n) o[i] = i < n ? a.x[(long long)b * k + i] : -1;
         if (tid == 0) {
             a.nacc[b] = n;
             a.seqstat[b] = (degenerate ? SV_DEV_DEGENERATE : 0u) | (fallback ? SV_DEV_PRECISE : 0u);
+            if (deferred) {
+                const uint32_t j = atomicAdd(a.plist_count, 1u);
+                if (j < (uint32_t)a.B) a.plist[j] = (uint32_t)b;  // at most B entries
+            }
         }
     }
-    cluster.sync();
+}
+
+// The precise draws of a large batch, left by sv_finish_sample_kernel in the
+// workspace list: persistent clusters of kMaxG CTAs, cluster c taking entries
+// c, c + clusters, ...  Each draw is the precise pass of the finish kernel over
+// a slice of V / kMaxG elements per CTA.
+struct PreciseArgs {
+    const void* logits;
+    const float* q;
+    const float* ur;
+    const RowRec* rows;
+    const int32_t* nacc;
+    const uint32_t* plist_count;
+    const uint32_t* plist;
+    uint32_t* seqstat;
+    int32_t* out;
+    int B, k, V;
+    int draw_level;
+    float c;
+    ff c2;
+};
+
+template <typename DT>
+__global__ void __launch_bounds__(kThreads, 2) sv_precise_kernel(PreciseArgs a) {
+    extern __shared__ __align__(16) unsigned char dyn[];
+    __shared__ DrawShared ds;
+    cg::cluster_group cluster = cg::this_cluster();
+    constexpr int G = kMaxG;
+    const int tid = threadIdx.x;
+    const int rank = blockIdx.x % G, cid = blockIdx.x / G, ncl = gridDim.x / G;
+    const int k = a.k, V = a.V;
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the list is complete
+    const uint32_t cnt = min(*a.plist_count, (uint32_t)a.B);
+    for (uint32_t j = cid; j < cnt; j += ncl) {
+        const int b = (int)a.plist[j];
+        const int n = a.nacc[b];
+        const DT* drow = static_cast<const DT*>(a.logits) + ((long long)b * (k + 1) + n) * V;
+        const float* qrow = n < k ? a.q + ((long long)b * k + n) * V : nullptr;
+        const float m = a.rows[(long long)b * (k + 1) + n].mraw;
+        const DrawCtx<DT> dc = make_draw_ctx<DT>(dyn, a.draw_level, false, drow, qrow, n < k, V,
+                                                 m, a.c, a.c2, a.ur[b], rank, G);
+        if (tid == 0) ds.token = -1;
+        __syncthreads();
+        bool degenerate = false;
+        draw_precise<DT>(cluster, ds, dc, degenerate);
+        __syncthreads();
+        if (tid == 0 && ds.token >= 0) a.out[(long long)b * (k + 1) + n] = ds.token;
+        if (rank == 0 && tid == 0 && degenerate)
+            a.seqstat[b] = SV_DEV_PRECISE | SV_DEV_DEGENERATE;
+        cluster.sync();  // the exchange slots serve the next draw
+    }
 }
 
 // ------------------------------------------------------------------ debug kernel
@@ -1253,13 +1870,32 @@ static std::atomic<int> g_force_precise{0};
 
 struct DeviceInfo {
     int sms = 0;
+    int clusters[5] = {0, 0, 0, 0, 0};  // resident clusters of 1, 2, 4, 8, 16 drawing CTAs
     bool ok = false;
     bool configured = false;
 };
 static std::mutex g_mu;
 static DeviceInfo g_dev[64];
 
-constexpr size_t kDynSmemMax = 160 * 1024;  // chunk sums: up to kSliceMax bytes
+constexpr size_t kDynSmemMax = 160 * 1024;  // attribute of the kernels that draw
+// Dynamic shared memory a draw may use for its slice cache: two 512-thread CTAs
+// of the drawing kernels still fit on one SM.
+constexpr size_t kDrawSmemBudget = 96 * 1024;
+
+// Whether the draws of a launch prefetch their slices (decision row and q row)
+// into L2 in bulk: only when all of them fit in a third of the L2 together, so
+// that no prefetched line is evicted before it is read.
+static int draw_prefetch(int B, int V, sv_dtype dt) {
+    const double bytes = (double)B * V * ((dt == SV_BF16 ? 2 : 4) + 4);
+    return bytes <= 40.0 * 1024 * 1024 ? 1 : 0;
+}
+
+// Cache level of a draw with G CTAs per row: the largest that fits the budget.
+static int draw_level(int V, int G) {
+    for (int lv = 2; lv >= 1; --lv)
+        if (draw_smem_bytes(V, G, lv) <= kDrawSmemBudget) return lv;
+    return 0;
+}
 
 template <typename K> static cudaError_t cluster_attrs(K kernel, bool dyn) {
     cudaError_t e =
@@ -1268,6 +1904,15 @@ template <typename K> static cudaError_t cluster_attrs(K kernel, bool dyn) {
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)kDynSmemMax);
     return e;
+}
+
+static cudaLaunchAttribute cluster_attr(int G) {
+    cudaLaunchAttribute at;
+    at.id = cudaLaunchAttributeClusterDimension;
+    at.val.clusterDim.x = G;
+    at.val.clusterDim.y = 1;
+    at.val.clusterDim.z = 1;
+    return at;
 }
 
 static sv_status device_setup(int* sms) {
@@ -1292,6 +1937,8 @@ static sv_status device_setup(int* sms) {
             SV_TRY(cluster_attrs(sv_verify_kernel<float, false>, false));
             SV_TRY(cluster_attrs(sv_finish_sample_kernel<__nv_bfloat16>, true));
             SV_TRY(cluster_attrs(sv_finish_sample_kernel<float>, true));
+            SV_TRY(cluster_attrs(sv_precise_kernel<__nv_bfloat16>, true));
+            SV_TRY(cluster_attrs(sv_precise_kernel<float>, true));
             SV_TRY(cluster_attrs(sv_rows_kernel<__nv_bfloat16, true, 128>, false));
             SV_TRY(cluster_attrs(sv_rows_kernel<__nv_bfloat16, true, 256>, false));
             SV_TRY(cluster_attrs(sv_rows_kernel<__nv_bfloat16, true, 512>, false));
@@ -1306,6 +1953,23 @@ static sv_status device_setup(int* sms) {
             SV_TRY(cluster_attrs(sv_rows_kernel<float, false, 512>, false));
 #undef SV_TRY
             if (e != cudaSuccess) return SV_ERR_CUDA;
+            // How many clusters of the drawing kernel fit at once, per cluster
+            // size, at the largest shared memory a draw uses.
+            for (int lg = 0; lg < 5; ++lg) {
+                cudaLaunchConfig_t cfg = {};
+                cfg.gridDim = dim3(1u << lg, 1, 1);
+                cfg.blockDim = dim3(kThreads, 1, 1);
+                cfg.dynamicSmemBytes = kDrawSmemBudget;
+                cudaLaunchAttribute at = cluster_attr(1 << lg);
+                cfg.attrs = &at;
+                cfg.numAttrs = 1;
+                int n = 0;
+                if (cudaOccupancyMaxActiveClusters(&n, sv_finish_sample_kernel<__nv_bfloat16>,
+                                                   &cfg) != cudaSuccess)
+                    n = 0;
+                d.clusters[lg] = n;
+            }
+            (void)cudaGetLastError();
         }
         d.configured = true;
     }
@@ -1344,25 +2008,31 @@ static sv_status check_sample(const float* q, const float* ua, const float* ur, 
     return SV_OK;
 }
 
-static cudaLaunchAttribute cluster_attr(int G) {
-    cudaLaunchAttribute at;
-    at.id = cudaLaunchAttributeClusterDimension;
-    at.val.clusterDim.x = G;
-    at.val.clusterDim.y = 1;
-    at.val.clusterDim.z = 1;
-    return at;
+// Resident clusters of G drawing CTAs on the current device (0 if unknown).
+static int resident_clusters(int G) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    int lg = 0;
+    while ((1 << lg) < G && lg < 4) ++lg;
+    std::lock_guard<std::mutex> lk(g_mu);
+    return g_dev[dev].clusters[lg];
 }
 
-// Cluster size of the per-sequence kernels.  Sampled: about four CTAs per SM
-// over the whole batch (a 512-thread CTA of these kernels needs little shared
-// memory, so four fit on an SM), but no CTA draws from more than kSliceMax
-// elements of a row and none from fewer than 2048.  Greedy: enough CTAs to give
-// each SM four, with at least 4 KiB of every row per CTA.
+// Cluster size of the per-sequence kernels.  Sampled: the whole batch resident
+// at once (B clusters of G CTAs, as the occupancy query counts them, else two
+// 512-thread CTAs per SM), but no CTA draws from more than kSliceMax elements
+// of a row and none from fewer than 2048.
+// Greedy: enough CTAs to give each SM four, with at least 4 KiB of every row
+// per CTA.
 static int seq_split(bool sampled, int B, int V, int esz, int sms) {
     int G = 1;
     if (sampled) {
         while (G < 16 && (V + G - 1) / G > kSliceMax) G *= 2;
-        while (G < 16 && (long long)B * G * 2 <= 4LL * sms && V / (2 * G) >= 2048) G *= 2;
+        while (G < 16 && V / (2 * G) >= 2048) {
+            const int rc = resident_clusters(2 * G);
+            if (rc > 0 ? B > rc : (long long)B * 2 * G > 2LL * sms) break;
+            G *= 2;
+        }
     } else {
         while (G < 16 && (long long)B * G < 4LL * sms && (long long)V * esz / (2LL * G) >= 4096)
             G *= 2;
@@ -1380,6 +2050,59 @@ static int wave_rows(int B, int k, int V, int esz) {
     if (W < 1) W = 1;
     if (W > k + 1) W = k + 1;
     return W > kWarps ? kWarps : W;
+}
+
+// The precise draws listed by a draw kernel of a large batch (plist_count and
+// plist in the workspace): persistent 16-CTA clusters, launched as a
+// programmatic dependent of that kernel.
+// Tuning hooks of the fused kernel (spec_verify_debug_fused_tuning): whether
+// it defers the precise draws (0 automatic: when B >= SMs; 1 always; 2 never)
+// and a minimum of dynamic shared memory per CTA in KiB (0: none), which
+// limits how many of its CTAs share an SM.
+static std::atomic<int> g_fused_defer{0};
+static std::atomic<int> g_fused_pad{0};
+
+static sv_status launch_precise(const void* logits, sv_dtype dt, const float* q, const float* ur,
+                                const RowRec* rows, const int32_t* nacc,
+                                const uint32_t* plist_count, const uint32_t* plist,
+                                uint32_t* seqstat, int32_t* out, int B, int k, int V, float c,
+                                ff c2, cudaStream_t stream) {
+    cudaError_t e;
+    cudaLaunchAttribute pdl;
+    pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl.val.programmaticStreamSerializationAllowed = 1;
+    PreciseArgs pa;
+    pa.logits = logits;
+    pa.q = q;
+    pa.ur = ur;
+    pa.rows = rows;
+    pa.nacc = nacc;
+    pa.plist_count = plist_count;
+    pa.plist = plist;
+    pa.seqstat = seqstat;
+    pa.out = out;
+    pa.B = B;
+    pa.k = k;
+    pa.V = V;
+    pa.draw_level = draw_level(V, kMaxG);
+    pa.c = c;
+    pa.c2 = c2;
+    const size_t psmem = draw_smem_bytes(V, kMaxG, pa.draw_level);
+    if (psmem > kDynSmemMax) return SV_ERR_UNSUPPORTED;
+    int ncl = resident_clusters(kMaxG);
+    if (ncl <= 0) ncl = 8;
+    if (ncl > B) ncl = B;
+    cudaLaunchConfig_t pc = {};
+    pc.gridDim = dim3((unsigned)(ncl * kMaxG), 1, 1);
+    pc.blockDim = dim3(kThreads, 1, 1);
+    pc.dynamicSmemBytes = psmem;
+    pc.stream = stream;
+    cudaLaunchAttribute pattr[2] = {cluster_attr(kMaxG), pdl};
+    pc.attrs = pattr;
+    pc.numAttrs = 2;
+    e = dt == SV_BF16 ? cudaLaunchKernelEx(&pc, sv_precise_kernel<__nv_bfloat16>, pa)
+                      : cudaLaunchKernelEx(&pc, sv_precise_kernel<float>, pa);
+    return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
 static sv_status launch_fused(bool sampled, const void* logits, sv_dtype dt, const float* q,
@@ -1406,11 +2129,25 @@ static sv_status launch_fused(bool sampled, const void* logits, sv_dtype dt, con
     a.c2 = log2e_over(sampled ? T : 1.0f);
     a.c = a.c2.hi;
     a.force_precise = g_force_precise.load();
+    a.plist_count = nullptr;
+    a.plist = nullptr;
+    a.prefetch = draw_prefetch(B, V, dt);
     size_t smem = 0;
+    a.draw_level = 0;
+    // Large sampled batches defer the precise draws to sv_precise_kernel.
+    const int dmode = g_fused_defer.load();
+    const bool defer = sampled && (dmode == 1 || (dmode == 0 && B >= sms));
     if (sampled) {
-        const long long nch = (V + kChunk - 1) / kChunk;
-        smem = (size_t)((nch + a.G - 1) / a.G) * 8;  // chunk sums of this CTA's slice
+        a.draw_level = draw_level(V, a.G);
+        smem = draw_smem_bytes(V, a.G, a.draw_level);
+        if (const int pad = g_fused_pad.load()) smem = std::max(smem, (size_t)pad * 1024);
         if (smem > kDynSmemMax) return SV_ERR_UNSUPPORTED;
+        if (defer) {
+            a.plist_count =
+                reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + ws_plist_offset(B, k));
+            a.plist = a.plist_count + 4;
+            if (cudaMemsetAsync(a.plist_count, 0, 16, stream) != cudaSuccess) return SV_ERR_CUDA;
+        }
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((long long)B * a.G), 1, 1);
@@ -1427,7 +2164,10 @@ static sv_status launch_fused(bool sampled, const void* logits, sv_dtype dt, con
     else
         e = sampled ? cudaLaunchKernelEx(&cfg, sv_verify_kernel<float, true>, a)
                     : cudaLaunchKernelEx(&cfg, sv_verify_kernel<float, false>, a);
-    return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+    if (e != cudaSuccess) return SV_ERR_CUDA;
+    if (!defer) return SV_OK;
+    return launch_precise(logits, dt, q, ur, a.rows, nacc, a.plist_count, a.plist, a.seqstat, out,
+                          B, k, V, a.c, a.c2, stream);
 }
 
 // Vocabulary split of the per-row kernel: enough CTAs to give every SM about
@@ -1446,16 +2186,21 @@ static int rows_threads(long long ctas, long long nvec_cta, int sms) {
     return t;
 }
 
+// With `skip`: one 512-thread CTA per row, rows position-major, stop[] reset
+// first (a memset on the same stream).
 static sv_status launch_rows(bool sampled, const void* logits, sv_dtype dt, const float* q,
-                             const int32_t* x, float T, int B, int k, int V, void* ws,
-                             cudaStream_t stream, int sms) {
+                             const int32_t* x, const float* ua, float T, int B, int k, int V,
+                             void* ws, cudaStream_t stream, int sms, bool skip) {
     const long long R = (long long)B * (k + 1);
     RowsArgs a;
     a.logits = logits;
     a.q = q;
     a.x = x;
+    a.ua = ua;
     a.hdr = static_cast<Header*>(ws);
     a.rows = reinterpret_cast<RowRec*>(static_cast<char*>(ws) + ws_rows_offset());
+    a.stop = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + ws_stop_offset(B, k));
+    a.skip = skip ? 1 : 0;
     a.B = B;
     a.k = k;
     a.V = V;
@@ -1464,8 +2209,10 @@ static sv_status launch_rows(bool sampled, const void* logits, sv_dtype dt, cons
     a.c = a.c2.hi;
     const int esz = dt == SV_BF16 ? 2 : 4;
     const long long nvec_row = ((long long)V * esz + 15) / 16;
-    a.G = rows_split(R, nvec_row, sms);
-    const int nt = rows_threads(R * a.G, nvec_row / a.G, sms);
+    a.G = skip ? 1 : rows_split(R, nvec_row, sms);
+    const int nt = skip ? 512 : rows_threads(R * a.G, nvec_row / a.G, sms);
+    if (skip && cudaMemsetAsync(a.stop, 0xFF, (size_t)B * sizeof(uint32_t), stream) != cudaSuccess)
+        return SV_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(R * a.G), 1, 1);
     cfg.blockDim = dim3(nt, 1, 1);
@@ -1489,10 +2236,27 @@ static sv_status launch_rows(bool sampled, const void* logits, sv_dtype dt, cons
     return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
+// Test / tuning hook (spec_verify_debug_draw_split): a fixed cluster size for
+// every draw kernel launch, 0 for the automatic choice.
+static std::atomic<int> g_force_draw_split{0};
+
+// Cluster size of the draw kernel of a large batch (B >= SMs): one CTA per
+// sequence (no cluster barriers, every CTA resident at once, the scheduler
+// starting each as a slot frees), unless a row exceeds the largest slice one
+// CTA draws from.  The precise draws go to sv_precise_kernel's 16-CTA clusters.
+static int draw_split_wide(int B, int V, int sms) {
+    (void)B;
+    (void)sms;
+    int G = 1;
+    while (G < 16 && (V + G - 1) / G > kSliceMax) G *= 2;
+    return G;
+}
+
+// `wide`: the draw kernel of a large batch (draw_split_wide), else seq_split.
 static sv_status launch_finish(bool sampled, const void* logits, sv_dtype dt, const float* q,
                                const int32_t* x, const float* ua, const float* ur, float T,
                                int B, int k, int V, int32_t* out, int32_t* nacc, void* ws,
-                               cudaStream_t stream, int sms) {
+                               cudaStream_t stream, int sms, bool wide) {
     const RowRec* rows =
         reinterpret_cast<const RowRec*>(static_cast<char*>(ws) + ws_rows_offset());
     uint32_t* seqstat = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + ws_seq_offset(B, k));
@@ -1523,13 +2287,25 @@ static sv_status launch_finish(bool sampled, const void* logits, sv_dtype dt, co
     a.B = B;
     a.k = k;
     a.V = V;
-    a.G = seq_split(true, B, V, dt == SV_BF16 ? 2 : 4, sms);
+    a.G = wide ? draw_split_wide(B, V, sms) : seq_split(true, B, V, dt == SV_BF16 ? 2 : 4, sms);
+    if (const int fg = g_force_draw_split.load()) a.G = fg;
     a.c2 = log2e_over(T);
     a.c = a.c2.hi;
     a.force_precise = g_force_precise.load();
-    const long long nch = (V + kChunk - 1) / kChunk;
-    const size_t smem = (size_t)((nch + a.G - 1) / a.G) * 8;
+    a.draw_level = draw_level(V, a.G);
+    a.prefetch = draw_prefetch(B, V, dt);
+    a.plist_count = nullptr;
+    a.plist = nullptr;
+    const size_t smem = draw_smem_bytes(V, a.G, a.draw_level);
     if (smem > kDynSmemMax) return SV_ERR_UNSUPPORTED;
+    // Large batches: the precise draws go to sv_precise_kernel through a list
+    // whose counter is reset here (so this kernel follows a memset, not the row
+    // stream, and is launched without the programmatic dependency).
+    if (wide) {
+        a.plist_count = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + ws_plist_offset(B, k));
+        a.plist = a.plist_count + 4;
+        if (cudaMemsetAsync(a.plist_count, 0, 16, stream) != cudaSuccess) return SV_ERR_CUDA;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((long long)B * a.G), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
@@ -1537,21 +2313,46 @@ static sv_status launch_finish(bool sampled, const void* logits, sv_dtype dt, co
     cfg.stream = stream;
     cudaLaunchAttribute attr[2] = {cluster_attr(a.G), pdl};
     cfg.attrs = attr;
-    cfg.numAttrs = 2;
+    cfg.numAttrs = wide ? 1 : 2;
     e = dt == SV_BF16 ? cudaLaunchKernelEx(&cfg, sv_finish_sample_kernel<__nv_bfloat16>, a)
                       : cudaLaunchKernelEx(&cfg, sv_finish_sample_kernel<float>, a);
-    return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+    if (e != cudaSuccess || !wide) return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+
+    return launch_precise(logits, dt, q, ur, rows, nacc, a.plist_count, a.plist, seqstat, out, B,
+                          k, V, a.c, a.c2, stream);
 }
 
-// The one-call entry points run the fused per-sequence kernel (rows read in
-// waves, early exit) when the batch alone has a sequence for every SM; smaller
-// batches take the two-kernel path, whose row stream spreads every row over
-// all SMs.
-// Test hook (spec_verify_debug_force_path): 0 automatic, 1 two-kernel, 2 fused.
+// Paths of the one-call entry points.  Batches with a sequence for every SM
+// take the row-skipping path (the row stream in position-major order, rows past
+// a sequence's first stop never read, then one draw CTA per sequence and the
+// precise draws in 16-CTA clusters).  Smaller sampled batches whose clusters
+// still cover every SM take the fused per-sequence kernel (rows in waves, early
+// exit, the draw in the same launch, no second launch); the rest take the
+// two-kernel path, whose row stream spreads every row over all SMs.
+enum Path { kPathTwoKernel = 1, kPathFused = 2, kPathSkip = 3 };
+// Test hook (spec_verify_debug_force_path): 0 automatic, else a Path.
 static std::atomic<int> g_force_path{0};
-static bool prefer_fused(int B, int sms) {
+static Path choose_path(bool sampled, int B, int V, int esz, int sms) {
     const int f = g_force_path.load();
-    return f == 2 || (f == 0 && B >= sms);
+    if (f >= kPathTwoKernel && f <= kPathSkip) return (Path)f;
+    if (B >= sms) return kPathSkip;
+    if (sampled && (long long)B * seq_split(true, B, V, esz, sms) >= sms) return kPathFused;
+    return kPathTwoKernel;
+}
+
+static sv_status run_verify(bool sampled, const void* logits, sv_dtype dt, const float* q,
+                            const int32_t* x, const float* ua, const float* ur, float T, int B,
+                            int k, int V, int32_t* out, int32_t* nacc, void* ws,
+                            cudaStream_t stream, int sms) {
+    const Path path = choose_path(sampled, B, V, dt == SV_BF16 ? 2 : 4, sms);
+    if (path == kPathFused)
+        return launch_fused(sampled, logits, dt, q, x, ua, ur, T, B, k, V, out, nacc, ws, stream,
+                            sms);
+    const bool skip = path == kPathSkip;
+    sv_status st = launch_rows(sampled, logits, dt, q, x, ua, T, B, k, V, ws, stream, sms, skip);
+    if (st != SV_OK) return st;
+    return launch_finish(sampled, logits, dt, q, x, ua, ur, T, B, k, V, out, nacc, ws, stream,
+                         sms, skip);
 }
 
 }  // namespace sv
@@ -1580,8 +2381,8 @@ sv_status spec_verify_rows(sv_mode mode, const void* logits, sv_dtype dtype,
     int sms = 0;
     if ((st = device_setup(&sms)) != SV_OK) return st;
     if (B == 0) return SV_OK;
-    return launch_rows(sampled, logits, dtype, draft_probs, draft_tokens, T, B, k, V, ws, stream,
-                       sms);
+    return launch_rows(sampled, logits, dtype, draft_probs, draft_tokens, nullptr, T, B, k, V, ws,
+                       stream, sms, false);
 }
 
 sv_status spec_verify_finish(sv_mode mode, const void* logits, sv_dtype dtype,
@@ -1599,7 +2400,7 @@ sv_status spec_verify_finish(sv_mode mode, const void* logits, sv_dtype dtype,
     if ((st = device_setup(&sms)) != SV_OK) return st;
     if (B == 0) return SV_OK;
     return launch_finish(sampled, logits, dtype, draft_probs, draft_tokens, u_accept, u_resample,
-                         T, B, k, V, out_tokens, num_accepted, ws, stream, sms);
+                         T, B, k, V, out_tokens, num_accepted, ws, stream, sms, B >= sms);
 }
 
 sv_status spec_verify_greedy(const void* logits, sv_dtype dtype, const int32_t* draft_tokens,
@@ -1611,13 +2412,8 @@ sv_status spec_verify_greedy(const void* logits, sv_dtype dtype, const int32_t* 
     int sms = 0;
     if ((st = device_setup(&sms)) != SV_OK) return st;
     if (B == 0) return SV_OK;
-    if (prefer_fused(B, sms))
-        return launch_fused(false, logits, dtype, nullptr, draft_tokens, nullptr, nullptr, 1.0f, B,
-                            k, V, out_tokens, num_accepted, ws, stream, sms);
-    st = launch_rows(false, logits, dtype, nullptr, draft_tokens, 1.0f, B, k, V, ws, stream, sms);
-    if (st != SV_OK) return st;
-    return launch_finish(false, logits, dtype, nullptr, draft_tokens, nullptr, nullptr, 1.0f, B, k,
-                         V, out_tokens, num_accepted, ws, stream, sms);
+    return run_verify(false, logits, dtype, nullptr, draft_tokens, nullptr, nullptr, 1.0f, B, k, V,
+                      out_tokens, num_accepted, ws, stream, sms);
 }
 
 sv_status spec_verify_sample(const void* logits, sv_dtype dtype, const float* draft_probs,
@@ -1632,13 +2428,8 @@ sv_status spec_verify_sample(const void* logits, sv_dtype dtype, const float* dr
     int sms = 0;
     if ((st = device_setup(&sms)) != SV_OK) return st;
     if (B == 0) return SV_OK;
-    if (prefer_fused(B, sms))
-        return launch_fused(true, logits, dtype, draft_probs, draft_tokens, u_accept, u_resample,
-                            T, B, k, V, out_tokens, num_accepted, ws, stream, sms);
-    st = launch_rows(true, logits, dtype, draft_probs, draft_tokens, T, B, k, V, ws, stream, sms);
-    if (st != SV_OK) return st;
-    return launch_finish(true, logits, dtype, draft_probs, draft_tokens, u_accept, u_resample, T,
-                         B, k, V, out_tokens, num_accepted, ws, stream, sms);
+    return run_verify(true, logits, dtype, draft_probs, draft_tokens, u_accept, u_resample, T, B,
+                      k, V, out_tokens, num_accepted, ws, stream, sms);
 }
 
 sv_status spec_verify_read_status(const void* ws, cudaStream_t stream, uint32_t* device_status,
@@ -1727,13 +2518,50 @@ void spec_verify_debug_force_precise(int on) { g_force_precise.store(on != 0 ? 1
 // Test hook (declared in include/specverify_debug.h): choose the one-call path.
 void spec_verify_debug_force_path(int path) { g_force_path.store(path >= 0 && path <= 2 ? path : 0); }
 
-// Introspection (declared in include/specverify_debug.h): 1 if the one-call
-// entry points run the fused per-sequence kernel for a batch of B sequences on
-// the current device, 0 for the two-kernel path, -1 on error.
-int spec_verify_debug_uses_fused(int B) {
+// Introspection (declared in include/specverify_debug.h): the path the one-call
+// entry points take for these sizes on the current device (1 two-kernel, 2
+// fused, 3 row-skipping), -1 on error.
+int spec_verify_debug_path(sv_mode mode, int B, int V, sv_dtype dtype) {
     int sms = 0;
     if (device_setup(&sms) != SV_OK) return -1;
-    return prefer_fused(B, sms) ? 1 : 0;
+    if (B < 1 || V < 1 || (dtype != SV_BF16 && dtype != SV_F32)) return -1;
+    return (int)choose_path(mode == SV_MODE_SAMPLE, B, V, dtype == SV_BF16 ? 2 : 4, sms);
+}
+
+// Tuning hook: deferral of the fused kernel's precise draws and its minimum
+// dynamic shared memory per CTA (KiB, 0..160).
+void spec_verify_debug_fused_tuning(int defer_mode, int pad_kib) {
+    if (defer_mode >= 0 && defer_mode <= 2) g_fused_defer.store(defer_mode);
+    if (pad_kib >= 0 && pad_kib <= 160) g_fused_pad.store(pad_kib);
+}
+
+// Tuning hook: a fixed cluster size (1, 2, 4, 8 or 16) for the draw kernel, 0
+// for the automatic choice.  Other values are ignored.
+void spec_verify_debug_draw_split(int G) {
+    if (G == 0 || G == 1 || G == 2 || G == 4 || G == 8 || G == 16) g_force_draw_split.store(G);
+}
+
+// Test / timing hook: the first stage of the row-skipping path alone (the reset
+// of the stop rows and the position-major row stream).  Argument checks as for
+// spec_verify_rows; u_accept is required in sampled mode.
+sv_status spec_verify_debug_rows_skip(sv_mode mode, const void* logits, sv_dtype dtype,
+                                      const float* draft_probs, const int32_t* draft_tokens,
+                                      const float* u_accept, float T, int B, int k, int V,
+                                      void* ws, size_t ws_bytes, cudaStream_t stream) {
+    if (mode != SV_MODE_SAMPLE && mode != SV_MODE_GREEDY) return SV_ERR_INVALID_ARG;
+    sv_status st = check_common(logits, dtype, draft_tokens, B, k, V, ws, ws_bytes);
+    if (st != SV_OK) return st;
+    const bool sampled = mode == SV_MODE_SAMPLE;
+    if (sampled) {
+        if (!(T > 0.0f) || !std::isfinite(T)) return SV_ERR_INVALID_ARG;
+        if (B > 0 && (!draft_probs || !u_accept || !aligned16(draft_probs) || !aligned16(u_accept)))
+            return SV_ERR_INVALID_ARG;
+    }
+    int sms = 0;
+    if ((st = device_setup(&sms)) != SV_OK) return st;
+    if (B == 0) return SV_OK;
+    return launch_rows(sampled, logits, dtype, draft_probs, draft_tokens, u_accept, T, B, k, V, ws,
+                       stream, sms, true);
 }
 
 // Test hook: the largest relative error of ex2.approx.ftz.f32 against the
@@ -1763,7 +2591,7 @@ namespace sv {
 
 constexpr size_t kNoAllocScratchBytes = SV_NOALLOC_SCRATCH_BYTES;
 static_assert(kNoAllocScratchBytes >= 256 + 32 * (size_t)SV_NOALLOC_MAX_ROWS +
-                                          4 * (size_t)(SV_NOALLOC_MAX_ROWS / 2) + 255,
+                                          12 * (size_t)(SV_NOALLOC_MAX_ROWS / 2) + 31 + 255,
               "scratch size");
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];

@@ -27,7 +27,7 @@ EXPORTS = ("spec_verify_workspace_size", "spec_verify_greedy", "spec_verify_samp
            "spec_verify_rows", "spec_verify_finish", "spec_verify_read_status",
            "spec_verify_row_stats", "spec_verify_status_string", "spec_verify_sample_noalloc")
 SV_NOALLOC_SCRATCH_BYTES = 1048576
-SV_NOALLOC_MAX_ROWS = 30720
+SV_NOALLOC_MAX_ROWS = 27000
 
 _lib = None
 
@@ -58,6 +58,12 @@ def load():
     lib.spec_verify_rows.restype = I
     lib.spec_verify_finish.argtypes = [I, P, I, P, P, P, P, F, I, I, I, P, P, P, Z, P]
     lib.spec_verify_finish.restype = I
+    lib.spec_verify_debug_fused_tuning.argtypes = [I, I]
+    lib.spec_verify_debug_fused_tuning.restype = None
+    lib.spec_verify_debug_draw_split.argtypes = [I]
+    lib.spec_verify_debug_draw_split.restype = None
+    lib.spec_verify_debug_rows_skip.argtypes = [I, P, I, P, P, P, F, I, I, I, P, Z, P]
+    lib.spec_verify_debug_rows_skip.restype = I
     lib.spec_verify_read_status.argtypes = [P, P, P, P]
     lib.spec_verify_read_status.restype = I
     lib.spec_verify_row_stats.argtypes = [P, P, I, I, P, P, P, P, P]
@@ -72,8 +78,8 @@ def load():
     lib.spec_verify_debug_force_precise.restype = None
     lib.spec_verify_debug_force_path.argtypes = [I]
     lib.spec_verify_debug_force_path.restype = None
-    lib.spec_verify_debug_uses_fused.argtypes = [I]
-    lib.spec_verify_debug_uses_fused.restype = I
+    lib.spec_verify_debug_path.argtypes = [I, I, I, I]
+    lib.spec_verify_debug_path.restype = I
     lib.spec_verify_debug_ex2_error.argtypes = [F, F, P, P]
     lib.spec_verify_debug_ex2_error.restype = I
     _lib = lib
@@ -158,6 +164,26 @@ def spec_verify_rows(mode, logits, draft_probs, draft_tokens, T, ws, stream=None
     _check(st, "spec_verify_rows")
 
 
+def debug_fused_tuning(defer_mode: int, pad_kib: int):
+    """Tuning hook of the fused kernel (precise-draw deferral, shared-memory floor)."""
+    load().spec_verify_debug_fused_tuning(int(defer_mode), int(pad_kib))
+
+
+def debug_draw_split(G: int):
+    """Tuning hook: a fixed cluster size for the draw kernel (0 = automatic)."""
+    load().spec_verify_debug_draw_split(int(G))
+
+
+def debug_rows_skip(mode, logits, draft_probs, draft_tokens, u_accept, T, ws, stream=None):
+    """Timing hook: the row-skipping path's first stage (stop reset + row stream)."""
+    B, k1, V = logits.shape
+    st = load().spec_verify_debug_rows_skip(int(mode), _ptr(logits), _dtype(logits),
+                                            _ptr(draft_probs), _ptr(draft_tokens), _ptr(u_accept),
+                                            float(T), B, k1 - 1, V, _ptr(ws), ws.numel(),
+                                            _stream(stream))
+    _check(st, "spec_verify_debug_rows_skip")
+
+
 def spec_verify_finish(mode, logits, draft_probs, draft_tokens, u_accept, u_resample, T,
                        out_tokens, num_accepted, ws, stream=None):
     B, k1, V = logits.shape
@@ -215,17 +241,21 @@ def debug_force_precise(on: bool):
     load().spec_verify_debug_force_precise(1 if on else 0)
 
 
+PATH_TWO_KERNEL, PATH_FUSED, PATH_SKIP = 1, 2, 3
+
+
 def debug_force_path(path: int):
-    """Test hook: 0 automatic, 1 two-kernel path, 2 fused kernel."""
+    """Test hook: 0 automatic, 1 two-kernel path, 2 fused kernel, 3 row-skipping path."""
     load().spec_verify_debug_force_path(int(path))
 
 
-def uses_fused(B: int) -> bool:
-    """Whether the one-call entry points run the fused kernel for B sequences."""
-    r = load().spec_verify_debug_uses_fused(int(B))
+def debug_path(mode: int, B: int, V: int, dtype) -> int:
+    """The path (PATH_*) the one-call entry points take for these sizes."""
+    dt = SV_BF16 if dtype in (torch.bfloat16, "bf16") else SV_F32
+    r = load().spec_verify_debug_path(int(mode), int(B), int(V), dt)
     if r < 0:
-        raise SpecVerifyError(SV_ERR_CUDA, "spec_verify_debug_uses_fused")
-    return bool(r)
+        raise SpecVerifyError(SV_ERR_CUDA, "spec_verify_debug_path")
+    return r
 
 
 def debug_ex2_error(a0: float, a1: float, stream=None) -> float:

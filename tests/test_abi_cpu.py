@@ -37,9 +37,9 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_workspace_size(lib):
     from speculative_decoding_verification_18_gb300 import specverify as sv
-    assert sv.spec_verify_workspace_size(64, 4, 32000) == 256 + 64 * 5 * 32 + 64 * 4
+    assert sv.spec_verify_workspace_size(64, 4, 32000) == 256 + 64 * 5 * 32 + 64 * 4 * 3 + 256
     assert sv.spec_verify_workspace_size(1, 1, 1) == 512
-    assert sv.spec_verify_workspace_size(0, 4, 10) == 256
+    assert sv.spec_verify_workspace_size(0, 4, 10) == 512
     assert sv.spec_verify_workspace_size(1, 0, 10) == 0
     assert sv.spec_verify_workspace_size(1, 65, 10) == 0
     assert sv.spec_verify_workspace_size(1, 4, (1 << 21) + 1) == 0

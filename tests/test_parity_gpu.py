@@ -48,7 +48,7 @@ SMALL = [
 ]
 
 
-@pytest.fixture(params=[1, 2], ids=["two_kernel", "fused"])
+@pytest.fixture(params=[1, 2, 3], ids=["two_kernel", "fused", "skip"])
 def path(request):
     """Run a test once through each one-call path (forced by the test hook)."""
     from speculative_decoding_verification_18_gb300 import specverify as sv
@@ -104,6 +104,50 @@ def test_workload_fused_path(name):
     rep = compare_outputs(inp, out, n, ref)
     assert rep.hard == 0 and rep.near_threshold <= 1, rep.hard_detail
     compare_stats(inp, stats, ref, n)
+
+
+@pytest.mark.parametrize("mode", ["sample", "greedy"])
+def test_skip_path_skips_rows_and_matches(mode):
+    """The row-skipping path on a batch of many waves of rows: later rows of a
+    sequence that has already stopped are not read (their statistics come back
+    unset), and every output still equals the oracle's."""
+    from speculative_decoding_verification_18_gb300 import specverify as sv
+    inp = _gen(mode=mode, B=2048, k=6, V=2000, dtype="bf16", T=0.9, kind="zipf", p_argmax=0.6,
+               seed=77)
+    sv.debug_force_path(sv.PATH_SKIP)
+    try:
+        out, n, stats, (st, bits, _) = run_gpu(inp)
+    finally:
+        sv.debug_force_path(0)
+    ref = run_oracle(inp)
+    if mode == "greedy":
+        assert np.array_equal(n, ref.n) and np.array_equal(out, ref.out)
+    else:
+        rep = compare_outputs(inp, out, n, ref)
+        assert rep.hard == 0 and rep.near_threshold <= 2, rep.hard_detail
+    assert st == 0 and (bits & 0xF) == 0
+    compare_stats(inp, stats, ref, n)
+    argmax = stats["argmax"].reshape(inp.B, inp.k + 1)
+    skipped = argmax < 0
+    # never a row at or before the decision row
+    assert not any(skipped[b, : n[b] + 1].any() for b in range(inp.B))
+    assert skipped.sum() > 0
+
+
+@pytest.mark.parametrize("name", ["c4"])
+def test_workload_fused_path_large(name):
+    """The fused per-sequence kernel on the large-batch workload."""
+    from speculative_decoding_verification_18_gb300 import specverify as sv
+    from speculative_decoding_verification_18_gb300.inputs import workload
+    inp = workload(name, seed=12)
+    sv.debug_force_path(sv.PATH_FUSED)
+    try:
+        out, n, stats, (st, bits, _) = run_gpu(inp)
+    finally:
+        sv.debug_force_path(0)
+    ref = run_oracle(inp)
+    rep = compare_outputs(inp, out, n, ref)
+    assert rep.hard == 0 and rep.near_threshold <= 1, rep.hard_detail
 
 
 @pytest.mark.parametrize("name", ["c1", "c2", "c3", "c4", "c5"])
