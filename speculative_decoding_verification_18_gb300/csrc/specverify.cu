@@ -2516,7 +2516,7 @@ sv_status spec_verify_debug_ffexp(const float* l, float m, float T, int n, doubl
 void spec_verify_debug_force_precise(int on) { g_force_precise.store(on != 0 ? 1 : 0); }
 
 // Test hook (declared in include/specverify_debug.h): choose the one-call path.
-void spec_verify_debug_force_path(int path) { g_force_path.store(path >= 0 && path <= 2 ? path : 0); }
+void spec_verify_debug_force_path(int path) { g_force_path.store(path >= 0 && path <= 3 ? path : 0); }
 
 // Introspection (declared in include/specverify_debug.h): the path the one-call
 // entry points take for these sizes on the current device (1 two-kernel, 2
