@@ -417,7 +417,10 @@ def main():
         if fused:
             stage_times = {"sv_verify_kernel": ms / K}
         else:
+            # the draw stage of a large sampled batch is two kernels: the fast draw
+            # and the precise draws it hands on
             fin_name = ("sv_finish_greedy_kernel" if inp.mode == "greedy"
+                        else "sv_finish_sample_kernel+sv_precise_kernel" if path == sv.PATH_SKIP
                         else "sv_finish_sample_kernel")
             stage_times = {"sv_rows_kernel": stage_ms(rows_stage),
                            fin_name: stage_ms(finish_stage)}
@@ -540,7 +543,8 @@ def main():
         "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
-        "gpu_launches": (1 if fused else 2) * K,
+        "gpu_launches": (1 if fused else 3 if (path == sv.PATH_SKIP and inp.mode == "sample")
+                         else 2) * K,
         "roofline": roofline,
         "cpu_baseline": {"value": cpu_value, "unit": "rows/s", "cores": nt, "kind": "oracle",
                          "sample": f"first {seqs} of {B} sequences ({seqs * (k + 1)} rows), "
