@@ -127,7 +127,42 @@ sv_status spec_verify_sample(const void* logits, sv_dtype dtype, const float* dr
                              int32_t* out_tokens, int32_t* num_accepted,
                              void* ws, size_t ws_bytes, cudaStream_t stream);
 
-/* The same work as the two calls above, split at its one internal dependency so
+/* Counters a verify can add to (spec_verify_*_kv), for generation loops that
+ * keep speculation statistics on the device ("Speculative Decoding" (ch15, LLM
+ * serving from scratch), the stats argument of speculative_generate; the
+ * tokens-per-target-pass figure of "Decodificação especulativa explicada",
+ * §"Quanto mais rápido: a matemática" is emitted / rounds). */
+typedef struct {
+    unsigned long long rounds;    /* valid sequences verified: one target pass each */
+    unsigned long long proposed;  /* drafted tokens judged: k per valid sequence */
+    unsigned long long accepted;  /* accepted drafts: the sum of num_accepted */
+    unsigned long long emitted;   /* tokens emitted: the sum of num_accepted + 1 */
+    unsigned long long invalid;   /* sequences marked invalid (num_accepted = -1) */
+} sv_spec_stats;
+
+/* spec_verify_sample / spec_verify_greedy with the bookkeeping of a generation
+ * loop fused into the kernel that writes num_accepted ("Decodificação
+ * especulativa explicada", §"O ciclo de rascunho e verificação", bookkeeping
+ * paragraph: the entries after the first rejection are dropped):
+ *   kv_len [B] int32 DEVICE (may be NULL): kv_len[b] += num_accepted[b] + 1 for
+ *          every valid sequence (the n accepted drafts and the drawn token);
+ *          unchanged for an invalid one.
+ *   stats  DEVICE sv_spec_stats (may be NULL): counters added atomically; the
+ *          caller zeroes them when it wants a fresh count.
+ * Both 16-byte aligned.  All other arguments, results and errors as for the
+ * calls without _kv. */
+sv_status spec_verify_sample_kv(const void* logits, sv_dtype dtype, const float* draft_probs,
+                                const int32_t* draft_tokens, const float* u_accept,
+                                const float* u_resample, float T, int B, int k, int V,
+                                int32_t* out_tokens, int32_t* num_accepted, void* ws,
+                                size_t ws_bytes, int32_t* kv_len, sv_spec_stats* stats,
+                                cudaStream_t stream);
+sv_status spec_verify_greedy_kv(const void* logits, sv_dtype dtype, const int32_t* draft_tokens,
+                                int B, int k, int V, int32_t* out_tokens, int32_t* num_accepted,
+                                void* ws, size_t ws_bytes, int32_t* kv_len, sv_spec_stats* stats,
+                                cudaStream_t stream);
+
+/* The work of spec_verify_greedy / spec_verify_sample, split at its one internal dependency so
  * that each half can be timed or overlapped separately.  spec_verify_rows
  * streams every logits row once and leaves per-row statistics (max, normaliser,
  * argmax, gathered l(x), q(x), p(x)) in ws; spec_verify_finish then runs the

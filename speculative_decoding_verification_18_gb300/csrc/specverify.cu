@@ -1199,6 +1199,29 @@ __device__ bool draw(cg::cluster_group& cluster, DrawShared& sh, const DrawCtx<D
 
 // ------------------------------------------------------------------ the fused kernel
 
+// Optional epilogue of a verify, done by the thread that writes num_accepted[b]:
+// kv_len[b] += n + 1 for a valid sequence (the round's committed tokens: the n
+// accepted drafts and the drawn one; entries past the first rejection are
+// dropped, "Decodificação especulativa explicada", §"O ciclo de rascunho e
+// verificação", bookkeeping paragraph), and the counters of sv_spec_stats.
+struct Epilogue {
+    int32_t* kv_len;               // [B] or null
+    unsigned long long* stats;     // sv_spec_stats as 5 counters, or null
+};
+__device__ __forceinline__ void commit_sequence(const Epilogue& ep, int b, int n, int k) {
+    if (n >= 0) {
+        if (ep.kv_len) ep.kv_len[b] += n + 1;
+        if (ep.stats) {
+            atomicAdd(ep.stats + 0, 1ull);
+            atomicAdd(ep.stats + 1, (unsigned long long)k);
+            atomicAdd(ep.stats + 2, (unsigned long long)n);
+            atomicAdd(ep.stats + 3, (unsigned long long)(n + 1));
+        }
+    } else if (ep.stats) {
+        atomicAdd(ep.stats + 4, 1ull);
+    }
+}
+
 struct VerifyArgs {
     const void* logits;
     const float* q;
@@ -1212,6 +1235,7 @@ struct VerifyArgs {
     int32_t* nacc;
     uint32_t* plist_count;  // with plist: draws needing the precise pass are
     uint32_t* plist;        // appended here for sv_precise_kernel (else run here)
+    Epilogue ep;
     int B, k, V, G, W;
     int draw_level;     // shared-memory cache level of the draw
     int prefetch;       // the draws bulk-prefetch their slices into L2
@@ -1417,6 +1441,7 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(VerifyArgs a) {
             if (tid == 0) {
                 a.nacc[b] = bits ? -1 : n;
                 a.seqstat[b] = (uint32_t)bits;
+                commit_sequence(a.ep, b, bits ? -1 : n, k);
             }
         }
         if (G > 1) cluster.sync();  // partial slots may still be read by other ranks
@@ -1431,6 +1456,7 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(VerifyArgs a) {
             if (tid == 0) {
                 a.nacc[b] = -1;
                 a.seqstat[b] = SV_DEV_BAD_UNIFORM;
+                commit_sequence(a.ep, b, -1, k);
             }
         }
         if (G > 1) cluster.sync();
@@ -1451,6 +1477,7 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(VerifyArgs a) {
         if (tid == 0) {
             a.nacc[b] = n;
             a.seqstat[b] = (degenerate ? SV_DEV_DEGENERATE : 0u) | (fallback ? SV_DEV_PRECISE : 0u);
+            commit_sequence(a.ep, b, n, k);
             if (deferred) {
                 const uint32_t j = atomicAdd(a.plist_count, 1u);
                 if (j < (uint32_t)a.B) a.plist[j] = (uint32_t)b;  // at most B entries
@@ -1551,7 +1578,9 @@ __global__ void __launch_bounds__(NT) sv_rows_kernel(RowsArgs a) {
     row_layout<DT>(rowp, V, head, nvec, tail0);
     const int lgG = log2_pow2(G);
     const long long vb = (nvec * rank) >> lgG, ve = (nvec * (rank + 1)) >> lgG;
-    Partial p = stream_slice<DT, SAMPLED, 4>(rowp, V, vb, ve, head, tail0, rank == 0,
+    // Eight 16-byte loads in flight per thread: a row slice of up to 8 vectors
+    // per thread costs one round trip.
+    Partial p = stream_slice<DT, SAMPLED, 8>(rowp, V, vb, ve, head, tail0, rank == 0,
                                              rank == G - 1, tid, NT, a.c);
     p = warp_merge<SAMPLED>(p, a.c);
     if (lane == 0) wpart[warp] = p;
@@ -1618,7 +1647,8 @@ __global__ void __launch_bounds__(NT) sv_rows_kernel(RowsArgs a) {
 __global__ void sv_finish_greedy_kernel(const int32_t* __restrict__ x,
                                         const RowRec* __restrict__ rows,
                                         uint32_t* __restrict__ seqstat, int B, int k,
-                                        int32_t* __restrict__ out, int32_t* __restrict__ nacc) {
+                                        int32_t* __restrict__ out, int32_t* __restrict__ nacc,
+                                        Epilogue ep) {
     __shared__ RowRec recs[4][kMaxK + 1];
     __shared__ int xs[4][kMaxK];
     const int wi = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1644,12 +1674,14 @@ __global__ void sv_finish_greedy_kernel(const int32_t* __restrict__ x,
     if (bits) {
         for (int i = 0; i <= k; ++i) o[i] = -1;
         nacc[b] = -1;
+        commit_sequence(ep, b, -1, k);
         return;
     }
     for (int i = 0; i < n; ++i) o[i] = xx[i];
     o[n] = rr[n].argmax;
     for (int i = n + 1; i <= k; ++i) o[i] = -1;
     nacc[b] = n;
+    commit_sequence(ep, b, n, k);
 }
 
 struct FinishArgs {
@@ -1664,6 +1696,7 @@ struct FinishArgs {
     int32_t* nacc;
     uint32_t* plist_count;  // with plist: draws needing the precise pass are
     uint32_t* plist;        // appended here for sv_precise_kernel (else run here)
+    Epilogue ep;
     int B, k, V, G;
     int draw_level;
     int prefetch;  // the draws bulk-prefetch their slices into L2
@@ -1734,6 +1767,7 @@ __global__ void __launch_bounds__(kThreads, 2) sv_finish_sample_kernel(FinishArg
             if (tid == 0) {
                 a.nacc[b] = -1;
                 a.seqstat[b] = (uint32_t)s_bits;
+                commit_sequence(a.ep, b, -1, k);
             }
         }
         return;  // every CTA of the cluster takes this branch together
@@ -1751,6 +1785,7 @@ __global__ void __launch_bounds__(kThreads, 2) sv_finish_sample_kernel(FinishArg
         if (tid == 0) {
             a.nacc[b] = n;
             a.seqstat[b] = (degenerate ? SV_DEV_DEGENERATE : 0u) | (fallback ? SV_DEV_PRECISE : 0u);
+            commit_sequence(a.ep, b, n, k);
             if (deferred) {
                 const uint32_t j = atomicAdd(a.plist_count, 1u);
                 if (j < (uint32_t)a.B) a.plist[j] = (uint32_t)b;  // at most B entries
@@ -2108,8 +2143,9 @@ static sv_status launch_precise(const void* logits, sv_dtype dt, const float* q,
 static sv_status launch_fused(bool sampled, const void* logits, sv_dtype dt, const float* q,
                               const int32_t* x, const float* ua, const float* ur, float T, int B,
                               int k, int V, int32_t* out, int32_t* nacc, void* ws,
-                              cudaStream_t stream, int sms) {
+                              cudaStream_t stream, int sms, Epilogue ep) {
     VerifyArgs a;
+    a.ep = ep;
     a.logits = logits;
     a.q = q;
     a.x = x;
@@ -2256,7 +2292,7 @@ static int draw_split_wide(int B, int V, int sms) {
 static sv_status launch_finish(bool sampled, const void* logits, sv_dtype dt, const float* q,
                                const int32_t* x, const float* ua, const float* ur, float T,
                                int B, int k, int V, int32_t* out, int32_t* nacc, void* ws,
-                               cudaStream_t stream, int sms, bool wide) {
+                               cudaStream_t stream, int sms, bool wide, Epilogue ep) {
     const RowRec* rows =
         reinterpret_cast<const RowRec*>(static_cast<char*>(ws) + ws_rows_offset());
     uint32_t* seqstat = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + ws_seq_offset(B, k));
@@ -2271,10 +2307,12 @@ static sv_status launch_finish(bool sampled, const void* logits, sv_dtype dt, co
         cfg.stream = stream;
         cfg.attrs = &pdl;
         cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, sv_finish_greedy_kernel, x, rows, seqstat, B, k, out, nacc);
+        e = cudaLaunchKernelEx(&cfg, sv_finish_greedy_kernel, x, rows, seqstat, B, k, out, nacc,
+                               ep);
         return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
     }
     FinishArgs a;
+    a.ep = ep;
     a.logits = logits;
     a.q = q;
     a.x = x;
@@ -2343,16 +2381,16 @@ static Path choose_path(bool sampled, int B, int V, int esz, int sms) {
 static sv_status run_verify(bool sampled, const void* logits, sv_dtype dt, const float* q,
                             const int32_t* x, const float* ua, const float* ur, float T, int B,
                             int k, int V, int32_t* out, int32_t* nacc, void* ws,
-                            cudaStream_t stream, int sms) {
+                            cudaStream_t stream, int sms, Epilogue ep) {
     const Path path = choose_path(sampled, B, V, dt == SV_BF16 ? 2 : 4, sms);
     if (path == kPathFused)
         return launch_fused(sampled, logits, dt, q, x, ua, ur, T, B, k, V, out, nacc, ws, stream,
-                            sms);
+                            sms, ep);
     const bool skip = path == kPathSkip;
     sv_status st = launch_rows(sampled, logits, dt, q, x, ua, T, B, k, V, ws, stream, sms, skip);
     if (st != SV_OK) return st;
     return launch_finish(sampled, logits, dt, q, x, ua, ur, T, B, k, V, out, nacc, ws, stream,
-                         sms, skip);
+                         sms, skip, ep);
 }
 
 }  // namespace sv
@@ -2400,7 +2438,8 @@ sv_status spec_verify_finish(sv_mode mode, const void* logits, sv_dtype dtype,
     if ((st = device_setup(&sms)) != SV_OK) return st;
     if (B == 0) return SV_OK;
     return launch_finish(sampled, logits, dtype, draft_probs, draft_tokens, u_accept, u_resample,
-                         T, B, k, V, out_tokens, num_accepted, ws, stream, sms, B >= sms);
+                         T, B, k, V, out_tokens, num_accepted, ws, stream, sms, B >= sms,
+                         Epilogue{nullptr, nullptr});
 }
 
 sv_status spec_verify_greedy(const void* logits, sv_dtype dtype, const int32_t* draft_tokens,
@@ -2413,7 +2452,23 @@ sv_status spec_verify_greedy(const void* logits, sv_dtype dtype, const int32_t* 
     if ((st = device_setup(&sms)) != SV_OK) return st;
     if (B == 0) return SV_OK;
     return run_verify(false, logits, dtype, nullptr, draft_tokens, nullptr, nullptr, 1.0f, B, k, V,
-                      out_tokens, num_accepted, ws, stream, sms);
+                      out_tokens, num_accepted, ws, stream, sms, Epilogue{nullptr, nullptr});
+}
+
+sv_status spec_verify_greedy_kv(const void* logits, sv_dtype dtype, const int32_t* draft_tokens,
+                                int B, int k, int V, int32_t* out_tokens, int32_t* num_accepted,
+                                void* ws, size_t ws_bytes, int32_t* kv_len, sv_spec_stats* stats,
+                                cudaStream_t stream) {
+    sv_status st = check_common(logits, dtype, draft_tokens, B, k, V, ws, ws_bytes);
+    if (st != SV_OK) return st;
+    if ((st = check_outputs(out_tokens, num_accepted, B)) != SV_OK) return st;
+    if ((kv_len && !aligned16(kv_len)) || (stats && !aligned16(stats))) return SV_ERR_INVALID_ARG;
+    int sms = 0;
+    if ((st = device_setup(&sms)) != SV_OK) return st;
+    if (B == 0) return SV_OK;
+    return run_verify(false, logits, dtype, nullptr, draft_tokens, nullptr, nullptr, 1.0f, B, k, V,
+                      out_tokens, num_accepted, ws, stream, sms,
+                      Epilogue{kv_len, reinterpret_cast<unsigned long long*>(stats)});
 }
 
 sv_status spec_verify_sample(const void* logits, sv_dtype dtype, const float* draft_probs,
@@ -2429,7 +2484,26 @@ sv_status spec_verify_sample(const void* logits, sv_dtype dtype, const float* dr
     if ((st = device_setup(&sms)) != SV_OK) return st;
     if (B == 0) return SV_OK;
     return run_verify(true, logits, dtype, draft_probs, draft_tokens, u_accept, u_resample, T, B,
-                      k, V, out_tokens, num_accepted, ws, stream, sms);
+                      k, V, out_tokens, num_accepted, ws, stream, sms, Epilogue{nullptr, nullptr});
+}
+
+sv_status spec_verify_sample_kv(const void* logits, sv_dtype dtype, const float* draft_probs,
+                                const int32_t* draft_tokens, const float* u_accept,
+                                const float* u_resample, float T, int B, int k, int V,
+                                int32_t* out_tokens, int32_t* num_accepted, void* ws,
+                                size_t ws_bytes, int32_t* kv_len, sv_spec_stats* stats,
+                                cudaStream_t stream) {
+    sv_status st = check_common(logits, dtype, draft_tokens, B, k, V, ws, ws_bytes);
+    if (st != SV_OK) return st;
+    if ((st = check_outputs(out_tokens, num_accepted, B)) != SV_OK) return st;
+    if ((st = check_sample(draft_probs, u_accept, u_resample, T, B)) != SV_OK) return st;
+    if ((kv_len && !aligned16(kv_len)) || (stats && !aligned16(stats))) return SV_ERR_INVALID_ARG;
+    int sms = 0;
+    if ((st = device_setup(&sms)) != SV_OK) return st;
+    if (B == 0) return SV_OK;
+    return run_verify(true, logits, dtype, draft_probs, draft_tokens, u_accept, u_resample, T, B,
+                      k, V, out_tokens, num_accepted, ws, stream, sms,
+                      Epilogue{kv_len, reinterpret_cast<unsigned long long*>(stats)});
 }
 
 sv_status spec_verify_read_status(const void* ws, cudaStream_t stream, uint32_t* device_status,

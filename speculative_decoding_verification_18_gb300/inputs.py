@@ -207,3 +207,16 @@ def workload(name: str, seed: int | None = None) -> VerifyInputs:
     inp = make_inputs(**cfg)
     inp.meta["workload"] = name
     return inp
+
+
+def toy_language(seed: int = 2, V: int = 4, keep: float = 0.55):
+    """The bigram toy language of "Decodificação especulativa explicada", §"Amostragem
+    especulativa em numpy, com prova": target rows P[t] = p(next | previous t) are
+    Dirichlet(1) draws, and the draft blurs them, Q = keep * P + (1 - keep) * D with
+    D another set of Dirichlet(1) rows.  The two draws are made with the page's
+    generator calls in the page's order, the only order that reproduces its
+    printed acceptance per context.  Returns float64 arrays P, Q of shape [V, V]."""
+    g = np.random.default_rng(seed)
+    P = g.dirichlet(np.ones(V), size=V)
+    D = g.dirichlet(np.ones(V), size=V)
+    return P, keep * P + (1.0 - keep) * D

@@ -53,6 +53,10 @@ def load():
     lib.spec_verify_greedy.argtypes = [P, I, P, I, I, I, P, P, P, Z, P]
     lib.spec_verify_greedy.restype = I
     lib.spec_verify_sample.argtypes = [P, I, P, P, P, P, F, I, I, I, P, P, P, Z, P]
+    lib.spec_verify_sample_kv.argtypes = [P, I, P, P, P, P, F, I, I, I, P, P, P, Z, P, P, P]
+    lib.spec_verify_sample_kv.restype = I
+    lib.spec_verify_greedy_kv.argtypes = [P, I, P, I, I, I, P, P, P, Z, P, P, P]
+    lib.spec_verify_greedy_kv.restype = I
     lib.spec_verify_sample.restype = I
     lib.spec_verify_rows.argtypes = [I, P, I, P, P, F, I, I, I, P, Z, P]
     lib.spec_verify_rows.restype = I
@@ -142,6 +146,42 @@ def spec_verify_sample(logits, draft_probs, draft_tokens, u_accept, u_resample, 
                                    B, k1 - 1, V, _ptr(out_tokens), _ptr(num_accepted), _ptr(ws),
                                    ws.numel(), _stream(stream))
     _check(st, "spec_verify_sample")
+
+
+STATS_FIELDS = ("rounds", "proposed", "accepted", "emitted", "invalid")
+
+
+def stats_tensor(device=None):
+    """Zeroed device counters laid out as sv_spec_stats (int64[5], 16-byte aligned)."""
+    return torch.zeros(len(STATS_FIELDS), dtype=torch.int64, device=device or "cuda")
+
+
+def stats_dict(stats):
+    """sv_spec_stats counters (a stats_tensor) as a dict of ints."""
+    v = stats.cpu().tolist()
+    return dict(zip(STATS_FIELDS, (int(x) for x in v)))
+
+
+def spec_verify_sample_kv(logits, draft_probs, draft_tokens, u_accept, u_resample, T, out_tokens,
+                          num_accepted, ws, kv_len=None, stats=None, stream=None):
+    """spec_verify_sample, then kv_len[b] += n + 1 and the stats counters, in the kernel."""
+    B, k1, V = logits.shape
+    st = load().spec_verify_sample_kv(_ptr(logits), _dtype(logits), _ptr(draft_probs),
+                                      _ptr(draft_tokens), _ptr(u_accept), _ptr(u_resample),
+                                      float(T), B, k1 - 1, V, _ptr(out_tokens),
+                                      _ptr(num_accepted), _ptr(ws), ws.numel(), _ptr(kv_len),
+                                      _ptr(stats), _stream(stream))
+    _check(st, "spec_verify_sample_kv")
+
+
+def spec_verify_greedy_kv(logits, draft_tokens, out_tokens, num_accepted, ws, kv_len=None,
+                          stats=None, stream=None):
+    """spec_verify_greedy, then kv_len[b] += n + 1 and the stats counters, in the kernel."""
+    B, k1, V = logits.shape
+    st = load().spec_verify_greedy_kv(_ptr(logits), _dtype(logits), _ptr(draft_tokens), B,
+                                      k1 - 1, V, _ptr(out_tokens), _ptr(num_accepted), _ptr(ws),
+                                      ws.numel(), _ptr(kv_len), _ptr(stats), _stream(stream))
+    _check(st, "spec_verify_greedy_kv")
 
 
 def spec_verify_sample_noalloc(logits, draft_probs, draft_tokens, u_accept, u_resample, T,
