@@ -48,6 +48,12 @@ void spec_verify_debug_draw_split(int G);
  * of range values are ignored.  A process-wide setting read at launch time. */
 void spec_verify_debug_fused_tuning(int defer_mode, int pad_kib);
 
+/* Fix the row stream's vocabulary split G (1, 2, 4, 8 or 16 CTAs per row) and
+ * threads per CTA (128, 256 or 512) on the two-kernel path; 0 restores the
+ * automatic choice of either; other values are ignored.  A process-wide setting
+ * read at launch time, for tuning. */
+void spec_verify_debug_rows_split(int G, int nt);
+
 /* The first stage of the row-skipping path alone: resets the per-sequence stop
  * rows in `ws` and runs the position-major row stream, leaving the row records
  * that spec_verify_finish reads (as spec_verify_rows does for the two-kernel

@@ -2206,11 +2206,13 @@ static sv_status launch_fused(bool sampled, const void* logits, sv_dtype dt, con
                           B, k, V, a.c, a.c2, stream);
 }
 
-// Vocabulary split of the per-row kernel: enough CTAs to give every SM about
-// four, while keeping each CTA's slice at 512 16-byte vectors (8 KiB) or more.
+// Vocabulary split of the per-row kernel: rows are split over a cluster only
+// while there are fewer than two CTAs per SM (the cluster barriers and the
+// DSMEM merge cost more than the imbalance of whole rows beyond that), and each
+// CTA keeps at least 512 16-byte vectors (8 KiB) of its row.
 static int rows_split(long long R, long long nvec_row, int sms) {
     int G = 1;
-    while (G < 16 && R * G < 4LL * sms && nvec_row / (2LL * G) >= 512) G *= 2;
+    while (G < 16 && R * G < 2LL * sms && nvec_row / (2LL * G) >= 512) G *= 2;
     return G;
 }
 
@@ -2224,6 +2226,10 @@ static int rows_threads(long long ctas, long long nvec_cta, int sms) {
 
 // With `skip`: one 512-thread CTA per row, rows position-major, stop[] reset
 // first (a memset on the same stream).
+// Tuning hook (spec_verify_debug_rows_split): a fixed vocabulary split and
+// thread count for the row stream of the two-kernel path (0: automatic).
+static std::atomic<int> g_force_rows_G{0}, g_force_rows_nt{0};
+
 static sv_status launch_rows(bool sampled, const void* logits, sv_dtype dt, const float* q,
                              const int32_t* x, const float* ua, float T, int B, int k, int V,
                              void* ws, cudaStream_t stream, int sms, bool skip) {
@@ -2246,7 +2252,9 @@ static sv_status launch_rows(bool sampled, const void* logits, sv_dtype dt, cons
     const int esz = dt == SV_BF16 ? 2 : 4;
     const long long nvec_row = ((long long)V * esz + 15) / 16;
     a.G = skip ? 1 : rows_split(R, nvec_row, sms);
-    const int nt = skip ? 512 : rows_threads(R * a.G, nvec_row / a.G, sms);
+    int nt = skip ? 512 : rows_threads(R * a.G, nvec_row / a.G, sms);
+    if (!skip && g_force_rows_G.load()) a.G = g_force_rows_G.load();
+    if (!skip && g_force_rows_nt.load()) nt = g_force_rows_nt.load();
     if (skip && cudaMemsetAsync(a.stop, 0xFF, (size_t)B * sizeof(uint32_t), stream) != cudaSuccess)
         return SV_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
@@ -2607,6 +2615,13 @@ int spec_verify_debug_path(sv_mode mode, int B, int V, sv_dtype dtype) {
 void spec_verify_debug_fused_tuning(int defer_mode, int pad_kib) {
     if (defer_mode >= 0 && defer_mode <= 2) g_fused_defer.store(defer_mode);
     if (pad_kib >= 0 && pad_kib <= 160) g_fused_pad.store(pad_kib);
+}
+
+// Tuning hook: the row stream's split (G in 1..16, a power of two) and threads
+// per CTA (128, 256 or 512) on the two-kernel path; 0 for the automatic choice.
+void spec_verify_debug_rows_split(int G, int nt) {
+    if (G == 0 || G == 1 || G == 2 || G == 4 || G == 8 || G == 16) g_force_rows_G.store(G);
+    if (nt == 0 || nt == 128 || nt == 256 || nt == 512) g_force_rows_nt.store(nt);
 }
 
 // Tuning hook: a fixed cluster size (1, 2, 4, 8 or 16) for the draw kernel, 0

@@ -64,6 +64,8 @@ def load():
     lib.spec_verify_finish.restype = I
     lib.spec_verify_debug_fused_tuning.argtypes = [I, I]
     lib.spec_verify_debug_fused_tuning.restype = None
+    lib.spec_verify_debug_rows_split.argtypes = [I, I]
+    lib.spec_verify_debug_rows_split.restype = None
     lib.spec_verify_debug_draw_split.argtypes = [I]
     lib.spec_verify_debug_draw_split.restype = None
     lib.spec_verify_debug_rows_skip.argtypes = [I, P, I, P, P, P, F, I, I, I, P, Z, P]
@@ -207,6 +209,11 @@ def spec_verify_rows(mode, logits, draft_probs, draft_tokens, T, ws, stream=None
 def debug_fused_tuning(defer_mode: int, pad_kib: int):
     """Tuning hook of the fused kernel (precise-draw deferral, shared-memory floor)."""
     load().spec_verify_debug_fused_tuning(int(defer_mode), int(pad_kib))
+
+
+def debug_rows_split(G: int, nt: int):
+    """Tuning hook: the row stream's split and threads per CTA (0 = automatic)."""
+    load().spec_verify_debug_rows_split(int(G), int(nt))
 
 
 def debug_draw_split(G: int):
