@@ -68,7 +68,7 @@ sv_status spec_verify_debug_rows_skip(sv_mode mode, const void* logits, sv_dtype
 /* Writes to *out (a DEVICE float) the largest relative error of the
  * ex2.approx.ftz.f32 instruction against the float-float 2^a over every float a
  * in [a0, a1], -126 <= a0 <= a1 <= 0.  The fast draw's error bound assumes this
- * is below 2^-21.  Synchronises `stream`.  SV_ERR_INVALID_ARG for a bad range
+ * is at most 2^-22 over [-126, 0] (a test checks it exhaustively).  Synchronises `stream`.  SV_ERR_INVALID_ARG for a bad range
  * or a null pointer. */
 sv_status spec_verify_debug_ex2_error(float a0, float a1, float* out, cudaStream_t stream);
 

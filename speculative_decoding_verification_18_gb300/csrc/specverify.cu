@@ -286,18 +286,22 @@ constexpr int kChunk = 8;           // contiguous elements per draw work item
 constexpr int kSliceMax = 163840;   // largest slice of a row one CTA draws from
 
 // Error model of the fast fp32 draw.  ex2.approx.ftz.f32 is taken to be within
-// kEx2RelErr of 2^a (relative) on [-126, 0]; a test measures its worst case
-// exhaustively on that range and checks it is at least 2x below this bound.
-constexpr float kEx2RelErr = 4.76837158e-07f;  // 2^-21
-// Relative error bound of p = ex2(a)/S per element, apart from the argument
-// term: ex2 itself; the normaliser's ex2 errors and the three roundings deep
-// pairwise sums of its chunks (the chunk sums are then carried to 2^-47); the
-// roundings of 1/S (two: the reciprocal and the dropped low part) and of
-// e * (1/S).
-constexpr float kFastE0 = 2.0f * kEx2RelErr + 6.0f * 5.96046448e-08f;
-// The fp32 argument a = fl(fl(l - m) * fl(log2(e)/T)) is off by at most
-// 3 * 2^-24 * |a|, i.e. 2^a by a relative 3 * 2^-24 * ln2 * |a|.
-constexpr float kFastKappa = 3.0f * 5.96046448e-08f * 0.693147181f;
+// kEx2RelErr of 2^a (relative) on [-126, 0]: a test measures its worst case
+// exhaustively over every float of that range (on GB300: 1.715e-7, 2^-22.48)
+// and requires it to be at most this value.
+constexpr float kEx2RelErr = 2.38418579e-07f;  // 2^-22
+// Relative error bound of p = y/S per element, apart from the exponent term:
+// y = ex2(a) corrected for the exponent's product roundings (ex2 itself and the
+// correction's rounding); the normaliser's ex2 errors, corrections and the
+// three roundings deep pairwise sums of its chunks (the chunk sums are then
+// carried to 2^-47); the roundings of 1/S (two: the reciprocal and the dropped
+// low part) and of y * (1/S).
+constexpr float kFastE0 = 2.0f * kEx2RelErr + 7.0f * 5.96046448e-08f;
+// The exponent a = (l - m) * log2(e)/T: the product's rounding and that of
+// log2(e)/T are recovered exactly (an FMA and the low part of log2(e)/T) and
+// corrected for; the difference l - m keeps one rounding, 2^-24 * |a|, i.e. a
+// relative 2^-24 * ln2 * |a| in 2^a.
+constexpr float kFastKappa = 5.96046448e-08f * 0.693147181f;
 // Elements with p < q (1 - kRelSlack) for sure weigh exactly 0 in both passes.
 constexpr float kRelSlack = 4.0e-5f;
 
@@ -539,7 +543,8 @@ struct DrawCtx {
     const float* qrow;
     int V;
     bool residual;
-    float m, c;     // row max (raw logit), log2(e)/T in float
+    float m, c;     // row max (raw logit), log2(e)/T in float (its high part)
+    float clo;      // low part of log2(e)/T
     ff c2;          // log2(e)/T in float-float
     float u;
     long long c0;
@@ -641,39 +646,50 @@ __device__ __forceinline__ void raw_unpack_q(const RawQ& r, float* f) {
     Elt<float>::unpack(r.v[1], f + 4);
 }
 
-// Exponents a = (l - m) * log2(e)/T of one chunk, rounded the same way
-// wherever they are formed.
-__device__ __forceinline__ void fast_exponents(const float* l, float m, float c, float* a) {
+// 2^((l - m) * log2(e)/T) for one chunk in fp32, formed the same way wherever
+// it is formed: a = fl(d * c_hi) with d = fl(l - m); the product's rounding
+// error (exact, by an FMA) plus d * c_lo corrects ex2(a) to first order.  Also
+// |a| for the error bound.  y = 0 for l = -inf (and below 2^-126, flushed).
+__device__ __forceinline__ void fast_y(const float* l, float m, float chi, float clo, float* y,
+                                       float* absa) {
 #pragma unroll
-    for (int e = 0; e < kChunk; ++e) a[e] = __fmul_rn(__fsub_rn(l[e], m), c);
-}
-
-// The exponents of chunk ci: from the cache when there is one, else formed
-// from the logits (identical values either way).
-template <typename DT>
-__device__ __forceinline__ void chunk_exponents(const DrawCtx<DT>& d, int ci, const float* l,
-                                                float* a) {
-    if (d.acache) {
-        load8(d.acache + (size_t)ci * kChunk, a);
-    } else {
-        fast_exponents(l, d.m, d.c, a);
+    for (int e = 0; e < kChunk; ++e) {
+        const float d = __fsub_rn(l[e], m);
+        const float a = __fmul_rn(d, chi);
+        float err = __fmaf_rn(d, chi, -a);  // exact
+        err = __fmaf_rn(d, clo, err);
+        const float y0 = ex2_approx(a);
+        y[e] = y0 > 0.0f ? __fmaf_rn(y0, __fmul_rn(err, 0.693147181f), y0) : 0.0f;
+        absa[e] = fabsf(a);
     }
 }
 
-// Weights of one chunk in fp32 (p = ex2(a) / S, or max(0, p - q) when RES)
-// with their error-bound contribution added to *bd.
+// The corrected exponentials of chunk ci: from the cache when there is one,
+// else formed from the logits (identical values either way).
+template <typename DT>
+__device__ __forceinline__ void chunk_y(const DrawCtx<DT>& d, int ci, const float* l, float* y) {
+    if (d.acache) {
+        load8(d.acache + (size_t)ci * kChunk, y);
+    } else {
+        float unused[kChunk];
+        fast_y(l, d.m, d.c, d.clo, y, unused);
+    }
+}
+
+// Weights of one chunk in fp32 (p = y / S, or max(0, p - q) when RES), and the
+// sum of p over the elements the bound counts added to *relp.
 template <bool RES>
-__device__ __forceinline__ void fast_weights(const float* a, const float* q, float inv, float* w,
-                                             float* bd) {
+__device__ __forceinline__ void fast_weights(const float* y, const float* q, float inv, float* w,
+                                             float* relp) {
     float b = 0.0f;
 #pragma unroll
     for (int e = 0; e < kChunk; ++e) {
-        const float p = __fmul_rn(ex2_approx(a[e]), inv);
+        const float p = __fmul_rn(y[e], inv);
         w[e] = RES ? fmaxf(__fsub_rn(p, q[e]), 0.0f) : p;
         const bool rel = !RES || p >= q[e] * (1.0f - kRelSlack);
-        b = fmaf(rel ? p : 0.0f, fmaf(kFastKappa, fabsf(a[e]), kFastE0), b);
+        b += rel ? p : 0.0f;
     }
-    *bd += b;
+    *relp += b;
 }
 
 // Fixed-point value of a chunk: its weights summed left to right in fp32, the
@@ -783,16 +799,12 @@ __device__ bool draw_fast(cg::cluster_group& cluster, DrawShared& sh, const Draw
         for (int u = 0; u < UA; ++u) {
             const int ci = base + u * kThreads;
             if (ci >= d.mych) break;
-            float l[kChunk], a[kChunk];
+            float l[kChunk], y[kChunk], absa[kChunk];
             raw_unpack(raw[u], l);
-            fast_exponents(l, d.m, d.c, a);
-            if (d.acache) store8(d.acache + (size_t)ci * kChunk, a);
-            float y[kChunk];
+            fast_y(l, d.m, d.c, d.clo, y, absa);
+            if (d.acache) store8(d.acache + (size_t)ci * kChunk, y);
 #pragma unroll
-            for (int e = 0; e < kChunk; ++e) {
-                y[e] = ex2_approx(a[e]);
-                accA = fmaf(y[e], fabsf(a[e]), accA);
-            }
+            for (int e = 0; e < kChunk; ++e) accA = fmaf(y[e], absa[e], accA);
             const float s = __fadd_rn(__fadd_rn(__fadd_rn(y[0], y[1]), __fadd_rn(y[2], y[3])),
                                       __fadd_rn(__fadd_rn(y[4], y[5]), __fadd_rn(y[6], y[7])));
             const ff t = two_sum(accS.hi, s);
@@ -803,9 +815,9 @@ __device__ bool draw_fast(cg::cluster_group& cluster, DrawShared& sh, const Draw
     const ff S = cluster_sum_ff(cluster, sh, sh.xS[0], accS, d.rank, d.G, sh.xA, accA);
     const float inv = __frcp_rn(S.hi);
 
-    // Pass B: fixed-point chunk values, block totals, the error bound.
+    // Pass B: fixed-point chunk values, block totals, the mass the bound counts.
     unsigned long long tacc = 0;
-    float bound = 0.0f;
+    float relp = 0.0f;
     // Two blocks per warp in flight: the q chunks, and the logits when they
     // are not cached.
     constexpr int UB = 2;
@@ -827,11 +839,11 @@ __device__ bool draw_fast(cg::cluster_group& cluster, DrawShared& sh, const Draw
             const int ci = base + lane;
             unsigned long long W = 0;
             if (ci < d.mych) {
-                float q[kChunk] = {}, l[kChunk] = {}, a[kChunk], w[kChunk];
+                float q[kChunk] = {}, l[kChunk] = {}, y[kChunk], w[kChunk];
                 if (RES) raw_unpack_q(rq[u], q);
                 if (!d.acache) raw_unpack(rl[u], l);
-                chunk_exponents(d, ci, l, a);
-                fast_weights<RES>(a, q, inv, w, &bound);
+                chunk_y(d, ci, l, y);
+                fast_weights<RES>(y, q, inv, w, &relp);
                 W = fast_chunk_value(w);
                 // the cache now keeps the weights, for the owner's search
                 if (d.acache) store8(d.acache + (size_t)ci * kChunk, w);
@@ -843,18 +855,19 @@ __device__ bool draw_fast(cg::cluster_group& cluster, DrawShared& sh, const Draw
             }
         }
     }
-    cluster_prefix(cluster, sh, sh.xW[0], sh.xD, tacc, bound, d.rank, d.G);
+    cluster_prefix(cluster, sh, sh.xW[0], sh.xD, tacc, relp, d.rank, d.G);
     const unsigned long long prefix = sh.prefix, total = sh.total, mytot = sh.mytot;
-    // Bound in fixed-point units: the element bounds; for the residual, the
-    // argument roundings inside S (kappa * sum_j p_j |a_j|, times the mass of
-    // the counted elements, at most about 1; a common factor of all p, so
-    // irrelevant to the draw from p), both with a margin for their own fp32
-    // sums; the roundings of p - q and of the sequential chunk sums (8 units of
-    // 2^-24 of the total); one unit of truncation per chunk value plus two for
-    // the bin edges.
+    // Bound in fixed-point units: kFastE0 times the mass of the counted
+    // elements (sum of p with p >= q (1 - kRelSlack), or all of p); the
+    // exponents' roundings, kappa * sum_j p_j |a_j| over every element, once for
+    // the elements' own exponents and once (times the counted mass, at most
+    // about 1) for those inside S; margins for their own fp32 sums; the
+    // roundings of p - q and of the sequential chunk sums (8 units of 2^-24 of
+    // the total); one unit of truncation per chunk value plus two for the bin
+    // edges.
     const long long nch = ((long long)d.V + kChunk - 1) / kChunk;
-    const float sarg = RES ? kFastKappa * sh.A_tot * inv * 1.0009765625f : 0.0f;
-    float dunits = (sh.D_tot + sarg) * 1.0009765625f * 1.152921504606847e18f +
+    const float kpa = kFastKappa * sh.A_tot * inv * 1.0009765625f;  // kappa * sum p |a|
+    float dunits = (kFastE0 * sh.D_tot + 2.0f * kpa) * 1.0009765625f * 1.152921504606847e18f +
                    (float)total * (8.0f * 5.96046448e-08f) + (float)nch + 4.0f;
     dunits = fminf(dunits, 1.0e18f);  // beyond any total: certifies nothing
     const unsigned long long D = (unsigned long long)dunits + 1ull;
@@ -875,11 +888,11 @@ __device__ bool draw_fast(cg::cluster_group& cluster, DrawShared& sh, const Draw
                 if (d.acache) {
                     load8(d.acache + (size_t)ci * kChunk, w);
                 } else {
-                    float l[kChunk], q[kChunk], a[kChunk], unused = 0.0f;
+                    float l[kChunk], q[kChunk], y[kChunk], absa[kChunk], unused = 0.0f;
                     load_l(d, ci, l);
                     load_q(d, ci, RES, q);
-                    fast_exponents(l, d.m, d.c, a);
-                    fast_weights<RES>(a, q, inv, w, &unused);
+                    fast_y(l, d.m, d.c, d.clo, y, absa);
+                    fast_weights<RES>(y, q, inv, w, &unused);
                 }
                 W = fast_chunk_value(w);
             }
@@ -1140,7 +1153,9 @@ __device__ __forceinline__ DrawCtx<DT> make_draw_ctx(unsigned char* dyn, int lev
     d.V = V;
     d.residual = residual;
     d.m = m;
-    d.c = c;
+    d.c = c2.hi;
+    d.clo = c2.lo;
+    (void)c;
     d.c2 = c2;
     d.u = u;
     const long long nch = ((long long)V + kChunk - 1) / kChunk;

@@ -216,9 +216,9 @@ def test_ffexp_accuracy():
 
 
 def test_ex2_approx_error_within_the_fast_draw_bound():
-    """The fast draw's error bound takes ex2.approx.ftz.f32 to be within 2^-21 of
-    2^a; measured exhaustively over every float in [-126, 0] it must be at least
-    twice better."""
+    """The fast draw's error bound takes ex2.approx.ftz.f32 to be within 2^-22 of
+    2^a (relative); measured exhaustively over every float in [-126, 0] against
+    the float-float exponential it must be no worse (GB300: 1.715e-7)."""
     from speculative_decoding_verification_18_gb300 import specverify as sv
     worst = sv.debug_ex2_error(-126.0, 0.0)
     assert 0.0 < worst <= 2.0 ** -22, worst
