@@ -54,6 +54,10 @@ void spec_verify_debug_fused_tuning(int defer_mode, int pad_kib);
  * read at launch time, for tuning. */
 void spec_verify_debug_rows_split(int G, int nt);
 
+/* Fix the cluster size of the precise-draw kernel of large batches to G in
+ * {1, 2, 4, 8, 16}; 0 restores the default.  For tuning. */
+void spec_verify_debug_precise_split(int G);
+
 /* The first stage of the row-skipping path alone: resets the per-sequence stop
  * rows in `ws` and runs the position-major row stream, leaving the row records
  * that spec_verify_finish reads (as spec_verify_rows does for the two-kernel

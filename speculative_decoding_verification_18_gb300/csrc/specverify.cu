@@ -1810,9 +1810,9 @@ __global__ void __launch_bounds__(kThreads, 2) sv_finish_sample_kernel(FinishArg
 }
 
 // The precise draws of a large batch, left by sv_finish_sample_kernel in the
-// workspace list: persistent clusters of kMaxG CTAs, cluster c taking entries
-// c, c + clusters, ...  Each draw is the precise pass of the finish kernel over
-// a slice of V / kMaxG elements per CTA.
+// workspace list: persistent clusters of G CTAs (as many as fit at once),
+// cluster c taking entries c, c + clusters, ...  Each draw is the precise pass
+// of the finish kernel over a slice of V / G elements per CTA.
 struct PreciseArgs {
     const void* logits;
     const float* q;
@@ -1823,7 +1823,7 @@ struct PreciseArgs {
     const uint32_t* plist;
     uint32_t* seqstat;
     int32_t* out;
-    int B, k, V;
+    int B, k, V, G;
     int draw_level;
     float c;
     ff c2;
@@ -1834,7 +1834,7 @@ __global__ void __launch_bounds__(kThreads, 2) sv_precise_kernel(PreciseArgs a) 
     extern __shared__ __align__(16) unsigned char dyn[];
     __shared__ DrawShared ds;
     cg::cluster_group cluster = cg::this_cluster();
-    constexpr int G = kMaxG;
+    const int G = a.G;
     const int tid = threadIdx.x;
     const int rank = blockIdx.x % G, cid = blockIdx.x / G, ncl = gridDim.x / G;
     const int k = a.k, V = a.V;
@@ -2111,6 +2111,14 @@ static int wave_rows(int B, int k, int V, int esz) {
 // limits how many of its CTAs share an SM.
 static std::atomic<int> g_fused_defer{0};
 static std::atomic<int> g_fused_pad{0};
+// Cluster size of sv_precise_kernel, and its tuning hook
+// (spec_verify_debug_precise_split; 0: this default).  Four CTAs per draw:
+// each draw's chain of barriers and single-warp search costs about the same at
+// any size, so more clusters at once (76 of 4 against 14 of 16 on GB300)
+// finish a batch's precise draws sooner (measured on B=256, V=151936: the
+// draws take 157 us with clusters of 4, 192 us with 16, 172 with 8).
+constexpr int kPreciseG = 4;
+static std::atomic<int> g_force_precise_split{0};
 
 static sv_status launch_precise(const void* logits, sv_dtype dt, const float* q, const float* ur,
                                 const RowRec* rows, const int32_t* nacc,
@@ -2134,20 +2142,21 @@ static sv_status launch_precise(const void* logits, sv_dtype dt, const float* q,
     pa.B = B;
     pa.k = k;
     pa.V = V;
-    pa.draw_level = draw_level(V, kMaxG);
+    pa.G = g_force_precise_split.load() ? g_force_precise_split.load() : kPreciseG;
+    pa.draw_level = draw_level(V, pa.G);
     pa.c = c;
     pa.c2 = c2;
-    const size_t psmem = draw_smem_bytes(V, kMaxG, pa.draw_level);
+    const size_t psmem = draw_smem_bytes(V, pa.G, pa.draw_level);
     if (psmem > kDynSmemMax) return SV_ERR_UNSUPPORTED;
-    int ncl = resident_clusters(kMaxG);
+    int ncl = resident_clusters(pa.G);
     if (ncl <= 0) ncl = 8;
     if (ncl > B) ncl = B;
     cudaLaunchConfig_t pc = {};
-    pc.gridDim = dim3((unsigned)(ncl * kMaxG), 1, 1);
+    pc.gridDim = dim3((unsigned)(ncl * pa.G), 1, 1);
     pc.blockDim = dim3(kThreads, 1, 1);
     pc.dynamicSmemBytes = psmem;
     pc.stream = stream;
-    cudaLaunchAttribute pattr[2] = {cluster_attr(kMaxG), pdl};
+    cudaLaunchAttribute pattr[2] = {cluster_attr(pa.G), pdl};
     pc.attrs = pattr;
     pc.numAttrs = 2;
     e = dt == SV_BF16 ? cudaLaunchKernelEx(&pc, sv_precise_kernel<__nv_bfloat16>, pa)
@@ -2623,6 +2632,12 @@ int spec_verify_debug_path(sv_mode mode, int B, int V, sv_dtype dtype) {
     if (device_setup(&sms) != SV_OK) return -1;
     if (B < 1 || V < 1 || (dtype != SV_BF16 && dtype != SV_F32)) return -1;
     return (int)choose_path(mode == SV_MODE_SAMPLE, B, V, dtype == SV_BF16 ? 2 : 4, sms);
+}
+
+// Tuning hook: the cluster size of the precise-draw kernel (1, 2, 4, 8 or 16;
+// 0 for the default).
+void spec_verify_debug_precise_split(int G) {
+    if (G == 0 || G == 1 || G == 2 || G == 4 || G == 8 || G == 16) g_force_precise_split.store(G);
 }
 
 // Tuning hook: deferral of the fused kernel's precise draws and its minimum

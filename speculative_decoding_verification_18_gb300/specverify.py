@@ -66,6 +66,8 @@ def load():
     lib.spec_verify_debug_fused_tuning.restype = None
     lib.spec_verify_debug_rows_split.argtypes = [I, I]
     lib.spec_verify_debug_rows_split.restype = None
+    lib.spec_verify_debug_precise_split.argtypes = [I]
+    lib.spec_verify_debug_precise_split.restype = None
     lib.spec_verify_debug_draw_split.argtypes = [I]
     lib.spec_verify_debug_draw_split.restype = None
     lib.spec_verify_debug_rows_skip.argtypes = [I, P, I, P, P, P, F, I, I, I, P, Z, P]
@@ -214,6 +216,11 @@ def debug_fused_tuning(defer_mode: int, pad_kib: int):
 def debug_rows_split(G: int, nt: int):
     """Tuning hook: the row stream's split and threads per CTA (0 = automatic)."""
     load().spec_verify_debug_rows_split(int(G), int(nt))
+
+
+def debug_precise_split(G: int):
+    """Tuning hook: the precise-draw kernel's cluster size (0 = default)."""
+    load().spec_verify_debug_precise_split(int(G))
 
 
 def debug_draw_split(G: int):
