@@ -21,7 +21,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 SRC = os.path.join(HERE, "oracle.c")
 LIB = os.path.join(HERE, "liboracle.so")
 
-SAMPLE, GREEDY, SAMPLE_BUGGY = 0, 1, 2
+SAMPLE, GREEDY, SAMPLE_BUGGY, MATCH = 0, 1, 2, 3
 F_BAD, F_DEGENERATE, F_OVERFLOW = 1, 2, 4
 
 _lib = None
@@ -141,8 +141,9 @@ def verify_batch(mode, logits, dtype: str, q, x, ua, ur, T, nthreads: int = 0) -
     """Batch verify over inputs in the device layouts.
 
     logits: [B, k+1, V] uint16 bf16 bit patterns (dtype "bf16") or float32 ("f32");
-    q: [B, k, V] float32 or None (greedy); x: [B, k] int32; ua: [B, k] float32;
-    ur: [B] float32.
+    q: [B, k, V] float32 or None (greedy, sample-and-match); x: [B, k] int32;
+    ua: [B, k] float32; ur: [B] float32 (sample-and-match: the draws at positions
+    0..k-1 and k).
     """
     B, k1, V = logits.shape
     k = k1 - 1
@@ -155,7 +156,7 @@ def verify_batch(mode, logits, dtype: str, q, x, ua, ur, T, nthreads: int = 0) -
     else:
         raise ValueError(dtype)
     greedy = mode == GREEDY
-    qq = None if greedy else np.ascontiguousarray(q, dtype=np.float32)
+    qq = np.ascontiguousarray(q, dtype=np.float32) if mode in (SAMPLE, SAMPLE_BUGGY) else None
     x = np.ascontiguousarray(x, dtype=np.int32)
     uu = None if greedy else np.ascontiguousarray(ua, dtype=np.float32)
     rr = None if greedy else np.ascontiguousarray(ur, dtype=np.float32)

@@ -22,7 +22,7 @@ from fractions import Fraction
 
 import numpy as np
 
-from . import GREEDY, SAMPLE, draw_cdf, verify_seq
+from . import GREEDY, MATCH, SAMPLE, draw_cdf, verify_seq
 
 
 def _cells(bounds):
@@ -85,6 +85,39 @@ def outcome_distribution(mode, logits, q, T=1.0):
                 res = verify_seq(mode, logits, q, x, ua, 0.5 * (a + b), T)
                 key = (tuple(int(t) for t in res.out), res.n)
                 dist[key] = dist.get(key, Fraction(0)) + wx * wu * (Fraction(b) - Fraction(a))
+    return dist
+
+
+def match_outcome_distribution(logits, q, T=1.0):
+    """Exact distribution of (out tokens, n) under sample-and-match for one
+    sequence whose drafts x_i ~ q_i ([DEE] §"A regra de amostragem por
+    rejeição", the simpler exact scheme).  The uniform of each position's draw
+    ranges over the cells of that row's bins, so every outcome is enumerated with
+    its exact probability.  Same layout and result type as outcome_distribution.
+    """
+    logits = np.asarray(logits, dtype=np.float64)
+    q = np.asarray(q, dtype=np.float64)
+    k1, V = logits.shape
+    k = k1 - 1
+    cells = [_cells(draw_cdf(logits[i], None, T).tolist()) for i in range(k + 1)]
+    dist = {}
+    for x in itertools.product(range(V), repeat=k):
+        wx = Fraction(1)
+        for i, xi in enumerate(x):
+            wx *= Fraction(float(q[i, xi]))
+        if wx == 0:
+            continue
+        for ucells in itertools.product(*cells):
+            wu = Fraction(1)
+            u = np.empty(k + 1)
+            for i, (a, b) in enumerate(ucells):
+                wu *= Fraction(b) - Fraction(a)
+                u[i] = 0.5 * (a + b)
+            res = verify_seq(MATCH, logits, None, x, u[:k], u[k], T)
+            if res.n < 0:
+                raise RuntimeError("oracle marked a valid enumeration input invalid")
+            key = (tuple(int(t) for t in res.out), res.n)
+            dist[key] = dist.get(key, Fraction(0)) + wx * wu
     return dist
 
 

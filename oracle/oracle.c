@@ -164,10 +164,72 @@ static void mark_invalid(int k, int32_t* out, int32_t* n_acc, int32_t* flags) {
     if (flags) *flags |= ORC_F_BAD;
 }
 
+/* Sample-and-match ([DEE] §"A regra de amostragem por rejeição", the simpler
+ * exact scheme some engines use): at positions i = 0, 1, .. draw y_i from p_i
+ * (the draw of step 4, with ua[i], or ur at position k) and keep the draft token
+ * while y_i == x_i; the first position where they differ, or position k, emits
+ * y_i.  Every emitted token is a draw from p, so the output is exact; a draft
+ * survives position i with probability sum_v p_i(v) q_i(v).  A row, token or
+ * uniform the scan reaches that is invalid invalidates the sequence.
+ * *draw_lo / *draw_hi: the bin of the emitted draw. */
+static void verify_match(const double* logits, const int32_t* x, const double* ua, double ur,
+                         double T, int k, int V, int32_t* out, int32_t* n_acc,
+                         double* draw_lo, double* draw_hi, int32_t* flags) {
+    double* w = (double*)malloc(sizeof(double) * (size_t)V);
+    int n = k, token = -1;
+    for (int i = 0; i <= k; ++i) {
+        const double* li = logits + (size_t)i * V;
+        double m, S;
+        int32_t am;
+        if (orc_row_stats(li, T, V, &m, &S, &am)) {
+            free(w);
+            mark_invalid(k, out, n_acc, flags);
+            return;
+        }
+        if (i < k && (x[i] < 0 || x[i] >= V)) {
+            free(w);
+            mark_invalid(k, out, n_acc, flags);
+            return;
+        }
+        const double u = i < k ? ua[i] : ur;
+        if (!(u >= 0.0 && u < 1.0)) {
+            free(w);
+            mark_invalid(k, out, n_acc, flags);
+            return;
+        }
+        draw_weights(li, NULL, T, m, S, V, w);
+        double lo, hi;
+        int ovf;
+        const int y = categorical(w, V, u, &lo, &hi, &ovf);
+        if (ovf && flags) *flags |= ORC_F_OVERFLOW;
+        if (i == k || y != x[i]) {
+            n = i;
+            token = y;
+            if (draw_lo) *draw_lo = lo;
+            if (draw_hi) *draw_hi = hi;
+            break;
+        }
+    }
+    free(w);
+    for (int i = 0; i < n; ++i) out[i] = x[i];
+    out[n] = token;
+    for (int i = n + 1; i <= k; ++i) out[i] = -1;
+    *n_acc = n;
+}
+
 void orc_verify_seq(int mode, const double* logits, const double* q, const int32_t* x,
                     const double* ua, double ur, double T, int k, int V,
                     int32_t* out, int32_t* n_acc, double* thr, double* draw_lo,
                     double* draw_hi, int32_t* flags) {
+    if (mode == ORC_MATCH) {
+        if (flags) *flags = 0;
+        if (thr)
+            for (int i = 0; i < k; ++i) thr[i] = NAN;
+        if (draw_lo) *draw_lo = NAN;
+        if (draw_hi) *draw_hi = NAN;
+        verify_match(logits, x, ua, ur, T, k, V, out, n_acc, draw_lo, draw_hi, flags);
+        return;
+    }
     const int greedy = (mode == ORC_GREEDY);
     const double Tr = greedy ? 1.0 : T;
     if (flags) *flags = 0;
@@ -270,7 +332,9 @@ int orc_verify_batch(int mode, const void* logits, int dtype, const float* q,
     if (B < 0 || k < 1 || V < 1 || !logits || !x || !out || !n_acc) return -1;
     if (dtype != 0 && dtype != 1) return -1;
     const int greedy = (mode == ORC_GREEDY);
-    if (!greedy && (!q || !ua || !ur)) return -1;
+    const int uses_q = (mode == ORC_SAMPLE || mode == ORC_SAMPLE_BUGGY);
+    if (uses_q && !q) return -1;
+    if (!greedy && (!ua || !ur)) return -1;
     const double Td = greedy ? 1.0 : (double)T;
     const size_t rowsz = (size_t)V;
     const size_t seqsz = (size_t)(k + 1) * rowsz;
@@ -280,7 +344,7 @@ int orc_verify_batch(int mode, const void* logits, int dtype, const float* q,
 #pragma omp parallel num_threads(nt)
     {
         double* L = (double*)malloc(sizeof(double) * seqsz);
-        double* Qd = greedy ? NULL : (double*)malloc(sizeof(double) * (size_t)k * rowsz);
+        double* Qd = uses_q ? (double*)malloc(sizeof(double) * (size_t)k * rowsz) : NULL;
         double* ua_d = (double*)malloc(sizeof(double) * (size_t)k);
 #pragma omp for schedule(dynamic, 1)
         for (int b = 0; b < B; ++b) {
@@ -292,11 +356,12 @@ int orc_verify_batch(int mode, const void* logits, int dtype, const float* q,
                 const float* src = (const float*)logits + (size_t)b * seqsz;
                 for (size_t j = 0; j < seqsz; ++j) L[j] = (double)src[j];
             }
-            if (!greedy) {
+            if (uses_q) {
                 const float* qs = q + (size_t)b * k * rowsz;
                 for (size_t j = 0; j < (size_t)k * rowsz; ++j) Qd[j] = (double)qs[j];
-                for (int i = 0; i < k; ++i) ua_d[i] = (double)ua[(size_t)b * k + i];
             }
+            if (!greedy)
+                for (int i = 0; i < k; ++i) ua_d[i] = (double)ua[(size_t)b * k + i];
             /* Per-row statistics of every row, for parity of the stats. */
             for (int i = 0; i <= k; ++i) {
                 size_t r = (size_t)b * (k + 1) + i;
@@ -311,7 +376,7 @@ int orc_verify_batch(int mode, const void* logits, int dtype, const float* q,
                     int xi = x[(size_t)b * k + i];
                     if (xi >= 0 && xi < V) {
                         if (!bad) px = row_p(L + (size_t)i * rowsz, Td, m, S, xi);
-                        if (!greedy) qx = Qd[(size_t)i * rowsz + xi];
+                        if (uses_q) qx = Qd[(size_t)i * rowsz + xi];
                     }
                 }
                 if (row_px) row_px[r] = px;

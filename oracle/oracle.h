@@ -27,9 +27,13 @@ extern "C" {
 enum {
     ORC_SAMPLE = 0,       /* rejection sampling, [DEE] §"A regra de amostragem por rejeição" */
     ORC_GREEDY = 1,       /* accept while draft == argmax, [DEE] same section, last paragraph */
-    ORC_SAMPLE_BUGGY = 2  /* negative control: resample from p instead of the residual,
+    ORC_SAMPLE_BUGGY = 2, /* negative control: resample from p instead of the residual,
                              [DEE] §"A regra de amostragem por rejeição" (the "Júnior" aside),
                              [SD15] §"Why the result is exactly the target model" */
+    ORC_MATCH = 3         /* sample-and-match: draw a target token at every position and keep
+                             the draft's while they agree, [DEE] §"A regra de amostragem por
+                             rejeição", the simpler exact scheme; the draw at position i < k
+                             uses ua[i], the one at position k uses ur; q is not used */
 };
 
 /* Per-sequence flag bits written by the oracle. */

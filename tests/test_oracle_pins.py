@@ -135,6 +135,42 @@ def test_greedy_enumeration(orc):
     assert abs(reach1 - q[0, am[0]]) < 1e-12
 
 
+@pytest.mark.parametrize("k,V", [(1, 3), (2, 4), (2, 5)])
+def test_match_enumeration_reproduces_target(orc, k, V):
+    """Sample-and-match ([DEE] §"A regra de amostragem por rejeição", the simpler
+    exact scheme) is exact too: the emitted token at position i, jointly with
+    reaching i, has probability prod_{j<i} beta_j * p_i(b), where a draft
+    survives position j with probability beta_j = sum_v p_j(v) q_j(v), never
+    more than rejection sampling's sum_v min(p_j(v), q_j(v))."""
+    g = np.random.default_rng(300 + 10 * k + V)
+    for T in (1.0, 0.7):
+        logits, q = _random_case(g, k, V, T)
+        dist = exact.match_outcome_distribution(logits, q, T)
+        marg, en = exact.position_marginals(dist, k, V)
+        p = np.array([softmax64(logits[i], T) for i in range(k + 1)])
+        beta = (p[:k] * q).sum(axis=1)
+        reach = np.concatenate([[1.0], np.cumprod(beta)])
+        assert np.abs(marg - reach[:, None] * p).max() < 1e-12
+        assert abs(en - reach[1:].sum()) < 1e-12
+        assert abs(sum(float(v) for v in dist.values()) - 1.0) < 1e-12
+        assert (beta <= np.minimum(p[:k], q).sum(axis=1) + 1e-15).all()
+
+
+def test_match_toy_acceptance(orc):
+    """On the page's seeded toy, sample-and-match keeps a draft with probability
+    sum_v P[c, v] Q[c, v] = [0.245 0.270 0.321 0.316] per context c (the oracle's
+    enumeration gives exactly that); the page's printed "0.39 to 0.55" does not
+    reproduce from its own setup and is not used as a pin."""
+    P, Q = exact.toy_bigram()
+    beta = (P * Q).sum(axis=1)
+    assert np.allclose(beta, [0.245, 0.270, 0.321, 0.316], atol=5e-4)
+    for c in range(4):
+        logits = np.log(np.stack([P[c], P[c]]))
+        dist = exact.match_outcome_distribution(logits, Q[c][None, :], 1.0)
+        accept = float(sum(pr for (out, n), pr in dist.items() if n >= 1))
+        assert abs(accept - beta[c]) < 1e-12
+
+
 # ---------------------------------------------------------------- the page's toy
 
 def test_toy_alpha_matches_page(orc):
