@@ -127,6 +127,26 @@ sv_status spec_verify_sample(const void* logits, sv_dtype dtype, const float* dr
                              int32_t* out_tokens, int32_t* num_accepted,
                              void* ws, size_t ws_bytes, cudaStream_t stream);
 
+/* Sample-and-match verify ("Decodificação especulativa explicada", §"A regra de
+ * amostragem por rejeição", the simpler exact scheme some engines use): a
+ * target token y_i is drawn from p_i = softmax(l_i / T) at every position, the
+ * draft token kept while y_i == x_i; the first position i < k where they
+ * differ, or position k, emits y_i.  Every emitted token is a draw from p, so
+ * the output is exact, but a draft survives position i only with probability
+ * sum_v p_i(v) q_i(v), never more than spec_verify_sample's acceptance.  The
+ * draft's q is not needed.
+ *   u_draw  [B, k] fp32 in [0, 1): the uniform of the draw at position i < k.
+ *   u_bonus [B] fp32 in [0, 1): the uniform of the draw at position k.
+ *   out_tokens [B, k+1]: y_0..y_n (= the accepted drafts, then the emitted
+ *   draw), -1 after; num_accepted [B] = n, or -1 for an invalid sequence (a bad
+ *   row, draft token or uniform at a position the scan reaches).
+ * The draws are those of spec_verify_sample (certified fp32 pass, float-float
+ * fallback, exact integer prefix sums).  Workspace as for the other calls. */
+sv_status spec_verify_match(const void* logits, sv_dtype dtype, const int32_t* draft_tokens,
+                            const float* u_draw, const float* u_bonus, float T, int B, int k,
+                            int V, int32_t* out_tokens, int32_t* num_accepted, void* ws,
+                            size_t ws_bytes, cudaStream_t stream);
+
 /* Counters a verify can add to (spec_verify_*_kv), for generation loops that
  * keep speculation statistics on the device ("Speculative Decoding" (ch15, LLM
  * serving from scratch), the stats argument of speculative_generate; the

@@ -1860,6 +1860,104 @@ __global__ void __launch_bounds__(kThreads, 2) sv_precise_kernel(PreciseArgs a) 
     }
 }
 
+// ------------------------------------------------------------------ sample-and-match
+
+// Sample-and-match ("Decodificação especulativa explicada", §"A regra de
+// amostragem por rejeição", the simpler exact scheme some engines use): a
+// target token y_i is drawn from p_i at every position and the draft is kept
+// while y_i == x_i; the first position where they differ (or position k)
+// emits y_i.  Here every row's draw runs at once, one cluster per row, after
+// the row stream has left each row's max and validity; out_tokens[b, i]
+// receives y_i, and sv_finish_match_kernel then finds the first mismatch.
+struct MatchArgs {
+    const void* logits;
+    const float* ua;   // u for the draw at positions 0..k-1
+    const float* ur;   // u for the draw at position k
+    const RowRec* rows;
+    int32_t* out;
+    int B, k, V, G;
+    int draw_level, prefetch, force_precise;
+    float c;
+    ff c2;
+};
+
+template <typename DT>
+__global__ void __launch_bounds__(kThreads, 2) sv_match_draw_kernel(MatchArgs a) {
+    extern __shared__ __align__(16) unsigned char dyn[];
+    __shared__ DrawShared ds;
+    __shared__ RowRec rec;
+    __shared__ float s_u;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int tid = threadIdx.x, G = a.G, k = a.k, V = a.V;
+    const long long row = blockIdx.x / G;
+    const int rank = blockIdx.x % G;
+    const int b = (int)(row / (k + 1)), i = (int)(row % (k + 1));
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the row records are complete
+    if (tid == 0) {
+        rec = a.rows[row];
+        s_u = i < k ? a.ua[(long long)b * k + i] : a.ur[b];
+    }
+    __syncthreads();
+    // A bad row or uniform draws nothing (the finish kernel marks the sequence
+    // if its scan reaches the row); every CTA of the cluster sees the same values.
+    if ((rec.flags & (kRowBad | kRowSkipped)) || !(s_u >= 0.0f && s_u < 1.0f)) return;
+    const DT* rowp = static_cast<const DT*>(a.logits) + row * (long long)V;
+    const DrawCtx<DT> dc = make_draw_ctx<DT>(dyn, a.draw_level, a.prefetch != 0, rowp, nullptr,
+                                             false, V, rec.mraw, a.c, a.c2, s_u, rank, G);
+    bool degenerate = false, fallback = false;
+    draw<DT>(cluster, ds, dc, a.force_precise != 0, false, a.out + row, degenerate, fallback);
+}
+
+// One warp per sequence: lanes test positions in parallel (a bad row, a bad
+// draft token, a bad uniform, or the first y_i != x_i, or position k, ends the
+// scan), in the order of the oracle's checks; then the outputs past n are -1.
+__global__ void sv_finish_match_kernel(const int32_t* __restrict__ x,
+                                       const float* __restrict__ ua,
+                                       const float* __restrict__ ur,
+                                       const RowRec* __restrict__ rows,
+                                       uint32_t* __restrict__ seqstat, int B, int k, int V,
+                                       int32_t* __restrict__ out, int32_t* __restrict__ nacc,
+                                       Epilogue ep) {
+    const int wi = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = blockIdx.x * 4 + wi;
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the draws are complete
+    if (b >= B) return;
+    const RowRec* rr = rows + (long long)b * (k + 1);
+    const int32_t* xx = x + (long long)b * k;
+    int32_t* o = out + (long long)b * (k + 1);
+    int first = k, code = 0;  // 1 emit, 2 bad row, 3 bad token, 4 bad uniform
+    for (int base = 0; base <= k; base += 32) {
+        const int i = base + lane;
+        int c = 0;
+        if (i <= k) {
+            const float u = i < k ? ua[(long long)b * k + i] : ur[b];
+            const int xi = i < k ? xx[i] : -1;
+            if (rr[i].flags & (kRowBad | kRowSkipped)) c = 2;
+            else if (i < k && (xi < 0 || xi >= V)) c = 3;
+            else if (!(u >= 0.0f && u < 1.0f)) c = 4;
+            else c = (i == k || o[i] != xi) ? 1 : 0;
+        }
+        const unsigned m = __ballot_sync(0xffffffffu, c != 0);
+        if (m) {  // uniform across the warp
+            const int src = __ffs(m) - 1;
+            first = base + src;
+            code = __shfl_sync(0xffffffffu, c, src);
+            break;
+        }
+    }
+    const bool bad = code != 1;
+    const int n = first;
+    __syncwarp();
+    for (int i = lane; i <= k; i += 32)
+        if (bad || i > n) o[i] = -1;
+    if (lane == 0) {
+        nacc[b] = bad ? -1 : n;
+        seqstat[b] = code == 2 ? SV_DEV_BAD_ROW : code == 3 ? SV_DEV_BAD_TOKEN
+                   : code == 4 ? SV_DEV_BAD_UNIFORM : 0u;
+        commit_sequence(ep, b, bad ? -1 : n, k);
+    }
+}
+
 // ------------------------------------------------------------------ debug kernel
 
 __global__ void sv_debug_ffexp_kernel(const float* l, float m, int n, ff c2, double* out) {
@@ -1988,6 +2086,8 @@ static sv_status device_setup(int* sms) {
             SV_TRY(cluster_attrs(sv_finish_sample_kernel<__nv_bfloat16>, true));
             SV_TRY(cluster_attrs(sv_finish_sample_kernel<float>, true));
             SV_TRY(cluster_attrs(sv_precise_kernel<__nv_bfloat16>, true));
+            SV_TRY(cluster_attrs(sv_match_draw_kernel<__nv_bfloat16>, true));
+            SV_TRY(cluster_attrs(sv_match_draw_kernel<float>, true));
             SV_TRY(cluster_attrs(sv_precise_kernel<float>, true));
             SV_TRY(cluster_attrs(sv_rows_kernel<__nv_bfloat16, true, 128>, false));
             SV_TRY(cluster_attrs(sv_rows_kernel<__nv_bfloat16, true, 256>, false));
@@ -2392,6 +2492,67 @@ static sv_status launch_finish(bool sampled, const void* logits, sv_dtype dt, co
                           k, V, a.c, a.c2, stream);
 }
 
+// Sample-and-match: the row stream (greedy statistics: max, argmax, validity),
+// one draw per row (a cluster of G CTAs per row, G by the row stream's rule for
+// the draw: rows split only while there are fewer than two CTAs per SM and each
+// keeps 2048 elements), then the scan.  Both later kernels are programmatic
+// dependents of the one before.
+static sv_status launch_match(const void* logits, sv_dtype dt, const int32_t* x, const float* ua,
+                              const float* ur, float T, int B, int k, int V, int32_t* out,
+                              int32_t* nacc, void* ws, cudaStream_t stream, int sms,
+                              Epilogue ep) {
+    sv_status st = launch_rows(false, logits, dt, nullptr, x, nullptr, 1.0f, B, k, V, ws, stream,
+                               sms, false);
+    if (st != SV_OK) return st;
+    const RowRec* rows =
+        reinterpret_cast<const RowRec*>(static_cast<char*>(ws) + ws_rows_offset());
+    uint32_t* seqstat = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + ws_seq_offset(B, k));
+    const long long R = (long long)B * (k + 1);
+    MatchArgs a;
+    a.logits = logits;
+    a.ua = ua;
+    a.ur = ur;
+    a.rows = rows;
+    a.out = out;
+    a.B = B;
+    a.k = k;
+    a.V = V;
+    int G = 1;
+    while (G < 16 && R * G < 2LL * sms && V / (2 * G) >= 2048) G *= 2;
+    while (G < 16 && (V + G - 1) / G > kSliceMax) G *= 2;
+    a.G = G;
+    a.draw_level = draw_level(V, G);
+    a.prefetch = draw_prefetch((int)std::min<long long>(R, 1 << 30), V, dt);
+    a.force_precise = g_force_precise.load();
+    a.c2 = log2e_over(T);
+    a.c = a.c2.hi;
+    const size_t smem = draw_smem_bytes(V, G, a.draw_level);
+    if (smem > kDynSmemMax) return SV_ERR_UNSUPPORTED;
+    cudaLaunchAttribute pdl;
+    pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl.val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(R * G), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2] = {cluster_attr(G), pdl};
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    cudaError_t e = dt == SV_BF16 ? cudaLaunchKernelEx(&cfg, sv_match_draw_kernel<__nv_bfloat16>, a)
+                                  : cudaLaunchKernelEx(&cfg, sv_match_draw_kernel<float>, a);
+    if (e != cudaSuccess) return SV_ERR_CUDA;
+    cudaLaunchConfig_t fc = {};
+    fc.gridDim = dim3((unsigned)((B + 3) / 4), 1, 1);
+    fc.blockDim = dim3(128, 1, 1);
+    fc.stream = stream;
+    fc.attrs = &pdl;
+    fc.numAttrs = 1;
+    e = cudaLaunchKernelEx(&fc, sv_finish_match_kernel, x, ua, ur, rows, seqstat, B, k, V, out,
+                           nacc, ep);
+    return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
 // Paths of the one-call entry points.  Batches with a sequence for every SM
 // take the row-skipping path (the row stream in position-major order, rows past
 // a sequence's first stop never read, then one draw CTA per sequence and the
@@ -2536,6 +2697,23 @@ sv_status spec_verify_sample_kv(const void* logits, sv_dtype dtype, const float*
     return run_verify(true, logits, dtype, draft_probs, draft_tokens, u_accept, u_resample, T, B,
                       k, V, out_tokens, num_accepted, ws, stream, sms,
                       Epilogue{kv_len, reinterpret_cast<unsigned long long*>(stats)});
+}
+
+sv_status spec_verify_match(const void* logits, sv_dtype dtype, const int32_t* draft_tokens,
+                            const float* u_draw, const float* u_bonus, float T, int B, int k,
+                            int V, int32_t* out_tokens, int32_t* num_accepted, void* ws,
+                            size_t ws_bytes, cudaStream_t stream) {
+    sv_status st = check_common(logits, dtype, draft_tokens, B, k, V, ws, ws_bytes);
+    if (st != SV_OK) return st;
+    if ((st = check_outputs(out_tokens, num_accepted, B)) != SV_OK) return st;
+    if (!(T > 0.0f) || !std::isfinite(T)) return SV_ERR_INVALID_ARG;
+    if (B > 0 && (!u_draw || !u_bonus || !aligned16(u_draw) || !aligned16(u_bonus)))
+        return SV_ERR_INVALID_ARG;
+    int sms = 0;
+    if ((st = device_setup(&sms)) != SV_OK) return st;
+    if (B == 0) return SV_OK;
+    return launch_match(logits, dtype, draft_tokens, u_draw, u_bonus, T, B, k, V, out_tokens,
+                        num_accepted, ws, stream, sms, Epilogue{nullptr, nullptr});
 }
 
 sv_status spec_verify_read_status(const void* ws, cudaStream_t stream, uint32_t* device_status,

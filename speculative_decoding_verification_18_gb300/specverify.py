@@ -53,6 +53,8 @@ def load():
     lib.spec_verify_greedy.argtypes = [P, I, P, I, I, I, P, P, P, Z, P]
     lib.spec_verify_greedy.restype = I
     lib.spec_verify_sample.argtypes = [P, I, P, P, P, P, F, I, I, I, P, P, P, Z, P]
+    lib.spec_verify_match.argtypes = [P, I, P, P, P, F, I, I, I, P, P, P, Z, P]
+    lib.spec_verify_match.restype = I
     lib.spec_verify_sample_kv.argtypes = [P, I, P, P, P, P, F, I, I, I, P, P, P, Z, P, P, P]
     lib.spec_verify_sample_kv.restype = I
     lib.spec_verify_greedy_kv.argtypes = [P, I, P, I, I, I, P, P, P, Z, P, P, P]
@@ -150,6 +152,16 @@ def spec_verify_sample(logits, draft_probs, draft_tokens, u_accept, u_resample, 
                                    B, k1 - 1, V, _ptr(out_tokens), _ptr(num_accepted), _ptr(ws),
                                    ws.numel(), _stream(stream))
     _check(st, "spec_verify_sample")
+
+
+def spec_verify_match(logits, draft_tokens, u_draw, u_bonus, T, out_tokens, num_accepted, ws,
+                      stream=None):
+    """Sample-and-match verify: a target draw per position, drafts kept while equal."""
+    B, k1, V = logits.shape
+    st = load().spec_verify_match(_ptr(logits), _dtype(logits), _ptr(draft_tokens), _ptr(u_draw),
+                                  _ptr(u_bonus), float(T), B, k1 - 1, V, _ptr(out_tokens),
+                                  _ptr(num_accepted), _ptr(ws), ws.numel(), _stream(stream))
+    _check(st, "spec_verify_match")
 
 
 STATS_FIELDS = ("rounds", "proposed", "accepted", "emitted", "invalid")
