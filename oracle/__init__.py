@@ -59,6 +59,9 @@ def _load():
                                      ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P,
                                      P, P, P, P, P, P, P, P, P, ctypes.c_int]
     lib.orc_verify_batch.restype = ctypes.c_int
+    lib.orc_ngram_draft.argtypes = [P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                    ctypes.c_int, ctypes.c_int, P, P]
+    lib.orc_ngram_draft.restype = ctypes.c_int
     lib.orc_max_threads.argtypes = []
     lib.orc_max_threads.restype = ctypes.c_int
     _lib = lib
@@ -174,3 +177,18 @@ def verify_batch(mode, logits, dtype: str, q, x, ua, ur, T, nthreads: int = 0) -
     if rc != 0:
         raise ValueError("oracle rejected its arguments")
     return r
+
+
+def ngram_draft(history, lengths, k: int, n_min: int, n_max: int):
+    """N-gram drafter over padded histories [B, Lmax] int32 with lengths [B]:
+    returns (draft [B, k] int32, -1 padded; num [B] int32)."""
+    history = np.ascontiguousarray(history, dtype=np.int32)
+    lengths = np.ascontiguousarray(lengths, dtype=np.int32)
+    B, Lmax = history.shape
+    draft = np.zeros((B, k), np.int32)
+    num = np.zeros(B, np.int32)
+    rc = _load().orc_ngram_draft(_ptr(history), _ptr(lengths), B, Lmax, int(k), int(n_min),
+                                 int(n_max), _ptr(draft), _ptr(num))
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    return draft, num

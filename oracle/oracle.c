@@ -316,6 +316,37 @@ void orc_verify_seq(int mode, const double* logits, const double* q, const int32
     *n_acc = n;
 }
 
+int orc_ngram_draft(const int32_t* history, const int32_t* lengths, int B, int Lmax, int k,
+                    int n_min, int n_max, int32_t* draft, int32_t* num) {
+    if (B < 0 || Lmax < 0 || k < 1 || n_min < 1 || n_max < n_min) return -1;
+    if (B > 0 && (!history || !lengths || !draft || !num)) return -1;
+    for (int b = 0; b < B; ++b) {
+        const int32_t* h = history + (size_t)b * Lmax;
+        int L = lengths[b];
+        if (L < 0) L = 0;
+        if (L > Lmax) L = Lmax;
+        int best = -1;
+        for (int n = n_max; n >= n_min && best < 0; --n) {
+            if (L < n + 1) continue;
+            for (int e = L - 2; e >= n - 1; --e) { /* most recent first */
+                int t = 0;
+                while (t < n && h[e - t] == h[L - 1 - t]) ++t;
+                if (t == n) {
+                    best = e;
+                    break;
+                }
+            }
+        }
+        int32_t* d = draft + (size_t)b * k;
+        int cnt = 0;
+        if (best >= 0)
+            for (int i = 0; i < k && best + 1 + i <= L - 1; ++i) d[cnt++] = h[best + 1 + i];
+        for (int i = cnt; i < k; ++i) d[i] = -1;
+        num[b] = cnt;
+    }
+    return 0;
+}
+
 static double bf16_to_double(uint16_t h) {
     uint32_t bits = ((uint32_t)h) << 16;
     float f;

@@ -85,6 +85,19 @@ int orc_verify_batch(int mode, const void* logits, int dtype, const float* q,
 /* Number of OpenMP threads a batch call with nthreads <= 0 would use. */
 int orc_max_threads(void);
 
+/* N-gram (prompt-lookup) drafter ([DEE] §"A família de rascunhos", prompt
+ * lookup: find the last tokens earlier in the context and propose what
+ * followed them there; [SD15] §"What proposes the tokens", NgramDrafter).  For
+ * each sequence b with history h = history[b*Lmax .. b*Lmax + lengths[b]):
+ * for n = n_max down to n_min, look for earlier occurrences of the last n
+ * tokens, h[e-n+1 .. e] == h[L-n .. L-1] with e <= L-2; the first n with an
+ * occurrence wins, and of its occurrences the most recent (largest e).  The
+ * draft is h[e+1 .. e+k], cut at the end of the history: num[b] tokens, -1
+ * after.  No occurrence (or L < n_min + 1): num[b] = 0.  Returns 0, or -1 for
+ * bad arguments. */
+int orc_ngram_draft(const int32_t* history, const int32_t* lengths, int B, int Lmax, int k,
+                    int n_min, int n_max, int32_t* draft, int32_t* num);
+
 #ifdef __cplusplus
 }
 #endif

@@ -408,3 +408,48 @@ def test_planted_mistakes_are_caught(orc):
     m1, S1, _, _ = orc.row_stats(l, 1.0)
     m2, S2, _, _ = orc.row_stats(l, 0.5)
     assert abs(S1 - S2) > 1e-3 and m2 == 2 * m1
+
+
+# ---------------------------------------------------------------- n-gram drafter
+
+def test_ngram_drafter_worked_cases(orc):
+    """The prompt-lookup rule ([DEE] §"A família de rascunhos"; [SD15] §"What
+    proposes the tokens"): the longest suffix n-gram (n_max down to n_min) that
+    occurred before, its most recent occurrence, the tokens that followed it."""
+    pad = -9
+    cases = [
+        # history, k, n_min, n_max, expected draft
+        ([1, 2, 3, 4, 1, 2], 3, 1, 2, [3, 4, 1]),       # "1 2" seen at 0..1: copy 3 4 1
+        ([1, 2, 3, 4, 1, 2], 5, 1, 2, [3, 4, 1, 2]),    # cut at the end of the history
+        ([5, 6, 7, 8], 3, 1, 3, []),                    # nothing repeats: no draft
+        ([7, 1, 9, 2, 9, 3, 9], 2, 1, 2, [3, 9]),       # "9" most recent earlier at 4 -> 3 9
+        ([1, 2, 9, 5, 2, 9, 6, 2, 9], 2, 1, 2, [6, 2]),  # "2 9" at 4..5 (most recent) -> 6 2
+        ([4, 2, 9, 5, 8, 2, 9], 3, 1, 3, [5, 8, 2]),    # "8 2 9" absent, "2 9" at 1..2
+        ([3, 3, 3, 3], 2, 1, 2, [3]),                   # overlapping run: e = 2, one token left
+        ([1], 2, 1, 1, []),                             # too short to hold an occurrence
+    ]
+    Lmax = max(len(c[0]) for c in cases)
+    hist = np.full((len(cases), Lmax), pad, np.int32)
+    for b, c in enumerate(cases):
+        hist[b, :len(c[0])] = c[0]
+    lens = np.array([len(c[0]) for c in cases], np.int32)
+    for b, (h, k, n_min, n_max, want) in enumerate(cases):
+        d, num = orc.ngram_draft(hist[b:b + 1], lens[b:b + 1], k, n_min, n_max)
+        assert num[0] == len(want), (b, d, num)
+        assert list(d[0, :num[0]]) == want and (d[0, num[0]:] == -1).all(), (b, d)
+
+
+def test_ngram_drafter_periodic_stream(orc):
+    """On a stream of period P >= n_max the draft is exactly the next k tokens of
+    the period; on a stream without repeats it is empty."""
+    g = np.random.default_rng(4)
+    P, k = 11, 6
+    period = g.permutation(1000)[:P].astype(np.int32)
+    for L in (2 * P, 3 * P + 5, 5 * P - 1):
+        h = np.resize(period, L)[None, :]
+        d, num = orc.ngram_draft(h, np.array([L], np.int32), k, 1, 4)
+        want = np.resize(period, L + k)[L:L + k]
+        assert num[0] == k and np.array_equal(d[0], want)
+    h = np.arange(50, dtype=np.int32)[None, :]
+    d, num = orc.ngram_draft(h, np.array([50], np.int32), k, 1, 4)
+    assert num[0] == 0 and (d == -1).all()
