@@ -147,6 +147,23 @@ sv_status spec_verify_match(const void* logits, sv_dtype dtype, const int32_t* d
                             int V, int32_t* out_tokens, int32_t* num_accepted, void* ws,
                             size_t ws_bytes, cudaStream_t stream);
 
+/* N-gram (prompt-lookup) drafter: proposals that need no draft model
+ * ("Decodificação especulativa explicada", §"A família de rascunhos";
+ * "Speculative Decoding" (ch15), §"What proposes the tokens", NgramDrafter).
+ *   history [B, Lmax] int32 DEVICE: each sequence's tokens so far, row-major;
+ *   lengths [B] int32 DEVICE: tokens in each row (clamped to [0, Lmax]).
+ * For n = n_max down to n_min, the last n tokens of a sequence are looked for
+ * earlier in its history; the first n that occurs wins, and of its occurrences
+ * the most recent; the draft is the up to k tokens that followed it.
+ *   draft_tokens [B, k] int32 (written): the proposal, -1 after num_drafted;
+ *   num_drafted [B] int32 (written): 0 when nothing occurs earlier.
+ * Such a proposal is a point mass: sampled verification takes q = one-hot at
+ * each proposed token.  Limits: 1 <= k <= 64, 1 <= n_min <= n_max <= 32.
+ * Asynchronous on `stream`; argument errors return before any launch. */
+sv_status spec_ngram_draft(const int32_t* history, const int32_t* lengths, int B, int Lmax,
+                           int k, int n_min, int n_max, int32_t* draft_tokens,
+                           int32_t* num_drafted, cudaStream_t stream);
+
 /* Counters a verify can add to (spec_verify_*_kv), for generation loops that
  * keep speculation statistics on the device ("Speculative Decoding" (ch15, LLM
  * serving from scratch), the stats argument of speculative_generate; the

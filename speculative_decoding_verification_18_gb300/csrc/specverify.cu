@@ -1958,6 +1958,84 @@ __global__ void sv_finish_match_kernel(const int32_t* __restrict__ x,
     }
 }
 
+// ------------------------------------------------------------------ n-gram drafter
+
+// Prompt-lookup / n-gram drafting ("Decodificação especulativa explicada",
+// §"A família de rascunhos": find the last tokens earlier in the context and
+// propose what followed them there; "Speculative Decoding" (ch15), §"What
+// proposes the tokens", the NgramDrafter).  Rule: for n = n_max down to n_min
+// the last n tokens are looked for earlier in the history (an occurrence ends
+// at e <= L - 2); the first n that occurs wins, and of its occurrences the most
+// recent; the draft is the up to k tokens after it.
+//
+// One CTA per sequence.  The last n_max tokens sit in shared memory; each
+// thread takes candidate end positions e (coalesced loads of h[e]) and extends
+// the common suffix of h[..e] and h[..L-1] only while it matches.  The winner
+// maximises (min(suffix, n_max), e): the longest n with an occurrence, then
+// the most recent one, which is the rule above.
+constexpr int kNgramThreads = 256;
+constexpr int kNgramMaxN = 32;
+
+__global__ void __launch_bounds__(kNgramThreads) sv_ngram_kernel(
+    const int32_t* __restrict__ history, const int32_t* __restrict__ lengths, int Lmax, int k,
+    int n_min, int n_max, int32_t* __restrict__ draft, int32_t* __restrict__ num) {
+    __shared__ int32_t suf[kNgramMaxN];
+    __shared__ unsigned long long red[kNgramThreads / 32];
+    const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int32_t* h = history + (long long)b * Lmax;
+    int L = lengths[b];
+    L = L < 0 ? 0 : (L > Lmax ? Lmax : L);
+    for (int t = tid; t < n_max; t += kNgramThreads) suf[t] = t < L ? h[L - 1 - t] : -1;
+    __syncthreads();
+    unsigned long long best = 0;  // (match length << 32) | (e + 1); 0 = none
+    // Eight candidates per thread in flight: their last tokens are loaded
+    // together; only those equal to the history's last token extend the match.
+    constexpr int U = 8;
+    const int32_t last = suf[0];
+    for (int base = L - 2 - tid; base >= 0; base -= U * kNgramThreads) {
+        int32_t v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int e = base - u * kNgramThreads;
+            v[u] = e >= 0 ? __ldg(h + e) : ~last;
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int e = base - u * kNgramThreads;
+            if (e >= 0 && v[u] == last) {
+                int t = 1;
+                const int tmax = min(n_max, e + 1);
+                while (t < tmax && __ldg(h + e - t) == suf[t]) ++t;
+                if (t >= n_min) {
+                    const unsigned long long key =
+                        ((unsigned long long)t << 32) | (unsigned)(e + 1);
+                    best = key > best ? key : best;
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const unsigned long long o = __shfl_xor_sync(0xffffffffu, best, off);
+        best = o > best ? o : best;
+    }
+    if (lane == 0) red[warp] = best;
+    __syncthreads();
+    if (warp == 0) {
+        best = lane < kNgramThreads / 32 ? red[lane] : 0ull;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const unsigned long long o = __shfl_xor_sync(0xffffffffu, best, off);
+            best = o > best ? o : best;
+        }
+        const int e = best ? (int)(best & 0xFFFFFFFFull) - 1 : -1;
+        const int cnt = e >= 0 ? min(k, L - 1 - e) : 0;
+        for (int i = lane; i < k; i += 32)
+            draft[(long long)b * k + i] = i < cnt ? h[e + 1 + i] : -1;
+        if (lane == 0) num[b] = cnt;
+    }
+}
+
 // ------------------------------------------------------------------ debug kernel
 
 __global__ void sv_debug_ffexp_kernel(const float* l, float m, int n, ff c2, double* out) {
@@ -2714,6 +2792,26 @@ sv_status spec_verify_match(const void* logits, sv_dtype dtype, const int32_t* d
     if (B == 0) return SV_OK;
     return launch_match(logits, dtype, draft_tokens, u_draw, u_bonus, T, B, k, V, out_tokens,
                         num_accepted, ws, stream, sms, Epilogue{nullptr, nullptr});
+}
+
+sv_status spec_ngram_draft(const int32_t* history, const int32_t* lengths, int B, int Lmax,
+                           int k, int n_min, int n_max, int32_t* draft_tokens,
+                           int32_t* num_drafted, cudaStream_t stream) {
+    if (B < 0 || Lmax < 0 || k < 1 || k > kMaxK || n_min < 1 || n_max < n_min ||
+        n_max > kNgramMaxN)
+        return SV_ERR_INVALID_ARG;
+    if (B > 0 && (!history || !lengths || !draft_tokens || !num_drafted)) return SV_ERR_INVALID_ARG;
+    if (B > 0 && (!aligned16(history) || !aligned16(lengths) || !aligned16(draft_tokens) ||
+                  !aligned16(num_drafted)))
+        return SV_ERR_INVALID_ARG;
+    if ((long long)B * Lmax >= (1LL << 40) || B >= (1 << 30)) return SV_ERR_UNSUPPORTED;
+    int sms = 0;
+    sv_status st = device_setup(&sms);
+    if (st != SV_OK) return st;
+    if (B == 0) return SV_OK;
+    sv_ngram_kernel<<<B, kNgramThreads, 0, stream>>>(history, lengths, Lmax, k, n_min, n_max,
+                                                     draft_tokens, num_drafted);
+    return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
 sv_status spec_verify_read_status(const void* ws, cudaStream_t stream, uint32_t* device_status,

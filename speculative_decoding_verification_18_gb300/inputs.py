@@ -220,3 +220,29 @@ def toy_language(seed: int = 2, V: int = 4, keep: float = 0.55):
     P = g.dirichlet(np.ones(V), size=V)
     D = g.dirichlet(np.ones(V), size=V)
     return P, keep * P + (1.0 - keep) * D
+
+
+def ngram_histories(B: int, Lmax: int, V: int = 32000, seed: int = 0, pool: int = 64,
+                    p_phrase: float = 0.8, min_len: int | None = None):
+    """Synthetic token streams that repeat themselves, for the n-gram drafter:
+    each history concatenates pieces that are, with probability p_phrase, one of
+    `pool` fixed phrases (3 to 12 tokens) and otherwise fresh random tokens (1 to
+    8), to a length drawn uniformly in [min_len, Lmax] (default Lmax / 2).
+    Returns (history [B, Lmax] int32 padded with -1, lengths [B] int32)."""
+    g = np.random.default_rng(seed)
+    phrases = [g.integers(0, V, size=int(g.integers(3, 13))).astype(np.int32) for _ in range(pool)]
+    lo = Lmax // 2 if min_len is None else min_len
+    hist = np.full((B, Lmax), -1, dtype=np.int32)
+    lengths = g.integers(lo, Lmax + 1, size=B).astype(np.int32)
+    for b in range(B):
+        parts, n = [], 0
+        while n < lengths[b]:
+            if g.random() < p_phrase:
+                piece = phrases[int(g.integers(0, pool))]
+            else:
+                piece = g.integers(0, V, size=int(g.integers(1, 9))).astype(np.int32)
+            parts.append(piece)
+            n += len(piece)
+        row = np.concatenate(parts)[:lengths[b]] if parts else np.zeros(0, np.int32)
+        hist[b, :len(row)] = row
+    return hist, lengths

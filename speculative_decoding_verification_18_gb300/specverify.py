@@ -53,6 +53,8 @@ def load():
     lib.spec_verify_greedy.argtypes = [P, I, P, I, I, I, P, P, P, Z, P]
     lib.spec_verify_greedy.restype = I
     lib.spec_verify_sample.argtypes = [P, I, P, P, P, P, F, I, I, I, P, P, P, Z, P]
+    lib.spec_ngram_draft.argtypes = [P, P, I, I, I, I, I, P, P, P]
+    lib.spec_ngram_draft.restype = I
     lib.spec_verify_match.argtypes = [P, I, P, P, P, F, I, I, I, P, P, P, Z, P]
     lib.spec_verify_match.restype = I
     lib.spec_verify_sample_kv.argtypes = [P, I, P, P, P, P, F, I, I, I, P, P, P, Z, P, P, P]
@@ -162,6 +164,16 @@ def spec_verify_match(logits, draft_tokens, u_draw, u_bonus, T, out_tokens, num_
                                   _ptr(u_bonus), float(T), B, k1 - 1, V, _ptr(out_tokens),
                                   _ptr(num_accepted), _ptr(ws), ws.numel(), _stream(stream))
     _check(st, "spec_verify_match")
+
+
+def spec_ngram_draft(history, lengths, k, n_min, n_max, draft_tokens, num_drafted, stream=None):
+    """N-gram drafter: history [B, Lmax] int32, lengths [B] int32 -> draft_tokens [B, k],
+    num_drafted [B]."""
+    B, Lmax = history.shape
+    st = load().spec_ngram_draft(_ptr(history), _ptr(lengths), B, Lmax, int(k), int(n_min),
+                                 int(n_max), _ptr(draft_tokens), _ptr(num_drafted),
+                                 _stream(stream))
+    _check(st, "spec_ngram_draft")
 
 
 STATS_FIELDS = ("rounds", "proposed", "accepted", "emitted", "invalid")

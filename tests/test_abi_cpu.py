@@ -91,3 +91,16 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(sv, "LIB", str(tmp_path / "missing.so"))
     with pytest.raises(ImportError):
         sv.load()
+
+
+def test_ngram_argument_errors(lib):
+    """Argument errors come back before any launch (no GPU needed)."""
+    from speculative_decoding_verification_18_gb300 import specverify as sv
+    f = lib.spec_ngram_draft
+    assert f(None, None, 1, 10, 4, 1, 4, None, None, None) == sv.SV_ERR_INVALID_ARG
+    assert f(None, None, 0, 10, 0, 1, 4, None, None, None) == sv.SV_ERR_INVALID_ARG   # k < 1
+    assert f(None, None, 0, 10, 65, 1, 4, None, None, None) == sv.SV_ERR_INVALID_ARG  # k > 64
+    assert f(None, None, 0, 10, 4, 0, 4, None, None, None) == sv.SV_ERR_INVALID_ARG  # n_min < 1
+    assert f(None, None, 0, 10, 4, 3, 2, None, None, None) == sv.SV_ERR_INVALID_ARG  # n_max < n_min
+    assert f(None, None, 0, 10, 4, 1, 33, None, None, None) == sv.SV_ERR_INVALID_ARG  # n_max > 32
+    assert f(None, None, -1, 10, 4, 1, 4, None, None, None) == sv.SV_ERR_INVALID_ARG  # B < 0
