@@ -1,12 +1,14 @@
 """Run the one-call verify a few times on a named workload (for profilers).
 
     python -m speculative_decoding_verification_18_gb300.run_case c4 --batch 64 --path 3 --reps 4
+    python -m speculative_decoding_verification_18_gb300.run_case c3 --match
 
 Builds the seeded inputs of the workload (optionally with another batch size),
 copies them to the GPU, and calls spec_verify_sample / spec_verify_greedy
 `reps` times on one stream, then prints the status word.  `--path` forces the
 two-kernel (1), fused (2) or row-skipping (3) path; 0 keeps the automatic
-choice.  Nothing is timed here: the point is a fixed, short sequence of
+choice; `--match` runs the sample-and-match verify (spec_verify_match) on a
+sampled workload instead.  Nothing is timed here: the point is a fixed, short sequence of
 launches that a profiler can select from with its skip / count options.
 """
 from __future__ import annotations
@@ -26,6 +28,7 @@ def main(argv=None):
     ap.add_argument("--batch", type=int, default=0, help="override B (0: the workload's)")
     ap.add_argument("--path", type=int, default=0, choices=[0, 1, 2, 3])
     ap.add_argument("--reps", type=int, default=4)
+    ap.add_argument("--match", action="store_true", help="sample-and-match verify")
     a = ap.parse_args(argv)
     kw = dict(I.WORKLOADS[a.workload])
     if a.batch > 0:
@@ -46,6 +49,11 @@ def main(argv=None):
         if inp.mode == "greedy":
             for _ in range(a.reps):
                 sv.spec_verify_greedy(logits, x, out, n, ws)
+        elif a.match:
+            ua = torch.from_numpy(inp.ua).to(dev)
+            ur = torch.from_numpy(inp.ur).to(dev)
+            for _ in range(a.reps):
+                sv.spec_verify_match(logits, x, ua, ur, inp.T, out, n, ws)
         else:
             q = torch.from_numpy(inp.q).to(dev)
             ua = torch.from_numpy(inp.ua).to(dev)
@@ -56,7 +64,7 @@ def main(argv=None):
     finally:
         sv.debug_force_path(0)
     st, bits, ndeg = sv.spec_verify_read_status(ws)
-    print(f"{a.workload} B={B} k={k} V={V} path={a.path} reps={a.reps}: status {st} "
+    print(f"{a.workload} B={B} k={k} V={V} path={a.path} match={a.match} reps={a.reps}: status {st} "
           f"bits {bits:#x} degenerate {ndeg}")
 
 
