@@ -83,6 +83,19 @@ static_assert(sizeof(RowRec) == 32, "row record size");
 
 constexpr uint32_t kRowBad = 1u, kRowTokenBad = 2u, kRowQBad = 4u, kRowSkipped = 8u;
 
+// The record of a row that was never (or only partly) read.
+__device__ __forceinline__ RowRec skipped_record() {
+    RowRec rec;
+    rec.mraw = NAN;
+    rec.S = NAN;
+    rec.px = NAN;
+    rec.lx = NAN;
+    rec.qx = NAN;
+    rec.argmax = -1;
+    rec.flags = kRowSkipped;
+    return rec;
+}
+
 // Layout: header | B*(k+1) row records | B per-sequence status words | B
 // per-sequence stop rows (the row-skipping path) | a 16-byte counter and B
 // entries of the list of draws left to the precise kernel (large batches).
@@ -191,11 +204,15 @@ __device__ __forceinline__ Partial warp_merge(Partial p, float c) {
 // One thread's share of a vocabulary slice of one row: vectors [vb, ve) of the
 // row's aligned body handled by threads tg = 0..ng-1 (stride ng), plus the
 // unaligned head (if `head_here`) and tail (if `tail_here`) as scalars.
-template <typename DT, bool SAMPLED, int U>
+// With POLL: every batch also reads *poll, and once it holds a value below
+// `poll_row` the thread sets `aborted` and stops reading (its partial is then
+// meaningless; the caller discards the row).
+template <typename DT, bool SAMPLED, int U, bool POLL = false>
 __device__ __forceinline__ Partial stream_slice(const DT* __restrict__ rowp, int V, long long vb,
                                                 long long ve, int head, long long tail0,
                                                 bool head_here, bool tail_here, int tg, int ng,
-                                                float c) {
+                                                float c, const uint32_t* poll = nullptr,
+                                                uint32_t poll_row = 0, bool* aborted = nullptr) {
     using E = Elt<DT>;
     constexpr int VW = E::kVec;
     Partial p = empty_partial();
@@ -239,12 +256,18 @@ __device__ __forceinline__ Partial stream_slice(const DT* __restrict__ rowp, int
     // round trips.
     for (long long v = vb + tg; v < ve; v += (long long)U * ng) {
         uint4 buf[U];
+        uint32_t st = 0xFFFFFFFFu;
+        if (POLL) st = *reinterpret_cast<const volatile uint32_t*>(poll);
 #pragma unroll
         for (int u = 0; u < U; ++u)
             if (v + (long long)u * ng < ve) buf[u] = ld_stream16(vp + v + (long long)u * ng);
 #pragma unroll
         for (int u = 0; u < U; ++u)
             if (v + (long long)u * ng < ve) vector(buf[u], head + (v + (long long)u * ng) * VW);
+        if (POLL && st < poll_row) {
+            *aborted = true;
+            break;
+        }
     }
     if (tail_here)
         for (long long j = tail0 + tg; j < V; j += ng) scalar(j);
@@ -1434,17 +1457,8 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(VerifyArgs a) {
     }
     // Rows past the last wave were never read.
     if (rank == 0)
-        for (int i = last_wave_end + tid; i <= k; i += kThreads) {
-            RowRec rec;
-            rec.mraw = NAN;
-            rec.S = NAN;
-            rec.px = NAN;
-            rec.lx = NAN;
-            rec.qx = NAN;
-            rec.argmax = -1;
-            rec.flags = kRowSkipped;
-            a.rows[(long long)b * (k + 1) + i] = rec;
-        }
+        for (int i = last_wave_end + tid; i <= k; i += kThreads)
+            a.rows[(long long)b * (k + 1) + i] = skipped_record();
 
     const int n = fs.n;
     const int bits = fs.bits;
@@ -1529,8 +1543,10 @@ struct RowsArgs {
 // stopping row n, and no row at or before n can be skipped (that would need a
 // stopping row below n), so the finish kernel reads only rows this kernel
 // computed.  stop[] must hold 0xFFFFFFFF when the grid starts.
+// At most 64 registers per thread: 2048 threads' worth of CTAs per SM stay
+// resident (2 CTAs of 512 threads; 1 of 1024 threads).
 template <typename DT, bool SAMPLED, int NT>
-__global__ void __launch_bounds__(NT) sv_rows_kernel(RowsArgs a) {
+__global__ void __launch_bounds__(NT, 1024 / NT) sv_rows_kernel(RowsArgs a) {
     using E = Elt<DT>;
     constexpr int NW = NT / 32;
     __shared__ Partial wpart[NW];
@@ -1554,26 +1570,20 @@ __global__ void __launch_bounds__(NT) sv_rows_kernel(RowsArgs a) {
         a.hdr->V = V;
         a.hdr->mode = a.mode;
     }
+    // Set when the row turns out to lie past the stop row while it is read.
+    __shared__ int s_abort;
     if (a.skip && i > 0) {
         // One thread reads the stop row and the CTA follows its decision (the
         // value may change under concurrent CTAs, so each thread reading it
         // could decide differently).  G == 1: no other CTA shares the row.
         __shared__ int s_skip;
-        if (tid == 0)
+        if (tid == 0) {
             s_skip = *reinterpret_cast<volatile const uint32_t*>(a.stop + b) < (uint32_t)i;
+            s_abort = 0;
+        }
         __syncthreads();
         if (s_skip) {
-            if (tid == 0) {
-                RowRec rec;
-                rec.mraw = NAN;
-                rec.S = NAN;
-                rec.px = NAN;
-                rec.lx = NAN;
-                rec.qx = NAN;
-                rec.argmax = -1;
-                rec.flags = kRowSkipped;
-                a.rows[row] = rec;
-            }
+            if (tid == 0) a.rows[row] = skipped_record();
             return;
         }
     }
@@ -1594,12 +1604,28 @@ __global__ void __launch_bounds__(NT) sv_rows_kernel(RowsArgs a) {
     const int lgG = log2_pow2(G);
     const long long vb = (nvec * rank) >> lgG, ve = (nvec * (rank + 1)) >> lgG;
     // Eight 16-byte loads in flight per thread: a row slice of up to 8 vectors
-    // per thread costs one round trip.
-    Partial p = stream_slice<DT, SAMPLED, 8>(rowp, V, vb, ve, head, tail0, rank == 0,
-                                             rank == G - 1, tid, NT, a.c);
+    // per thread costs one round trip.  On the row-skipping stream every batch
+    // also re-reads stop[b]: a row that falls past the stop row while it is read
+    // is abandoned (stop[b] only decreases, so one observation suffices for
+    // the whole CTA, whatever the other threads saw).
+    const bool poll = a.skip && i > 0;
+    Partial p;
+    if (poll) {
+        bool aborted = false;
+        p = stream_slice<DT, SAMPLED, 8, true>(rowp, V, vb, ve, head, tail0, true, true, tid, NT,
+                                               a.c, a.stop + b, (uint32_t)i, &aborted);
+        if (aborted) s_abort = 1;
+    } else {
+        p = stream_slice<DT, SAMPLED, 8>(rowp, V, vb, ve, head, tail0, rank == 0, rank == G - 1,
+                                         tid, NT, a.c);
+    }
     p = warp_merge<SAMPLED>(p, a.c);
     if (lane == 0) wpart[warp] = p;
     __syncthreads();
+    if (poll && s_abort) {
+        if (tid == 0) a.rows[row] = skipped_record();
+        return;
+    }
     if (warp == 0) {
         Partial w = lane < NW ? wpart[lane] : empty_partial();
         w = warp_merge<SAMPLED>(w, a.c);
@@ -2170,15 +2196,19 @@ static sv_status device_setup(int* sms) {
             SV_TRY(cluster_attrs(sv_rows_kernel<__nv_bfloat16, true, 128>, false));
             SV_TRY(cluster_attrs(sv_rows_kernel<__nv_bfloat16, true, 256>, false));
             SV_TRY(cluster_attrs(sv_rows_kernel<__nv_bfloat16, true, 512>, false));
+            SV_TRY(cluster_attrs(sv_rows_kernel<__nv_bfloat16, true, 1024>, false));
             SV_TRY(cluster_attrs(sv_rows_kernel<__nv_bfloat16, false, 128>, false));
             SV_TRY(cluster_attrs(sv_rows_kernel<__nv_bfloat16, false, 256>, false));
             SV_TRY(cluster_attrs(sv_rows_kernel<__nv_bfloat16, false, 512>, false));
+            SV_TRY(cluster_attrs(sv_rows_kernel<__nv_bfloat16, false, 1024>, false));
             SV_TRY(cluster_attrs(sv_rows_kernel<float, true, 128>, false));
             SV_TRY(cluster_attrs(sv_rows_kernel<float, true, 256>, false));
             SV_TRY(cluster_attrs(sv_rows_kernel<float, true, 512>, false));
+            SV_TRY(cluster_attrs(sv_rows_kernel<float, true, 1024>, false));
             SV_TRY(cluster_attrs(sv_rows_kernel<float, false, 128>, false));
             SV_TRY(cluster_attrs(sv_rows_kernel<float, false, 256>, false));
             SV_TRY(cluster_attrs(sv_rows_kernel<float, false, 512>, false));
+            SV_TRY(cluster_attrs(sv_rows_kernel<float, false, 1024>, false));
 #undef SV_TRY
             if (e != cudaSuccess) return SV_ERR_CUDA;
             // How many clusters of the drawing kernel fit at once, per cluster
@@ -2456,7 +2486,7 @@ static sv_status launch_rows(bool sampled, const void* logits, sv_dtype dt, cons
     a.G = skip ? 1 : rows_split(R, nvec_row, sms);
     int nt = skip ? 512 : rows_threads(R * a.G, nvec_row / a.G, sms);
     if (!skip && g_force_rows_G.load()) a.G = g_force_rows_G.load();
-    if (!skip && g_force_rows_nt.load()) nt = g_force_rows_nt.load();
+    if (g_force_rows_nt.load()) nt = g_force_rows_nt.load();
     if (skip && cudaMemsetAsync(a.stop, 0xFF, (size_t)B * sizeof(uint32_t), stream) != cudaSuccess)
         return SV_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
@@ -2468,7 +2498,8 @@ static sv_status launch_rows(bool sampled, const void* logits, sv_dtype dt, cons
     cfg.numAttrs = 1;
     cudaError_t e;
 #define SV_ROWS(DTY, S)                                                          \
-    e = nt == 512   ? cudaLaunchKernelEx(&cfg, sv_rows_kernel<DTY, S, 512>, a)     \
+    e = nt == 1024  ? cudaLaunchKernelEx(&cfg, sv_rows_kernel<DTY, S, 1024>, a)    \
+        : nt == 512 ? cudaLaunchKernelEx(&cfg, sv_rows_kernel<DTY, S, 512>, a)     \
         : nt == 256 ? cudaLaunchKernelEx(&cfg, sv_rows_kernel<DTY, S, 256>, a)     \
                     : cudaLaunchKernelEx(&cfg, sv_rows_kernel<DTY, S, 128>, a)
     if (dt == SV_BF16) {
@@ -2927,7 +2958,7 @@ void spec_verify_debug_fused_tuning(int defer_mode, int pad_kib) {
 // per CTA (128, 256 or 512) on the two-kernel path; 0 for the automatic choice.
 void spec_verify_debug_rows_split(int G, int nt) {
     if (G == 0 || G == 1 || G == 2 || G == 4 || G == 8 || G == 16) g_force_rows_G.store(G);
-    if (nt == 0 || nt == 128 || nt == 256 || nt == 512) g_force_rows_nt.store(nt);
+    if (nt == 0 || nt == 128 || nt == 256 || nt == 512 || nt == 1024) g_force_rows_nt.store(nt);
 }
 
 // Tuning hook: a fixed cluster size (1, 2, 4, 8 or 16) for the draw kernel, 0
