@@ -317,6 +317,9 @@ def main():
     path = sv.debug_path(sv.SV_MODE_GREEDY if inp.mode == "greedy" else sv.SV_MODE_SAMPLE, B, V,
                          inp.dtype)
     fused = path == sv.PATH_FUSED
+    # greedy batches of about one row per resident CTA take the flat row stream
+    flat_ctas = sv.debug_flat_ctas(B, k, V, inp.dtype) if inp.mode == "greedy" else 0
+    rows_kname = "sv_flat_greedy_kernel" if flat_ctas else "sv_rows_kernel"
     ws = [sv.workspace(B, k, V, sets[0]["logits"].dtype, dev) for _ in range(copies)]
     outs = [torch.empty((B, k + 1), dtype=torch.int32, device=dev) for _ in range(copies)]
     ns = [torch.empty(B, dtype=torch.int32, device=dev) for _ in range(copies)]
@@ -422,7 +425,7 @@ def main():
             fin_name = ("sv_finish_greedy_kernel" if inp.mode == "greedy"
                         else "sv_finish_sample_kernel+sv_precise_kernel" if path == sv.PATH_SKIP
                         else "sv_finish_sample_kernel")
-            stage_times = {"sv_rows_kernel": stage_ms(rows_stage),
+            stage_times = {rows_kname: stage_ms(rows_stage),
                            fin_name: stage_ms(finish_stage)}
     clocks = sampler.summary()
 
@@ -492,7 +495,7 @@ def main():
     def alg_bytes(kname):
         if kname == "sv_verify_kernel":
             return int(np.mean([algorithmic_bytes_fused(inp, nn) for nn in n_all]))
-        if kname == "sv_rows_kernel":
+        if kname in ("sv_rows_kernel", "sv_flat_greedy_kernel"):
             if path == sv.PATH_SKIP:
                 return int(np.mean([algorithmic_bytes_rows_needed(inp, nn) for nn in n_all]))
             return algorithmic_bytes_rows(inp)
@@ -538,7 +541,8 @@ def main():
                    "timing": f"{reps} replays of a CUDA graph of {copies} verifies",
                    "path": {sv.PATH_FUSED: "fused per-sequence kernel",
                             sv.PATH_SKIP: "position-major row stream with row skipping + draw kernel",
-                            sv.PATH_TWO_KERNEL: "row stream + draw kernels"}[path],
+                            sv.PATH_TWO_KERNEL: "row stream + draw kernels"}[path]
+                           + (f" (flat greedy stream over {flat_ctas} CTAs)" if flat_ctas else ""),
                    "parallelism": f"replicas x{world}"},
         "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": h2d,

@@ -35,6 +35,12 @@ void spec_verify_debug_force_path(int path);
  * sizes on the current device, -1 on error or bad sizes. */
 int spec_verify_debug_path(sv_mode mode, int B, int V, sv_dtype dtype);
 
+/* The number of CTAs of the flat greedy row stream that spec_verify_greedy (or
+ * spec_verify_rows in greedy mode) would launch for these sizes on the current
+ * device with 16-byte aligned logits; 0 when it would take the per-row stream;
+ * -1 on error or bad sizes. */
+int spec_verify_debug_flat_ctas(int B, int k, int V, sv_dtype dtype);
+
 /* Fix the cluster size of the sampled draw kernel (spec_verify_finish and the
  * two-stage paths' second kernel) to G in {1, 2, 4, 8, 16}; 0 restores the
  * automatic choice; other values are ignored.  A process-wide setting read at
@@ -53,6 +59,13 @@ void spec_verify_debug_fused_tuning(int defer_mode, int pad_kib);
  * automatic choice of either; other values are ignored.  A process-wide setting
  * read at launch time, for tuning. */
 void spec_verify_debug_rows_split(int G, int nt);
+
+/* off = 1: greedy batches never take the flat row stream (the whole logits
+ * tensor cut into one equal range per resident CTA, with per-row partial keys
+ * merged by the finish kernel); they take the per-row stream instead.  0
+ * restores the automatic choice.  A fixed split set with
+ * spec_verify_debug_rows_split also turns the flat stream off.  For tests. */
+void spec_verify_debug_flat(int off);
 
 /* Fix the cluster size of the precise-draw kernel of large batches to G in
  * {1, 2, 4, 8, 16}; 0 restores the default.  For tuning. */

@@ -65,7 +65,11 @@ constexpr int kMaxV = 1 << 21;
 struct alignas(16) Header {
     uint32_t magic;
     uint32_t B, k, V, mode;
-    uint32_t pad[59];
+    // Layout of the row records the greedy row stream left: 0 for one record per
+    // row; else the flat stream's CTA count, and the rows' length in 16-byte
+    // vectors (the records then hold per-CTA partial keys).
+    uint32_t flat_ctas, flat_vpr, flat_per, flat_rem;
+    uint32_t pad[55];
 };
 static_assert(sizeof(Header) == 256, "header size");
 
@@ -1569,6 +1573,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sv_rows_kernel(RowsArgs a) {
         a.hdr->k = k;
         a.hdr->V = V;
         a.hdr->mode = a.mode;
+        a.hdr->flat_ctas = 0;
     }
     // Set when the row turns out to lie past the stop row while it is read.
     __shared__ int s_abort;
@@ -1684,9 +1689,209 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sv_rows_kernel(RowsArgs a) {
     if (ends) atomicMin(a.stop + b, (uint32_t)i);
 }
 
+// ------------------------------------------------------------------ flat greedy stream
+//
+// Greedy only needs each row's argmax.  When the batch has about as many rows as
+// the GPU has resident CTAs, one CTA per row (or a fixed split of each row)
+// leaves a partial last wave; the flat stream instead cuts the whole logits
+// tensor, seen as one run of 16-byte vectors (rows are whole vectors), into P
+// equal ranges, one per resident CTA.  A range meets at most kFlatSlots rows
+// and a row at most kFlatSlots ranges.  Each CTA leaves one key per row it
+// meets, key = (order-preserving bits of the max) << 32 | (2^32 - 1 - index), so
+// that the largest key names the lowest index of the maximum; a NaN anywhere
+// gives the all-ones key.  The key of CTA c for row r goes to 64-bit word
+// c - c_first(r) of r's record; the finish kernel merges a row's words.
+
+constexpr int kFlatSlots = 4;
+constexpr int kFlatThreads = 512;
+
+struct FlatArgs {
+    const void* logits;
+    RowRec* rows;
+    Header* hdr;
+    int vpr;       // vectors per row
+    int P;         // CTAs
+    int per, rem;  // the tensor's R * vpr < 2^31 vectors = P * per + rem
+    int B, k, V;
+};
+
+// The ranges: the first `rem` hold per + 1 vectors, the others per.  First
+// vector of range c, and the range that holds vector x.
+__host__ __device__ __forceinline__ int flat_start(int c, int per, int rem) {
+    return c * per + min(c, rem);
+}
+__host__ __device__ __forceinline__ int flat_owner(int x, int per, int rem) {
+    const int big = rem * (per + 1);
+    return x < big ? x / (per + 1) : rem + (x - big) / per;
+}
+
+__device__ __forceinline__ uint32_t ordered_bits(float f) {
+    const uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float from_ordered_bits(uint32_t o) {
+    return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
+}
+
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const unsigned long long o = __shfl_xor_sync(0xffffffffu, v, off);
+        v = o > v ? o : v;
+    }
+    return v;
+}
+
+// NaN-propagating maximum of one 16-byte vector (bf16: pairwise on packed
+// halves first).
+__device__ __forceinline__ uint32_t bf16x2_max_nan(uint32_t a, uint32_t b) {
+    uint32_t y;
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(y) : "r"(a), "r"(b));
+    return y;
+}
+template <typename DT>
+__device__ __forceinline__ float vec_max(const uint4& v);
+template <>
+__device__ __forceinline__ float vec_max<__nv_bfloat16>(const uint4& v) {
+    const uint32_t w = bf16x2_max_nan(bf16x2_max_nan(v.x, v.y), bf16x2_max_nan(v.z, v.w));
+    return fmax_nan(bf16_lo(w), bf16_hi(w));
+}
+template <>
+__device__ __forceinline__ float vec_max<float>(const uint4& v) {
+    return fmax_nan(fmax_nan(__uint_as_float(v.x), __uint_as_float(v.y)),
+                    fmax_nan(__uint_as_float(v.z), __uint_as_float(v.w)));
+}
+// A vector of -inf, the padding of a batch past the end of a range.
+template <typename DT> struct kFlatPad;
+template <> struct kFlatPad<__nv_bfloat16> {
+    __device__ static __forceinline__ uint4 vec() {
+        return make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+    }
+};
+template <> struct kFlatPad<float> {
+    __device__ static __forceinline__ uint4 vec() {
+        return make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u);
+    }
+};
+
+// The range of a CTA falls into nseg <= kFlatSlots row segments; the 16 warps
+// are shared out among them in proportion to their lengths (at least one each),
+// so that every warp reads a contiguous part of a single row.
+template <typename DT>
+__global__ void __launch_bounds__(kFlatThreads, 2) sv_flat_greedy_kernel(FlatArgs a) {
+    using E = Elt<DT>;
+    constexpr int VW = E::kVec;
+    constexpr int U = 10;
+    constexpr int NW = kFlatThreads / 32;
+    __shared__ unsigned long long s_key[NW];
+    __shared__ int s_seg[NW];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int c = blockIdx.x;
+    // Launched as a programmatic dependent of whatever precedes it on the
+    // stream: wait for that grid (which may produce the logits, or still read
+    // this workspace) before touching memory; then let the finish kernel launch.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (c == 0 && tid == 0) {
+        a.hdr->magic = kMagic;
+        a.hdr->B = a.B;
+        a.hdr->k = a.k;
+        a.hdr->V = a.V;
+        a.hdr->mode = SV_MODE_GREEDY;
+        a.hdr->flat_ctas = (uint32_t)a.P;
+        a.hdr->flat_vpr = (uint32_t)a.vpr;
+        a.hdr->flat_per = (uint32_t)a.per;
+        a.hdr->flat_rem = (uint32_t)a.rem;
+    }
+    // The range: n vectors from s0; row r0 starts h vectors before it.  Segment
+    // i (row r0 + i) covers offsets [e_i, e_i+1) of the range.
+    const int s0 = flat_start(c, a.per, a.rem);
+    const int n = a.per + (c < a.rem ? 1 : 0);
+    const int r0 = s0 / a.vpr;
+    const int h = s0 - r0 * a.vpr;
+    const int e1 = min(n, a.vpr - h), e2 = min(n, e1 + a.vpr), e3 = min(n, e2 + a.vpr);
+    const int nseg = 1 + (e1 < n) + (e2 < n) + (e3 < n);
+    // First warp of segment i: i + round((NW - nseg) * e_i / n).
+    auto first_warp = [&](int i, int e) {
+        return i >= nseg ? NW : i + (2 * (NW - nseg) * e + n) / (2 * n);
+    };
+    const int w1 = first_warp(1, e1), w2 = first_warp(2, e2), w3 = first_warp(3, e3);
+    const int seg = (warp >= w1) + (warp >= w2) + (warp >= w3);
+    const int ws = seg == 0 ? 0 : seg == 1 ? w1 : seg == 2 ? w2 : w3;
+    const int we = seg == 0 ? w1 : seg == 1 ? w2 : seg == 2 ? w3 : NW;
+    const int eb = seg == 0 ? 0 : seg == 1 ? e1 : seg == 2 ? e2 : e3;
+    const int ee = seg == 0 ? e1 : seg == 1 ? e2 : seg == 2 ? e3 : n;
+    const int len = ee - eb, q = warp - ws, Q = we - ws;
+    const int lo = eb + (len * q) / Q, hi = eb + (len * (q + 1)) / Q;
+    const uint4* vp = static_cast<const uint4*>(a.logits) + s0;
+
+    float best = 0.0f;  // running maximum, valid once bidx >= 0
+    int bidx = -1;      // its element offset from the start of the range
+    bool nan = false;
+    for (int v = lo + lane; v < hi; v += U * 32) {
+        const int last = min(U - 1, (hi - 1 - v) / 32);  // last vector of the batch
+        uint4 buf[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            buf[u] = u <= last ? ld_stream16(vp + v + u * 32) : kFlatPad<DT>::vec();
+        // The batch maximum (padding is -inf, after every real vector), then
+        // the position of its first occurrence only when it beats the running
+        // maximum.
+        float m = vec_max<DT>(buf[0]);
+#pragma unroll
+        for (int u = 1; u < U; ++u) m = fmax_nan(m, vec_max<DT>(buf[u]));
+        if (m != m) {
+            nan = true;
+        } else if (bidx < 0 || m > best) {
+            int uf = 0;
+            uint4 sel = buf[0];
+#pragma unroll
+            for (int u = U - 1; u >= 0; --u)
+                if (vec_max<DT>(buf[u]) == m) {
+                    uf = u;
+                    sel = buf[u];
+                }
+            float f[VW];
+            E::unpack(sel, f);
+            int e = 0;  // the first element equal to the maximum
+#pragma unroll
+            for (int t = VW - 1; t >= 0; --t)
+                if (f[t] == m) e = t;
+            best = m;
+            bidx = (v + uf * 32) * VW + e;
+        }
+    }
+    unsigned long long kv = 0ull;
+    if (nan) {
+        kv = ~0ull;
+    } else if (bidx >= 0) {
+        // index in row r0 + seg; -0 counts as +0 (equal maxima are told apart by
+        // index alone)
+        const uint32_t idx = (uint32_t)(bidx + (h - seg * a.vpr) * VW);
+        kv = ((unsigned long long)ordered_bits(best + 0.0f) << 32) | (0xFFFFFFFFu - idx);
+    }
+    kv = warp_max_u64(kv);
+    if (lane == 0) {
+        s_key[warp] = kv;
+        s_seg[warp] = seg;
+    }
+    __syncthreads();
+    if (tid < nseg) {
+        unsigned long long m = 0ull;
+#pragma unroll
+        for (int i = 0; i < NW; ++i)
+            if (s_seg[i] == tid && s_key[i] > m) m = s_key[i];
+        const int r = r0 + tid;
+        const int word = c - flat_owner(r * a.vpr, a.per, a.rem);
+        reinterpret_cast<unsigned long long*>(a.rows + r)[word] = m;
+    }
+}
+
 // One warp per sequence: the lanes load the records in parallel, lane 0 scans.
-__global__ void sv_finish_greedy_kernel(const int32_t* __restrict__ x,
-                                        const RowRec* __restrict__ rows,
+// After the flat stream, the lanes first merge their rows' partial keys into
+// the row records (and store them, for the row statistics).
+__global__ void sv_finish_greedy_kernel(const int32_t* __restrict__ x, RowRec* __restrict__ rows,
+                                        const Header* __restrict__ hdr,
                                         uint32_t* __restrict__ seqstat, int B, int k,
                                         int32_t* __restrict__ out, int32_t* __restrict__ nacc,
                                         Epilogue ep) {
@@ -1695,11 +1900,40 @@ __global__ void sv_finish_greedy_kernel(const int32_t* __restrict__ x,
     const int wi = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.x * 4 + wi;
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the row records are complete
+    // A flat stream launched next waits for this whole grid before it writes.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (b >= B) return;
     RowRec* rr = recs[wi];
     int* xx = xs[wi];
-    for (int i = lane; i <= k; i += 32) rr[i] = rows[(long long)b * (k + 1) + i];
-    for (int i = lane; i < k; i += 32) xx[i] = x[(long long)b * k + i];
+    const uint32_t P = hdr->flat_ctas;
+    const int vpr = (int)hdr->flat_vpr, per = (int)hdr->flat_per, rem = (int)hdr->flat_rem;
+    const int V = (int)hdr->V;
+    for (int i = lane; i <= k; i += 32) {
+        const long long r = (long long)b * (k + 1) + i;
+        const int xi = i < k ? x[(long long)b * k + i] : 0;
+        RowRec rec = rows[r];
+        if (i < k) xx[i] = xi;
+        if (P) {
+            const int c0 = flat_owner((int)r * vpr, per, rem);
+            const int c1 = flat_owner((int)(r + 1) * vpr - 1, per, rem);
+            const unsigned long long* w = reinterpret_cast<const unsigned long long*>(&rec);
+            unsigned long long key = 0ull;
+            for (int c = c0; c <= c1 && c - c0 < kFlatSlots; ++c)
+                key = w[c - c0] > key ? w[c - c0] : key;
+            const bool nan = key == ~0ull;
+            const float m = from_ordered_bits((uint32_t)(key >> 32));
+            rec.mraw = nan ? NAN : m;
+            rec.S = 0.0f;
+            rec.px = i < k ? 0.0 : (double)NAN;
+            rec.lx = NAN;
+            rec.qx = NAN;
+            rec.argmax = nan ? 0 : (int32_t)(0xFFFFFFFFu - (uint32_t)key);
+            rec.flags = (nan || !(m > -INFINITY) || m == INFINITY) ? kRowBad : 0u;
+            if (i < k && (xi < 0 || xi >= V)) rec.flags |= kRowTokenBad;
+            rows[r] = rec;
+        }
+        rr[i] = rec;
+    }
     __syncwarp();
     if (lane != 0) return;
     int32_t* o = out + (long long)b * (k + 1);
@@ -2461,10 +2695,34 @@ static int rows_threads(long long ctas, long long nvec_cta, int sms) {
 // Tuning hook (spec_verify_debug_rows_split): a fixed vocabulary split and
 // thread count for the row stream of the two-kernel path (0: automatic).
 static std::atomic<int> g_force_rows_G{0}, g_force_rows_nt{0};
+// Hook (spec_verify_debug_flat): 0 automatic, 1 never the flat greedy stream.
+static std::atomic<int> g_flat_off{0};
 
+// Plan of the flat greedy stream: P ranges, one per resident CTA (two per SM)
+// and at least one per SM, each at least a third of a row long (a row meets at
+// most kFlatSlots ranges) and at most three rows long (a range meets at most
+// kFlatSlots rows).  Rows must be whole 16-byte vectors of an aligned tensor.
+static bool flat_plan(int B, int k, int V, int esz, const void* logits, int sms, FlatArgs* f) {
+    if (((long long)V * esz) % 16 != 0 || (reinterpret_cast<uintptr_t>(logits) & 15) != 0)
+        return false;
+    const long long w = (long long)V * esz / 16;
+    const long long n = (long long)B * (k + 1) * w;
+    if (n >= (1LL << 31)) return false;
+    const long long p = std::min<long long>(2LL * sms, n / ((w + 2) / 3));
+    if (p < sms || (n + p - 1) / p > 3 * w) return false;
+    f->P = (int)p;
+    f->vpr = (int)w;
+    f->per = (int)(n / p);
+    f->rem = (int)(n % p);
+    return true;
+}
+
+// `flat_ok`: a greedy stream may leave the flat layout (only the greedy finish
+// kernel reads it).
 static sv_status launch_rows(bool sampled, const void* logits, sv_dtype dt, const float* q,
                              const int32_t* x, const float* ua, float T, int B, int k, int V,
-                             void* ws, cudaStream_t stream, int sms, bool skip) {
+                             void* ws, cudaStream_t stream, int sms, bool skip,
+                             bool flat_ok = true) {
     const long long R = (long long)B * (k + 1);
     RowsArgs a;
     a.logits = logits;
@@ -2482,6 +2740,29 @@ static sv_status launch_rows(bool sampled, const void* logits, sv_dtype dt, cons
     a.c2 = log2e_over(sampled ? T : 1.0f);
     a.c = a.c2.hi;
     const int esz = dt == SV_BF16 ? 2 : 4;
+    FlatArgs f;
+    if (!sampled && !skip && flat_ok && !g_flat_off.load() && !g_force_rows_G.load() &&
+        !g_force_rows_nt.load() && flat_plan(B, k, V, esz, logits, sms, &f)) {
+        f.logits = logits;
+        f.rows = a.rows;
+        f.hdr = a.hdr;
+        f.B = B;
+        f.k = k;
+        f.V = V;
+        cudaLaunchConfig_t fc = {};
+        fc.gridDim = dim3((unsigned)f.P, 1, 1);
+        fc.blockDim = dim3(kFlatThreads, 1, 1);
+        fc.stream = stream;
+        cudaLaunchAttribute pdl;
+        pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        pdl.val.programmaticStreamSerializationAllowed = 1;
+        fc.attrs = &pdl;
+        fc.numAttrs = 1;
+        const cudaError_t fe = dt == SV_BF16
+                                   ? cudaLaunchKernelEx(&fc, sv_flat_greedy_kernel<__nv_bfloat16>, f)
+                                   : cudaLaunchKernelEx(&fc, sv_flat_greedy_kernel<float>, f);
+        return fe == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+    }
     const long long nvec_row = ((long long)V * esz + 15) / 16;
     a.G = skip ? 1 : rows_split(R, nvec_row, sms);
     int nt = skip ? 512 : rows_threads(R * a.G, nvec_row / a.G, sms);
@@ -2548,7 +2829,8 @@ static sv_status launch_finish(bool sampled, const void* logits, sv_dtype dt, co
         cfg.stream = stream;
         cfg.attrs = &pdl;
         cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, sv_finish_greedy_kernel, x, rows, seqstat, B, k, out, nacc,
+        e = cudaLaunchKernelEx(&cfg, sv_finish_greedy_kernel, x, const_cast<RowRec*>(rows),
+                               static_cast<const Header*>(ws), seqstat, B, k, out, nacc,
                                ep);
         return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
     }
@@ -2611,7 +2893,7 @@ static sv_status launch_match(const void* logits, sv_dtype dt, const int32_t* x,
                               int32_t* nacc, void* ws, cudaStream_t stream, int sms,
                               Epilogue ep) {
     sv_status st = launch_rows(false, logits, dt, nullptr, x, nullptr, 1.0f, B, k, V, ws, stream,
-                               sms, false);
+                               sms, false, false);
     if (st != SV_OK) return st;
     const RowRec* rows =
         reinterpret_cast<const RowRec*>(static_cast<char*>(ws) + ws_rows_offset());
@@ -2941,6 +3223,20 @@ int spec_verify_debug_path(sv_mode mode, int B, int V, sv_dtype dtype) {
     return (int)choose_path(mode == SV_MODE_SAMPLE, B, V, dtype == SV_BF16 ? 2 : 4, sms);
 }
 
+// Introspection (declared in include/specverify_debug.h): the flat greedy
+// stream's CTA count for these sizes (16-byte aligned logits) on the current
+// device, 0 when a greedy verify would not take it, -1 on error.
+int spec_verify_debug_flat_ctas(int B, int k, int V, sv_dtype dtype) {
+    int sms = 0;
+    if (device_setup(&sms) != SV_OK) return -1;
+    if (B < 1 || k < 1 || k > kMaxK || V < 1 || (dtype != SV_BF16 && dtype != SV_F32)) return -1;
+    if (choose_path(false, B, V, dtype == SV_BF16 ? 2 : 4, sms) != kPathTwoKernel) return 0;
+    if (g_flat_off.load() || g_force_rows_G.load() || g_force_rows_nt.load()) return 0;
+    FlatArgs f;
+    static const uint4 aligned = {};
+    return flat_plan(B, k, V, dtype == SV_BF16 ? 2 : 4, &aligned, sms, &f) ? f.P : 0;
+}
+
 // Tuning hook: the cluster size of the precise-draw kernel (1, 2, 4, 8 or 16;
 // 0 for the default).
 void spec_verify_debug_precise_split(int G) {
@@ -2956,6 +3252,8 @@ void spec_verify_debug_fused_tuning(int defer_mode, int pad_kib) {
 
 // Tuning hook: the row stream's split (G in 1..16, a power of two) and threads
 // per CTA (128, 256 or 512) on the two-kernel path; 0 for the automatic choice.
+void spec_verify_debug_flat(int off) { g_flat_off.store(off ? 1 : 0); }
+
 void spec_verify_debug_rows_split(int G, int nt) {
     if (G == 0 || G == 1 || G == 2 || G == 4 || G == 8 || G == 16) g_force_rows_G.store(G);
     if (nt == 0 || nt == 128 || nt == 256 || nt == 512 || nt == 1024) g_force_rows_nt.store(nt);

@@ -70,6 +70,10 @@ def load():
     lib.spec_verify_debug_fused_tuning.restype = None
     lib.spec_verify_debug_rows_split.argtypes = [I, I]
     lib.spec_verify_debug_rows_split.restype = None
+    lib.spec_verify_debug_flat.argtypes = [I]
+    lib.spec_verify_debug_flat.restype = None
+    lib.spec_verify_debug_flat_ctas.argtypes = [I, I, I, I]
+    lib.spec_verify_debug_flat_ctas.restype = I
     lib.spec_verify_debug_precise_split.argtypes = [I]
     lib.spec_verify_debug_precise_split.restype = None
     lib.spec_verify_debug_draw_split.argtypes = [I]
@@ -240,6 +244,20 @@ def debug_fused_tuning(defer_mode: int, pad_kib: int):
 def debug_rows_split(G: int, nt: int):
     """Tuning hook: the row stream's split and threads per CTA (0 = automatic)."""
     load().spec_verify_debug_rows_split(int(G), int(nt))
+
+
+def debug_flat(off: int):
+    """Test hook: 1 keeps greedy batches off the flat row stream (0 = automatic)."""
+    load().spec_verify_debug_flat(int(off))
+
+
+def debug_flat_ctas(B: int, k: int, V: int, dtype) -> int:
+    """CTAs of the flat greedy row stream for these sizes (0: the per-row stream)."""
+    dt = SV_BF16 if dtype in (torch.bfloat16, "bf16") else SV_F32
+    r = load().spec_verify_debug_flat_ctas(int(B), int(k), int(V), dt)
+    if r < 0:
+        raise SpecVerifyError(SV_ERR_CUDA, "spec_verify_debug_flat_ctas")
+    return r
 
 
 def debug_precise_split(G: int):
