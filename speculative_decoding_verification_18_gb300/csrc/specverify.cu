@@ -2944,10 +2944,10 @@ static sv_status launch_match(const void* logits, sv_dtype dt, const int32_t* x,
     return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
-// Paths of the one-call entry points.  Batches with a sequence for every SM
-// take the row-skipping path (the row stream in position-major order, rows past
-// a sequence's first stop never read, then one draw CTA per sequence and the
-// precise draws in 16-CTA clusters).  Smaller sampled batches whose clusters
+// Paths of the one-call entry points.  Batches with a sequence for every SM (for
+// sampled batches, every other SM) take the row-skipping path (the row stream
+// in position-major order, rows past a sequence's first stop never read, then
+// one draw CTA per sequence and the precise draws in 4-CTA clusters).  Smaller sampled batches whose clusters
 // still cover every SM take the fused per-sequence kernel (rows in waves, early
 // exit, the draw in the same launch, no second launch); the rest take the
 // two-kernel path, whose row stream spreads every row over all SMs.
@@ -2958,6 +2958,10 @@ static Path choose_path(bool sampled, int B, int V, int esz, int sms) {
     const int f = g_force_path.load();
     if (f >= kPathTwoKernel && f <= kPathSkip) return (Path)f;
     if (B >= sms) return kPathSkip;
+    // Sampled batches of at least half an SM count: measured on B = 80..128 at
+    // k = 8, V = 151936 fp32 (skipping 15-18 % faster) and B = 96 at k = 5,
+    // V = 128256 bf16 (12 % faster; 4 % slower at B = 128).
+    if (sampled && 2 * B >= sms) return kPathSkip;
     if (sampled && (long long)B * seq_split(true, B, V, esz, sms) >= sms) return kPathFused;
     return kPathTwoKernel;
 }
