@@ -584,6 +584,10 @@ struct DrawCtx {
     ff* ecache;                // [mych * 8] precise exponentials, or null
     float* thi;                // [kExpTable] each; loaded by the precise pass
     float* tlo;
+    float s_row;               // the row stream's fp32 normaliser (relative to m)
+    ff* pY;                    // [mych] one-read precise pass: chunk sums, or null
+    ff* pQ;                    // [mych]
+    unsigned char* pamb;       // [mych]
 };
 
 template <typename DT>
@@ -911,15 +915,19 @@ __device__ bool draw_fast(cg::cluster_group& cluster, DrawShared& sh, const Draw
             const int ci = blk * kBlockChunks + lane;
             float w[kChunk] = {};
             unsigned long long W = 0;
+            // this chunk's counted mass and sum of y |a| (for its own bound)
+            float relc = 0.0f, ac = 0.0f;
             if (ci < d.mych) {
                 if (d.acache) {
                     load8(d.acache + (size_t)ci * kChunk, w);
                 } else {
-                    float l[kChunk], q[kChunk], y[kChunk], absa[kChunk], unused = 0.0f;
+                    float l[kChunk], q[kChunk], y[kChunk], absa[kChunk];
                     load_l(d, ci, l);
                     load_q(d, ci, RES, q);
                     fast_y(l, d.m, d.c, d.clo, y, absa);
-                    fast_weights<RES>(y, q, inv, w, &unused);
+                    fast_weights<RES>(y, q, inv, w, &relc);
+#pragma unroll
+                    for (int e = 0; e < kChunk; ++e) ac = fmaf(y[e], absa[e], ac);
                 }
                 W = fast_chunk_value(w);
             }
@@ -941,11 +949,42 @@ __device__ bool draw_fast(cg::cluster_group& cluster, DrawShared& sh, const Draw
                         hi = h;
                     }
                 }
-                // bin edges relative to `want`: want - lo >= 2D and hi - want > 2D + 1
-                // certify the bin
+                // Bin edges relative to `want`: want - lo >= 2D and hi - want >
+                // 2D + 1 certify the bin (the edge and u times the total each
+                // within D).  Failing that, a finer certificate: the edge's and
+                // u times the total's errors sum, element by element, to (u - 1)
+                // times the errors before the edge plus u times those after it,
+                // at most max(u, 1 - u) D over the other chunks plus twice this
+                // chunk's own part b (its value and its partial sums), b being
+                // the same bound over this chunk alone.  Its mass and exponent
+                // sums come from the logits again when pass B's weights were
+                // cached.
                 if (tok >= 0) {
+                    int ok = (wc - lo >= 2 * D && hi - wc > 2 * D + 1) ? 1 : 0;
+                    if (!ok) {
+                        if (d.acache) {
+                            float l[kChunk], q[kChunk], y[kChunk], absa[kChunk], wr[kChunk];
+                            load_l(d, ci, l);
+                            load_q(d, ci, RES, q);
+                            fast_y(l, d.m, d.c, d.clo, y, absa);
+                            fast_weights<RES>(y, q, inv, wr, &relc);
+#pragma unroll
+                            for (int e = 0; e < kChunk; ++e) ac = fmaf(y[e], absa[e], ac);
+                        }
+                        const float bc =
+                            (kFastE0 * relc +
+                             kFastKappa * (ac + sh.A_tot * relc) * inv * 1.0009765625f) *
+                                1.0009765625f * 1.152921504606847e18f +
+                            (float)W * (8.0f * 5.96046448e-08f) + 3.0f;
+                        const unsigned long long b =
+                            (unsigned long long)fminf(bc, 1.0e18f) + 1ull;
+                        const float um = fmaxf(d.u, __fsub_rn(1.0f, d.u));
+                        const unsigned long long Dp =
+                            scale_floor(um, D) + (D >> 22) + 2ull + 2ull * b;
+                        ok = (wc - lo >= Dp && hi - wc > Dp + 1) ? 1 : 0;
+                    }
                     sh.token = (int)((d.c0 + ci) * kChunk + tok);
-                    sh.cert = (wc - lo >= 2 * D && hi - wc > 2 * D + 1) ? 1 : 0;
+                    sh.cert = ok;
                 }
             }
         }
@@ -1144,6 +1183,175 @@ __device__ void draw_precise(cg::cluster_group& cluster, DrawShared& sh, const D
     }
 }
 
+// ---- precise pass in one read
+//
+// The weight of element j is p_j = e_j / S (bonus draw) or max(0, e_j / S - q_j)
+// (residual), with e_j = exp((l_j - m)/T) in float-float.  Whether e_j / S
+// exceeds q_j is settled for almost every element by the row stream's fp32
+// normaliser: with it within 2^-12 of S (checked), e_j.hi / S_row above
+// q_j (1 + 2^-10) means a positive weight and below q_j (1 - 2^-10) a zero one.
+// A chunk whose elements are all settled has the weight Y_c / S - Q_c, with Y_c
+// and Q_c the float-float sums of e_j and q_j over its positive elements, so a
+// single pass over the logits and q forms S and every (Y_c, Q_c) at once; a
+// chunk with an unsettled element is recomputed element by element once S is
+// known.  Inside a chunk the cumulative weights are the same linear form of the
+// partial sums, accumulated in the same order, so the last equals the chunk's.
+
+constexpr float kP1Hi = 1.0f + 1.0f / 1024.0f, kP1Lo = 1.0f - 1.0f / 1024.0f;
+
+// y * inv - q for float-float y, inv, q (the difference of two non-negative
+// values), clamped at zero.
+__device__ __forceinline__ ff p1_linear(ff y, ff inv, ff q) {
+    const ff a = ff_mul(ff_normalize(y), inv);
+    const ff qn = ff_normalize(q);
+    const ff s = two_sum(a.hi, -qn.hi);
+    const ff w = fast_two_sum(s.hi, __fadd_rn(s.lo, __fsub_rn(a.lo, qn.lo)));
+    return w.hi > 0.0f ? w : ff{0.0f, 0.0f};
+}
+
+// One chunk's pass: the exponentials into S, and into (Y, Q) those of settled
+// positive elements; `amb` when an element is not settled.  With `want` and
+// `token` (the search inside a settled chunk), also the first element whose
+// cumulative weight exceeds `want`.
+template <typename DT, bool RES>
+__device__ __forceinline__ void p1_chunk(const DrawCtx<DT>& d, const float* l, const float* q,
+                                         float inv_row, ff& S, ff& Y, ff& Q, bool& amb,
+                                         ff inv = ff{0.0f, 0.0f}, unsigned long long want = 0ull,
+                                         int* token = nullptr) {
+#pragma unroll
+    for (int e = 0; e < kChunk; ++e) {
+        const ff ev = exp_rel(l[e], d.m, d.c2, d.thi, d.tlo);
+        ff_accumulate(S, ev);
+        bool pos = true;
+        if (RES) {
+            const float ph = __fmul_rn(ev.hi, inv_row), qe = q[e];
+            pos = qe >= 0.0f && ph > __fmul_rn(qe, kP1Hi);
+            const bool zero = qe >= 0.0f && (ev.hi == 0.0f || ph < __fmul_rn(qe, kP1Lo));
+            amb |= !pos && !zero;
+            if (pos) ff_accumulate(Q, ff{qe, 0.0f});
+        }
+        if (pos) ff_accumulate(Y, ev);
+        if (token && *token < 0 && pos && ev.hi > 0.0f &&
+            to_fixed(ff_normalize(p1_linear(Y, inv, Q))) > want)
+            *token = e;
+    }
+}
+
+// Fixed-point weight of chunk ci from the table (or, for an unsettled chunk,
+// recomputed element by element as the two-pass precise draw does).
+template <typename DT, bool RES>
+__device__ __forceinline__ unsigned long long p1_value(const DrawCtx<DT>& d, int ci, ff inv) {
+    if (RES && d.pamb[ci]) {
+        float l[kChunk], q[kChunk];
+        load_l(d, ci, l);
+        load_q(d, ci, true, q);
+        return precise_chunk<DT, true, false, false>(d, ci, l, q, inv, 0ull, nullptr);
+    }
+    return to_fixed(ff_normalize(p1_linear(d.pY[ci], inv, d.pQ[ci])));
+}
+
+// The precise draw in one read of the slices (the chunk table must fit:
+// d.pY).  Returns false, in every thread of every CTA, when it cannot decide:
+// the row stream's normaliser is more than 2^-12 from S, or the residual has no
+// mass; the caller then runs the two-pass draw.
+template <typename DT, bool RES>
+__device__ bool draw_precise_1p(cg::cluster_group& cluster, DrawShared& sh, const DrawCtx<DT>& d) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int i = tid; i < kExpTable; i += kThreads) {
+        d.thi[i] = g_exp2_table.hi[i];
+        d.tlo[i] = g_exp2_table.lo[i];
+    }
+    __syncthreads();
+    const float inv_row = RES ? __frcp_rn(d.s_row) : 0.0f;
+    // The pass: S, and each chunk's (Y, Q) and flag into the table.
+    ff accS{0.0f, 0.0f};
+    float nl[kChunk] = {}, nq[kChunk] = {};
+    if (tid < d.mych) {
+        load_l(d, tid, nl);
+        load_q(d, tid, RES, nq);
+    }
+    for (int ci = tid; ci < d.mych; ci += kThreads) {
+        float l[kChunk], q[kChunk];
+#pragma unroll
+        for (int e = 0; e < kChunk; ++e) {
+            l[e] = nl[e];
+            q[e] = nq[e];
+        }
+        if (ci + kThreads < d.mych) {
+            load_l(d, ci + kThreads, nl);
+            load_q(d, ci + kThreads, RES, nq);
+        }
+        ff Y{0.0f, 0.0f}, Q{0.0f, 0.0f};
+        bool amb = false;
+        p1_chunk<DT, RES>(d, l, q, inv_row, accS, Y, Q, amb);
+        d.pY[ci] = Y;
+        d.pQ[ci] = Q;
+        d.pamb[ci] = amb ? 1 : 0;
+    }
+    const ff S = cluster_sum_ff(cluster, sh, sh.xS[1], accS, d.rank, d.G);
+    if (RES && !(fabsf(__fsub_rn(S.hi, d.s_row)) <= S.hi * (1.0f / 4096.0f))) return false;
+    const ff inv = ff_recip(S);
+    // Chunk values into block totals, then the cluster prefix.
+    unsigned long long tacc = 0;
+    for (int base = warp * kBlockChunks; base < d.mych; base += kThreads) {
+        const int ci = base + lane;
+        const unsigned long long W = ci < d.mych ? p1_value<DT, RES>(d, ci, inv) : 0ull;
+        const unsigned long long bw = warp_sum(W);
+        if (lane == 0) {
+            d.bsum[base / kBlockChunks] = bw;
+            tacc += bw;
+        }
+    }
+    cluster_prefix(cluster, sh, sh.xW[1], nullptr, tacc, 0.0f, d.rank, d.G);
+    const unsigned long long prefix = sh.prefix, total = sh.total, mytot = sh.mytot;
+    if (total == 0) return false;  // zero residual mass: the two-pass draw handles it
+    const unsigned long long tau = scale_floor(d.u, total);
+    const bool owner = mytot > 0 && prefix <= tau && tau - prefix < mytot;
+    if (owner) {  // uniform across the CTA
+        const unsigned long long want = tau - prefix;
+        int blk;
+        unsigned long long bbefore;
+        find_block(sh, d.bsum, d.nblk, want, &blk, &bbefore);
+        if (warp == 0) {
+            const int ci = blk * kBlockChunks + lane;
+            const unsigned long long W = ci < d.mych ? p1_value<DT, RES>(d, ci, inv) : 0ull;
+            const unsigned long long wb = want - bbefore;
+            unsigned long long cb;
+            if (find_lane(W, wb, &cb)) {
+                int tok = -1;
+                float l[kChunk], q[kChunk] = {};
+                load_l(d, ci, l);
+                load_q(d, ci, RES, q);
+                if (RES && d.pamb[ci]) {
+                    precise_chunk<DT, true, false, false>(d, ci, l, q, inv, wb - cb, &tok);
+                } else {
+                    ff S1{0.0f, 0.0f}, Y{0.0f, 0.0f}, Q{0.0f, 0.0f};
+                    bool amb = false;
+                    p1_chunk<DT, RES>(d, l, q, inv_row, S1, Y, Q, amb, inv, wb - cb, &tok);
+                }
+                if (tok >= 0) sh.token = (int)((d.c0 + ci) * kChunk + tok);
+            }
+        }
+    }
+    return true;
+}
+
+// The precise draw: in one read when the chunk table fits and the row's
+// normaliser settles the residual's signs, else in two passes.
+template <typename DT>
+__device__ void draw_precise_any(cg::cluster_group& cluster, DrawShared& sh,
+                                 const DrawCtx<DT>& d, bool& degenerate) {
+    degenerate = false;
+    if (d.pY) {
+        const bool done = d.residual ? draw_precise_1p<DT, true>(cluster, sh, d)
+                                     : draw_precise_1p<DT, false>(cluster, sh, d);
+        if (done) return;
+        if (threadIdx.x == 0) sh.token = -1;
+        xsync(cluster, d.G);  // the table's place is the two-pass draw's cache
+    }
+    draw_precise<DT>(cluster, sh, d, degenerate);
+}
+
 // Dynamic shared memory of a draw: block totals, the 2^(i/1024) table, and a
 // cache of the CTA's slice (level 1: fp32 exponents for the fast pass; level 2:
 // also room for the float-float exponentials of the precise pass).
@@ -1162,17 +1370,30 @@ __host__ __device__ inline size_t draw_bsum_bytes(int V, int G) {
     const long long nblk = (draw_slice_chunks(V, G) + kBlockChunks - 1) / kBlockChunks;
     return ((size_t)nblk * 8 + 15) & ~(size_t)15;
 }
+// Dynamic shared memory a draw may use: two 512-thread CTAs of the drawing
+// kernels still fit on one SM.
+constexpr size_t kDrawSmemBudget = 96 * 1024;
+// The one-read precise pass's chunk table: two float-float sums and a flag
+// per chunk of the slice.
+__host__ __device__ inline size_t precise_table_bytes(int V, int G) {
+    const size_t nch = (size_t)draw_slice_chunks(V, G);
+    return nch * 2 * sizeof(ff) + ((nch + 15) & ~(size_t)15);
+}
 __host__ __device__ inline size_t draw_smem_bytes(int V, int G, int level) {
     const size_t slice = (size_t)draw_slice_chunks(V, G) * kChunk;
-    return draw_bsum_bytes(V, G) + 2 * kExpTable * sizeof(float) +
-           (level >= 2 ? slice * sizeof(ff) : level == 1 ? slice * sizeof(float) : 0);
+    const size_t base = draw_bsum_bytes(V, G) + 2 * kExpTable * sizeof(float);
+    const size_t cache =
+        level >= 2 ? slice * sizeof(ff) : level == 1 ? slice * sizeof(float) : 0;
+    const size_t tab = precise_table_bytes(V, G);
+    return base + (tab > cache && base + tab <= kDrawSmemBudget ? tab : cache);
 }
 
 template <typename DT>
 __device__ __forceinline__ DrawCtx<DT> make_draw_ctx(unsigned char* dyn, int level, bool prefetch,
                                                     const DT* rowp, const float* qrow,
                                                     bool residual, int V, float m, float c,
-                                                    ff c2, float u, int rank, int G) {
+                                                    ff c2, float u, int rank, int G,
+                                                    float s_row) {
     DrawCtx<DT> d;
     d.prefetch = prefetch;
     d.rowp = rowp;
@@ -1201,6 +1422,14 @@ __device__ __forceinline__ DrawCtx<DT> make_draw_ctx(unsigned char* dyn, int lev
     unsigned char* cache = dyn + bb + 2 * kExpTable * sizeof(float);
     d.acache = level >= 1 ? reinterpret_cast<float*>(cache) : nullptr;
     d.ecache = level >= 2 ? reinterpret_cast<ff*>(cache) : nullptr;
+    // The chunk table of the one-read precise pass shares the cache's place
+    // (the fast pass is over when it is written).
+    d.s_row = s_row;
+    const bool tab = bb + 2 * kExpTable * sizeof(float) + precise_table_bytes(V, G) <=
+                     kDrawSmemBudget;
+    d.pY = tab ? reinterpret_cast<ff*>(cache) : nullptr;
+    d.pQ = tab ? d.pY + d.mych : nullptr;
+    d.pamb = tab ? reinterpret_cast<unsigned char*>(d.pQ + d.mych) : nullptr;
     return d;
 }
 
@@ -1233,7 +1462,7 @@ __device__ bool draw(cg::cluster_group& cluster, DrawShared& sh, const DrawCtx<D
     if (defer_precise) return true;
     if (threadIdx.x == 0) sh.token = -1;
     __syncthreads();
-    draw_precise<DT>(cluster, sh, d, degenerate);
+    draw_precise_any<DT>(cluster, sh, d, degenerate);
     __syncthreads();
     if (threadIdx.x == 0 && sh.token >= 0) *token_out = sh.token;
     return false;
@@ -1501,7 +1730,7 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(VerifyArgs a) {
     bool degenerate = false, fallback = false;
     const DrawCtx<DT> dc =
         make_draw_ctx<DT>(dyn, a.draw_level, a.prefetch != 0, drow, qrow, n < k, V, m, a.c, a.c2,
-                          u, rank, G);
+                          u, rank, G, fs.rowstat[n - wave_row0].s);
     const bool deferred = draw<DT>(cluster, ds, dc, a.force_precise != 0, a.plist != nullptr,
                                    o + n, degenerate, fallback);
     if (rank == 0) {
@@ -2051,7 +2280,8 @@ __global__ void __launch_bounds__(kThreads, 2) sv_finish_sample_kernel(FinishArg
     const float* qrow = n < k ? a.q + ((long long)b * k + n) * V : nullptr;
     bool degenerate = false, fallback = false;
     const DrawCtx<DT> dc = make_draw_ctx<DT>(dyn, a.draw_level, a.prefetch != 0, drow, qrow, n < k,
-                                             V, recs[n].mraw, a.c, a.c2, s_ur, rank, G);
+                                             V, recs[n].mraw, a.c, a.c2, s_ur, rank, G,
+                                             recs[n].S);
     const bool deferred = draw<DT>(cluster, ds, dc, a.force_precise != 0, a.plist != nullptr,
                                    o + n, degenerate, fallback);
     if (rank == 0) {
@@ -2105,13 +2335,13 @@ __global__ void __launch_bounds__(kThreads, 2) sv_precise_kernel(PreciseArgs a) 
         const int n = a.nacc[b];
         const DT* drow = static_cast<const DT*>(a.logits) + ((long long)b * (k + 1) + n) * V;
         const float* qrow = n < k ? a.q + ((long long)b * k + n) * V : nullptr;
-        const float m = a.rows[(long long)b * (k + 1) + n].mraw;
+        const RowRec& rec = a.rows[(long long)b * (k + 1) + n];
         const DrawCtx<DT> dc = make_draw_ctx<DT>(dyn, a.draw_level, false, drow, qrow, n < k, V,
-                                                 m, a.c, a.c2, a.ur[b], rank, G);
+                                                 rec.mraw, a.c, a.c2, a.ur[b], rank, G, rec.S);
         if (tid == 0) ds.token = -1;
         __syncthreads();
         bool degenerate = false;
-        draw_precise<DT>(cluster, ds, dc, degenerate);
+        draw_precise_any<DT>(cluster, ds, dc, degenerate);
         __syncthreads();
         if (tid == 0 && ds.token >= 0) a.out[(long long)b * (k + 1) + n] = ds.token;
         if (rank == 0 && tid == 0 && degenerate)
@@ -2163,7 +2393,7 @@ __global__ void __launch_bounds__(kThreads, 2) sv_match_draw_kernel(MatchArgs a)
     if ((rec.flags & (kRowBad | kRowSkipped)) || !(s_u >= 0.0f && s_u < 1.0f)) return;
     const DT* rowp = static_cast<const DT*>(a.logits) + row * (long long)V;
     const DrawCtx<DT> dc = make_draw_ctx<DT>(dyn, a.draw_level, a.prefetch != 0, rowp, nullptr,
-                                             false, V, rec.mraw, a.c, a.c2, s_u, rank, G);
+                                             false, V, rec.mraw, a.c, a.c2, s_u, rank, G, rec.S);
     bool degenerate = false, fallback = false;
     draw<DT>(cluster, ds, dc, a.force_precise != 0, false, a.out + row, degenerate, fallback);
 }
@@ -2364,9 +2594,6 @@ static std::mutex g_mu;
 static DeviceInfo g_dev[64];
 
 constexpr size_t kDynSmemMax = 160 * 1024;  // attribute of the kernels that draw
-// Dynamic shared memory a draw may use for its slice cache: two 512-thread CTAs
-// of the drawing kernels still fit on one SM.
-constexpr size_t kDrawSmemBudget = 96 * 1024;
 
 // Whether the draws of a launch prefetch their slices (decision row and q row)
 // into L2 in bulk: only when all of them fit in a third of the L2 together, so
