@@ -64,6 +64,13 @@ def _load():
     lib.orc_ngram_draft.restype = ctypes.c_int
     lib.orc_max_threads.argtypes = []
     lib.orc_max_threads.restype = ctypes.c_int
+    lib.orc_tree_seq.argtypes = [ctypes.c_int, P, P, P, P, P, ctypes.c_double, ctypes.c_double,
+                                 ctypes.c_int, ctypes.c_int, P, P, P, P, P, P, P]
+    lib.orc_tree_seq.restype = None
+    lib.orc_tree_batch.argtypes = [ctypes.c_int, P, ctypes.c_int, P, P, P, P, P, ctypes.c_float,
+                                   ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, P, P, P, P,
+                                   P, P, P, ctypes.c_int]
+    lib.orc_tree_batch.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -192,3 +199,70 @@ def ngram_draft(history, lengths, k: int, n_min: int, n_max: int):
     if rc != 0:
         raise ValueError("oracle rejected its arguments")
     return draft, num
+
+
+@dataclass
+class TreeResult:
+    out: np.ndarray         # [N] or [B, N] accepted tokens, the emitted token, -1 after
+    nodes: np.ndarray       # [N] or [B, N] accepted node indices, -1 after
+    n: np.ndarray           # accepted count(s), -1 for an invalid sequence
+    thr: np.ndarray         # min(1, r(x)/q(x)) of each tested child, NaN elsewhere
+    draw_lo: np.ndarray
+    draw_hi: np.ndarray
+    flags: np.ndarray
+    row_m: np.ndarray = None       # [B, N] (batch form)
+    row_argmax: np.ndarray = None  # [B, N] (batch form)
+
+
+def tree_seq(mode, logits, q, tok, par, ua, ur, T) -> TreeResult:
+    """One sequence's tree walk with float64 inputs: logits [N, V], q [N, V]
+    (sampled), tok / par [N], ua [N], ur."""
+    logits = np.ascontiguousarray(logits, dtype=np.float64)
+    N, V = logits.shape
+    qq = None if q is None else np.ascontiguousarray(q, dtype=np.float64)
+    tok = np.ascontiguousarray(tok, dtype=np.int32)
+    par = np.ascontiguousarray(par, dtype=np.int32)
+    uu = None if ua is None else np.ascontiguousarray(ua, dtype=np.float64)
+    out = np.zeros(N, np.int32)
+    nodes = np.zeros(N, np.int32)
+    n = np.zeros(1, np.int32)
+    thr = np.zeros(N)
+    lo, hi = np.zeros(1), np.zeros(1)
+    fl = np.zeros(1, np.int32)
+    _load().orc_tree_seq(int(mode), _ptr(logits), _ptr(qq), _ptr(tok), _ptr(par), _ptr(uu),
+                         float(0.0 if ur is None else ur), float(T), N, V, _ptr(out),
+                         _ptr(nodes), _ptr(n), _ptr(thr), _ptr(lo), _ptr(hi), _ptr(fl))
+    return TreeResult(out, nodes, int(n[0]), thr, float(lo[0]), float(hi[0]), int(fl[0]))
+
+
+def tree_batch(mode, logits, dtype: str, q, tok, par, ua, ur, T, nthreads: int = 0):
+    """Batch tree walk over inputs in the device layouts: logits [B, N, V] (uint16
+    bf16 bit patterns or float32), q [B, N, V] float32 (sampled), tok / par
+    [B, N] int32, ua [B, N] float32, ur [B] float32."""
+    B, N, V = logits.shape
+    if dtype == "bf16":
+        logits = np.ascontiguousarray(logits, dtype=np.uint16)
+        dt = 0
+    elif dtype == "f32":
+        logits = np.ascontiguousarray(logits, dtype=np.float32)
+        dt = 1
+    else:
+        raise ValueError(dtype)
+    greedy = mode == GREEDY
+    qq = None if greedy else np.ascontiguousarray(q, dtype=np.float32)
+    uu = None if greedy else np.ascontiguousarray(ua, dtype=np.float32)
+    rr = None if greedy else np.ascontiguousarray(ur, dtype=np.float32)
+    tok = np.ascontiguousarray(tok, dtype=np.int32)
+    par = np.ascontiguousarray(par, dtype=np.int32)
+    r = TreeResult(out=np.zeros((B, N), np.int32), nodes=np.zeros((B, N), np.int32),
+                   n=np.zeros(B, np.int32), thr=np.zeros((B, N)), draw_lo=np.zeros(B),
+                   draw_hi=np.zeros(B), flags=np.zeros(B, np.int32),
+                   row_m=np.zeros((B, N)), row_argmax=np.zeros((B, N), np.int32))
+    rc = _load().orc_tree_batch(
+        int(mode), _ptr(logits), dt, _ptr(qq), _ptr(tok), _ptr(par), _ptr(uu), _ptr(rr),
+        float(T), B, N, V, _ptr(r.out), _ptr(r.nodes), _ptr(r.n), _ptr(r.row_m),
+        _ptr(r.row_argmax), _ptr(r.thr), _ptr(r.draw_lo), _ptr(r.draw_hi), _ptr(r.flags),
+        int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    return r

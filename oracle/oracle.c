@@ -426,3 +426,182 @@ int orc_verify_batch(int mode, const void* logits, int dtype, const float* q,
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------ tree walk */
+
+static void tree_invalid(int N, int32_t* out, int32_t* nodes, int32_t* n_acc,
+                         int32_t* flags) {
+    for (int i = 0; i < N; ++i) {
+        out[i] = -1;
+        nodes[i] = -1;
+    }
+    *n_acc = -1;
+    if (flags) *flags |= ORC_F_BAD;
+}
+
+void orc_tree_seq(int mode, const double* logits, const double* q, const int32_t* tok,
+                  const int32_t* par, const double* ua, double ur, double T, int N, int V,
+                  int32_t* out, int32_t* nodes, int32_t* n_acc, double* thr, double* draw_lo,
+                  double* draw_hi, int32_t* flags) {
+    const int greedy = (mode == ORC_GREEDY);
+    const double Tr = greedy ? 1.0 : T;
+    if (flags) *flags = 0;
+    if (thr)
+        for (int j = 0; j < N; ++j) thr[j] = NAN;
+    if (draw_lo) *draw_lo = NAN;
+    if (draw_hi) *draw_hi = NAN;
+    for (int j = 1; j < N; ++j)
+        if (par[j] < 0 || par[j] >= j) {
+            tree_invalid(N, out, nodes, n_acc, flags);
+            return;
+        }
+    double* p = greedy ? NULL : (double*)malloc(sizeof(double) * (size_t)V);
+    double* r = greedy ? NULL : (double*)malloc(sizeof(double) * (size_t)V);
+    double* w = greedy ? NULL : (double*)malloc(sizeof(double) * (size_t)V);
+    int cur = 0, n = 0, token = -1, bad = 0;
+    for (;;) {
+        const double* lc = logits + (size_t)cur * V;
+        double m, S;
+        int32_t am;
+        if (orc_row_stats(lc, Tr, V, &m, &S, &am)) {
+            bad = 1;
+            break;
+        }
+        if (!greedy) {
+            /* r = p, and w (the weights r is the normalisation of) = p too */
+            for (int j = 0; j < V; ++j) {
+                p[j] = row_p(lc, Tr, m, S, j);
+                r[j] = p[j];
+                w[j] = p[j];
+            }
+        }
+        const double* qc = greedy ? NULL : q + (size_t)cur * V;
+        int next = -1;
+        for (int j = cur + 1; j < N && next < 0 && !bad; ++j) {
+            if (par[j] != cur) continue;
+            const int x = tok[j];
+            if (x < 0 || x >= V) {
+                bad = 1;
+                break;
+            }
+            if (greedy) {
+                if (x == am) next = j;
+                continue;
+            }
+            const double u = ua[j], Q = qc[x], P = r[x];
+            if (!(u >= 0.0 && u < 1.0) || isnan(Q) || Q < 0.0) {
+                bad = 1;
+                break;
+            }
+            if (thr) thr[j] = (P >= Q) ? 1.0 : P / Q;
+            if (P >= Q || u < P / Q) {
+                next = j;
+                break;
+            }
+            /* rejected: r becomes the normalised residual max(0, r - q) */
+            double Z = 0.0;
+            for (int v = 0; v < V; ++v) {
+                w[v] = (r[v] > qc[v]) ? r[v] - qc[v] : 0.0;
+                Z += w[v];
+            }
+            if (Z > 0.0) {
+                for (int v = 0; v < V; ++v) r[v] = w[v] / Z;
+            } else { /* zero residual mass: back to p */
+                for (int v = 0; v < V; ++v) {
+                    r[v] = p[v];
+                    w[v] = p[v];
+                }
+                if (flags) *flags |= ORC_F_DEGENERATE;
+            }
+        }
+        if (bad) break;
+        if (next >= 0) {
+            nodes[n] = next;
+            out[n] = tok[next];
+            ++n;
+            cur = next;
+            continue;
+        }
+        if (greedy) {
+            token = am;
+        } else {
+            if (!(ur >= 0.0 && ur < 1.0)) {
+                bad = 1;
+                break;
+            }
+            double lo, hi;
+            int ovf;
+            token = categorical(w, V, ur, &lo, &hi, &ovf);
+            if (ovf && flags) *flags |= ORC_F_OVERFLOW;
+            if (draw_lo) *draw_lo = lo;
+            if (draw_hi) *draw_hi = hi;
+        }
+        break;
+    }
+    free(p);
+    free(r);
+    free(w);
+    if (bad) {
+        tree_invalid(N, out, nodes, n_acc, flags);
+        return;
+    }
+    out[n] = token;
+    for (int i = n + 1; i < N; ++i) out[i] = -1;
+    for (int i = n; i < N; ++i) nodes[i] = -1;
+    *n_acc = n;
+}
+
+int orc_tree_batch(int mode, const void* logits, int dtype, const float* q, const int32_t* tok,
+                   const int32_t* par, const float* ua, const float* ur, float T, int B, int N,
+                   int V, int32_t* out, int32_t* nodes, int32_t* n_acc, double* row_m,
+                   int32_t* row_argmax, double* thr, double* draw_lo, double* draw_hi,
+                   int32_t* flags, int nthreads) {
+    if (B < 0 || N < 1 || V < 1 || !logits || !tok || !par || !out || !nodes || !n_acc)
+        return -1;
+    if (dtype != 0 && dtype != 1) return -1;
+    if (mode != ORC_SAMPLE && mode != ORC_GREEDY) return -1;
+    const int greedy = (mode == ORC_GREEDY);
+    if (!greedy && (!q || !ua || !ur)) return -1;
+    const double Td = greedy ? 1.0 : (double)T;
+    const size_t seqsz = (size_t)N * V;
+    int nt = nthreads > 0 ? nthreads : orc_max_threads();
+    (void)nt;
+#pragma omp parallel num_threads(nt)
+    {
+        double* L = (double*)malloc(sizeof(double) * seqsz);
+        double* Qd = greedy ? NULL : (double*)malloc(sizeof(double) * seqsz);
+        double* ua_d = (double*)malloc(sizeof(double) * (size_t)N);
+#pragma omp for schedule(dynamic, 1)
+        for (int b = 0; b < B; ++b) {
+            if (dtype == 0) {
+                const uint16_t* src = (const uint16_t*)logits + (size_t)b * seqsz;
+                for (size_t j = 0; j < seqsz; ++j) L[j] = bf16_to_double(src[j]);
+            } else {
+                const float* src = (const float*)logits + (size_t)b * seqsz;
+                for (size_t j = 0; j < seqsz; ++j) L[j] = (double)src[j];
+            }
+            if (!greedy) {
+                const float* qs = q + (size_t)b * seqsz;
+                for (size_t j = 0; j < seqsz; ++j) Qd[j] = (double)qs[j];
+                for (int j = 0; j < N; ++j) ua_d[j] = (double)ua[(size_t)b * N + j];
+            }
+            for (int i = 0; i < N; ++i) {
+                double m, S;
+                int32_t am;
+                orc_row_stats(L + (size_t)i * V, Td, V, &m, &S, &am);
+                if (row_m) row_m[(size_t)b * N + i] = m;
+                if (row_argmax) row_argmax[(size_t)b * N + i] = am;
+            }
+            int32_t fl = 0;
+            orc_tree_seq(mode, L, Qd, tok + (size_t)b * N, par + (size_t)b * N, ua_d,
+                         greedy ? 0.0 : (double)ur[b], Td, N, V, out + (size_t)b * N,
+                         nodes + (size_t)b * N, n_acc + b, thr ? thr + (size_t)b * N : NULL,
+                         draw_lo ? draw_lo + b : NULL, draw_hi ? draw_hi + b : NULL, &fl);
+            if (flags) flags[b] = fl;
+        }
+        free(L);
+        free(Qd);
+        free(ua_d);
+    }
+    return 0;
+}

@@ -98,6 +98,52 @@ int orc_max_threads(void);
 int orc_ngram_draft(const int32_t* history, const int32_t* lengths, int B, int Lmax, int k,
                     int n_min, int n_max, int32_t* draft, int32_t* num);
 
+/* Tree verification of several candidates at once ([DEE] §"A família de
+ * rascunhos", Medusa: extra heads propose several continuations that the
+ * target checks in one pass with tree attention; [SDF] §"Tree attention": how
+ * Medusa and EAGLE-2 verify several candidates).  The pages give the idea, not
+ * a rule; this is the plainest exact reading, which reduces to the chain rule
+ * when every node has one child.
+ *
+ * One sequence's tree of N nodes: node 0 is the root (the last committed
+ * token); node j >= 1 carries the drafted token tok[j] and its parent par[j],
+ * 0 <= par[j] < j.  logits [N][V]: the target's logits at each node (the
+ * distribution of the token after it).  q [N][V] (sampled): the draft
+ * distribution at each node, from which its children were drawn independently.
+ * ua [N]: the uniform of the test of child j (ua[0] unused); ur: the final draw.
+ *
+ * The walk starts at the root.  Greedy: the first child (in index order) whose
+ * token is the argmax of the current node is accepted and the walk moves to
+ * it; when none is, the argmax is emitted.  Sampled (recursive rejection over
+ * the children): the current distribution r starts as p = softmax(l/T) of the
+ * node; each child j in index order is accepted iff r(x) >= q(x) or
+ * ua[j] < r(x)/q(x), x = tok[j], q the node's draft distribution; on
+ * rejection r becomes the normalised residual max(0, r - q) (or p again, with
+ * ORC_F_DEGENERATE, when that has no mass).  After an acceptance the walk
+ * moves to the child with r = its own p; when no child is accepted the final
+ * token is drawn from r (step 4's rule on the unnormalised residual weights)
+ * with ur.  Each tested child contributes thr[j] = min(1, r(x)/q(x)).
+ *
+ * Outputs: out [N] (the accepted tokens, the emitted token, -1 after),
+ * nodes [N] (the accepted node indices, -1 after), *n_acc (-1 if invalid:
+ * a bad parent anywhere, or a row, token, uniform or q(x) the walk needs),
+ * thr [N] (NaN for untested nodes), draw_lo / draw_hi, flags. */
+void orc_tree_seq(int mode, const double* logits, const double* q, const int32_t* tok,
+                  const int32_t* par, const double* ua, double ur, double T, int N, int V,
+                  int32_t* out, int32_t* nodes, int32_t* n_acc, double* thr, double* draw_lo,
+                  double* draw_hi, int32_t* flags);
+
+/* Batch form: logits [B][N][V] (bf16 bit patterns, dtype 0, or float32,
+ * dtype 1), q [B][N][V] float32, tok / par [B][N] int32, ua [B][N] float32,
+ * ur [B] float32; out / nodes [B][N], n_acc [B]; row_m, row_argmax [B][N] and
+ * thr [B][N], draw_lo, draw_hi, flags [B] may be NULL.  Returns 0, or -1 on
+ * bad arguments. */
+int orc_tree_batch(int mode, const void* logits, int dtype, const float* q, const int32_t* tok,
+                   const int32_t* par, const float* ua, const float* ur, float T, int B, int N,
+                   int V, int32_t* out, int32_t* nodes, int32_t* n_acc, double* row_m,
+                   int32_t* row_argmax, double* thr, double* draw_lo, double* draw_hi,
+                   int32_t* flags, int nthreads);
+
 #ifdef __cplusplus
 }
 #endif
