@@ -86,6 +86,7 @@ typedef enum { SV_MODE_SAMPLE = 0, SV_MODE_GREEDY = 1 } sv_mode;
 #define SV_DEV_BAD_Q 0x8u        /* q_i(x_i) NaN or negative at a reached position */
 #define SV_DEV_DEGENERATE 0x10u  /* informational: a zero-mass residual drew from p */
 #define SV_DEV_PRECISE 0x20u     /* informational: a draw needed the float-float pass */
+#define SV_DEV_BAD_TREE 0x40u    /* spec_verify_tree: a parent index outside [0, j) at node j */
 
 /* Bytes of workspace the calls below need for these sizes (0 for invalid sizes). */
 size_t spec_verify_workspace_size(int B, int k, int V, sv_dtype dtype);
@@ -146,6 +147,47 @@ sv_status spec_verify_match(const void* logits, sv_dtype dtype, const int32_t* d
                             const float* u_draw, const float* u_bonus, float T, int B, int k,
                             int V, int32_t* out_tokens, int32_t* num_accepted, void* ws,
                             size_t ws_bytes, cudaStream_t stream);
+
+/* Tree verification: several drafted continuations checked at once
+ * ("Decodificação especulativa explicada", §"A família de rascunhos": Medusa
+ * verifies candidate continuations with tree attention; "Speculative decoding:
+ * el secretario...", §"Tree attention").  The pages name the technique but give
+ * no acceptance rule; this is the plainest exact one, and with one child per
+ * node it is spec_verify_greedy / spec_verify_sample.
+ *   Each sequence drafts a tree of N nodes (2 <= N <= 65): node 0 is the root
+ *   (the last committed token), node j >= 1 a drafted token whose parent
+ *   precedes it.
+ *   logits [B, N, V] bf16/fp32: the target's logits at each node (row j: the
+ *     distribution of the token after node j), e.g. from one tree-attention pass;
+ *   tree_tokens [B, N] int32: node j's token (entry 0 unused);
+ *   tree_parents [B, N] int32: node j's parent, 0 <= parent < j (entry 0 unused);
+ *   draft_probs [B, N, V] fp32 (sampled): the draft distribution at each node,
+ *     from which that node's children were drawn, independently;
+ *   u_accept [B, N] fp32 (sampled): the uniform of child j's test (entry 0 unused);
+ *   u_resample [B] fp32 (sampled): the uniform of the final draw.
+ * The walk starts at the root.  Greedy: the first child (in index order) whose
+ * token is the node's argmax is accepted and the walk moves on to it; when none
+ * is, the argmax is emitted.  Sampled: the node's current distribution r starts
+ * as p = softmax(logits/T); child j (token x) is accepted iff r(x) >= q(x) or
+ * u_accept[j] < r(x)/q(x); a rejection replaces r by the normalised residual
+ * max(0, r - q) (by p again when that has no mass: SV_DEV_DEGENERATE); an
+ * accepted child continues the walk with its own p; when no child of the node
+ * is accepted the token is drawn from r with u_resample (the categorical rule
+ * of spec_verify_sample, in fp32 weights with float64 sums).
+ *   out_tokens [B, N]: the accepted tokens, then the emitted one, -1 after;
+ *   out_nodes [B, N]: the accepted node indices (to keep their KV entries), -1
+ *     after;
+ *   num_accepted [B]: the accepted count, or -1 for an invalid sequence (a
+ *     parent outside [0, j): SV_DEV_BAD_TREE; or a row, token, uniform or q(x)
+ *     the walk reaches that is bad, as for the chain).
+ * Workspace: spec_verify_workspace_size(B, N - 1, V, dtype) bytes; status and
+ * row statistics as for the chain calls (row_stats with k = N - 1). */
+sv_status spec_verify_tree(sv_mode mode, const void* logits, sv_dtype dtype,
+                           const float* draft_probs, const int32_t* tree_tokens,
+                           const int32_t* tree_parents, const float* u_accept,
+                           const float* u_resample, float T, int B, int N, int V,
+                           int32_t* out_tokens, int32_t* out_nodes, int32_t* num_accepted,
+                           void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* N-gram (prompt-lookup) drafter: proposals that need no draft model
  * ("Decodificação especulativa explicada", §"A família de rascunhos";

@@ -1824,7 +1824,8 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sv_rows_kernel(RowsArgs a) {
     // The gathers of this row, issued now and used after the stream.
     int xi = -1;
     float lx = NAN, qx = NAN, ua = 0.0f;
-    if (rank == 0 && tid == 0 && i < k) {
+    // (no drafted tokens, a.x null: the tree verify's rows, statistics only)
+    if (rank == 0 && tid == 0 && i < k && a.x) {
         xi = a.x[(long long)b * k + i];
         if (xi >= 0 && xi < V) {
             lx = E::load1(rowp + xi);
@@ -1885,7 +1886,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sv_rows_kernel(RowsArgs a) {
     rec.qx = NAN;
     uint32_t fl = row_flags<SAMPLED>(p);
     bool ends = false;  // the scan stops at this row (sequences with `skip`)
-    if (i < k) {
+    if (i < k && a.x) {
         if (xi < 0 || xi >= V) {
             fl |= kRowTokenBad;
         } else {
@@ -2186,6 +2187,429 @@ __global__ void sv_finish_greedy_kernel(const int32_t* __restrict__ x, RowRec* _
     for (int i = n + 1; i <= k; ++i) o[i] = -1;
     nacc[b] = n;
     commit_sequence(ep, b, n, k);
+}
+
+// ------------------------------------------------------------------ tree verification
+//
+// Several drafted continuations checked at once ("Decodificação especulativa
+// explicada", §"A família de rascunhos": Medusa's tree attention; "Speculative
+// decoding: el secretario...", §"Tree attention").  A sequence's tree has N
+// nodes: node 0 the root, node j >= 1 a drafted token with a parent before it;
+// logits row j is the target's distribution after node j.  The walk starts at
+// the root.  Greedy: the first child (in index order) whose token is the
+// node's argmax is accepted.  Sampled: recursive rejection over the node's
+// children, drawn independently from the node's draft distribution q: the
+// current distribution r starts as p; child j is accepted iff r(x) >= q(x) or
+// u_j < r(x)/q(x); a rejection replaces r by the normalised residual
+// max(0, r - q) (by p again, flagged, when that has no mass).  With no child
+// accepted the final token is drawn from r.  One child per node is the chain
+// rule.  The row stream provides each row's max, normaliser and argmax; this
+// kernel (one CTA per sequence) walks the tree, making a pass over a node's
+// logits and q rows for each rejected child and for the final draw.
+
+constexpr int kTreeMaxN = kMaxK + 1;
+
+// Dynamic shared memory of the sampled walk: the final draw's block sums, a
+// double per 32 chunks of 8 elements.
+__host__ __device__ inline size_t tree_bsum_bytes(int V) {
+    const long long nch = ((long long)V + kChunk - 1) / kChunk;
+    return (size_t)((nch + 31) / 32) * sizeof(double);
+}
+
+struct TreeArgs {
+    const void* logits;
+    const float* q;
+    const int32_t* tok;
+    const int32_t* par;
+    const float* ua;
+    const float* ur;
+    const Header* hdr;
+    RowRec* rows;
+    uint32_t* seqstat;
+    int32_t* out;
+    int32_t* nodes;
+    int32_t* nacc;
+    int B, N, V;
+    ff c2;  // log2(e)/T
+};
+
+// A row's record, with the flat stream's partial keys merged when it left them.
+__device__ __forceinline__ RowRec row_record(const RowRec* rows, long long r, uint32_t P,
+                                             int vpr, int per, int rem) {
+    RowRec rec = rows[r];
+    if (P) {
+        const int c0 = flat_owner((int)r * vpr, per, rem);
+        const int c1 = flat_owner((int)(r + 1) * vpr - 1, per, rem);
+        const unsigned long long* w = reinterpret_cast<const unsigned long long*>(&rec);
+        unsigned long long key = 0ull;
+        for (int c = c0; c <= c1 && c - c0 < kFlatSlots; ++c) key = w[c - c0] > key ? w[c - c0] : key;
+        const bool nan = key == ~0ull;
+        const float m = from_ordered_bits((uint32_t)(key >> 32));
+        rec.mraw = nan ? NAN : m;
+        rec.S = 0.0f;
+        rec.px = NAN;
+        rec.lx = NAN;
+        rec.qx = NAN;
+        rec.argmax = nan ? 0 : (int32_t)(0xFFFFFFFFu - (uint32_t)key);
+        rec.flags = (nan || !(m > -INFINITY) || m == INFINITY) ? kRowBad : 0u;
+    }
+    return rec;
+}
+
+// p_v = 2^((l_v - m) c) / S in fp32 (the fast pass's corrected exponential).
+__device__ __forceinline__ float tree_p(float l, float m, ff c2, float inv_s) {
+    const float d = __fsub_rn(l, m);
+    const float a = __fmul_rn(d, c2.hi);
+    float err = __fmaf_rn(d, c2.hi, -a);
+    err = __fmaf_rn(d, c2.lo, err);
+    const float y0 = ex2_approx(a);
+    const float y = y0 > 0.0f ? __fmaf_rn(y0, __fmul_rn(err, 0.693147181f), y0) : 0.0f;
+    return __fmul_rn(y, inv_s);
+}
+
+// r_t(v): p_v through t residual steps r <- max(0, r - q_v) / Z.
+__device__ __forceinline__ float tree_r(float p, float qv, const float* invz, int t) {
+    float r = p;
+    for (int s = 0; s < t; ++s) r = __fmul_rn(fmaxf(__fsub_rn(r, qv), 0.0f), invz[s]);
+    return r;
+}
+
+template <int NT>
+__device__ __forceinline__ double block_sum_d(double v, double* red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    __syncthreads();
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    double t = 0.0;
+    for (int i = 0; i < NT / 32; ++i) t += red[i];
+    return t;
+}
+
+template <typename DT, bool SAMPLED>
+__global__ void __launch_bounds__(SAMPLED ? kThreads : 64)
+    sv_tree_kernel(TreeArgs a) {
+    using E = Elt<DT>;
+    constexpr int NT = SAMPLED ? kThreads : 64;
+    __shared__ int s_tok[kTreeMaxN], s_par[kTreeMaxN];
+    __shared__ RowRec s_rec[kTreeMaxN];  // greedy: every row's record
+    __shared__ float s_invz[kTreeMaxN];  // 1 / Z_t of the current node's residual steps
+    __shared__ double s_red[NT / 32];
+    __shared__ int s_bits, s_info, s_n, s_cur, s_next, s_nrej, s_token, s_path[kTreeMaxN];
+    __shared__ int s_lp[NT / 32];
+    __shared__ double s_red2;
+    extern __shared__ double tree_bsum[];  // sampled: block sums of the final draw
+    const int tid = threadIdx.x;
+    const int b = blockIdx.x, N = a.N, V = a.V;
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the row records are complete
+    for (int i = tid; i < N; i += NT) {
+        s_tok[i] = a.tok[(long long)b * N + i];
+        s_par[i] = a.par[(long long)b * N + i];
+    }
+    if (tid == 0) {
+        s_bits = 0;
+        s_info = 0;
+        s_n = 0;
+        s_cur = 0;
+        s_token = -1;
+    }
+    __syncthreads();
+    if (tid == 0)
+        for (int j = 1; j < N; ++j)
+            if (s_par[j] < 0 || s_par[j] >= j) s_bits |= SV_DEV_BAD_TREE;
+    const DT* seq = static_cast<const DT*>(a.logits) + (long long)b * N * V;
+    if (!SAMPLED) {
+        // every row's record (merged from the flat stream's keys when needed)
+        const uint32_t P = a.hdr->flat_ctas;
+        const int vpr = (int)a.hdr->flat_vpr, per = (int)a.hdr->flat_per,
+                  rem = (int)a.hdr->flat_rem;
+        for (int i = tid; i < N; i += NT) {
+            const long long r = (long long)b * N + i;
+            s_rec[i] = row_record(a.rows, r, P, vpr, per, rem);
+            if (P) a.rows[r] = s_rec[i];
+        }
+        __syncthreads();
+        if (tid == 0 && !s_bits) {
+            int cur = 0, n = 0;
+            for (;;) {
+                if (s_rec[cur].flags & kRowBad) {
+                    s_bits |= SV_DEV_BAD_ROW;
+                    break;
+                }
+                const int am = s_rec[cur].argmax;
+                int next = -1;
+                for (int j = cur + 1; j < N; ++j) {
+                    if (s_par[j] != cur) continue;
+                    if (s_tok[j] < 0 || s_tok[j] >= V) {
+                        s_bits |= SV_DEV_BAD_TOKEN;
+                        break;
+                    }
+                    if (s_tok[j] == am) {
+                        next = j;
+                        break;
+                    }
+                }
+                if (s_bits) break;
+                if (next < 0) {
+                    s_token = am;
+                    break;
+                }
+                s_path[n++] = next;
+                cur = next;
+            }
+            s_n = n;
+        }
+    } else {
+        const float* qseq = a.q + (long long)b * N * V;
+        for (;;) {
+            __syncthreads();
+            if (s_bits || s_token >= 0) break;
+            const int cur = s_cur;
+            const RowRec rec = a.rows[(long long)b * N + cur];
+            if (rec.flags & kRowBad) {
+                if (tid == 0) s_bits |= SV_DEV_BAD_ROW;
+                continue;
+            }
+            const float m = rec.mraw, inv_s = __frcp_rn(rec.S);
+            const DT* lrow = seq + (long long)cur * V;
+            const float* qrow = qseq + (long long)cur * V;
+            // the rows in chunks of 8 elements (16-byte loads when aligned)
+            const bool al_l = (reinterpret_cast<uintptr_t>(lrow) & 15) == 0;
+            const bool al_q = (reinterpret_cast<uintptr_t>(qrow) & 15) == 0;
+            const int nch = (V + kChunk - 1) / kChunk;
+            if (tid == 0) {
+                s_nrej = 0;
+                s_next = -1;
+            }
+            __syncthreads();
+            // the children in index order
+            for (int j = cur + 1; j < N; ++j) {
+                if (s_par[j] != cur) continue;  // uniform: shared data
+                if (tid == 0) {
+                    const int x = s_tok[j];
+                    if (x < 0 || x >= V) {
+                        s_bits |= SV_DEV_BAD_TOKEN;
+                    } else {
+                        const float u = a.ua[(long long)b * N + j], Q = qrow[x];
+                        if (!(u >= 0.0f && u < 1.0f)) s_bits |= SV_DEV_BAD_UNIFORM;
+                        else if (!(Q >= 0.0f)) s_bits |= SV_DEV_BAD_Q;
+                        else {
+                            const float P =
+                                tree_r(tree_p(E::load1(lrow + x), m, a.c2, inv_s), Q, s_invz,
+                                       s_nrej);
+                            if (P >= Q || u < __fdiv_rn(P, Q)) s_next = j;
+                        }
+                    }
+                }
+                __syncthreads();
+                if (s_bits || s_next >= 0) break;
+                // rejected: Z = sum_v max(0, r(v) - q(v)) over the row, two
+                // chunks per thread in flight
+                const int t = s_nrej;
+                double z = 0.0;
+                for (int c0 = tid; c0 < nch; c0 += 2 * NT) {
+                    float l[2][kChunk], qv[2][kChunk];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u)
+                        if (c0 + u * NT < nch) {
+                            load_chunk<DT>(lrow, (long long)(c0 + u * NT) * kChunk, V, al_l, l[u]);
+                            load_q_chunk(qrow, (long long)(c0 + u * NT) * kChunk, V, al_q, qv[u]);
+                        }
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        if (c0 + u * NT >= nch) break;
+                        float zc = 0.0f;
+#pragma unroll
+                        for (int e = 0; e < kChunk; ++e) {
+                            const float r =
+                                tree_r(tree_p(l[u][e], m, a.c2, inv_s), qv[u][e], s_invz, t);
+                            zc += fmaxf(__fsub_rn(r, qv[u][e]), 0.0f);
+                        }
+                        z += (double)zc;
+                    }
+                }
+                z = block_sum_d<NT>(z, s_red);
+                if (tid == 0) {
+                    if (z > 0.0) {
+                        s_invz[t] = (float)(1.0 / z);
+                        s_nrej = t + 1;
+                    } else {  // zero residual mass: back to p
+                        s_nrej = 0;
+                        s_info |= SV_DEV_DEGENERATE;
+                    }
+                }
+                __syncthreads();
+            }
+            if (s_bits) continue;
+            if (s_next >= 0) {
+                if (tid == 0) {
+                    s_path[s_n++] = s_next;
+                    s_cur = s_next;
+                }
+                continue;
+            }
+            // No child accepted: draw from r with u_resample.  Weights: p, or the
+            // last rejection's residual max(0, r - q) (unnormalised).  A pass
+            // sums blocks of 32 chunks (a warp, a chunk per lane) into shared
+            // memory; the block holding u * C is found from their prefix; its
+            // warp reloads it and one lane finds the element.
+            const float u = a.ur[b];
+            if (!(u >= 0.0f && u < 1.0f)) {
+                if (tid == 0) s_bits |= SV_DEV_BAD_UNIFORM;
+                continue;
+            }
+            const int t = s_nrej;
+            const int lane = tid & 31, warp = tid >> 5;
+            auto weights = [&](int c, float* w) {
+                float l[kChunk], qv[kChunk];
+                load_chunk<DT>(lrow, (long long)c * kChunk, V, al_l, l);
+                if (t > 0) load_q_chunk(qrow, (long long)c * kChunk, V, al_q, qv);
+#pragma unroll
+                for (int e = 0; e < kChunk; ++e) {
+                    const float p = tree_p(l[e], m, a.c2, inv_s);
+                    w[e] = t == 0 ? p
+                                  : fmaxf(__fsub_rn(tree_r(p, qv[e], s_invz, t - 1), qv[e]), 0.0f);
+                }
+            };
+            auto chunk_sum = [&](const float* w) {
+                double cs = 0.0;
+#pragma unroll
+                for (int e = 0; e < kChunk; ++e) cs += (double)w[e];
+                return cs;
+            };
+            const int nblk = (nch + 31) / 32;
+            for (int blk = warp; blk < nblk; blk += NT / 32) {
+                const int c = blk * 32 + lane;
+                double cs = 0.0;
+                if (c < nch) {
+                    float w[kChunk];
+                    weights(c, w);
+                    cs = chunk_sum(w);
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) cs += __shfl_xor_sync(0xffffffffu, cs, off);
+                if (lane == 0) tree_bsum[blk] = cs;
+            }
+            __syncthreads();
+            // prefix of the block sums: each thread a contiguous share
+            const int Lb = (nblk + NT - 1) / NT, b0 = min(nblk, tid * Lb), b1 = min(nblk, b0 + Lb);
+            double mine = 0.0;
+            for (int i = b0; i < b1; ++i) mine += tree_bsum[i];
+            double incl = mine;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const double o = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += o;
+            }
+            if (lane == 31) s_red[warp] = incl;
+            if (tid == 0) {
+                s_next = -1;  // the block holding u * C
+                s_token = -1;
+            }
+            __syncthreads();
+            double before = 0.0, total = 0.0;
+            for (int i = 0; i < NT / 32; ++i) {
+                if (i < warp) before += s_red[i];
+                total += s_red[i];
+            }
+            before += incl - mine;
+            const double tau = (double)u * total;
+            if (mine > 0.0 && before <= tau && tau < before + mine) {
+                double run = before;
+                int i = b0;
+                for (; i < b1 - 1; ++i) {
+                    if (tau < run + tree_bsum[i]) break;
+                    run += tree_bsum[i];
+                }
+                s_next = i;
+                s_red2 = run;
+            }
+            __syncthreads();
+            if (warp == 0 && s_next >= 0) {
+                const int c = s_next * 32 + lane;
+                float w[kChunk] = {};
+                double cs = 0.0;
+                if (c < nch) {
+                    weights(c, w);
+                    cs = chunk_sum(w);
+                }
+                double ci = cs;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const double o = __shfl_up_sync(0xffffffffu, ci, off);
+                    if (lane >= off) ci += o;
+                }
+                const double cb = s_red2 + ci - cs;  // weight before this lane's chunk
+                bool mine_c = cs > 0.0 && cb <= tau && tau < cb + cs;
+                if (!__any_sync(0xffffffffu, mine_c)) {
+                    // the block's own sums rounded differently: the last chunk
+                    // starting at or before u * C
+                    const unsigned mk = __ballot_sync(0xffffffffu, cs > 0.0 && cb <= tau);
+                    mine_c = mk != 0u && lane == 31 - __clz(mk);
+                }
+                if (mine_c) {
+                    double cum = cb;
+                    int tok = -1;
+#pragma unroll
+                    for (int e = 0; e < kChunk; ++e) {
+                        cum += (double)w[e];
+                        if (tok < 0 && w[e] > 0.0f && cum > tau) tok = c * kChunk + e;
+                    }
+                    if (tok < 0)  // rounding at the chunk's end: its last positive element
+#pragma unroll
+                        for (int e = 0; e < kChunk; ++e)
+                            if (w[e] > 0.0f) tok = c * kChunk + e;
+                    s_token = tok;
+                }
+            }
+            __syncthreads();
+            if (s_token < 0) {
+                // u * C fell outside every bin (rounding): the last positive bin
+                int lp = -1;
+                for (int c = tid; c < nch; c += NT) {
+                    float w[kChunk];
+                    weights(c, w);
+#pragma unroll
+                    for (int e = 0; e < kChunk; ++e)
+                        if (w[e] > 0.0f) lp = max(lp, c * kChunk + e);
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1)
+                    lp = max(lp, __shfl_xor_sync(0xffffffffu, lp, off));
+                if (lane == 0) s_lp[warp] = lp;
+                __syncthreads();
+                if (tid == 0) {
+                    int best = -1;
+                    for (int i = 0; i < NT / 32; ++i) best = max(best, s_lp[i]);
+                    s_token = best < 0 ? 0 : best;
+                }
+            }
+        }
+    }
+    __syncthreads();
+    if (tid != 0) return;
+    int32_t* o = a.out + (long long)b * N;
+    int32_t* nd = a.nodes + (long long)b * N;
+    const uint32_t bits = (uint32_t)s_bits;
+    a.seqstat[b] = bits | (uint32_t)s_info;
+    if (bits) {
+        for (int i = 0; i < N; ++i) {
+            o[i] = -1;
+            nd[i] = -1;
+        }
+        a.nacc[b] = -1;
+        return;
+    }
+    const int n = s_n;
+    for (int i = 0; i < n; ++i) {
+        o[i] = s_tok[s_path[i]];
+        nd[i] = s_path[i];
+    }
+    o[n] = s_token;
+    for (int i = n + 1; i < N; ++i) o[i] = -1;
+    for (int i = n; i < N; ++i) nd[i] = -1;
+    a.nacc[b] = n;
 }
 
 struct FinishArgs {
@@ -2670,6 +3094,12 @@ static sv_status device_setup(int* sms) {
             SV_TRY(cluster_attrs(sv_rows_kernel<float, false, 256>, false));
             SV_TRY(cluster_attrs(sv_rows_kernel<float, false, 512>, false));
             SV_TRY(cluster_attrs(sv_rows_kernel<float, false, 1024>, false));
+            SV_TRY(cudaFuncSetAttribute(sv_tree_kernel<__nv_bfloat16, true>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)tree_bsum_bytes(kMaxV)));
+            SV_TRY(cudaFuncSetAttribute(sv_tree_kernel<float, true>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)tree_bsum_bytes(kMaxV)));
 #undef SV_TRY
             if (e != cudaSuccess) return SV_ERR_CUDA;
             // How many clusters of the drawing kernel fit at once, per cluster
@@ -3208,6 +3638,55 @@ static sv_status run_verify(bool sampled, const void* logits, sv_dtype dt, const
                          sms, skip, ep);
 }
 
+// Tree verification: the row stream over all B*N rows (statistics only, no
+// gathers; greedy batches may take the flat stream), then the walk kernel as
+// its programmatic dependent, one CTA per sequence.
+static sv_status run_tree(bool sampled, const void* logits, sv_dtype dt, const float* q,
+                          const int32_t* tok, const int32_t* par, const float* ua,
+                          const float* ur, float T, int B, int N, int V, int32_t* out,
+                          int32_t* nodes, int32_t* nacc, void* ws, cudaStream_t stream, int sms) {
+    const int k = N - 1;
+    sv_status st = launch_rows(sampled, logits, dt, nullptr, nullptr, nullptr, T, B, k, V, ws,
+                               stream, sms, false, !sampled);
+    if (st != SV_OK) return st;
+    TreeArgs a;
+    a.logits = logits;
+    a.q = q;
+    a.tok = tok;
+    a.par = par;
+    a.ua = ua;
+    a.ur = ur;
+    a.hdr = static_cast<const Header*>(ws);
+    a.rows = reinterpret_cast<RowRec*>(static_cast<char*>(ws) + ws_rows_offset());
+    a.seqstat = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + ws_seq_offset(B, k));
+    a.out = out;
+    a.nodes = nodes;
+    a.nacc = nacc;
+    a.B = B;
+    a.N = N;
+    a.V = V;
+    a.c2 = log2e_over(sampled ? T : 1.0f);
+    cudaLaunchAttribute pdl;
+    pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl.val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)B, 1, 1);
+    cfg.blockDim = dim3(sampled ? kThreads : 64, 1, 1);
+    // the final draw's block sums: a double per 32 chunks of 8 elements
+    cfg.dynamicSmemBytes = sampled ? tree_bsum_bytes(V) : 0;
+    cfg.stream = stream;
+    cfg.attrs = &pdl;
+    cfg.numAttrs = 1;
+    cudaError_t e;
+    if (sampled)
+        e = dt == SV_BF16 ? cudaLaunchKernelEx(&cfg, sv_tree_kernel<__nv_bfloat16, true>, a)
+                          : cudaLaunchKernelEx(&cfg, sv_tree_kernel<float, true>, a);
+    else
+        e = dt == SV_BF16 ? cudaLaunchKernelEx(&cfg, sv_tree_kernel<__nv_bfloat16, false>, a)
+                          : cudaLaunchKernelEx(&cfg, sv_tree_kernel<float, false>, a);
+    return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
 }  // namespace sv
 
 using namespace sv;
@@ -3300,6 +3779,29 @@ sv_status spec_verify_sample(const void* logits, sv_dtype dtype, const float* dr
     if (B == 0) return SV_OK;
     return run_verify(true, logits, dtype, draft_probs, draft_tokens, u_accept, u_resample, T, B,
                       k, V, out_tokens, num_accepted, ws, stream, sms, Epilogue{nullptr, nullptr});
+}
+
+sv_status spec_verify_tree(sv_mode mode, const void* logits, sv_dtype dtype,
+                           const float* draft_probs, const int32_t* tree_tokens,
+                           const int32_t* tree_parents, const float* u_accept,
+                           const float* u_resample, float T, int B, int N, int V,
+                           int32_t* out_tokens, int32_t* out_nodes, int32_t* num_accepted,
+                           void* ws, size_t ws_bytes, cudaStream_t stream) {
+    if (mode != SV_MODE_SAMPLE && mode != SV_MODE_GREEDY) return SV_ERR_INVALID_ARG;
+    if (N < 2) return SV_ERR_INVALID_ARG;
+    if (N > kTreeMaxN) return SV_ERR_UNSUPPORTED;
+    sv_status st = check_common(logits, dtype, tree_tokens, B, N - 1, V, ws, ws_bytes);
+    if (st != SV_OK) return st;
+    if ((st = check_outputs(out_tokens, num_accepted, B)) != SV_OK) return st;
+    if (B > 0 && (!tree_parents || !aligned16(tree_parents) || !out_nodes || !aligned16(out_nodes)))
+        return SV_ERR_INVALID_ARG;
+    const bool sampled = mode == SV_MODE_SAMPLE;
+    if (sampled && (st = check_sample(draft_probs, u_accept, u_resample, T, B)) != SV_OK) return st;
+    int sms = 0;
+    if ((st = device_setup(&sms)) != SV_OK) return st;
+    if (B == 0) return SV_OK;
+    return run_tree(sampled, logits, dtype, draft_probs, tree_tokens, tree_parents, u_accept,
+                    u_resample, T, B, N, V, out_tokens, out_nodes, num_accepted, ws, stream, sms);
 }
 
 sv_status spec_verify_sample_kv(const void* logits, sv_dtype dtype, const float* draft_probs,

@@ -246,3 +246,93 @@ def ngram_histories(B: int, Lmax: int, V: int = 32000, seed: int = 0, pool: int 
         row = np.concatenate(parts)[:lengths[b]] if parts else np.zeros(0, np.int32)
         hist[b, :len(row)] = row
     return hist, lengths
+
+
+@dataclass
+class TreeInputs:
+    mode: str                 # "sample" or "greedy"
+    dtype: str                # "bf16" or "f32"
+    B: int
+    N: int
+    V: int
+    T: float
+    logits: np.ndarray        # [B, N, V] uint16 bf16 bit patterns or float32
+    q: np.ndarray | None      # [B, N, V] float32: the draft distribution at each node
+    tok: np.ndarray           # [B, N] int32 (entry 0 unused: -1)
+    par: np.ndarray           # [B, N] int32 (entry 0: -1)
+    ua: np.ndarray | None     # [B, N] float32
+    ur: np.ndarray | None     # [B] float32
+    meta: dict = field(default_factory=dict)
+
+
+def tree_parents(N: int, branching=(4, 2, 2)) -> np.ndarray:
+    """Parents of a tree built level by level (the shape of a Medusa-style static
+    tree): the root has branching[0] children, each of those branching[1], and
+    so on (the last entry repeats), nodes numbered breadth-first, cut at N."""
+    par = [-1]
+    level = [0]
+    depth = 0
+    while len(par) < N:
+        nxt = []
+        bf = branching[min(depth, len(branching) - 1)]
+        for p in level:
+            for _ in range(bf):
+                if len(par) < N:
+                    par.append(p)
+                    nxt.append(len(par) - 1)
+        if not nxt:
+            break
+        level = nxt
+        depth += 1
+    return np.asarray(par, dtype=np.int32)
+
+
+def make_tree_inputs(mode="sample", B=1, N=16, V=32000, dtype="bf16", T=1.0,
+                     branching=(4, 2, 2), random_shape=False, slope=1.1, noise=1.0,
+                     draft_sigma=0.5, p_argmax=0.7, seed=0) -> TreeInputs:
+    """A seeded batch of drafted trees.  Logits rows are Zipf-shaped as in
+    make_inputs; the draft at node j is q_j = softmax((l_j + N(0, sigma^2)) / T);
+    sampled: the children of node j are drawn independently from q_j; greedy:
+    a node's first child is its argmax with probability p_argmax, the other
+    children uniform tokens.  The shape is the level-by-level tree of
+    ``branching`` for every sequence, or (random_shape) each node's parent
+    uniform among the nodes before it."""
+    s = _streams(seed)
+    R = B * N
+    rows = _zipf_rows(s["logits"], s["perm"], R, V, slope, noise)
+    if dtype == "bf16":
+        bits = bf16_bits(rows)
+        logits = bits.reshape(B, N, V)
+        vals = (bits.astype(np.uint32) << 16).view(np.float32).reshape(B, N, V)
+    elif dtype == "f32":
+        logits = rows.reshape(B, N, V)
+        vals = logits
+    else:
+        raise ValueError(dtype)
+    gt = np.random.default_rng(s["draft_sample"])
+    if random_shape:
+        par = np.full((B, N), -1, np.int32)
+        for j in range(1, N):
+            par[:, j] = gt.integers(0, j, B)
+    else:
+        par = np.tile(tree_parents(N, branching), (B, 1))
+    tok = np.full((B, N), -1, np.int32)
+    if mode == "greedy":
+        am = np.argmax(vals, axis=2)
+        for j in range(1, N):
+            p = par[:, j]
+            first = np.array([not (par[b, 1:j] == p[b]).any() for b in range(B)])
+            keep = first & (gt.random(B) < p_argmax)
+            tok[:, j] = np.where(keep, am[np.arange(B), p], gt.integers(0, V, B))
+        return TreeInputs(mode, dtype, B, N, V, float(T), logits, None, tok, par, None, None,
+                          meta=dict(seed=seed, branching=branching))
+    q = _draft_q(vals.reshape(R, V), s["draft_noise"], draft_sigma, T).reshape(B, N, V)
+    cdf = np.cumsum(q.astype(np.float64), axis=2)
+    for j in range(1, N):
+        c = cdf[np.arange(B), par[:, j]]
+        u = gt.random(B) * c[:, -1]
+        tok[:, j] = np.minimum((c <= u[:, None]).sum(axis=1), V - 1)
+    ua = np.random.default_rng(s["u_accept"]).random((B, N), dtype=np.float32)
+    ur = np.random.default_rng(s["u_resample"]).random(B, dtype=np.float32)
+    return TreeInputs(mode, dtype, B, N, V, float(T), logits, q, tok, par, ua, ur,
+                      meta=dict(seed=seed, branching=branching))

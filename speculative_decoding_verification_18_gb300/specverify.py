@@ -22,6 +22,7 @@ SV_MODE_SAMPLE, SV_MODE_GREEDY = 0, 1
 SV_DEV_BAD_ROW, SV_DEV_BAD_TOKEN, SV_DEV_BAD_UNIFORM, SV_DEV_BAD_Q, SV_DEV_DEGENERATE = (
     0x1, 0x2, 0x4, 0x8, 0x10)
 SV_DEV_PRECISE = 0x20
+SV_DEV_BAD_TREE = 0x40
 
 EXPORTS = ("spec_verify_workspace_size", "spec_verify_greedy", "spec_verify_sample",
            "spec_verify_rows", "spec_verify_finish", "spec_verify_read_status",
@@ -57,6 +58,8 @@ def load():
     lib.spec_ngram_draft.restype = I
     lib.spec_verify_match.argtypes = [P, I, P, P, P, F, I, I, I, P, P, P, Z, P]
     lib.spec_verify_match.restype = I
+    lib.spec_verify_tree.argtypes = [I, P, I, P, P, P, P, P, F, I, I, I, P, P, P, P, Z, P]
+    lib.spec_verify_tree.restype = I
     lib.spec_verify_sample_kv.argtypes = [P, I, P, P, P, P, F, I, I, I, P, P, P, Z, P, P, P]
     lib.spec_verify_sample_kv.restype = I
     lib.spec_verify_greedy_kv.argtypes = [P, I, P, I, I, I, P, P, P, Z, P, P, P]
@@ -168,6 +171,20 @@ def spec_verify_match(logits, draft_tokens, u_draw, u_bonus, T, out_tokens, num_
                                   _ptr(u_bonus), float(T), B, k1 - 1, V, _ptr(out_tokens),
                                   _ptr(num_accepted), _ptr(ws), ws.numel(), _stream(stream))
     _check(st, "spec_verify_match")
+
+
+def spec_verify_tree(mode, logits, draft_probs, tree_tokens, tree_parents, u_accept, u_resample,
+                     T, out_tokens, out_nodes, num_accepted, ws, stream=None):
+    """Tree verify: logits [B, N, V], draft_probs [B, N, V] (sampled), tree_tokens and
+    tree_parents [B, N] int32, u_accept [B, N], u_resample [B] -> out_tokens,
+    out_nodes [B, N], num_accepted [B].  Workspace: workspace(B, N - 1, V, ...)."""
+    B, N, V = logits.shape
+    st = load().spec_verify_tree(int(mode), _ptr(logits), _dtype(logits), _ptr(draft_probs),
+                                 _ptr(tree_tokens), _ptr(tree_parents), _ptr(u_accept),
+                                 _ptr(u_resample), float(T), B, N, V, _ptr(out_tokens),
+                                 _ptr(out_nodes), _ptr(num_accepted), _ptr(ws), ws.numel(),
+                                 _stream(stream))
+    _check(st, "spec_verify_tree")
 
 
 def spec_ngram_draft(history, lengths, k, n_min, n_max, draft_tokens, num_drafted, stream=None):

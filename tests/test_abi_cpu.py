@@ -104,3 +104,28 @@ def test_ngram_argument_errors(lib):
     assert f(None, None, 0, 10, 4, 3, 2, None, None, None) == sv.SV_ERR_INVALID_ARG  # n_max < n_min
     assert f(None, None, 0, 10, 4, 1, 33, None, None, None) == sv.SV_ERR_INVALID_ARG  # n_max > 32
     assert f(None, None, -1, 10, 4, 1, 4, None, None, None) == sv.SV_ERR_INVALID_ARG  # B < 0
+
+
+def test_tree_argument_errors(lib):
+    """spec_verify_tree rejects bad arguments before any launch (no GPU needed)."""
+    from speculative_decoding_verification_18_gb300 import specverify as sv
+    P = 4096
+    ws = sv.spec_verify_workspace_size(2, 4, 100)
+
+    def tree(mode=sv.SV_MODE_SAMPLE, l=P, q=P, tok=P, par=P, ua=P, ur=P, T=1.0, B=2, N=5,
+             V=100, out=P, nodes=P, n=P, wsp=P, wsb=ws):
+        return lib.spec_verify_tree(mode, l, sv.SV_F32, q, tok, par, ua, ur, T, B, N, V, out,
+                                    nodes, n, wsp, wsb, None)
+
+    assert tree(mode=7) == sv.SV_ERR_INVALID_ARG
+    assert tree(N=1) == sv.SV_ERR_INVALID_ARG
+    assert tree(N=66, wsb=1 << 20) == sv.SV_ERR_UNSUPPORTED
+    assert tree(par=None) == sv.SV_ERR_INVALID_ARG
+    assert tree(nodes=None) == sv.SV_ERR_INVALID_ARG
+    assert tree(tok=P + 4) == sv.SV_ERR_INVALID_ARG
+    assert tree(q=None) == sv.SV_ERR_INVALID_ARG
+    assert tree(T=0.0) == sv.SV_ERR_INVALID_ARG
+    assert tree(wsb=ws - 1) == sv.SV_ERR_WORKSPACE
+    # greedy needs no q, uniforms or temperature: its errors are the others
+    assert tree(mode=sv.SV_MODE_GREEDY, q=None, ua=None, ur=None, T=0.0,
+                par=None) == sv.SV_ERR_INVALID_ARG
