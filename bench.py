@@ -27,6 +27,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -60,12 +61,23 @@ def dist_env():
     return world, rank, local
 
 
-def kernel_source_hash():
-    h = hashlib.sha256()
-    for f in ("specverify.cu", "ff.cuh"):
-        with open(os.path.join(ROOT, "speculative_decoding_verification_18_gb300", "csrc", f),
-                  "rb") as fh:
-            h.update(fh.read())
+def kernel_source_hash(kernel=None):
+    """Hash of the sources a kernel's counters depend on: the section of
+    specverify.cu (between its '// ----' section headers) that defines the
+    kernel, and ff.cuh; the whole file when the kernel is not found."""
+    csrc = os.path.join(ROOT, "speculative_decoding_verification_18_gb300", "csrc")
+    with open(os.path.join(csrc, "specverify.cu")) as fh:
+        text = fh.read()
+    if kernel:
+        m = re.search(r"__global__[^;{]*?\b" + re.escape(kernel) + r"\s*\(", text)
+        if m:
+            heads = [h.start() for h in re.finditer(r"^// -{40,} ", text, re.M)]
+            lo = max([h for h in heads if h <= m.start()], default=0)
+            hi = min([h for h in heads if h > m.start()], default=len(text))
+            text = text[lo:hi]
+    h = hashlib.sha256(text.encode())
+    with open(os.path.join(csrc, "ff.cuh"), "rb") as fh:
+        h.update(fh.read())
     return h.hexdigest()[:16]
 
 
@@ -87,7 +99,7 @@ def ncu_traffic(workload, kernel):
     except Exception:
         return None
     e = d.get(workload, {}).get(kernel)
-    if not e or e.get("source_hash") != kernel_source_hash():
+    if not e or e.get("source_hash") != kernel_source_hash(kernel):
         return None
     return e.get("dram_bytes_per_launch")
 
