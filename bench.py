@@ -61,20 +61,31 @@ def dist_env():
     return world, rank, local
 
 
+# Sections of specverify.cu (between its '// ----' headers) that every kernel's
+# code draws on, and the kernels that also run the draw.
+_COMMON_SECTIONS = ("workspace", "small helpers", "online softmax partials")
+_DRAWING = ("sv_verify_kernel", "sv_finish_sample_kernel", "sv_precise_kernel",
+            "sv_match_draw_kernel")
+
+
 def kernel_source_hash(kernel=None):
     """Hash of the sources a kernel's counters depend on: the section of
-    specverify.cu (between its '// ----' section headers) that defines the
-    kernel, and ff.cuh; the whole file when the kernel is not found."""
+    specverify.cu that defines it, the common device sections, the draw
+    section for kernels that draw, and ff.cuh; the whole file when the kernel
+    is not found."""
     csrc = os.path.join(ROOT, "speculative_decoding_verification_18_gb300", "csrc")
     with open(os.path.join(csrc, "specverify.cu")) as fh:
         text = fh.read()
     if kernel:
         m = re.search(r"__global__[^;{]*?\b" + re.escape(kernel) + r"\s*\(", text)
         if m:
-            heads = [h.start() for h in re.finditer(r"^// -{40,} ", text, re.M)]
-            lo = max([h for h in heads if h <= m.start()], default=0)
-            hi = min([h for h in heads if h > m.start()], default=len(text))
-            text = text[lo:hi]
+            heads = [(h.start(), h.group(1).strip())
+                     for h in re.finditer(r"^// -{40,} (.*)$", text, re.M)]
+            bounds = [(a, heads[i + 1][0] if i + 1 < len(heads) else len(text), name)
+                      for i, (a, name) in enumerate(heads)]
+            want = set(_COMMON_SECTIONS) | ({"draw phase"} if kernel in _DRAWING else set())
+            parts = [text[a:b] for a, b, name in bounds if name in want or a <= m.start() < b]
+            text = "".join(parts)
     h = hashlib.sha256(text.encode())
     with open(os.path.join(csrc, "ff.cuh"), "rb") as fh:
         h.update(fh.read())
