@@ -157,3 +157,44 @@ def test_flat_two_stage_and_graph_replay():
             g.replay()
     torch.cuda.synchronize()
     assert np.array_equal(out.cpu().numpy(), out1) and np.array_equal(n.cpu().numpy(), n1)
+
+
+def test_workspace_reused_across_paths():
+    """One workspace through the flat greedy stream, a sampled verify, the
+    per-row greedy stream, a tree verify and the flat stream again: every
+    call's outputs equal the oracle's (each call rewrites the layout word the
+    finish kernels read)."""
+    from speculative_decoding_verification_18_gb300 import specverify as sv
+    from speculative_decoding_verification_18_gb300.inputs import make_inputs, make_tree_inputs
+    B, k, V = 64, 4, 8192
+    g_in = make_inputs(mode="greedy", B=B, k=k, V=V, dtype="bf16", kind="zipf", seed=41)
+    s_in = make_inputs(mode="sample", B=B, k=k, V=V, dtype="bf16", T=0.9, kind="zipf",
+                       draft_sigma=0.4, seed=42)
+    t_in = make_tree_inputs(mode="greedy", B=B, N=k + 1, V=V, dtype="bf16", branching=(2,),
+                            seed=43)
+    ws = sv.workspace(B, k, V, torch.bfloat16)
+    assert _flat_ctas(g_in) > 0
+    for step, off in enumerate([0, None, 1, "tree", 0]):
+        if off == "tree":
+            lg = torch.from_numpy(t_in.logits.view(np.int16)).view(torch.bfloat16).cuda()
+            out = torch.empty((B, k + 1), dtype=torch.int32, device="cuda")
+            nodes = torch.empty((B, k + 1), dtype=torch.int32, device="cuda")
+            n = torch.empty(B, dtype=torch.int32, device="cuda")
+            sv.spec_verify_tree(sv.SV_MODE_GREEDY, lg, None, torch.from_numpy(t_in.tok).cuda(),
+                                torch.from_numpy(t_in.par).cuda(), None, None, 1.0, out, nodes,
+                                n, ws)
+            torch.cuda.synchronize()
+            ref = oracle.tree_batch(oracle.GREEDY, t_in.logits, "bf16", None, t_in.tok, t_in.par,
+                                    None, None, 1.0)
+            assert np.array_equal(out.cpu().numpy(), ref.out), step
+            continue
+        inp = s_in if off is None else g_in
+        from speculative_decoding_verification_18_gb300 import specverify as svm
+        svm.debug_flat(off or 0)
+        try:
+            out, n, stats, _ = run_gpu(inp, ws=ws)
+        finally:
+            svm.debug_flat(0)
+        ref = run_oracle(inp)
+        rep = compare_outputs(inp, out, n, ref)
+        assert rep.hard == 0, (step, rep.hard_detail)
