@@ -244,8 +244,11 @@ sv_status spec_verify_greedy_kv(const void* logits, sv_dtype dtype, const int32_
 /* The work of spec_verify_greedy / spec_verify_sample, split at its one internal dependency so
  * that each half can be timed or overlapped separately.  spec_verify_rows
  * streams every logits row once and leaves per-row statistics (max, normaliser,
- * argmax, gathered l(x), q(x), p(x)) in ws; spec_verify_finish then runs the
- * accept scan and the draws from ws and writes the outputs.  Calling rows then
+ * argmax, gathered l(x), q(x), p(x)) in ws; for greedy batches that take the
+ * flat stream (the whole tensor cut into one range per resident CTA) it leaves
+ * each range's partial argmax keys instead, which spec_verify_finish merges
+ * into the row statistics.  spec_verify_finish then runs the accept scan and
+ * the draws from ws and writes the outputs.  Calling rows then
  * finish on one stream with the same arguments is exactly spec_verify_greedy
  * (mode SV_MODE_GREEDY; draft_probs, u_accept, u_resample may be NULL, T is
  * ignored) or spec_verify_sample (mode SV_MODE_SAMPLE). */
