@@ -251,6 +251,22 @@ def cores():
         return os.cpu_count() or 1
 
 
+def max_over_ranks(value: float, dist, device) -> float:
+    """The largest of the ranks' values (a job's time is its slowest rank's);
+    `dist` is torch.distributed with a process group, or None for one rank."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units: float, ms: float) -> float:
+    """Units processed by all ranks per second of the job's time."""
+    return units / (ms / 1e3)
+
+
 def run_reference(args, world, rank):
     """The reference arm: the float64 oracle on this host's cores, same workload."""
     if rank != 0:
@@ -452,11 +468,8 @@ def main():
                            fin_name: stage_ms(finish_stage)}
     clocks = sampler.summary()
 
-    ms_t = torch.tensor([ms], device=dev)
-    if dist:
-        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
-    ms = float(ms_t.item())
-    value = rows_per_step * K * world / (ms / 1e3)
+    ms = max_over_ranks(ms, dist, dev)
+    value = job_rate(rows_per_step * K * world, ms)
 
     # ---- end to end through the C ABI with host buffers
     pin = lambda a: torch.from_numpy(a).pin_memory()
@@ -496,11 +509,8 @@ def main():
             e2e_step()
         e1.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1)
-    et = torch.tensor([e2e_ms], device=dev)
-    if dist:
-        dist.all_reduce(et, op=dist.ReduceOp.MAX)
-    e2e_value = rows_per_step * e2e_steps * world / (float(et.item()) / 1e3)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
+    e2e_value = job_rate(rows_per_step * e2e_steps * world, e2e_ms)
 
     if rank != 0:
         if dist:
