@@ -26,7 +26,8 @@ void spec_verify_debug_force_precise(int on);
 /* Choose the path of spec_verify_greedy / spec_verify_sample: 0 automatic
  * (the default: the row-skipping path when B is at least the SM count, or in
  * sampled mode half of it; else, in sampled mode, the fused per-sequence kernel
- * when its clusters cover every SM; else the two-kernel path), 1 always the two-kernel path, 2 always the
+ * when rows are at most 1 KiB or its clusters cover every SM; else the
+ * two-kernel path), 1 always the two-kernel path, 2 always the
  * fused per-sequence kernel, 3 always the row-skipping path.  A process-wide
  * setting read at launch time, for tests. */
 void spec_verify_debug_force_path(int path);

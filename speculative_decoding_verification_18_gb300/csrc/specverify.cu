@@ -3619,6 +3619,10 @@ static Path choose_path(bool sampled, int B, int V, int esz, int sms) {
     // k = 8, V = 151936 fp32 (skipping 15-18 % faster) and B = 96 at k = 5,
     // V = 128256 bf16 (12 % faster; 4 % slower at B = 128).
     if (sampled && 2 * B >= sms) return kPathSkip;
+    // Rows of at most 1 KiB (toy vocabularies): the whole verify is launch
+    // latency, and one launch beats two (B = 1, V = 32: 11.3 against 12.0 us;
+    // B = 64: 11.7 against 13.6 us).
+    if (sampled && (long long)V * esz <= 1024) return kPathFused;
     if (sampled && (long long)B * seq_split(true, B, V, esz, sms) >= sms) return kPathFused;
     return kPathTwoKernel;
 }
