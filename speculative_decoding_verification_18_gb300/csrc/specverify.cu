@@ -2299,6 +2299,7 @@ __global__ void __launch_bounds__(SAMPLED ? kThreads : 64)
     __shared__ int s_bits, s_info, s_n, s_cur, s_next, s_nrej, s_token, s_path[kTreeMaxN];
     __shared__ int s_lp[NT / 32];
     __shared__ double s_red2;
+    __shared__ float s_cl[kTreeMaxN], s_cq[kTreeMaxN], s_cu[kTreeMaxN];  // children's l(x), q(x), u
     extern __shared__ double tree_bsum[];  // sampled: block sums of the final draw
     const int tid = threadIdx.x;
     const int b = blockIdx.x, N = a.N, V = a.V;
@@ -2382,6 +2383,15 @@ __global__ void __launch_bounds__(SAMPLED ? kThreads : 64)
                 s_nrej = 0;
                 s_next = -1;
             }
+            // every child's l(x), q(x) and uniform, gathered at once
+            for (int j = cur + 1 + tid; j < N; j += NT)
+                if (s_par[j] == cur) {
+                    const int x = s_tok[j];
+                    const bool ok = x >= 0 && x < V;
+                    s_cl[j] = ok ? E::load1(lrow + x) : 0.0f;
+                    s_cq[j] = ok ? qrow[x] : 0.0f;
+                    s_cu[j] = a.ua[(long long)b * N + j];
+                }
             __syncthreads();
             // the children in index order
             for (int j = cur + 1; j < N; ++j) {
@@ -2391,13 +2401,12 @@ __global__ void __launch_bounds__(SAMPLED ? kThreads : 64)
                     if (x < 0 || x >= V) {
                         s_bits |= SV_DEV_BAD_TOKEN;
                     } else {
-                        const float u = a.ua[(long long)b * N + j], Q = qrow[x];
+                        const float u = s_cu[j], Q = s_cq[j];
                         if (!(u >= 0.0f && u < 1.0f)) s_bits |= SV_DEV_BAD_UNIFORM;
                         else if (!(Q >= 0.0f)) s_bits |= SV_DEV_BAD_Q;
                         else {
                             const float P =
-                                tree_r(tree_p(E::load1(lrow + x), m, a.c2, inv_s), Q, s_invz,
-                                       s_nrej);
+                                tree_r(tree_p(s_cl[j], m, a.c2, inv_s), Q, s_invz, s_nrej);
                             if (P >= Q || u < __fdiv_rn(P, Q)) s_next = j;
                         }
                     }
