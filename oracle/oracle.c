@@ -504,6 +504,12 @@ void orc_tree_seq(int mode, const double* logits, const double* q, const int32_t
                 w[v] = (r[v] > qc[v]) ? r[v] - qc[v] : 0.0;
                 Z += w[v];
             }
+            if (mode == ORC_SAMPLE_BUGGY) {
+                /* negative control: every sibling tested against p itself and
+                   the residual taken once, as if each were a fresh chain step */
+                for (int v = 0; v < V; ++v) w[v] = (p[v] > qc[v]) ? p[v] - qc[v] : 0.0;
+                continue;
+            }
             if (Z > 0.0) {
                 for (int v = 0; v < V; ++v) r[v] = w[v] / Z;
             } else { /* zero residual mass: back to p */

@@ -124,6 +124,9 @@ int orc_ngram_draft(const int32_t* history, const int32_t* lengths, int B, int L
  * token is drawn from r (step 4's rule on the unnormalised residual weights)
  * with ur.  Each tested child contributes thr[j] = min(1, r(x)/q(x)).
  *
+ * Mode ORC_SAMPLE_BUGGY (a negative control for the tests): each sibling is
+ * tested against p itself and the final draw uses the residual of p taken once,
+ * as if each sibling were a fresh chain step; this does not preserve p.
  * Outputs: out [N] (the accepted tokens, the emitted token, -1 after),
  * nodes [N] (the accepted node indices, -1 after), *n_acc (-1 if invalid:
  * a bad parent anywhere, or a row, token, uniform or q(x) the walk needs),

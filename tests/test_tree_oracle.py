@@ -133,7 +133,7 @@ def test_sampled_walk_is_exact(seed):
     np.testing.assert_allclose(second / reach1, p1, rtol=0, atol=1e-12)
 
 
-def _enumerate_nodes(l, q, tok, par, T):
+def _enumerate_nodes(l, q, tok, par, T, mode=None):
     """Exact outcome distribution of the sampled walk for fixed drafts, keyed by
     (accepted nodes, emitted tokens).  The walk is piecewise constant in the
     uniforms, so u-space is cut at the thresholds the oracle reports (a tested
@@ -143,8 +143,10 @@ def _enumerate_nodes(l, q, tok, par, T):
     N = len(tok)
     dist = {}
 
+    mode = oracle.SAMPLE if mode is None else mode
+
     def run(ua, ur):
-        return oracle.tree_seq(oracle.SAMPLE, l, q, tok, par, ua, ur, T)
+        return oracle.tree_seq(mode, l, q, tok, par, ua, ur, T)
 
     def rec(fixed, weight):
         ua = np.full(N, 0.5)
@@ -173,6 +175,26 @@ def _enumerate_nodes(l, q, tok, par, T):
 
     rec({}, 1.0)
     return dist
+
+
+def test_enumeration_catches_a_plausible_mistake():
+    """Negative control: testing every sibling against p itself (no residual
+    update between siblings) breaks exactness, and the enumeration sees it."""
+    g = np.random.default_rng(7)
+    V, N, T = 3, 3, 1.0
+    l = g.normal(0, 1.5, (N, V))
+    q = g.dirichlet(np.ones(V), size=N)
+    par = np.array([-1, 0, 0], np.int32)
+    p0 = _softmax(l[0], T)
+    for mode, exact in ((oracle.SAMPLE, True), (oracle.SAMPLE_BUGGY, False)):
+        first = np.zeros(V)
+        for x1, x2 in itertools.product(range(V), repeat=2):
+            wx = q[0, x1] * q[0, x2]
+            tok = np.array([-1, x1, x2], np.int32)
+            for (nodes, outs), w in _enumerate_nodes(l, q, tok, par, T, mode).items():
+                first[outs[0]] += wx * w
+        err = np.abs(first - p0).max()
+        assert (err < 1e-12) == exact, (mode, err)
 
 
 def test_invalid_inputs():
