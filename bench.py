@@ -550,6 +550,11 @@ def main():
                 "algorithmic_bytes": alg, "peak_source": peak_src + " (copy bandwidth)",
                 "stages": stages,
                 "full_tensor_gbs": round(full_tensor_bytes(inp) / (ms / K / 1e3) / 1e9, 1)}
+    # The whole step against the HBM floor: the algorithmic bytes of every stage
+    # at the measured copy bandwidth, over the measured time per step.
+    step_bytes = sum(v["algorithmic_bytes"] for v in stages.values())
+    roofline["step_algorithmic_bytes"] = step_bytes
+    roofline["hbm_floor_frac"] = round((step_bytes / (peak * 1e9)) / (ms / K / 1e3), 4)
     if rows_read is not None:
         roofline["rows_read"] = rows_read
         roofline["rows_needed"] = int(np.mean([np.sum(np.clip(nn, 0, k) + 1) for nn in n_all]))
@@ -563,6 +568,7 @@ def main():
 
     line = {
         "metric": "verify rows/s", "value": value, "unit": "rows/s", "n_gpus": world,
+        "sequences_per_s": value / (k + 1),
         "steps": K, "warmup": warm_reps * copies, "ms_per_step": ms / K,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
