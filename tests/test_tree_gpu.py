@@ -208,3 +208,16 @@ def test_tree_first_token_follows_p():
         counts = np.bincount(first, minlength=4).astype(float)
         stat = float(((counts - M * P[c]) ** 2 / (M * P[c])).sum())
         assert chi2.sf(stat, 3) > 1e-4, (c, stat, counts / M, P[c])
+
+
+def test_tree_mismatch_rate_many_trees():
+    """20 000 sampled trees of 8 nodes (V = 1000): no hard mismatch, and the
+    near-threshold ones (fp32 weights against float64) rare."""
+    from speculative_decoding_verification_18_gb300.inputs import make_tree_inputs
+    t = make_tree_inputs(mode="sample", B=20000, N=8, V=1000, dtype="bf16", T=1.0,
+                         branching=(3, 2), draft_sigma=0.6, seed=77)
+    out, nodes, n, st, bits, _ = run_tree(t)
+    ref = run_oracle(t)
+    hard, near = compare(t, out, nodes, n, ref)
+    assert not hard, hard[:5]
+    assert near <= 2e-5 * t.B * t.N, near
