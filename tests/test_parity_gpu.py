@@ -394,3 +394,17 @@ def test_bf16_ties_lowest_index(path):
     ref = run_oracle(inp)
     assert np.array_equal(out, ref.out) and np.array_equal(n, ref.n)
     assert np.array_equal(stats["argmax"], am)
+
+
+@pytest.mark.parametrize("mode", ["sample", "greedy"])
+def test_maximum_k_and_vocabulary(mode, path):
+    """The largest sizes the ABI accepts: k = 64 drafts and V = 2^21 tokens
+    (one sequence, bf16), and k = 64 over a batch, through every path."""
+    for B, V in ((1, 1 << 21), (24, 3000)):
+        inp = _gen(mode=mode, B=B, k=64, V=V, dtype="bf16", T=1.0, kind="zipf",
+                   p_argmax=0.97, draft_sigma=0.05, seed=V + B)
+        out, n, stats, (st, bits, _) = run_gpu(inp)
+        ref = run_oracle(inp)
+        rep = compare_outputs(inp, out, n, ref)
+        assert rep.hard == 0, rep.hard_detail
+        assert st == 0
