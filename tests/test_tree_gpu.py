@@ -221,3 +221,25 @@ def test_tree_mismatch_rate_many_trees():
     hard, near = compare(t, out, nodes, n, ref)
     assert not hard, hard[:5]
     assert near <= 2e-5 * t.B * t.N, near
+
+
+def test_tree_greedy_invalid_data():
+    """Greedy trees on the flat stream's shape (64 trees of 5 nodes, V = 32000
+    bf16): a malformed parent, a bad token at a tested child and a NaN in a
+    reached row mark only their sequences; the others match the oracle."""
+    from speculative_decoding_verification_18_gb300 import specverify as sv
+    from speculative_decoding_verification_18_gb300.inputs import make_tree_inputs, bf16_bits
+    t = make_tree_inputs(mode="greedy", B=64, N=5, V=32000, dtype="bf16", branching=(2,),
+                         p_argmax=1.0, seed=12)
+    assert sv.debug_flat_ctas(64, 4, 32000, "bf16") > 0
+    t.par[1, 4] = 4                                    # malformed
+    t.tok[2, 1] = 32000                                # first child of the root: tested
+    t.logits[3, 0, 17] = bf16_bits(np.array([np.nan], np.float32))[0]  # the root row
+    out, nodes, n, st, bits, _ = run_tree(t)
+    ref = run_oracle(t)
+    assert np.array_equal(n, ref.n) and np.array_equal(out, ref.out)
+    assert np.array_equal(nodes, ref.nodes)
+    assert list(n[1:4]) == [-1, -1, -1] and (n[4:] >= 0).all() and n[0] >= 0
+    assert st == sv.SV_ERR_DATA
+    want = sv.SV_DEV_BAD_TREE | sv.SV_DEV_BAD_TOKEN | sv.SV_DEV_BAD_ROW
+    assert bits & want == want
