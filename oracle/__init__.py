@@ -62,6 +62,14 @@ def _load():
     lib.orc_ngram_draft.argtypes = [P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                     ctypes.c_int, ctypes.c_int, P, P]
     lib.orc_ngram_draft.restype = ctypes.c_int
+    lib.orc_row_stats_batch.argtypes = [P, ctypes.c_int, ctypes.c_float, ctypes.c_int,
+                                        ctypes.c_int, P, P, P, P, ctypes.c_int]
+    lib.orc_row_stats_batch.restype = ctypes.c_int
+    lib.orc_verify_batch_stats.argtypes = [ctypes.c_int, P, ctypes.c_int, P, P, P, P,
+                                           ctypes.c_float, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_int, P, P, P, P, P, P, P, P, P, P,
+                                           ctypes.c_int]
+    lib.orc_verify_batch_stats.restype = ctypes.c_int
     lib.orc_max_threads.argtypes = []
     lib.orc_max_threads.restype = ctypes.c_int
     lib.orc_tree_seq.argtypes = [ctypes.c_int, P, P, P, P, P, ctypes.c_double, ctypes.c_double,
@@ -184,6 +192,107 @@ def verify_batch(mode, logits, dtype: str, q, x, ua, ur, T, nthreads: int = 0) -
     if rc != 0:
         raise ValueError("oracle rejected its arguments")
     return r
+
+
+def _logits_arg(logits, dtype: str):
+    if dtype == "bf16":
+        return np.ascontiguousarray(logits, dtype=np.uint16), 0
+    if dtype == "f32":
+        return np.ascontiguousarray(logits, dtype=np.float32), 1
+    raise ValueError(dtype)
+
+
+@dataclass
+class RowStats:
+    m: np.ndarray       # [B, k+1] max_j l_j / T
+    S: np.ndarray       # [B, k+1] sum_j exp(l_j/T - m)
+    argmax: np.ndarray  # [B, k+1]
+    bad: np.ndarray     # [B, k+1] 1 for an invalid row
+
+
+def row_stats_batch(logits, dtype: str, T: float, nthreads: int = 0) -> RowStats:
+    """Step 1 on every row of logits [B, k+1, V] (device layout) at temperature T."""
+    B, k1, V = logits.shape
+    lg, dt = _logits_arg(logits, dtype)
+    st = RowStats(np.zeros((B, k1)), np.zeros((B, k1)), np.zeros((B, k1), np.int32),
+                  np.zeros((B, k1), np.int32))
+    rc = _load().orc_row_stats_batch(_ptr(lg), dt, float(T), B * k1, V, _ptr(st.m), _ptr(st.S),
+                                     _ptr(st.argmax), _ptr(st.bad), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    return st
+
+
+def verify_batch_stats(mode, logits, dtype: str, q, x, ua, ur, T, stats: RowStats,
+                       nthreads: int = 0) -> BatchResult:
+    """verify_batch (modes SAMPLE, GREEDY, SAMPLE_BUGGY) with the per-row statistics
+    of ``row_stats_batch`` on these logits (at T; at 1 for GREEDY) supplied instead of
+    recomputed.  The per-row fields of the result are None."""
+    B, k1, V = logits.shape
+    k = k1 - 1
+    lg, dt = _logits_arg(logits, dtype)
+    greedy = mode == GREEDY
+    qq = None if greedy else np.ascontiguousarray(q, dtype=np.float32)
+    x = np.ascontiguousarray(x, dtype=np.int32)
+    uu = None if greedy else np.ascontiguousarray(ua, dtype=np.float32)
+    rr = None if greedy else np.ascontiguousarray(ur, dtype=np.float32)
+    r = BatchResult(out=np.zeros((B, k1), np.int32), n=np.zeros(B, np.int32), row_m=None,
+                    row_S=None, row_argmax=None, row_px=None, row_qx=None,
+                    thr=np.zeros((B, k)), draw_lo=np.zeros(B), draw_hi=np.zeros(B),
+                    flags=np.zeros(B, np.int32))
+    c = lambda a: np.ascontiguousarray(a)
+    m, S, am, bad = c(stats.m), c(stats.S), c(stats.argmax), c(stats.bad)
+    rc = _load().orc_verify_batch_stats(
+        int(mode), _ptr(lg), dt, _ptr(qq), _ptr(x), _ptr(uu), _ptr(rr), float(T), B, k, V,
+        _ptr(m), _ptr(S), _ptr(am), _ptr(bad), _ptr(r.out), _ptr(r.n), _ptr(r.thr),
+        _ptr(r.draw_lo), _ptr(r.draw_hi), _ptr(r.flags), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    return r
+
+
+@dataclass
+class Comparison:
+    rows: int
+    sequences: int
+    mismatched_sequences: int
+    near_threshold: int
+    hard: int
+    hard_detail: list
+
+
+def compare_outputs(mode: str, ua, ur, out, n, ref: BatchResult, tol_u: float) -> Comparison:
+    """Integer outputs of a verify (out [B, k+1], n [B]) against the oracle's.
+
+    Greedy outputs must be equal.  In sampled mode a sequence that differs is a
+    near-threshold case when its first differing decision had its uniform
+    within tol_u of the oracle's threshold: min(1, P/Q) for an accept test (at
+    the first position where the two accepted lengths differ), a bin boundary
+    C_{t-1}/C_tot or C_t/C_tot for the draw; anything else is a hard mismatch.
+    """
+    B, k1 = out.shape
+    near = hard = mism = 0
+    detail = []
+    for b in np.flatnonzero((n != ref.n) | np.any(out != ref.out, axis=1)):
+        mism += 1
+        if mode == "greedy" or n[b] < 0 or ref.n[b] < 0:
+            hard += 1
+            detail.append((int(b), "greedy/invalid", int(n[b]), int(ref.n[b])))
+            continue
+        if n[b] != ref.n[b]:
+            i = int(min(n[b], ref.n[b]))
+            gap = abs(float(ua[b, i]) - float(ref.thr[b, i]))
+            kind = "accept"
+        else:
+            u = float(ur[b])
+            gap = min(abs(u - ref.draw_lo[b]), abs(u - ref.draw_hi[b]))
+            kind = "draw"
+        if gap < tol_u:
+            near += 1
+        else:
+            hard += 1
+            detail.append((int(b), kind, gap))
+    return Comparison(B * k1, B, mism, near, hard, detail[:10])
 
 
 def ngram_draft(history, lengths, k: int, n_min: int, n_max: int):

@@ -217,10 +217,43 @@ static void verify_match(const double* logits, const int32_t* x, const double* u
     *n_acc = n;
 }
 
+/* Per-row statistics of one sequence supplied by the caller: the values step 1
+ * (orc_row_stats) returned earlier for these same rows at the same T; rows i
+ * of the sequence at index i. */
+typedef struct {
+    const double* m;
+    const double* S;
+    const int32_t* argmax;
+    const int32_t* bad;
+} given_stats;
+
+/* Step 1 for row i: computed, or taken from `g` when the caller supplies it. */
+static int stats_of(const double* li, double T, int V, const given_stats* g, int i, double* m,
+                    double* S, int32_t* am) {
+    if (!g) return orc_row_stats(li, T, V, m, S, am);
+    *m = g->m[i];
+    *S = g->S[i];
+    *am = g->argmax[i];
+    return g->bad[i];
+}
+
+static void verify_seq(int mode, const double* logits, const double* q, const int32_t* x,
+                       const double* ua, double ur, double T, int k, int V, int32_t* out,
+                       int32_t* n_acc, double* thr, double* draw_lo, double* draw_hi,
+                       int32_t* flags, const given_stats* g);
+
 void orc_verify_seq(int mode, const double* logits, const double* q, const int32_t* x,
                     const double* ua, double ur, double T, int k, int V,
                     int32_t* out, int32_t* n_acc, double* thr, double* draw_lo,
                     double* draw_hi, int32_t* flags) {
+    verify_seq(mode, logits, q, x, ua, ur, T, k, V, out, n_acc, thr, draw_lo, draw_hi, flags,
+               NULL);
+}
+
+static void verify_seq(int mode, const double* logits, const double* q, const int32_t* x,
+                       const double* ua, double ur, double T, int k, int V, int32_t* out,
+                       int32_t* n_acc, double* thr, double* draw_lo, double* draw_hi,
+                       int32_t* flags, const given_stats* g) {
     if (mode == ORC_MATCH) {
         if (flags) *flags = 0;
         if (thr)
@@ -244,7 +277,7 @@ void orc_verify_seq(int mode, const double* logits, const double* q, const int32
         const double* li = logits + (size_t)i * V;
         double m, S;
         int32_t am;
-        if (orc_row_stats(li, Tr, V, &m, &S, &am)) {
+        if (stats_of(li, Tr, V, g, i, &m, &S, &am)) {
             mark_invalid(k, out, n_acc, flags);
             return;
         }
@@ -277,7 +310,7 @@ void orc_verify_seq(int mode, const double* logits, const double* q, const int32
     const double* ln = logits + (size_t)n * V;
     double m, S;
     int32_t am;
-    if (orc_row_stats(ln, Tr, V, &m, &S, &am)) {
+    if (stats_of(ln, Tr, V, g, n, &m, &S, &am)) {
         mark_invalid(k, out, n_acc, flags);
         return;
     }
@@ -418,6 +451,82 @@ int orc_verify_batch(int mode, const void* logits, int dtype, const float* q,
                            Td, k, V, out + (size_t)b * (k + 1), n_acc + b,
                            thr ? thr + (size_t)b * k : NULL, draw_lo ? draw_lo + b : NULL,
                            draw_hi ? draw_hi + b : NULL, &fl);
+            if (flags) flags[b] = fl;
+        }
+        free(L);
+        free(Qd);
+        free(ua_d);
+    }
+    return 0;
+}
+
+/* Step 0 for one sequence: its k+1 logits rows and k q rows as doubles. */
+static void seq_to_double(const void* logits, int dtype, const float* q, size_t b, size_t seqsz,
+                          size_t qsz, double* L, double* Qd) {
+    if (dtype == 0) {
+        const uint16_t* src = (const uint16_t*)logits + b * seqsz;
+        for (size_t j = 0; j < seqsz; ++j) L[j] = bf16_to_double(src[j]);
+    } else {
+        const float* src = (const float*)logits + b * seqsz;
+        for (size_t j = 0; j < seqsz; ++j) L[j] = (double)src[j];
+    }
+    if (Qd) {
+        const float* qs = q + b * qsz;
+        for (size_t j = 0; j < qsz; ++j) Qd[j] = (double)qs[j];
+    }
+}
+
+int orc_row_stats_batch(const void* logits, int dtype, float T, int R, int V, double* m,
+                        double* S, int32_t* argmax, int32_t* bad, int nthreads) {
+    if (R < 0 || V < 1 || !logits || !m || !S || !argmax || !bad) return -1;
+    if (dtype != 0 && dtype != 1) return -1;
+    int nt = nthreads > 0 ? nthreads : orc_max_threads();
+    (void)nt;
+#pragma omp parallel num_threads(nt)
+    {
+        double* L = (double*)malloc(sizeof(double) * (size_t)V);
+#pragma omp for schedule(dynamic, 1)
+        for (int r = 0; r < R; ++r) {
+            seq_to_double(logits, dtype, NULL, (size_t)r, (size_t)V, 0, L, NULL);
+            bad[r] = orc_row_stats(L, (double)T, V, m + r, S + r, argmax + r);
+        }
+        free(L);
+    }
+    return 0;
+}
+
+int orc_verify_batch_stats(int mode, const void* logits, int dtype, const float* q,
+                           const int32_t* x, const float* ua, const float* ur, float T, int B,
+                           int k, int V, const double* st_m, const double* st_S,
+                           const int32_t* st_argmax, const int32_t* st_bad, int32_t* out,
+                           int32_t* n_acc, double* thr, double* draw_lo, double* draw_hi,
+                           int32_t* flags, int nthreads) {
+    if (B < 0 || k < 1 || V < 1 || !logits || !x || !out || !n_acc) return -1;
+    if (!st_m || !st_S || !st_argmax || !st_bad) return -1;
+    if (dtype != 0 && dtype != 1) return -1;
+    if (mode != ORC_SAMPLE && mode != ORC_GREEDY && mode != ORC_SAMPLE_BUGGY) return -1;
+    const int greedy = (mode == ORC_GREEDY);
+    if (!greedy && (!q || !ua || !ur)) return -1;
+    const double Td = greedy ? 1.0 : (double)T;
+    const size_t seqsz = (size_t)(k + 1) * V, qsz = (size_t)k * V;
+    int nt = nthreads > 0 ? nthreads : orc_max_threads();
+    (void)nt;
+#pragma omp parallel num_threads(nt)
+    {
+        double* L = (double*)malloc(sizeof(double) * seqsz);
+        double* Qd = greedy ? NULL : (double*)malloc(sizeof(double) * qsz);
+        double* ua_d = (double*)malloc(sizeof(double) * (size_t)k);
+#pragma omp for schedule(dynamic, 1)
+        for (int b = 0; b < B; ++b) {
+            seq_to_double(logits, dtype, q, (size_t)b, seqsz, qsz, L, Qd);
+            if (!greedy)
+                for (int i = 0; i < k; ++i) ua_d[i] = (double)ua[(size_t)b * k + i];
+            const size_t r0 = (size_t)b * (k + 1);
+            const given_stats g = {st_m + r0, st_S + r0, st_argmax + r0, st_bad + r0};
+            int32_t fl = 0;
+            verify_seq(mode, L, Qd, x + (size_t)b * k, ua_d, greedy ? 0.0 : (double)ur[b], Td, k,
+                       V, out + (size_t)b * (k + 1), n_acc + b, thr ? thr + (size_t)b * k : NULL,
+                       draw_lo ? draw_lo + b : NULL, draw_hi ? draw_hi + b : NULL, &fl, &g);
             if (flags) flags[b] = fl;
         }
         free(L);

@@ -82,6 +82,26 @@ int orc_verify_batch(int mode, const void* logits, int dtype, const float* q,
                      double* row_px, double* row_qx, double* thr,
                      double* draw_lo, double* draw_hi, int32_t* flags, int nthreads);
 
+/* Step 1 over R rows in the device layout (bf16 bit patterns, dtype 0, or
+ * float32, dtype 1), R = B*(k+1) for a batch: m[r], S[r], argmax[r] as
+ * orc_row_stats gives them at temperature T, bad[r] its return value. */
+int orc_row_stats_batch(const void* logits, int dtype, float T, int R, int V, double* m,
+                        double* S, int32_t* argmax, int32_t* bad, int nthreads);
+
+/* orc_verify_batch for modes ORC_SAMPLE, ORC_GREEDY and ORC_SAMPLE_BUGGY with
+ * the per-row statistics supplied instead of recomputed: st_m, st_S,
+ * st_argmax, st_bad [B][k+1] as orc_row_stats_batch returned them for these
+ * logits (at T, or at 1 in greedy mode).  Wherever the scan or the draw needs a
+ * row's statistics it reads them there; every other step, and every output,
+ * is that of orc_verify_batch (which has no per-row outputs here).  For
+ * verifying one set of logits many times with fresh drafts and uniforms. */
+int orc_verify_batch_stats(int mode, const void* logits, int dtype, const float* q,
+                           const int32_t* x, const float* ua, const float* ur, float T, int B,
+                           int k, int V, const double* st_m, const double* st_S,
+                           const int32_t* st_argmax, const int32_t* st_bad, int32_t* out,
+                           int32_t* n_acc, double* thr, double* draw_lo, double* draw_hi,
+                           int32_t* flags, int nthreads);
+
 /* Number of OpenMP threads a batch call with nthreads <= 0 would use. */
 int orc_max_threads(void);
 

@@ -453,3 +453,55 @@ def test_ngram_drafter_periodic_stream(orc):
     h = np.arange(50, dtype=np.int32)[None, :]
     d, num = orc.ngram_draft(h, np.array([50], np.int32), k, 1, 4)
     assert num[0] == 0 and (d == -1).all()
+
+
+# ---------------------------------------------------------------- supplied statistics
+
+@pytest.mark.parametrize("mode", [SAMPLE, GREEDY, SAMPLE_BUGGY])
+def test_supplied_stats_batch_equals_plain_batch(orc, mode):
+    """verify_batch_stats with the statistics of row_stats_batch gives, bit for
+    bit, what verify_batch computes by itself: the supplied statistics are only
+    step 1's own values, read instead of recomputed.  Invalid rows, tokens and
+    uniforms are mixed in, and rows are scaled to T as the verify uses them."""
+    from speculative_decoding_verification_18_gb300.inputs import make_inputs
+    for dtype, V, T in (("f32", 37, 0.8), ("bf16", 1000, 1.3), ("f32", 5, 1.0)):
+        inp = make_inputs(mode="greedy" if mode == GREEDY else "sample", B=64, k=5, V=V,
+                          dtype=dtype, T=T, kind="zipf", draft_sigma=0.6, p_argmax=0.6,
+                          seed=V)
+        lg = inp.logits.copy()
+        x = inp.x.copy()
+        ua = None if inp.ua is None else inp.ua.copy()
+        bad_val = 0x7FC0 if dtype == "bf16" else np.float32(np.nan)
+        lg[3, 1, V // 2] = bad_val           # a NaN in a row the scan may reach
+        lg[7, 0, :] = 0xFF80 if dtype == "bf16" else -np.inf  # an all -inf row
+        x[9, 0] = V                           # a token out of range
+        if ua is not None:
+            ua[11, 0] = 1.0                   # a uniform out of range
+        Tv = 1.0 if mode == GREEDY else T
+        st = orc.row_stats_batch(lg, dtype, Tv)
+        a = orc.verify_batch(mode, lg, dtype, inp.q, x, ua, inp.ur, Tv)
+        b = orc.verify_batch_stats(mode, lg, dtype, inp.q, x, ua, inp.ur, Tv, st)
+        assert np.array_equal(a.out, b.out) and np.array_equal(a.n, b.n)
+        assert np.array_equal(a.flags, b.flags)
+        for f in ("thr", "draw_lo", "draw_hi"):
+            assert np.array_equal(getattr(a, f), getattr(b, f), equal_nan=True)
+        # the supplied statistics are the batch's own per-row values
+        assert np.array_equal(st.argmax, a.row_argmax)
+        assert np.array_equal(st.m, a.row_m)
+        assert np.array_equal(np.where(st.bad == 1, np.nan, st.S), a.row_S, equal_nan=True)
+        assert (a.n < 0).sum() >= 2
+
+
+def test_supplied_stats_are_read(orc):
+    """The supplied statistics are really used: a planted change to one row's
+    argmax changes the greedy outcome of that sequence and of no other."""
+    from speculative_decoding_verification_18_gb300.inputs import make_inputs
+    inp = make_inputs(mode="greedy", B=8, k=3, V=50, dtype="f32", kind="zipf", p_argmax=1.0,
+                      seed=4)
+    st = orc.row_stats_batch(inp.logits, "f32", 1.0)
+    a = orc.verify_batch_stats(GREEDY, inp.logits, "f32", None, inp.x, None, None, 1.0, st)
+    assert (a.n == 3).all()
+    st.argmax[2, 1] = (st.argmax[2, 1] + 1) % 50
+    b = orc.verify_batch_stats(GREEDY, inp.logits, "f32", None, inp.x, None, None, 1.0, st)
+    assert b.n[2] == 1 and b.out[2, 1] == st.argmax[2, 1]
+    assert np.array_equal(np.delete(a.out, 2, 0), np.delete(b.out, 2, 0))
