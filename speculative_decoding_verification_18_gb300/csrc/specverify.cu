@@ -1552,6 +1552,7 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(VerifyArgs a) {
         a.hdr->k = k;
         a.hdr->V = V;
         a.hdr->mode = SAMPLED ? SV_MODE_SAMPLE : SV_MODE_GREEDY;
+        a.hdr->flat_ctas = 0;  // one record per row
     }
     // Draft tokens, their logits and q values, and the uniforms of this sequence.
     for (int i = tid; i < k; i += kThreads) {
@@ -2119,8 +2120,10 @@ __global__ void __launch_bounds__(kFlatThreads, 2) sv_flat_greedy_kernel(FlatArg
 
 // One warp per sequence: the lanes load the records in parallel, lane 0 scans.
 // After the flat stream, the lanes first merge their rows' partial keys into
-// the row records (and store them, for the row statistics).
-__global__ void sv_finish_greedy_kernel(const int32_t* __restrict__ x, RowRec* __restrict__ rows,
+// row records of their own (the keys stay in the workspace, so running the
+// finish twice gives the same result, and the host merges them the same way
+// for the row statistics).
+__global__ void sv_finish_greedy_kernel(const int32_t* __restrict__ x, const RowRec* __restrict__ rows,
                                         const Header* __restrict__ hdr,
                                         uint32_t* __restrict__ seqstat, int B, int k,
                                         int32_t* __restrict__ out, int32_t* __restrict__ nacc,
@@ -2160,7 +2163,8 @@ __global__ void sv_finish_greedy_kernel(const int32_t* __restrict__ x, RowRec* _
             rec.argmax = nan ? 0 : (int32_t)(0xFFFFFFFFu - (uint32_t)key);
             rec.flags = (nan || !(m > -INFINITY) || m == INFINITY) ? kRowBad : 0u;
             if (i < k && (xi < 0 || xi >= V)) rec.flags |= kRowTokenBad;
-            rows[r] = rec;
+            // The keys stay in the workspace (not overwritten by the merged
+            // record), so the finish can run again on the same stream output.
         }
         rr[i] = rec;
     }
@@ -2328,7 +2332,6 @@ __global__ void __launch_bounds__(SAMPLED ? kThreads : 64)
         for (int i = tid; i < N; i += NT) {
             const long long r = (long long)b * N + i;
             s_rec[i] = row_record(a.rows, r, P, vpr, per, rem);
-            if (P) a.rows[r] = s_rec[i];
         }
         __syncthreads();
         if (tid == 0 && !s_bits) {
@@ -3495,7 +3498,7 @@ static sv_status launch_finish(bool sampled, const void* logits, sv_dtype dt, co
         cfg.stream = stream;
         cfg.attrs = &pdl;
         cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, sv_finish_greedy_kernel, x, const_cast<RowRec*>(rows),
+        e = cudaLaunchKernelEx(&cfg, sv_finish_greedy_kernel, x, rows,
                                static_cast<const Header*>(ws), seqstat, B, k, out, nacc,
                                ep);
         return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
@@ -3699,6 +3702,35 @@ static sv_status run_tree(bool sampled, const void* logits, sv_dtype dt, const f
                           : cudaLaunchKernelEx(&cfg, sv_tree_kernel<float, false>, a);
     return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
+
+// The row record that the flat greedy stream's partial keys of row r stand
+// for, merged on the host the way the finish kernel merges them on the device:
+// the largest key names the maximum and the lowest index holding it, an
+// all-ones key a NaN in the row.
+static RowRec merge_flat_keys_host(const RowRec& raw, long long r, int vpr, int per, int rem,
+                                   bool drafted) {
+    const int c0 = flat_owner((int)r * vpr, per, rem);
+    const int c1 = flat_owner((int)(r + 1) * vpr - 1, per, rem);
+    unsigned long long w[kFlatSlots];
+    std::memcpy(w, &raw, sizeof(w));
+    unsigned long long key = 0ull;
+    for (int c = c0; c <= c1 && c - c0 < kFlatSlots; ++c) key = w[c - c0] > key ? w[c - c0] : key;
+    const bool nan = key == ~0ull;
+    const uint32_t o = (uint32_t)(key >> 32);
+    const uint32_t bits = (o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o;
+    float m;
+    std::memcpy(&m, &bits, sizeof(m));
+    RowRec rec;
+    rec.mraw = nan ? NAN : m;
+    rec.S = 0.0f;
+    rec.px = drafted ? 0.0 : (double)NAN;
+    rec.lx = NAN;
+    rec.qx = NAN;
+    rec.argmax = nan ? 0 : (int32_t)(0xFFFFFFFFu - (uint32_t)key);
+    rec.flags = (nan || !(m > -INFINITY) || m == INFINITY) ? kRowBad : 0u;
+    return rec;
+}
+static_assert(kFlatSlots * sizeof(unsigned long long) == sizeof(RowRec), "flat key slots");
 
 }  // namespace sv
 
@@ -3918,11 +3950,16 @@ sv_status spec_verify_row_stats(const void* ws, cudaStream_t stream, int B, int 
         return SV_ERR_CUDA;
     }
     for (long long r = 0; r < R; ++r) {
-        if (m) m[r] = host[r].mraw;
-        if (S) S[r] = host[r].S;
-        if (argmax) argmax[r] = host[r].argmax;
-        if (px) px[r] = (float)host[r].px;
-        if (qx) qx[r] = host[r].qx;
+        RowRec rec = host[r];
+        // After the flat greedy stream the records hold per-range partial keys
+        // until a reader merges them (the finish kernel merges its own copies).
+        if (h.flat_ctas) rec = merge_flat_keys_host(rec, r, (int)h.flat_vpr, (int)h.flat_per,
+                                                    (int)h.flat_rem, (int)(r % (k + 1)) < k);
+        if (m) m[r] = rec.mraw;
+        if (S) S[r] = rec.S;
+        if (argmax) argmax[r] = rec.argmax;
+        if (px) px[r] = (float)rec.px;
+        if (qx) qx[r] = rec.qx;
     }
     delete[] host;
     return SV_OK;

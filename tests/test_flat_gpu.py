@@ -15,7 +15,7 @@ import pytest
 import torch
 
 import oracle
-from parity import compare_outputs, compare_stats, run_gpu, run_oracle
+from parity import Guarded, compare_outputs, compare_stats, run_gpu, run_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -141,9 +141,10 @@ def test_flat_two_stage_and_graph_replay():
     assert np.array_equal(out1, out2) and np.array_equal(n1, n2)
     lg = torch.from_numpy(inp.logits.view(np.int16)).view(torch.bfloat16).cuda()
     x = torch.from_numpy(inp.x).cuda()
-    out = torch.full((64, 5), -7, dtype=torch.int32, device="cuda")
-    n = torch.full((64,), -7, dtype=torch.int32, device="cuda")
-    ws = sv.workspace(64, 4, 32000, torch.bfloat16)
+    gd = Guarded()
+    out = gd.empty((64, 5), torch.int32, fill=-7)
+    n = gd.empty((64,), torch.int32, fill=-7)
+    ws = gd.workspace(64, 4, 32000, torch.bfloat16)
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
         sv.spec_verify_greedy(lg, x, out, n, ws)
@@ -156,6 +157,7 @@ def test_flat_two_stage_and_graph_replay():
         for _ in range(3):
             g.replay()
     torch.cuda.synchronize()
+    gd.check()
     assert np.array_equal(out.cpu().numpy(), out1) and np.array_equal(n.cpu().numpy(), n1)
 
 
@@ -172,18 +174,20 @@ def test_workspace_reused_across_paths():
                        draft_sigma=0.4, seed=42)
     t_in = make_tree_inputs(mode="greedy", B=B, N=k + 1, V=V, dtype="bf16", branching=(2,),
                             seed=43)
-    ws = sv.workspace(B, k, V, torch.bfloat16)
+    gd = Guarded()
+    ws = gd.workspace(B, k, V, torch.bfloat16)
     assert _flat_ctas(g_in) > 0
     for step, off in enumerate([0, None, 1, "tree", 0]):
         if off == "tree":
             lg = torch.from_numpy(t_in.logits.view(np.int16)).view(torch.bfloat16).cuda()
-            out = torch.empty((B, k + 1), dtype=torch.int32, device="cuda")
-            nodes = torch.empty((B, k + 1), dtype=torch.int32, device="cuda")
-            n = torch.empty(B, dtype=torch.int32, device="cuda")
+            out = gd.empty((B, k + 1), torch.int32)
+            nodes = gd.empty((B, k + 1), torch.int32)
+            n = gd.empty(B, torch.int32)
             sv.spec_verify_tree(sv.SV_MODE_GREEDY, lg, None, torch.from_numpy(t_in.tok).cuda(),
                                 torch.from_numpy(t_in.par).cuda(), None, None, 1.0, out, nodes,
                                 n, ws)
             torch.cuda.synchronize()
+            gd.check()
             ref = oracle.tree_batch(oracle.GREEDY, t_in.logits, "bf16", None, t_in.tok, t_in.par,
                                     None, None, 1.0)
             assert np.array_equal(out.cpu().numpy(), ref.out), step
@@ -198,3 +202,36 @@ def test_workspace_reused_across_paths():
         ref = run_oracle(inp)
         rep = compare_outputs(inp, out, n, ref)
         assert rep.hard == 0, (step, rep.hard_detail)
+
+
+def test_flat_finish_twice_and_stats_before_finish():
+    """After one flat spec_verify_rows, spec_verify_row_stats (which merges the
+    partial keys on the host) and two spec_verify_finish calls in a row all agree
+    with the oracle: the finish merges the keys into copies of its own and leaves
+    them in the workspace, so it can run again on the same row stream output."""
+    from speculative_decoding_verification_18_gb300 import specverify as sv
+    for B, k, V, dtype in ((64, 4, 32000, "bf16"), (40, 3, 12000, "f32")):
+        inp = _greedy(B, k, V, dtype, seed=B + V)
+        assert _flat_ctas(inp) > 0
+        ref = run_oracle(inp)
+        if dtype == "bf16":
+            lg = torch.from_numpy(inp.logits.view(np.int16)).view(torch.bfloat16).cuda()
+        else:
+            lg = torch.from_numpy(inp.logits).cuda()
+        x = torch.from_numpy(inp.x).cuda()
+        gd = Guarded()
+        ws = gd.workspace(B, k, V, lg.dtype)
+        sv.spec_verify_rows(sv.SV_MODE_GREEDY, lg, None, x, 1.0, ws)
+        stats = sv.spec_verify_row_stats(ws, B, k)
+        assert np.array_equal(stats["argmax"], ref.row_argmax)
+        assert np.array_equal(stats["m"].astype(np.float64), ref.row_m)
+        for rep in range(2):
+            out = gd.empty((B, k + 1), torch.int32, fill=-7)
+            n = gd.empty(B, torch.int32, fill=-7)
+            sv.spec_verify_finish(sv.SV_MODE_GREEDY, lg, None, x, None, None, 1.0, out, n, ws)
+            torch.cuda.synchronize()
+            assert np.array_equal(out.cpu().numpy(), ref.out), rep
+            assert np.array_equal(n.cpu().numpy(), ref.n), rep
+        stats = sv.spec_verify_row_stats(ws, B, k)
+        assert np.array_equal(stats["argmax"], ref.row_argmax)
+        gd.check()
