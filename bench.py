@@ -1,25 +1,31 @@
 #!/usr/bin/env python3
 """Benchmark of the batched speculative-decoding verify step on GB300.
 
-One step = one verify of one batch of the named workload (default c2: greedy,
-B=64, k=4, V=32000, bf16 logits): the row stream, the accept scan and the draw.
-Metric: verify rows per second, rows = B*(k+1) per step, summed over GPUs.
+One step = one verify of one batch of the named workload (default c4, the
+largest: sampled, B=256, k=8, V=151936, fp32 logits, T=1): the row stream, the
+accept scan and the draw.  Metric: verify rows per second, rows = B*(k+1) per
+step, summed over GPUs.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c1..c5]
                   [--impl ours|reference]
 
 Timing: inputs are resident in HBM and rotated over enough copies to exceed the
-129 MB L2 between reuses; K steps are replayed from CUDA graphs (one graph of
-`copies` consecutive verifies) and timed with CUDA events on the launching
-stream, bracketed by a barrier and a device synchronisation, max over ranks.
+129 MB L2 between reuses; exactly W warm-up steps, then exactly K timed steps,
+replayed from CUDA graphs (one graph of `copies` consecutive verifies, and one
+of the first K mod copies for the remainder) and timed with CUDA events on the
+launching stream, bracketed by a barrier and a device synchronisation, max over
+ranks.
 Each kernel of the path the one-call API takes is timed the same way for the
 roofline figure (the fused kernel is the whole verify; on the two-stage paths
 the row stream and the draw kernel are replayed alone), and the slower one is
 reported.  `e2e` repeats the measurement through the same C ABI with
 the inputs in pinned HOST memory: every step copies its inputs host-to-device,
 verifies and copies the outputs back.  `cpu_baseline` times the float64 oracle
-on a bounded sample on this host's cores.  With --impl reference the oracle is
-the reference arm.
+on a bounded sample on this host's cores (and on one core), and its outputs on
+the timed inputs are compared with the GPU's (mismatches, near-threshold cases);
+the realised acceptance rate alpha = sum min(p, q) of the inputs is reported
+beside the measured acceptance.  With --impl reference the oracle is the
+reference arm.
 """
 from __future__ import annotations
 
@@ -48,8 +54,8 @@ def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=0, help="timed steps (0: about 2 s worth)")
-    ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default="c2", choices=sorted(I.WORKLOADS))
+    ap.add_argument("--warmup", type=int, default=10, help="warm-up steps (at least 3)")
+    ap.add_argument("--workload", default="c4", choices=sorted(I.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     return ap.parse_args()
 
@@ -244,6 +250,43 @@ def oracle_time(inp, seqs, nthreads, min_seconds=3.0, min_reps=2):
     return (time.perf_counter() - t0) / reps
 
 
+def oracle_parity(inp, out, n, nthreads):
+    """The oracle on the whole timed batch, compared with the GPU's outputs by
+    the parity rule (greedy: equal; sampled: equal up to decisions whose uniform
+    lies within 1e-5 of the oracle's threshold)."""
+    import oracle
+    mode = oracle.GREEDY if inp.mode == "greedy" else oracle.SAMPLE
+    ref = oracle.verify_batch(mode, inp.logits, inp.dtype, inp.q, inp.x, inp.ua, inp.ur,
+                              inp.T if inp.mode == "sample" else 1.0, nthreads=nthreads)
+    c = oracle.compare_outputs(inp.mode, inp.ua, inp.ur, out, n, ref, 1e-5)
+    return {"rows": c.rows, "sequences": c.sequences,
+            "mismatched_sequences": c.mismatched_sequences,
+            "near_threshold": c.near_threshold, "hard": c.hard}
+
+
+def acceptance_report(inp, n_all):
+    """Realised acceptance of the timed inputs: alpha = sum_v min(p_i(v), q_i(v))
+    per drafted row (the chance a draft from q is accepted), its mean over the
+    batch, and the measured accepted fraction and tokens per verify."""
+    n = np.concatenate([np.asarray(v) for v in n_all])
+    rep = {"accepted_fraction": float(np.clip(n, 0, None).mean() / inp.k),
+           "tokens_per_verify": float((np.clip(n, 0, None) + 1).mean())}
+    if inp.mode != "sample":
+        return rep
+    lv = inp.logits_f32()
+    al = []
+    for b in range(inp.B):
+        z = lv[b, :inp.k].astype(np.float64) / inp.T
+        z -= z.max(axis=1, keepdims=True)
+        p = np.exp(z)
+        p /= p.sum(axis=1, keepdims=True)
+        al.append(np.minimum(p, inp.q[b]).sum(axis=1))
+    al = np.concatenate(al)
+    rep.update(alpha_mean=float(al.mean()), alpha_min=float(al.min()),
+               alpha_max=float(al.max()))
+    return rep
+
+
 def cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -376,23 +419,39 @@ def main():
         for i in range(copies):
             verify(i)  # device set-up outside capture
     torch.cuda.synchronize(dev)
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(stream):
-        with torch.cuda.graph(graph, stream=stream):
-            for i in range(copies):
-                verify(i)
-    torch.cuda.synchronize(dev)
+    def capture(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(n):
+                    verify(i)
+        torch.cuda.synchronize(dev)
+        return g
 
-    # Warm-up (at least 3 steps), then pick K if not given (about 2 s of steps).
-    warm_reps = max(1, -(-max(3, args.warmup) // copies))
+    graph = capture(copies)
+    partial = {}
+
+    def run_steps(n):
+        """Exactly n verify steps: whole graphs of `copies` steps, then a graph of
+        the first n mod copies."""
+        for _ in range(n // copies):
+            graph.replay()
+        r = n % copies
+        if r:
+            if r not in partial:
+                partial[r] = capture(r)
+            partial[r].replay()
+
+    # Exactly W warm-up steps (at least 3), then K (if not given, about 2 s of steps).
+    W = max(3, args.warmup)
     t0 = time.perf_counter()
-    for _ in range(warm_reps):
-        graph.replay()
+    with torch.cuda.stream(stream):
+        run_steps(W)
     torch.cuda.synchronize(dev)
-    est = (time.perf_counter() - t0) / (warm_reps * copies)
+    est = (time.perf_counter() - t0) / W
     K = args.steps if args.steps > 0 else int(min(200000, max(copies, 2.0 / max(est, 1e-7))))
-    reps = -(-K // copies)
-    K = reps * copies
+    if K % copies and (K % copies) not in partial:
+        partial[K % copies] = capture(K % copies)
 
     uuid = None
     try:
@@ -411,8 +470,7 @@ def main():
         ev1 = torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
             ev0.record(stream)
-            for _ in range(reps):
-                graph.replay()
+            run_steps(K)
             ev1.record(stream)
         torch.cuda.synchronize(dev)
         if dist:
@@ -433,7 +491,7 @@ def main():
                         fn(i)
                 g.replay()
                 torch.cuda.synchronize(dev)
-                r1 = max(1, reps // 2)
+                r1 = max(1, -(-K // copies) // 2)
                 a0 = torch.cuda.Event(enable_timing=True)
                 a1 = torch.cuda.Event(enable_timing=True)
                 a0.record(stream)
@@ -559,17 +617,24 @@ def main():
         roofline["rows_read"] = rows_read
         roofline["rows_needed"] = int(np.mean([np.sum(np.clip(nn, 0, k) + 1) for nn in n_all]))
 
-    # ---- CPU baseline: the oracle on a bounded sample
+    # ---- CPU baseline: the oracle on a bounded sample, on every core and on one
     nt = cores()
     per_call = oracle_time(inp, min(B, 1), nt, min_seconds=0.2, min_reps=1)
     seqs = int(max(1, min(B, 5.0 / max(per_call, 1e-9))))
     t_cpu = oracle_time(inp, seqs, nt, min_seconds=5.0, min_reps=2)
     cpu_value = seqs * (k + 1) / t_cpu
+    seqs1 = int(max(1, min(B, 3.0 / max(per_call * nt, 1e-9))))
+    t_cpu1 = oracle_time(inp, seqs1, 1, min_seconds=3.0, min_reps=1)
+    cpu_value1 = seqs1 * (k + 1) / t_cpu1
+
+    # ---- the oracle on the whole timed batch against the GPU's outputs (copy 0)
+    parity = oracle_parity(inp, outs[0].cpu().numpy(), ns[0].cpu().numpy(), nt)
+    accept = acceptance_report(inp, n_all)
 
     line = {
         "metric": "verify rows/s", "value": value, "unit": "rows/s", "n_gpus": world,
         "sequences_per_s": value / (k + 1),
-        "steps": K, "warmup": warm_reps * copies, "ms_per_step": ms / K,
+        "steps": K, "warmup": W, "ms_per_step": ms / K,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
         "config": {"workload": f"{args.workload}: {I.WORKLOAD_NAMES[args.workload]}",
@@ -577,7 +642,8 @@ def main():
                    "T": inp.T, "rows_per_step": rows_per_step,
                    "l2": f"inputs rotated over {copies} device copies "
                          f"({copies * set_bytes / 2**20:.0f} MiB > 129 MB L2)",
-                   "timing": f"{reps} replays of a CUDA graph of {copies} verifies",
+                   "timing": f"{K // copies} replays of a CUDA graph of {copies} verifies"
+                             + (f" and one of {K % copies}" if K % copies else ""),
                    "path": {sv.PATH_FUSED: "fused per-sequence kernel",
                             sv.PATH_SKIP: "position-major row stream with row skipping + draw kernel",
                             sv.PATH_TWO_KERNEL: "row stream + draw kernels"}[path]
@@ -591,7 +657,12 @@ def main():
         "roofline": roofline,
         "cpu_baseline": {"value": cpu_value, "unit": "rows/s", "cores": nt, "kind": "oracle",
                          "sample": f"first {seqs} of {B} sequences ({seqs * (k + 1)} rows), "
-                                   f"repeated for >= 5 s"},
+                                   f"repeated for >= 5 s",
+                         "value_1_thread": cpu_value1,
+                         "sample_1_thread": f"first {seqs1} of {B} sequences, one thread, "
+                                            f"repeated for >= 3 s"},
+        "parity": parity,
+        "acceptance": accept,
     }
     print(json.dumps(line), flush=True)
     if dist:

@@ -336,3 +336,36 @@ def make_tree_inputs(mode="sample", B=1, N=16, V=32000, dtype="bf16", T=1.0,
     ur = np.random.default_rng(s["u_resample"]).random(B, dtype=np.float32)
     return TreeInputs(mode, dtype, B, N, V, float(T), logits, q, tok, par, ua, ur,
                       meta=dict(seed=seed, branching=branching))
+
+
+@dataclass
+class Redraws:
+    """Fresh drafts and uniforms for `reps` repetitions of one sampled batch."""
+    x: np.ndarray    # [reps, B, k] int32, each x[r, b, i] drawn from q[b, i]
+    ua: np.ndarray   # [reps, B, k] float32 in [0, 1)
+    ur: np.ndarray   # [reps, B] float32 in [0, 1)
+
+
+def redraw(inp: VerifyInputs, reps: int, seed: int) -> Redraws:
+    """Seeded drafted tokens and uniforms for `reps` more verifies of the same
+    logits and q: each repetition draws every x[b, i] afresh from the float32 row
+    q[b, i] (numpy's ``Generator.choice``, as ``make_inputs`` does) and new
+    u_accept / u_resample.  Many seeded rows then cost one logits tensor."""
+    if inp.mode != "sample":
+        raise ValueError("redraw needs a sampled batch")
+    B, k, V = inp.B, inp.k, inp.V
+    s = np.random.SeedSequence(seed).spawn(3)
+    x = np.empty((reps, B, k), dtype=np.int32)
+    qrows = inp.q.reshape(B * k, V)
+    kids = s[0].spawn(B * k)
+
+    def fill(g, r0, r1):
+        for r in range(r0, r1):
+            p = qrows[r].astype(np.float64)
+            gr = np.random.default_rng(kids[r])
+            x[:, r // k, r % k] = gr.choice(V, size=reps, p=p / p.sum())
+
+    _chunked(B * k, s[1].spawn(1)[0], fill)
+    ua = np.random.default_rng(s[1]).random((reps, B, k), dtype=np.float32)
+    ur = np.random.default_rng(s[2]).random((reps, B), dtype=np.float32)
+    return Redraws(x, ua, ur)

@@ -11,7 +11,7 @@ import pytest
 import torch
 
 import oracle
-from parity import to_device
+from parity import Guarded, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -28,11 +28,13 @@ def run_match(inp, dev=None):
     from speculative_decoding_verification_18_gb300 import specverify as sv
     dev = dev or to_device(inp)
     B, k, V = inp.B, inp.k, inp.V
-    out = torch.full((B, k + 1), -7, dtype=torch.int32, device="cuda")
-    n = torch.full((B,), -7, dtype=torch.int32, device="cuda")
-    ws = sv.workspace(B, k, V, dev["logits"].dtype)
+    g = Guarded()
+    out = g.empty((B, k + 1), torch.int32, fill=-7)
+    n = g.empty((B,), torch.int32, fill=-7)
+    ws = g.workspace(B, k, V, dev["logits"].dtype)
     sv.spec_verify_match(dev["logits"], dev["x"], dev["ua"], dev["ur"], inp.T, out, n, ws)
     torch.cuda.synchronize()
+    g.check()
     st, bits, _ = sv.spec_verify_read_status(ws)
     return out.cpu().numpy(), n.cpu().numpy(), st, bits
 
@@ -146,11 +148,13 @@ def test_match_toy_acceptance_and_target_distribution():
         logits = torch.stack([lnP[c].expand(N, 4), lnP[x0.squeeze(1).long()]], dim=1).contiguous()
         ud = torch.rand((N, 1), device="cuda", generator=g)
         ub = torch.rand(N, device="cuda", generator=g)
-        out = torch.empty((N, 2), dtype=torch.int32, device="cuda")
-        n = torch.empty(N, dtype=torch.int32, device="cuda")
-        ws = sv.workspace(N, 1, 4, torch.float32)
+        gd = Guarded()
+        out = gd.empty((N, 2), torch.int32)
+        n = gd.empty(N, torch.int32)
+        ws = gd.workspace(N, 1, 4, torch.float32)
         sv.spec_verify_match(logits, x0.contiguous(), ud, ub, 1.0, out, n, ws)
         torch.cuda.synchronize()
+        gd.check()
         n = n.cpu().numpy()
         first = out[:, 0].cpu().numpy()
         beta = float((P[c] * Q[c]).sum())

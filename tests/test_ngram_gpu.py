@@ -9,6 +9,7 @@ import pytest
 import torch
 
 import oracle
+from parity import Guarded
 
 pytestmark = pytest.mark.gpu
 
@@ -26,10 +27,12 @@ def run_gpu_draft(hist, lengths, k, n_min, n_max):
     B = hist.shape[0]
     h = torch.from_numpy(np.ascontiguousarray(hist)).cuda()
     ln = torch.from_numpy(np.ascontiguousarray(lengths)).cuda()
-    d = torch.full((B, k), -7, dtype=torch.int32, device="cuda")
-    n = torch.full((B,), -7, dtype=torch.int32, device="cuda")
+    g = Guarded()
+    d = g.empty((B, k), torch.int32, fill=-7)
+    n = g.empty((B,), torch.int32, fill=-7)
     sv.spec_ngram_draft(h, ln, k, n_min, n_max, d, n)
     torch.cuda.synchronize()
+    g.check()
     return d.cpu().numpy(), n.cpu().numpy()
 
 

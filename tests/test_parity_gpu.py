@@ -12,7 +12,7 @@ import pytest
 import torch
 
 import oracle
-from parity import compare_outputs, compare_stats, run_gpu, run_oracle, to_device
+from parity import Guarded, compare_outputs, compare_stats, run_gpu, run_oracle, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -261,9 +261,10 @@ def test_graph_capture_replay():
     from speculative_decoding_verification_18_gb300 import specverify as sv
     inp = _gen(mode="sample", B=16, k=5, V=20000, dtype="bf16", T=0.8, kind="zipf", seed=8)
     dev = to_device(inp)
-    ws = sv.workspace(inp.B, inp.k, inp.V, torch.bfloat16)
-    out = torch.empty((inp.B, inp.k + 1), dtype=torch.int32, device="cuda")
-    n = torch.empty(inp.B, dtype=torch.int32, device="cuda")
+    gd = Guarded()
+    ws = gd.workspace(inp.B, inp.k, inp.V, torch.bfloat16)
+    out = gd.empty((inp.B, inp.k + 1), torch.int32)
+    n = gd.empty(inp.B, torch.int32)
     sv.spec_verify_sample(dev["logits"], dev["q"], dev["x"], dev["ua"], dev["ur"], inp.T, out, n,
                           ws)  # first call outside capture (device set-up)
     s = torch.cuda.Stream()
@@ -275,6 +276,7 @@ def test_graph_capture_replay():
     out.fill_(-9)
     g.replay()
     torch.cuda.synchronize()
+    gd.check()
     ref = run_oracle(inp)
     rep = compare_outputs(inp, out.cpu().numpy(), n.cpu().numpy(), ref)
     assert rep.hard == 0 and rep.near_threshold == 0

@@ -14,7 +14,7 @@ import torch
 import oracle
 from oracle import exact as oexact
 from conftest import read_golden
-from parity import run_gpu, to_device
+from parity import Guarded, run_gpu, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -68,11 +68,13 @@ def test_kv_and_stats_epilogue(mode, path):
         ref_out, ref_n, _, _ = run_gpu(inp, dev)
         B, k = inp.B, inp.k
         kv0 = torch.arange(100, 100 + B, dtype=torch.int32, device="cuda")
-        kv = kv0.clone()
-        stats = sv.stats_tensor()
-        out = torch.empty((B, k + 1), dtype=torch.int32, device="cuda")
-        n = torch.empty(B, dtype=torch.int32, device="cuda")
-        ws = sv.workspace(B, k, inp.V, dev["logits"].dtype)
+        gd = Guarded()
+        kv = gd.empty(B, torch.int32)
+        kv.copy_(kv0)
+        stats = gd.empty(len(sv.STATS_FIELDS), torch.int64, fill=0)
+        out = gd.empty((B, k + 1), torch.int32)
+        n = gd.empty(B, torch.int32)
+        ws = gd.workspace(B, k, inp.V, dev["logits"].dtype)
         if mode == "sample":
             sv.spec_verify_sample_kv(dev["logits"], dev["q"], dev["x"], dev["ua"], dev["ur"],
                                      inp.T, out, n, ws, kv_len=kv, stats=stats)
@@ -80,6 +82,7 @@ def test_kv_and_stats_epilogue(mode, path):
             sv.spec_verify_greedy_kv(dev["logits"], dev["x"], out, n, ws, kv_len=kv,
                                      stats=stats)
         torch.cuda.synchronize()
+        gd.check()
     finally:
         sv.debug_force_path(0)
     n = n.cpu().numpy()

@@ -13,6 +13,7 @@ import pytest
 import torch
 
 import oracle
+from parity import Guarded
 
 pytestmark = pytest.mark.gpu
 
@@ -40,13 +41,15 @@ def run_tree(t):
     ur = torch.from_numpy(t.ur).cuda() if sampled else None
     tok = torch.from_numpy(t.tok).cuda()
     par = torch.from_numpy(t.par).cuda()
-    out = torch.full((B, N), -7, dtype=torch.int32, device="cuda")
-    nodes = torch.full((B, N), -7, dtype=torch.int32, device="cuda")
-    n = torch.full((B,), -7, dtype=torch.int32, device="cuda")
-    ws = sv.workspace(B, N - 1, V, lg.dtype)
+    g = Guarded()
+    out = g.empty((B, N), torch.int32, fill=-7)
+    nodes = g.empty((B, N), torch.int32, fill=-7)
+    n = g.empty((B,), torch.int32, fill=-7)
+    ws = g.workspace(B, N - 1, V, lg.dtype)
     mode = sv.SV_MODE_SAMPLE if sampled else sv.SV_MODE_GREEDY
     sv.spec_verify_tree(mode, lg, q, tok, par, ua, ur, t.T, out, nodes, n, ws)
     torch.cuda.synchronize()
+    g.check()
     st, bits, _ = sv.spec_verify_read_status(ws)
     return out.cpu().numpy(), nodes.cpu().numpy(), n.cpu().numpy(), st, bits, ws
 
@@ -119,15 +122,16 @@ def test_chain_tree_equals_chain_verify(mode):
                       draft_sigma=0.4, seed=31)
     lg = torch.from_numpy(inp.logits.view(np.int16)).view(torch.bfloat16).cuda()
     x = torch.from_numpy(inp.x).cuda()
-    out_c = torch.empty((B, k + 1), dtype=torch.int32, device="cuda")
-    n_c = torch.empty(B, dtype=torch.int32, device="cuda")
-    ws = sv.workspace(B, k, V, lg.dtype)
+    g = Guarded()
+    out_c = g.empty((B, k + 1), torch.int32)
+    n_c = g.empty(B, torch.int32)
+    ws = g.workspace(B, k, V, lg.dtype)
     tok = torch.from_numpy(np.hstack([np.full((B, 1), -1, np.int32), inp.x])).cuda()
     par = torch.from_numpy(np.tile(np.r_[-1, np.arange(k)].astype(np.int32), (B, 1))).cuda()
-    out_t = torch.empty((B, k + 1), dtype=torch.int32, device="cuda")
-    nodes = torch.empty((B, k + 1), dtype=torch.int32, device="cuda")
-    n_t = torch.empty(B, dtype=torch.int32, device="cuda")
-    ws_t = sv.workspace(B, k, V, lg.dtype)
+    out_t = g.empty((B, k + 1), torch.int32)
+    nodes = g.empty((B, k + 1), torch.int32)
+    n_t = g.empty(B, torch.int32)
+    ws_t = g.workspace(B, k, V, lg.dtype)
     if mode == "greedy":
         sv.spec_verify_greedy(lg, x, out_c, n_c, ws)
         sv.spec_verify_tree(sv.SV_MODE_GREEDY, lg, None, tok, par, None, None, 1.0, out_t,
@@ -142,6 +146,7 @@ def test_chain_tree_equals_chain_verify(mode):
         sv.spec_verify_tree(sv.SV_MODE_SAMPLE, lg, qt, tok, par, uat, ur, inp.T, out_t, nodes,
                             n_t, ws_t)
     torch.cuda.synchronize()
+    g.check()
     a_o, a_n = out_c.cpu().numpy(), n_c.cpu().numpy()
     b_o, b_n = out_t.cpu().numpy(), n_t.cpu().numpy()
     same = (a_n == b_n) & (a_o == b_o).all(axis=1)
@@ -197,13 +202,15 @@ def test_tree_first_token_follows_p():
         tok[:, 0] = -1
         ua = torch.rand((M, N), device="cuda", generator=g)
         ur = torch.rand(M, device="cuda", generator=g)
-        out = torch.empty((M, N), dtype=torch.int32, device="cuda")
-        nodes = torch.empty((M, N), dtype=torch.int32, device="cuda")
-        n = torch.empty(M, dtype=torch.int32, device="cuda")
-        ws = sv.workspace(M, N - 1, V, torch.float32)
+        gd = Guarded()
+        out = gd.empty((M, N), torch.int32)
+        nodes = gd.empty((M, N), torch.int32)
+        n = gd.empty(M, torch.int32)
+        ws = gd.workspace(M, N - 1, V, torch.float32)
         sv.spec_verify_tree(sv.SV_MODE_SAMPLE, logits, q, tok.contiguous(), par, ua, ur, 1.0,
                             out, nodes, n, ws)
         torch.cuda.synchronize()
+        gd.check()
         first = out[:, 0].cpu().numpy()
         counts = np.bincount(first, minlength=4).astype(float)
         stat = float(((counts - M * P[c]) ** 2 / (M * P[c])).sum())
