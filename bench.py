@@ -629,6 +629,8 @@ def main():
 
     # ---- the oracle on the whole timed batch against the GPU's outputs (copy 0)
     parity = oracle_parity(inp, outs[0].cpu().numpy(), ns[0].cpu().numpy(), nt)
+    if inp.mode == "sample":  # draws of copy 0 that needed the float-float pass
+        parity["precise_draws"] = sv.debug_status_counts(ws[0])[5]
     accept = acceptance_report(inp, n_all)
 
     line = {

@@ -1,5 +1,6 @@
 /*
- * Test hooks of libspecverify (not part of the verify path).
+ * Test and tuning entry points of libspecverify (not part of the verify path):
+ * per-call options, introspection, and checks of the draw's arithmetic.
  */
 #ifndef SPECVERIFY_DEBUG_H
 #define SPECVERIFY_DEBUG_H
@@ -18,59 +19,91 @@ extern "C" {
 sv_status spec_verify_debug_ffexp(const float* l, float m, float T, int n, double* out,
                                   cudaStream_t stream);
 
-/* Route every sampled draw through the precise float-float pass (on != 0), or
- * back to the certified fast pass with fallback (on == 0, the default).  A
- * process-wide setting read at launch time, for tests only. */
-void spec_verify_debug_force_precise(int on);
+/* Options of one call, for tests and tuning.  Every field 0 means the
+ * automatic choice (what the entry points of specverify.h always use).  They
+ * apply to the one call they are passed to (the _tuned entry points below), so
+ * a test or a tuning script never changes the behaviour of another caller of
+ * the library.  A field outside its range makes the call return
+ * SV_ERR_INVALID_ARG.
+ *   path           1 the two-kernel path, 2 the fused per-sequence kernel, 3 the
+ *                  row-skipping path (0 automatic: the row-skipping path when B
+ *                  is at least the SM count, or in sampled mode half of it;
+ *                  else, in sampled mode, the fused kernel when rows are at most
+ *                  1 KiB or its clusters cover every SM; else the two-kernel
+ *                  path);
+ *   force_precise  1: every sampled draw takes the precise float-float pass;
+ *   draw_split     the sampled draw kernel's cluster size (1, 2, 4, 8, 16);
+ *   precise_split  the cluster size of the precise-draw kernel of large batches;
+ *   fused_defer    the fused kernel hands the draws that need the precise pass
+ *                  to a separate kernel: 1 always, 2 never (0: when B is at
+ *                  least the SM count);
+ *   fused_pad_kib  the fused kernel's minimum dynamic shared memory per CTA
+ *                  (KiB, up to 160), limiting how many share an SM;
+ *   rows_split     the two-kernel path's row stream: CTAs per row (1..16, a
+ *                  power of two);
+ *   rows_threads   its threads per CTA (128, 256, 512 or 1024);
+ *   flat_off       1: greedy batches never take the flat row stream (the whole
+ *                  logits tensor cut into one equal range per resident CTA);
+ *                  a fixed rows_split or rows_threads also keeps them off it. */
+typedef struct {
+    int path;
+    int force_precise;
+    int draw_split;
+    int precise_split;
+    int fused_defer;
+    int fused_pad_kib;
+    int rows_split;
+    int rows_threads;
+    int flat_off;
+} sv_tuning;
 
-/* Choose the path of spec_verify_greedy / spec_verify_sample: 0 automatic
- * (the default: the row-skipping path when B is at least the SM count, or in
- * sampled mode half of it; else, in sampled mode, the fused per-sequence kernel
- * when rows are at most 1 KiB or its clusters cover every SM; else the
- * two-kernel path), 1 always the two-kernel path, 2 always the
- * fused per-sequence kernel, 3 always the row-skipping path.  A process-wide
- * setting read at launch time, for tests. */
-void spec_verify_debug_force_path(int path);
+/* spec_verify_sample / spec_verify_sample_kv (kv_len and stats may be NULL),
+ * spec_verify_greedy / spec_verify_greedy_kv, spec_verify_rows,
+ * spec_verify_finish, spec_verify_tree and spec_verify_match with the options
+ * of `tuning` (NULL: the automatic choices).  Arguments, results and errors
+ * otherwise as for those calls. */
+sv_status spec_verify_sample_tuned(const void* logits, sv_dtype dtype, const float* draft_probs,
+                                   const int32_t* draft_tokens, const float* u_accept,
+                                   const float* u_resample, float T, int B, int k, int V,
+                                   int32_t* out_tokens, int32_t* num_accepted, void* ws,
+                                   size_t ws_bytes, int32_t* kv_len, sv_spec_stats* stats,
+                                   cudaStream_t stream, const sv_tuning* tuning);
+sv_status spec_verify_greedy_tuned(const void* logits, sv_dtype dtype,
+                                   const int32_t* draft_tokens, int B, int k, int V,
+                                   int32_t* out_tokens, int32_t* num_accepted, void* ws,
+                                   size_t ws_bytes, int32_t* kv_len, sv_spec_stats* stats,
+                                   cudaStream_t stream, const sv_tuning* tuning);
+sv_status spec_verify_rows_tuned(sv_mode mode, const void* logits, sv_dtype dtype,
+                                 const float* draft_probs, const int32_t* draft_tokens, float T,
+                                 int B, int k, int V, void* ws, size_t ws_bytes,
+                                 cudaStream_t stream, const sv_tuning* tuning);
+sv_status spec_verify_finish_tuned(sv_mode mode, const void* logits, sv_dtype dtype,
+                                   const float* draft_probs, const int32_t* draft_tokens,
+                                   const float* u_accept, const float* u_resample, float T,
+                                   int B, int k, int V, int32_t* out_tokens,
+                                   int32_t* num_accepted, void* ws, size_t ws_bytes,
+                                   cudaStream_t stream, const sv_tuning* tuning);
+sv_status spec_verify_tree_tuned(sv_mode mode, const void* logits, sv_dtype dtype,
+                                 const float* draft_probs, const int32_t* tree_tokens,
+                                 const int32_t* tree_parents, const float* u_accept,
+                                 const float* u_resample, float T, int B, int N, int V,
+                                 int32_t* out_tokens, int32_t* out_nodes, int32_t* num_accepted,
+                                 void* ws, size_t ws_bytes, cudaStream_t stream,
+                                 const sv_tuning* tuning);
+sv_status spec_verify_match_tuned(const void* logits, sv_dtype dtype, const int32_t* draft_tokens,
+                                  const float* u_draw, const float* u_bonus, float T, int B, int k,
+                                  int V, int32_t* out_tokens, int32_t* num_accepted, void* ws,
+                                  size_t ws_bytes, cudaStream_t stream, const sv_tuning* tuning);
 
-/* The path (1, 2 or 3 as above) the one-call entry points would take for these
- * sizes on the current device, -1 on error or bad sizes. */
+/* The path (1, 2 or 3 as above) the one-call entry points of specverify.h
+ * take for these sizes on the current device, -1 on error or bad sizes. */
 int spec_verify_debug_path(sv_mode mode, int B, int V, sv_dtype dtype);
 
 /* The number of CTAs of the flat greedy row stream that spec_verify_greedy (or
- * spec_verify_rows in greedy mode) would launch for these sizes on the current
- * device with 16-byte aligned logits; 0 when it would take the per-row stream;
+ * spec_verify_rows in greedy mode) launches for these sizes on the current
+ * device with 16-byte aligned logits; 0 when it takes the per-row stream;
  * -1 on error or bad sizes. */
 int spec_verify_debug_flat_ctas(int B, int k, int V, sv_dtype dtype);
-
-/* Fix the cluster size of the sampled draw kernel (spec_verify_finish and the
- * two-stage paths' second kernel) to G in {1, 2, 4, 8, 16}; 0 restores the
- * automatic choice; other values are ignored.  A process-wide setting read at
- * launch time, for tuning and tests. */
-void spec_verify_debug_draw_split(int G);
-
-/* Tuning of the fused per-sequence kernel: defer_mode 0 (default) hands the
- * draws that need the precise pass to a separate kernel when B is at least the
- * SM count, 1 always, 2 never; pad_kib > 0 gives every CTA at least that much
- * dynamic shared memory (KiB, up to 160), limiting how many share an SM.  Out
- * of range values are ignored.  A process-wide setting read at launch time. */
-void spec_verify_debug_fused_tuning(int defer_mode, int pad_kib);
-
-/* Fix the row stream's vocabulary split G (1, 2, 4, 8 or 16 CTAs per row) and
- * threads per CTA (128, 256 or 512) on the two-kernel path; 0 restores the
- * automatic choice of either; other values are ignored.  A process-wide setting
- * read at launch time, for tuning. */
-void spec_verify_debug_rows_split(int G, int nt);
-
-/* off = 1: greedy batches never take the flat row stream (the whole logits
- * tensor cut into one equal range per resident CTA, with per-row partial keys
- * merged by the finish kernel); they take the per-row stream instead.  0
- * restores the automatic choice.  A fixed split set with
- * spec_verify_debug_rows_split also turns the flat stream off.  For tests. */
-void spec_verify_debug_flat(int off);
-
-/* Fix the cluster size of the precise-draw kernel of large batches to G in
- * {1, 2, 4, 8, 16}; 0 restores the default.  For tuning. */
-void spec_verify_debug_precise_split(int G);
 
 /* The first stage of the row-skipping path alone: resets the per-sequence stop
  * rows in `ws` and runs the position-major row stream, leaving the row records
@@ -83,11 +116,17 @@ sv_status spec_verify_debug_rows_skip(sv_mode mode, const void* logits, sv_dtype
                                       const float* u_accept, float T, int B, int k, int V,
                                       void* ws, size_t ws_bytes, cudaStream_t stream);
 
+/* Synchronises `stream`; counts[i] receives the number of sequences of the
+ * last call on `ws` whose status word has bit i set (bit 5, SV_DEV_PRECISE:
+ * the draws that needed the float-float pass).  HOST array of 8. */
+sv_status spec_verify_debug_status_counts(const void* ws, cudaStream_t stream,
+                                          uint32_t counts[8]);
+
 /* Writes to *out (a DEVICE float) the largest relative error of the
  * ex2.approx.ftz.f32 instruction against the float-float 2^a over every float a
  * in [a0, a1], -126 <= a0 <= a1 <= 0.  The fast draw's error bound assumes this
- * is at most 2^-22 over [-126, 0] (a test checks it exhaustively).  Synchronises `stream`.  SV_ERR_INVALID_ARG for a bad range
- * or a null pointer. */
+ * is at most 1.75e-7 over [-126, 0] (a test checks it exhaustively).
+ * Synchronises `stream`.  SV_ERR_INVALID_ARG for a bad range or a null pointer. */
 sv_status spec_verify_debug_ex2_error(float a0, float a1, float* out, cudaStream_t stream);
 
 #ifdef __cplusplus

@@ -7,7 +7,8 @@ import subprocess
 HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 SRC = os.path.join(HERE, "csrc", "specverify.cu")
-DEPS = [SRC, os.path.join(HERE, "csrc", "ff.cuh"), os.path.join(ROOT, "include", "specverify.h")]
+DEPS = [SRC, os.path.join(HERE, "csrc", "ff.cuh"), os.path.join(ROOT, "include", "specverify.h"),
+        os.path.join(ROOT, "include", "specverify_debug.h")]
 LIB = os.path.join(HERE, "libspecverify.so")
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 

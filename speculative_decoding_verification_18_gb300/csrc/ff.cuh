@@ -185,6 +185,19 @@ __device__ __forceinline__ unsigned long long fix_mag(float x) {
     return ex == 0 ? 0ull : v;  // zero or subnormal: below the resolution
 }
 
+// floor(x 2^s) for a float x >= 0 with x 2^s < 2^64, from the float's bits by
+// integer shifts (a 64-bit float-to-integer conversion would run on the
+// FP64 pipe, which is narrow on this GPU); 0 for zero and subnormals.
+__device__ __forceinline__ unsigned long long fix_pow2(float x, int s) {
+    const uint32_t b = __float_as_uint(x);
+    const int ex = (int)(b >> 23);
+    const unsigned long long mant = (unsigned long long)((b & 0x7FFFFFu) | 0x800000u);
+    const int sh = ex - 150 + s;  // x 2^s = mant 2^sh
+    const unsigned long long left = mant << (sh > 0 ? sh : 0);
+    const unsigned long long right = mant >> (sh < 0 ? (sh > -63 ? -sh : 63) : 0);
+    return ex == 0 ? 0ull : (sh >= 0 ? left : right);
+}
+
 // Fixed-point value of a non-negative float-float (hi >= 0, |lo| <= ulp(hi)).
 __device__ __forceinline__ unsigned long long to_fixed(ff v) {
     unsigned long long h = fix_mag(v.hi);

@@ -50,6 +50,7 @@
 #include <new>
 
 #include "../../include/specverify.h"
+#include "../../include/specverify_debug.h"
 #include "ff.cuh"
 
 namespace cg = cooperative_groups;
@@ -315,22 +316,29 @@ constexpr int kSliceMax = 163840;   // largest slice of a row one CTA draws from
 // Error model of the fast fp32 draw.  ex2.approx.ftz.f32 is taken to be within
 // kEx2RelErr of 2^a (relative) on [-126, 0]: a test measures its worst case
 // exhaustively over every float of that range (on GB300: 1.715e-7, 2^-22.48)
-// and requires it to be at most this value.
-constexpr float kEx2RelErr = 2.38418579e-07f;  // 2^-22
-// Relative error bound of p = y/S per element, apart from the exponent term:
-// y = ex2(a) corrected for the exponent's product roundings (ex2 itself and the
-// correction's rounding); the normaliser's ex2 errors, corrections and the
-// three roundings deep pairwise sums of its chunks (the chunk sums are then
-// carried to 2^-47); the roundings of 1/S (two: the reciprocal and the dropped
-// low part) and of y * (1/S).
-constexpr float kFastE0 = 2.0f * kEx2RelErr + 7.0f * 5.96046448e-08f;
+// and requires it to be at most this value, so the bound holds for every input
+// the draw can see on this GPU (inputs below -126 give 0 and are counted as 0).
+constexpr float kEx2RelErr = 1.75e-7f;
+// Relative error of one element's corrected exponential y apart from the
+// rounding of its exponent: ex2 itself, and the two roundings of the
+// first-order correction (its product and its FMA).
+constexpr float kFastEy = kEx2RelErr + 2.0f * 5.96046448e-08f;
 // The exponent a = (l - m) * log2(e)/T: the product's rounding and that of
 // log2(e)/T are recovered exactly (an FMA and the low part of log2(e)/T) and
 // corrected for; the difference l - m keeps one rounding, 2^-24 * |a|, i.e. a
 // relative 2^-24 * ln2 * |a| in 2^a.
 constexpr float kFastKappa = 5.96046448e-08f * 0.693147181f;
-// Elements with p < q (1 - kRelSlack) for sure weigh exactly 0 in both passes.
-constexpr float kRelSlack = 4.0e-5f;
+// Classes of a residual's elements, decided during the one pass with the row
+// stream's normaliser S_row in place of the pass's own S (which is checked
+// afterwards to lie within 2^-13 of S_row): p > q for sure when
+// y / (S_row (1 + 2^-12)) > q, p < q for sure when y / (S_row (1 - 2^-12)) < q
+// (the margin exceeds 2^-13, the relative errors of y and of S, and the few
+// roundings of the scaled reciprocals and the product).  An element in between
+// is left out of the weights and its exact weight, at most kUndecided q
+// (2^-12 + 2^-13 + those errors, about 3.8e-4), goes into the error bound.
+constexpr float kClassHi = 1.0f + 1.0f / 4096.0f, kClassLo = 1.0f - 1.0f / 4096.0f;
+constexpr double kRowSigma = 1.0 / 8192.0;
+constexpr float kUndecided = 3.9e-4f;
 
 template <typename DT>
 __device__ __forceinline__ void load_chunk(const DT* __restrict__ rowp, long long j0, int V,
@@ -416,6 +424,13 @@ __device__ __forceinline__ unsigned long long scale_floor(float u, unsigned long
 // CTA computes the same totals, and no CTA touches another's shared memory
 // after the last barrier it passes.  Every slot array is written once per draw.
 constexpr int kMaxG = 16;
+// Per-thread sums of the fast pass.
+struct FastTotals {
+    ff S;                        // y of the elements that are not positive
+    unsigned long long Y, Q;     // fixed-point sums of the positive elements' y and q
+    float A, Aq;                 // y|a| of all elements; q of the undecided ones
+    float qmin;                  // the smallest q (negative: the precise pass decides)
+};
 struct DrawShared {
     ff red_ff[kWarps];
     float red_f[kWarps];
@@ -434,6 +449,14 @@ struct DrawShared {
     int blk;
     int cert, cert_all;
     int token;
+    // the fast pass
+    FastTotals red_t[kWarps];
+    FastTotals xT[kMaxG];             // each rank's sums
+    unsigned long long f_M, f_tau;    // floor(2^(123 - EY) / S), floor(u C_tot)
+    unsigned long long f_Y, f_Q;      // this rank's starting point (sums of the ranks before)
+    unsigned long long f_bY, f_bQ;    // the owner's block's starting point
+    float f_D, f_eS;                  // the error bound's parts (units of 2^-62)
+    int f_ok, f_owner;
 };
 
 __device__ const Exp2Table g_exp2_table = make_exp2_table();
@@ -442,26 +465,6 @@ __device__ const Exp2Table g_exp2_table = make_exp2_table();
 __device__ __forceinline__ void xsync(cg::cluster_group& cluster, int G) {
     if (G > 1) cluster.sync();
     else __syncthreads();
-}
-
-// Prefetches a CTA's slice (chunks [c0, c0 + mych) of a row) into L2 with bulk
-// prefetches of at most 32 KiB; the part before the first 16-byte boundary and
-// the ragged end are left to the ordinary loads.
-template <typename T>
-__device__ __forceinline__ void prefetch_slice_l2(const T* row, long long c0, int mych, int V) {
-    const long long j0 = c0 * kChunk;
-    const long long n = min((long long)mych * kChunk, (long long)V - j0);
-    if (n <= 0) return;
-    const char* p = reinterpret_cast<const char*>(row + j0);
-    long long bytes = n * (long long)sizeof(T);
-    const long long skip = (long long)((16 - (reinterpret_cast<uintptr_t>(p) & 15)) & 15);
-    p += skip;
-    bytes = (bytes - skip) & ~15ll;
-    for (long long off = 0; off < bytes; off += 32768) {
-        const uint32_t sz = (uint32_t)min(32768ll, bytes - off);
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p + off), "r"(sz)
-                     : "memory");
-    }
 }
 
 // Cluster sum of a float-float value (and, with `xa`, of one float into
@@ -578,9 +581,7 @@ struct DrawCtx {
     int mych, nblk;
     bool al_l, al_q;
     int rank, G;
-    bool prefetch;             // bulk-prefetch the slices into L2 first
-    unsigned long long* bsum;  // [nblk]
-    float* acache;             // [mych * 8] fast-pass exponents, or null
+    unsigned long long* bsum;  // block sums (the fast pass: Y then Q per 64 elements)
     ff* ecache;                // [mych * 8] precise exponentials, or null
     float* thi;                // [kExpTable] each; loaded by the precise pass
     float* tlo;
@@ -604,18 +605,6 @@ __device__ __forceinline__ void load_q(const DrawCtx<DT>& d, int ci, bool use, f
     }
 }
 
-__device__ __forceinline__ void store8(float* p, const float* v) {
-    float4* q = reinterpret_cast<float4*>(p);
-    q[0] = make_float4(v[0], v[1], v[2], v[3]);
-    q[1] = make_float4(v[4], v[5], v[6], v[7]);
-}
-__device__ __forceinline__ void load8(const float* p, float* v) {
-    const float4* q = reinterpret_cast<const float4*>(p);
-    const float4 x = q[0], y = q[1];
-    v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
-    v[4] = y.x; v[5] = y.y; v[6] = y.z; v[7] = y.w;
-}
-
 // Raw bits of one chunk, so that a thread can hold several chunks in flight in
 // few registers: 8 logits (one or two 16-byte vectors) or 8 q values.  Elements
 // past V read as -inf (logits) or 0 (q), the fill of the scalar loads.
@@ -630,7 +619,7 @@ __device__ __forceinline__ void raw_load_l(const DrawCtx<DT>& d, int ci, RawL<DT
     constexpr int NV = (int)(sizeof(RawL<DT>) / 16);
     if (d.al_l && j0 + kChunk <= d.V) {
 #pragma unroll
-        for (int w = 0; w < NV; ++w) r.v[w] = reinterpret_cast<const uint4*>(d.rowp + j0)[w];
+        for (int w = 0; w < NV; ++w) r.v[w] = ld_stream16(reinterpret_cast<const uint4*>(d.rowp + j0) + w);
     } else {
         float f[kChunk];
         load_chunk<DT>(d.rowp, j0, d.V, d.al_l, f);
@@ -661,8 +650,8 @@ template <typename DT>
 __device__ __forceinline__ void raw_load_q(const DrawCtx<DT>& d, int ci, RawQ& r) {
     const long long j0 = (d.c0 + ci) * kChunk;
     if (d.al_q && j0 + kChunk <= d.V) {
-        r.v[0] = reinterpret_cast<const uint4*>(d.qrow + j0)[0];
-        r.v[1] = reinterpret_cast<const uint4*>(d.qrow + j0)[1];
+        r.v[0] = ld_stream16(reinterpret_cast<const uint4*>(d.qrow + j0));
+        r.v[1] = ld_stream16(reinterpret_cast<const uint4*>(d.qrow + j0) + 1);
     } else {
         float f[kChunk];
         load_q_chunk(d.qrow, j0, d.V, d.al_q, f);
@@ -675,62 +664,6 @@ __device__ __forceinline__ void raw_load_q(const DrawCtx<DT>& d, int ci, RawQ& r
 __device__ __forceinline__ void raw_unpack_q(const RawQ& r, float* f) {
     Elt<float>::unpack(r.v[0], f);
     Elt<float>::unpack(r.v[1], f + 4);
-}
-
-// 2^((l - m) * log2(e)/T) for one chunk in fp32, formed the same way wherever
-// it is formed: a = fl(d * c_hi) with d = fl(l - m); the product's rounding
-// error (exact, by an FMA) plus d * c_lo corrects ex2(a) to first order.  Also
-// |a| for the error bound.  y = 0 for l = -inf (and below 2^-126, flushed).
-__device__ __forceinline__ void fast_y(const float* l, float m, float chi, float clo, float* y,
-                                       float* absa) {
-#pragma unroll
-    for (int e = 0; e < kChunk; ++e) {
-        const float d = __fsub_rn(l[e], m);
-        const float a = __fmul_rn(d, chi);
-        float err = __fmaf_rn(d, chi, -a);  // exact
-        err = __fmaf_rn(d, clo, err);
-        const float y0 = ex2_approx(a);
-        y[e] = y0 > 0.0f ? __fmaf_rn(y0, __fmul_rn(err, 0.693147181f), y0) : 0.0f;
-        absa[e] = fabsf(a);
-    }
-}
-
-// The corrected exponentials of chunk ci: from the cache when there is one,
-// else formed from the logits (identical values either way).
-template <typename DT>
-__device__ __forceinline__ void chunk_y(const DrawCtx<DT>& d, int ci, const float* l, float* y) {
-    if (d.acache) {
-        load8(d.acache + (size_t)ci * kChunk, y);
-    } else {
-        float unused[kChunk];
-        fast_y(l, d.m, d.c, d.clo, y, unused);
-    }
-}
-
-// Weights of one chunk in fp32 (p = y / S, or max(0, p - q) when RES), and the
-// sum of p over the elements the bound counts added to *relp.
-template <bool RES>
-__device__ __forceinline__ void fast_weights(const float* y, const float* q, float inv, float* w,
-                                             float* relp) {
-    float b = 0.0f;
-#pragma unroll
-    for (int e = 0; e < kChunk; ++e) {
-        const float p = __fmul_rn(y[e], inv);
-        w[e] = RES ? fmaxf(__fsub_rn(p, q[e]), 0.0f) : p;
-        const bool rel = !RES || p >= q[e] * (1.0f - kRelSlack);
-        b += rel ? p : 0.0f;
-    }
-    *relp += b;
-}
-
-// Fixed-point value of a chunk: its weights summed left to right in fp32, the
-// sum quantised.  The same partial sums quantised give the element-level
-// cumulative values, so the last of them equals the chunk value.
-__device__ __forceinline__ unsigned long long fast_chunk_value(const float* w) {
-    float cs = 0.0f;
-#pragma unroll
-    for (int e = 0; e < kChunk; ++e) cs = __fadd_rn(cs, w[e]);
-    return fix_mag(cs);
 }
 
 // Inside the CTA: the block holding `want` (0 <= want < the CTA's total) and
@@ -799,60 +732,285 @@ __device__ __forceinline__ bool find_lane(unsigned long long v, unsigned long lo
     return v > 0 && excl <= want && want - excl < v;
 }
 
-// ---- fast pass: fp32 exponentials, exact integer prefix sums, error bound
+// ---- fast pass: one read, fp32 exponentials, fixed-point sums, error bound
+//
+// One pass over the CTA's slice of the decision row (and of its q row) forms,
+// per element, y = 2^((l - m) log2(e)/T) in fp32 and decides whether p = y/S
+// exceeds q (the classes above).  The weight max(0, p - q) is then the linear
+// form p - q over the positive elements, so the cumulative weight up to any
+// point is Y/S - Q, Y and Q the sums of y and of q over the positive elements
+// before it.  Each lane sums the positive y and q of its chunk of 8 elements
+// and turns the two sums into fixed point (Y in units 2^-EY, Q in units 2^-62):
+// EXACT, in element order in float-float (error ~2^-44); otherwise pairwise in
+// fp32 (three roundings, counted in the error bound), which is about half the
+// work per element.  From there on everything is exact integer arithmetic:
+// the sums per block of 8 chunks (64 elements), per CTA and per cluster, and
+// the cumulative weight C = floor(Y M / 2^61) - Q (units 2^-62 of p) with
+// M = floor(2^(123 - EY) / S).  The normaliser S is Y plus the other elements'
+// y (summed pairwise per chunk, in float-float across chunks).  One cluster
+// exchange gives every CTA the totals and its starting point; the owning CTA
+// finds the block from its block sums in shared memory, and the block's 8
+// lanes the element, recomputing only those 64 elements with the pass's own
+// arithmetic, so that the lanes' and elements' boundaries inside the block
+// agree exactly with the block sums.  No step uses FP64 (slow on this GPU) or
+// 64-bit float-to-integer conversions.
+
+// The fixed-point scale 2^EY of y: EY = 61 - e with S_row < 2^e, so that Y stays
+// below 2^62 (S is within 2^-9 of S_row for any valid row).
+__device__ __forceinline__ int fast_ey(float s_row) {
+    int e = 0;
+    (void)frexpf(s_row, &e);
+    return max(0, min(61, 61 - e));
+}
+
+constexpr int kClsZero = 0, kClsPos = 1, kClsUndecided = 2;
+constexpr int kFastGroup = 8;  // lanes (chunks of 8 elements) per block of the fast pass
+
+struct FastScale {
+    float m, chi, clo;  // row max (raw logit); log2(e)/T in float-float
+    float ih, il;       // 1 / (S_row (1 + 2^-12)), 1 / (S_row (1 - 2^-12)) (residual draws)
+    int ey;             // EY
+};
+
+// One element of the fast pass: y (the exponent's product rounding and the low
+// part of log2(e)/T corrected to first order), y |a| for the error bound, and
+// the class.  Every float operation is explicitly rounded, so the pass and the
+// owner's search compute identical values.  l = -inf gives y = 0.  A NaN q is
+// undecided (its bound is NaN, so the draw goes to the precise pass, which
+// weighs it 0); a negative q is caught by the caller.
+template <bool RES>
+__device__ __forceinline__ int fast_elem(float l, float q, const FastScale& f, float& y,
+                                         float& ya) {
+    const float dd = __fsub_rn(l, f.m);
+    const float a = __fmul_rn(dd, f.chi);
+    float err = __fmaf_rn(dd, f.chi, -a);  // exact
+    err = __fmaf_rn(dd, f.clo, err);
+    const float y0 = ex2_approx(a);
+    y = y0 > 0.0f ? __fmaf_rn(y0, __fmul_rn(err, 0.693147181f), y0) : 0.0f;
+    ya = y > 0.0f ? __fmul_rn(y, fabsf(a)) : 0.0f;
+    if (!RES) return kClsPos;
+    if (__fmul_rn(y, f.ih) > q) return kClsPos;
+    if (__fmul_rn(y, f.il) < q) return kClsZero;
+    return kClsUndecided;
+}
+
+// acc += v in float-float (TwoSum into the high part, its error into lo).
+__device__ __forceinline__ void ff_acc1(ff& acc, float v) {
+    const ff s = two_sum(acc.hi, v);
+    acc.hi = s.hi;
+    acc.lo = __fadd_rn(acc.lo, s.lo);
+}
+
+// Pairwise sum of 8 floats (three rounding levels).
+__device__ __forceinline__ float sum8(const float* v) {
+    return __fadd_rn(__fadd_rn(__fadd_rn(v[0], v[1]), __fadd_rn(v[2], v[3])),
+                     __fadd_rn(__fadd_rn(v[4], v[5]), __fadd_rn(v[6], v[7])));
+}
+
+// The pairwise prefix of 8 floats up to element e (the nodes of sum8's tree
+// left of e, then e's own partial nodes): monotone in e, and for e = 7 equal to
+// sum8 exactly.
+__device__ __forceinline__ float prefix8(const float* v, int e) {
+    const float n01 = __fadd_rn(v[0], v[1]), n45 = __fadd_rn(v[4], v[5]);
+    const float n03 = __fadd_rn(n01, __fadd_rn(v[2], v[3]));
+    float left, part;
+    if (e < 4) {
+        left = 0.0f;
+        part = e == 0 ? v[0] : e == 1 ? n01 : e == 2 ? __fadd_rn(n01, v[2]) : n03;
+        return part;
+    }
+    left = n03;
+    part = e == 4 ? v[4] : e == 5 ? n45 : e == 6 ? __fadd_rn(n45, v[6])
+                                               : __fadd_rn(n45, __fadd_rn(v[6], v[7]));
+    return __fadd_rn(left, part);
+}
+
+// The fixed-point value of a non-negative float-float v = hi + lo (|lo| small):
+// floor(hi 2^s) plus or minus floor(|lo| 2^s).
+__device__ __forceinline__ unsigned long long ff_fixed(ff v, int s) {
+    const unsigned long long h = fix_pow2(v.hi, s);
+    const unsigned long long l = fix_pow2(fabsf(v.lo), s);
+    return v.lo < 0.0f ? h - l : h + l;
+}
+
+// Pairwise tree of 8 values fed in index order: ((v0+v1)+(v2+v3)) + ((v4+v5)+(v6+v7)),
+// folded as the values arrive (sum8's order, few live registers).
+struct Tree8 {
+    float a, p, h;  // the pending value, the pending pair, the first half
+    template <int E>
+    __device__ __forceinline__ void add(float v) {
+        if (E % 2 == 0) {
+            a = v;
+        } else if (E == 1 || E == 5) {
+            p = __fadd_rn(a, v);
+        } else if (E == 3) {
+            h = __fadd_rn(p, __fadd_rn(a, v));
+        } else {  // E == 7
+            h = __fadd_rn(h, __fadd_rn(p, __fadd_rn(a, v)));
+        }
+    }
+};
+
+template <int E, bool RES, bool EXACT, bool WANT>
+__device__ __forceinline__ void fast_chunk_elem(const float* l, const float* q, const FastScale& f,
+                                                ff& Y, ff& Q, Tree8& ty, Tree8& tq, Tree8& tr,
+                                                float& a, float& aq, float& qmin, float* yp,
+                                                float* qp) {
+    float y, ya;
+    const int cls = fast_elem<RES>(l[E], RES ? q[E] : 0.0f, f, y, ya);
+    const bool pos = cls == kClsPos;
+    const float yv = pos ? y : 0.0f, qv = (RES && pos) ? q[E] : 0.0f;
+    if (WANT) {
+        yp[E] = yv;
+        qp[E] = qv;
+    }
+    if (EXACT) {
+        ff_acc1(Y, yv);
+        if (RES) ff_acc1(Q, qv);
+    } else {
+        ty.add<E>(yv);
+        if (RES) tq.add<E>(qv);
+    }
+    tr.add<E>(pos ? 0.0f : y);
+    a = __fadd_rn(a, ya);
+    if (RES) {
+        aq = __fadd_rn(aq, cls == kClsUndecided ? q[E] : 0.0f);
+        qmin = fminf(qmin, q[E]);
+    }
+}
+
+// One chunk (8 elements, logits l and q): the fixed-point sums of the positive
+// elements' y and q (cy, cq), the other elements' y summed pairwise (returned),
+// the bound's sums into a and aq, the smallest q into qmin; with WANT, yp and
+// qp receive each element's y and q when it is positive, else 0.
+template <bool RES, bool EXACT, bool WANT>
+__device__ __forceinline__ float fast_chunk(const float* l, const float* q, const FastScale& f,
+                                            unsigned long long& cy, unsigned long long& cq,
+                                            float& a, float& aq, float& qmin, float* yp,
+                                            float* qp) {
+    ff Y{0.0f, 0.0f}, Q{0.0f, 0.0f};
+    Tree8 ty{}, tq{}, tr{};
+    fast_chunk_elem<0, RES, EXACT, WANT>(l, q, f, Y, Q, ty, tq, tr, a, aq, qmin, yp, qp);
+    fast_chunk_elem<1, RES, EXACT, WANT>(l, q, f, Y, Q, ty, tq, tr, a, aq, qmin, yp, qp);
+    fast_chunk_elem<2, RES, EXACT, WANT>(l, q, f, Y, Q, ty, tq, tr, a, aq, qmin, yp, qp);
+    fast_chunk_elem<3, RES, EXACT, WANT>(l, q, f, Y, Q, ty, tq, tr, a, aq, qmin, yp, qp);
+    fast_chunk_elem<4, RES, EXACT, WANT>(l, q, f, Y, Q, ty, tq, tr, a, aq, qmin, yp, qp);
+    fast_chunk_elem<5, RES, EXACT, WANT>(l, q, f, Y, Q, ty, tq, tr, a, aq, qmin, yp, qp);
+    fast_chunk_elem<6, RES, EXACT, WANT>(l, q, f, Y, Q, ty, tq, tr, a, aq, qmin, yp, qp);
+    fast_chunk_elem<7, RES, EXACT, WANT>(l, q, f, Y, Q, ty, tq, tr, a, aq, qmin, yp, qp);
+    if (EXACT) {
+        cy = ff_fixed(ff_normalize(Y), f.ey);
+        cq = RES ? ff_fixed(ff_normalize(Q), 62) : 0ull;
+    } else {
+        cy = fix_pow2(ty.h, f.ey);
+        cq = RES ? fix_pow2(tq.h, 62) : 0ull;
+    }
+    return tr.h;
+}
+
+// The fixed-point sums of the first e + 1 elements of a chunk, in the
+// arithmetic of fast_chunk (for e = 7 its cy and cq exactly).
+template <bool RES, bool EXACT>
+__device__ __forceinline__ void fast_prefix(const float* yp, const float* qp, int e,
+                                            const FastScale& f, unsigned long long& py,
+                                            unsigned long long& pq) {
+    if (EXACT) {
+        ff Y{0.0f, 0.0f}, Q{0.0f, 0.0f};
+#pragma unroll
+        for (int j = 0; j < kChunk; ++j) {
+            if (j > e) break;
+            ff_acc1(Y, yp[j]);
+            if (RES) ff_acc1(Q, qp[j]);
+        }
+        py = ff_fixed(ff_normalize(Y), f.ey);
+        pq = RES ? ff_fixed(ff_normalize(Q), 62) : 0ull;
+    } else {
+        py = fix_pow2(prefix8(yp, e), f.ey);
+        pq = RES ? fix_pow2(prefix8(qp, e), 62) : 0ull;
+    }
+}
+
+// A 64-bit unsigned integer as float-float (each 32-bit half converted; the
+// low half's rounding is 2^-24 of it).
+__device__ __forceinline__ ff u64_to_ff(unsigned long long v) {
+    const float hi = __fmul_rn(__uint2float_rn((uint32_t)(v >> 32)), 4294967296.0f);
+    const float lo = __uint2float_rn((uint32_t)v);
+    return ff_normalize(two_sum(hi, lo));
+}
+
+__device__ __forceinline__ FastTotals warp_fast_totals(FastTotals t) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const ff so{__shfl_xor_sync(0xffffffffu, t.S.hi, off),
+                    __shfl_xor_sync(0xffffffffu, t.S.lo, off)};
+        t.S = ff_add(t.S, so);
+        t.Y += __shfl_xor_sync(0xffffffffu, t.Y, off);
+        t.Q += __shfl_xor_sync(0xffffffffu, t.Q, off);
+        t.A += __shfl_xor_sync(0xffffffffu, t.A, off);
+        t.Aq += __shfl_xor_sync(0xffffffffu, t.Aq, off);
+        t.qmin = fminf(t.qmin, __shfl_xor_sync(0xffffffffu, t.qmin, off));
+    }
+    return t;
+}
+
+// C = floor(Y M / 2^61) - Q (Y M < 2^125 for Y within S 2^EY).
+__device__ __forceinline__ long long fast_cval(unsigned long long Y, unsigned long long Q,
+                                               unsigned long long M) {
+    const unsigned long long lo = Y * M, hi = __umul64hi(Y, M);
+    return (long long)((hi << 3) | (lo >> 61)) - (long long)Q;
+}
+
+// The sum of v over lanes [g*8, g*8 + 8) of the warp (every lane of the group
+// ends with it).
+__device__ __forceinline__ unsigned long long group_sum_u64(unsigned long long v) {
+#pragma unroll
+    for (int off = 1; off < kFastGroup; off <<= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    return v;
+}
 
 // The fast draw by the G CTAs of a cluster (RES: the residual max(0, p - q),
 // else p).  Returns true (in every thread of every CTA) when the token is
-// certified: u * C lies farther than twice the accumulated error bound from
-// both edges of the chosen bin, so the exact draw picks the same bin.  The owner
-// CTA then holds the token in sh.token.
-template <typename DT, bool RES>
+// certified: u C lies far enough inside the chosen bin that the exact draw
+// picks the same one.  The owner CTA then holds the token in sh.token.
+//
+// Error bound.  Each positive element's p_fast = y/S carries its own error
+// e_j <= kFastEy + kappa |a_j| and the normaliser's e_S (kFastEy + kappa A,
+// A = sum p|a|, and the roundings of its pairwise chunk sums); p_fast =
+// p (1 + eta_j) / (1 + eta_S).  The error of u C_tot - C at a bin edge is,
+// element by element, (u - 1) times the errors before the edge plus u times
+// those after it, so the elements' own errors, the undecided elements' weights
+// (at most kUndecided q) and, without EXACT, the chunk sums' three roundings
+// contribute at most max(u, 1 - u) times their sum; the normaliser's common
+// factor contributes eta_S (u P_tot - P_edge) = eta_S (u Q_tot - Q_edge +
+// (u C_tot - C_edge)), at most e_S (max(u, 1 - u) Q_tot + the bin's width).
+// The float-float sums (2^-44), M (2^-44) and the fixed-point truncations add
+// at most 2^20 + 2 (chunks) + 64 units.  The token is kept when u C lies more
+// than this bound (plus 2 units) inside both edges of its bin.
+template <typename DT, bool RES, bool EXACT>
 __device__ bool draw_fast(cg::cluster_group& cluster, DrawShared& sh, const DrawCtx<DT>& d) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int grp = lane / kFastGroup, gl = lane % kFastGroup;
     if (tid == 0) {
         sh.token = -1;
         sh.cert = 0;
     }
+    FastScale f;
+    f.m = d.m;
+    f.chi = d.c;
+    f.clo = d.clo;
+    f.ih = RES ? __frcp_rn(__fmul_rn(d.s_row, kClassHi)) : 0.0f;
+    f.il = RES ? __frcp_rn(__fmul_rn(d.s_row, kClassLo)) : 0.0f;
+    f.ey = fast_ey(d.s_row);
+    const int fnb = (d.mych + kFastGroup - 1) / kFastGroup;  // blocks of this CTA's slice
+    unsigned long long* Yb = d.bsum;
+    unsigned long long* Qb = d.bsum + fnb;
 
-    // Pass A: S = sum_j ex2(a_j); each chunk summed pairwise in fp32 (3 roundings
-    // deep), the chunk sums accumulated in float-float.  Also A = sum_j ex2(a_j)|a_j|
-    // for the argument-rounding part of S's error.
-    ff accS{0.0f, 0.0f};
-    float accA = 0.0f;
-    // UA chunks per thread in flight (16 registers of raw logits).
-    constexpr int UA = sizeof(DT) == 2 ? 4 : 2;
-    for (int base = tid; base < d.mych; base += UA * kThreads) {
-        RawL<DT> raw[UA];
-#pragma unroll
-        for (int u = 0; u < UA; ++u)
-            if (base + u * kThreads < d.mych) raw_load_l(d, base + u * kThreads, raw[u]);
-#pragma unroll
-        for (int u = 0; u < UA; ++u) {
-            const int ci = base + u * kThreads;
-            if (ci >= d.mych) break;
-            float l[kChunk], y[kChunk], absa[kChunk];
-            raw_unpack(raw[u], l);
-            fast_y(l, d.m, d.c, d.clo, y, absa);
-            if (d.acache) store8(d.acache + (size_t)ci * kChunk, y);
-#pragma unroll
-            for (int e = 0; e < kChunk; ++e) accA = fmaf(y[e], absa[e], accA);
-            const float s = __fadd_rn(__fadd_rn(__fadd_rn(y[0], y[1]), __fadd_rn(y[2], y[3])),
-                                      __fadd_rn(__fadd_rn(y[4], y[5]), __fadd_rn(y[6], y[7])));
-            const ff t = two_sum(accS.hi, s);
-            accS.hi = t.hi;
-            accS.lo = __fadd_rn(accS.lo, t.lo);
-        }
-    }
-    const ff S = cluster_sum_ff(cluster, sh, sh.xS[0], accS, d.rank, d.G, sh.xA, accA);
-    const float inv = __frcp_rn(S.hi);
-
-    // Pass B: fixed-point chunk values, block totals, the mass the bound counts.
-    unsigned long long tacc = 0;
-    float relp = 0.0f;
-    // Two blocks per warp in flight: the q chunks, and the logits when they
-    // are not cached.
+    // The pass: each warp takes 32 consecutive chunks (a chunk per lane, four
+    // blocks), two such rounds in flight.
+    constexpr FastTotals kZeroT{ff{0.0f, 0.0f}, 0ull, 0ull, 0.0f, 0.0f, 0.0f};
+    FastTotals t = kZeroT;
     constexpr int UB = 2;
-    for (int base0 = warp * kBlockChunks; base0 < d.mych; base0 += UB * kThreads) {
+    for (int base0 = warp * 32; base0 < d.mych; base0 += UB * kThreads) {
         RawQ rq[UB];
         RawL<DT> rl[UB];
 #pragma unroll
@@ -860,146 +1018,241 @@ __device__ bool draw_fast(cg::cluster_group& cluster, DrawShared& sh, const Draw
             const int ci = base0 + u * kThreads + lane;
             if (ci < d.mych) {
                 if (RES) raw_load_q(d, ci, rq[u]);
-                if (!d.acache) raw_load_l(d, ci, rl[u]);
+                raw_load_l(d, ci, rl[u]);
             }
         }
 #pragma unroll
         for (int u = 0; u < UB; ++u) {
             const int base = base0 + u * kThreads;
             if (base >= d.mych) break;  // uniform across the warp
-            const int ci = base + lane;
-            unsigned long long W = 0;
-            if (ci < d.mych) {
-                float q[kChunk] = {}, l[kChunk] = {}, y[kChunk], w[kChunk];
+            unsigned long long cy = 0ull, cq = 0ull;
+            if (base + lane < d.mych) {
+                float l[kChunk], q[kChunk] = {};
+                raw_unpack(rl[u], l);
                 if (RES) raw_unpack_q(rq[u], q);
-                if (!d.acache) raw_unpack(rl[u], l);
-                chunk_y(d, ci, l, y);
-                fast_weights<RES>(y, q, inv, w, &relp);
-                W = fast_chunk_value(w);
-                // the cache now keeps the weights, for the owner's search
-                if (d.acache) store8(d.acache + (size_t)ci * kChunk, w);
+                const float rest = fast_chunk<RES, EXACT, false>(l, q, f, cy, cq, t.A, t.Aq,
+                                                                 t.qmin, nullptr, nullptr);
+                ff_acc1(t.S, rest);
             }
-            const unsigned long long bw = warp_sum(W);
-            if (lane == 0) {
-                d.bsum[base / kBlockChunks] = bw;
-                tacc += bw;
+            t.Y += cy;
+            t.Q += cq;
+            const unsigned long long by = group_sum_u64(cy);
+            const unsigned long long bq = RES ? group_sum_u64(cq) : 0ull;
+            const int blk = (base + grp * kFastGroup) / kFastGroup;
+            if (gl == 0 && blk < fnb) {
+                Yb[blk] = by;
+                Qb[blk] = bq;
             }
         }
     }
-    cluster_prefix(cluster, sh, sh.xW[0], sh.xD, tacc, relp, d.rank, d.G);
-    const unsigned long long prefix = sh.prefix, total = sh.total, mytot = sh.mytot;
-    // Bound in fixed-point units: kFastE0 times the mass of the counted
-    // elements (sum of p with p >= q (1 - kRelSlack), or all of p); the
-    // exponents' roundings, kappa * sum_j p_j |a_j| over every element, once for
-    // the elements' own exponents and once (times the counted mass, at most
-    // about 1) for those inside S; margins for their own fp32 sums; the
-    // roundings of p - q and of the sequential chunk sums (8 units of 2^-24 of
-    // the total); one unit of truncation per chunk value plus two for the bin
-    // edges.
-    const long long nch = ((long long)d.V + kChunk - 1) / kChunk;
-    const float kpa = kFastKappa * sh.A_tot * inv * 1.0009765625f;  // kappa * sum p |a|
-    float dunits = (kFastE0 * sh.D_tot + 2.0f * kpa) * 1.0009765625f * 1.152921504606847e18f +
-                   (float)total * (8.0f * 5.96046448e-08f) + (float)nch + 4.0f;
-    dunits = fminf(dunits, 1.0e18f);  // beyond any total: certifies nothing
-    const unsigned long long D = (unsigned long long)dunits + 1ull;
+    // The CTA's totals, pushed to slot [rank] of every CTA of the cluster.
+    t = warp_fast_totals(t);
+    if (lane == 0) sh.red_t[warp] = t;
+    __syncthreads();
+    if (warp == 0) {
+        FastTotals c = lane < kWarps ? sh.red_t[lane] : kZeroT;
+        c = warp_fast_totals(c);
+        if (lane < d.G) *cluster.map_shared_rank(&sh.xT[d.rank], lane) = c;
+    }
+    xsync(cluster, d.G);
 
-    const unsigned long long tau = scale_floor(d.u, total);
-    const bool owner = total > 0 && mytot > 0 && prefix <= tau && tau - prefix < mytot;
-    int cert = 1;
-    if (owner) {  // uniform across the CTA
-        const unsigned long long want = tau - prefix;
-        int blk;
-        unsigned long long bbefore;
-        find_block(sh, d.bsum, d.nblk, want, &blk, &bbefore);
-        if (warp == 0) {
-            const int ci = blk * kBlockChunks + lane;
-            float w[kChunk] = {};
-            unsigned long long W = 0;
-            // this chunk's counted mass and sum of y |a| (for its own bound)
-            float relc = 0.0f, ac = 0.0f;
-            if (ci < d.mych) {
-                if (d.acache) {
-                    load8(d.acache + (size_t)ci * kChunk, w);
-                } else {
-                    float l[kChunk], q[kChunk], y[kChunk], absa[kChunk];
-                    load_l(d, ci, l);
-                    load_q(d, ci, RES, q);
-                    fast_y(l, d.m, d.c, d.clo, y, absa);
-                    fast_weights<RES>(y, q, inv, w, &relc);
-#pragma unroll
-                    for (int e = 0; e < kChunk; ++e) ac = fmaf(y[e], absa[e], ac);
-                }
-                W = fast_chunk_value(w);
+    // Every CTA, from the same slots in the same order: the totals, the check
+    // of S against S_row, M, C_tot, u C_tot, the owning rank and this rank's
+    // starting point.  Float, float-float and integer arithmetic only.
+    if (warp == 0) {
+        // Every lane adds the G slots in rank order (no shuffles: a lone warp's
+        // shuffles right after the barrier measured several microseconds here).
+        FastTotals tot = kZeroT;
+        unsigned long long ybef = 0ull, qbef = 0ull, yend = 0ull, qend = 0ull;
+        for (int r = 0; r < d.G; ++r) {
+            const FastTotals x = sh.xT[r];
+            if (r == d.rank) {
+                ybef = tot.Y;
+                qbef = tot.Q;
             }
-            const unsigned long long wb = want - bbefore;
-            unsigned long long cb;
-            if (find_lane(W, wb, &cb)) {
-                const unsigned long long wc = wb - cb;  // `want` inside the chunk
-                float cs = 0.0f;
+            tot.S = ff_add(tot.S, x.S);
+            tot.Y += x.Y;
+            tot.Q += x.Q;
+            tot.A += x.A;
+            tot.Aq += x.Aq;
+            tot.qmin = fminf(tot.qmin, x.qmin);
+            if (r == lane) {  // lane r: the sums up to and including rank r
+                yend = tot.Y;
+                qend = tot.Q;
+            }
+        }
+        const unsigned long long Yall = tot.Y, Qall = tot.Q;
+        // S = Yall 2^-EY + the other elements' sum
+        const float pw = __int_as_float((127 - f.ey) << 23);  // 2^-EY
+        const ff Yf = u64_to_ff(Yall);
+        const ff S = ff_normalize(ff_add(ff{__fmul_rn(Yf.hi, pw), __fmul_rn(Yf.lo, pw)}, tot.S));
+        bool ok = tot.qmin >= 0.0f && S.hi > 0.0f &&
+                  fabsf(__fsub_rn(S.hi, d.s_row)) <= S.hi * (float)kRowSigma;
+        // M = floor(2^(123 - EY) / S): below 2^63 once S is within 2^-13 of S_row
+        const unsigned long long M = ok ? ff_fixed(ff_recip(S), 123 - f.ey) : 0ull;
+        const long long Ctot = ok ? fast_cval(Yall, Qall, M) : 0ll;
+        ok = ok && Ctot > 0;
+        const unsigned long long tau = ok ? scale_floor(d.u, (unsigned long long)Ctot) : 0ull;
+        const bool past = lane < d.G && ok && fast_cval(yend, qend, M) > (long long)tau;
+        const unsigned ballot = __ballot_sync(0xffffffffu, past);
+        const int owner = ballot ? __ffs(ballot) - 1 : -1;
+        if (lane == 0) {
+            sh.f_ok = ok && owner >= 0;
+            sh.f_owner = owner;
+            sh.f_M = M;
+            sh.f_tau = tau;
+            sh.f_Y = ybef;
+            sh.f_Q = qbef;
+            // The bound's parts (fractions of the total mass of p; float sums of
+            // positive terms, inflated for their own roundings; the positive
+            // elements' share of sum p|a| is bounded by all of it).
+            constexpr float u24 = 5.96046448e-08f;
+            const float invS = __frcp_rn(S.hi);
+            const float Ppos = __fmul_rn(__fmul_rn(Yf.hi, pw), invS);
+            const float Qpos = __fmul_rn(u64_to_ff(Qall).hi, 2.16840434e-19f);  // 2^-62
+            const float eS = kFastEy + kFastKappa * (tot.A * invS) * 1.001f +
+                             3.0f * u24 * (EXACT ? fmaxf(0.0f, 1.0f - Ppos) : 1.0f);
+            sh.f_eS = eS;
+            sh.f_D = (kFastEy * Ppos + kFastKappa * (tot.A * invS) * 1.001f + eS * Qpos +
+                      kUndecided * tot.Aq + (EXACT ? 0.0f : 3.0f * u24 * (Ppos + Qpos))) *
+                         1.004f * 4.611686018427388e18f +
+                     1048576.0f + 2.0f * (float)d.mych * (float)d.G + 64.0f;
+        }
+    }
+    __syncthreads();
+    if (!sh.f_ok) return false;  // uniform across the cluster
+    const unsigned long long M = sh.f_M, tau = sh.f_tau;
+
+    int cert = 1;
+    if (d.rank == sh.f_owner) {  // uniform across the CTA
+        // The block: each thread sums a contiguous range of block sums; a block
+        // scan of (Y, Q) gives each range's start; the first range whose end
+        // passes tau holds the block.
+        const int L = (fnb + kThreads - 1) / kThreads;
+        const int cb = min(fnb, tid * L), ce = min(fnb, cb + L);
+        unsigned long long my = 0ull, mq = 0ull;
+        for (int i = cb; i < ce; ++i) {
+            my += Yb[i];
+            mq += Qb[i];
+        }
+        unsigned long long iy = my, iq = mq;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const unsigned long long yo = __shfl_up_sync(0xffffffffu, iy, off);
+            const unsigned long long qo = __shfl_up_sync(0xffffffffu, iq, off);
+            if (lane >= off) {
+                iy += yo;
+                iq += qo;
+            }
+        }
+        if (lane == 31) {
+            sh.red_u[warp] = iy;
+            sh.woff[warp] = iq;
+        }
+        __syncthreads();
+        unsigned long long wy = 0ull, wq = 0ull;  // totals of the warps before this one
+        for (int w = 0; w < warp; ++w) {
+            wy += sh.red_u[w];
+            wq += sh.woff[w];
+        }
+        const unsigned long long sy0 = sh.f_Y + wy + iy - my, sq0 = sh.f_Q + wq + iq - mq;
+        const bool past = ce > cb && fast_cval(sy0 + my, sq0 + mq, M) > (long long)tau;
+        const unsigned bw = __ballot_sync(0xffffffffu, past);
+        if (lane == 0) sh.red_f[warp] = bw ? (float)(__ffs(bw) - 1) : -1.0f;
+        __syncthreads();
+        int first = -1;  // the first thread (by index) whose range passes tau
+        for (int w = 0; w < kWarps && first < 0; ++w)
+            if (sh.red_f[w] >= 0.0f) first = w * 32 + (int)sh.red_f[w];
+        if (tid == first) {
+            unsigned long long ry = sy0, rq = sq0;
+            int i = cb;
+            for (; i < ce - 1; ++i) {
+                if (fast_cval(ry + Yb[i], rq + Qb[i], M) > (long long)tau) break;
+                ry += Yb[i];
+                rq += Qb[i];
+            }
+            sh.blk = i;
+            sh.f_bY = ry;
+            sh.f_bQ = rq;
+        }
+        __syncthreads();
+        if (first < 0) {
+            cert = 0;  // not reachable: the owner's end passes tau
+        } else if (warp == 0) {
+            // The element: lanes 0..7 take the block's chunks in the pass's
+            // arithmetic (the same fixed-point values as the block sums); the
+            // first lane whose end passes tau walks its elements.
+            const int ci = sh.blk * kFastGroup + lane;
+            float l[kChunk], q[kChunk] = {}, yp[kChunk] = {}, qp[kChunk] = {};
+            unsigned long long cy = 0ull, cq = 0ull;
+            if (lane < kFastGroup && ci < d.mych) {
+                RawL<DT> rl;
+                raw_load_l(d, ci, rl);
+                raw_unpack(rl, l);
+                if (RES) {
+                    RawQ rq;
+                    raw_load_q(d, ci, rq);
+                    raw_unpack_q(rq, q);
+                }
+                float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f;
+                (void)fast_chunk<RES, EXACT, true>(l, q, f, cy, cq, a0, a1, a2, yp, qp);
+            }
+            unsigned long long iy2 = cy, iq2 = cq;
+#pragma unroll
+            for (int off = 1; off < kFastGroup; off <<= 1) {
+                const unsigned long long yo = __shfl_up_sync(0xffffffffu, iy2, off);
+                const unsigned long long qo = __shfl_up_sync(0xffffffffu, iq2, off);
+                if (lane >= off) {
+                    iy2 += yo;
+                    iq2 += qo;
+                }
+            }
+            const unsigned long long ly = sh.f_bY + iy2 - cy, lq = sh.f_bQ + iq2 - cq;
+            const bool lp = lane < kFastGroup && ci < d.mych &&
+                            fast_cval(ly + cy, lq + cq, M) > (long long)tau;
+            const unsigned bl = __ballot_sync(0xffffffffu, lp);
+            if (bl && lane == __ffs(bl) - 1) {
+                long long lo = fast_cval(ly, lq, M), hi = lo;
                 int tok = -1;
-                unsigned long long lo = 0, hi = 0;
 #pragma unroll
                 for (int e = 0; e < kChunk; ++e) {
-                    const float prev = cs;
-                    cs = __fadd_rn(cs, w[e]);
-                    const unsigned long long h = fix_mag(cs);
-                    if (tok < 0 && h > wc) {
+                    if (tok >= 0 || !(yp[e] > 0.0f)) continue;  // weight 0: never chosen
+                    unsigned long long py, pq;
+                    fast_prefix<RES, EXACT>(yp, qp, e, f, py, pq);
+                    const long long h = fast_cval(ly + py, lq + pq, M);
+                    if (h > (long long)tau) {
                         tok = e;
-                        lo = fix_mag(prev);
                         hi = h;
+                    } else {
+                        lo = h;
                     }
                 }
-                // Bin edges relative to `want`: want - lo >= 2D and hi - want >
-                // 2D + 1 certify the bin (the edge and u times the total each
-                // within D).  Failing that, a finer certificate: the edge's and
-                // u times the total's errors sum, element by element, to (u - 1)
-                // times the errors before the edge plus u times those after it,
-                // at most max(u, 1 - u) D over the other chunks plus twice this
-                // chunk's own part b (its value and its partial sums), b being
-                // the same bound over this chunk alone.  Its mass and exponent
-                // sums come from the logits again when pass B's weights were
-                // cached.
+                int ok = 0;
                 if (tok >= 0) {
-                    int ok = (wc - lo >= 2 * D && hi - wc > 2 * D + 1) ? 1 : 0;
-                    if (!ok) {
-                        if (d.acache) {
-                            float l[kChunk], q[kChunk], y[kChunk], absa[kChunk], wr[kChunk];
-                            load_l(d, ci, l);
-                            load_q(d, ci, RES, q);
-                            fast_y(l, d.m, d.c, d.clo, y, absa);
-                            fast_weights<RES>(y, q, inv, wr, &relc);
-#pragma unroll
-                            for (int e = 0; e < kChunk; ++e) ac = fmaf(y[e], absa[e], ac);
-                        }
-                        const float bc =
-                            (kFastE0 * relc +
-                             kFastKappa * (ac + sh.A_tot * relc) * inv * 1.0009765625f) *
-                                1.0009765625f * 1.152921504606847e18f +
-                            (float)W * (8.0f * 5.96046448e-08f) + 3.0f;
-                        const unsigned long long b =
-                            (unsigned long long)fminf(bc, 1.0e18f) + 1ull;
-                        const float um = fmaxf(d.u, __fsub_rn(1.0f, d.u));
-                        const unsigned long long Dp =
-                            scale_floor(um, D) + (D >> 22) + 2ull + 2ull * b;
-                        ok = (wc - lo >= Dp && hi - wc > Dp + 1) ? 1 : 0;
-                    }
+                    const float um = fmaxf(d.u, __fsub_rn(1.0f, d.u));
+                    const float dp = um * sh.f_D + sh.f_eS * 1.004f * (float)(hi - lo) + 2.0f;
+                    const long long Dp = (long long)fminf(dp, 4.0e18f) + 1ll;
+                    ok = ((long long)tau - lo >= Dp && hi - (long long)tau > Dp) ? 1 : 0;
                     sh.token = (int)((d.c0 + ci) * kChunk + tok);
-                    sh.cert = ok;
                 }
+                sh.cert = ok;
             }
         }
         __syncthreads();
         cert = sh.cert;
     }
-    if (tid < d.G) *cluster.map_shared_rank(&sh.xC[d.rank], tid) = cert;
-    xsync(cluster, d.G);
-    if (warp == 0) {
-        int ok = lane < d.G ? sh.xC[lane] : 1;
-        ok = __all_sync(0xffffffffu, ok);
-        if (lane == 0) sh.cert_all = ok && total > 0;
+    if (d.G > 1) {
+        if (tid < d.G) *cluster.map_shared_rank(&sh.xC[d.rank], tid) = cert;
+        xsync(cluster, d.G);
+        if (warp == 0) {
+            int ok = lane < d.G ? sh.xC[lane] : 1;
+            ok = __all_sync(0xffffffffu, ok);
+            if (lane == 0) sh.cert_all = ok;
+        }
+        __syncthreads();
+        return sh.cert_all != 0;
     }
-    __syncthreads();
-    return sh.cert_all != 0;
+    return cert != 0;
 }
 
 // ---- precise pass: float-float exponentials, exact integer prefix sums
@@ -1352,9 +1605,9 @@ __device__ void draw_precise_any(cg::cluster_group& cluster, DrawShared& sh,
     draw_precise<DT>(cluster, sh, d, degenerate);
 }
 
-// Dynamic shared memory of a draw: block totals, the 2^(i/1024) table, and a
-// cache of the CTA's slice (level 1: fp32 exponents for the fast pass; level 2:
-// also room for the float-float exponentials of the precise pass).
+// Dynamic shared memory of a draw: block sums, the 2^(i/1024) table, and room
+// for the precise pass: its one-read chunk table, or (level 2) a cache of the
+// slice's float-float exponentials.
 // log2 of a cluster size (a power of two, at most 16): slices are cut with
 // shifts, not 64-bit divisions.
 __host__ __device__ inline int log2_pow2(int G) {
@@ -1366,9 +1619,11 @@ __host__ __device__ inline long long draw_slice_chunks(int V, int G) {
     const long long nch = ((long long)V + kChunk - 1) / kChunk;
     return (nch + G - 1) >> log2_pow2(G);
 }
+// Block sums: two 64-bit sums per 64-element block of the fast pass (the
+// precise pass's one per 256 elements fits in the same room).
 __host__ __device__ inline size_t draw_bsum_bytes(int V, int G) {
-    const long long nblk = (draw_slice_chunks(V, G) + kBlockChunks - 1) / kBlockChunks;
-    return ((size_t)nblk * 8 + 15) & ~(size_t)15;
+    const long long nblk = (draw_slice_chunks(V, G) + 7) / 8;
+    return (size_t)nblk * 16;
 }
 // Dynamic shared memory a draw may use: two 512-thread CTAs of the drawing
 // kernels still fit on one SM.
@@ -1382,20 +1637,18 @@ __host__ __device__ inline size_t precise_table_bytes(int V, int G) {
 __host__ __device__ inline size_t draw_smem_bytes(int V, int G, int level) {
     const size_t slice = (size_t)draw_slice_chunks(V, G) * kChunk;
     const size_t base = draw_bsum_bytes(V, G) + 2 * kExpTable * sizeof(float);
-    const size_t cache =
-        level >= 2 ? slice * sizeof(ff) : level == 1 ? slice * sizeof(float) : 0;
+    const size_t cache = level >= 2 ? slice * sizeof(ff) : 0;
     const size_t tab = precise_table_bytes(V, G);
     return base + (tab > cache && base + tab <= kDrawSmemBudget ? tab : cache);
 }
 
 template <typename DT>
-__device__ __forceinline__ DrawCtx<DT> make_draw_ctx(unsigned char* dyn, int level, bool prefetch,
+__device__ __forceinline__ DrawCtx<DT> make_draw_ctx(unsigned char* dyn, int level,
                                                     const DT* rowp, const float* qrow,
                                                     bool residual, int V, float m, float c,
                                                     ff c2, float u, int rank, int G,
                                                     float s_row) {
     DrawCtx<DT> d;
-    d.prefetch = prefetch;
     d.rowp = rowp;
     d.qrow = qrow;
     d.V = V;
@@ -1420,7 +1673,6 @@ __device__ __forceinline__ DrawCtx<DT> make_draw_ctx(unsigned char* dyn, int lev
     d.thi = reinterpret_cast<float*>(dyn + bb);
     d.tlo = d.thi + kExpTable;
     unsigned char* cache = dyn + bb + 2 * kExpTable * sizeof(float);
-    d.acache = level >= 1 ? reinterpret_cast<float*>(cache) : nullptr;
     d.ecache = level >= 2 ? reinterpret_cast<ff*>(cache) : nullptr;
     // The chunk table of the one-read precise pass shares the cache's place
     // (the fast pass is over when it is written).
@@ -1437,23 +1689,18 @@ __device__ __forceinline__ DrawCtx<DT> make_draw_ctx(unsigned char* dyn, int lev
 // cannot certify its bin (or when `force_precise`).  Every CTA calls it; the
 // owner CTA's thread 0 writes the token to *token_out.  Sets `degenerate` and
 // `fallback` in all threads.  The CTA's slices of the decision row and of the
-// q row are first prefetched into L2 in bulk when the launch's draws fit in L2
-// together (d.prefetch).  With `defer_precise` a draw that
+// q row are read with loads that do not allocate in L1.  With `defer_precise` a draw that
 // needs the precise pass returns true at once (in every thread) and writes no
 // token: the caller hands it to the precise kernel.
-template <typename DT>
+template <typename DT, bool EXACT>
 __device__ bool draw(cg::cluster_group& cluster, DrawShared& sh, const DrawCtx<DT>& d,
                      bool force_precise, bool defer_precise, int32_t* token_out,
                      bool& degenerate, bool& fallback) {
-    if (d.prefetch && threadIdx.x == 0) {
-        prefetch_slice_l2(d.rowp, d.c0, d.mych, d.V);
-        if (d.residual) prefetch_slice_l2(d.qrow, d.c0, d.mych, d.V);
-    }
     degenerate = false;
     fallback = true;
     const bool certified =
-        !force_precise && (d.residual ? draw_fast<DT, true>(cluster, sh, d)
-                                      : draw_fast<DT, false>(cluster, sh, d));
+        !force_precise && (d.residual ? draw_fast<DT, true, EXACT>(cluster, sh, d)
+                                      : draw_fast<DT, false, EXACT>(cluster, sh, d));
     if (certified) {
         fallback = false;
         if (threadIdx.x == 0 && sh.token >= 0) *token_out = sh.token;
@@ -1509,7 +1756,6 @@ struct VerifyArgs {
     Epilogue ep;
     int B, k, V, G, W;
     int draw_level;     // shared-memory cache level of the draw
-    int prefetch;       // the draws bulk-prefetch their slices into L2
     int force_precise;  // test hook: skip the fast draw
     float c;     // log2(e)/T (float, for the row statistics and the fast draw)
     ff c2;       // log2(e)/T in float-float (p(x) and the precise draw)
@@ -1730,10 +1976,10 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(VerifyArgs a) {
     const float m = fs.rowstat[n - wave_row0].m;
     bool degenerate = false, fallback = false;
     const DrawCtx<DT> dc =
-        make_draw_ctx<DT>(dyn, a.draw_level, a.prefetch != 0, drow, qrow, n < k, V, m, a.c, a.c2,
+        make_draw_ctx<DT>(dyn, a.draw_level, drow, qrow, n < k, V, m, a.c, a.c2,
                           u, rank, G, fs.rowstat[n - wave_row0].s);
-    const bool deferred = draw<DT>(cluster, ds, dc, a.force_precise != 0, a.plist != nullptr,
-                                   o + n, degenerate, fallback);
+    const bool deferred = draw<DT, true>(cluster, ds, dc, a.force_precise != 0,
+                                         a.plist != nullptr, o + n, degenerate, fallback);
     if (rank == 0) {
         for (int i = tid; i <= k; i += kThreads)
             if (i != n) o[i] = i < n ? fs.xs[i] : -1;
@@ -2639,13 +2885,15 @@ struct FinishArgs {
     Epilogue ep;
     int B, k, V, G;
     int draw_level;
-    int prefetch;  // the draws bulk-prefetch their slices into L2
     int force_precise;
     float c;
     ff c2;
 };
 
-template <typename DT>
+// EXACT: the fast draw's chunk sums in float-float (small batches, whose
+// precise draws run here); else pairwise (large batches, whose precise draws
+// go to sv_precise_kernel in one wave, so a few more of them cost little).
+template <typename DT, bool EXACT>
 __global__ void __launch_bounds__(kThreads, 2) sv_finish_sample_kernel(FinishArgs a) {
     extern __shared__ __align__(16) unsigned char dyn[];
     __shared__ DrawShared ds;
@@ -2715,11 +2963,11 @@ __global__ void __launch_bounds__(kThreads, 2) sv_finish_sample_kernel(FinishArg
     const DT* drow = static_cast<const DT*>(a.logits) + ((long long)b * (k + 1) + n) * V;
     const float* qrow = n < k ? a.q + ((long long)b * k + n) * V : nullptr;
     bool degenerate = false, fallback = false;
-    const DrawCtx<DT> dc = make_draw_ctx<DT>(dyn, a.draw_level, a.prefetch != 0, drow, qrow, n < k,
+    const DrawCtx<DT> dc = make_draw_ctx<DT>(dyn, a.draw_level, drow, qrow, n < k,
                                              V, recs[n].mraw, a.c, a.c2, s_ur, rank, G,
                                              recs[n].S);
-    const bool deferred = draw<DT>(cluster, ds, dc, a.force_precise != 0, a.plist != nullptr,
-                                   o + n, degenerate, fallback);
+    const bool deferred = draw<DT, EXACT>(cluster, ds, dc, a.force_precise != 0,
+                                          a.plist != nullptr, o + n, degenerate, fallback);
     if (rank == 0) {
         for (int i = tid; i <= k; i += kThreads)
             if (i != n) o[i] = i < n ? a.x[(long long)b * k + i] : -1;
@@ -2772,7 +3020,7 @@ __global__ void __launch_bounds__(kThreads, 2) sv_precise_kernel(PreciseArgs a) 
         const DT* drow = static_cast<const DT*>(a.logits) + ((long long)b * (k + 1) + n) * V;
         const float* qrow = n < k ? a.q + ((long long)b * k + n) * V : nullptr;
         const RowRec& rec = a.rows[(long long)b * (k + 1) + n];
-        const DrawCtx<DT> dc = make_draw_ctx<DT>(dyn, a.draw_level, false, drow, qrow, n < k, V,
+        const DrawCtx<DT> dc = make_draw_ctx<DT>(dyn, a.draw_level, drow, qrow, n < k, V,
                                                  rec.mraw, a.c, a.c2, a.ur[b], rank, G, rec.S);
         if (tid == 0) ds.token = -1;
         __syncthreads();
@@ -2802,7 +3050,7 @@ struct MatchArgs {
     const RowRec* rows;
     int32_t* out;
     int B, k, V, G;
-    int draw_level, prefetch, force_precise;
+    int draw_level, force_precise;
     float c;
     ff c2;
 };
@@ -2828,10 +3076,11 @@ __global__ void __launch_bounds__(kThreads, 2) sv_match_draw_kernel(MatchArgs a)
     // if its scan reaches the row); every CTA of the cluster sees the same values.
     if ((rec.flags & (kRowBad | kRowSkipped)) || !(s_u >= 0.0f && s_u < 1.0f)) return;
     const DT* rowp = static_cast<const DT*>(a.logits) + row * (long long)V;
-    const DrawCtx<DT> dc = make_draw_ctx<DT>(dyn, a.draw_level, a.prefetch != 0, rowp, nullptr,
+    const DrawCtx<DT> dc = make_draw_ctx<DT>(dyn, a.draw_level, rowp, nullptr,
                                              false, V, rec.mraw, a.c, a.c2, s_u, rank, G, rec.S);
     bool degenerate = false, fallback = false;
-    draw<DT>(cluster, ds, dc, a.force_precise != 0, false, a.out + row, degenerate, fallback);
+    draw<DT, true>(cluster, ds, dc, a.force_precise != 0, false, a.out + row, degenerate,
+                   fallback);
 }
 
 // One warp per sequence: lanes test positions in parallel (a bad row, a bad
@@ -3016,8 +3265,11 @@ static ff log2e_over(float T) {
     return ff{hi, (float)(v - (double)hi)};
 }
 
-// Test hook (spec_verify_debug_force_precise): every draw takes the precise pass.
-static std::atomic<int> g_force_precise{0};
+// The options of one call (sv_tuning, specverify_debug.h): all zero, the
+// automatic choices, for the entry points of specverify.h; the caller's for
+// the _tuned entry points, so that a test's or a tuning script's setting
+// affects its own calls only.
+static const sv_tuning kAuto = {0, 0, 0, 0, 0, 0, 0, 0, 0};
 
 
 struct DeviceInfo {
@@ -3031,19 +3283,10 @@ static DeviceInfo g_dev[64];
 
 constexpr size_t kDynSmemMax = 160 * 1024;  // attribute of the kernels that draw
 
-// Whether the draws of a launch prefetch their slices (decision row and q row)
-// into L2 in bulk: only when all of them fit in a third of the L2 together, so
-// that no prefetched line is evicted before it is read.
-static int draw_prefetch(int B, int V, sv_dtype dt) {
-    const double bytes = (double)B * V * ((dt == SV_BF16 ? 2 : 4) + 4);
-    return bytes <= 40.0 * 1024 * 1024 ? 1 : 0;
-}
-
-// Cache level of a draw with G CTAs per row: the largest that fits the budget.
+// Cache level of a draw with G CTAs per row: 2 (the precise pass keeps its
+// exponentials) when that fits the budget, else 0.
 static int draw_level(int V, int G) {
-    for (int lv = 2; lv >= 1; --lv)
-        if (draw_smem_bytes(V, G, lv) <= kDrawSmemBudget) return lv;
-    return 0;
+    return draw_smem_bytes(V, G, 2) <= kDrawSmemBudget ? 2 : 0;
 }
 
 template <typename K> static cudaError_t cluster_attrs(K kernel, bool dyn) {
@@ -3084,8 +3327,10 @@ static sv_status device_setup(int* sms) {
             SV_TRY(cluster_attrs(sv_verify_kernel<float, true>, true));
             SV_TRY(cluster_attrs(sv_verify_kernel<__nv_bfloat16, false>, false));
             SV_TRY(cluster_attrs(sv_verify_kernel<float, false>, false));
-            SV_TRY(cluster_attrs(sv_finish_sample_kernel<__nv_bfloat16>, true));
-            SV_TRY(cluster_attrs(sv_finish_sample_kernel<float>, true));
+            SV_TRY(cluster_attrs(sv_finish_sample_kernel<__nv_bfloat16, true>, true));
+            SV_TRY(cluster_attrs(sv_finish_sample_kernel<float, true>, true));
+            SV_TRY(cluster_attrs(sv_finish_sample_kernel<__nv_bfloat16, false>, true));
+            SV_TRY(cluster_attrs(sv_finish_sample_kernel<float, false>, true));
             SV_TRY(cluster_attrs(sv_precise_kernel<__nv_bfloat16>, true));
             SV_TRY(cluster_attrs(sv_match_draw_kernel<__nv_bfloat16>, true));
             SV_TRY(cluster_attrs(sv_match_draw_kernel<float>, true));
@@ -3125,7 +3370,7 @@ static sv_status device_setup(int* sms) {
                 cfg.attrs = &at;
                 cfg.numAttrs = 1;
                 int n = 0;
-                if (cudaOccupancyMaxActiveClusters(&n, sv_finish_sample_kernel<__nv_bfloat16>,
+                if (cudaOccupancyMaxActiveClusters(&n, sv_finish_sample_kernel<__nv_bfloat16, true>,
                                                    &cfg) != cudaSuccess)
                     n = 0;
                 d.clusters[lg] = n;
@@ -3216,26 +3461,19 @@ static int wave_rows(int B, int k, int V, int esz) {
 // The precise draws listed by a draw kernel of a large batch (plist_count and
 // plist in the workspace): persistent 16-CTA clusters, launched as a
 // programmatic dependent of that kernel.
-// Tuning hooks of the fused kernel (spec_verify_debug_fused_tuning): whether
-// it defers the precise draws (0 automatic: when B >= SMs; 1 always; 2 never)
-// and a minimum of dynamic shared memory per CTA in KiB (0: none), which
-// limits how many of its CTAs share an SM.
-static std::atomic<int> g_fused_defer{0};
-static std::atomic<int> g_fused_pad{0};
-// Cluster size of sv_precise_kernel, and its tuning hook
-// (spec_verify_debug_precise_split; 0: this default).  Four CTAs per draw:
+// Cluster size of sv_precise_kernel (sv_tuning.precise_split overrides it).
+// Four CTAs per draw:
 // each draw's chain of barriers and single-warp search costs about the same at
 // any size, so more clusters at once (76 of 4 against 14 of 16 on GB300)
 // finish a batch's precise draws sooner (measured on B=256, V=151936: the
 // draws take 157 us with clusters of 4, 192 us with 16, 172 with 8).
 constexpr int kPreciseG = 4;
-static std::atomic<int> g_force_precise_split{0};
 
 static sv_status launch_precise(const void* logits, sv_dtype dt, const float* q, const float* ur,
                                 const RowRec* rows, const int32_t* nacc,
                                 const uint32_t* plist_count, const uint32_t* plist,
                                 uint32_t* seqstat, int32_t* out, int B, int k, int V, float c,
-                                ff c2, cudaStream_t stream) {
+                                ff c2, cudaStream_t stream, const sv_tuning& tu) {
     cudaError_t e;
     cudaLaunchAttribute pdl;
     pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -3253,7 +3491,7 @@ static sv_status launch_precise(const void* logits, sv_dtype dt, const float* q,
     pa.B = B;
     pa.k = k;
     pa.V = V;
-    pa.G = g_force_precise_split.load() ? g_force_precise_split.load() : kPreciseG;
+    pa.G = tu.precise_split ? tu.precise_split : kPreciseG;
     pa.draw_level = draw_level(V, pa.G);
     pa.c = c;
     pa.c2 = c2;
@@ -3278,7 +3516,7 @@ static sv_status launch_precise(const void* logits, sv_dtype dt, const float* q,
 static sv_status launch_fused(bool sampled, const void* logits, sv_dtype dt, const float* q,
                               const int32_t* x, const float* ua, const float* ur, float T, int B,
                               int k, int V, int32_t* out, int32_t* nacc, void* ws,
-                              cudaStream_t stream, int sms, Epilogue ep) {
+                              cudaStream_t stream, int sms, Epilogue ep, const sv_tuning& tu) {
     VerifyArgs a;
     a.ep = ep;
     a.logits = logits;
@@ -3299,19 +3537,18 @@ static sv_status launch_fused(bool sampled, const void* logits, sv_dtype dt, con
     a.W = wave_rows(B, k, V, esz);
     a.c2 = log2e_over(sampled ? T : 1.0f);
     a.c = a.c2.hi;
-    a.force_precise = g_force_precise.load();
+    a.force_precise = tu.force_precise != 0;
     a.plist_count = nullptr;
     a.plist = nullptr;
-    a.prefetch = draw_prefetch(B, V, dt);
     size_t smem = 0;
     a.draw_level = 0;
     // Large sampled batches defer the precise draws to sv_precise_kernel.
-    const int dmode = g_fused_defer.load();
+    const int dmode = tu.fused_defer;
     const bool defer = sampled && (dmode == 1 || (dmode == 0 && B >= sms));
     if (sampled) {
         a.draw_level = draw_level(V, a.G);
         smem = draw_smem_bytes(V, a.G, a.draw_level);
-        if (const int pad = g_fused_pad.load()) smem = std::max(smem, (size_t)pad * 1024);
+        if (const int pad = tu.fused_pad_kib) smem = std::max(smem, (size_t)pad * 1024);
         if (smem > kDynSmemMax) return SV_ERR_UNSUPPORTED;
         if (defer) {
             a.plist_count =
@@ -3338,7 +3575,7 @@ static sv_status launch_fused(bool sampled, const void* logits, sv_dtype dt, con
     if (e != cudaSuccess) return SV_ERR_CUDA;
     if (!defer) return SV_OK;
     return launch_precise(logits, dt, q, ur, a.rows, nacc, a.plist_count, a.plist, a.seqstat, out,
-                          B, k, V, a.c, a.c2, stream);
+                          B, k, V, a.c, a.c2, stream, tu);
 }
 
 // Vocabulary split of the per-row kernel: rows are split over a cluster only
@@ -3360,12 +3597,9 @@ static int rows_threads(long long ctas, long long nvec_cta, int sms) {
 }
 
 // With `skip`: one 512-thread CTA per row, rows position-major, stop[] reset
-// first (a memset on the same stream).
-// Tuning hook (spec_verify_debug_rows_split): a fixed vocabulary split and
-// thread count for the row stream of the two-kernel path (0: automatic).
-static std::atomic<int> g_force_rows_G{0}, g_force_rows_nt{0};
-// Hook (spec_verify_debug_flat): 0 automatic, 1 never the flat greedy stream.
-static std::atomic<int> g_flat_off{0};
+// first (a memset on the same stream).  sv_tuning.rows_split / rows_threads
+// fix the split and thread count of the two-kernel path's stream (which also
+// keeps greedy batches off the flat stream, as sv_tuning.flat_off does).
 
 // Plan of the flat greedy stream: P ranges, one per resident CTA (two per SM)
 // and at least one per SM, each at least a third of a row long (a row meets at
@@ -3391,7 +3625,7 @@ static bool flat_plan(int B, int k, int V, int esz, const void* logits, int sms,
 static sv_status launch_rows(bool sampled, const void* logits, sv_dtype dt, const float* q,
                              const int32_t* x, const float* ua, float T, int B, int k, int V,
                              void* ws, cudaStream_t stream, int sms, bool skip,
-                             bool flat_ok = true) {
+                             const sv_tuning& tu, bool flat_ok = true) {
     const long long R = (long long)B * (k + 1);
     RowsArgs a;
     a.logits = logits;
@@ -3410,8 +3644,8 @@ static sv_status launch_rows(bool sampled, const void* logits, sv_dtype dt, cons
     a.c = a.c2.hi;
     const int esz = dt == SV_BF16 ? 2 : 4;
     FlatArgs f;
-    if (!sampled && !skip && flat_ok && !g_flat_off.load() && !g_force_rows_G.load() &&
-        !g_force_rows_nt.load() && flat_plan(B, k, V, esz, logits, sms, &f)) {
+    if (!sampled && !skip && flat_ok && !tu.flat_off && !tu.rows_split && !tu.rows_threads &&
+        flat_plan(B, k, V, esz, logits, sms, &f)) {
         f.logits = logits;
         f.rows = a.rows;
         f.hdr = a.hdr;
@@ -3435,8 +3669,8 @@ static sv_status launch_rows(bool sampled, const void* logits, sv_dtype dt, cons
     const long long nvec_row = ((long long)V * esz + 15) / 16;
     a.G = skip ? 1 : rows_split(R, nvec_row, sms);
     int nt = skip ? 512 : rows_threads(R * a.G, nvec_row / a.G, sms);
-    if (!skip && g_force_rows_G.load()) a.G = g_force_rows_G.load();
-    if (g_force_rows_nt.load()) nt = g_force_rows_nt.load();
+    if (!skip && tu.rows_split) a.G = tu.rows_split;
+    if (tu.rows_threads) nt = tu.rows_threads;
     if (skip && cudaMemsetAsync(a.stop, 0xFF, (size_t)B * sizeof(uint32_t), stream) != cudaSuccess)
         return SV_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
@@ -3463,9 +3697,6 @@ static sv_status launch_rows(bool sampled, const void* logits, sv_dtype dt, cons
     return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
-// Test / tuning hook (spec_verify_debug_draw_split): a fixed cluster size for
-// every draw kernel launch, 0 for the automatic choice.
-static std::atomic<int> g_force_draw_split{0};
 
 // Cluster size of the draw kernel of a large batch (B >= SMs): one CTA per
 // sequence (no cluster barriers, every CTA resident at once, the scheduler
@@ -3483,7 +3714,8 @@ static int draw_split_wide(int B, int V, int sms) {
 static sv_status launch_finish(bool sampled, const void* logits, sv_dtype dt, const float* q,
                                const int32_t* x, const float* ua, const float* ur, float T,
                                int B, int k, int V, int32_t* out, int32_t* nacc, void* ws,
-                               cudaStream_t stream, int sms, bool wide, Epilogue ep) {
+                               cudaStream_t stream, int sms, bool wide, Epilogue ep,
+                               const sv_tuning& tu) {
     const RowRec* rows =
         reinterpret_cast<const RowRec*>(static_cast<char*>(ws) + ws_rows_offset());
     uint32_t* seqstat = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + ws_seq_offset(B, k));
@@ -3518,12 +3750,11 @@ static sv_status launch_finish(bool sampled, const void* logits, sv_dtype dt, co
     a.k = k;
     a.V = V;
     a.G = wide ? draw_split_wide(B, V, sms) : seq_split(true, B, V, dt == SV_BF16 ? 2 : 4, sms);
-    if (const int fg = g_force_draw_split.load()) a.G = fg;
+    if (const int fg = tu.draw_split) a.G = fg;
     a.c2 = log2e_over(T);
     a.c = a.c2.hi;
-    a.force_precise = g_force_precise.load();
+    a.force_precise = tu.force_precise != 0;
     a.draw_level = draw_level(V, a.G);
-    a.prefetch = draw_prefetch(B, V, dt);
     a.plist_count = nullptr;
     a.plist = nullptr;
     const size_t smem = draw_smem_bytes(V, a.G, a.draw_level);
@@ -3544,12 +3775,16 @@ static sv_status launch_finish(bool sampled, const void* logits, sv_dtype dt, co
     cudaLaunchAttribute attr[2] = {cluster_attr(a.G), pdl};
     cfg.attrs = attr;
     cfg.numAttrs = wide ? 1 : 2;
-    e = dt == SV_BF16 ? cudaLaunchKernelEx(&cfg, sv_finish_sample_kernel<__nv_bfloat16>, a)
-                      : cudaLaunchKernelEx(&cfg, sv_finish_sample_kernel<float>, a);
+    if (wide)  // large batches: the cheaper fast pass (its precise draws are deferred)
+        e = dt == SV_BF16 ? cudaLaunchKernelEx(&cfg, sv_finish_sample_kernel<__nv_bfloat16, false>, a)
+                          : cudaLaunchKernelEx(&cfg, sv_finish_sample_kernel<float, false>, a);
+    else
+        e = dt == SV_BF16 ? cudaLaunchKernelEx(&cfg, sv_finish_sample_kernel<__nv_bfloat16, true>, a)
+                          : cudaLaunchKernelEx(&cfg, sv_finish_sample_kernel<float, true>, a);
     if (e != cudaSuccess || !wide) return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 
     return launch_precise(logits, dt, q, ur, rows, nacc, a.plist_count, a.plist, seqstat, out, B,
-                          k, V, a.c, a.c2, stream);
+                          k, V, a.c, a.c2, stream, tu);
 }
 
 // Sample-and-match: the row stream (greedy statistics: max, argmax, validity),
@@ -3560,9 +3795,9 @@ static sv_status launch_finish(bool sampled, const void* logits, sv_dtype dt, co
 static sv_status launch_match(const void* logits, sv_dtype dt, const int32_t* x, const float* ua,
                               const float* ur, float T, int B, int k, int V, int32_t* out,
                               int32_t* nacc, void* ws, cudaStream_t stream, int sms,
-                              Epilogue ep) {
+                              Epilogue ep, const sv_tuning& tu) {
     sv_status st = launch_rows(false, logits, dt, nullptr, x, nullptr, 1.0f, B, k, V, ws, stream,
-                               sms, false, false);
+                               sms, false, tu, false);
     if (st != SV_OK) return st;
     const RowRec* rows =
         reinterpret_cast<const RowRec*>(static_cast<char*>(ws) + ws_rows_offset());
@@ -3582,8 +3817,7 @@ static sv_status launch_match(const void* logits, sv_dtype dt, const int32_t* x,
     while (G < 16 && (V + G - 1) / G > kSliceMax) G *= 2;
     a.G = G;
     a.draw_level = draw_level(V, G);
-    a.prefetch = draw_prefetch((int)std::min<long long>(R, 1 << 30), V, dt);
-    a.force_precise = g_force_precise.load();
+    a.force_precise = tu.force_precise != 0;
     a.c2 = log2e_over(T);
     a.c = a.c2.hi;
     const size_t smem = draw_smem_bytes(V, G, a.draw_level);
@@ -3621,10 +3855,9 @@ static sv_status launch_match(const void* logits, sv_dtype dt, const int32_t* x,
 // exit, the draw in the same launch, no second launch); the rest take the
 // two-kernel path, whose row stream spreads every row over all SMs.
 enum Path { kPathTwoKernel = 1, kPathFused = 2, kPathSkip = 3 };
-// Test hook (spec_verify_debug_force_path): 0 automatic, else a Path.
-static std::atomic<int> g_force_path{0};
-static Path choose_path(bool sampled, int B, int V, int esz, int sms) {
-    const int f = g_force_path.load();
+// sv_tuning.path: 0 automatic, else a Path.
+static Path choose_path(bool sampled, int B, int V, int esz, int sms, const sv_tuning& tu) {
+    const int f = tu.path;
     if (f >= kPathTwoKernel && f <= kPathSkip) return (Path)f;
     if (B >= sms) return kPathSkip;
     // Sampled batches of at least half an SM count: measured on B = 80..128 at
@@ -3638,20 +3871,24 @@ static Path choose_path(bool sampled, int B, int V, int esz, int sms) {
     if (sampled && (long long)B * seq_split(true, B, V, esz, sms) >= sms) return kPathFused;
     return kPathTwoKernel;
 }
+static Path choose_path(bool sampled, int B, int V, int esz, int sms) {
+    return choose_path(sampled, B, V, esz, sms, kAuto);
+}
 
 static sv_status run_verify(bool sampled, const void* logits, sv_dtype dt, const float* q,
                             const int32_t* x, const float* ua, const float* ur, float T, int B,
                             int k, int V, int32_t* out, int32_t* nacc, void* ws,
-                            cudaStream_t stream, int sms, Epilogue ep) {
-    const Path path = choose_path(sampled, B, V, dt == SV_BF16 ? 2 : 4, sms);
+                            cudaStream_t stream, int sms, Epilogue ep, const sv_tuning& tu) {
+    const Path path = choose_path(sampled, B, V, dt == SV_BF16 ? 2 : 4, sms, tu);
     if (path == kPathFused)
         return launch_fused(sampled, logits, dt, q, x, ua, ur, T, B, k, V, out, nacc, ws, stream,
-                            sms, ep);
+                            sms, ep, tu);
     const bool skip = path == kPathSkip;
-    sv_status st = launch_rows(sampled, logits, dt, q, x, ua, T, B, k, V, ws, stream, sms, skip);
+    sv_status st =
+        launch_rows(sampled, logits, dt, q, x, ua, T, B, k, V, ws, stream, sms, skip, tu);
     if (st != SV_OK) return st;
     return launch_finish(sampled, logits, dt, q, x, ua, ur, T, B, k, V, out, nacc, ws, stream,
-                         sms, skip, ep);
+                         sms, skip, ep, tu);
 }
 
 // Tree verification: the row stream over all B*N rows (statistics only, no
@@ -3660,10 +3897,11 @@ static sv_status run_verify(bool sampled, const void* logits, sv_dtype dt, const
 static sv_status run_tree(bool sampled, const void* logits, sv_dtype dt, const float* q,
                           const int32_t* tok, const int32_t* par, const float* ua,
                           const float* ur, float T, int B, int N, int V, int32_t* out,
-                          int32_t* nodes, int32_t* nacc, void* ws, cudaStream_t stream, int sms) {
+                          int32_t* nodes, int32_t* nacc, void* ws, cudaStream_t stream, int sms,
+                          const sv_tuning& tu) {
     const int k = N - 1;
     sv_status st = launch_rows(sampled, logits, dt, nullptr, nullptr, nullptr, T, B, k, V, ws,
-                               stream, sms, false, !sampled);
+                               stream, sms, false, tu, !sampled);
     if (st != SV_OK) return st;
     TreeArgs a;
     a.logits = logits;
@@ -3744,9 +3982,24 @@ size_t spec_verify_workspace_size(int B, int k, int V, sv_dtype dtype) {
     return ws_bytes_for(B, k);
 }
 
-sv_status spec_verify_rows(sv_mode mode, const void* logits, sv_dtype dtype,
+}  // extern "C"
+
+namespace sv {
+
+// The options of a _tuned call are checked like any other argument.
+static bool tuning_valid(const sv_tuning& t) {
+    auto pow2 = [](int g) { return g == 0 || g == 1 || g == 2 || g == 4 || g == 8 || g == 16; };
+    return t.path >= 0 && t.path <= 3 && pow2(t.draw_split) && pow2(t.precise_split) &&
+           pow2(t.rows_split) && t.fused_defer >= 0 && t.fused_defer <= 2 &&
+           t.fused_pad_kib >= 0 && t.fused_pad_kib <= 160 &&
+           (t.rows_threads == 0 || t.rows_threads == 128 || t.rows_threads == 256 ||
+            t.rows_threads == 512 || t.rows_threads == 1024);
+}
+
+static sv_status rows_impl(sv_mode mode, const void* logits, sv_dtype dtype,
                            const float* draft_probs, const int32_t* draft_tokens, float T, int B,
-                           int k, int V, void* ws, size_t ws_bytes, cudaStream_t stream) {
+                           int k, int V, void* ws, size_t ws_bytes, cudaStream_t stream,
+                           const sv_tuning& tu) {
     if (mode != SV_MODE_SAMPLE && mode != SV_MODE_GREEDY) return SV_ERR_INVALID_ARG;
     sv_status st = check_common(logits, dtype, draft_tokens, B, k, V, ws, ws_bytes);
     if (st != SV_OK) return st;
@@ -3759,14 +4012,14 @@ sv_status spec_verify_rows(sv_mode mode, const void* logits, sv_dtype dtype,
     if ((st = device_setup(&sms)) != SV_OK) return st;
     if (B == 0) return SV_OK;
     return launch_rows(sampled, logits, dtype, draft_probs, draft_tokens, nullptr, T, B, k, V, ws,
-                       stream, sms, false);
+                       stream, sms, false, tu);
 }
 
-sv_status spec_verify_finish(sv_mode mode, const void* logits, sv_dtype dtype,
+static sv_status finish_impl(sv_mode mode, const void* logits, sv_dtype dtype,
                              const float* draft_probs, const int32_t* draft_tokens,
                              const float* u_accept, const float* u_resample, float T, int B,
                              int k, int V, int32_t* out_tokens, int32_t* num_accepted, void* ws,
-                             size_t ws_bytes, cudaStream_t stream) {
+                             size_t ws_bytes, cudaStream_t stream, const sv_tuning& tu) {
     if (mode != SV_MODE_SAMPLE && mode != SV_MODE_GREEDY) return SV_ERR_INVALID_ARG;
     sv_status st = check_common(logits, dtype, draft_tokens, B, k, V, ws, ws_bytes);
     if (st != SV_OK) return st;
@@ -3778,60 +4031,37 @@ sv_status spec_verify_finish(sv_mode mode, const void* logits, sv_dtype dtype,
     if (B == 0) return SV_OK;
     return launch_finish(sampled, logits, dtype, draft_probs, draft_tokens, u_accept, u_resample,
                          T, B, k, V, out_tokens, num_accepted, ws, stream, sms, B >= sms,
-                         Epilogue{nullptr, nullptr});
+                         Epilogue{nullptr, nullptr}, tu);
 }
 
-sv_status spec_verify_greedy(const void* logits, sv_dtype dtype, const int32_t* draft_tokens,
-                             int B, int k, int V, int32_t* out_tokens, int32_t* num_accepted,
-                             void* ws, size_t ws_bytes, cudaStream_t stream) {
+// spec_verify_greedy[_kv] (sampled = false: q, u_accept, u_resample unused, T
+// ignored) and spec_verify_sample[_kv].
+static sv_status verify_impl(bool sampled, const void* logits, sv_dtype dtype,
+                             const float* draft_probs, const int32_t* draft_tokens,
+                             const float* u_accept, const float* u_resample, float T, int B,
+                             int k, int V, int32_t* out_tokens, int32_t* num_accepted, void* ws,
+                             size_t ws_bytes, int32_t* kv_len, sv_spec_stats* stats,
+                             cudaStream_t stream, const sv_tuning& tu) {
     sv_status st = check_common(logits, dtype, draft_tokens, B, k, V, ws, ws_bytes);
     if (st != SV_OK) return st;
     if ((st = check_outputs(out_tokens, num_accepted, B)) != SV_OK) return st;
-    int sms = 0;
-    if ((st = device_setup(&sms)) != SV_OK) return st;
-    if (B == 0) return SV_OK;
-    return run_verify(false, logits, dtype, nullptr, draft_tokens, nullptr, nullptr, 1.0f, B, k, V,
-                      out_tokens, num_accepted, ws, stream, sms, Epilogue{nullptr, nullptr});
-}
-
-sv_status spec_verify_greedy_kv(const void* logits, sv_dtype dtype, const int32_t* draft_tokens,
-                                int B, int k, int V, int32_t* out_tokens, int32_t* num_accepted,
-                                void* ws, size_t ws_bytes, int32_t* kv_len, sv_spec_stats* stats,
-                                cudaStream_t stream) {
-    sv_status st = check_common(logits, dtype, draft_tokens, B, k, V, ws, ws_bytes);
-    if (st != SV_OK) return st;
-    if ((st = check_outputs(out_tokens, num_accepted, B)) != SV_OK) return st;
+    if (sampled && (st = check_sample(draft_probs, u_accept, u_resample, T, B)) != SV_OK) return st;
     if ((kv_len && !aligned16(kv_len)) || (stats && !aligned16(stats))) return SV_ERR_INVALID_ARG;
     int sms = 0;
     if ((st = device_setup(&sms)) != SV_OK) return st;
     if (B == 0) return SV_OK;
-    return run_verify(false, logits, dtype, nullptr, draft_tokens, nullptr, nullptr, 1.0f, B, k, V,
-                      out_tokens, num_accepted, ws, stream, sms,
-                      Epilogue{kv_len, reinterpret_cast<unsigned long long*>(stats)});
+    return run_verify(sampled, logits, dtype, sampled ? draft_probs : nullptr, draft_tokens,
+                      sampled ? u_accept : nullptr, sampled ? u_resample : nullptr,
+                      sampled ? T : 1.0f, B, k, V, out_tokens, num_accepted, ws, stream, sms,
+                      Epilogue{kv_len, reinterpret_cast<unsigned long long*>(stats)}, tu);
 }
 
-sv_status spec_verify_sample(const void* logits, sv_dtype dtype, const float* draft_probs,
-                             const int32_t* draft_tokens, const float* u_accept,
-                             const float* u_resample, float T, int B, int k, int V,
-                             int32_t* out_tokens, int32_t* num_accepted, void* ws,
-                             size_t ws_bytes, cudaStream_t stream) {
-    sv_status st = check_common(logits, dtype, draft_tokens, B, k, V, ws, ws_bytes);
-    if (st != SV_OK) return st;
-    if ((st = check_outputs(out_tokens, num_accepted, B)) != SV_OK) return st;
-    if ((st = check_sample(draft_probs, u_accept, u_resample, T, B)) != SV_OK) return st;
-    int sms = 0;
-    if ((st = device_setup(&sms)) != SV_OK) return st;
-    if (B == 0) return SV_OK;
-    return run_verify(true, logits, dtype, draft_probs, draft_tokens, u_accept, u_resample, T, B,
-                      k, V, out_tokens, num_accepted, ws, stream, sms, Epilogue{nullptr, nullptr});
-}
-
-sv_status spec_verify_tree(sv_mode mode, const void* logits, sv_dtype dtype,
+static sv_status tree_impl(sv_mode mode, const void* logits, sv_dtype dtype,
                            const float* draft_probs, const int32_t* tree_tokens,
                            const int32_t* tree_parents, const float* u_accept,
                            const float* u_resample, float T, int B, int N, int V,
                            int32_t* out_tokens, int32_t* out_nodes, int32_t* num_accepted,
-                           void* ws, size_t ws_bytes, cudaStream_t stream) {
+                           void* ws, size_t ws_bytes, cudaStream_t stream, const sv_tuning& tu) {
     if (mode != SV_MODE_SAMPLE && mode != SV_MODE_GREEDY) return SV_ERR_INVALID_ARG;
     if (N < 2) return SV_ERR_INVALID_ARG;
     if (N > kTreeMaxN) return SV_ERR_UNSUPPORTED;
@@ -3846,32 +4076,14 @@ sv_status spec_verify_tree(sv_mode mode, const void* logits, sv_dtype dtype,
     if ((st = device_setup(&sms)) != SV_OK) return st;
     if (B == 0) return SV_OK;
     return run_tree(sampled, logits, dtype, draft_probs, tree_tokens, tree_parents, u_accept,
-                    u_resample, T, B, N, V, out_tokens, out_nodes, num_accepted, ws, stream, sms);
+                    u_resample, T, B, N, V, out_tokens, out_nodes, num_accepted, ws, stream, sms,
+                    tu);
 }
 
-sv_status spec_verify_sample_kv(const void* logits, sv_dtype dtype, const float* draft_probs,
-                                const int32_t* draft_tokens, const float* u_accept,
-                                const float* u_resample, float T, int B, int k, int V,
-                                int32_t* out_tokens, int32_t* num_accepted, void* ws,
-                                size_t ws_bytes, int32_t* kv_len, sv_spec_stats* stats,
-                                cudaStream_t stream) {
-    sv_status st = check_common(logits, dtype, draft_tokens, B, k, V, ws, ws_bytes);
-    if (st != SV_OK) return st;
-    if ((st = check_outputs(out_tokens, num_accepted, B)) != SV_OK) return st;
-    if ((st = check_sample(draft_probs, u_accept, u_resample, T, B)) != SV_OK) return st;
-    if ((kv_len && !aligned16(kv_len)) || (stats && !aligned16(stats))) return SV_ERR_INVALID_ARG;
-    int sms = 0;
-    if ((st = device_setup(&sms)) != SV_OK) return st;
-    if (B == 0) return SV_OK;
-    return run_verify(true, logits, dtype, draft_probs, draft_tokens, u_accept, u_resample, T, B,
-                      k, V, out_tokens, num_accepted, ws, stream, sms,
-                      Epilogue{kv_len, reinterpret_cast<unsigned long long*>(stats)});
-}
-
-sv_status spec_verify_match(const void* logits, sv_dtype dtype, const int32_t* draft_tokens,
+static sv_status match_impl(const void* logits, sv_dtype dtype, const int32_t* draft_tokens,
                             const float* u_draw, const float* u_bonus, float T, int B, int k,
                             int V, int32_t* out_tokens, int32_t* num_accepted, void* ws,
-                            size_t ws_bytes, cudaStream_t stream) {
+                            size_t ws_bytes, cudaStream_t stream, const sv_tuning& tu) {
     sv_status st = check_common(logits, dtype, draft_tokens, B, k, V, ws, ws_bytes);
     if (st != SV_OK) return st;
     if ((st = check_outputs(out_tokens, num_accepted, B)) != SV_OK) return st;
@@ -3882,8 +4094,152 @@ sv_status spec_verify_match(const void* logits, sv_dtype dtype, const int32_t* d
     if ((st = device_setup(&sms)) != SV_OK) return st;
     if (B == 0) return SV_OK;
     return launch_match(logits, dtype, draft_tokens, u_draw, u_bonus, T, B, k, V, out_tokens,
-                        num_accepted, ws, stream, sms, Epilogue{nullptr, nullptr});
+                        num_accepted, ws, stream, sms, Epilogue{nullptr, nullptr}, tu);
 }
+
+}  // namespace sv
+
+extern "C" {
+
+sv_status spec_verify_rows(sv_mode mode, const void* logits, sv_dtype dtype,
+                           const float* draft_probs, const int32_t* draft_tokens, float T, int B,
+                           int k, int V, void* ws, size_t ws_bytes, cudaStream_t stream) {
+    return rows_impl(mode, logits, dtype, draft_probs, draft_tokens, T, B, k, V, ws, ws_bytes,
+                     stream, kAuto);
+}
+
+sv_status spec_verify_finish(sv_mode mode, const void* logits, sv_dtype dtype,
+                             const float* draft_probs, const int32_t* draft_tokens,
+                             const float* u_accept, const float* u_resample, float T, int B,
+                             int k, int V, int32_t* out_tokens, int32_t* num_accepted, void* ws,
+                             size_t ws_bytes, cudaStream_t stream) {
+    return finish_impl(mode, logits, dtype, draft_probs, draft_tokens, u_accept, u_resample, T, B,
+                       k, V, out_tokens, num_accepted, ws, ws_bytes, stream, kAuto);
+}
+
+sv_status spec_verify_greedy(const void* logits, sv_dtype dtype, const int32_t* draft_tokens,
+                             int B, int k, int V, int32_t* out_tokens, int32_t* num_accepted,
+                             void* ws, size_t ws_bytes, cudaStream_t stream) {
+    return verify_impl(false, logits, dtype, nullptr, draft_tokens, nullptr, nullptr, 1.0f, B, k,
+                       V, out_tokens, num_accepted, ws, ws_bytes, nullptr, nullptr, stream, kAuto);
+}
+
+sv_status spec_verify_greedy_kv(const void* logits, sv_dtype dtype, const int32_t* draft_tokens,
+                                int B, int k, int V, int32_t* out_tokens, int32_t* num_accepted,
+                                void* ws, size_t ws_bytes, int32_t* kv_len, sv_spec_stats* stats,
+                                cudaStream_t stream) {
+    return verify_impl(false, logits, dtype, nullptr, draft_tokens, nullptr, nullptr, 1.0f, B, k,
+                       V, out_tokens, num_accepted, ws, ws_bytes, kv_len, stats, stream, kAuto);
+}
+
+sv_status spec_verify_sample(const void* logits, sv_dtype dtype, const float* draft_probs,
+                             const int32_t* draft_tokens, const float* u_accept,
+                             const float* u_resample, float T, int B, int k, int V,
+                             int32_t* out_tokens, int32_t* num_accepted, void* ws,
+                             size_t ws_bytes, cudaStream_t stream) {
+    return verify_impl(true, logits, dtype, draft_probs, draft_tokens, u_accept, u_resample, T, B,
+                       k, V, out_tokens, num_accepted, ws, ws_bytes, nullptr, nullptr, stream,
+                       kAuto);
+}
+
+sv_status spec_verify_sample_kv(const void* logits, sv_dtype dtype, const float* draft_probs,
+                                const int32_t* draft_tokens, const float* u_accept,
+                                const float* u_resample, float T, int B, int k, int V,
+                                int32_t* out_tokens, int32_t* num_accepted, void* ws,
+                                size_t ws_bytes, int32_t* kv_len, sv_spec_stats* stats,
+                                cudaStream_t stream) {
+    return verify_impl(true, logits, dtype, draft_probs, draft_tokens, u_accept, u_resample, T, B,
+                       k, V, out_tokens, num_accepted, ws, ws_bytes, kv_len, stats, stream, kAuto);
+}
+
+sv_status spec_verify_tree(sv_mode mode, const void* logits, sv_dtype dtype,
+                           const float* draft_probs, const int32_t* tree_tokens,
+                           const int32_t* tree_parents, const float* u_accept,
+                           const float* u_resample, float T, int B, int N, int V,
+                           int32_t* out_tokens, int32_t* out_nodes, int32_t* num_accepted,
+                           void* ws, size_t ws_bytes, cudaStream_t stream) {
+    return tree_impl(mode, logits, dtype, draft_probs, tree_tokens, tree_parents, u_accept,
+                     u_resample, T, B, N, V, out_tokens, out_nodes, num_accepted, ws, ws_bytes,
+                     stream, kAuto);
+}
+
+sv_status spec_verify_match(const void* logits, sv_dtype dtype, const int32_t* draft_tokens,
+                            const float* u_draw, const float* u_bonus, float T, int B, int k,
+                            int V, int32_t* out_tokens, int32_t* num_accepted, void* ws,
+                            size_t ws_bytes, cudaStream_t stream) {
+    return match_impl(logits, dtype, draft_tokens, u_draw, u_bonus, T, B, k, V, out_tokens,
+                      num_accepted, ws, ws_bytes, stream, kAuto);
+}
+
+// The same calls with the options of sv_tuning (specverify_debug.h); a null
+// `tuning` means the automatic choices.
+#define SV_TUNING_OR_AUTO(t)                                         \
+    const sv_tuning& tu = (t) ? *(t) : kAuto;                        \
+    if (!tuning_valid(tu)) return SV_ERR_INVALID_ARG
+
+sv_status spec_verify_rows_tuned(sv_mode mode, const void* logits, sv_dtype dtype,
+                                 const float* draft_probs, const int32_t* draft_tokens, float T,
+                                 int B, int k, int V, void* ws, size_t ws_bytes,
+                                 cudaStream_t stream, const sv_tuning* tuning) {
+    SV_TUNING_OR_AUTO(tuning);
+    return rows_impl(mode, logits, dtype, draft_probs, draft_tokens, T, B, k, V, ws, ws_bytes,
+                     stream, tu);
+}
+
+sv_status spec_verify_finish_tuned(sv_mode mode, const void* logits, sv_dtype dtype,
+                                   const float* draft_probs, const int32_t* draft_tokens,
+                                   const float* u_accept, const float* u_resample, float T,
+                                   int B, int k, int V, int32_t* out_tokens,
+                                   int32_t* num_accepted, void* ws, size_t ws_bytes,
+                                   cudaStream_t stream, const sv_tuning* tuning) {
+    SV_TUNING_OR_AUTO(tuning);
+    return finish_impl(mode, logits, dtype, draft_probs, draft_tokens, u_accept, u_resample, T, B,
+                       k, V, out_tokens, num_accepted, ws, ws_bytes, stream, tu);
+}
+
+sv_status spec_verify_greedy_tuned(const void* logits, sv_dtype dtype,
+                                   const int32_t* draft_tokens, int B, int k, int V,
+                                   int32_t* out_tokens, int32_t* num_accepted, void* ws,
+                                   size_t ws_bytes, int32_t* kv_len, sv_spec_stats* stats,
+                                   cudaStream_t stream, const sv_tuning* tuning) {
+    SV_TUNING_OR_AUTO(tuning);
+    return verify_impl(false, logits, dtype, nullptr, draft_tokens, nullptr, nullptr, 1.0f, B, k,
+                       V, out_tokens, num_accepted, ws, ws_bytes, kv_len, stats, stream, tu);
+}
+
+sv_status spec_verify_sample_tuned(const void* logits, sv_dtype dtype, const float* draft_probs,
+                                   const int32_t* draft_tokens, const float* u_accept,
+                                   const float* u_resample, float T, int B, int k, int V,
+                                   int32_t* out_tokens, int32_t* num_accepted, void* ws,
+                                   size_t ws_bytes, int32_t* kv_len, sv_spec_stats* stats,
+                                   cudaStream_t stream, const sv_tuning* tuning) {
+    SV_TUNING_OR_AUTO(tuning);
+    return verify_impl(true, logits, dtype, draft_probs, draft_tokens, u_accept, u_resample, T, B,
+                       k, V, out_tokens, num_accepted, ws, ws_bytes, kv_len, stats, stream, tu);
+}
+
+sv_status spec_verify_tree_tuned(sv_mode mode, const void* logits, sv_dtype dtype,
+                                 const float* draft_probs, const int32_t* tree_tokens,
+                                 const int32_t* tree_parents, const float* u_accept,
+                                 const float* u_resample, float T, int B, int N, int V,
+                                 int32_t* out_tokens, int32_t* out_nodes, int32_t* num_accepted,
+                                 void* ws, size_t ws_bytes, cudaStream_t stream,
+                                 const sv_tuning* tuning) {
+    SV_TUNING_OR_AUTO(tuning);
+    return tree_impl(mode, logits, dtype, draft_probs, tree_tokens, tree_parents, u_accept,
+                     u_resample, T, B, N, V, out_tokens, out_nodes, num_accepted, ws, ws_bytes,
+                     stream, tu);
+}
+
+sv_status spec_verify_match_tuned(const void* logits, sv_dtype dtype, const int32_t* draft_tokens,
+                                  const float* u_draw, const float* u_bonus, float T, int B, int k,
+                                  int V, int32_t* out_tokens, int32_t* num_accepted, void* ws,
+                                  size_t ws_bytes, cudaStream_t stream, const sv_tuning* tuning) {
+    SV_TUNING_OR_AUTO(tuning);
+    return match_impl(logits, dtype, draft_tokens, u_draw, u_bonus, T, B, k, V, out_tokens,
+                      num_accepted, ws, ws_bytes, stream, tu);
+}
+#undef SV_TUNING_OR_AUTO
 
 sv_status spec_ngram_draft(const int32_t* history, const int32_t* lengths, int B, int Lmax,
                            int k, int n_min, int n_max, int32_t* draft_tokens,
@@ -3988,13 +4344,27 @@ sv_status spec_verify_debug_ffexp(const float* l, float m, float T, int n, doubl
     return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
-// Test hook (declared in include/specverify_debug.h): route every sampled draw
-// through the precise float-float pass (on != 0) or back to the certified fast
-// pass with fallback (on == 0).  Affects launches made after the call.
-void spec_verify_debug_force_precise(int on) { g_force_precise.store(on != 0 ? 1 : 0); }
-
-// Test hook (declared in include/specverify_debug.h): choose the one-call path.
-void spec_verify_debug_force_path(int path) { g_force_path.store(path >= 0 && path <= 3 ? path : 0); }
+// Introspection (declared in include/specverify_debug.h): per status bit, the
+// number of sequences of the last call on `ws` whose status word has it.
+sv_status spec_verify_debug_status_counts(const void* ws, cudaStream_t stream,
+                                          uint32_t counts[8]) {
+    if (!ws || !counts) return SV_ERR_INVALID_ARG;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return SV_ERR_CUDA;
+    Header h;
+    if (cudaMemcpy(&h, ws, sizeof(Header), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return SV_ERR_CUDA;
+    if (h.magic != kMagic || h.k < 1 || h.k > (uint32_t)kMaxK) return SV_ERR_INVALID_ARG;
+    uint32_t* st = new (std::nothrow) uint32_t[h.B > 0 ? h.B : 1];
+    if (!st) return SV_ERR_INVALID_ARG;
+    const cudaError_t e = cudaMemcpy(st, static_cast<const char*>(ws) + ws_seq_offset(h.B, (int)h.k),
+                                     (size_t)h.B * sizeof(uint32_t), cudaMemcpyDeviceToHost);
+    for (int i = 0; i < 8; ++i) counts[i] = 0;
+    if (e == cudaSuccess)
+        for (uint32_t b = 0; b < h.B; ++b)
+            for (int i = 0; i < 8; ++i) counts[i] += (st[b] >> i) & 1u;
+    delete[] st;
+    return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
 
 // Introspection (declared in include/specverify_debug.h): the path the one-call
 // entry points take for these sizes on the current device (1 two-kernel, 2
@@ -4014,38 +4384,9 @@ int spec_verify_debug_flat_ctas(int B, int k, int V, sv_dtype dtype) {
     if (device_setup(&sms) != SV_OK) return -1;
     if (B < 1 || k < 1 || k > kMaxK || V < 1 || (dtype != SV_BF16 && dtype != SV_F32)) return -1;
     if (choose_path(false, B, V, dtype == SV_BF16 ? 2 : 4, sms) != kPathTwoKernel) return 0;
-    if (g_flat_off.load() || g_force_rows_G.load() || g_force_rows_nt.load()) return 0;
     FlatArgs f;
     static const uint4 aligned = {};
     return flat_plan(B, k, V, dtype == SV_BF16 ? 2 : 4, &aligned, sms, &f) ? f.P : 0;
-}
-
-// Tuning hook: the cluster size of the precise-draw kernel (1, 2, 4, 8 or 16;
-// 0 for the default).
-void spec_verify_debug_precise_split(int G) {
-    if (G == 0 || G == 1 || G == 2 || G == 4 || G == 8 || G == 16) g_force_precise_split.store(G);
-}
-
-// Tuning hook: deferral of the fused kernel's precise draws and its minimum
-// dynamic shared memory per CTA (KiB, 0..160).
-void spec_verify_debug_fused_tuning(int defer_mode, int pad_kib) {
-    if (defer_mode >= 0 && defer_mode <= 2) g_fused_defer.store(defer_mode);
-    if (pad_kib >= 0 && pad_kib <= 160) g_fused_pad.store(pad_kib);
-}
-
-// Tuning hook: the row stream's split (G in 1..16, a power of two) and threads
-// per CTA (128, 256 or 512) on the two-kernel path; 0 for the automatic choice.
-void spec_verify_debug_flat(int off) { g_flat_off.store(off ? 1 : 0); }
-
-void spec_verify_debug_rows_split(int G, int nt) {
-    if (G == 0 || G == 1 || G == 2 || G == 4 || G == 8 || G == 16) g_force_rows_G.store(G);
-    if (nt == 0 || nt == 128 || nt == 256 || nt == 512 || nt == 1024) g_force_rows_nt.store(nt);
-}
-
-// Tuning hook: a fixed cluster size (1, 2, 4, 8 or 16) for the draw kernel, 0
-// for the automatic choice.  Other values are ignored.
-void spec_verify_debug_draw_split(int G) {
-    if (G == 0 || G == 1 || G == 2 || G == 4 || G == 8 || G == 16) g_force_draw_split.store(G);
 }
 
 // Test / timing hook: the first stage of the row-skipping path alone (the reset
@@ -4068,7 +4409,7 @@ sv_status spec_verify_debug_rows_skip(sv_mode mode, const void* logits, sv_dtype
     if ((st = device_setup(&sms)) != SV_OK) return st;
     if (B == 0) return SV_OK;
     return launch_rows(sampled, logits, dtype, draft_probs, draft_tokens, u_accept, T, B, k, V, ws,
-                       stream, sms, true);
+                       stream, sms, true, kAuto);
 }
 
 // Test hook: the largest relative error of ex2.approx.ftz.f32 against the

@@ -44,25 +44,22 @@ def main(argv=None):
     ws = sv.workspace(B, k, V, logits.dtype, dev)
     out = torch.empty((B, k + 1), dtype=torch.int32, device=dev)
     n = torch.empty(B, dtype=torch.int32, device=dev)
-    sv.debug_force_path(a.path)
-    try:
-        if inp.mode == "greedy":
-            for _ in range(a.reps):
-                sv.spec_verify_greedy(logits, x, out, n, ws)
-        elif a.match:
-            ua = torch.from_numpy(inp.ua).to(dev)
-            ur = torch.from_numpy(inp.ur).to(dev)
-            for _ in range(a.reps):
-                sv.spec_verify_match(logits, x, ua, ur, inp.T, out, n, ws)
-        else:
-            q = torch.from_numpy(inp.q).to(dev)
-            ua = torch.from_numpy(inp.ua).to(dev)
-            ur = torch.from_numpy(inp.ur).to(dev)
-            for _ in range(a.reps):
-                sv.spec_verify_sample(logits, q, x, ua, ur, inp.T, out, n, ws)
-        torch.cuda.synchronize(dev)
-    finally:
-        sv.debug_force_path(0)
+    tu = sv.Tuning(path=a.path) if a.path else None
+    if inp.mode == "greedy":
+        for _ in range(a.reps):
+            sv.spec_verify_greedy(logits, x, out, n, ws, tuning=tu)
+    elif a.match:
+        ua = torch.from_numpy(inp.ua).to(dev)
+        ur = torch.from_numpy(inp.ur).to(dev)
+        for _ in range(a.reps):
+            sv.spec_verify_match(logits, x, ua, ur, inp.T, out, n, ws, tuning=tu)
+    else:
+        q = torch.from_numpy(inp.q).to(dev)
+        ua = torch.from_numpy(inp.ua).to(dev)
+        ur = torch.from_numpy(inp.ur).to(dev)
+        for _ in range(a.reps):
+            sv.spec_verify_sample(logits, q, x, ua, ur, inp.T, out, n, ws, tuning=tu)
+    torch.cuda.synchronize(dev)
     st, bits, ndeg = sv.spec_verify_read_status(ws)
     print(f"{a.workload} B={B} k={k} V={V} path={a.path} match={a.match} reps={a.reps}: status {st} "
           f"bits {bits:#x} degenerate {ndeg}")

@@ -33,6 +33,15 @@ SV_NOALLOC_MAX_ROWS = 27000
 _lib = None
 
 
+class Tuning(ctypes.Structure):
+    """sv_tuning (specverify_debug.h): options of one call, for tests and tuning;
+    every field 0 is the automatic choice.  Passed as ``tuning=`` to the wrappers
+    below, it affects that call only."""
+    _fields_ = [(name, ctypes.c_int) for name in (
+        "path", "force_precise", "draw_split", "precise_split", "fused_defer",
+        "fused_pad_kib", "rows_split", "rows_threads", "flat_off")]
+
+
 class SpecVerifyError(RuntimeError):
     def __init__(self, status: int, where: str):
         super().__init__(f"{where}: {status_string(status)} (status {status})")
@@ -69,18 +78,20 @@ def load():
     lib.spec_verify_rows.restype = I
     lib.spec_verify_finish.argtypes = [I, P, I, P, P, P, P, F, I, I, I, P, P, P, Z, P]
     lib.spec_verify_finish.restype = I
-    lib.spec_verify_debug_fused_tuning.argtypes = [I, I]
-    lib.spec_verify_debug_fused_tuning.restype = None
-    lib.spec_verify_debug_rows_split.argtypes = [I, I]
-    lib.spec_verify_debug_rows_split.restype = None
-    lib.spec_verify_debug_flat.argtypes = [I]
-    lib.spec_verify_debug_flat.restype = None
     lib.spec_verify_debug_flat_ctas.argtypes = [I, I, I, I]
     lib.spec_verify_debug_flat_ctas.restype = I
-    lib.spec_verify_debug_precise_split.argtypes = [I]
-    lib.spec_verify_debug_precise_split.restype = None
-    lib.spec_verify_debug_draw_split.argtypes = [I]
-    lib.spec_verify_debug_draw_split.restype = None
+    lib.spec_verify_sample_tuned.argtypes = [P, I, P, P, P, P, F, I, I, I, P, P, P, Z, P, P, P, P]
+    lib.spec_verify_sample_tuned.restype = I
+    lib.spec_verify_greedy_tuned.argtypes = [P, I, P, I, I, I, P, P, P, Z, P, P, P, P]
+    lib.spec_verify_greedy_tuned.restype = I
+    lib.spec_verify_rows_tuned.argtypes = [I, P, I, P, P, F, I, I, I, P, Z, P, P]
+    lib.spec_verify_rows_tuned.restype = I
+    lib.spec_verify_finish_tuned.argtypes = [I, P, I, P, P, P, P, F, I, I, I, P, P, P, Z, P, P]
+    lib.spec_verify_finish_tuned.restype = I
+    lib.spec_verify_tree_tuned.argtypes = [I, P, I, P, P, P, P, P, F, I, I, I, P, P, P, P, Z, P, P]
+    lib.spec_verify_tree_tuned.restype = I
+    lib.spec_verify_match_tuned.argtypes = [P, I, P, P, P, F, I, I, I, P, P, P, Z, P, P]
+    lib.spec_verify_match_tuned.restype = I
     lib.spec_verify_debug_rows_skip.argtypes = [I, P, I, P, P, P, F, I, I, I, P, Z, P]
     lib.spec_verify_debug_rows_skip.restype = I
     lib.spec_verify_read_status.argtypes = [P, P, P, P]
@@ -93,12 +104,10 @@ def load():
     lib.spec_verify_sample_noalloc.restype = I
     lib.spec_verify_debug_ffexp.argtypes = [P, F, F, I, P, P]
     lib.spec_verify_debug_ffexp.restype = I
-    lib.spec_verify_debug_force_precise.argtypes = [I]
-    lib.spec_verify_debug_force_precise.restype = None
-    lib.spec_verify_debug_force_path.argtypes = [I]
-    lib.spec_verify_debug_force_path.restype = None
     lib.spec_verify_debug_path.argtypes = [I, I, I, I]
     lib.spec_verify_debug_path.restype = I
+    lib.spec_verify_debug_status_counts.argtypes = [P, P, P]
+    lib.spec_verify_debug_status_counts.restype = I
     lib.spec_verify_debug_ex2_error.argtypes = [F, F, P, P]
     lib.spec_verify_debug_ex2_error.restype = I
     _lib = lib
@@ -144,46 +153,64 @@ def spec_verify_workspace_size(B: int, k: int, V: int, dtype=SV_BF16) -> int:
     return int(load().spec_verify_workspace_size(B, k, V, dtype))
 
 
-def spec_verify_greedy(logits, draft_tokens, out_tokens, num_accepted, ws, stream=None):
+def _tun(tuning):
+    return None if tuning is None else ctypes.byref(tuning)
+
+
+def spec_verify_greedy(logits, draft_tokens, out_tokens, num_accepted, ws, stream=None,
+                       tuning=None):
     """logits [B,k+1,V] bf16/fp32, draft_tokens [B,k] int32 -> out_tokens [B,k+1], num_accepted [B]."""
     B, k1, V = logits.shape
-    st = load().spec_verify_greedy(_ptr(logits), _dtype(logits), _ptr(draft_tokens), B, k1 - 1, V,
-                                   _ptr(out_tokens), _ptr(num_accepted), _ptr(ws), ws.numel(),
-                                   _stream(stream))
+    args = (_ptr(logits), _dtype(logits), _ptr(draft_tokens), B, k1 - 1, V, _ptr(out_tokens),
+            _ptr(num_accepted), _ptr(ws), ws.numel())
+    if tuning is None:
+        st = load().spec_verify_greedy(*args, _stream(stream))
+    else:
+        st = load().spec_verify_greedy_tuned(*args, None, None, _stream(stream), _tun(tuning))
     _check(st, "spec_verify_greedy")
 
 
 def spec_verify_sample(logits, draft_probs, draft_tokens, u_accept, u_resample, T, out_tokens,
-                       num_accepted, ws, stream=None):
+                       num_accepted, ws, stream=None, tuning=None):
     B, k1, V = logits.shape
-    st = load().spec_verify_sample(_ptr(logits), _dtype(logits), _ptr(draft_probs),
-                                   _ptr(draft_tokens), _ptr(u_accept), _ptr(u_resample), float(T),
-                                   B, k1 - 1, V, _ptr(out_tokens), _ptr(num_accepted), _ptr(ws),
-                                   ws.numel(), _stream(stream))
+    args = (_ptr(logits), _dtype(logits), _ptr(draft_probs), _ptr(draft_tokens), _ptr(u_accept),
+            _ptr(u_resample), float(T), B, k1 - 1, V, _ptr(out_tokens), _ptr(num_accepted),
+            _ptr(ws), ws.numel())
+    if tuning is None:
+        st = load().spec_verify_sample(*args, _stream(stream))
+    else:
+        st = load().spec_verify_sample_tuned(*args, None, None, _stream(stream), _tun(tuning))
     _check(st, "spec_verify_sample")
 
 
 def spec_verify_match(logits, draft_tokens, u_draw, u_bonus, T, out_tokens, num_accepted, ws,
-                      stream=None):
+                      stream=None, tuning=None):
     """Sample-and-match verify: a target draw per position, drafts kept while equal."""
     B, k1, V = logits.shape
-    st = load().spec_verify_match(_ptr(logits), _dtype(logits), _ptr(draft_tokens), _ptr(u_draw),
-                                  _ptr(u_bonus), float(T), B, k1 - 1, V, _ptr(out_tokens),
-                                  _ptr(num_accepted), _ptr(ws), ws.numel(), _stream(stream))
+    args = (_ptr(logits), _dtype(logits), _ptr(draft_tokens), _ptr(u_draw), _ptr(u_bonus),
+            float(T), B, k1 - 1, V, _ptr(out_tokens), _ptr(num_accepted), _ptr(ws), ws.numel(),
+            _stream(stream))
+    if tuning is None:
+        st = load().spec_verify_match(*args)
+    else:
+        st = load().spec_verify_match_tuned(*args, _tun(tuning))
     _check(st, "spec_verify_match")
 
 
 def spec_verify_tree(mode, logits, draft_probs, tree_tokens, tree_parents, u_accept, u_resample,
-                     T, out_tokens, out_nodes, num_accepted, ws, stream=None):
+                     T, out_tokens, out_nodes, num_accepted, ws, stream=None, tuning=None):
     """Tree verify: logits [B, N, V], draft_probs [B, N, V] (sampled), tree_tokens and
     tree_parents [B, N] int32, u_accept [B, N], u_resample [B] -> out_tokens,
     out_nodes [B, N], num_accepted [B].  Workspace: workspace(B, N - 1, V, ...)."""
     B, N, V = logits.shape
-    st = load().spec_verify_tree(int(mode), _ptr(logits), _dtype(logits), _ptr(draft_probs),
-                                 _ptr(tree_tokens), _ptr(tree_parents), _ptr(u_accept),
-                                 _ptr(u_resample), float(T), B, N, V, _ptr(out_tokens),
-                                 _ptr(out_nodes), _ptr(num_accepted), _ptr(ws), ws.numel(),
-                                 _stream(stream))
+    args = (int(mode), _ptr(logits), _dtype(logits), _ptr(draft_probs), _ptr(tree_tokens),
+            _ptr(tree_parents), _ptr(u_accept), _ptr(u_resample), float(T), B, N, V,
+            _ptr(out_tokens), _ptr(out_nodes), _ptr(num_accepted), _ptr(ws), ws.numel(),
+            _stream(stream))
+    if tuning is None:
+        st = load().spec_verify_tree(*args)
+    else:
+        st = load().spec_verify_tree_tuned(*args, _tun(tuning))
     _check(st, "spec_verify_tree")
 
 
@@ -212,24 +239,29 @@ def stats_dict(stats):
 
 
 def spec_verify_sample_kv(logits, draft_probs, draft_tokens, u_accept, u_resample, T, out_tokens,
-                          num_accepted, ws, kv_len=None, stats=None, stream=None):
+                          num_accepted, ws, kv_len=None, stats=None, stream=None, tuning=None):
     """spec_verify_sample, then kv_len[b] += n + 1 and the stats counters, in the kernel."""
     B, k1, V = logits.shape
-    st = load().spec_verify_sample_kv(_ptr(logits), _dtype(logits), _ptr(draft_probs),
-                                      _ptr(draft_tokens), _ptr(u_accept), _ptr(u_resample),
-                                      float(T), B, k1 - 1, V, _ptr(out_tokens),
-                                      _ptr(num_accepted), _ptr(ws), ws.numel(), _ptr(kv_len),
-                                      _ptr(stats), _stream(stream))
+    args = (_ptr(logits), _dtype(logits), _ptr(draft_probs), _ptr(draft_tokens), _ptr(u_accept),
+            _ptr(u_resample), float(T), B, k1 - 1, V, _ptr(out_tokens), _ptr(num_accepted),
+            _ptr(ws), ws.numel(), _ptr(kv_len), _ptr(stats), _stream(stream))
+    if tuning is None:
+        st = load().spec_verify_sample_kv(*args)
+    else:
+        st = load().spec_verify_sample_tuned(*args, _tun(tuning))
     _check(st, "spec_verify_sample_kv")
 
 
 def spec_verify_greedy_kv(logits, draft_tokens, out_tokens, num_accepted, ws, kv_len=None,
-                          stats=None, stream=None):
+                          stats=None, stream=None, tuning=None):
     """spec_verify_greedy, then kv_len[b] += n + 1 and the stats counters, in the kernel."""
     B, k1, V = logits.shape
-    st = load().spec_verify_greedy_kv(_ptr(logits), _dtype(logits), _ptr(draft_tokens), B,
-                                      k1 - 1, V, _ptr(out_tokens), _ptr(num_accepted), _ptr(ws),
-                                      ws.numel(), _ptr(kv_len), _ptr(stats), _stream(stream))
+    args = (_ptr(logits), _dtype(logits), _ptr(draft_tokens), B, k1 - 1, V, _ptr(out_tokens),
+            _ptr(num_accepted), _ptr(ws), ws.numel(), _ptr(kv_len), _ptr(stats), _stream(stream))
+    if tuning is None:
+        st = load().spec_verify_greedy_kv(*args)
+    else:
+        st = load().spec_verify_greedy_tuned(*args, _tun(tuning))
     _check(st, "spec_verify_greedy_kv")
 
 
@@ -245,27 +277,15 @@ def spec_verify_sample_noalloc(logits, draft_probs, draft_tokens, u_accept, u_re
     _check(st, "spec_verify_sample_noalloc")
 
 
-def spec_verify_rows(mode, logits, draft_probs, draft_tokens, T, ws, stream=None):
+def spec_verify_rows(mode, logits, draft_probs, draft_tokens, T, ws, stream=None, tuning=None):
     B, k1, V = logits.shape
-    st = load().spec_verify_rows(int(mode), _ptr(logits), _dtype(logits), _ptr(draft_probs),
-                                 _ptr(draft_tokens), float(T), B, k1 - 1, V, _ptr(ws), ws.numel(),
-                                 _stream(stream))
+    args = (int(mode), _ptr(logits), _dtype(logits), _ptr(draft_probs), _ptr(draft_tokens),
+            float(T), B, k1 - 1, V, _ptr(ws), ws.numel(), _stream(stream))
+    if tuning is None:
+        st = load().spec_verify_rows(*args)
+    else:
+        st = load().spec_verify_rows_tuned(*args, _tun(tuning))
     _check(st, "spec_verify_rows")
-
-
-def debug_fused_tuning(defer_mode: int, pad_kib: int):
-    """Tuning hook of the fused kernel (precise-draw deferral, shared-memory floor)."""
-    load().spec_verify_debug_fused_tuning(int(defer_mode), int(pad_kib))
-
-
-def debug_rows_split(G: int, nt: int):
-    """Tuning hook: the row stream's split and threads per CTA (0 = automatic)."""
-    load().spec_verify_debug_rows_split(int(G), int(nt))
-
-
-def debug_flat(off: int):
-    """Test hook: 1 keeps greedy batches off the flat row stream (0 = automatic)."""
-    load().spec_verify_debug_flat(int(off))
 
 
 def debug_flat_ctas(B: int, k: int, V: int, dtype) -> int:
@@ -275,16 +295,6 @@ def debug_flat_ctas(B: int, k: int, V: int, dtype) -> int:
     if r < 0:
         raise SpecVerifyError(SV_ERR_CUDA, "spec_verify_debug_flat_ctas")
     return r
-
-
-def debug_precise_split(G: int):
-    """Tuning hook: the precise-draw kernel's cluster size (0 = default)."""
-    load().spec_verify_debug_precise_split(int(G))
-
-
-def debug_draw_split(G: int):
-    """Tuning hook: a fixed cluster size for the draw kernel (0 = automatic)."""
-    load().spec_verify_debug_draw_split(int(G))
 
 
 def debug_rows_skip(mode, logits, draft_probs, draft_tokens, u_accept, T, ws, stream=None):
@@ -298,12 +308,15 @@ def debug_rows_skip(mode, logits, draft_probs, draft_tokens, u_accept, T, ws, st
 
 
 def spec_verify_finish(mode, logits, draft_probs, draft_tokens, u_accept, u_resample, T,
-                       out_tokens, num_accepted, ws, stream=None):
+                       out_tokens, num_accepted, ws, stream=None, tuning=None):
     B, k1, V = logits.shape
-    st = load().spec_verify_finish(int(mode), _ptr(logits), _dtype(logits), _ptr(draft_probs),
-                                   _ptr(draft_tokens), _ptr(u_accept), _ptr(u_resample), float(T),
-                                   B, k1 - 1, V, _ptr(out_tokens), _ptr(num_accepted), _ptr(ws),
-                                   ws.numel(), _stream(stream))
+    args = (int(mode), _ptr(logits), _dtype(logits), _ptr(draft_probs), _ptr(draft_tokens),
+            _ptr(u_accept), _ptr(u_resample), float(T), B, k1 - 1, V, _ptr(out_tokens),
+            _ptr(num_accepted), _ptr(ws), ws.numel(), _stream(stream))
+    if tuning is None:
+        st = load().spec_verify_finish(*args)
+    else:
+        st = load().spec_verify_finish_tuned(*args, _tun(tuning))
     _check(st, "spec_verify_finish")
 
 
@@ -349,17 +362,16 @@ def debug_ffexp(l, m: float, T: float, stream=None):
     return out
 
 
-def debug_force_precise(on: bool):
-    """Test hook: every sampled draw takes the precise float-float pass."""
-    load().spec_verify_debug_force_precise(1 if on else 0)
+def debug_status_counts(ws, stream=None):
+    """Per status bit (0..7), the number of sequences of the last call on ``ws``
+    with it set; syncs the stream."""
+    counts = (ctypes.c_uint32 * 8)()
+    st = load().spec_verify_debug_status_counts(_ptr(ws), _stream(stream), counts)
+    _check(st, "spec_verify_debug_status_counts")
+    return [int(c) for c in counts]
 
 
 PATH_TWO_KERNEL, PATH_FUSED, PATH_SKIP = 1, 2, 3
-
-
-def debug_force_path(path: int):
-    """Test hook: 0 automatic, 1 two-kernel path, 2 fused kernel, 3 row-skipping path."""
-    load().spec_verify_debug_force_path(int(path))
 
 
 def debug_path(mode: int, B: int, V: int, dtype) -> int:

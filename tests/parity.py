@@ -79,8 +79,9 @@ def to_device(inp, device="cuda"):
     return d
 
 
-def run_gpu(inp, dev=None, ws=None, two_stage=False):
-    """One verify of `inp` through the C ABI.  The outputs (and the workspace,
+def run_gpu(inp, dev=None, ws=None, two_stage=False, tuning=None):
+    """One verify of `inp` through the C ABI (with the per-call options `tuning`,
+    an sv.Tuning, or the automatic choices).  The outputs (and the workspace,
     unless one is given) carry guard bytes, checked after the call."""
     from speculative_decoding_verification_18_gb300 import specverify as sv
     dev = dev or to_device(inp)
@@ -92,19 +93,21 @@ def run_gpu(inp, dev=None, ws=None, two_stage=False):
         ws = g.workspace(B, k, V, dev["logits"].dtype)
     if inp.mode == "greedy":
         if two_stage:
-            sv.spec_verify_rows(sv.SV_MODE_GREEDY, dev["logits"], None, dev["x"], 1.0, ws)
+            sv.spec_verify_rows(sv.SV_MODE_GREEDY, dev["logits"], None, dev["x"], 1.0, ws,
+                                tuning=tuning)
             sv.spec_verify_finish(sv.SV_MODE_GREEDY, dev["logits"], None, dev["x"], None, None,
-                                  1.0, out, n, ws)
+                                  1.0, out, n, ws, tuning=tuning)
         else:
-            sv.spec_verify_greedy(dev["logits"], dev["x"], out, n, ws)
+            sv.spec_verify_greedy(dev["logits"], dev["x"], out, n, ws, tuning=tuning)
     else:
         if two_stage:
-            sv.spec_verify_rows(sv.SV_MODE_SAMPLE, dev["logits"], dev["q"], dev["x"], inp.T, ws)
+            sv.spec_verify_rows(sv.SV_MODE_SAMPLE, dev["logits"], dev["q"], dev["x"], inp.T, ws,
+                                tuning=tuning)
             sv.spec_verify_finish(sv.SV_MODE_SAMPLE, dev["logits"], dev["q"], dev["x"], dev["ua"],
-                                  dev["ur"], inp.T, out, n, ws)
+                                  dev["ur"], inp.T, out, n, ws, tuning=tuning)
         else:
             sv.spec_verify_sample(dev["logits"], dev["q"], dev["x"], dev["ua"], dev["ur"], inp.T,
-                                  out, n, ws)
+                                  out, n, ws, tuning=tuning)
     torch.cuda.synchronize()
     g.check()
     st, bits, ndeg = sv.spec_verify_read_status(ws)

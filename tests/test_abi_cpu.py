@@ -129,3 +129,27 @@ def test_tree_argument_errors(lib):
     # greedy needs no q, uniforms or temperature: its errors are the others
     assert tree(mode=sv.SV_MODE_GREEDY, q=None, ua=None, ur=None, T=0.0,
                 par=None) == sv.SV_ERR_INVALID_ARG
+
+
+def test_tuning_options_are_per_call_and_checked(lib):
+    """The test and tuning options travel with the call (sv_tuning): there is no
+    process-wide setter left in the library, and an out-of-range option is an
+    argument error returned before any launch."""
+    from speculative_decoding_verification_18_gb300 import specverify as sv
+    for gone in ("spec_verify_debug_force_path", "spec_verify_debug_force_precise",
+                 "spec_verify_debug_draw_split", "spec_verify_debug_precise_split",
+                 "spec_verify_debug_rows_split", "spec_verify_debug_flat",
+                 "spec_verify_debug_fused_tuning"):
+        assert not hasattr(lib, gone), gone
+    P = 4096
+    ws = sv.spec_verify_workspace_size(2, 3, 100)
+    for bad in (dict(path=4), dict(path=-1), dict(draw_split=3), dict(precise_split=32),
+                dict(rows_split=5), dict(rows_threads=200), dict(fused_defer=3),
+                dict(fused_pad_kib=161)):
+        t = sv.Tuning(**bad)
+        st = lib.spec_verify_sample_tuned(P, sv.SV_F32, P, P, P, P, 1.0, 2, 3, 100, P, P, P, ws,
+                                          None, None, None, ctypes.byref(t))
+        assert st == sv.SV_ERR_INVALID_ARG, bad
+        st = lib.spec_verify_greedy_tuned(P, sv.SV_F32, P, 2, 3, 100, P, P, P, ws, None, None,
+                                          None, ctypes.byref(t))
+        assert st == sv.SV_ERR_INVALID_ARG, bad

@@ -30,10 +30,14 @@ def built():
 
 @pytest.fixture(params=[0, 1], ids=["flat", "per_row"])
 def flat_off(request):
+    """0: the automatic choice (the flat stream for these shapes); 1: the per-row
+    stream, through the per-call option."""
+    return request.param
+
+
+def _tuning(off):
     from speculative_decoding_verification_18_gb300 import specverify as sv
-    sv.debug_flat(request.param)
-    yield request.param
-    sv.debug_flat(0)
+    return sv.Tuning(flat_off=1) if off else None
 
 
 def _greedy(B, k, V, dtype, seed, p_argmax=0.7):
@@ -47,8 +51,8 @@ def _flat_ctas(inp):
     return sv.debug_flat_ctas(inp.B, inp.k, inp.V, inp.dtype)
 
 
-def _check(inp):
-    out, n, stats, (st, bits, _) = run_gpu(inp)
+def _check(inp, off=0):
+    out, n, stats, (st, bits, _) = run_gpu(inp, tuning=_tuning(off))
     ref = run_oracle(inp)
     rep = compare_outputs(inp, out, n, ref)
     assert rep.hard == 0 and rep.mismatched_sequences == 0, rep.hard_detail
@@ -72,7 +76,7 @@ def test_flat_matches_oracle(B, k, V, dtype, flat_off):
     inp = _greedy(B, k, V, dtype, seed=B + k + V)
     if not flat_off:
         assert _flat_ctas(inp) > 0, "shape expected on the flat stream"
-    _check(inp)
+    _check(inp, flat_off)
 
 
 def test_flat_is_taken_by_the_greedy_workload():
@@ -102,7 +106,7 @@ def test_flat_ties_across_ranges(dtype, flat_off):
     inp = VerifyInputs("greedy", dtype, B, k, V, 1.0, logits, None, x, None, None)
     if not flat_off:
         assert _flat_ctas(inp) > 0
-    out, n, stats, st, bits, ref = _check(inp)
+    out, n, stats, st, bits, ref = _check(inp, flat_off)
     assert np.array_equal(stats["argmax"], am)
 
 
@@ -121,7 +125,7 @@ def test_flat_invalid_rows_and_tokens(flat_off):
     lg[6, 3, 7] = np.nan                      # ... so this NaN row is never judged
     if not flat_off:
         assert _flat_ctas(inp) > 0
-    out, n, stats, (st, bits, _) = run_gpu(inp)
+    out, n, stats, (st, bits, _) = run_gpu(inp, tuning=_tuning(flat_off))
     ref = run_oracle(inp)
     assert np.array_equal(n, ref.n) and np.array_equal(out, ref.out)
     assert list(n[1:7]) == [-1, -1, -1, -1, -1, 0]
@@ -193,12 +197,7 @@ def test_workspace_reused_across_paths():
             assert np.array_equal(out.cpu().numpy(), ref.out), step
             continue
         inp = s_in if off is None else g_in
-        from speculative_decoding_verification_18_gb300 import specverify as svm
-        svm.debug_flat(off or 0)
-        try:
-            out, n, stats, _ = run_gpu(inp, ws=ws)
-        finally:
-            svm.debug_flat(0)
+        out, n, stats, _ = run_gpu(inp, ws=ws, tuning=_tuning(off))
         ref = run_oracle(inp)
         rep = compare_outputs(inp, out, n, ref)
         assert rep.hard == 0, (step, rep.hard_detail)

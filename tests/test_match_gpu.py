@@ -24,7 +24,7 @@ def built():
     assert torch.cuda.is_available(), "GPU tests need a CUDA device"
 
 
-def run_match(inp, dev=None):
+def run_match(inp, dev=None, tuning=None):
     from speculative_decoding_verification_18_gb300 import specverify as sv
     dev = dev or to_device(inp)
     B, k, V = inp.B, inp.k, inp.V
@@ -32,7 +32,8 @@ def run_match(inp, dev=None):
     out = g.empty((B, k + 1), torch.int32, fill=-7)
     n = g.empty((B,), torch.int32, fill=-7)
     ws = g.workspace(B, k, V, dev["logits"].dtype)
-    sv.spec_verify_match(dev["logits"], dev["x"], dev["ua"], dev["ur"], inp.T, out, n, ws)
+    sv.spec_verify_match(dev["logits"], dev["x"], dev["ua"], dev["ur"], inp.T, out, n, ws,
+                         tuning=tuning)
     torch.cuda.synchronize()
     g.check()
     st, bits, _ = sv.spec_verify_read_status(ws)
@@ -102,11 +103,7 @@ def test_match_precise_draws_only():
     from speculative_decoding_verification_18_gb300.inputs import make_inputs
     inp = make_inputs(mode="sample", B=24, k=4, V=70001, dtype="bf16", T=0.9, kind="zipf",
                       draft_sigma=0.3, seed=5)
-    sv.debug_force_precise(1)
-    try:
-        out, n, st, bits = run_match(inp)
-    finally:
-        sv.debug_force_precise(0)
+    out, n, st, bits = run_match(inp, tuning=sv.Tuning(force_precise=1))
     ref, hard, near = compare_match(inp, out, n)
     assert not hard and near <= 1
 

@@ -84,6 +84,7 @@ def test_mismatch_rate_over_a_million_rows(name):
     wss = [g.workspace(B_launch, k, V, lg.dtype) for _ in range(nl)]
     t_setup = time.perf_counter() - t0
     near = hard = differing = 0
+    precise = counted = 0  # draws that needed the float-float pass, over the first reps
     for r in range(reps):
         x = torch.from_numpy(rd.x[r]).cuda()
         ua = torch.from_numpy(rd.ua[r]).cuda()
@@ -92,6 +93,10 @@ def test_mismatch_rate_over_a_million_rows(name):
             b0, b1 = j * B_launch, (j + 1) * B_launch
             sv.spec_verify_sample(lg[b0:b1], q[b0:b1], _aligned(x[b0:b1]), _aligned(ua[b0:b1]),
                                   _aligned(ur[b0:b1]), T, outs[j], ns[j], wss[j])
+        if r < 200:
+            for j in range(nl):
+                precise += sv.debug_status_counts(wss[j])[5]
+            counted += B_big
         ref = oracle.verify_batch_stats(oracle.SAMPLE, inp.logits, inp.dtype, inp.q, rd.x[r],
                                         rd.ua[r], rd.ur[r], T, stats)
         out = torch.cat(outs).cpu().numpy()
@@ -106,7 +111,8 @@ def test_mismatch_rate_over_a_million_rows(name):
     rows = reps * per_rep
     print(f"\n{name} (path {path}): {rows} rows in {reps} x {nl} launches of B={B_launch}, "
           f"{differing} differing sequences, {near} near-threshold "
-          f"(rate {near / rows:.2e}, limit {RATE:.0e}), {hard} hard; "
+          f"(rate {near / rows:.2e}, limit {RATE:.0e}), {hard} hard; precise draws "
+          f"{precise}/{counted} ({precise / max(counted, 1):.2%}); "
           f"setup {t_setup:.1f} s, total {time.perf_counter() - t0:.1f} s")
     assert rows >= ROWS
     assert hard == 0

@@ -63,28 +63,25 @@ def test_kv_and_stats_epilogue(mode, path):
     if mode == "sample":
         inp.ur[7] = 1.5              # invalid uniform for the draw
     dev = to_device(inp)
-    sv.debug_force_path(path)
-    try:
-        ref_out, ref_n, _, _ = run_gpu(inp, dev)
-        B, k = inp.B, inp.k
-        kv0 = torch.arange(100, 100 + B, dtype=torch.int32, device="cuda")
-        gd = Guarded()
-        kv = gd.empty(B, torch.int32)
-        kv.copy_(kv0)
-        stats = gd.empty(len(sv.STATS_FIELDS), torch.int64, fill=0)
-        out = gd.empty((B, k + 1), torch.int32)
-        n = gd.empty(B, torch.int32)
-        ws = gd.workspace(B, k, inp.V, dev["logits"].dtype)
-        if mode == "sample":
-            sv.spec_verify_sample_kv(dev["logits"], dev["q"], dev["x"], dev["ua"], dev["ur"],
-                                     inp.T, out, n, ws, kv_len=kv, stats=stats)
-        else:
-            sv.spec_verify_greedy_kv(dev["logits"], dev["x"], out, n, ws, kv_len=kv,
-                                     stats=stats)
-        torch.cuda.synchronize()
-        gd.check()
-    finally:
-        sv.debug_force_path(0)
+    tu = sv.Tuning(path=path)
+    ref_out, ref_n, _, _ = run_gpu(inp, dev, tuning=tu)
+    B, k = inp.B, inp.k
+    kv0 = torch.arange(100, 100 + B, dtype=torch.int32, device="cuda")
+    gd = Guarded()
+    kv = gd.empty(B, torch.int32)
+    kv.copy_(kv0)
+    stats = gd.empty(len(sv.STATS_FIELDS), torch.int64, fill=0)
+    out = gd.empty((B, k + 1), torch.int32)
+    n = gd.empty(B, torch.int32)
+    ws = gd.workspace(B, k, inp.V, dev["logits"].dtype)
+    if mode == "sample":
+        sv.spec_verify_sample_kv(dev["logits"], dev["q"], dev["x"], dev["ua"], dev["ur"],
+                                 inp.T, out, n, ws, kv_len=kv, stats=stats, tuning=tu)
+    else:
+        sv.spec_verify_greedy_kv(dev["logits"], dev["x"], out, n, ws, kv_len=kv, stats=stats,
+                                 tuning=tu)
+    torch.cuda.synchronize()
+    gd.check()
     n = n.cpu().numpy()
     assert np.array_equal(n, ref_n) and np.array_equal(out.cpu().numpy(), ref_out)
     valid = n >= 0
