@@ -278,13 +278,15 @@ sv_status spec_verify_finish(sv_mode mode, const void* logits, sv_dtype dtype,
  *     device address (cudaGetSymbolAddress) and caches it; make that first call
  *     before any stream capture begins on that device.
  *   - Every call shares the one array and leaves its contents behind; nothing in
- *     it needs to start at zero, because each call writes every header field and
- *     row record before reading it.  Calls that overlap on the GPU (for example
- *     on two streams at once) race on the array and must be avoided.
+ *     it needs to start at zero: each call writes every header field and row
+ *     record before reading it, and clears the counters that must start at zero
+ *     itself (cudaMemsetAsync on the call's stream).  Calls that overlap on the
+ *     GPU (for example on two streams at once) race on the array and must be
+ *     avoided.
  *   - It allocates nothing and calls no allocating routine; the result and the
  *     device-detected data errors (num_accepted = -1) are as for
  *     spec_verify_sample. */
-#define SV_NOALLOC_SCRATCH_BYTES 1048576
+#define SV_NOALLOC_SCRATCH_BYTES 2097152
 #define SV_NOALLOC_MAX_ROWS 27000
 sv_status spec_verify_sample_noalloc(const void* logits, sv_dtype dtype,
                                      const float* draft_probs, const int32_t* draft_tokens,

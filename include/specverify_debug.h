@@ -44,7 +44,12 @@ sv_status spec_verify_debug_ffexp(const float* l, float m, float T, int n, doubl
  *   rows_threads   its threads per CTA (128, 256, 512 or 1024);
  *   flat_off       1: greedy batches never take the flat row stream (the whole
  *                  logits tensor cut into one equal range per resident CTA);
- *                  a fixed rows_split or rows_threads also keeps them off it. */
+ *                  a fixed rows_split or rows_threads also keeps them off it;
+ *   draw_mode      the sampled draw of the two-kernel and row-skipping paths:
+ *                  1 the split draw (slices of the decision row on separate
+ *                  CTAs, when the workspace holds its sums), 2 the cluster
+ *                  draw (one cluster per sequence); 0 automatic (the cluster
+ *                  draw). */
 typedef struct {
     int path;
     int force_precise;
@@ -55,6 +60,7 @@ typedef struct {
     int rows_split;
     int rows_threads;
     int flat_off;
+    int draw_mode;
 } sv_tuning;
 
 /* spec_verify_sample / spec_verify_sample_kv (kv_len and stats may be NULL),

@@ -114,8 +114,14 @@ __host__ __device__ inline size_t ws_stop_offset(long long B, int k) {
 __host__ __device__ inline size_t ws_plist_offset(long long B, int k) {
     return (ws_stop_offset(B, k) + (size_t)B * sizeof(uint32_t) + 15) & ~(size_t)15;
 }
-__host__ __device__ inline size_t ws_bytes_for(long long B, int k) {
-    size_t b = ws_plist_offset(B, k) + 16 + (size_t)B * sizeof(uint32_t);
+// The split draws' region follows, 16-byte aligned (its size depends on V:
+// split_ws_bytes, defined with the split draw).
+__host__ __device__ inline size_t ws_split_offset(long long B, int k) {
+    return (ws_plist_offset(B, k) + 16 + (size_t)B * sizeof(uint32_t) + 15) & ~(size_t)15;
+}
+__host__ __device__ size_t split_ws_bytes(long long B, int V);
+__host__ __device__ inline size_t ws_bytes_for(long long B, int k, int V) {
+    size_t b = ws_split_offset(B, k) + split_ws_bytes(B, V);
     return (b + 255) & ~(size_t)255;
 }
 
@@ -319,15 +325,14 @@ constexpr int kSliceMax = 163840;   // largest slice of a row one CTA draws from
 // and requires it to be at most this value, so the bound holds for every input
 // the draw can see on this GPU (inputs below -126 give 0 and are counted as 0).
 constexpr float kEx2RelErr = 1.75e-7f;
-// Relative error of one element's corrected exponential y apart from the
-// rounding of its exponent: ex2 itself, and the two roundings of the
-// first-order correction (its product and its FMA).
-constexpr float kFastEy = kEx2RelErr + 2.0f * 5.96046448e-08f;
-// The exponent a = (l - m) * log2(e)/T: the product's rounding and that of
-// log2(e)/T are recovered exactly (an FMA and the low part of log2(e)/T) and
-// corrected for; the difference l - m keeps one rounding, 2^-24 * |a|, i.e. a
-// relative 2^-24 * ln2 * |a| in 2^a.
-constexpr float kFastKappa = 5.96046448e-08f * 0.693147181f;
+// Relative error of one element's y.  The exponent's parts are all recovered:
+// l - m exactly (TwoSum), the rounding of a = (l - m) c_hi exactly (an FMA),
+// and the low part of c = log2(e)/T; their sum t (at most 3 2^-24 |a|, so below
+// 2^-15 for |a| < 126; below that y is 0) corrects ex2(a) to first order,
+// y = ex2(a) (1 + t ln2).  What is left: ex2 itself, the one rounding of that
+// FMA, and terms below 2^-33 (the second order of t ln2, the roundings inside
+// t, c's float-float residual), covered by the extra 2^-28.
+constexpr float kFastEy = kEx2RelErr + 1.0625f * 5.96046448e-08f;
 // Classes of a residual's elements, decided during the one pass with the row
 // stream's normaliser S_row in place of the pass's own S (which is checked
 // afterwards to lie within 2^-13 of S_row): p > q for sure when
@@ -428,9 +433,10 @@ constexpr int kMaxG = 16;
 struct FastTotals {
     ff S;                        // y of the elements that are not positive
     unsigned long long Y, Q;     // fixed-point sums of the positive elements' y and q
-    float A, Aq;                 // y|a| of all elements; q of the undecided ones
+    float Aq;                    // q of the undecided elements
     float qmin;                  // the smallest q (negative: the precise pass decides)
 };
+static_assert(sizeof(FastTotals) == 32, "fast totals");
 struct DrawShared {
     ff red_ff[kWarps];
     float red_f[kWarps];
@@ -767,27 +773,40 @@ constexpr int kClsZero = 0, kClsPos = 1, kClsUndecided = 2;
 constexpr int kFastGroup = 8;  // lanes (chunks of 8 elements) per block of the fast pass
 
 struct FastScale {
-    float m, chi, clo;  // row max (raw logit); log2(e)/T in float-float
+    float m, chi;       // row max (raw logit); log2(e)/T rounded to float
+    float cll, chl;     // (log2(e)/T - chi) ln2 and chi ln2, for the correction
     float ih, il;       // 1 / (S_row (1 + 2^-12)), 1 / (S_row (1 - 2^-12)) (residual draws)
     int ey;             // EY
 };
 
-// One element of the fast pass: y (the exponent's product rounding and the low
-// part of log2(e)/T corrected to first order), y |a| for the error bound, and
-// the class.  Every float operation is explicitly rounded, so the pass and the
-// owner's search compute identical values.  l = -inf gives y = 0.  A NaN q is
-// undecided (its bound is NaN, so the draw goes to the precise pass, which
-// weighs it 0); a negative q is caught by the caller.
+__device__ __forceinline__ FastScale make_fast_scale(float m, ff c2, float s_row, bool res) {
+    FastScale f;
+    f.m = m;
+    f.chi = c2.hi;
+    f.cll = __fmul_rn(c2.lo, 0.693147181f);
+    f.chl = __fmul_rn(c2.hi, 0.693147181f);
+    f.ih = res ? __frcp_rn(__fmul_rn(s_row, kClassHi)) : 0.0f;
+    f.il = res ? __frcp_rn(__fmul_rn(s_row, kClassLo)) : 0.0f;
+    f.ey = fast_ey(s_row);
+    return f;
+}
+
+// One element of the fast pass: y and the class.  d = l - m is exact; a = d
+// c_hi rounded; t = (the product's rounding + d c_lo + d_lo c_hi) ln2; y =
+// ex2(a) (1 + t).  Every float operation is explicitly rounded, so the pass and
+// the owner's search compute identical values.  l = -inf gives a NaN t and
+// y = max(NaN, 0) = 0.  A NaN q is undecided (its bound is NaN, so the draw
+// goes to the precise pass, which weighs it 0); a negative q is caught by the
+// caller.
 template <bool RES>
-__device__ __forceinline__ int fast_elem(float l, float q, const FastScale& f, float& y,
-                                         float& ya) {
-    const float dd = __fsub_rn(l, f.m);
-    const float a = __fmul_rn(dd, f.chi);
-    float err = __fmaf_rn(dd, f.chi, -a);  // exact
-    err = __fmaf_rn(dd, f.clo, err);
+__device__ __forceinline__ int fast_elem(float l, float q, const FastScale& f, float& y) {
+    const ff d = two_sum(l, -f.m);
+    const float a = __fmul_rn(d.hi, f.chi);
+    const float r = __fmaf_rn(d.hi, f.chi, -a);  // exact
+    float t = __fmaf_rn(d.hi, f.cll, __fmul_rn(d.lo, f.chl));
+    t = __fmaf_rn(r, 0.693147181f, t);
     const float y0 = ex2_approx(a);
-    y = y0 > 0.0f ? __fmaf_rn(y0, __fmul_rn(err, 0.693147181f), y0) : 0.0f;
-    ya = y > 0.0f ? __fmul_rn(y, fabsf(a)) : 0.0f;
+    y = fmaxf(__fmaf_rn(y0, t, y0), 0.0f);
     if (!RES) return kClsPos;
     if (__fmul_rn(y, f.ih) > q) return kClsPos;
     if (__fmul_rn(y, f.il) < q) return kClsZero;
@@ -854,10 +873,9 @@ struct Tree8 {
 template <int E, bool RES, bool EXACT, bool WANT>
 __device__ __forceinline__ void fast_chunk_elem(const float* l, const float* q, const FastScale& f,
                                                 ff& Y, ff& Q, Tree8& ty, Tree8& tq, Tree8& tr,
-                                                float& a, float& aq, float& qmin, float* yp,
-                                                float* qp) {
-    float y, ya;
-    const int cls = fast_elem<RES>(l[E], RES ? q[E] : 0.0f, f, y, ya);
+                                                float& aq, float& qmin, float* yp, float* qp) {
+    float y;
+    const int cls = fast_elem<RES>(l[E], RES ? q[E] : 0.0f, f, y);
     const bool pos = cls == kClsPos;
     const float yv = pos ? y : 0.0f, qv = (RES && pos) ? q[E] : 0.0f;
     if (WANT) {
@@ -872,7 +890,6 @@ __device__ __forceinline__ void fast_chunk_elem(const float* l, const float* q, 
         if (RES) tq.add<E>(qv);
     }
     tr.add<E>(pos ? 0.0f : y);
-    a = __fadd_rn(a, ya);
     if (RES) {
         aq = __fadd_rn(aq, cls == kClsUndecided ? q[E] : 0.0f);
         qmin = fminf(qmin, q[E]);
@@ -881,23 +898,22 @@ __device__ __forceinline__ void fast_chunk_elem(const float* l, const float* q, 
 
 // One chunk (8 elements, logits l and q): the fixed-point sums of the positive
 // elements' y and q (cy, cq), the other elements' y summed pairwise (returned),
-// the bound's sums into a and aq, the smallest q into qmin; with WANT, yp and
-// qp receive each element's y and q when it is positive, else 0.
+// the undecided elements' q into aq, the smallest q into qmin; with WANT, yp
+// and qp receive each element's y and q when it is positive, else 0.
 template <bool RES, bool EXACT, bool WANT>
 __device__ __forceinline__ float fast_chunk(const float* l, const float* q, const FastScale& f,
                                             unsigned long long& cy, unsigned long long& cq,
-                                            float& a, float& aq, float& qmin, float* yp,
-                                            float* qp) {
+                                            float& aq, float& qmin, float* yp, float* qp) {
     ff Y{0.0f, 0.0f}, Q{0.0f, 0.0f};
     Tree8 ty{}, tq{}, tr{};
-    fast_chunk_elem<0, RES, EXACT, WANT>(l, q, f, Y, Q, ty, tq, tr, a, aq, qmin, yp, qp);
-    fast_chunk_elem<1, RES, EXACT, WANT>(l, q, f, Y, Q, ty, tq, tr, a, aq, qmin, yp, qp);
-    fast_chunk_elem<2, RES, EXACT, WANT>(l, q, f, Y, Q, ty, tq, tr, a, aq, qmin, yp, qp);
-    fast_chunk_elem<3, RES, EXACT, WANT>(l, q, f, Y, Q, ty, tq, tr, a, aq, qmin, yp, qp);
-    fast_chunk_elem<4, RES, EXACT, WANT>(l, q, f, Y, Q, ty, tq, tr, a, aq, qmin, yp, qp);
-    fast_chunk_elem<5, RES, EXACT, WANT>(l, q, f, Y, Q, ty, tq, tr, a, aq, qmin, yp, qp);
-    fast_chunk_elem<6, RES, EXACT, WANT>(l, q, f, Y, Q, ty, tq, tr, a, aq, qmin, yp, qp);
-    fast_chunk_elem<7, RES, EXACT, WANT>(l, q, f, Y, Q, ty, tq, tr, a, aq, qmin, yp, qp);
+    fast_chunk_elem<0, RES, EXACT, WANT>(l, q, f, Y, Q, ty, tq, tr, aq, qmin, yp, qp);
+    fast_chunk_elem<1, RES, EXACT, WANT>(l, q, f, Y, Q, ty, tq, tr, aq, qmin, yp, qp);
+    fast_chunk_elem<2, RES, EXACT, WANT>(l, q, f, Y, Q, ty, tq, tr, aq, qmin, yp, qp);
+    fast_chunk_elem<3, RES, EXACT, WANT>(l, q, f, Y, Q, ty, tq, tr, aq, qmin, yp, qp);
+    fast_chunk_elem<4, RES, EXACT, WANT>(l, q, f, Y, Q, ty, tq, tr, aq, qmin, yp, qp);
+    fast_chunk_elem<5, RES, EXACT, WANT>(l, q, f, Y, Q, ty, tq, tr, aq, qmin, yp, qp);
+    fast_chunk_elem<6, RES, EXACT, WANT>(l, q, f, Y, Q, ty, tq, tr, aq, qmin, yp, qp);
+    fast_chunk_elem<7, RES, EXACT, WANT>(l, q, f, Y, Q, ty, tq, tr, aq, qmin, yp, qp);
     if (EXACT) {
         cy = ff_fixed(ff_normalize(Y), f.ey);
         cq = RES ? ff_fixed(ff_normalize(Q), 62) : 0ull;
@@ -946,7 +962,6 @@ __device__ __forceinline__ FastTotals warp_fast_totals(FastTotals t) {
         t.S = ff_add(t.S, so);
         t.Y += __shfl_xor_sync(0xffffffffu, t.Y, off);
         t.Q += __shfl_xor_sync(0xffffffffu, t.Q, off);
-        t.A += __shfl_xor_sync(0xffffffffu, t.A, off);
         t.Aq += __shfl_xor_sync(0xffffffffu, t.Aq, off);
         t.qmin = fminf(t.qmin, __shfl_xor_sync(0xffffffffu, t.qmin, off));
     }
@@ -968,47 +983,29 @@ __device__ __forceinline__ unsigned long long group_sum_u64(unsigned long long v
     return v;
 }
 
-// The fast draw by the G CTAs of a cluster (RES: the residual max(0, p - q),
-// else p).  Returns true (in every thread of every CTA) when the token is
-// certified: u C lies far enough inside the chosen bin that the exact draw
-// picks the same one.  The owner CTA then holds the token in sh.token.
-//
-// Error bound.  Each positive element's p_fast = y/S carries its own error
-// e_j <= kFastEy + kappa |a_j| and the normaliser's e_S (kFastEy + kappa A,
-// A = sum p|a|, and the roundings of its pairwise chunk sums); p_fast =
-// p (1 + eta_j) / (1 + eta_S).  The error of u C_tot - C at a bin edge is,
-// element by element, (u - 1) times the errors before the edge plus u times
-// those after it, so the elements' own errors, the undecided elements' weights
-// (at most kUndecided q) and, without EXACT, the chunk sums' three roundings
-// contribute at most max(u, 1 - u) times their sum; the normaliser's common
-// factor contributes eta_S (u P_tot - P_edge) = eta_S (u Q_tot - Q_edge +
-// (u C_tot - C_edge)), at most e_S (max(u, 1 - u) Q_tot + the bin's width).
-// The float-float sums (2^-44), M (2^-44) and the fixed-point truncations add
-// at most 2^20 + 2 (chunks) + 64 units.  The token is kept when u C lies more
-// than this bound (plus 2 units) inside both edges of its bin.
-template <typename DT, bool RES, bool EXACT>
-__device__ bool draw_fast(cg::cluster_group& cluster, DrawShared& sh, const DrawCtx<DT>& d) {
+__device__ __forceinline__ FastTotals zero_totals() {
+    return FastTotals{ff{0.0f, 0.0f}, 0ull, 0ull, 0.0f, 0.0f};
+}
+
+__device__ __forceinline__ FastTotals add_fast_totals(FastTotals t, const FastTotals& x) {
+    t.S = ff_add(t.S, x.S);
+    t.Y += x.Y;
+    t.Q += x.Q;
+    t.Aq = __fadd_rn(t.Aq, x.Aq);
+    t.qmin = fminf(t.qmin, x.qmin);
+    return t;
+}
+
+// The fast pass over the CTA's slice of the decision row (and of its q row):
+// this thread's sums.  Each warp takes 32 consecutive chunks (a chunk per lane,
+// four blocks of 8 chunks), two such rounds in flight.  With BLOCKS the sums of
+// each block (Y then Q, fixed point) go to d.bsum[blk] and d.bsum[nblk8 + blk].
+template <typename DT, bool RES, bool EXACT, bool BLOCKS>
+__device__ __forceinline__ FastTotals fast_pass(const DrawCtx<DT>& d, const FastScale& f) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int grp = lane / kFastGroup, gl = lane % kFastGroup;
-    if (tid == 0) {
-        sh.token = -1;
-        sh.cert = 0;
-    }
-    FastScale f;
-    f.m = d.m;
-    f.chi = d.c;
-    f.clo = d.clo;
-    f.ih = RES ? __frcp_rn(__fmul_rn(d.s_row, kClassHi)) : 0.0f;
-    f.il = RES ? __frcp_rn(__fmul_rn(d.s_row, kClassLo)) : 0.0f;
-    f.ey = fast_ey(d.s_row);
     const int fnb = (d.mych + kFastGroup - 1) / kFastGroup;  // blocks of this CTA's slice
-    unsigned long long* Yb = d.bsum;
-    unsigned long long* Qb = d.bsum + fnb;
-
-    // The pass: each warp takes 32 consecutive chunks (a chunk per lane, four
-    // blocks), two such rounds in flight.
-    constexpr FastTotals kZeroT{ff{0.0f, 0.0f}, 0ull, 0ull, 0.0f, 0.0f, 0.0f};
-    FastTotals t = kZeroT;
+    FastTotals t = zero_totals();
     constexpr int UB = 2;
     for (int base0 = warp * 32; base0 < d.mych; base0 += UB * kThreads) {
         RawQ rq[UB];
@@ -1030,39 +1027,250 @@ __device__ bool draw_fast(cg::cluster_group& cluster, DrawShared& sh, const Draw
                 float l[kChunk], q[kChunk] = {};
                 raw_unpack(rl[u], l);
                 if (RES) raw_unpack_q(rq[u], q);
-                const float rest = fast_chunk<RES, EXACT, false>(l, q, f, cy, cq, t.A, t.Aq,
-                                                                 t.qmin, nullptr, nullptr);
+                const float rest =
+                    fast_chunk<RES, EXACT, false>(l, q, f, cy, cq, t.Aq, t.qmin, nullptr, nullptr);
                 ff_acc1(t.S, rest);
             }
             t.Y += cy;
             t.Q += cq;
-            const unsigned long long by = group_sum_u64(cy);
-            const unsigned long long bq = RES ? group_sum_u64(cq) : 0ull;
-            const int blk = (base + grp * kFastGroup) / kFastGroup;
-            if (gl == 0 && blk < fnb) {
-                Yb[blk] = by;
-                Qb[blk] = bq;
+            if (BLOCKS) {
+                const unsigned long long by = group_sum_u64(cy);
+                const unsigned long long bq = RES ? group_sum_u64(cq) : 0ull;
+                const int blk = (base + grp * kFastGroup) / kFastGroup;
+                if (gl == 0 && blk < fnb) {
+                    d.bsum[blk] = by;
+                    d.bsum[fnb + blk] = bq;
+                }
             }
         }
     }
-    // The CTA's totals, pushed to slot [rank] of every CTA of the cluster.
+    return t;
+}
+
+// The CTA's totals of the fast pass, left in *out (shared memory) for every
+// thread after the barrier at the end.
+__device__ __forceinline__ void cta_fast_totals(DrawShared& sh, FastTotals t, FastTotals* out) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     t = warp_fast_totals(t);
     if (lane == 0) sh.red_t[warp] = t;
     __syncthreads();
     if (warp == 0) {
-        FastTotals c = lane < kWarps ? sh.red_t[lane] : kZeroT;
+        FastTotals c = lane < kWarps ? sh.red_t[lane] : zero_totals();
         c = warp_fast_totals(c);
-        if (lane < d.G) *cluster.map_shared_rank(&sh.xT[d.rank], lane) = c;
+        if (lane == 0) *out = c;
     }
+    __syncthreads();
+}
+
+// The normaliser, the check against S_row, M = floor(2^(123 - EY) / S), C_tot,
+// tau = floor(u C_tot) and the error bound's parts from a row's totals.
+//
+// Error bound.  Each positive element's p_fast = y/S carries its own error
+// eta_j <= kFastEy (ex2 and the correction's FMA) and the normaliser's common
+// eta_S <= e_S (kFastEy, and without EXACT the roundings of the pairwise chunk
+// sums, 3 2^-24); p_fast = p (1 + eta_j) / (1 + eta_S).  The error of
+// u C_tot - C at a bin edge is, element by element, (u - 1) times the errors
+// before the edge plus u times those after it, so the elements' own errors,
+// the undecided elements' weights (at most kUndecided q) and, without EXACT, the
+// chunk sums' three roundings contribute at most max(u, 1 - u) times their sum;
+// the normaliser's common factor contributes eta_S (u P_tot - P_edge) = eta_S
+// (u Q_tot - Q_edge + (u C_tot - C_edge)), at most e_S (max(u, 1 - u) Q_tot +
+// the bin's width).  The float-float sums (2^-44), M (2^-44) and the
+// fixed-point truncations add at most 2^20 + 2 (chunks) + 64 units.  The token
+// is kept when u C lies more than this bound (plus 2 units) inside both edges
+// of its bin.
+struct FastBound {
+    unsigned long long M, tau;
+    float D, eS;
+    bool ok;
+};
+template <bool EXACT>
+__device__ __forceinline__ FastBound fast_bound(const FastTotals& tot, float s_row, float u,
+                                                int ey, long long nch) {
+    FastBound fb;
+    const unsigned long long Yall = tot.Y, Qall = tot.Q;
+    const float pw = __int_as_float((127 - ey) << 23);  // 2^-EY
+    const ff Yf = u64_to_ff(Yall);
+    const ff S = ff_normalize(ff_add(ff{__fmul_rn(Yf.hi, pw), __fmul_rn(Yf.lo, pw)}, tot.S));
+    bool ok = tot.qmin >= 0.0f && S.hi > 0.0f &&
+              fabsf(__fsub_rn(S.hi, s_row)) <= S.hi * (float)kRowSigma;
+    // M = floor(2^(123 - EY) / S): below 2^63 once S is within 2^-13 of S_row
+    fb.M = ok ? ff_fixed(ff_recip(S), 123 - ey) : 0ull;
+    const long long Ctot = ok ? fast_cval(Yall, Qall, fb.M) : 0ll;
+    ok = ok && Ctot > 0;
+    fb.tau = ok ? scale_floor(u, (unsigned long long)Ctot) : 0ull;
+    fb.ok = ok;
+    // The bound's parts (fractions of the total mass of p; float sums of
+    // positive terms, inflated for their own roundings).
+    constexpr float u24 = 5.96046448e-08f;
+    const float invS = __frcp_rn(S.hi);
+    const float Ppos = __fmul_rn(__fmul_rn(Yf.hi, pw), invS);
+    const float Qpos = __fmul_rn(u64_to_ff(Qall).hi, 2.16840434e-19f);  // 2^-62
+    fb.eS = kFastEy + 3.0f * u24 * (EXACT ? fmaxf(0.0f, 1.0f - Ppos) : 1.0f);
+    fb.D = (kFastEy * Ppos + fb.eS * Qpos + kUndecided * tot.Aq +
+            (EXACT ? 0.0f : 3.0f * u24 * (Ppos + Qpos))) *
+               1.004f * 4.611686018427388e18f +
+           1048576.0f + 2.0f * (float)nch + 64.0f;
+    return fb;
+}
+
+// The owner CTA's search: given M, tau, D, e_S and the starting point (Y0, Q0)
+// of its slice, find the block from the block sums in d.bsum, then the
+// element, and certify it.  Every thread of the CTA calls it; sh.token and
+// sh.cert hold the result after the last barrier.
+template <typename DT, bool RES, bool EXACT>
+__device__ __forceinline__ void fast_search(DrawShared& sh, const DrawCtx<DT>& d,
+                                            const FastScale& f, unsigned long long M,
+                                            unsigned long long tau, unsigned long long Y0,
+                                            unsigned long long Q0, float D, float eS) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int fnb = (d.mych + kFastGroup - 1) / kFastGroup;
+    const unsigned long long* Yb = d.bsum;
+    const unsigned long long* Qb = d.bsum + fnb;
+    // The block: each thread sums a contiguous range of block sums; a block
+    // scan of (Y, Q) gives each range's start; the first range whose end
+    // passes tau holds the block.
+    const int L = (fnb + kThreads - 1) / kThreads;
+    const int cb = min(fnb, tid * L), ce = min(fnb, cb + L);
+    unsigned long long my = 0ull, mq = 0ull;
+    for (int i = cb; i < ce; ++i) {
+        my += Yb[i];
+        mq += Qb[i];
+    }
+    unsigned long long iy = my, iq = mq;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const unsigned long long yo = __shfl_up_sync(0xffffffffu, iy, off);
+        const unsigned long long qo = __shfl_up_sync(0xffffffffu, iq, off);
+        if (lane >= off) {
+            iy += yo;
+            iq += qo;
+        }
+    }
+    if (lane == 31) {
+        sh.red_u[warp] = iy;
+        sh.woff[warp] = iq;
+    }
+    if (tid == 0) {
+        sh.token = -1;
+        sh.cert = 0;
+    }
+    __syncthreads();
+    unsigned long long wy = 0ull, wq = 0ull;  // totals of the warps before this one
+    for (int w = 0; w < warp; ++w) {
+        wy += sh.red_u[w];
+        wq += sh.woff[w];
+    }
+    const unsigned long long sy0 = Y0 + wy + iy - my, sq0 = Q0 + wq + iq - mq;
+    const bool past = ce > cb && fast_cval(sy0 + my, sq0 + mq, M) > (long long)tau;
+    const unsigned bw = __ballot_sync(0xffffffffu, past);
+    if (lane == 0) sh.red_f[warp] = bw ? (float)(__ffs(bw) - 1) : -1.0f;
+    __syncthreads();
+    int first = -1;  // the first thread (by index) whose range passes tau
+    for (int w = 0; w < kWarps && first < 0; ++w)
+        if (sh.red_f[w] >= 0.0f) first = w * 32 + (int)sh.red_f[w];
+    if (tid == first) {
+        unsigned long long ry = sy0, rq = sq0;
+        int i = cb;
+        for (; i < ce - 1; ++i) {
+            if (fast_cval(ry + Yb[i], rq + Qb[i], M) > (long long)tau) break;
+            ry += Yb[i];
+            rq += Qb[i];
+        }
+        sh.blk = i;
+        sh.f_bY = ry;
+        sh.f_bQ = rq;
+    }
+    __syncthreads();
+    if (first >= 0 && warp == 0) {  // (first < 0 is not reachable: the slice's end passes tau)
+        // The element: lanes 0..7 take the block's chunks in the pass's
+        // arithmetic (the same fixed-point values as the block sums); the
+        // first lane whose end passes tau walks its elements.
+        const int ci = sh.blk * kFastGroup + lane;
+        float l[kChunk], q[kChunk] = {}, yp[kChunk] = {}, qp[kChunk] = {};
+        unsigned long long cy = 0ull, cq = 0ull;
+        if (lane < kFastGroup && ci < d.mych) {
+            RawL<DT> rl;
+            raw_load_l(d, ci, rl);
+            raw_unpack(rl, l);
+            if (RES) {
+                RawQ rq;
+                raw_load_q(d, ci, rq);
+                raw_unpack_q(rq, q);
+            }
+            float a1 = 0.0f, a2 = 0.0f;
+            (void)fast_chunk<RES, EXACT, true>(l, q, f, cy, cq, a1, a2, yp, qp);
+        }
+        unsigned long long iy2 = cy, iq2 = cq;
+#pragma unroll
+        for (int off = 1; off < kFastGroup; off <<= 1) {
+            const unsigned long long yo = __shfl_up_sync(0xffffffffu, iy2, off);
+            const unsigned long long qo = __shfl_up_sync(0xffffffffu, iq2, off);
+            if (lane >= off) {
+                iy2 += yo;
+                iq2 += qo;
+            }
+        }
+        const unsigned long long ly = sh.f_bY + iy2 - cy, lq = sh.f_bQ + iq2 - cq;
+        const bool lp = lane < kFastGroup && ci < d.mych &&
+                        fast_cval(ly + cy, lq + cq, M) > (long long)tau;
+        const unsigned bl = __ballot_sync(0xffffffffu, lp);
+        if (bl && lane == __ffs(bl) - 1) {
+            long long lo = fast_cval(ly, lq, M), hi = lo;
+            int tok = -1;
+#pragma unroll
+            for (int e = 0; e < kChunk; ++e) {
+                if (tok >= 0 || !(yp[e] > 0.0f)) continue;  // weight 0: never chosen
+                unsigned long long py, pq;
+                fast_prefix<RES, EXACT>(yp, qp, e, f, py, pq);
+                const long long h = fast_cval(ly + py, lq + pq, M);
+                if (h > (long long)tau) {
+                    tok = e;
+                    hi = h;
+                } else {
+                    lo = h;
+                }
+            }
+            int ok = 0;
+            if (tok >= 0) {
+                const float um = fmaxf(d.u, __fsub_rn(1.0f, d.u));
+                const float dp = um * D + eS * 1.004f * (float)(hi - lo) + 2.0f;
+                const long long Dp = (long long)fminf(dp, 4.0e18f) + 1ll;
+                ok = ((long long)tau - lo >= Dp && hi - (long long)tau > Dp) ? 1 : 0;
+                sh.token = (int)((d.c0 + ci) * kChunk + tok);
+            }
+            sh.cert = ok;
+        }
+    }
+    __syncthreads();
+}
+
+// The fast draw by the G CTAs of a cluster (RES: the residual max(0, p - q),
+// else p).  Returns true (in every thread of every CTA) when the token is
+// certified: u C lies far enough inside the chosen bin that the exact draw
+// picks the same one (the bound of fast_bound).  The owner CTA then holds the
+// token in sh.token.
+template <typename DT, bool RES, bool EXACT>
+__device__ bool draw_fast(cg::cluster_group& cluster, DrawShared& sh, const DrawCtx<DT>& d) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) {
+        sh.token = -1;
+        sh.cert = 0;
+    }
+    const FastScale f = make_fast_scale(d.m, d.c2, d.s_row, RES);
+    const FastTotals t = fast_pass<DT, RES, EXACT, true>(d, f);
+    // The CTA's totals, pushed to slot [rank] of every CTA of the cluster.
+    cta_fast_totals(sh, t, &sh.red_t[0]);
+    if (warp == 0 && lane < d.G) *cluster.map_shared_rank(&sh.xT[d.rank], lane) = sh.red_t[0];
     xsync(cluster, d.G);
 
-    // Every CTA, from the same slots in the same order: the totals, the check
-    // of S against S_row, M, C_tot, u C_tot, the owning rank and this rank's
-    // starting point.  Float, float-float and integer arithmetic only.
+    // Every CTA, from the same slots in the same order: the totals, the bound,
+    // the owning rank and this rank's starting point.  Float, float-float and
+    // integer arithmetic only.
     if (warp == 0) {
         // Every lane adds the G slots in rank order (no shuffles: a lone warp's
         // shuffles right after the barrier measured several microseconds here).
-        FastTotals tot = kZeroT;
+        FastTotals tot = zero_totals();
         unsigned long long ybef = 0ull, qbef = 0ull, yend = 0ull, qend = 0ull;
         for (int r = 0; r < d.G; ++r) {
             const FastTotals x = sh.xT[r];
@@ -1070,175 +1278,34 @@ __device__ bool draw_fast(cg::cluster_group& cluster, DrawShared& sh, const Draw
                 ybef = tot.Y;
                 qbef = tot.Q;
             }
-            tot.S = ff_add(tot.S, x.S);
-            tot.Y += x.Y;
-            tot.Q += x.Q;
-            tot.A += x.A;
-            tot.Aq += x.Aq;
-            tot.qmin = fminf(tot.qmin, x.qmin);
+            tot = add_fast_totals(tot, x);
             if (r == lane) {  // lane r: the sums up to and including rank r
                 yend = tot.Y;
                 qend = tot.Q;
             }
         }
-        const unsigned long long Yall = tot.Y, Qall = tot.Q;
-        // S = Yall 2^-EY + the other elements' sum
-        const float pw = __int_as_float((127 - f.ey) << 23);  // 2^-EY
-        const ff Yf = u64_to_ff(Yall);
-        const ff S = ff_normalize(ff_add(ff{__fmul_rn(Yf.hi, pw), __fmul_rn(Yf.lo, pw)}, tot.S));
-        bool ok = tot.qmin >= 0.0f && S.hi > 0.0f &&
-                  fabsf(__fsub_rn(S.hi, d.s_row)) <= S.hi * (float)kRowSigma;
-        // M = floor(2^(123 - EY) / S): below 2^63 once S is within 2^-13 of S_row
-        const unsigned long long M = ok ? ff_fixed(ff_recip(S), 123 - f.ey) : 0ull;
-        const long long Ctot = ok ? fast_cval(Yall, Qall, M) : 0ll;
-        ok = ok && Ctot > 0;
-        const unsigned long long tau = ok ? scale_floor(d.u, (unsigned long long)Ctot) : 0ull;
-        const bool past = lane < d.G && ok && fast_cval(yend, qend, M) > (long long)tau;
+        const FastBound fb =
+            fast_bound<EXACT>(tot, d.s_row, d.u, f.ey, ((long long)d.V + kChunk - 1) / kChunk);
+        const bool past = lane < d.G && fb.ok && fast_cval(yend, qend, fb.M) > (long long)fb.tau;
         const unsigned ballot = __ballot_sync(0xffffffffu, past);
         const int owner = ballot ? __ffs(ballot) - 1 : -1;
         if (lane == 0) {
-            sh.f_ok = ok && owner >= 0;
+            sh.f_ok = fb.ok && owner >= 0;
             sh.f_owner = owner;
-            sh.f_M = M;
-            sh.f_tau = tau;
+            sh.f_M = fb.M;
+            sh.f_tau = fb.tau;
             sh.f_Y = ybef;
             sh.f_Q = qbef;
-            // The bound's parts (fractions of the total mass of p; float sums of
-            // positive terms, inflated for their own roundings; the positive
-            // elements' share of sum p|a| is bounded by all of it).
-            constexpr float u24 = 5.96046448e-08f;
-            const float invS = __frcp_rn(S.hi);
-            const float Ppos = __fmul_rn(__fmul_rn(Yf.hi, pw), invS);
-            const float Qpos = __fmul_rn(u64_to_ff(Qall).hi, 2.16840434e-19f);  // 2^-62
-            const float eS = kFastEy + kFastKappa * (tot.A * invS) * 1.001f +
-                             3.0f * u24 * (EXACT ? fmaxf(0.0f, 1.0f - Ppos) : 1.0f);
-            sh.f_eS = eS;
-            sh.f_D = (kFastEy * Ppos + kFastKappa * (tot.A * invS) * 1.001f + eS * Qpos +
-                      kUndecided * tot.Aq + (EXACT ? 0.0f : 3.0f * u24 * (Ppos + Qpos))) *
-                         1.004f * 4.611686018427388e18f +
-                     1048576.0f + 2.0f * (float)d.mych * (float)d.G + 64.0f;
+            sh.f_eS = fb.eS;
+            sh.f_D = fb.D;
         }
     }
     __syncthreads();
     if (!sh.f_ok) return false;  // uniform across the cluster
-    const unsigned long long M = sh.f_M, tau = sh.f_tau;
 
     int cert = 1;
     if (d.rank == sh.f_owner) {  // uniform across the CTA
-        // The block: each thread sums a contiguous range of block sums; a block
-        // scan of (Y, Q) gives each range's start; the first range whose end
-        // passes tau holds the block.
-        const int L = (fnb + kThreads - 1) / kThreads;
-        const int cb = min(fnb, tid * L), ce = min(fnb, cb + L);
-        unsigned long long my = 0ull, mq = 0ull;
-        for (int i = cb; i < ce; ++i) {
-            my += Yb[i];
-            mq += Qb[i];
-        }
-        unsigned long long iy = my, iq = mq;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const unsigned long long yo = __shfl_up_sync(0xffffffffu, iy, off);
-            const unsigned long long qo = __shfl_up_sync(0xffffffffu, iq, off);
-            if (lane >= off) {
-                iy += yo;
-                iq += qo;
-            }
-        }
-        if (lane == 31) {
-            sh.red_u[warp] = iy;
-            sh.woff[warp] = iq;
-        }
-        __syncthreads();
-        unsigned long long wy = 0ull, wq = 0ull;  // totals of the warps before this one
-        for (int w = 0; w < warp; ++w) {
-            wy += sh.red_u[w];
-            wq += sh.woff[w];
-        }
-        const unsigned long long sy0 = sh.f_Y + wy + iy - my, sq0 = sh.f_Q + wq + iq - mq;
-        const bool past = ce > cb && fast_cval(sy0 + my, sq0 + mq, M) > (long long)tau;
-        const unsigned bw = __ballot_sync(0xffffffffu, past);
-        if (lane == 0) sh.red_f[warp] = bw ? (float)(__ffs(bw) - 1) : -1.0f;
-        __syncthreads();
-        int first = -1;  // the first thread (by index) whose range passes tau
-        for (int w = 0; w < kWarps && first < 0; ++w)
-            if (sh.red_f[w] >= 0.0f) first = w * 32 + (int)sh.red_f[w];
-        if (tid == first) {
-            unsigned long long ry = sy0, rq = sq0;
-            int i = cb;
-            for (; i < ce - 1; ++i) {
-                if (fast_cval(ry + Yb[i], rq + Qb[i], M) > (long long)tau) break;
-                ry += Yb[i];
-                rq += Qb[i];
-            }
-            sh.blk = i;
-            sh.f_bY = ry;
-            sh.f_bQ = rq;
-        }
-        __syncthreads();
-        if (first < 0) {
-            cert = 0;  // not reachable: the owner's end passes tau
-        } else if (warp == 0) {
-            // The element: lanes 0..7 take the block's chunks in the pass's
-            // arithmetic (the same fixed-point values as the block sums); the
-            // first lane whose end passes tau walks its elements.
-            const int ci = sh.blk * kFastGroup + lane;
-            float l[kChunk], q[kChunk] = {}, yp[kChunk] = {}, qp[kChunk] = {};
-            unsigned long long cy = 0ull, cq = 0ull;
-            if (lane < kFastGroup && ci < d.mych) {
-                RawL<DT> rl;
-                raw_load_l(d, ci, rl);
-                raw_unpack(rl, l);
-                if (RES) {
-                    RawQ rq;
-                    raw_load_q(d, ci, rq);
-                    raw_unpack_q(rq, q);
-                }
-                float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f;
-                (void)fast_chunk<RES, EXACT, true>(l, q, f, cy, cq, a0, a1, a2, yp, qp);
-            }
-            unsigned long long iy2 = cy, iq2 = cq;
-#pragma unroll
-            for (int off = 1; off < kFastGroup; off <<= 1) {
-                const unsigned long long yo = __shfl_up_sync(0xffffffffu, iy2, off);
-                const unsigned long long qo = __shfl_up_sync(0xffffffffu, iq2, off);
-                if (lane >= off) {
-                    iy2 += yo;
-                    iq2 += qo;
-                }
-            }
-            const unsigned long long ly = sh.f_bY + iy2 - cy, lq = sh.f_bQ + iq2 - cq;
-            const bool lp = lane < kFastGroup && ci < d.mych &&
-                            fast_cval(ly + cy, lq + cq, M) > (long long)tau;
-            const unsigned bl = __ballot_sync(0xffffffffu, lp);
-            if (bl && lane == __ffs(bl) - 1) {
-                long long lo = fast_cval(ly, lq, M), hi = lo;
-                int tok = -1;
-#pragma unroll
-                for (int e = 0; e < kChunk; ++e) {
-                    if (tok >= 0 || !(yp[e] > 0.0f)) continue;  // weight 0: never chosen
-                    unsigned long long py, pq;
-                    fast_prefix<RES, EXACT>(yp, qp, e, f, py, pq);
-                    const long long h = fast_cval(ly + py, lq + pq, M);
-                    if (h > (long long)tau) {
-                        tok = e;
-                        hi = h;
-                    } else {
-                        lo = h;
-                    }
-                }
-                int ok = 0;
-                if (tok >= 0) {
-                    const float um = fmaxf(d.u, __fsub_rn(1.0f, d.u));
-                    const float dp = um * sh.f_D + sh.f_eS * 1.004f * (float)(hi - lo) + 2.0f;
-                    const long long Dp = (long long)fminf(dp, 4.0e18f) + 1ll;
-                    ok = ((long long)tau - lo >= Dp && hi - (long long)tau > Dp) ? 1 : 0;
-                    sh.token = (int)((d.c0 + ci) * kChunk + tok);
-                }
-                sh.cert = ok;
-            }
-        }
-        __syncthreads();
+        fast_search<DT, RES, EXACT>(sh, d, f, sh.f_M, sh.f_tau, sh.f_Y, sh.f_Q, sh.f_D, sh.f_eS);
         cert = sh.cert;
     }
     if (d.G > 1) {
@@ -2893,29 +2960,28 @@ struct FinishArgs {
 // EXACT: the fast draw's chunk sums in float-float (small batches, whose
 // precise draws run here); else pairwise (large batches, whose precise draws
 // go to sv_precise_kernel in one wave, so a few more of them cost little).
-template <typename DT, bool EXACT>
-__global__ void __launch_bounds__(kThreads, 2) sv_finish_sample_kernel(FinishArgs a) {
-    extern __shared__ __align__(16) unsigned char dyn[];
-    __shared__ DrawShared ds;
-    __shared__ RowRec recs[kMaxK + 1];
-    __shared__ float uas[kMaxK];
-    __shared__ uint32_t codes[kMaxK];
-    __shared__ float s_ur;
-    __shared__ int s_n, s_bits;
-    cg::cluster_group cluster = cg::this_cluster();
+// The scan of sequence b over its row records, by every thread of the CTA:
+// each row's test in parallel ("Decodificação especulativa explicada",
+// §"A regra de amostragem por rejeição": accept x_i when p >= q or u < p/q),
+// then the first row that stops the scan.  Leaves the records, the decision
+// row n and the error bits (0: a valid sequence) in `sc`.
+struct ScanShared {
+    RowRec recs[kMaxK + 1];
+    float uas[kMaxK];
+    uint32_t codes[kMaxK];
+    float ur;
+    int n, bits;
+};
+__device__ __forceinline__ void scan_sequence(ScanShared& sc, const RowRec* rows, const float* ua,
+                                              const float* ur, int b, int k) {
     const int tid = threadIdx.x;
-    const int G = a.G;
-    const int b = blockIdx.x / G;
-    const int rank = blockIdx.x % G;
-    const int k = a.k, V = a.V;
-    asm volatile("griddepcontrol.wait;" ::: "memory");  // the row records are complete
-    for (int i = tid; i <= k; i += kThreads) recs[i] = a.rows[(long long)b * (k + 1) + i];
-    for (int i = tid; i < k; i += kThreads) uas[i] = a.ua[(long long)b * k + i];
-    if (tid == kThreads - 1) s_ur = a.ur[b];
+    for (int i = tid; i <= k; i += blockDim.x) sc.recs[i] = rows[(long long)b * (k + 1) + i];
+    for (int i = tid; i < k; i += blockDim.x) sc.uas[i] = ua[(long long)b * k + i];
+    if (tid == blockDim.x - 1) sc.ur = ur[b];
     __syncthreads();
-    for (int i = tid; i < k; i += kThreads) {  // each row's test, in parallel
-        const RowRec& r = recs[i];
-        const float u = uas[i];
+    for (int i = tid; i < k; i += blockDim.x) {  // each row's test, in parallel
+        const RowRec& r = sc.recs[i];
+        const float u = sc.uas[i];
         uint32_t c;
         if (r.flags & (kRowBad | kRowSkipped)) {  // a skipped row is never reached
             c = kCodeError | SV_DEV_BAD_ROW;
@@ -2929,24 +2995,42 @@ __global__ void __launch_bounds__(kThreads, 2) sv_finish_sample_kernel(FinishArg
             const float P = (float)r.px, Q = r.qx;
             c = ((P >= Q) || (u < __fdiv_rn(P, Q))) ? kCodeAccept : kCodeReject;
         }
-        codes[i] = c;
+        sc.codes[i] = c;
     }
     __syncthreads();
     if (tid == 0) {  // the first row that stops the scan
         int bits = 0, n = k;
         for (int i = 0; i < k; ++i) {
-            const uint32_t c = codes[i];
+            const uint32_t c = sc.codes[i];
             if (c == kCodeAccept) continue;
             if (c & kCodeError) bits = (int)(c & ~kCodeError);
             else n = i;
             break;
         }
-        if (!bits && (recs[n].flags & (kRowBad | kRowSkipped))) bits = SV_DEV_BAD_ROW;
-        if (!bits && !(s_ur >= 0.0f && s_ur < 1.0f)) bits = SV_DEV_BAD_UNIFORM;
-        s_n = n;
-        s_bits = bits;
+        if (!bits && (sc.recs[n].flags & (kRowBad | kRowSkipped))) bits = SV_DEV_BAD_ROW;
+        if (!bits && !(sc.ur >= 0.0f && sc.ur < 1.0f)) bits = SV_DEV_BAD_UNIFORM;
+        sc.n = n;
+        sc.bits = bits;
     }
     __syncthreads();
+}
+
+template <typename DT, bool EXACT>
+__global__ void __launch_bounds__(kThreads, 2) sv_finish_sample_kernel(FinishArgs a) {
+    extern __shared__ __align__(16) unsigned char dyn[];
+    __shared__ DrawShared ds;
+    __shared__ ScanShared sc;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int tid = threadIdx.x;
+    const int G = a.G;
+    const int b = blockIdx.x / G;
+    const int rank = blockIdx.x % G;
+    const int k = a.k, V = a.V;
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the row records are complete
+    scan_sequence(sc, a.rows, a.ua, a.ur, b, k);
+    const RowRec* recs = sc.recs;
+    const int s_n = sc.n, s_bits = sc.bits;
+    const float s_ur = sc.ur;
     const int n = s_n;
     int32_t* o = a.out + (long long)b * (k + 1);
     if (s_bits) {
@@ -3031,6 +3115,490 @@ __global__ void __launch_bounds__(kThreads, 2) sv_precise_kernel(PreciseArgs a) 
         if (rank == 0 && tid == 0 && degenerate)
             a.seqstat[b] = SV_DEV_PRECISE | SV_DEV_DEGENERATE;
         cluster.sync();  // the exchange slots serve the next draw
+    }
+}
+
+// ------------------------------------------------------------------ split draw
+//
+// The draw of a sampled verify with each decision row cut into NS slices, one
+// CTA per slice and no cluster, so that a batch's draws spread over every SM in
+// small, equal pieces.  Every CTA runs its sequence's scan from the row records,
+// then the fast pass over its slice, and leaves the slice's sums in the
+// workspace.  The CTA that completes a sequence's set (an arrival counter: the
+// last to arrive sees NS - 1) finishes the draw: the totals and the bound of
+// fast_bound, the owning slice (a prefix over the slices' sums), and the
+// owner's block and element by the owner slice's pass repeated with block sums
+// (the same arithmetic, so its values agree with the slice's sums exactly).  A
+// draw the bound cannot certify is listed for the split precise draw, which
+// runs in the same fashion in two launches: the float-float normaliser's
+// slice sums, then each slice's fixed-point weight total, the last CTA of an
+// entry finding the token.  No CTA waits for another: the arrival counter
+// only tells the last one that the others' sums are in memory.
+
+constexpr int kSplitTarget = 1024;      // CTAs a fast split draw aims for
+constexpr int kSplitMinChunks = 128;    // smallest slice (chunks of 8 elements)
+constexpr int kSplitMaxChunks = 8192;   // largest slice (its block sums fit 16 KiB)
+constexpr int kSplitMaxSlices = kThreads;
+constexpr int kPreciseMinChunks = 256;  // precise slices: at least 2048 elements
+constexpr int kPreciseMaxChunks = 2048; // and at most 16384
+
+// Slices per sequence of the fast split draw: about kSplitTarget CTAs in all,
+// slices between kSplitMinChunks and kSplitMaxChunks chunks, at most
+// kSplitMaxSlices.  Returns the slice length in chunks in *sc.
+__host__ __device__ inline int split_slices(int B, int V, int* sc) {
+    const long long nch = ((long long)V + kChunk - 1) / kChunk;
+    long long ns = (kSplitTarget + (long long)B - 1) / (B > 0 ? B : 1);
+    const long long lo = (nch + kSplitMaxChunks - 1) / kSplitMaxChunks;
+    const long long hi = (nch + kSplitMinChunks - 1) / kSplitMinChunks;
+    if (ns > hi) ns = hi;
+    if (ns < lo) ns = lo;
+    if (ns > kSplitMaxSlices) ns = kSplitMaxSlices;
+    if (ns < 1) ns = 1;
+    long long c = (nch + ns - 1) / ns;
+    if (c < 1) c = 1;
+    *sc = (int)c;
+    return (int)((nch + c - 1) / c);
+}
+// Slices per draw of the split precise pass: about 2 CTAs per SM's worth of
+// items when an eighth of the batch needs the precise pass, slices between
+// kPreciseMinChunks and kPreciseMaxChunks chunks (the owner's repeat stays short).
+__host__ __device__ inline int precise_slices(int B, int V, int* sc) {
+    const long long nch = ((long long)V + kChunk - 1) / kChunk;
+    const long long expect = B / 8 > 1 ? B / 8 : 1;
+    long long ns = (512 + expect - 1) / expect;
+    const long long lo = (nch + kPreciseMaxChunks - 1) / kPreciseMaxChunks;
+    const long long hi = (nch + kPreciseMinChunks - 1) / kPreciseMinChunks;
+    if (ns > hi) ns = hi;
+    if (ns < lo) ns = lo;
+    if (ns > kSplitMaxSlices) ns = kSplitMaxSlices;
+    if (ns < 1) ns = 1;
+    long long c = (nch + ns - 1) / ns;
+    if (c < 1) c = 1;
+    *sc = (int)c;
+    return (int)((nch + c - 1) / c);
+}
+// The split draws' part of the workspace (after the list of precise draws):
+// B fast arrival counters (zeroed with the list's counter, which they follow),
+// B precise arrival counters, B * NS slice sums, B * NSP precise partials
+// (a float-float normaliser part and a weight total each).
+constexpr long long kSplitMaxTotal = 16384;  // slices of a launch (bounds the workspace)
+__host__ __device__ inline bool split_fits(long long B, int V) {
+    int sc = 0, scp = 0;
+    return B > 0 && B * split_slices((int)B, V, &sc) <= kSplitMaxTotal &&
+           B * precise_slices((int)B, V, &scp) <= kSplitMaxTotal;
+}
+__host__ __device__ size_t split_ws_bytes(long long B, int V) {
+    if (!split_fits(B, V)) return 0;
+    int sc = 0, scp = 0;
+    const int ns = split_slices((int)B, V, &sc), nsp = precise_slices((int)B, V, &scp);
+    size_t b = (size_t)B * 2 * sizeof(uint32_t);
+    b = (b + 15) & ~(size_t)15;
+    b += (size_t)B * ns * sizeof(FastTotals);
+    b += (size_t)B * nsp * (sizeof(ff) + sizeof(unsigned long long));
+    return b;
+}
+
+struct SplitArgs {
+    const void* logits;
+    const float* q;
+    const int32_t* x;
+    const float* ua;
+    const float* ur;
+    const RowRec* rows;
+    uint32_t* seqstat;
+    int32_t* out;
+    int32_t* nacc;
+    uint32_t* plist_count;  // the draws for the precise pass (count, entries)
+    uint32_t* plist;
+    uint32_t* arrive;       // [B] slices done per sequence (zero before the launch)
+    uint32_t* parrive;      // [B] per entry of the list (zeroed when it is listed)
+    FastTotals* srec;       // [B * NS] the slices' sums
+    Epilogue ep;
+    int B, k, V, NS, SC;    // slices per sequence, chunks per slice
+    int force_precise;
+    ff c2;
+};
+
+// A slice of the decision row as a draw context (rank 0 of a cluster of one).
+template <typename DT>
+__device__ __forceinline__ DrawCtx<DT> slice_ctx(unsigned char* dyn, const DT* rowp,
+                                                 const float* qrow, bool residual, int V, float m,
+                                                 ff c2, float u, long long c0, int mych,
+                                                 float s_row) {
+    DrawCtx<DT> d;
+    d.rowp = rowp;
+    d.qrow = qrow;
+    d.V = V;
+    d.residual = residual;
+    d.m = m;
+    d.c = c2.hi;
+    d.clo = c2.lo;
+    d.c2 = c2;
+    d.u = u;
+    d.c0 = c0;
+    d.mych = mych > 0 ? mych : 0;
+    d.nblk = (d.mych + kBlockChunks - 1) / kBlockChunks;
+    d.al_l = (reinterpret_cast<uintptr_t>(rowp) & 15) == 0;
+    d.al_q = residual && (reinterpret_cast<uintptr_t>(qrow) & 15) == 0;
+    d.rank = 0;
+    d.G = 1;
+    d.bsum = reinterpret_cast<unsigned long long*>(dyn);
+    d.thi = nullptr;
+    d.tlo = nullptr;
+    d.s_row = s_row;
+    d.ecache = nullptr;
+    d.pY = nullptr;
+    d.pQ = nullptr;
+    d.pamb = nullptr;
+    return d;
+}
+
+// 32-byte slice sums read past L1 (another SM wrote them).
+__device__ __forceinline__ FastTotals load_totals_cg(const FastTotals* p) {
+    const uint4* v = reinterpret_cast<const uint4*>(p);
+    const uint4 x = __ldcg(v), y = __ldcg(v + 1);
+    FastTotals t;
+    t.S.hi = __uint_as_float(x.x);
+    t.S.lo = __uint_as_float(x.y);
+    t.Y = ((unsigned long long)x.w << 32) | x.z;
+    t.Q = ((unsigned long long)y.y << 32) | y.x;
+    t.Aq = __uint_as_float(y.z);
+    t.qmin = __uint_as_float(y.w);
+    return t;
+}
+
+struct SplitShared {
+    FastTotals tot;
+    unsigned long long woffY[kWarps], woffQ[kWarps];
+    unsigned long long M, tau, Y0, Q0;
+    float D, eS;
+    int ok, owner, last;
+};
+
+// Dynamic shared memory of the fast split draw: the owner slice's block sums.
+__host__ __device__ inline size_t split_smem_bytes(int SC) {
+    return (size_t)((SC + kFastGroup - 1) / kFastGroup) * 2 * sizeof(unsigned long long);
+}
+
+template <typename DT, bool EXACT>
+__global__ void __launch_bounds__(kThreads, 2) sv_split_draw_kernel(SplitArgs a) {
+    extern __shared__ __align__(16) unsigned char dyn[];
+    __shared__ DrawShared ds;
+    __shared__ ScanShared sc;
+    __shared__ SplitShared ss;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int NS = a.NS;
+    const int b = blockIdx.x / NS, s = blockIdx.x % NS;
+    const int k = a.k, V = a.V;
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the row records are complete
+    scan_sequence(sc, a.rows, a.ua, a.ur, b, k);
+    const int n = sc.n;
+    int32_t* o = a.out + (long long)b * (k + 1);
+    if (sc.bits) {  // an invalid sequence: no draw (every slice returns here)
+        if (s == 0) {
+            for (int i = tid; i <= k; i += kThreads) o[i] = -1;
+            if (tid == 0) {
+                a.nacc[b] = -1;
+                a.seqstat[b] = (uint32_t)sc.bits;
+                commit_sequence(a.ep, b, -1, k);
+            }
+        }
+        return;
+    }
+    const bool res = n < k;
+    const DT* drow = static_cast<const DT*>(a.logits) + ((long long)b * (k + 1) + n) * V;
+    const float* qrow = res ? a.q + ((long long)b * k + n) * V : nullptr;
+    const long long nch = ((long long)V + kChunk - 1) / kChunk;
+    const float m = sc.recs[n].mraw, s_row = sc.recs[n].S, u = sc.ur;
+    const FastScale f = make_fast_scale(m, a.c2, s_row, res);
+    {
+        const long long c0 = (long long)s * a.SC;
+        const DrawCtx<DT> d = slice_ctx<DT>(dyn, drow, qrow, res, V, m, a.c2, u, c0,
+                                            (int)min((long long)a.SC, nch - c0), s_row);
+        FastTotals t = zero_totals();
+        if (!a.force_precise)
+            t = res ? fast_pass<DT, true, EXACT, false>(d, f) : fast_pass<DT, false, EXACT, false>(d, f);
+        cta_fast_totals(ds, t, &ss.tot);
+    }
+    if (tid == 0) {
+        a.srec[(long long)b * NS + s] = ss.tot;
+        __threadfence();
+        ss.last = atomicAdd(&a.arrive[b], 1u) == (uint32_t)(NS - 1);
+    }
+    __syncthreads();
+    if (!ss.last) return;
+
+    // ---- the last CTA of the sequence: the totals, the owning slice, the token
+    __threadfence();
+    if (tid == 0) a.arrive[b] = 0;  // for the next call on this workspace
+    FastTotals mine = tid < NS ? load_totals_cg(a.srec + (long long)b * NS + tid) : zero_totals();
+    if (tid >= NS) mine.qmin = 0.0f;
+    // Exclusive prefix of (Y, Q) over the slices (one slice per thread).
+    unsigned long long iy = mine.Y, iq = mine.Q;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const unsigned long long yo = __shfl_up_sync(0xffffffffu, iy, off);
+        const unsigned long long qo = __shfl_up_sync(0xffffffffu, iq, off);
+        if (lane >= off) {
+            iy += yo;
+            iq += qo;
+        }
+    }
+    if (lane == 31) {
+        ss.woffY[warp] = iy;
+        ss.woffQ[warp] = iq;
+    }
+    cta_fast_totals(ds, mine, &ss.tot);  // (its barriers also publish woff*)
+    unsigned long long wy = 0ull, wq = 0ull;
+    for (int w = 0; w < warp; ++w) {
+        wy += ss.woffY[w];
+        wq += ss.woffQ[w];
+    }
+    const unsigned long long yend = wy + iy, qend = wq + iq;  // through this slice
+    const FastBound fb = fast_bound<EXACT>(ss.tot, s_row, u, f.ey, nch);
+    const bool past = !a.force_precise && fb.ok && tid < NS &&
+                      fast_cval(yend, qend, fb.M) > (long long)fb.tau;
+    const unsigned bw = __ballot_sync(0xffffffffu, past);
+    if (lane == 0) ds.red_f[warp] = bw ? (float)(__ffs(bw) - 1) : -1.0f;
+    __syncthreads();
+    int owner = -1;
+    for (int w = 0; w < kWarps && owner < 0; ++w)
+        if (ds.red_f[w] >= 0.0f) owner = w * 32 + (int)ds.red_f[w];
+    if (tid == owner) {
+        ss.Y0 = yend - mine.Y;
+        ss.Q0 = qend - mine.Q;
+    }
+    __syncthreads();
+    bool cert = false;
+    int token = -1;
+    if (owner >= 0) {  // uniform across the CTA
+        const long long c0 = (long long)owner * a.SC;
+        const DrawCtx<DT> d = slice_ctx<DT>(dyn, drow, qrow, res, V, m, a.c2, u, c0,
+                                            (int)min((long long)a.SC, nch - c0), s_row);
+        if (res) {
+            (void)fast_pass<DT, true, EXACT, true>(d, f);
+            __syncthreads();
+            fast_search<DT, true, EXACT>(ds, d, f, fb.M, fb.tau, ss.Y0, ss.Q0, fb.D, fb.eS);
+        } else {
+            (void)fast_pass<DT, false, EXACT, true>(d, f);
+            __syncthreads();
+            fast_search<DT, false, EXACT>(ds, d, f, fb.M, fb.tau, ss.Y0, ss.Q0, fb.D, fb.eS);
+        }
+        cert = ds.cert != 0 && ds.token >= 0;
+        token = ds.token;
+    }
+    for (int i = tid; i <= k; i += kThreads)
+        if (i != n) o[i] = i < n ? a.x[(long long)b * k + i] : -1;
+    if (tid == 0) {
+        if (cert) o[n] = token;
+        a.nacc[b] = n;
+        a.seqstat[b] = cert ? 0u : SV_DEV_PRECISE;
+        commit_sequence(a.ep, b, n, k);
+        if (!cert) {
+            const uint32_t j = atomicAdd(a.plist_count, 1u);
+            if (j < (uint32_t)a.B) {  // at most B entries
+                a.parrive[j] = 0u;
+                a.plist[j] = (uint32_t)b;
+            }
+        }
+    }
+}
+
+// ---- the split precise draw
+struct SplitPreciseArgs {
+    const void* logits;
+    const float* q;
+    const float* ur;
+    const RowRec* rows;
+    const int32_t* nacc;
+    const uint32_t* plist_count;
+    const uint32_t* plist;
+    uint32_t* parrive;            // [B] per list entry
+    ff* spart;                    // [B * NSP] the slices' float-float normaliser parts
+    unsigned long long* wpart;    // [B * NSP] the slices' weight totals
+    uint32_t* seqstat;
+    int32_t* out;
+    int B, k, V, NSP, SCP;
+    ff c2;
+};
+
+__device__ __forceinline__ void load_exp_table(float* thi, float* tlo) {
+    for (int i = threadIdx.x; i < kExpTable; i += blockDim.x) {
+        thi[i] = g_exp2_table.hi[i];
+        tlo[i] = g_exp2_table.lo[i];
+    }
+    __syncthreads();
+}
+
+// Dynamic shared memory of the precise split kernels: the 2^(i/1024) table and
+// the block sums of a slice (or, for a draw from p after a residual without
+// mass, of the whole row).
+__host__ __device__ inline size_t split_precise_smem_bytes(int V, int SCP) {
+    const long long nch = ((long long)V + kChunk - 1) / kChunk;
+    const long long c = nch > SCP ? nch : SCP;
+    return 2 * kExpTable * sizeof(float) +
+           (size_t)((c + kBlockChunks - 1) / kBlockChunks) * sizeof(unsigned long long);
+}
+
+template <typename DT>
+__device__ __forceinline__ DrawCtx<DT> precise_slice_ctx(unsigned char* dyn, const SplitPreciseArgs& a,
+                                                         int b, int n, long long c0, int mych) {
+    const int k = a.k, V = a.V;
+    const DT* drow = static_cast<const DT*>(a.logits) + ((long long)b * (k + 1) + n) * V;
+    const float* qrow = n < k ? a.q + ((long long)b * k + n) * V : nullptr;
+    const RowRec& rec = a.rows[(long long)b * (k + 1) + n];
+    DrawCtx<DT> d = slice_ctx<DT>(dyn + 2 * kExpTable * sizeof(float), drow, qrow, n < k, V,
+                                  rec.mraw, a.c2, a.ur[b], c0, mych, rec.S);
+    d.thi = reinterpret_cast<float*>(dyn);
+    d.tlo = d.thi + kExpTable;
+    return d;
+}
+
+// First launch: each (entry, slice) item's float-float normaliser part.
+template <typename DT>
+__global__ void __launch_bounds__(kThreads, 2) sv_split_precise_a_kernel(SplitPreciseArgs a) {
+    extern __shared__ __align__(16) unsigned char dyn[];
+    __shared__ ff red[kWarps];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the list is complete
+    const uint32_t cnt = min(*a.plist_count, (uint32_t)a.B);
+    const long long items = (long long)cnt * a.NSP;
+    if (blockIdx.x >= items) return;
+    load_exp_table(reinterpret_cast<float*>(dyn), reinterpret_cast<float*>(dyn) + kExpTable);
+    const long long nch = ((long long)a.V + kChunk - 1) / kChunk;
+    for (long long it = blockIdx.x; it < items; it += gridDim.x) {
+        const int j = (int)(it / a.NSP), s = (int)(it % a.NSP);
+        const int b = (int)a.plist[j];
+        const int n = a.nacc[b];
+        const long long c0 = (long long)s * a.SCP;
+        const DrawCtx<DT> d =
+            precise_slice_ctx<DT>(dyn, a, b, n, c0, (int)min((long long)a.SCP, nch - c0));
+        ff acc = warp_sum_ff(ff_normalize(precise_pass_a<DT, false>(d)));
+        if (lane == 0) red[warp] = acc;
+        __syncthreads();
+        if (warp == 0) {
+            ff w = lane < kWarps ? red[lane] : ff{0.0f, 0.0f};
+            w = warp_sum_ff(w);
+            if (lane == 0) a.spart[(long long)j * a.NSP + s] = ff_normalize(w);
+        }
+        __syncthreads();
+    }
+}
+
+// Second launch: each item's weight total; the last item of an entry to finish
+// finds the token.
+template <typename DT>
+__global__ void __launch_bounds__(kThreads, 2) sv_split_precise_b_kernel(SplitPreciseArgs a) {
+    extern __shared__ __align__(16) unsigned char dyn[];
+    __shared__ DrawShared ds;
+    __shared__ unsigned long long woff[kWarps];
+    __shared__ int s_last, s_owner;
+    __shared__ unsigned long long s_pre;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the normaliser parts are complete
+    const uint32_t cnt = min(*a.plist_count, (uint32_t)a.B);
+    const long long items = (long long)cnt * a.NSP;
+    if (blockIdx.x >= items) return;
+    load_exp_table(reinterpret_cast<float*>(dyn), reinterpret_cast<float*>(dyn) + kExpTable);
+    const long long nch = ((long long)a.V + kChunk - 1) / kChunk;
+    cg::cluster_group cluster = cg::this_cluster();
+    for (long long it = blockIdx.x; it < items; it += gridDim.x) {
+        const int j = (int)(it / a.NSP), s = (int)(it % a.NSP);
+        const int b = (int)a.plist[j];
+        const int n = a.nacc[b];
+        const bool res = n < a.k;
+        // S in one fixed order (every CTA of the entry computes the same value)
+        ff S{0.0f, 0.0f};
+        for (int i = 0; i < a.NSP; ++i) S = ff_add(S, a.spart[(long long)j * a.NSP + i]);
+        const ff inv = ff_recip(ff_normalize(S));
+        long long c0 = (long long)s * a.SCP;
+        DrawCtx<DT> d = precise_slice_ctx<DT>(dyn, a, b, n, c0, (int)min((long long)a.SCP, nch - c0));
+        unsigned long long t = res ? precise_pass_b<DT, true, false, false>(d, inv)
+                                   : precise_pass_b<DT, false, false, false>(d, inv);
+        t = warp_sum(t);
+        if (lane == 0) woff[warp] = t;
+        __syncthreads();
+        if (tid == 0) {
+            unsigned long long tot = 0ull;
+            for (int w = 0; w < kWarps; ++w) tot += woff[w];
+            a.wpart[(long long)j * a.NSP + s] = tot;
+            __threadfence();
+            s_last = atomicAdd(&a.parrive[j], 1u) == (uint32_t)(a.NSP - 1);
+        }
+        __syncthreads();
+        if (!s_last) continue;
+        // ---- the last item of entry j: the owning slice, then its block and element
+        __threadfence();
+        const unsigned long long mine =
+            tid < a.NSP ? __ldcg(a.wpart + (long long)j * a.NSP + tid) : 0ull;
+        unsigned long long incl = mine;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const unsigned long long o = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += o;
+        }
+        if (lane == 31) woff[warp] = incl;
+        __syncthreads();
+        unsigned long long wb = 0ull, total = 0ull;
+        for (int w = 0; w < kWarps; ++w) {
+            if (w < warp) wb += woff[w];
+            total += woff[w];
+        }
+        const unsigned long long pre = wb + incl - mine;  // weight of the slices before
+        const unsigned long long tau = scale_floor(d.u, total);
+        if (tid == 0) s_owner = -1;
+        __syncthreads();
+        if (total > 0 && tid < a.NSP && mine > 0 && pre <= tau && tau - pre < mine) {
+            s_owner = tid;  // exactly one slice holds tau
+            s_pre = pre;
+        }
+        if (tid == 0) ds.token = -1;
+        __syncthreads();
+        bool degenerate = false;
+        if (total == 0) {
+            // The residual has no mass (reachable only through rounding or an
+            // unnormalised q): draw from p over the whole row (counted).
+            DrawCtx<DT> w = precise_slice_ctx<DT>(dyn, a, b, n, 0, (int)nch);
+            w.residual = false;
+            draw_precise<DT>(cluster, ds, w, degenerate);
+            degenerate = true;
+        } else if (s_owner >= 0) {
+            c0 = (long long)s_owner * a.SCP;
+            d = precise_slice_ctx<DT>(dyn, a, b, n, c0, (int)min((long long)a.SCP, nch - c0));
+            if (res) (void)precise_pass_b<DT, true, false, false>(d, inv);
+            else (void)precise_pass_b<DT, false, false, false>(d, inv);
+            __syncthreads();
+            const unsigned long long want = tau - s_pre;
+            int blk;
+            unsigned long long bbefore;
+            find_block(ds, d.bsum, d.nblk, want, &blk, &bbefore);
+            if (warp == 0) {
+                const int ci = blk * kBlockChunks + lane;
+                float l[kChunk] = {}, q[kChunk] = {};
+                unsigned long long W = 0;
+                if (ci < d.mych) {
+                    load_l(d, ci, l);
+                    load_q(d, ci, res, q);
+                    W = res ? precise_chunk<DT, true, false, false>(d, ci, l, q, inv, 0ull, nullptr)
+                            : precise_chunk<DT, false, false, false>(d, ci, l, q, inv, 0ull, nullptr);
+                }
+                const unsigned long long wb2 = want - bbefore;
+                unsigned long long cb;
+                if (find_lane(W, wb2, &cb)) {
+                    int tok = -1;
+                    if (res) precise_chunk<DT, true, false, false>(d, ci, l, q, inv, wb2 - cb, &tok);
+                    else precise_chunk<DT, false, false, false>(d, ci, l, q, inv, wb2 - cb, &tok);
+                    if (tok >= 0) ds.token = (int)((d.c0 + ci) * kChunk + tok);
+                }
+            }
+        }
+        __syncthreads();
+        if (tid == 0) {
+            if (ds.token >= 0) a.out[(long long)b * (a.k + 1) + n] = ds.token;
+            if (degenerate) a.seqstat[b] = SV_DEV_PRECISE | SV_DEV_DEGENERATE;
+            a.parrive[j] = 0u;
+        }
+        __syncthreads();
     }
 }
 
@@ -3269,7 +3837,7 @@ static ff log2e_over(float T) {
 // automatic choices, for the entry points of specverify.h; the caller's for
 // the _tuned entry points, so that a test's or a tuning script's setting
 // affects its own calls only.
-static const sv_tuning kAuto = {0, 0, 0, 0, 0, 0, 0, 0, 0};
+static const sv_tuning kAuto = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
 
 
 struct DeviceInfo {
@@ -3335,6 +3903,10 @@ static sv_status device_setup(int* sms) {
             SV_TRY(cluster_attrs(sv_match_draw_kernel<__nv_bfloat16>, true));
             SV_TRY(cluster_attrs(sv_match_draw_kernel<float>, true));
             SV_TRY(cluster_attrs(sv_precise_kernel<float>, true));
+            SV_TRY(cluster_attrs(sv_split_precise_a_kernel<__nv_bfloat16>, true));
+            SV_TRY(cluster_attrs(sv_split_precise_a_kernel<float>, true));
+            SV_TRY(cluster_attrs(sv_split_precise_b_kernel<__nv_bfloat16>, true));
+            SV_TRY(cluster_attrs(sv_split_precise_b_kernel<float>, true));
             SV_TRY(cluster_attrs(sv_rows_kernel<__nv_bfloat16, true, 128>, false));
             SV_TRY(cluster_attrs(sv_rows_kernel<__nv_bfloat16, true, 256>, false));
             SV_TRY(cluster_attrs(sv_rows_kernel<__nv_bfloat16, true, 512>, false));
@@ -3397,7 +3969,7 @@ static sv_status check_common(const void* logits, sv_dtype dt, const int32_t* x,
     if (B > 0 && (!aligned16(logits) || !aligned16(x))) return SV_ERR_INVALID_ARG;
     if (!ws) return SV_ERR_WORKSPACE;
     if (!aligned16(ws)) return SV_ERR_INVALID_ARG;
-    if (ws_bytes < ws_bytes_for(B, k)) return SV_ERR_WORKSPACE;
+    if (ws_bytes < ws_bytes_for(B, k, V)) return SV_ERR_WORKSPACE;
     return SV_OK;
 }
 
@@ -3710,6 +4282,91 @@ static int draw_split_wide(int B, int V, int sms) {
     return G;
 }
 
+// The split draw of a sampled verify: a memset of the list's counter and the
+// arrival counters, sv_split_draw_kernel (B * NS CTAs), then the two precise
+// launches (persistent, 2 CTAs per SM; they return at once when no draw was
+// listed), each a programmatic dependent of the one before.
+static sv_status launch_split(const void* logits, sv_dtype dt, const float* q, const int32_t* x,
+                              const float* ua, const float* ur, float T, int B, int k, int V,
+                              int32_t* out, int32_t* nacc, void* ws, cudaStream_t stream, int sms,
+                              Epilogue ep, const sv_tuning& tu) {
+    char* w = static_cast<char*>(ws);
+    SplitArgs a;
+    a.logits = logits;
+    a.q = q;
+    a.x = x;
+    a.ua = ua;
+    a.ur = ur;
+    a.rows = reinterpret_cast<const RowRec*>(w + ws_rows_offset());
+    a.seqstat = reinterpret_cast<uint32_t*>(w + ws_seq_offset(B, k));
+    a.out = out;
+    a.nacc = nacc;
+    a.plist_count = reinterpret_cast<uint32_t*>(w + ws_plist_offset(B, k));
+    a.plist = a.plist_count + 4;
+    a.arrive = reinterpret_cast<uint32_t*>(w + ws_split_offset(B, k));
+    a.parrive = a.arrive + B;
+    const size_t srec_off = (ws_split_offset(B, k) + (size_t)B * 2 * sizeof(uint32_t) + 15) &
+                            ~(size_t)15;
+    a.srec = reinterpret_cast<FastTotals*>(w + srec_off);
+    a.ep = ep;
+    a.B = B;
+    a.k = k;
+    a.V = V;
+    a.NS = split_slices(B, V, &a.SC);
+    a.force_precise = tu.force_precise != 0;
+    a.c2 = log2e_over(T);
+    // the list's counter, its entries and the arrival counters, in one memset
+    const size_t zlen = ws_split_offset(B, k) + (size_t)B * sizeof(uint32_t) - ws_plist_offset(B, k);
+    if (cudaMemsetAsync(a.plist_count, 0, zlen, stream) != cudaSuccess) return SV_ERR_CUDA;
+    cudaError_t e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((long long)B * a.NS), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = split_smem_bytes(a.SC);
+    cfg.stream = stream;
+    e = dt == SV_BF16 ? cudaLaunchKernelEx(&cfg, sv_split_draw_kernel<__nv_bfloat16, true>, a)
+                      : cudaLaunchKernelEx(&cfg, sv_split_draw_kernel<float, true>, a);
+    if (e != cudaSuccess) return SV_ERR_CUDA;
+
+    SplitPreciseArgs pa;
+    pa.logits = logits;
+    pa.q = q;
+    pa.ur = ur;
+    pa.rows = a.rows;
+    pa.nacc = nacc;
+    pa.plist_count = a.plist_count;
+    pa.plist = a.plist;
+    pa.parrive = a.parrive;
+    pa.seqstat = a.seqstat;
+    pa.out = out;
+    pa.B = B;
+    pa.k = k;
+    pa.V = V;
+    pa.NSP = precise_slices(B, V, &pa.SCP);
+    pa.c2 = a.c2;
+    pa.spart = reinterpret_cast<ff*>(w + srec_off + (size_t)B * a.NS * sizeof(FastTotals));
+    pa.wpart = reinterpret_cast<unsigned long long*>(pa.spart + (size_t)B * pa.NSP);
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1] = cluster_attr(1);
+    cudaLaunchConfig_t pc = {};
+    const long long maxitems = (long long)B * pa.NSP;
+    pc.gridDim = dim3((unsigned)std::min<long long>(2LL * sms, maxitems), 1, 1);
+    pc.blockDim = dim3(kThreads, 1, 1);
+    pc.dynamicSmemBytes = split_precise_smem_bytes(V, pa.SCP);
+    pc.stream = stream;
+    pc.attrs = attr;
+    pc.numAttrs = 1;
+    e = dt == SV_BF16 ? cudaLaunchKernelEx(&pc, sv_split_precise_a_kernel<__nv_bfloat16>, pa)
+                      : cudaLaunchKernelEx(&pc, sv_split_precise_a_kernel<float>, pa);
+    if (e != cudaSuccess) return SV_ERR_CUDA;
+    pc.numAttrs = 2;
+    e = dt == SV_BF16 ? cudaLaunchKernelEx(&pc, sv_split_precise_b_kernel<__nv_bfloat16>, pa)
+                      : cudaLaunchKernelEx(&pc, sv_split_precise_b_kernel<float>, pa);
+    return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
 // `wide`: the draw kernel of a large batch (draw_split_wide), else seq_split.
 static sv_status launch_finish(bool sampled, const void* logits, sv_dtype dt, const float* q,
                                const int32_t* x, const float* ua, const float* ur, float T,
@@ -3735,6 +4392,9 @@ static sv_status launch_finish(bool sampled, const void* logits, sv_dtype dt, co
                                ep);
         return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
     }
+    if (tu.draw_mode == 1 && split_fits(B, V))
+        return launch_split(logits, dt, q, x, ua, ur, T, B, k, V, out, nacc, ws, stream, sms, ep,
+                            tu);
     FinishArgs a;
     a.ep = ep;
     a.logits = logits;
@@ -3979,7 +4639,7 @@ extern "C" {
 size_t spec_verify_workspace_size(int B, int k, int V, sv_dtype dtype) {
     if (B < 0 || k < 1 || V < 1 || k > kMaxK || V > kMaxV) return 0;
     if (dtype != SV_BF16 && dtype != SV_F32) return 0;
-    return ws_bytes_for(B, k);
+    return ws_bytes_for(B, k, V);
 }
 
 }  // extern "C"
@@ -3993,7 +4653,8 @@ static bool tuning_valid(const sv_tuning& t) {
            pow2(t.rows_split) && t.fused_defer >= 0 && t.fused_defer <= 2 &&
            t.fused_pad_kib >= 0 && t.fused_pad_kib <= 160 &&
            (t.rows_threads == 0 || t.rows_threads == 128 || t.rows_threads == 256 ||
-            t.rows_threads == 512 || t.rows_threads == 1024);
+            t.rows_threads == 512 || t.rows_threads == 1024) &&
+           t.draw_mode >= 0 && t.draw_mode <= 2;
 }
 
 static sv_status rows_impl(sv_mode mode, const void* logits, sv_dtype dtype,
@@ -4439,7 +5100,11 @@ namespace sv {
 
 constexpr size_t kNoAllocScratchBytes = SV_NOALLOC_SCRATCH_BYTES;
 static_assert(kNoAllocScratchBytes >= 256 + 32 * (size_t)SV_NOALLOC_MAX_ROWS +
-                                          12 * (size_t)(SV_NOALLOC_MAX_ROWS / 2) + 31 + 255,
+                                          12 * (size_t)(SV_NOALLOC_MAX_ROWS / 2) + 31 +
+                                          8 * (size_t)(SV_NOALLOC_MAX_ROWS / 2) + 31 +
+                                          (size_t)kSplitMaxTotal *
+                                              (sizeof(FastTotals) + sizeof(ff) + 8) +
+                                          255,
               "scratch size");
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];

@@ -37,7 +37,13 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_workspace_size(lib):
     from speculative_decoding_verification_18_gb300 import specverify as sv
-    assert sv.spec_verify_workspace_size(64, 4, 32000) == 256 + 64 * 5 * 32 + 64 * 4 * 3 + 256
+    # header, 5 row records per sequence, status and stop words, the precise
+    # list (a 16-byte counter and B entries); then the split draw's arrival
+    # counters (2B words), 16 slice sums of 32 bytes and 16 precise parts of 16
+    # bytes per sequence (V = 32000: 4000 chunks, 16 slices of 250); rounded to 256
+    base = 256 + 64 * 5 * 32 + 64 * 4 * 2 + 16 + 64 * 4
+    split = 64 * 2 * 4 + 64 * 16 * 32 + 64 * 16 * 16
+    assert sv.spec_verify_workspace_size(64, 4, 32000) == -(-(base + split) // 256) * 256
     assert sv.spec_verify_workspace_size(1, 1, 1) == 512
     assert sv.spec_verify_workspace_size(0, 4, 10) == 512
     assert sv.spec_verify_workspace_size(1, 0, 10) == 0
@@ -145,7 +151,7 @@ def test_tuning_options_are_per_call_and_checked(lib):
     ws = sv.spec_verify_workspace_size(2, 3, 100)
     for bad in (dict(path=4), dict(path=-1), dict(draw_split=3), dict(precise_split=32),
                 dict(rows_split=5), dict(rows_threads=200), dict(fused_defer=3),
-                dict(fused_pad_kib=161)):
+                dict(fused_pad_kib=161), dict(draw_mode=3)):
         t = sv.Tuning(**bad)
         st = lib.spec_verify_sample_tuned(P, sv.SV_F32, P, P, P, P, 1.0, 2, 3, 100, P, P, P, ws,
                                           None, None, None, ctypes.byref(t))

@@ -4,7 +4,9 @@ The GPU's fast draw ("Decodificação especulativa explicada", §"A regra de
 amostragem por rejeição": the residual norm(max(0, p - q)) at a rejection, p
 itself for the bonus; the categorical rule of §"Amostragem especulativa em
 numpy, com prova") forms each p from one fp32 hardware exponential whose
-relative error is only bounded (1.75e-7, checked exhaustively on the GPU),
+relative error is only bounded (1.75e-7, checked exhaustively on the GPU)
+and whose exponent is otherwise exact to first order (l - m by TwoSum, the
+product's rounding and log2(e)/T's low part recovered),
 sums the positive elements' y and q without rounding error that matters, and
 keeps its token only when u C lies farther than an error bound D from both
 edges of the chosen bin.  This test restates that arithmetic in Python: float32
@@ -25,8 +27,7 @@ import pytest
 
 E = 1.75e-7                    # the assumed worst relative error of ex2.approx (kEx2RelErr)
 U = 2.0 ** -24
-K_EY = E + 2 * U               # kFastEy
-KAPPA = U * 0.693147181        # kFastKappa
+K_EY = E + 1.0625 * U          # kFastEy
 K_HI, K_LO = 1 + 2.0 ** -12, 1 - 2.0 ** -12
 K_UND = 3.9e-4
 LN2F = float(np.float32(0.693147181))
@@ -71,15 +72,17 @@ def emulate_fast_draw(l, q, T, u, s_row, signs, d_scale=1.0, s_sign=1.0, exact=T
     v = 1.4426950408889634 / T
     chi = float(np.float32(v))
     clo = float(np.float32(v - chi))
-    d = f32(l - m)
-    a = f32(d * chi)
-    err = f32(d * chi - a)              # exact FMA residual
-    err = f32(d * clo + err)
+    d = l - m                           # exact in float64 (float32 operands)
+    dh = f32(d)                         # TwoSum: the float32 difference and its error
+    dl = d - dh
+    a = f32(dh * chi)
+    # the exponent's residual (the product's rounding, c's low part, the
+    # difference's error), applied to first order; its own roundings are far
+    # below 2^-33 of y
+    t = ((dh * chi - a) + dh * clo + dl * chi) * math.log(2.0)
     with np.errstate(over="ignore", invalid="ignore"):
         y0 = np.where(a >= -126.0, f32(np.exp2(a) * (1.0 + signs * E)), 0.0)
-    t = f32(err * LN2F)
     y = np.where(y0 > 0, f32(y0 * t + y0), 0.0)
-    ya = np.where(y > 0, f32(y * np.abs(a)), 0.0)
     if q is None:
         pos = np.ones(V, bool)
         und = np.zeros(V, bool)
@@ -133,9 +136,8 @@ def emulate_fast_draw(l, q, T, u, s_row, signs, d_scale=1.0, s_sign=1.0, exact=T
     hi = C[tok]
     Ppos = float(num(Cy[-1]) // S_int) * 2.0 ** -62
     Qpos = Cq[-1] * 2.0 ** -62
-    eS = (K_EY + 3 * U * (max(0.0, 1.0 - Ppos) if exact else 1.0)
-          + KAPPA * (ya.sum() / Sd) * 1.001)
-    D = ((K_EY * Ppos + KAPPA * (ya.sum() / Sd) * 1.001 + eS * Qpos + K_UND * qv[und].sum()
+    eS = K_EY + 3 * U * (max(0.0, 1.0 - Ppos) if exact else 1.0)
+    D = ((K_EY * Ppos + eS * Qpos + K_UND * qv[und].sum()
           + (0.0 if exact else 3 * U * (Ppos + Qpos))) * 1.004 * 2.0 ** 62
          + 2.0 ** 20 + 2.0 * (V / 8) + 64.0) * d_scale
     um = max(u, 1.0 - u)

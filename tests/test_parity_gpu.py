@@ -48,12 +48,16 @@ SMALL = [
 ]
 
 
-@pytest.fixture(params=[1, 2, 3], ids=["two_kernel", "fused", "skip"])
+@pytest.fixture(params=[(1, 0), (1, 1), (2, 0), (3, 0), (3, 1)],
+                ids=["two_kernel", "two_kernel_split_draw", "fused", "skip", "skip_split_draw"])
 def path(request):
     """Run a test once through each one-call path: the per-call options that
-    force it (passed as run_gpu's `tuning`)."""
+    force it (passed as run_gpu's `tuning`).  The two-kernel and row-skipping
+    paths draw with one cluster per sequence, or with the split draw (slices
+    on separate CTAs) under draw_mode 1."""
     from speculative_decoding_verification_18_gb300 import specverify as sv
-    return sv.Tuning(path=request.param)
+    p, dm = request.param
+    return sv.Tuning(path=p, draw_mode=dm)
 
 
 @pytest.mark.parametrize("B,k,V,dtype,T,kind", SMALL)
@@ -211,13 +215,18 @@ def test_ex2_approx_error_within_the_fast_draw_bound():
     assert 0.0 < worst <= 1.75e-7, worst
 
 
-@pytest.mark.parametrize("name", ["c3", "c4", "c5"])
-def test_workload_precise_draw_only(name):
-    """Every draw through the float-float pass (the fast pass switched off)."""
+@pytest.mark.parametrize("name,path,draw_mode", [
+    ("c3", 2, 0), ("c3", 1, 1), ("c3", 1, 2), ("c4", 0, 1), ("c4", 0, 2), ("c5", 0, 1),
+    ("c5", 0, 2)], ids=["c3-fused", "c3-split", "c3-cluster", "c4-split", "c4-cluster",
+                        "c5-split", "c5-cluster"])
+def test_workload_precise_draw_only(name, path, draw_mode):
+    """Every draw through the float-float pass (the fast pass switched off), in
+    the fused kernel, the split precise draw and the cluster draw."""
     from speculative_decoding_verification_18_gb300 import specverify as sv
     from speculative_decoding_verification_18_gb300.inputs import workload
     inp = workload(name, seed=77)
-    out, n, stats, (st, bits, _) = run_gpu(inp, tuning=sv.Tuning(force_precise=1))
+    out, n, stats, (st, bits, _) = run_gpu(
+        inp, tuning=sv.Tuning(force_precise=1, path=path, draw_mode=draw_mode))
     ref = run_oracle(inp)
     rep = compare_outputs(inp, out, n, ref)
     assert rep.hard == 0, rep.hard_detail
