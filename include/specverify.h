@@ -286,7 +286,7 @@ sv_status spec_verify_finish(sv_mode mode, const void* logits, sv_dtype dtype,
  *   - It allocates nothing and calls no allocating routine; the result and the
  *     device-detected data errors (num_accepted = -1) are as for
  *     spec_verify_sample. */
-#define SV_NOALLOC_SCRATCH_BYTES 2097152
+#define SV_NOALLOC_SCRATCH_BYTES 1048576
 #define SV_NOALLOC_MAX_ROWS 27000
 sv_status spec_verify_sample_noalloc(const void* logits, sv_dtype dtype,
                                      const float* draft_probs, const int32_t* draft_tokens,

@@ -124,6 +124,10 @@ __host__ __device__ inline size_t ws_bytes_for(long long B, int k, int V) {
     size_t b = ws_split_offset(B, k) + split_ws_bytes(B, V);
     return (b + 255) & ~(size_t)255;
 }
+// Without the split region (every path but the split draw).
+__host__ __device__ inline size_t ws_base_bytes(long long B, int k) {
+    return (ws_split_offset(B, k) + 255) & ~(size_t)255;
+}
 
 // ------------------------------------------------------------------ small helpers
 
@@ -769,7 +773,6 @@ __device__ __forceinline__ int fast_ey(float s_row) {
     return max(0, min(61, 61 - e));
 }
 
-constexpr int kClsZero = 0, kClsPos = 1, kClsUndecided = 2;
 constexpr int kFastGroup = 8;  // lanes (chunks of 8 elements) per block of the fast pass
 
 struct FastScale {
@@ -789,28 +792,6 @@ __device__ __forceinline__ FastScale make_fast_scale(float m, ff c2, float s_row
     f.il = res ? __frcp_rn(__fmul_rn(s_row, kClassLo)) : 0.0f;
     f.ey = fast_ey(s_row);
     return f;
-}
-
-// One element of the fast pass: y and the class.  d = l - m is exact; a = d
-// c_hi rounded; t = (the product's rounding + d c_lo + d_lo c_hi) ln2; y =
-// ex2(a) (1 + t).  Every float operation is explicitly rounded, so the pass and
-// the owner's search compute identical values.  l = -inf gives a NaN t and
-// y = max(NaN, 0) = 0.  A NaN q is undecided (its bound is NaN, so the draw
-// goes to the precise pass, which weighs it 0); a negative q is caught by the
-// caller.
-template <bool RES>
-__device__ __forceinline__ int fast_elem(float l, float q, const FastScale& f, float& y) {
-    const ff d = two_sum(l, -f.m);
-    const float a = __fmul_rn(d.hi, f.chi);
-    const float r = __fmaf_rn(d.hi, f.chi, -a);  // exact
-    float t = __fmaf_rn(d.hi, f.cll, __fmul_rn(d.lo, f.chl));
-    t = __fmaf_rn(r, 0.693147181f, t);
-    const float y0 = ex2_approx(a);
-    y = fmaxf(__fmaf_rn(y0, t, y0), 0.0f);
-    if (!RES) return kClsPos;
-    if (__fmul_rn(y, f.ih) > q) return kClsPos;
-    if (__fmul_rn(y, f.il) < q) return kClsZero;
-    return kClsUndecided;
 }
 
 // acc += v in float-float (TwoSum into the high part, its error into lo).
@@ -852,6 +833,20 @@ __device__ __forceinline__ unsigned long long ff_fixed(ff v, int s) {
     return v.lo < 0.0f ? h - l : h + l;
 }
 
+// y of one element: d = l - m exact; a = d c_hi rounded; t = (the product's
+// rounding + d c_lo + d_lo c_hi) ln2; y = ex2(a) (1 + t).  Every float
+// operation is explicitly rounded, so the pass and the owner's search compute
+// identical values.  l = -inf gives a NaN t and y = max(NaN, 0) = 0.
+__device__ __forceinline__ float fast_y(float l, const FastScale& f) {
+    const ff d = two_sum(l, -f.m);
+    const float a = __fmul_rn(d.hi, f.chi);
+    const float r = __fmaf_rn(d.hi, f.chi, -a);  // exact
+    float t = __fmaf_rn(d.hi, f.cll, __fmul_rn(d.lo, f.chl));
+    t = __fmaf_rn(r, 0.693147181f, t);
+    const float y0 = ex2_approx(a);
+    return fmaxf(__fmaf_rn(y0, t, y0), 0.0f);
+}
+
 // Pairwise tree of 8 values fed in index order: ((v0+v1)+(v2+v3)) + ((v4+v5)+(v6+v7)),
 // folded as the values arrive (sum8's order, few live registers).
 struct Tree8 {
@@ -870,15 +865,25 @@ struct Tree8 {
     }
 };
 
-template <int E, bool RES, bool EXACT, bool WANT>
+// Element E of a chunk of the fast pass: y, and (residual draws) its class:
+// positive when y / (S_row (1 + 2^-12)) > q, zero when y / (S_row (1 - 2^-12))
+// < q, undecided otherwise (its q goes to aq, for the bound).  The positive
+// elements' y and q go to the chunk's sums (EXACT: in element order in
+// float-float, else the pairwise trees), the others' y to tr.
+template <int E, bool RES, bool EXACT>
 __device__ __forceinline__ void fast_chunk_elem(const float* l, const float* q, const FastScale& f,
                                                 ff& Y, ff& Q, Tree8& ty, Tree8& tq, Tree8& tr,
                                                 float& aq, float& qmin, float* yp, float* qp) {
-    float y;
-    const int cls = fast_elem<RES>(l[E], RES ? q[E] : 0.0f, f, y);
-    const bool pos = cls == kClsPos;
+    const float y = fast_y(l[E], f);
+    bool pos = true;
+    if (RES) {
+        pos = __fmul_rn(y, f.ih) > q[E];
+        const bool und = !pos && !(__fmul_rn(y, f.il) < q[E]);
+        aq = und ? __fadd_rn(aq, q[E]) : aq;
+        qmin = fminf(qmin, q[E]);
+    }
     const float yv = pos ? y : 0.0f, qv = (RES && pos) ? q[E] : 0.0f;
-    if (WANT) {
+    if (yp) {
         yp[E] = yv;
         qp[E] = qv;
     }
@@ -890,30 +895,29 @@ __device__ __forceinline__ void fast_chunk_elem(const float* l, const float* q, 
         if (RES) tq.add<E>(qv);
     }
     tr.add<E>(pos ? 0.0f : y);
-    if (RES) {
-        aq = __fadd_rn(aq, cls == kClsUndecided ? q[E] : 0.0f);
-        qmin = fminf(qmin, q[E]);
-    }
 }
 
-// One chunk (8 elements, logits l and q): the fixed-point sums of the positive
-// elements' y and q (cy, cq), the other elements' y summed pairwise (returned),
-// the undecided elements' q into aq, the smallest q into qmin; with WANT, yp
-// and qp receive each element's y and q when it is positive, else 0.
-template <bool RES, bool EXACT, bool WANT>
+// One chunk (8 elements, logits l and q) of the fast pass: the fixed-point
+// sums of the positive elements' y and q (cy, cq), the other elements' y
+// summed pairwise (returned), the undecided elements' q into aq, the smallest q
+// into qmin; with `yp`, yp and qp receive each element's y and q when it is
+// positive, else 0.  A NaN q is undecided (its bound is NaN, so the draw goes
+// to the precise pass, which weighs it 0); a negative q is caught by the
+// caller through qmin.
+template <bool RES, bool EXACT>
 __device__ __forceinline__ float fast_chunk(const float* l, const float* q, const FastScale& f,
                                             unsigned long long& cy, unsigned long long& cq,
                                             float& aq, float& qmin, float* yp, float* qp) {
     ff Y{0.0f, 0.0f}, Q{0.0f, 0.0f};
     Tree8 ty{}, tq{}, tr{};
-    fast_chunk_elem<0, RES, EXACT, WANT>(l, q, f, Y, Q, ty, tq, tr, aq, qmin, yp, qp);
-    fast_chunk_elem<1, RES, EXACT, WANT>(l, q, f, Y, Q, ty, tq, tr, aq, qmin, yp, qp);
-    fast_chunk_elem<2, RES, EXACT, WANT>(l, q, f, Y, Q, ty, tq, tr, aq, qmin, yp, qp);
-    fast_chunk_elem<3, RES, EXACT, WANT>(l, q, f, Y, Q, ty, tq, tr, aq, qmin, yp, qp);
-    fast_chunk_elem<4, RES, EXACT, WANT>(l, q, f, Y, Q, ty, tq, tr, aq, qmin, yp, qp);
-    fast_chunk_elem<5, RES, EXACT, WANT>(l, q, f, Y, Q, ty, tq, tr, aq, qmin, yp, qp);
-    fast_chunk_elem<6, RES, EXACT, WANT>(l, q, f, Y, Q, ty, tq, tr, aq, qmin, yp, qp);
-    fast_chunk_elem<7, RES, EXACT, WANT>(l, q, f, Y, Q, ty, tq, tr, aq, qmin, yp, qp);
+    fast_chunk_elem<0, RES, EXACT>(l, q, f, Y, Q, ty, tq, tr, aq, qmin, yp, qp);
+    fast_chunk_elem<1, RES, EXACT>(l, q, f, Y, Q, ty, tq, tr, aq, qmin, yp, qp);
+    fast_chunk_elem<2, RES, EXACT>(l, q, f, Y, Q, ty, tq, tr, aq, qmin, yp, qp);
+    fast_chunk_elem<3, RES, EXACT>(l, q, f, Y, Q, ty, tq, tr, aq, qmin, yp, qp);
+    fast_chunk_elem<4, RES, EXACT>(l, q, f, Y, Q, ty, tq, tr, aq, qmin, yp, qp);
+    fast_chunk_elem<5, RES, EXACT>(l, q, f, Y, Q, ty, tq, tr, aq, qmin, yp, qp);
+    fast_chunk_elem<6, RES, EXACT>(l, q, f, Y, Q, ty, tq, tr, aq, qmin, yp, qp);
+    fast_chunk_elem<7, RES, EXACT>(l, q, f, Y, Q, ty, tq, tr, aq, qmin, yp, qp);
     if (EXACT) {
         cy = ff_fixed(ff_normalize(Y), f.ey);
         cq = RES ? ff_fixed(ff_normalize(Q), 62) : 0ull;
@@ -998,15 +1002,16 @@ __device__ __forceinline__ FastTotals add_fast_totals(FastTotals t, const FastTo
 
 // The fast pass over the CTA's slice of the decision row (and of its q row):
 // this thread's sums.  Each warp takes 32 consecutive chunks (a chunk per lane,
-// four blocks of 8 chunks), two such rounds in flight.  With BLOCKS the sums of
-// each block (Y then Q, fixed point) go to d.bsum[blk] and d.bsum[nblk8 + blk].
+// four blocks of 8 chunks), two such rounds in flight.  With BLOCKS the fixed-
+// point sums of each block, {Y, Q}, go to d.bsum[2 blk], d.bsum[2 blk + 1]
+// (shared or global memory, 16-byte aligned).
 template <typename DT, bool RES, bool EXACT, bool BLOCKS>
 __device__ __forceinline__ FastTotals fast_pass(const DrawCtx<DT>& d, const FastScale& f) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int grp = lane / kFastGroup, gl = lane % kFastGroup;
     const int fnb = (d.mych + kFastGroup - 1) / kFastGroup;  // blocks of this CTA's slice
     FastTotals t = zero_totals();
-    constexpr int UB = 2;
+    constexpr int UB = 1;  // (two in flight spill at 64 registers; 32 warps per SM cover it)
     for (int base0 = warp * 32; base0 < d.mych; base0 += UB * kThreads) {
         RawQ rq[UB];
         RawL<DT> rl[UB];
@@ -1028,7 +1033,7 @@ __device__ __forceinline__ FastTotals fast_pass(const DrawCtx<DT>& d, const Fast
                 raw_unpack(rl[u], l);
                 if (RES) raw_unpack_q(rq[u], q);
                 const float rest =
-                    fast_chunk<RES, EXACT, false>(l, q, f, cy, cq, t.Aq, t.qmin, nullptr, nullptr);
+                    fast_chunk<RES, EXACT>(l, q, f, cy, cq, t.Aq, t.qmin, nullptr, nullptr);
                 ff_acc1(t.S, rest);
             }
             t.Y += cy;
@@ -1037,10 +1042,8 @@ __device__ __forceinline__ FastTotals fast_pass(const DrawCtx<DT>& d, const Fast
                 const unsigned long long by = group_sum_u64(cy);
                 const unsigned long long bq = RES ? group_sum_u64(cq) : 0ull;
                 const int blk = (base + grp * kFastGroup) / kFastGroup;
-                if (gl == 0 && blk < fnb) {
-                    d.bsum[blk] = by;
-                    d.bsum[fnb + blk] = bq;
-                }
+                if (gl == 0 && blk < fnb)
+                    reinterpret_cast<ulonglong2*>(d.bsum)[blk] = make_ulonglong2(by, bq);
             }
         }
     }
@@ -1082,6 +1085,7 @@ __device__ __forceinline__ void cta_fast_totals(DrawShared& sh, FastTotals t, Fa
 struct FastBound {
     unsigned long long M, tau;
     float D, eS;
+    float S;  // the normaliser (high part)
     bool ok;
 };
 template <bool EXACT>
@@ -1092,6 +1096,7 @@ __device__ __forceinline__ FastBound fast_bound(const FastTotals& tot, float s_r
     const float pw = __int_as_float((127 - ey) << 23);  // 2^-EY
     const ff Yf = u64_to_ff(Yall);
     const ff S = ff_normalize(ff_add(ff{__fmul_rn(Yf.hi, pw), __fmul_rn(Yf.lo, pw)}, tot.S));
+    fb.S = S.hi;
     bool ok = tot.qmin >= 0.0f && S.hi > 0.0f &&
               fabsf(__fsub_rn(S.hi, s_row)) <= S.hi * (float)kRowSigma;
     // M = floor(2^(123 - EY) / S): below 2^63 once S is within 2^-13 of S_row
@@ -1114,19 +1119,26 @@ __device__ __forceinline__ FastBound fast_bound(const FastTotals& tot, float s_r
     return fb;
 }
 
+// Block sums {Y, Q} of a slice: from shared memory, or (GLOBAL) written to the
+// workspace by other CTAs of this launch, read past L1.
+template <bool GLOBAL>
+__device__ __forceinline__ ulonglong2 load_block(const unsigned long long* bsum, int i) {
+    const ulonglong2* p = reinterpret_cast<const ulonglong2*>(bsum) + i;
+    if (GLOBAL) return __ldcg(p);
+    return *p;
+}
+
 // The owner CTA's search: given M, tau, D, e_S and the starting point (Y0, Q0)
-// of its slice, find the block from the block sums in d.bsum, then the
-// element, and certify it.  Every thread of the CTA calls it; sh.token and
-// sh.cert hold the result after the last barrier.
-template <typename DT, bool RES, bool EXACT>
+// of its slice, find the block from the slice's block sums (d.bsum), then the
+// chunk and the element, and certify it.  Every thread of the CTA calls it;
+// sh.token and sh.cert hold the result after the last barrier.
+template <typename DT, bool RES, bool EXACT, bool GLOBAL>
 __device__ __forceinline__ void fast_search(DrawShared& sh, const DrawCtx<DT>& d,
                                             const FastScale& f, unsigned long long M,
                                             unsigned long long tau, unsigned long long Y0,
                                             unsigned long long Q0, float D, float eS) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int fnb = (d.mych + kFastGroup - 1) / kFastGroup;
-    const unsigned long long* Yb = d.bsum;
-    const unsigned long long* Qb = d.bsum + fnb;
     // The block: each thread sums a contiguous range of block sums; a block
     // scan of (Y, Q) gives each range's start; the first range whose end
     // passes tau holds the block.
@@ -1134,8 +1146,9 @@ __device__ __forceinline__ void fast_search(DrawShared& sh, const DrawCtx<DT>& d
     const int cb = min(fnb, tid * L), ce = min(fnb, cb + L);
     unsigned long long my = 0ull, mq = 0ull;
     for (int i = cb; i < ce; ++i) {
-        my += Yb[i];
-        mq += Qb[i];
+        const ulonglong2 v = load_block<GLOBAL>(d.bsum, i);
+        my += v.x;
+        mq += v.y;
     }
     unsigned long long iy = my, iq = mq;
 #pragma unroll
@@ -1173,9 +1186,10 @@ __device__ __forceinline__ void fast_search(DrawShared& sh, const DrawCtx<DT>& d
         unsigned long long ry = sy0, rq = sq0;
         int i = cb;
         for (; i < ce - 1; ++i) {
-            if (fast_cval(ry + Yb[i], rq + Qb[i], M) > (long long)tau) break;
-            ry += Yb[i];
-            rq += Qb[i];
+            const ulonglong2 v = load_block<GLOBAL>(d.bsum, i);
+            if (fast_cval(ry + v.x, rq + v.y, M) > (long long)tau) break;
+            ry += v.x;
+            rq += v.y;
         }
         sh.blk = i;
         sh.f_bY = ry;
@@ -1183,13 +1197,14 @@ __device__ __forceinline__ void fast_search(DrawShared& sh, const DrawCtx<DT>& d
     }
     __syncthreads();
     if (first >= 0 && warp == 0) {  // (first < 0 is not reachable: the slice's end passes tau)
-        // The element: lanes 0..7 take the block's chunks in the pass's
+        // The chunk: lanes 0..7 take the block's chunks in the pass's
         // arithmetic (the same fixed-point values as the block sums); the
-        // first lane whose end passes tau walks its elements.
-        const int ci = sh.blk * kFastGroup + lane;
+        // first lane whose end passes tau holds it.
+        const int ci = sh.blk * kFastGroup + (lane & (kFastGroup - 1));
         float l[kChunk], q[kChunk] = {}, yp[kChunk] = {}, qp[kChunk] = {};
         unsigned long long cy = 0ull, cq = 0ull;
-        if (lane < kFastGroup && ci < d.mych) {
+        const bool have = lane < kFastGroup && ci < d.mych;
+        if (have) {
             RawL<DT> rl;
             raw_load_l(d, ci, rl);
             raw_unpack(rl, l);
@@ -1199,7 +1214,7 @@ __device__ __forceinline__ void fast_search(DrawShared& sh, const DrawCtx<DT>& d
                 raw_unpack_q(rq, q);
             }
             float a1 = 0.0f, a2 = 0.0f;
-            (void)fast_chunk<RES, EXACT, true>(l, q, f, cy, cq, a1, a2, yp, qp);
+            (void)fast_chunk<RES, EXACT>(l, q, f, cy, cq, a1, a2, yp, qp);
         }
         unsigned long long iy2 = cy, iq2 = cq;
 #pragma unroll
@@ -1212,34 +1227,43 @@ __device__ __forceinline__ void fast_search(DrawShared& sh, const DrawCtx<DT>& d
             }
         }
         const unsigned long long ly = sh.f_bY + iy2 - cy, lq = sh.f_bQ + iq2 - cq;
-        const bool lp = lane < kFastGroup && ci < d.mych &&
-                        fast_cval(ly + cy, lq + cq, M) > (long long)tau;
+        const bool lp = have && fast_cval(ly + cy, lq + cq, M) > (long long)tau;
         const unsigned bl = __ballot_sync(0xffffffffu, lp);
-        if (bl && lane == __ffs(bl) - 1) {
-            long long lo = fast_cval(ly, lq, M), hi = lo;
-            int tok = -1;
+        const int oc = bl ? __ffs(bl) - 1 : 0;  // the chunk's lane
+        // The element: lane e < 8 takes element e of that chunk (its y and q
+        // and the chunk's start shuffled from the chunk's lane) and forms the
+        // cumulative weight through e; the first positive e past tau is it.
+        float ype[kChunk], qpe[kChunk];
 #pragma unroll
-            for (int e = 0; e < kChunk; ++e) {
-                if (tok >= 0 || !(yp[e] > 0.0f)) continue;  // weight 0: never chosen
-                unsigned long long py, pq;
-                fast_prefix<RES, EXACT>(yp, qp, e, f, py, pq);
-                const long long h = fast_cval(ly + py, lq + pq, M);
-                if (h > (long long)tau) {
-                    tok = e;
-                    hi = h;
-                } else {
-                    lo = h;
-                }
-            }
-            int ok = 0;
-            if (tok >= 0) {
-                const float um = fmaxf(d.u, __fsub_rn(1.0f, d.u));
-                const float dp = um * D + eS * 1.004f * (float)(hi - lo) + 2.0f;
-                const long long Dp = (long long)fminf(dp, 4.0e18f) + 1ll;
-                ok = ((long long)tau - lo >= Dp && hi - (long long)tau > Dp) ? 1 : 0;
-                sh.token = (int)((d.c0 + ci) * kChunk + tok);
-            }
-            sh.cert = ok;
+        for (int e = 0; e < kChunk; ++e) {
+            ype[e] = __shfl_sync(0xffffffffu, yp[e], oc);
+            qpe[e] = __shfl_sync(0xffffffffu, qp[e], oc);
+        }
+        const unsigned long long cly = __shfl_sync(0xffffffffu, ly, oc);
+        const unsigned long long clq = __shfl_sync(0xffffffffu, lq, oc);
+        const int e = lane & (kChunk - 1);
+        float mine = ype[0];  // ype[e] without indexing a register array at run time
+#pragma unroll
+        for (int j = 1; j < kChunk; ++j) mine = j == e ? ype[j] : mine;
+        unsigned long long py, pq;
+        fast_prefix<RES, EXACT>(ype, qpe, e, f, py, pq);
+        const long long h = fast_cval(cly + py, clq + pq, M);
+        const bool ep = bl && lane < kChunk && mine > 0.0f && h > (long long)tau;
+        const unsigned be = __ballot_sync(0xffffffffu, ep);
+        // lo: the cumulative weight before the element (the last positive
+        // element before it, or the chunk's start)
+        const bool before = lane < kChunk && mine > 0.0f && h <= (long long)tau;
+        const unsigned bb = __ballot_sync(0xffffffffu, before) & (be ? ((1u << (__ffs(be) - 1)) - 1u) : 0u);
+        const int te = be ? __ffs(be) - 1 : -1;
+        const long long hi = __shfl_sync(0xffffffffu, h, te >= 0 ? te : 0);
+        const long long hb = __shfl_sync(0xffffffffu, h, bb ? 31 - __clz(bb) : 0);
+        if (lane == 0 && te >= 0) {
+            const long long lo = bb ? hb : fast_cval(cly, clq, M);
+            const float um = fmaxf(d.u, __fsub_rn(1.0f, d.u));
+            const float dp = um * D + eS * 1.004f * (float)(hi - lo) + 2.0f;
+            const long long Dp = (long long)fminf(dp, 4.0e18f) + 1ll;
+            sh.cert = ((long long)tau - lo >= Dp && hi - (long long)tau > Dp) ? 1 : 0;
+            sh.token = (int)((d.c0 + sh.blk * kFastGroup + oc) * kChunk + te);
         }
     }
     __syncthreads();
@@ -1305,7 +1329,8 @@ __device__ bool draw_fast(cg::cluster_group& cluster, DrawShared& sh, const Draw
 
     int cert = 1;
     if (d.rank == sh.f_owner) {  // uniform across the CTA
-        fast_search<DT, RES, EXACT>(sh, d, f, sh.f_M, sh.f_tau, sh.f_Y, sh.f_Q, sh.f_D, sh.f_eS);
+        fast_search<DT, RES, EXACT, false>(sh, d, f, sh.f_M, sh.f_tau, sh.f_Y, sh.f_Q, sh.f_D,
+                                           sh.f_eS);
         cert = sh.cert;
     }
     if (d.G > 1) {
@@ -3126,9 +3151,10 @@ __global__ void __launch_bounds__(kThreads, 2) sv_precise_kernel(PreciseArgs a) 
 // then the fast pass over its slice, and leaves the slice's sums in the
 // workspace.  The CTA that completes a sequence's set (an arrival counter: the
 // last to arrive sees NS - 1) finishes the draw: the totals and the bound of
-// fast_bound, the owning slice (a prefix over the slices' sums), and the
-// owner's block and element by the owner slice's pass repeated with block sums
-// (the same arithmetic, so its values agree with the slice's sums exactly).  A
+// fast_bound, the owning slice (a prefix over the slices' sums), the owner's
+// block (from the block sums every slice leaves in the workspace) and its
+// element (that block's 64 elements recomputed in the same arithmetic, so they
+// agree with the block sums exactly).  A
 // draw the bound cannot certify is listed for the split precise draw, which
 // runs in the same fashion in two launches: the float-float normaliser's
 // slice sums, then each slice's fixed-point weight total, the last CTA of an
@@ -3139,8 +3165,6 @@ constexpr int kSplitTarget = 1024;      // CTAs a fast split draw aims for
 constexpr int kSplitMinChunks = 128;    // smallest slice (chunks of 8 elements)
 constexpr int kSplitMaxChunks = 8192;   // largest slice (its block sums fit 16 KiB)
 constexpr int kSplitMaxSlices = kThreads;
-constexpr int kPreciseMinChunks = 256;  // precise slices: at least 2048 elements
-constexpr int kPreciseMaxChunks = 2048; // and at most 16384
 
 // Slices per sequence of the fast split draw: about kSplitTarget CTAs in all,
 // slices between kSplitMinChunks and kSplitMaxChunks chunks, at most
@@ -3155,47 +3179,66 @@ __host__ __device__ inline int split_slices(int B, int V, int* sc) {
     if (ns > kSplitMaxSlices) ns = kSplitMaxSlices;
     if (ns < 1) ns = 1;
     long long c = (nch + ns - 1) / ns;
-    if (c < 1) c = 1;
+    c = (c + kFastGroup - 1) / kFastGroup * kFastGroup;  // whole blocks of 8 chunks
     *sc = (int)c;
     return (int)((nch + c - 1) / c);
 }
-// Slices per draw of the split precise pass: about 2 CTAs per SM's worth of
-// items when an eighth of the batch needs the precise pass, slices between
-// kPreciseMinChunks and kPreciseMaxChunks chunks (the owner's repeat stays short).
-__host__ __device__ inline int precise_slices(int B, int V, int* sc) {
-    const long long nch = ((long long)V + kChunk - 1) / kChunk;
-    const long long expect = B / 8 > 1 ? B / 8 : 1;
-    long long ns = (512 + expect - 1) / expect;
-    const long long lo = (nch + kPreciseMaxChunks - 1) / kPreciseMaxChunks;
-    const long long hi = (nch + kPreciseMinChunks - 1) / kPreciseMinChunks;
-    if (ns > hi) ns = hi;
-    if (ns < lo) ns = lo;
-    if (ns > kSplitMaxSlices) ns = kSplitMaxSlices;
-    if (ns < 1) ns = 1;
-    long long c = (nch + ns - 1) / ns;
-    if (c < 1) c = 1;
-    *sc = (int)c;
-    return (int)((nch + c - 1) / c);
-}
+// The split precise draw's persistent grid (at most this many CTAs; its
+// per-CTA item sums are sized for it) and the list of ambiguous elements each
+// listed draw can hold.
+constexpr int kPreciseGrid = 512;
+constexpr int kAmbCap = 32;
+struct AmbElem {
+    int idx;      // element index in the row
+    float q;      // its q
+    float ehi, elo;  // its e = exp((l - m)/T) in float-float
+};
+struct PreciseItem {
+    unsigned long long Y, Q;  // the slice's fixed-point sums of the positive elements
+    ff S;                     // the slice's float-float sum of e
+    unsigned long long pad;
+};
+static_assert(sizeof(AmbElem) == 16 && sizeof(PreciseItem) == 32, "precise records");
+
 // The split draws' part of the workspace (after the list of precise draws):
-// B fast arrival counters (zeroed with the list's counter, which they follow),
-// B precise arrival counters, B * NS slice sums, B * NSP precise partials
-// (a float-float normaliser part and a weight total each).
-constexpr long long kSplitMaxTotal = 16384;  // slices of a launch (bounds the workspace)
+// B fast arrival counters (zeroed with the list's counter, which they follow);
+// per list entry (B of them) an arrival counter, an ambiguous-element count,
+// the classifying normaliser and its margin, and kAmbCap ambiguous elements;
+// B * NS slice sums; max(kPreciseGrid, B) precise item sums; and the fast
+// pass's block sums, {Y, Q} per 64 elements of each decision row (reused by
+// the precise pass for the rows it draws).
+constexpr long long kSplitMaxTotal = 16384;          // slices of a launch
+constexpr size_t kSplitMaxBlockBytes = 64ull << 20;  // block sums of a launch
+__host__ __device__ inline long long split_row_blocks(int V) {
+    const long long nch = ((long long)V + kChunk - 1) / kChunk;
+    return (nch + kFastGroup - 1) / kFastGroup;
+}
 __host__ __device__ inline bool split_fits(long long B, int V) {
-    int sc = 0, scp = 0;
+    int sc = 0;
     return B > 0 && B * split_slices((int)B, V, &sc) <= kSplitMaxTotal &&
-           B * precise_slices((int)B, V, &scp) <= kSplitMaxTotal;
+           (size_t)B * split_row_blocks(V) * 16 <= kSplitMaxBlockBytes;
+}
+struct SplitLayout {
+    size_t parrive, pambn, pS, pD, amb, srec, items, bsum, end;  // from the region's start
+};
+__host__ __device__ inline SplitLayout split_layout(long long B, int V) {
+    int sc = 0;
+    const int ns = split_slices((int)B, V, &sc);
+    const size_t nb = (size_t)B;
+    SplitLayout L;
+    L.parrive = nb * 4;
+    L.pambn = L.parrive + nb * 4;
+    L.pS = L.pambn + nb * 4;
+    L.pD = L.pS + nb * 4;
+    L.amb = (L.pD + nb * 4 + 15) & ~(size_t)15;
+    L.srec = L.amb + nb * kAmbCap * sizeof(AmbElem);
+    L.items = L.srec + nb * ns * sizeof(FastTotals);
+    L.bsum = L.items + (size_t)(B > kPreciseGrid ? B : kPreciseGrid) * sizeof(PreciseItem);
+    L.end = L.bsum + nb * split_row_blocks(V) * 16;
+    return L;
 }
 __host__ __device__ size_t split_ws_bytes(long long B, int V) {
-    if (!split_fits(B, V)) return 0;
-    int sc = 0, scp = 0;
-    const int ns = split_slices((int)B, V, &sc), nsp = precise_slices((int)B, V, &scp);
-    size_t b = (size_t)B * 2 * sizeof(uint32_t);
-    b = (b + 15) & ~(size_t)15;
-    b += (size_t)B * ns * sizeof(FastTotals);
-    b += (size_t)B * nsp * (sizeof(ff) + sizeof(unsigned long long));
-    return b;
+    return split_fits(B, V) ? split_layout(B, V).end : 0;
 }
 
 struct SplitArgs {
@@ -3212,7 +3255,12 @@ struct SplitArgs {
     uint32_t* plist;
     uint32_t* arrive;       // [B] slices done per sequence (zero before the launch)
     uint32_t* parrive;      // [B] per entry of the list (zeroed when it is listed)
+    uint32_t* pambn;        // [B] ambiguous elements per entry (zeroed when it is listed)
+    float* pS;              // [B] per entry: the fast pass's normaliser S (or S_row)
+    float* pD;              // [B] per entry: the classification margin delta
     FastTotals* srec;       // [B * NS] the slices' sums
+    unsigned long long* bsum;  // [B][row blocks][2] the fast pass's block sums
+    long long nbr;          // blocks per row
     Epilogue ep;
     int B, k, V, NS, SC;    // slices per sequence, chunks per slice
     int force_precise;
@@ -3275,14 +3323,8 @@ struct SplitShared {
     int ok, owner, last;
 };
 
-// Dynamic shared memory of the fast split draw: the owner slice's block sums.
-__host__ __device__ inline size_t split_smem_bytes(int SC) {
-    return (size_t)((SC + kFastGroup - 1) / kFastGroup) * 2 * sizeof(unsigned long long);
-}
-
 template <typename DT, bool EXACT>
 __global__ void __launch_bounds__(kThreads, 2) sv_split_draw_kernel(SplitArgs a) {
-    extern __shared__ __align__(16) unsigned char dyn[];
     __shared__ DrawShared ds;
     __shared__ ScanShared sc;
     __shared__ SplitShared ss;
@@ -3311,13 +3353,14 @@ __global__ void __launch_bounds__(kThreads, 2) sv_split_draw_kernel(SplitArgs a)
     const long long nch = ((long long)V + kChunk - 1) / kChunk;
     const float m = sc.recs[n].mraw, s_row = sc.recs[n].S, u = sc.ur;
     const FastScale f = make_fast_scale(m, a.c2, s_row, res);
+    unsigned long long* rowblk = a.bsum + (long long)b * a.nbr * 2;  // this row's block sums
     {
         const long long c0 = (long long)s * a.SC;
-        const DrawCtx<DT> d = slice_ctx<DT>(dyn, drow, qrow, res, V, m, a.c2, u, c0,
-                                            (int)min((long long)a.SC, nch - c0), s_row);
-        FastTotals t = zero_totals();
-        if (!a.force_precise)
-            t = res ? fast_pass<DT, true, EXACT, false>(d, f) : fast_pass<DT, false, EXACT, false>(d, f);
+        const DrawCtx<DT> d =
+            slice_ctx<DT>(reinterpret_cast<unsigned char*>(rowblk + (c0 / kFastGroup) * 2), drow,
+                          qrow, res, V, m, a.c2, u, c0, (int)min((long long)a.SC, nch - c0), s_row);
+        const FastTotals t =
+            res ? fast_pass<DT, true, EXACT, true>(d, f) : fast_pass<DT, false, EXACT, true>(d, f);
         cta_fast_totals(ds, t, &ss.tot);
     }
     if (tid == 0) {
@@ -3373,17 +3416,13 @@ __global__ void __launch_bounds__(kThreads, 2) sv_split_draw_kernel(SplitArgs a)
     int token = -1;
     if (owner >= 0) {  // uniform across the CTA
         const long long c0 = (long long)owner * a.SC;
-        const DrawCtx<DT> d = slice_ctx<DT>(dyn, drow, qrow, res, V, m, a.c2, u, c0,
-                                            (int)min((long long)a.SC, nch - c0), s_row);
-        if (res) {
-            (void)fast_pass<DT, true, EXACT, true>(d, f);
-            __syncthreads();
-            fast_search<DT, true, EXACT>(ds, d, f, fb.M, fb.tau, ss.Y0, ss.Q0, fb.D, fb.eS);
-        } else {
-            (void)fast_pass<DT, false, EXACT, true>(d, f);
-            __syncthreads();
-            fast_search<DT, false, EXACT>(ds, d, f, fb.M, fb.tau, ss.Y0, ss.Q0, fb.D, fb.eS);
-        }
+        const DrawCtx<DT> d =
+            slice_ctx<DT>(reinterpret_cast<unsigned char*>(rowblk + (c0 / kFastGroup) * 2), drow,
+                          qrow, res, V, m, a.c2, u, c0, (int)min((long long)a.SC, nch - c0), s_row);
+        if (res)
+            fast_search<DT, true, EXACT, true>(ds, d, f, fb.M, fb.tau, ss.Y0, ss.Q0, fb.D, fb.eS);
+        else
+            fast_search<DT, false, EXACT, true>(ds, d, f, fb.M, fb.tau, ss.Y0, ss.Q0, fb.D, fb.eS);
         cert = ds.cert != 0 && ds.token >= 0;
         token = ds.token;
     }
@@ -3398,6 +3437,13 @@ __global__ void __launch_bounds__(kThreads, 2) sv_split_draw_kernel(SplitArgs a)
             const uint32_t j = atomicAdd(a.plist_count, 1u);
             if (j < (uint32_t)a.B) {  // at most B entries
                 a.parrive[j] = 0u;
+                a.pambn[j] = 0u;
+                // The precise pass classifies each element against q with this
+                // normaliser: the fast pass's S (within e_S of the exact one)
+                // when it is a positive number, else the row stream's.
+                const bool sok = fb.S > 0.0f && fb.S < INFINITY;
+                a.pS[j] = sok ? fb.S : s_row;
+                a.pD[j] = sok ? 2.0f * fb.eS + 8.0f * 5.96046448e-08f : 1.0f / 2048.0f;
                 a.plist[j] = (uint32_t)b;
             }
         }
@@ -3405,6 +3451,29 @@ __global__ void __launch_bounds__(kThreads, 2) sv_split_draw_kernel(SplitArgs a)
 }
 
 // ---- the split precise draw
+//
+// The draws the fast pass could not certify, each cut into slices of whole
+// 64-element blocks spread over a persistent grid (as many slices per draw as
+// the grid holds, so that the listed draws take one round).  Each slice's CTA
+// forms e = exp((l - m)/T) in float-float for its elements and classifies each
+// against q with the fast pass's normaliser S' (within e_S of the exact S):
+// positive when e / S' > q (1 + delta), zero when e / S' < q (1 - delta) or q
+// is not a non-negative number (such entries weigh 0), otherwise ambiguous
+// (listed, with its e and q).  The weight max(0, e/S - q) of the positive
+// elements is the linear form e/S - q, so as in the fast pass each chunk's
+// positive e and q are summed (float-float, in element order) and turned into
+// fixed point (Y in units 2^-EY, Q in 2^-62); the block sums go to the
+// workspace, the slice's sums of Y, Q and S to its item record.  The last CTA
+// of a draw (an arrival counter): S, M = floor(2^(123 - EY) / S), each listed
+// element decided exactly (e/S - q > 0 in float-float) and added at its
+// position, C = floor(Y M / 2^61) - Q, tau = floor(u C_tot), then the slice,
+// block, chunk and element holding tau, recomputed where needed in the same
+// arithmetic.  The token equals the exact-arithmetic one unless u C_tot lies
+// within a few units of 2^-62 of a bin edge (float-float exponentials to about
+// 2^-45, fixed-point sums exact).  A draw with more ambiguous elements than the
+// list holds, an S beyond the margin of S', or a residual without mass takes
+// the two-pass precise draw in that CTA alone (a zero-mass residual is drawn
+// from p there, counted).
 struct SplitPreciseArgs {
     const void* logits;
     const float* q;
@@ -3414,11 +3483,16 @@ struct SplitPreciseArgs {
     const uint32_t* plist_count;
     const uint32_t* plist;
     uint32_t* parrive;            // [B] per list entry
-    ff* spart;                    // [B * NSP] the slices' float-float normaliser parts
-    unsigned long long* wpart;    // [B * NSP] the slices' weight totals
+    uint32_t* pambn;              // [B] per list entry
+    const float* pS;              // [B]
+    const float* pD;              // [B]
+    AmbElem* amb;                 // [B][kAmbCap]
+    PreciseItem* items;           // [max(kPreciseGrid, B)]
+    unsigned long long* bsum;     // [B][row blocks][2] (the fast pass's array, reused)
+    long long nbr;                // blocks per row
     uint32_t* seqstat;
     int32_t* out;
-    int B, k, V, NSP, SCP;
+    int B, k, V;
     ff c2;
 };
 
@@ -3430,171 +3504,465 @@ __device__ __forceinline__ void load_exp_table(float* thi, float* tlo) {
     __syncthreads();
 }
 
-// Dynamic shared memory of the precise split kernels: the 2^(i/1024) table and
-// the block sums of a slice (or, for a draw from p after a residual without
-// mass, of the whole row).
-__host__ __device__ inline size_t split_precise_smem_bytes(int V, int SCP) {
+// Dynamic shared memory of the precise split kernel: the 2^(i/1024) table and
+// the block sums of the two-pass fallback over a whole row.
+__host__ __device__ inline size_t split_precise_smem_bytes(int V) {
     const long long nch = ((long long)V + kChunk - 1) / kChunk;
-    const long long c = nch > SCP ? nch : SCP;
     return 2 * kExpTable * sizeof(float) +
-           (size_t)((c + kBlockChunks - 1) / kBlockChunks) * sizeof(unsigned long long);
+           (size_t)((nch + kBlockChunks - 1) / kBlockChunks) * sizeof(unsigned long long);
 }
 
-template <typename DT>
-__device__ __forceinline__ DrawCtx<DT> precise_slice_ctx(unsigned char* dyn, const SplitPreciseArgs& a,
-                                                         int b, int n, long long c0, int mych) {
-    const int k = a.k, V = a.V;
-    const DT* drow = static_cast<const DT*>(a.logits) + ((long long)b * (k + 1) + n) * V;
-    const float* qrow = n < k ? a.q + ((long long)b * k + n) * V : nullptr;
-    const RowRec& rec = a.rows[(long long)b * (k + 1) + n];
-    DrawCtx<DT> d = slice_ctx<DT>(dyn + 2 * kExpTable * sizeof(float), drow, qrow, n < k, V,
-                                  rec.mraw, a.c2, a.ur[b], c0, mych, rec.S);
-    d.thi = reinterpret_cast<float*>(dyn);
-    d.tlo = d.thi + kExpTable;
-    return d;
+// Classes of the precise pass.
+constexpr int kPcZero = 0, kPcPos = 1, kPcAmb = 2;
+struct PreciseCls {
+    float inv;         // 1 / S' (rounded)
+    float hi, lo;      // 1 + delta, 1 - delta
+    int ey;
+};
+__device__ __forceinline__ int precise_class(ff e, float q, const PreciseCls& c, bool res) {
+    if (!res) return kPcPos;
+    if (!(q >= 0.0f) || e.hi == 0.0f) return kPcZero;  // NaN or negative q, or e = 0: weight 0
+    const float r = __fmul_rn(e.hi, c.inv);
+    if (r > __fmul_rn(q, c.hi)) return kPcPos;
+    if (r < __fmul_rn(q, c.lo)) return kPcZero;
+    return kPcAmb;
 }
 
-// First launch: each (entry, slice) item's float-float normaliser part.
+// One chunk of the precise pass: the fixed-point sums of its positive
+// elements' e and q (not counting ambiguous ones); `es`, `cls` receive each
+// element's e and class when not null; the chunk's e total goes into S.
 template <typename DT>
-__global__ void __launch_bounds__(kThreads, 2) sv_split_precise_a_kernel(SplitPreciseArgs a) {
-    extern __shared__ __align__(16) unsigned char dyn[];
-    __shared__ ff red[kWarps];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    asm volatile("griddepcontrol.wait;" ::: "memory");  // the list is complete
-    const uint32_t cnt = min(*a.plist_count, (uint32_t)a.B);
-    const long long items = (long long)cnt * a.NSP;
-    if (blockIdx.x >= items) return;
-    load_exp_table(reinterpret_cast<float*>(dyn), reinterpret_cast<float*>(dyn) + kExpTable);
-    const long long nch = ((long long)a.V + kChunk - 1) / kChunk;
-    for (long long it = blockIdx.x; it < items; it += gridDim.x) {
-        const int j = (int)(it / a.NSP), s = (int)(it % a.NSP);
-        const int b = (int)a.plist[j];
-        const int n = a.nacc[b];
-        const long long c0 = (long long)s * a.SCP;
-        const DrawCtx<DT> d =
-            precise_slice_ctx<DT>(dyn, a, b, n, c0, (int)min((long long)a.SCP, nch - c0));
-        ff acc = warp_sum_ff(ff_normalize(precise_pass_a<DT, false>(d)));
-        if (lane == 0) red[warp] = acc;
-        __syncthreads();
-        if (warp == 0) {
-            ff w = lane < kWarps ? red[lane] : ff{0.0f, 0.0f};
-            w = warp_sum_ff(w);
-            if (lane == 0) a.spart[(long long)j * a.NSP + s] = ff_normalize(w);
+__device__ __forceinline__ void precise_lin_chunk(const DrawCtx<DT>& d, int ci, const float* l,
+                                                  const float* q, const PreciseCls& c, bool res,
+                                                  ff& S, unsigned long long& cy,
+                                                  unsigned long long& cq, ff* es, int* cls) {
+    ff Y{0.0f, 0.0f}, Q{0.0f, 0.0f};
+#pragma unroll
+    for (int e = 0; e < kChunk; ++e) {
+        const ff ev = exp_rel(l[e], d.m, d.c2, d.thi, d.tlo);
+        ff_accumulate(S, ev);
+        const int k = precise_class(ev, q[e], c, res);
+        if (k == kPcPos) {
+            ff_accumulate(Y, ev);
+            if (res) ff_acc1(Q, q[e]);
         }
-        __syncthreads();
+        if (es) {
+            es[e] = ev;
+            cls[e] = k;
+        }
     }
+    cy = ff_fixed(ff_normalize(Y), c.ey);
+    cq = res ? ff_fixed(ff_normalize(Q), 62) : 0ull;
 }
 
-// Second launch: each item's weight total; the last item of an entry to finish
-// finds the token.
+struct PreciseShared {
+    AmbElem amb[kAmbCap];              // the listed elements, sorted by index
+    unsigned long long ay[kAmbCap], aq[kAmbCap];  // their fixed-point y and q (0: not positive)
+    unsigned long long ry[kWarps], rq[kWarps];
+    ff rs[kWarps];
+    unsigned long long Y, Q, Y0, Q0, bY, bQ, M, tau;
+    ff S;
+    int nb_amb, owner, blk, chunk, token, last, fallback;
+};
+
+// Sums of the listed positive elements with index in [lo, hi).
+__device__ __forceinline__ void amb_in(const PreciseShared& ps, long long lo, long long hi,
+                                       unsigned long long& y, unsigned long long& q) {
+    for (int i = 0; i < ps.nb_amb; ++i)
+        if (ps.amb[i].idx >= lo && ps.amb[i].idx < hi) {
+            y += ps.ay[i];
+            q += ps.aq[i];
+        }
+}
+
 template <typename DT>
-__global__ void __launch_bounds__(kThreads, 2) sv_split_precise_b_kernel(SplitPreciseArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) sv_split_precise_kernel(SplitPreciseArgs a) {
     extern __shared__ __align__(16) unsigned char dyn[];
     __shared__ DrawShared ds;
-    __shared__ unsigned long long woff[kWarps];
-    __shared__ int s_last, s_owner;
-    __shared__ unsigned long long s_pre;
+    __shared__ PreciseShared ps;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    asm volatile("griddepcontrol.wait;" ::: "memory");  // the normaliser parts are complete
+    const int grp = lane / kFastGroup, gl = lane % kFastGroup;
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the list is complete
     const uint32_t cnt = min(*a.plist_count, (uint32_t)a.B);
-    const long long items = (long long)cnt * a.NSP;
-    if (blockIdx.x >= items) return;
-    load_exp_table(reinterpret_cast<float*>(dyn), reinterpret_cast<float*>(dyn) + kExpTable);
+    if (cnt == 0) return;
+    const int P = gridDim.x;
+    const long long nbr = a.nbr;
     const long long nch = ((long long)a.V + kChunk - 1) / kChunk;
+    // Slices per draw: as many as the grid holds (whole blocks each).
+    long long nsl = P / (long long)cnt;
+    if (nsl < 1) nsl = 1;
+    if (nsl > nbr) nsl = nbr;
+    const long long slb = (nbr + nsl - 1) / nsl;  // blocks per slice
+    nsl = (nbr + slb - 1) / slb;
+    const long long items = (long long)cnt * nsl;
+    if (blockIdx.x >= items) return;
+    float* thi = reinterpret_cast<float*>(dyn);
+    float* tlo = thi + kExpTable;
+    load_exp_table(thi, tlo);
     cg::cluster_group cluster = cg::this_cluster();
-    for (long long it = blockIdx.x; it < items; it += gridDim.x) {
-        const int j = (int)(it / a.NSP), s = (int)(it % a.NSP);
+    const int k = a.k, V = a.V;
+    for (long long it = blockIdx.x; it < items; it += P) {
+        const int j = (int)(it / nsl), s = (int)(it % nsl);
         const int b = (int)a.plist[j];
         const int n = a.nacc[b];
-        const bool res = n < a.k;
-        // S in one fixed order (every CTA of the entry computes the same value)
-        ff S{0.0f, 0.0f};
-        for (int i = 0; i < a.NSP; ++i) S = ff_add(S, a.spart[(long long)j * a.NSP + i]);
-        const ff inv = ff_recip(ff_normalize(S));
-        long long c0 = (long long)s * a.SCP;
-        DrawCtx<DT> d = precise_slice_ctx<DT>(dyn, a, b, n, c0, (int)min((long long)a.SCP, nch - c0));
-        unsigned long long t = res ? precise_pass_b<DT, true, false, false>(d, inv)
-                                   : precise_pass_b<DT, false, false, false>(d, inv);
-        t = warp_sum(t);
-        if (lane == 0) woff[warp] = t;
-        __syncthreads();
-        if (tid == 0) {
-            unsigned long long tot = 0ull;
-            for (int w = 0; w < kWarps; ++w) tot += woff[w];
-            a.wpart[(long long)j * a.NSP + s] = tot;
-            __threadfence();
-            s_last = atomicAdd(&a.parrive[j], 1u) == (uint32_t)(a.NSP - 1);
-        }
-        __syncthreads();
-        if (!s_last) continue;
-        // ---- the last item of entry j: the owning slice, then its block and element
-        __threadfence();
-        const unsigned long long mine =
-            tid < a.NSP ? __ldcg(a.wpart + (long long)j * a.NSP + tid) : 0ull;
-        unsigned long long incl = mine;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const unsigned long long o = __shfl_up_sync(0xffffffffu, incl, off);
-            if (lane >= off) incl += o;
-        }
-        if (lane == 31) woff[warp] = incl;
-        __syncthreads();
-        unsigned long long wb = 0ull, total = 0ull;
-        for (int w = 0; w < kWarps; ++w) {
-            if (w < warp) wb += woff[w];
-            total += woff[w];
-        }
-        const unsigned long long pre = wb + incl - mine;  // weight of the slices before
-        const unsigned long long tau = scale_floor(d.u, total);
-        if (tid == 0) s_owner = -1;
-        __syncthreads();
-        if (total > 0 && tid < a.NSP && mine > 0 && pre <= tau && tau - pre < mine) {
-            s_owner = tid;  // exactly one slice holds tau
-            s_pre = pre;
-        }
-        if (tid == 0) ds.token = -1;
-        __syncthreads();
-        bool degenerate = false;
-        if (total == 0) {
-            // The residual has no mass (reachable only through rounding or an
-            // unnormalised q): draw from p over the whole row (counted).
-            DrawCtx<DT> w = precise_slice_ctx<DT>(dyn, a, b, n, 0, (int)nch);
-            w.residual = false;
-            draw_precise<DT>(cluster, ds, w, degenerate);
-            degenerate = true;
-        } else if (s_owner >= 0) {
-            c0 = (long long)s_owner * a.SCP;
-            d = precise_slice_ctx<DT>(dyn, a, b, n, c0, (int)min((long long)a.SCP, nch - c0));
-            if (res) (void)precise_pass_b<DT, true, false, false>(d, inv);
-            else (void)precise_pass_b<DT, false, false, false>(d, inv);
-            __syncthreads();
-            const unsigned long long want = tau - s_pre;
-            int blk;
-            unsigned long long bbefore;
-            find_block(ds, d.bsum, d.nblk, want, &blk, &bbefore);
-            if (warp == 0) {
-                const int ci = blk * kBlockChunks + lane;
-                float l[kChunk] = {}, q[kChunk] = {};
-                unsigned long long W = 0;
+        const bool res = n < k;
+        const RowRec rec = a.rows[(long long)b * (k + 1) + n];
+        const DT* drow = static_cast<const DT*>(a.logits) + ((long long)b * (k + 1) + n) * V;
+        const float* qrow = res ? a.q + ((long long)b * k + n) * V : nullptr;
+        unsigned long long* rowblk = a.bsum + (long long)b * nbr * 2;
+        PreciseCls cl;
+        const float Sc = a.pS[j], dl = a.pD[j];
+        cl.inv = __frcp_rn(Sc);
+        cl.hi = 1.0f + dl;
+        cl.lo = 1.0f - dl;
+        cl.ey = fast_ey(Sc);
+        const float u = a.ur[b];
+        // ---- the slice's pass
+        {
+            const long long c0 = (long long)s * slb * kFastGroup;
+            DrawCtx<DT> d = slice_ctx<DT>(reinterpret_cast<unsigned char*>(rowblk + (c0 / kFastGroup) * 2),
+                                          drow, qrow, res, V, rec.mraw, a.c2, u, c0,
+                                          (int)min(slb * kFastGroup, nch - c0), rec.S);
+            d.thi = thi;
+            d.tlo = tlo;
+            const int fnb = (d.mych + kFastGroup - 1) / kFastGroup;
+            ff S{0.0f, 0.0f};
+            unsigned long long Yt = 0ull, Qt = 0ull;
+            for (int base = warp * 32; base < d.mych; base += kThreads) {
+                const int ci = base + lane;
+                unsigned long long cy = 0ull, cq = 0ull;
                 if (ci < d.mych) {
+                    float l[kChunk], q[kChunk] = {};
                     load_l(d, ci, l);
                     load_q(d, ci, res, q);
-                    W = res ? precise_chunk<DT, true, false, false>(d, ci, l, q, inv, 0ull, nullptr)
-                            : precise_chunk<DT, false, false, false>(d, ci, l, q, inv, 0ull, nullptr);
+                    ff es[kChunk];
+                    int cls[kChunk];
+                    precise_lin_chunk<DT>(d, ci, l, q, cl, res, S, cy, cq, es, cls);
+#pragma unroll
+                    for (int e = 0; e < kChunk; ++e)
+                        if (cls[e] == kPcAmb) {  // rare: list it
+                            const uint32_t w = atomicAdd(a.pambn + j, 1u);
+                            if (w < (uint32_t)kAmbCap) {
+                                AmbElem ae;
+                                ae.idx = (int)((d.c0 + ci) * kChunk + e);
+                                ae.q = q[e];
+                                ae.ehi = es[e].hi;
+                                ae.elo = es[e].lo;
+                                a.amb[(long long)j * kAmbCap + w] = ae;
+                            }
+                        }
                 }
-                const unsigned long long wb2 = want - bbefore;
-                unsigned long long cb;
-                if (find_lane(W, wb2, &cb)) {
-                    int tok = -1;
-                    if (res) precise_chunk<DT, true, false, false>(d, ci, l, q, inv, wb2 - cb, &tok);
-                    else precise_chunk<DT, false, false, false>(d, ci, l, q, inv, wb2 - cb, &tok);
-                    if (tok >= 0) ds.token = (int)((d.c0 + ci) * kChunk + tok);
+                Yt += cy;
+                Qt += cq;
+                const unsigned long long by = group_sum_u64(cy);
+                const unsigned long long bq = group_sum_u64(cq);
+                const int blk = (base + grp * kFastGroup) / kFastGroup;
+                if (gl == 0 && blk < fnb)
+                    reinterpret_cast<ulonglong2*>(d.bsum)[blk] = make_ulonglong2(by, bq);
+            }
+            // the slice's sums
+            Yt = warp_sum(Yt);
+            Qt = warp_sum(Qt);
+            S = warp_sum_ff(ff_normalize(S));
+            if (lane == 0) {
+                ps.ry[warp] = Yt;
+                ps.rq[warp] = Qt;
+                ps.rs[warp] = S;
+            }
+            __syncthreads();
+            if (tid == 0) {
+                PreciseItem r;
+                r.Y = 0ull;
+                r.Q = 0ull;
+                r.S = ff{0.0f, 0.0f};
+                r.pad = 0ull;
+                for (int w = 0; w < kWarps; ++w) {
+                    r.Y += ps.ry[w];
+                    r.Q += ps.rq[w];
+                    r.S = ff_add(r.S, ps.rs[w]);
                 }
+                a.items[it] = r;
+                __threadfence();
+                ps.last = atomicAdd(a.parrive + j, 1u) == (uint32_t)(nsl - 1);
+            }
+            __syncthreads();
+        }
+        if (!ps.last) continue;
+
+        // ---- the last slice of entry j: the token
+        __threadfence();
+        const long long ib = (long long)j * nsl;  // this entry's items: it - s .. + nsl
+        const long long it0 = it - s;
+        (void)ib;
+        PreciseItem mine;
+        mine.Y = 0ull;
+        mine.Q = 0ull;
+        mine.S = ff{0.0f, 0.0f};
+        if (tid < nsl) {
+            const ulonglong2 v0 = __ldcg(reinterpret_cast<const ulonglong2*>(a.items + it0 + tid));
+            const ulonglong2 v1 = __ldcg(reinterpret_cast<const ulonglong2*>(a.items + it0 + tid) + 1);
+            mine.Y = v0.x;
+            mine.Q = v0.y;
+            mine.S = ff{__uint_as_float((uint32_t)v1.x), __uint_as_float((uint32_t)(v1.x >> 32))};
+        }
+        // S, Y, Q totals (a block reduction in a fixed order)
+        {
+            const unsigned long long y = warp_sum(mine.Y), q = warp_sum(mine.Q);
+            const ff sw = warp_sum_ff(ff_normalize(mine.S));
+            if (lane == 0) {
+                ps.ry[warp] = y;
+                ps.rq[warp] = q;
+                ps.rs[warp] = sw;
+            }
+            __syncthreads();
+            if (tid == 0) {
+                unsigned long long Y = 0ull, Q = 0ull;
+                ff St{0.0f, 0.0f};
+                for (int w = 0; w < kWarps; ++w) {
+                    Y += ps.ry[w];
+                    Q += ps.rq[w];
+                    St = ff_add(St, ps.rs[w]);
+                }
+                ps.Y = Y;
+                ps.Q = Q;
+                ps.S = ff_normalize(St);
+                const uint32_t na = __ldcg(a.pambn + j);
+                ps.nb_amb = (int)min(na, (uint32_t)kAmbCap);
+                ps.fallback = na > (uint32_t)kAmbCap ||
+                              !(fabsf(__fsub_rn(ps.S.hi, Sc)) <= 0.5f * dl * ps.S.hi);
+                ps.token = -1;
+            }
+            __syncthreads();
+        }
+        const ff inv = ff_recip(ps.S);
+        if (!ps.fallback && warp == 0) {
+            // the listed elements: decided exactly, then sorted by index
+            AmbElem ae;
+            ae.idx = 0x7fffffff;
+            ae.q = 0.0f;
+            ae.ehi = 0.0f;
+            ae.elo = 0.0f;
+            if (lane < ps.nb_amb) {
+                const uint4 v = __ldcg(reinterpret_cast<const uint4*>(a.amb + (long long)j * kAmbCap + lane));
+                ae.idx = (int)v.x;
+                ae.q = __uint_as_float(v.y);
+                ae.ehi = __uint_as_float(v.z);
+                ae.elo = __uint_as_float(v.w);
+            }
+            unsigned long long y = 0ull, qq = 0ull;
+            if (lane < ps.nb_amb) {
+                const ff e{ae.ehi, ae.elo};
+                const ff pr = ff_mul(e, inv);
+                const ff d = two_sum(pr.hi, -ae.q);
+                const float w = __fadd_rn(d.hi, __fadd_rn(d.lo, pr.lo));
+                if (w > 0.0f) {
+                    y = ff_fixed(ff_normalize(e), cl.ey);
+                    qq = fix_pow2(ae.q, 62);
+                }
+            }
+            int rank = 0;
+            for (int o = 0; o < ps.nb_amb; ++o) {
+                const int oi = __shfl_sync(0xffffffffu, ae.idx, o);
+                rank += (oi < ae.idx || (oi == ae.idx && o < lane)) ? 1 : 0;
+            }
+            if (lane < ps.nb_amb) {
+                ps.amb[rank] = ae;
+                ps.ay[rank] = y;
+                ps.aq[rank] = qq;
             }
         }
         __syncthreads();
+        if (!ps.fallback && tid == 0) {
+            unsigned long long Y = ps.Y, Q = ps.Q;
+            for (int i = 0; i < ps.nb_amb; ++i) {
+                Y += ps.ay[i];
+                Q += ps.aq[i];
+            }
+            ps.M = ff_fixed(inv, 123 - cl.ey);
+            const long long Ctot = fast_cval(Y, Q, ps.M);
+            if (Ctot <= 0) ps.fallback = 1;  // no mass: the two-pass draw, from p
+            else ps.tau = scale_floor(u, (unsigned long long)Ctot);
+            ps.owner = -1;
+        }
+        __syncthreads();
+        bool degenerate = false;
+        if (ps.fallback) {
+            DrawCtx<DT> w = slice_ctx<DT>(dyn + 2 * kExpTable * sizeof(float), drow, qrow, res, V,
+                                          rec.mraw, a.c2, u, 0, (int)nch, rec.S);
+            w.thi = thi;
+            w.tlo = tlo;
+            if (tid == 0) ds.token = -1;
+            __syncthreads();
+            draw_precise<DT>(cluster, ds, w, degenerate);
+            __syncthreads();
+            if (tid == 0) ps.token = ds.token;
+            __syncthreads();
+        } else {
+            const unsigned long long M = ps.M, tau = ps.tau;
+            // the slice: each thread one slice's sums (and the listed elements in it)
+            unsigned long long sy = mine.Y, sq = mine.Q;
+            if (tid < nsl)
+                amb_in(ps, (long long)tid * slb * kFastGroup * kChunk,
+                       (long long)(tid + 1) * slb * kFastGroup * kChunk, sy, sq);
+            unsigned long long iy = sy, iq = sq;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const unsigned long long yo = __shfl_up_sync(0xffffffffu, iy, off);
+                const unsigned long long qo = __shfl_up_sync(0xffffffffu, iq, off);
+                if (lane >= off) {
+                    iy += yo;
+                    iq += qo;
+                }
+            }
+            if (lane == 31) {
+                ps.ry[warp] = iy;
+                ps.rq[warp] = iq;
+            }
+            __syncthreads();
+            unsigned long long wy = 0ull, wq = 0ull;
+            for (int w = 0; w < warp; ++w) {
+                wy += ps.ry[w];
+                wq += ps.rq[w];
+            }
+            const bool past = tid < nsl && fast_cval(wy + iy, wq + iq, M) > (long long)tau;
+            const unsigned bw = __ballot_sync(0xffffffffu, past);
+            if (lane == 0) ds.red_f[warp] = bw ? (float)(__ffs(bw) - 1) : -1.0f;
+            __syncthreads();
+            int owner = -1;
+            for (int w = 0; w < kWarps && owner < 0; ++w)
+                if (ds.red_f[w] >= 0.0f) owner = w * 32 + (int)ds.red_f[w];
+            if (tid == owner) {
+                ps.Y0 = wy + iy - sy;
+                ps.Q0 = wq + iq - sq;
+            }
+            __syncthreads();
+            if (owner >= 0) {  // uniform
+                // the block: one block per thread (a slice has at most kThreads blocks?
+                // no: each thread sums a contiguous range of them)
+                const long long b0 = (long long)owner * slb;
+                const int nbs = (int)min(slb, nbr - b0);
+                const int L = (nbs + kThreads - 1) / kThreads;
+                const int cb = min(nbs, tid * L), ce = min(nbs, cb + L);
+                const unsigned long long* bs = rowblk + b0 * 2;
+                unsigned long long my = 0ull, mq = 0ull;
+                for (int i = cb; i < ce; ++i) {
+                    const ulonglong2 v = __ldcg(reinterpret_cast<const ulonglong2*>(bs) + i);
+                    my += v.x;
+                    mq += v.y;
+                }
+                if (ce > cb)
+                    amb_in(ps, (b0 + cb) * kFastGroup * kChunk, (b0 + ce) * kFastGroup * kChunk, my, mq);
+                unsigned long long jy = my, jq = mq;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const unsigned long long yo = __shfl_up_sync(0xffffffffu, jy, off);
+                    const unsigned long long qo = __shfl_up_sync(0xffffffffu, jq, off);
+                    if (lane >= off) {
+                        jy += yo;
+                        jq += qo;
+                    }
+                }
+                __syncthreads();
+                if (lane == 31) {
+                    ps.ry[warp] = jy;
+                    ps.rq[warp] = jq;
+                }
+                __syncthreads();
+                unsigned long long vy = ps.Y0, vq = ps.Q0;
+                for (int w = 0; w < warp; ++w) {
+                    vy += ps.ry[w];
+                    vq += ps.rq[w];
+                }
+                const unsigned long long ty0 = vy + jy - my, tq0 = vq + jq - mq;  // before cb
+                const bool bp = ce > cb && fast_cval(ty0 + my, tq0 + mq, M) > (long long)tau;
+                const unsigned bb = __ballot_sync(0xffffffffu, bp);
+                __syncthreads();
+                if (lane == 0) ds.red_f[warp] = bb ? (float)(__ffs(bb) - 1) : -1.0f;
+                __syncthreads();
+                int first = -1;
+                for (int w = 0; w < kWarps && first < 0; ++w)
+                    if (ds.red_f[w] >= 0.0f) first = w * 32 + (int)ds.red_f[w];
+                if (tid == first) {
+                    unsigned long long ry = ty0, rq = tq0;
+                    int i = cb;
+                    for (; i < ce - 1; ++i) {
+                        const ulonglong2 v = __ldcg(reinterpret_cast<const ulonglong2*>(bs) + i);
+                        unsigned long long y = v.x, q = v.y;
+                        amb_in(ps, (b0 + i) * kFastGroup * kChunk, (b0 + i + 1) * kFastGroup * kChunk, y, q);
+                        if (fast_cval(ry + y, rq + q, M) > (long long)tau) break;
+                        ry += y;
+                        rq += q;
+                    }
+                    ps.blk = (int)(b0 + i);
+                    ps.bY = ry;
+                    ps.bQ = rq;
+                }
+                __syncthreads();
+                if (first >= 0 && warp == 0) {
+                    // the chunk: lanes 0..7 recompute the block's chunks
+                    DrawCtx<DT> d = slice_ctx<DT>(dyn, drow, qrow, res, V, rec.mraw, a.c2, u, 0,
+                                                  (int)nch, rec.S);
+                    d.thi = thi;
+                    d.tlo = tlo;
+                    const int ci = ps.blk * kFastGroup + (lane & (kFastGroup - 1));
+                    const bool have = lane < kFastGroup && ci < nch;
+                    float l[kChunk] = {}, q[kChunk] = {};
+                    ff es[kChunk];
+                    int cls[kChunk];
+                    ff Sd{0.0f, 0.0f};
+                    unsigned long long cy = 0ull, cq = 0ull;
+                    if (have) {
+                        load_l(d, ci, l);
+                        load_q(d, ci, res, q);
+                        precise_lin_chunk<DT>(d, ci, l, q, cl, res, Sd, cy, cq, es, cls);
+                        amb_in(ps, (long long)ci * kChunk, (long long)(ci + 1) * kChunk, cy, cq);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < kChunk; ++e) {
+                            es[e] = ff{0.0f, 0.0f};
+                            cls[e] = kPcZero;
+                        }
+                    }
+                    unsigned long long iy2 = cy, iq2 = cq;
+#pragma unroll
+                    for (int off = 1; off < kFastGroup; off <<= 1) {
+                        const unsigned long long yo = __shfl_up_sync(0xffffffffu, iy2, off);
+                        const unsigned long long qo = __shfl_up_sync(0xffffffffu, iq2, off);
+                        if (lane >= off) {
+                            iy2 += yo;
+                            iq2 += qo;
+                        }
+                    }
+                    const unsigned long long ly = ps.bY + iy2 - cy, lq = ps.bQ + iq2 - cq;
+                    const bool lp = have && fast_cval(ly + cy, lq + cq, M) > (long long)tau;
+                    const unsigned bl = __ballot_sync(0xffffffffu, lp);
+                    if (bl && lane == __ffs(bl) - 1) {
+                        // the element: walk the chunk in the pass's order
+                        ff Y{0.0f, 0.0f}, Q{0.0f, 0.0f};
+                        int tok = -1;
+                        for (int e = 0; e < kChunk && tok < 0; ++e) {
+                            const long long idx = (long long)ci * kChunk + e;
+                            bool pos = cls[e] == kPcPos;
+                            if (pos) {
+                                ff_accumulate(Y, es[e]);
+                                if (res) ff_acc1(Q, q[e]);
+                            }
+                            unsigned long long py = ff_fixed(ff_normalize(Y), cl.ey);
+                            unsigned long long pq = res ? ff_fixed(ff_normalize(Q), 62) : 0ull;
+                            unsigned long long ea = 0ull, eq = 0ull;
+                            amb_in(ps, (long long)ci * kChunk, idx + 1, ea, eq);
+                            for (int i = 0; i < ps.nb_amb; ++i)
+                                if (ps.amb[i].idx == idx && ps.ay[i] > 0ull) pos = true;
+                            if (pos && fast_cval(ly + py + ea, lq + pq + eq, M) > (long long)tau) tok = e;
+                        }
+                        if (tok >= 0) ps.token = (int)(ci * kChunk + tok);
+                    }
+                }
+                __syncthreads();
+            }
+        }
         if (tid == 0) {
-            if (ds.token >= 0) a.out[(long long)b * (a.k + 1) + n] = ds.token;
+            if (ps.token >= 0) a.out[(long long)b * (k + 1) + n] = ps.token;
             if (degenerate) a.seqstat[b] = SV_DEV_PRECISE | SV_DEV_DEGENERATE;
             a.parrive[j] = 0u;
         }
@@ -3903,10 +4271,8 @@ static sv_status device_setup(int* sms) {
             SV_TRY(cluster_attrs(sv_match_draw_kernel<__nv_bfloat16>, true));
             SV_TRY(cluster_attrs(sv_match_draw_kernel<float>, true));
             SV_TRY(cluster_attrs(sv_precise_kernel<float>, true));
-            SV_TRY(cluster_attrs(sv_split_precise_a_kernel<__nv_bfloat16>, true));
-            SV_TRY(cluster_attrs(sv_split_precise_a_kernel<float>, true));
-            SV_TRY(cluster_attrs(sv_split_precise_b_kernel<__nv_bfloat16>, true));
-            SV_TRY(cluster_attrs(sv_split_precise_b_kernel<float>, true));
+            SV_TRY(cluster_attrs(sv_split_precise_kernel<__nv_bfloat16>, true));
+            SV_TRY(cluster_attrs(sv_split_precise_kernel<float>, true));
             SV_TRY(cluster_attrs(sv_rows_kernel<__nv_bfloat16, true, 128>, false));
             SV_TRY(cluster_attrs(sv_rows_kernel<__nv_bfloat16, true, 256>, false));
             SV_TRY(cluster_attrs(sv_rows_kernel<__nv_bfloat16, true, 512>, false));
@@ -3959,7 +4325,7 @@ static sv_status device_setup(int* sms) {
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 static sv_status check_common(const void* logits, sv_dtype dt, const int32_t* x, int B, int k,
-                              int V, void* ws, size_t ws_bytes) {
+                              int V, void* ws, size_t ws_bytes, bool base_ws = false) {
     if (dt != SV_BF16 && dt != SV_F32) return SV_ERR_INVALID_ARG;
     if (B < 0 || k < 1 || V < 1) return SV_ERR_INVALID_ARG;
     if (k > kMaxK || V > kMaxV) return SV_ERR_UNSUPPORTED;
@@ -3969,7 +4335,7 @@ static sv_status check_common(const void* logits, sv_dtype dt, const int32_t* x,
     if (B > 0 && (!aligned16(logits) || !aligned16(x))) return SV_ERR_INVALID_ARG;
     if (!ws) return SV_ERR_WORKSPACE;
     if (!aligned16(ws)) return SV_ERR_INVALID_ARG;
-    if (ws_bytes < ws_bytes_for(B, k, V)) return SV_ERR_WORKSPACE;
+    if (ws_bytes < (base_ws ? ws_base_bytes(B, k) : ws_bytes_for(B, k, V))) return SV_ERR_WORKSPACE;
     return SV_OK;
 }
 
@@ -4283,9 +4649,9 @@ static int draw_split_wide(int B, int V, int sms) {
 }
 
 // The split draw of a sampled verify: a memset of the list's counter and the
-// arrival counters, sv_split_draw_kernel (B * NS CTAs), then the two precise
-// launches (persistent, 2 CTAs per SM; they return at once when no draw was
-// listed), each a programmatic dependent of the one before.
+// arrival counters, sv_split_draw_kernel (B * NS CTAs), then the precise launch
+// (persistent, 2 CTAs per SM, a programmatic dependent; it returns at once when
+// no draw was listed).
 static sv_status launch_split(const void* logits, sv_dtype dt, const float* q, const int32_t* x,
                               const float* ua, const float* ur, float T, int B, int k, int V,
                               int32_t* out, int32_t* nacc, void* ws, cudaStream_t stream, int sms,
@@ -4303,11 +4669,16 @@ static sv_status launch_split(const void* logits, sv_dtype dt, const float* q, c
     a.nacc = nacc;
     a.plist_count = reinterpret_cast<uint32_t*>(w + ws_plist_offset(B, k));
     a.plist = a.plist_count + 4;
-    a.arrive = reinterpret_cast<uint32_t*>(w + ws_split_offset(B, k));
-    a.parrive = a.arrive + B;
-    const size_t srec_off = (ws_split_offset(B, k) + (size_t)B * 2 * sizeof(uint32_t) + 15) &
-                            ~(size_t)15;
-    a.srec = reinterpret_cast<FastTotals*>(w + srec_off);
+    const size_t so = ws_split_offset(B, k);
+    const SplitLayout lay = split_layout(B, V);
+    a.arrive = reinterpret_cast<uint32_t*>(w + so);
+    a.parrive = reinterpret_cast<uint32_t*>(w + so + lay.parrive);
+    a.pambn = reinterpret_cast<uint32_t*>(w + so + lay.pambn);
+    a.pS = reinterpret_cast<float*>(w + so + lay.pS);
+    a.pD = reinterpret_cast<float*>(w + so + lay.pD);
+    a.srec = reinterpret_cast<FastTotals*>(w + so + lay.srec);
+    a.bsum = reinterpret_cast<unsigned long long*>(w + so + lay.bsum);
+    a.nbr = split_row_blocks(V);
     a.ep = ep;
     a.B = B;
     a.k = k;
@@ -4322,10 +4693,16 @@ static sv_status launch_split(const void* logits, sv_dtype dt, const float* q, c
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((long long)B * a.NS), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = split_smem_bytes(a.SC);
     cfg.stream = stream;
-    e = dt == SV_BF16 ? cudaLaunchKernelEx(&cfg, sv_split_draw_kernel<__nv_bfloat16, true>, a)
-                      : cudaLaunchKernelEx(&cfg, sv_split_draw_kernel<float, true>, a);
+    // float-float chunk sums (a tighter bound, fewer precise draws) on small
+    // batches, whose draws are latency; pairwise on large ones, whose fast pass
+    // is instruction-bound
+    if (B < sms)
+        e = dt == SV_BF16 ? cudaLaunchKernelEx(&cfg, sv_split_draw_kernel<__nv_bfloat16, true>, a)
+                          : cudaLaunchKernelEx(&cfg, sv_split_draw_kernel<float, true>, a);
+    else
+        e = dt == SV_BF16 ? cudaLaunchKernelEx(&cfg, sv_split_draw_kernel<__nv_bfloat16, false>, a)
+                          : cudaLaunchKernelEx(&cfg, sv_split_draw_kernel<float, false>, a);
     if (e != cudaSuccess) return SV_ERR_CUDA;
 
     SplitPreciseArgs pa;
@@ -4337,33 +4714,32 @@ static sv_status launch_split(const void* logits, sv_dtype dt, const float* q, c
     pa.plist_count = a.plist_count;
     pa.plist = a.plist;
     pa.parrive = a.parrive;
+    pa.pambn = a.pambn;
+    pa.pS = a.pS;
+    pa.pD = a.pD;
+    pa.amb = reinterpret_cast<AmbElem*>(w + so + lay.amb);
+    pa.items = reinterpret_cast<PreciseItem*>(w + so + lay.items);
+    pa.bsum = a.bsum;
+    pa.nbr = a.nbr;
     pa.seqstat = a.seqstat;
     pa.out = out;
     pa.B = B;
     pa.k = k;
     pa.V = V;
-    pa.NSP = precise_slices(B, V, &pa.SCP);
     pa.c2 = a.c2;
-    pa.spart = reinterpret_cast<ff*>(w + srec_off + (size_t)B * a.NS * sizeof(FastTotals));
-    pa.wpart = reinterpret_cast<unsigned long long*>(pa.spart + (size_t)B * pa.NSP);
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     attr[1] = cluster_attr(1);
     cudaLaunchConfig_t pc = {};
-    const long long maxitems = (long long)B * pa.NSP;
-    pc.gridDim = dim3((unsigned)std::min<long long>(2LL * sms, maxitems), 1, 1);
+    pc.gridDim = dim3((unsigned)std::min(2 * sms, kPreciseGrid), 1, 1);
     pc.blockDim = dim3(kThreads, 1, 1);
-    pc.dynamicSmemBytes = split_precise_smem_bytes(V, pa.SCP);
+    pc.dynamicSmemBytes = split_precise_smem_bytes(V);
     pc.stream = stream;
     pc.attrs = attr;
-    pc.numAttrs = 1;
-    e = dt == SV_BF16 ? cudaLaunchKernelEx(&pc, sv_split_precise_a_kernel<__nv_bfloat16>, pa)
-                      : cudaLaunchKernelEx(&pc, sv_split_precise_a_kernel<float>, pa);
-    if (e != cudaSuccess) return SV_ERR_CUDA;
     pc.numAttrs = 2;
-    e = dt == SV_BF16 ? cudaLaunchKernelEx(&pc, sv_split_precise_b_kernel<__nv_bfloat16>, pa)
-                      : cudaLaunchKernelEx(&pc, sv_split_precise_b_kernel<float>, pa);
+    e = dt == SV_BF16 ? cudaLaunchKernelEx(&pc, sv_split_precise_kernel<__nv_bfloat16>, pa)
+                      : cudaLaunchKernelEx(&pc, sv_split_precise_kernel<float>, pa);
     return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
@@ -4647,6 +5023,10 @@ size_t spec_verify_workspace_size(int B, int k, int V, sv_dtype dtype) {
 namespace sv {
 
 // The options of a _tuned call are checked like any other argument.
+static sv_tuning cluster_draw(sv_tuning t) {
+    t.draw_mode = 2;
+    return t;
+}
 static bool tuning_valid(const sv_tuning& t) {
     auto pow2 = [](int g) { return g == 0 || g == 1 || g == 2 || g == 4 || g == 8 || g == 16; };
     return t.path >= 0 && t.path <= 3 && pow2(t.draw_split) && pow2(t.precise_split) &&
@@ -4702,8 +5082,10 @@ static sv_status verify_impl(bool sampled, const void* logits, sv_dtype dtype,
                              const float* u_accept, const float* u_resample, float T, int B,
                              int k, int V, int32_t* out_tokens, int32_t* num_accepted, void* ws,
                              size_t ws_bytes, int32_t* kv_len, sv_spec_stats* stats,
-                             cudaStream_t stream, const sv_tuning& tu) {
-    sv_status st = check_common(logits, dtype, draft_tokens, B, k, V, ws, ws_bytes);
+                             cudaStream_t stream, const sv_tuning& tu, bool base_ws = false) {
+    // base_ws: a workspace without the split draw's region (the no-allocation
+    // entry point), so the draw is the cluster draw
+    sv_status st = check_common(logits, dtype, draft_tokens, B, k, V, ws, ws_bytes, base_ws);
     if (st != SV_OK) return st;
     if ((st = check_outputs(out_tokens, num_accepted, B)) != SV_OK) return st;
     if (sampled && (st = check_sample(draft_probs, u_accept, u_resample, T, B)) != SV_OK) return st;
@@ -4714,7 +5096,8 @@ static sv_status verify_impl(bool sampled, const void* logits, sv_dtype dtype,
     return run_verify(sampled, logits, dtype, sampled ? draft_probs : nullptr, draft_tokens,
                       sampled ? u_accept : nullptr, sampled ? u_resample : nullptr,
                       sampled ? T : 1.0f, B, k, V, out_tokens, num_accepted, ws, stream, sms,
-                      Epilogue{kv_len, reinterpret_cast<unsigned long long*>(stats)}, tu);
+                      Epilogue{kv_len, reinterpret_cast<unsigned long long*>(stats)},
+                      base_ws ? cluster_draw(tu) : tu);
 }
 
 static sv_status tree_impl(sv_mode mode, const void* logits, sv_dtype dtype,
@@ -5100,11 +5483,7 @@ namespace sv {
 
 constexpr size_t kNoAllocScratchBytes = SV_NOALLOC_SCRATCH_BYTES;
 static_assert(kNoAllocScratchBytes >= 256 + 32 * (size_t)SV_NOALLOC_MAX_ROWS +
-                                          12 * (size_t)(SV_NOALLOC_MAX_ROWS / 2) + 31 +
-                                          8 * (size_t)(SV_NOALLOC_MAX_ROWS / 2) + 31 +
-                                          (size_t)kSplitMaxTotal *
-                                              (sizeof(FastTotals) + sizeof(ff) + 8) +
-                                          255,
+                                          12 * (size_t)(SV_NOALLOC_MAX_ROWS / 2) + 31 + 255,
               "scratch size");
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
@@ -5144,7 +5523,7 @@ extern "C" sv_status spec_verify_sample_noalloc(const void* logits, sv_dtype dty
     void* ws = nullptr;
     sv_status st = sv::noalloc_scratch(&ws);
     if (st != SV_OK) return st;
-    return spec_verify_sample(logits, dtype, draft_probs, draft_tokens, u_accept, u_resample, T,
-                              B, k, V, out_tokens, num_accepted, ws, sv::kNoAllocScratchBytes,
-                              stream);
+    return sv::verify_impl(true, logits, dtype, draft_probs, draft_tokens, u_accept, u_resample,
+                           T, B, k, V, out_tokens, num_accepted, ws, sv::kNoAllocScratchBytes,
+                           nullptr, nullptr, stream, sv::kAuto, true);
 }

@@ -7,7 +7,7 @@ Builds the seeded inputs of the workload (optionally with another batch size),
 copies them to the GPU, and calls spec_verify_sample / spec_verify_greedy
 `reps` times on one stream, then prints the status word.  `--path` forces the
 two-kernel (1), fused (2) or row-skipping (3) path; 0 keeps the automatic
-choice; `--match` runs the sample-and-match verify (spec_verify_match) on a
+choice; `--draw-mode` the sampled draw (1 split, 2 cluster); `--match` runs the sample-and-match verify (spec_verify_match) on a
 sampled workload instead.  Nothing is timed here: the point is a fixed, short sequence of
 launches that a profiler can select from with its skip / count options.
 """
@@ -29,6 +29,8 @@ def main(argv=None):
     ap.add_argument("--path", type=int, default=0, choices=[0, 1, 2, 3])
     ap.add_argument("--reps", type=int, default=4)
     ap.add_argument("--match", action="store_true", help="sample-and-match verify")
+    ap.add_argument("--draw-mode", type=int, default=0, choices=[0, 1, 2],
+                    help="sampled draw: 1 split, 2 cluster (0 automatic)")
     a = ap.parse_args(argv)
     kw = dict(I.WORKLOADS[a.workload])
     if a.batch > 0:
@@ -44,7 +46,7 @@ def main(argv=None):
     ws = sv.workspace(B, k, V, logits.dtype, dev)
     out = torch.empty((B, k + 1), dtype=torch.int32, device=dev)
     n = torch.empty(B, dtype=torch.int32, device=dev)
-    tu = sv.Tuning(path=a.path) if a.path else None
+    tu = sv.Tuning(path=a.path, draw_mode=a.draw_mode) if (a.path or a.draw_mode) else None
     if inp.mode == "greedy":
         for _ in range(a.reps):
             sv.spec_verify_greedy(logits, x, out, n, ws, tuning=tu)
@@ -61,7 +63,8 @@ def main(argv=None):
             sv.spec_verify_sample(logits, q, x, ua, ur, inp.T, out, n, ws, tuning=tu)
     torch.cuda.synchronize(dev)
     st, bits, ndeg = sv.spec_verify_read_status(ws)
-    print(f"{a.workload} B={B} k={k} V={V} path={a.path} match={a.match} reps={a.reps}: status {st} "
+    print(f"{a.workload} B={B} k={k} V={V} path={a.path} draw_mode={a.draw_mode} match={a.match} "
+          f"reps={a.reps}: status {st} "
           f"bits {bits:#x} degenerate {ndeg}")
 
 

@@ -27,7 +27,7 @@ SV_DEV_BAD_TREE = 0x40
 EXPORTS = ("spec_verify_workspace_size", "spec_verify_greedy", "spec_verify_sample",
            "spec_verify_rows", "spec_verify_finish", "spec_verify_read_status",
            "spec_verify_row_stats", "spec_verify_status_string", "spec_verify_sample_noalloc")
-SV_NOALLOC_SCRATCH_BYTES = 2097152
+SV_NOALLOC_SCRATCH_BYTES = 1048576
 SV_NOALLOC_MAX_ROWS = 27000
 
 _lib = None
