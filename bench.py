@@ -71,7 +71,7 @@ def dist_env():
 # code draws on, and the kernels that also run the draw.
 _COMMON_SECTIONS = ("workspace", "small helpers", "online softmax partials")
 _DRAWING = ("sv_verify_kernel", "sv_finish_sample_kernel", "sv_precise_kernel",
-            "sv_match_draw_kernel")
+            "sv_match_draw_kernel", "sv_split_draw_kernel", "sv_split_precise_kernel")
 
 
 def kernel_source_hash(kernel=None):
@@ -520,7 +520,7 @@ def main():
             # the draw stage of a large sampled batch is two kernels: the fast draw
             # and the precise draws it hands on
             fin_name = ("sv_finish_greedy_kernel" if inp.mode == "greedy"
-                        else "sv_finish_sample_kernel+sv_precise_kernel" if path == sv.PATH_SKIP
+                        else "sv_split_draw_kernel+sv_split_precise_kernel" if path == sv.PATH_SKIP
                         else "sv_finish_sample_kernel")
             stage_times = {rows_kname: stage_ms(rows_stage),
                            fin_name: stage_ms(finish_stage)}

@@ -32,15 +32,18 @@ sv_status spec_verify_debug_ffexp(const float* l, float m, float T, int n, doubl
  *                  1 KiB or its clusters cover every SM; else the two-kernel
  *                  path);
  *   force_precise  1: every sampled draw takes the precise float-float pass;
- *   draw_split     the sampled draw kernel's cluster size (1, 2, 4, 8, 16);
+ *   draw_split     the sampled draw kernel's cluster size (1, 2, 4, 8, 16); under
+ *                  the split draw, at most this many slices per row;
  *   precise_split  the cluster size of the precise-draw kernel of large batches;
  *   fused_defer    the fused kernel hands the draws that need the precise pass
  *                  to a separate kernel: 1 always, 2 never (0: when B is at
  *                  least the SM count);
  *   fused_pad_kib  the fused kernel's minimum dynamic shared memory per CTA
  *                  (KiB, up to 160), limiting how many share an SM;
- *   rows_split     the two-kernel path's row stream: CTAs per row (1..16, a
- *                  power of two);
+ *   rows_split     the row stream's CTAs per row (1..16, a power of two): a
+ *                  cluster per row on the two-kernel path; on the row-skipping
+ *                  path (at most 8; automatic: 1) separate CTAs merged through
+ *                  the workspace;
  *   rows_threads   its threads per CTA (128, 256, 512 or 1024);
  *   flat_off       1: greedy batches never take the flat row stream (the whole
  *                  logits tensor cut into one equal range per resident CTA);
@@ -48,8 +51,8 @@ sv_status spec_verify_debug_ffexp(const float* l, float m, float T, int n, doubl
  *   draw_mode      the sampled draw of the two-kernel and row-skipping paths:
  *                  1 the split draw (slices of the decision row on separate
  *                  CTAs, when the workspace holds its sums), 2 the cluster
- *                  draw (one cluster per sequence); 0 automatic (the cluster
- *                  draw). */
+ *                  draw (one cluster per sequence); 0 automatic (the split
+ *                  draw on the row-skipping path, else the cluster draw). */
 typedef struct {
     int path;
     int force_precise;

@@ -185,17 +185,19 @@ __device__ __forceinline__ unsigned long long fix_mag(float x) {
     return ex == 0 ? 0ull : v;  // zero or subnormal: below the resolution
 }
 
-// floor(x 2^s) for a float x >= 0 with x 2^s < 2^64, from the float's bits by
-// integer shifts (a 64-bit float-to-integer conversion would run on the
-// FP64 pipe, which is narrow on this GPU); 0 for zero and subnormals.
+// floor(x 2^s) for a float x >= 0 and 0 <= s <= 127 with x 2^s < 2^64.  The
+// scaled value v = x 2^s is exact, and so are its two halves: h = floor(v /
+// 2^32) has at most 24 significant bits (v has 24), and v - h 2^32, a multiple
+// of ulp(v) below 2^32, fits a float too; each half is converted toward zero
+// (32-bit conversions: a 64-bit one runs on the narrow FP64 pipe).  Zero and
+// subnormal x give 0 (x 2^s < 2^-3 then).
 __device__ __forceinline__ unsigned long long fix_pow2(float x, int s) {
-    const uint32_t b = __float_as_uint(x);
-    const int ex = (int)(b >> 23);
-    const unsigned long long mant = (unsigned long long)((b & 0x7FFFFFu) | 0x800000u);
-    const int sh = ex - 150 + s;  // x 2^s = mant 2^sh
-    const unsigned long long left = mant << (sh > 0 ? sh : 0);
-    const unsigned long long right = mant >> (sh < 0 ? (sh > -63 ? -sh : 63) : 0);
-    return ex == 0 ? 0ull : (sh >= 0 ? left : right);
+    const float v = __fmul_rn(x, __int_as_float((127 + s) << 23));
+    const float hf = __fmul_rn(v, 2.3283064365386963e-10f);  // v / 2^32
+    const uint32_t h = __float2uint_rz(hf);
+    const float lf = __fmaf_rn(-__uint2float_rn(h), 4294967296.0f, v);
+    const uint32_t l = __float2uint_rz(lf);
+    return ((unsigned long long)h << 32) | l;
 }
 
 // Fixed-point value of a non-negative float-float (hi >= 0, |lo| <= ulp(hi)).

@@ -120,8 +120,17 @@ __host__ __device__ inline size_t ws_split_offset(long long B, int k) {
     return (ws_plist_offset(B, k) + 16 + (size_t)B * sizeof(uint32_t) + 15) & ~(size_t)15;
 }
 __host__ __device__ size_t split_ws_bytes(long long B, int V);
+// Then the split row-skipping stream's region: per row an arrival counter, up
+// to 8 partial statistics of 16 bytes and a 16-byte record of its gathers.
+__host__ __device__ inline size_t ws_rowsplit_offset(long long B, int k, int V) {
+    return (ws_split_offset(B, k) + split_ws_bytes(B, V) + 15) & ~(size_t)15;
+}
+__host__ __device__ inline size_t rowsplit_bytes(long long B, int k) {
+    const size_t R = (size_t)B * (k + 1);
+    return ((R * 4 + 15) & ~(size_t)15) + R * 8 * 16 + R * 16;
+}
 __host__ __device__ inline size_t ws_bytes_for(long long B, int k, int V) {
-    size_t b = ws_split_offset(B, k) + split_ws_bytes(B, V);
+    size_t b = ws_rowsplit_offset(B, k, V) + rowsplit_bytes(B, k);
     return (b + 255) & ~(size_t)255;
 }
 // Without the split region (every path but the split draw).
@@ -873,14 +882,14 @@ struct Tree8 {
 template <int E, bool RES, bool EXACT>
 __device__ __forceinline__ void fast_chunk_elem(const float* l, const float* q, const FastScale& f,
                                                 ff& Y, ff& Q, Tree8& ty, Tree8& tq, Tree8& tr,
-                                                float& aq, float& qmin, float* yp, float* qp) {
+                                                float& aq, uint32_t& qor, float* yp, float* qp) {
     const float y = fast_y(l[E], f);
     bool pos = true;
     if (RES) {
         pos = __fmul_rn(y, f.ih) > q[E];
         const bool und = !pos && !(__fmul_rn(y, f.il) < q[E]);
         aq = und ? __fadd_rn(aq, q[E]) : aq;
-        qmin = fminf(qmin, q[E]);
+        qor |= __float_as_uint(q[E]);  // the sign bits: a negative q
     }
     const float yv = pos ? y : 0.0f, qv = (RES && pos) ? q[E] : 0.0f;
     if (yp) {
@@ -894,30 +903,32 @@ __device__ __forceinline__ void fast_chunk_elem(const float* l, const float* q, 
         ty.add<E>(yv);
         if (RES) tq.add<E>(qv);
     }
-    tr.add<E>(pos ? 0.0f : y);
+    tr.add<E>(__fsub_rn(y, yv));  // the other elements' y (exact: yv is y or 0)
 }
 
 // One chunk (8 elements, logits l and q) of the fast pass: the fixed-point
 // sums of the positive elements' y and q (cy, cq), the other elements' y
-// summed pairwise (returned), the undecided elements' q into aq, the smallest q
-// into qmin; with `yp`, yp and qp receive each element's y and q when it is
-// positive, else 0.  A NaN q is undecided (its bound is NaN, so the draw goes
-// to the precise pass, which weighs it 0); a negative q is caught by the
-// caller through qmin.
+// summed pairwise (returned), the undecided elements' q into aq; qmin becomes
+// -1 when a q of the chunk has its sign bit set (a negative q, caught by the
+// caller; -0 too, conservatively); with `yp`, yp and qp receive each element's
+// y and q when it is positive, else 0.  A NaN q is undecided (its bound is NaN,
+// so the draw goes to the precise pass, which weighs it 0).
 template <bool RES, bool EXACT>
 __device__ __forceinline__ float fast_chunk(const float* l, const float* q, const FastScale& f,
                                             unsigned long long& cy, unsigned long long& cq,
                                             float& aq, float& qmin, float* yp, float* qp) {
     ff Y{0.0f, 0.0f}, Q{0.0f, 0.0f};
     Tree8 ty{}, tq{}, tr{};
-    fast_chunk_elem<0, RES, EXACT>(l, q, f, Y, Q, ty, tq, tr, aq, qmin, yp, qp);
-    fast_chunk_elem<1, RES, EXACT>(l, q, f, Y, Q, ty, tq, tr, aq, qmin, yp, qp);
-    fast_chunk_elem<2, RES, EXACT>(l, q, f, Y, Q, ty, tq, tr, aq, qmin, yp, qp);
-    fast_chunk_elem<3, RES, EXACT>(l, q, f, Y, Q, ty, tq, tr, aq, qmin, yp, qp);
-    fast_chunk_elem<4, RES, EXACT>(l, q, f, Y, Q, ty, tq, tr, aq, qmin, yp, qp);
-    fast_chunk_elem<5, RES, EXACT>(l, q, f, Y, Q, ty, tq, tr, aq, qmin, yp, qp);
-    fast_chunk_elem<6, RES, EXACT>(l, q, f, Y, Q, ty, tq, tr, aq, qmin, yp, qp);
-    fast_chunk_elem<7, RES, EXACT>(l, q, f, Y, Q, ty, tq, tr, aq, qmin, yp, qp);
+    uint32_t qor = 0u;
+    fast_chunk_elem<0, RES, EXACT>(l, q, f, Y, Q, ty, tq, tr, aq, qor, yp, qp);
+    fast_chunk_elem<1, RES, EXACT>(l, q, f, Y, Q, ty, tq, tr, aq, qor, yp, qp);
+    fast_chunk_elem<2, RES, EXACT>(l, q, f, Y, Q, ty, tq, tr, aq, qor, yp, qp);
+    fast_chunk_elem<3, RES, EXACT>(l, q, f, Y, Q, ty, tq, tr, aq, qor, yp, qp);
+    fast_chunk_elem<4, RES, EXACT>(l, q, f, Y, Q, ty, tq, tr, aq, qor, yp, qp);
+    fast_chunk_elem<5, RES, EXACT>(l, q, f, Y, Q, ty, tq, tr, aq, qor, yp, qp);
+    fast_chunk_elem<6, RES, EXACT>(l, q, f, Y, Q, ty, tq, tr, aq, qor, yp, qp);
+    fast_chunk_elem<7, RES, EXACT>(l, q, f, Y, Q, ty, tq, tr, aq, qor, yp, qp);
+    if (RES && (qor >> 31)) qmin = -1.0f;
     if (EXACT) {
         cy = ff_fixed(ff_normalize(Y), f.ey);
         cq = RES ? ff_fixed(ff_normalize(Q), 62) : 0ull;
@@ -2117,6 +2128,57 @@ struct RowsArgs {
 // computed.  stop[] must hold 0xFFFFFFFF when the grid starts.
 // At most 64 registers per thread: 2048 threads' worth of CTAs per SM stay
 // resident (2 CTAs of 512 threads; 1 of 1024 threads).
+// The record of row `row` (sequence b, position i) from its merged statistics
+// p and its gathers (token xi, l(x), q(x), u_accept); on the row-skipping
+// stream also the row's test, and the sequence's stop row lowered when the
+// scan would end here.
+template <bool SAMPLED>
+__device__ __forceinline__ void write_row_record(const RowsArgs& a, const Partial& p, int b, int i,
+                                                 long long row, int xi, float lx, float qx,
+                                                 float ua) {
+    const int k = a.k, V = a.V;
+    RowRec rec;
+    rec.mraw = p.m;
+    rec.S = SAMPLED ? p.s : 0.0f;
+    rec.argmax = p.idx < 0 ? 0 : p.idx;
+    rec.px = 0.0;
+    rec.lx = NAN;
+    rec.qx = NAN;
+    uint32_t fl = row_flags<SAMPLED>(p);
+    bool ends = false;  // the scan stops at this row (sequences with `skip`)
+    if (i < k && a.x) {
+        if (xi < 0 || xi >= V) {
+            fl |= kRowTokenBad;
+        } else {
+            rec.lx = lx;
+            if (SAMPLED) {
+                rec.qx = qx;
+                if (!(qx >= 0.0f)) fl |= kRowQBad;
+                if (!(fl & kRowBad)) {
+                    ff ex = exp_rel(lx, p.m, a.c2, g_exp2_table.hi, g_exp2_table.lo);
+                    rec.px = (double)__fdiv_rn(ex.hi, p.s);
+                }
+            }
+        }
+        if (a.skip) {
+            // The same tests, in the same arithmetic, as the finish kernels' scans.
+            if (fl & (kRowBad | kRowTokenBad | kRowQBad)) {
+                ends = true;
+            } else if (SAMPLED) {
+                const float P = (float)rec.px, Q = rec.qx;
+                ends = !(ua >= 0.0f && ua < 1.0f) || !((P >= Q) || (ua < __fdiv_rn(P, Q)));
+            } else {
+                ends = xi != rec.argmax;
+            }
+        }
+    } else {
+        rec.px = NAN;
+    }
+    rec.flags = fl;
+    a.rows[row] = rec;
+    if (ends) atomicMin(a.stop + b, (uint32_t)i);
+}
+
 template <typename DT, bool SAMPLED, int NT>
 __global__ void __launch_bounds__(NT, 1024 / NT) sv_rows_kernel(RowsArgs a) {
     using E = Elt<DT>;
@@ -2216,46 +2278,137 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sv_rows_kernel(RowsArgs a) {
         cluster.sync();
     }
     if (rank != 0 || tid != 0) return;
-    RowRec rec;
-    rec.mraw = p.m;
-    rec.S = SAMPLED ? p.s : 0.0f;
-    rec.argmax = p.idx < 0 ? 0 : p.idx;
-    rec.px = 0.0;
-    rec.lx = NAN;
-    rec.qx = NAN;
-    uint32_t fl = row_flags<SAMPLED>(p);
-    bool ends = false;  // the scan stops at this row (sequences with `skip`)
-    if (i < k && a.x) {
-        if (xi < 0 || xi >= V) {
-            fl |= kRowTokenBad;
-        } else {
-            rec.lx = lx;
-            if (SAMPLED) {
-                rec.qx = qx;
-                if (!(qx >= 0.0f)) fl |= kRowQBad;
-                if (!(fl & kRowBad)) {
-                    ff ex = exp_rel(lx, p.m, a.c2, g_exp2_table.hi, g_exp2_table.lo);
-                    rec.px = (double)__fdiv_rn(ex.hi, p.s);
-                }
-            }
-        }
-        if (a.skip) {
-            // The same tests, in the same arithmetic, as the finish kernels' scans.
-            if (fl & (kRowBad | kRowTokenBad | kRowQBad)) {
-                ends = true;
-            } else if (SAMPLED) {
-                const float P = (float)rec.px, Q = rec.qx;
-                ends = !(ua >= 0.0f && ua < 1.0f) || !((P >= Q) || (ua < __fdiv_rn(P, Q)));
-            } else {
-                ends = xi != rec.argmax;
-            }
-        }
-    } else {
-        rec.px = NAN;
+    write_row_record<SAMPLED>(a, p, b, i, row, xi, lx, qx, ua);
+}
+
+// The row-skipping stream with each row cut into G parts, one CTA each and no
+// cluster, so that a row's statistics (and its test) are ready G times sooner
+// and fewer rows are read before an earlier row of their sequence has stopped
+// the scan.  Each CTA streams its part unless the row lies past its sequence's
+// known stop row (checked at the start and with every batch of loads, as the
+// one-CTA stream does), leaves its partial statistics in the workspace, and the
+// last CTA of the row (an arrival counter, zeroed before the launch) merges the
+// G partials in rank order and writes the record and the test.  A row any part
+// of which was skipped or abandoned is marked skipped: it lies past the stop.
+struct RowPart {
+    float m, s;
+    int idx;
+    uint32_t flags;  // 1: NaN seen; 2: skipped or abandoned
+};
+struct RowGather {
+    int xi;
+    float lx, qx, ua;
+};
+static_assert(sizeof(RowPart) == 16 && sizeof(RowGather) == 16, "row parts");
+constexpr int kRowSplitMax = 8;
+struct RowSplitArgs {
+    RowPart* parts;       // [R * G]
+    RowGather* gath;      // [R] written by rank 0
+    uint32_t* rowcnt;     // [R] CTAs done per row
+};
+
+template <typename DT, bool SAMPLED>
+__global__ void __launch_bounds__(512, 2) sv_rows_skip_kernel(RowsArgs a, RowSplitArgs rs) {
+    using E = Elt<DT>;
+    constexpr int NT = 512, NW = NT / 32;
+    __shared__ Partial wpart[NW];
+    __shared__ int s_skip, s_abort, s_last;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int G = a.G;
+    const long long r0 = blockIdx.x / G;
+    const int rank = blockIdx.x % G;
+    const int V = a.V, k = a.k;
+    const int b = (int)(r0 % a.B), i = (int)(r0 / a.B);
+    const long long row = (long long)b * (k + 1) + i;
+    const DT* rowp = static_cast<const DT*>(a.logits) + row * (long long)V;
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (blockIdx.x == 0 && tid == 0) {
+        a.hdr->magic = kMagic;
+        a.hdr->B = a.B;
+        a.hdr->k = k;
+        a.hdr->V = V;
+        a.hdr->mode = a.mode;
+        a.hdr->flat_ctas = 0;
     }
-    rec.flags = fl;
-    a.rows[row] = rec;
-    if (ends) atomicMin(a.stop + b, (uint32_t)i);
+    if (tid == 0) {
+        s_skip = i > 0 && *reinterpret_cast<volatile const uint32_t*>(a.stop + b) < (uint32_t)i;
+        s_abort = 0;
+    }
+    __syncthreads();
+    Partial p = empty_partial();
+    if (!s_skip) {
+        int xi = -1;
+        float lx = NAN, qx = NAN, ua = 0.0f;
+        if (rank == 0 && tid == 0 && i < k && a.x) {
+            xi = a.x[(long long)b * k + i];
+            if (xi >= 0 && xi < V) {
+                lx = E::load1(rowp + xi);
+                if (SAMPLED) qx = a.q[((long long)b * k + i) * V + xi];
+            }
+            if (SAMPLED) ua = a.ua[(long long)b * k + i];
+        }
+        int head;
+        long long nvec, tail0;
+        row_layout<DT>(rowp, V, head, nvec, tail0);
+        const long long vb = nvec * rank / G, ve = nvec * (rank + 1) / G;
+        bool aborted = false;
+        if (i > 0)
+            p = stream_slice<DT, SAMPLED, 8, true>(rowp, V, vb, ve, head, tail0, rank == 0,
+                                                   rank == G - 1, tid, NT, a.c, a.stop + b,
+                                                   (uint32_t)i, &aborted);
+        else
+            p = stream_slice<DT, SAMPLED, 8>(rowp, V, vb, ve, head, tail0, rank == 0,
+                                             rank == G - 1, tid, NT, a.c);
+        if (aborted) s_abort = 1;
+        p = warp_merge<SAMPLED>(p, a.c);
+        if (lane == 0) wpart[warp] = p;
+        if (rank == 0 && tid == 0 && i < k && a.x) rs.gath[r0] = RowGather{xi, lx, qx, ua};
+        __syncthreads();
+        if (warp == 0) {
+            Partial w = lane < NW ? wpart[lane] : empty_partial();
+            p = warp_merge<SAMPLED>(w, a.c);
+        }
+    }
+    if (tid == 0) {
+        RowPart part;
+        part.m = p.m;
+        part.s = p.s;
+        part.idx = p.idx;
+        part.flags = (p.nan ? 1u : 0u) | ((s_skip || s_abort) ? 2u : 0u);
+        rs.parts[r0 * G + rank] = part;
+        __threadfence();
+        s_last = atomicAdd(rs.rowcnt + r0, 1u) == (uint32_t)(G - 1);
+    }
+    __syncthreads();
+    if (!s_last || tid != 0) return;
+    __threadfence();
+    // the last part of the row: merge in rank order, then the record and the test
+    Partial mp = empty_partial();
+    bool skipped = false;
+    for (int r = 0; r < G; ++r) {
+        const uint4 v = __ldcg(reinterpret_cast<const uint4*>(rs.parts + r0 * G + r));
+        Partial q;
+        q.m = __uint_as_float(v.x);
+        q.s = __uint_as_float(v.y);
+        q.idx = (int)v.z;
+        q.nan = (v.w & 1u) ? 1 : 0;
+        skipped |= (v.w & 2u) != 0;
+        merge<SAMPLED>(mp, q, a.c);
+    }
+    if (skipped) {
+        a.rows[row] = skipped_record();
+        return;
+    }
+    int xi = -1;
+    float lx = NAN, qx = NAN, ua = 0.0f;
+    if (i < k && a.x) {
+        const uint4 g = __ldcg(reinterpret_cast<const uint4*>(rs.gath + r0));
+        xi = (int)g.x;
+        lx = __uint_as_float(g.y);
+        qx = __uint_as_float(g.z);
+        ua = __uint_as_float(g.w);
+    }
+    write_row_record<SAMPLED>(a, mp, b, i, row, xi, lx, qx, ua);
 }
 
 // ------------------------------------------------------------------ flat greedy stream
@@ -3161,13 +3314,14 @@ __global__ void __launch_bounds__(kThreads, 2) sv_precise_kernel(PreciseArgs a) 
 // entry finding the token.  No CTA waits for another: the arrival counter
 // only tells the last one that the others' sums are in memory.
 
-constexpr int kSplitTarget = 1024;      // CTAs a fast split draw aims for
+constexpr int kSplitTarget = 128;       // CTAs a fast split draw aims for (at least one per row)
 constexpr int kSplitMinChunks = 128;    // smallest slice (chunks of 8 elements)
-constexpr int kSplitMaxChunks = 8192;   // largest slice (its block sums fit 16 KiB)
+constexpr int kSplitMaxChunks = 1 << 18;  // largest slice (a whole row of the largest V)
 constexpr int kSplitMaxSlices = kThreads;
 
-// Slices per sequence of the fast split draw: about kSplitTarget CTAs in all,
-// slices between kSplitMinChunks and kSplitMaxChunks chunks, at most
+// Slices per sequence of the fast split draw: about kSplitTarget CTAs in all
+// (measured on B = 256, V = 151936: one slice per row 3 us faster than two,
+// 6 us faster than four), slices of at least kSplitMinChunks chunks, at most
 // kSplitMaxSlices.  Returns the slice length in chunks in *sc.
 __host__ __device__ inline int split_slices(int B, int V, int* sc) {
     const long long nch = ((long long)V + kChunk - 1) / kChunk;
@@ -4563,7 +4717,7 @@ static bool flat_plan(int B, int k, int V, int esz, const void* logits, int sms,
 static sv_status launch_rows(bool sampled, const void* logits, sv_dtype dt, const float* q,
                              const int32_t* x, const float* ua, float T, int B, int k, int V,
                              void* ws, cudaStream_t stream, int sms, bool skip,
-                             const sv_tuning& tu, bool flat_ok = true) {
+                             const sv_tuning& tu, bool flat_ok = true, bool full_ws = false) {
     const long long R = (long long)B * (k + 1);
     RowsArgs a;
     a.logits = logits;
@@ -4611,6 +4765,33 @@ static sv_status launch_rows(bool sampled, const void* logits, sv_dtype dt, cons
     if (tu.rows_threads) nt = tu.rows_threads;
     if (skip && cudaMemsetAsync(a.stop, 0xFF, (size_t)B * sizeof(uint32_t), stream) != cudaSuccess)
         return SV_ERR_CUDA;
+    // The row-skipping stream with rows cut into G CTAs (a full workspace only;
+    // a tuning option: on B = 256, k = 8, V = 151936 fp32, 4 CTAs per row took
+    // 36 us longer than one, the many short CTAs costing more than the earlier
+    // decisions save).
+    const int gs = tu.rows_split ? std::min(tu.rows_split, kRowSplitMax) : 1;
+    if (skip && full_ws && gs > 1) {
+        a.G = gs;
+        char* w = static_cast<char*>(ws);
+        RowSplitArgs rs;
+        const size_t ro = ws_rowsplit_offset(B, k, V);
+        rs.rowcnt = reinterpret_cast<uint32_t*>(w + ro);
+        rs.parts = reinterpret_cast<RowPart*>(w + ro + ((R * 4 + 15) & ~15ll));
+        rs.gath = reinterpret_cast<RowGather*>(reinterpret_cast<char*>(rs.parts) + R * 8 * 16);
+        if (cudaMemsetAsync(rs.rowcnt, 0, (size_t)R * 4, stream) != cudaSuccess) return SV_ERR_CUDA;
+        cudaLaunchConfig_t sc = {};
+        sc.gridDim = dim3((unsigned)(R * gs), 1, 1);
+        sc.blockDim = dim3(512, 1, 1);
+        sc.stream = stream;
+        cudaError_t se;
+        if (dt == SV_BF16)
+            se = sampled ? cudaLaunchKernelEx(&sc, sv_rows_skip_kernel<__nv_bfloat16, true>, a, rs)
+                         : cudaLaunchKernelEx(&sc, sv_rows_skip_kernel<__nv_bfloat16, false>, a, rs);
+        else
+            se = sampled ? cudaLaunchKernelEx(&sc, sv_rows_skip_kernel<float, true>, a, rs)
+                         : cudaLaunchKernelEx(&sc, sv_rows_skip_kernel<float, false>, a, rs);
+        return se == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(R * a.G), 1, 1);
     cfg.blockDim = dim3(nt, 1, 1);
@@ -4684,6 +4865,13 @@ static sv_status launch_split(const void* logits, sv_dtype dt, const float* q, c
     a.k = k;
     a.V = V;
     a.NS = split_slices(B, V, &a.SC);
+    if (tu.draw_split && tu.draw_split < a.NS) {  // fewer, longer slices (tuning)
+        const long long nch = ((long long)V + kChunk - 1) / kChunk;
+        long long c = (nch + tu.draw_split - 1) / tu.draw_split;
+        c = (c + kFastGroup - 1) / kFastGroup * kFastGroup;
+        a.SC = (int)c;
+        a.NS = (int)((nch + c - 1) / c);
+    }
     a.force_precise = tu.force_precise != 0;
     a.c2 = log2e_over(T);
     // the list's counter, its entries and the arrival counters, in one memset
@@ -4768,7 +4956,9 @@ static sv_status launch_finish(bool sampled, const void* logits, sv_dtype dt, co
                                ep);
         return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
     }
-    if (tu.draw_mode == 1 && split_fits(B, V))
+    // The split draw on large batches (automatic), or when asked for.
+    const bool split = tu.draw_mode == 1 || (tu.draw_mode == 0 && wide);
+    if (split && split_fits(B, V))
         return launch_split(logits, dt, q, x, ua, ur, T, B, k, V, out, nacc, ws, stream, sms, ep,
                             tu);
     FinishArgs a;
@@ -4914,14 +5104,15 @@ static Path choose_path(bool sampled, int B, int V, int esz, int sms) {
 static sv_status run_verify(bool sampled, const void* logits, sv_dtype dt, const float* q,
                             const int32_t* x, const float* ua, const float* ur, float T, int B,
                             int k, int V, int32_t* out, int32_t* nacc, void* ws,
-                            cudaStream_t stream, int sms, Epilogue ep, const sv_tuning& tu) {
+                            cudaStream_t stream, int sms, Epilogue ep, const sv_tuning& tu,
+                            bool full_ws = true) {
     const Path path = choose_path(sampled, B, V, dt == SV_BF16 ? 2 : 4, sms, tu);
     if (path == kPathFused)
         return launch_fused(sampled, logits, dt, q, x, ua, ur, T, B, k, V, out, nacc, ws, stream,
                             sms, ep, tu);
     const bool skip = path == kPathSkip;
-    sv_status st =
-        launch_rows(sampled, logits, dt, q, x, ua, T, B, k, V, ws, stream, sms, skip, tu);
+    sv_status st = launch_rows(sampled, logits, dt, q, x, ua, T, B, k, V, ws, stream, sms, skip,
+                               tu, true, full_ws);
     if (st != SV_OK) return st;
     return launch_finish(sampled, logits, dt, q, x, ua, ur, T, B, k, V, out, nacc, ws, stream,
                          sms, skip, ep, tu);
@@ -5097,7 +5288,7 @@ static sv_status verify_impl(bool sampled, const void* logits, sv_dtype dtype,
                       sampled ? u_accept : nullptr, sampled ? u_resample : nullptr,
                       sampled ? T : 1.0f, B, k, V, out_tokens, num_accepted, ws, stream, sms,
                       Epilogue{kv_len, reinterpret_cast<unsigned long long*>(stats)},
-                      base_ws ? cluster_draw(tu) : tu);
+                      base_ws ? cluster_draw(tu) : tu, !base_ws);
 }
 
 static sv_status tree_impl(sv_mode mode, const void* logits, sv_dtype dtype,
@@ -5453,7 +5644,7 @@ sv_status spec_verify_debug_rows_skip(sv_mode mode, const void* logits, sv_dtype
     if ((st = device_setup(&sms)) != SV_OK) return st;
     if (B == 0) return SV_OK;
     return launch_rows(sampled, logits, dtype, draft_probs, draft_tokens, u_accept, T, B, k, V, ws,
-                       stream, sms, true, kAuto);
+                       stream, sms, true, kAuto, true, true);
 }
 
 // Test hook: the largest relative error of ex2.approx.ftz.f32 against the

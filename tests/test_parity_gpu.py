@@ -48,16 +48,19 @@ SMALL = [
 ]
 
 
-@pytest.fixture(params=[(1, 0), (1, 1), (2, 0), (3, 0), (3, 1)],
-                ids=["two_kernel", "two_kernel_split_draw", "fused", "skip", "skip_split_draw"])
+@pytest.fixture(params=[(1, 0, 0), (1, 1, 0), (2, 0, 0), (3, 0, 0), (3, 1, 0), (3, 0, 4)],
+                ids=["two_kernel", "two_kernel_split_draw", "fused", "skip", "skip_split_draw",
+                     "skip_rows_in_4"])
 def path(request):
     """Run a test once through each one-call path: the per-call options that
     force it (passed as run_gpu's `tuning`).  The two-kernel and row-skipping
     paths draw with one cluster per sequence, or with the split draw (slices
-    on separate CTAs) under draw_mode 1."""
+    on separate CTAs) under draw_mode 1; the row-skipping stream cuts each row
+    into rows_split CTAs merged through the workspace (automatic: about 8192
+    16-byte vectors per CTA, so one CTA per row on these small shapes)."""
     from speculative_decoding_verification_18_gb300 import specverify as sv
-    p, dm = request.param
-    return sv.Tuning(path=p, draw_mode=dm)
+    p, dm, rsplit = request.param
+    return sv.Tuning(path=p, draw_mode=dm, rows_split=rsplit)
 
 
 @pytest.mark.parametrize("B,k,V,dtype,T,kind", SMALL)
@@ -106,14 +109,17 @@ def test_workload_fused_path(name):
 
 
 @pytest.mark.parametrize("mode", ["sample", "greedy"])
-def test_skip_path_skips_rows_and_matches(mode):
+@pytest.mark.parametrize("rows_split", [0, 4], ids=["one_cta_per_row", "rows_in_4"])
+def test_skip_path_skips_rows_and_matches(mode, rows_split):
     """The row-skipping path on a batch of many waves of rows: later rows of a
     sequence that has already stopped are not read (their statistics come back
-    unset), and every output still equals the oracle's."""
+    unset), and every output still equals the oracle's; with each row cut into
+    four CTAs merged through the workspace too."""
     from speculative_decoding_verification_18_gb300 import specverify as sv
     inp = _gen(mode=mode, B=2048, k=6, V=2000, dtype="bf16", T=0.9, kind="zipf", p_argmax=0.6,
                seed=77)
-    out, n, stats, (st, bits, _) = run_gpu(inp, tuning=sv.Tuning(path=sv.PATH_SKIP))
+    out, n, stats, (st, bits, _) = run_gpu(inp, tuning=sv.Tuning(path=sv.PATH_SKIP,
+                                                                 rows_split=rows_split))
     ref = run_oracle(inp)
     if mode == "greedy":
         assert np.array_equal(n, ref.n) and np.array_equal(out, ref.out)
@@ -387,7 +393,12 @@ def test_bf16_ties_lowest_index(path):
     out, n, stats, _ = run_gpu(inp, tuning=path)
     ref = run_oracle(inp)
     assert np.array_equal(out, ref.out) and np.array_equal(n, ref.n)
-    assert np.array_equal(stats["argmax"], am)
+    # every row the GPU read (the row-skipping path may leave rows past the
+    # decision row unread: argmax -1) has the lowest index of its maximum
+    got = stats["argmax"].reshape(B, k + 1)
+    read = got >= 0
+    assert all(read[b, : n[b] + 1].all() for b in range(B))
+    assert np.array_equal(got[read], am[read])
 
 
 @pytest.mark.parametrize("mode", ["sample", "greedy"])
