@@ -3314,13 +3314,13 @@ __global__ void __launch_bounds__(kThreads, 2) sv_precise_kernel(PreciseArgs a) 
 // entry finding the token.  No CTA waits for another: the arrival counter
 // only tells the last one that the others' sums are in memory.
 
-constexpr int kSplitTarget = 128;       // CTAs a fast split draw aims for (at least one per row)
+constexpr int kSplitTarget = 152;       // CTAs a fast split draw aims for (at least one per row)
 constexpr int kSplitMinChunks = 128;    // smallest slice (chunks of 8 elements)
 constexpr int kSplitMaxChunks = 1 << 18;  // largest slice (a whole row of the largest V)
 constexpr int kSplitMaxSlices = kThreads;
 
 // Slices per sequence of the fast split draw: about kSplitTarget CTAs in all
-// (measured on B = 256, V = 151936: one slice per row 3 us faster than two,
+// (measured on B = 256, V = 151936: one slice per row 1.5 us faster than two,
 // 6 us faster than four), slices of at least kSplitMinChunks chunks, at most
 // kSplitMaxSlices.  Returns the slice length in chunks in *sc.
 __host__ __device__ inline int split_slices(int B, int V, int* sc) {
@@ -3487,6 +3487,9 @@ __global__ void __launch_bounds__(kThreads, 2) sv_split_draw_kernel(SplitArgs a)
     const int b = blockIdx.x / NS, s = blockIdx.x % NS;
     const int k = a.k, V = a.V;
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the row records are complete
+    // The precise launch (a programmatic dependent) may start now: its CTAs
+    // wait for this grid's results, and it returns at once with no draw listed.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     scan_sequence(sc, a.rows, a.ua, a.ur, b, k);
     const int n = sc.n;
     int32_t* o = a.out + (long long)b * (k + 1);
