@@ -78,20 +78,27 @@ def kernel_source_hash(kernel=None):
     """Hash of the sources a kernel's counters depend on: the section of
     specverify.cu that defines it, the common device sections, the draw
     section for kernels that draw, and ff.cuh; the whole file when the kernel
-    is not found."""
+    is not found.  A stage of several kernels ('a+b') takes the union of their
+    sections."""
     csrc = os.path.join(ROOT, "speculative_decoding_verification_18_gb300", "csrc")
     with open(os.path.join(csrc, "specverify.cu")) as fh:
         text = fh.read()
     if kernel:
-        m = re.search(r"__global__[^;{]*?\b" + re.escape(kernel) + r"\s*\(", text)
-        if m:
-            heads = [(h.start(), h.group(1).strip())
-                     for h in re.finditer(r"^// -{40,} (.*)$", text, re.M)]
-            bounds = [(a, heads[i + 1][0] if i + 1 < len(heads) else len(text), name)
-                      for i, (a, name) in enumerate(heads)]
-            want = set(_COMMON_SECTIONS) | ({"draw phase"} if kernel in _DRAWING else set())
-            parts = [text[a:b] for a, b, name in bounds if name in want or a <= m.start() < b]
-            text = "".join(parts)
+        heads = [(h.start(), h.group(1).strip())
+                 for h in re.finditer(r"^// -{40,} (.*)$", text, re.M)]
+        bounds = [(a, heads[i + 1][0] if i + 1 < len(heads) else len(text), name)
+                  for i, (a, name) in enumerate(heads)]
+        keep, found = set(), True
+        for kn in kernel.split("+"):
+            m = re.search(r"__global__[^;{]*?\b" + re.escape(kn) + r"\s*\(", text)
+            if not m:
+                found = False
+                break
+            want = set(_COMMON_SECTIONS) | ({"draw phase"} if kn in _DRAWING else set())
+            keep |= {i for i, (a, b, name) in enumerate(bounds)
+                     if name in want or a <= m.start() < b}
+        if found:
+            text = "".join(text[bounds[i][0]:bounds[i][1]] for i in sorted(keep))
     h = hashlib.sha256(text.encode())
     with open(os.path.join(csrc, "ff.cuh"), "rb") as fh:
         h.update(fh.read())
@@ -520,8 +527,7 @@ def main():
             # the draw stage of a large sampled batch is two kernels: the fast draw
             # and the precise draws it hands on
             fin_name = ("sv_finish_greedy_kernel" if inp.mode == "greedy"
-                        else "sv_split_draw_kernel+sv_split_precise_kernel" if path == sv.PATH_SKIP
-                        else "sv_finish_sample_kernel")
+                        else "sv_split_draw_kernel+sv_split_precise_kernel")
             stage_times = {rows_kname: stage_ms(rows_stage),
                            fin_name: stage_ms(finish_stage)}
     clocks = sampler.summary()
@@ -647,15 +653,18 @@ def main():
                    "timing": f"{K // copies} replays of a CUDA graph of {copies} verifies"
                              + (f" and one of {K % copies}" if K % copies else ""),
                    "path": {sv.PATH_FUSED: "fused per-sequence kernel",
-                            sv.PATH_SKIP: "position-major row stream with row skipping + draw kernel",
-                            sv.PATH_TWO_KERNEL: "row stream + draw kernels"}[path]
+                            sv.PATH_SKIP: "position-major row stream with row skipping + "
+                                          + ("finish kernel" if inp.mode == "greedy"
+                                             else "split draw + split precise pass"),
+                            sv.PATH_TWO_KERNEL: "row stream + "
+                                                + ("finish kernel" if inp.mode == "greedy"
+                                                   else "split draw + split precise pass")}[path]
                            + (f" (flat greedy stream over {flat_ctas} CTAs)" if flat_ctas else ""),
                    "parallelism": f"replicas x{world}"},
         "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
-        "gpu_launches": (1 if fused else 3 if (path == sv.PATH_SKIP and inp.mode == "sample")
-                         else 2) * K,
+        "gpu_launches": (1 if fused else 3 if inp.mode == "sample" else 2) * K,
         "roofline": roofline,
         "cpu_baseline": {"value": cpu_value, "unit": "rows/s", "cores": nt, "kind": "oracle",
                          "sample": f"first {seqs} of {B} sequences ({seqs * (k + 1)} rows), "

@@ -52,7 +52,8 @@ sv_status spec_verify_debug_ffexp(const float* l, float m, float T, int n, doubl
  *                  1 the split draw (slices of the decision row on separate
  *                  CTAs, when the workspace holds its sums), 2 the cluster
  *                  draw (one cluster per sequence); 0 automatic (the split
- *                  draw on the row-skipping path, else the cluster draw). */
+ *                  draw when the workspace holds its sums, else the cluster
+ *                  draw). */
 typedef struct {
     int path;
     int force_precise;

@@ -2110,6 +2110,8 @@ struct RowsArgs {
     Header* hdr;
     RowRec* rows;
     uint32_t* stop;    // [B] lowest row known to end its sequence's scan (with `skip`)
+    uint32_t* zero;    // nzero words CTA 0 clears (the split draw's counters), or null
+    int nzero;
     int B, k, V, G, mode;
     int skip;          // rows in position-major order; rows past a known stop are skipped
     float c;        // log2(e) / T
@@ -2205,6 +2207,8 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sv_rows_kernel(RowsArgs a) {
         a.hdr->mode = a.mode;
         a.hdr->flat_ctas = 0;
     }
+    if (blockIdx.x == 0 && a.zero)  // read by the next launch only (after this grid)
+        for (int i0 = tid; i0 < a.nzero; i0 += NT) a.zero[i0] = 0u;
     // Set when the row turns out to lie past the stop row while it is read.
     __shared__ int s_abort;
     if (a.skip && i > 0) {
@@ -2330,6 +2334,8 @@ __global__ void __launch_bounds__(512, 2) sv_rows_skip_kernel(RowsArgs a, RowSpl
         a.hdr->mode = a.mode;
         a.hdr->flat_ctas = 0;
     }
+    if (blockIdx.x == 0 && a.zero)  // read by the next launch only (after this grid)
+        for (int i0 = tid; i0 < a.nzero; i0 += NT) a.zero[i0] = 0u;
     if (tid == 0) {
         s_skip = i > 0 && *reinterpret_cast<volatile const uint32_t*>(a.stop + b) < (uint32_t)i;
         s_abort = 0;
@@ -3687,7 +3693,9 @@ __device__ __forceinline__ int precise_class(ff e, float q, const PreciseCls& c,
 
 // One chunk of the precise pass: the fixed-point sums of its positive
 // elements' e and q (not counting ambiguous ones); `es`, `cls` receive each
-// element's e and class when not null; the chunk's e total goes into S.
+// element's e and class when not null; the chunk's e total goes into S.  (Not
+// inlining it, so that a row's last CTA would find its chunk search's code in
+// the instruction cache, made the slices' pass twice as slow: measured.)
 template <typename DT>
 __device__ __forceinline__ void precise_lin_chunk(const DrawCtx<DT>& d, int ci, const float* l,
                                                   const float* q, const PreciseCls& c, bool res,
@@ -4093,27 +4101,45 @@ __global__ void __launch_bounds__(kThreads, 2) sv_split_precise_kernel(SplitPrec
                     const unsigned long long ly = ps.bY + iy2 - cy, lq = ps.bQ + iq2 - cq;
                     const bool lp = have && fast_cval(ly + cy, lq + cq, M) > (long long)tau;
                     const unsigned bl = __ballot_sync(0xffffffffu, lp);
-                    if (bl && lane == __ffs(bl) - 1) {
-                        // the element: walk the chunk in the pass's order
-                        ff Y{0.0f, 0.0f}, Q{0.0f, 0.0f};
-                        int tok = -1;
-                        for (int e = 0; e < kChunk && tok < 0; ++e) {
-                            const long long idx = (long long)ci * kChunk + e;
-                            bool pos = cls[e] == kPcPos;
-                            if (pos) {
-                                ff_accumulate(Y, es[e]);
-                                if (res) ff_acc1(Q, q[e]);
-                            }
-                            unsigned long long py = ff_fixed(ff_normalize(Y), cl.ey);
-                            unsigned long long pq = res ? ff_fixed(ff_normalize(Q), 62) : 0ull;
-                            unsigned long long ea = 0ull, eq = 0ull;
-                            amb_in(ps, (long long)ci * kChunk, idx + 1, ea, eq);
-                            for (int i = 0; i < ps.nb_amb; ++i)
-                                if (ps.amb[i].idx == idx && ps.ay[i] > 0ull) pos = true;
-                            if (pos && fast_cval(ly + py + ea, lq + pq + eq, M) > (long long)tau) tok = e;
-                        }
-                        if (tok >= 0) ps.token = (int)(ci * kChunk + tok);
+                    // The element: lane e < 8 takes element e of the chunk of
+                    // lane oc (its class, e and q shuffled from there) and forms
+                    // the cumulative weight through e, in the pass's order; the
+                    // first positive element past tau is the token.
+                    const int oc = bl ? __ffs(bl) - 1 : 0;
+                    ff ese[kChunk];
+                    float qe[kChunk];
+                    int ce[kChunk];
+#pragma unroll
+                    for (int j = 0; j < kChunk; ++j) {
+                        ese[j] = ff{__shfl_sync(0xffffffffu, es[j].hi, oc),
+                                    __shfl_sync(0xffffffffu, es[j].lo, oc)};
+                        qe[j] = __shfl_sync(0xffffffffu, q[j], oc);
+                        ce[j] = __shfl_sync(0xffffffffu, cls[j], oc);
                     }
+                    const unsigned long long cly = __shfl_sync(0xffffffffu, ly, oc);
+                    const unsigned long long clq = __shfl_sync(0xffffffffu, lq, oc);
+                    const long long c8 = ((long long)ps.blk * kFastGroup + oc) * kChunk;
+                    const int e = lane & (kChunk - 1);
+                    ff Y{0.0f, 0.0f}, Q{0.0f, 0.0f};
+                    bool pe = false;
+#pragma unroll
+                    for (int j = 0; j < kChunk; ++j) {
+                        if (j <= e && ce[j] == kPcPos) {
+                            ff_accumulate(Y, ese[j]);
+                            if (res) ff_acc1(Q, qe[j]);
+                        }
+                        if (j == e) pe = ce[j] == kPcPos;
+                    }
+                    unsigned long long ea = 0ull, eq = 0ull;
+                    amb_in(ps, c8, c8 + e + 1, ea, eq);
+                    for (int i = 0; i < ps.nb_amb; ++i)
+                        if (ps.amb[i].idx == c8 + e && ps.ay[i] > 0ull) pe = true;
+                    const unsigned long long py = ff_fixed(ff_normalize(Y), cl.ey);
+                    const unsigned long long pq = res ? ff_fixed(ff_normalize(Q), 62) : 0ull;
+                    const bool hit = bl && lane < kChunk && pe &&
+                                     fast_cval(cly + py + ea, clq + pq + eq, M) > (long long)tau;
+                    const unsigned bh = __ballot_sync(0xffffffffu, hit);
+                    if (lane == 0 && bh) ps.token = (int)(c8 + __ffs(bh) - 1);
                 }
                 __syncthreads();
             }
@@ -4720,7 +4746,8 @@ static bool flat_plan(int B, int k, int V, int esz, const void* logits, int sms,
 static sv_status launch_rows(bool sampled, const void* logits, sv_dtype dt, const float* q,
                              const int32_t* x, const float* ua, float T, int B, int k, int V,
                              void* ws, cudaStream_t stream, int sms, bool skip,
-                             const sv_tuning& tu, bool flat_ok = true, bool full_ws = false) {
+                             const sv_tuning& tu, bool flat_ok = true, bool full_ws = false,
+                             bool zero_split = false) {
     const long long R = (long long)B * (k + 1);
     RowsArgs a;
     a.logits = logits;
@@ -4731,6 +4758,11 @@ static sv_status launch_rows(bool sampled, const void* logits, sv_dtype dt, cons
     a.rows = reinterpret_cast<RowRec*>(static_cast<char*>(ws) + ws_rows_offset());
     a.stop = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + ws_stop_offset(B, k));
     a.skip = skip ? 1 : 0;
+    // With zero_split the split draw that follows finds its list counter, list
+    // and arrival counters cleared by this launch (so it needs no memset).
+    a.zero = zero_split ? reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + ws_plist_offset(B, k))
+                        : nullptr;
+    a.nzero = zero_split ? (int)((ws_split_offset(B, k) - ws_plist_offset(B, k)) / 4 + B) : 0;
     a.B = B;
     a.k = k;
     a.V = V;
@@ -4839,7 +4871,7 @@ static int draw_split_wide(int B, int V, int sms) {
 static sv_status launch_split(const void* logits, sv_dtype dt, const float* q, const int32_t* x,
                               const float* ua, const float* ur, float T, int B, int k, int V,
                               int32_t* out, int32_t* nacc, void* ws, cudaStream_t stream, int sms,
-                              Epilogue ep, const sv_tuning& tu) {
+                              Epilogue ep, const sv_tuning& tu, bool zeroed) {
     char* w = static_cast<char*>(ws);
     SplitArgs a;
     a.logits = logits;
@@ -4877,14 +4909,24 @@ static sv_status launch_split(const void* logits, sv_dtype dt, const float* q, c
     }
     a.force_precise = tu.force_precise != 0;
     a.c2 = log2e_over(T);
-    // the list's counter, its entries and the arrival counters, in one memset
-    const size_t zlen = ws_split_offset(B, k) + (size_t)B * sizeof(uint32_t) - ws_plist_offset(B, k);
-    if (cudaMemsetAsync(a.plist_count, 0, zlen, stream) != cudaSuccess) return SV_ERR_CUDA;
+    // The list's counter, its entries and the arrival counters: cleared by the
+    // row stream just before (`zeroed`: then this launch is its programmatic
+    // dependent), else here in one memset.
+    cudaLaunchAttribute dep;
+    dep.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    dep.val.programmaticStreamSerializationAllowed = 1;
+    if (!zeroed) {
+        const size_t zlen =
+            ws_split_offset(B, k) + (size_t)B * sizeof(uint32_t) - ws_plist_offset(B, k);
+        if (cudaMemsetAsync(a.plist_count, 0, zlen, stream) != cudaSuccess) return SV_ERR_CUDA;
+    }
     cudaError_t e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((long long)B * a.NS), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.stream = stream;
+    cfg.attrs = &dep;
+    cfg.numAttrs = zeroed ? 1 : 0;
     // float-float chunk sums (a tighter bound, fewer precise draws) on small
     // batches, whose draws are latency; pairwise on large ones, whose fast pass
     // is instruction-bound
@@ -4934,12 +4976,21 @@ static sv_status launch_split(const void* logits, sv_dtype dt, const float* q, c
     return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
+// The split draw (automatic, or when asked for) if the workspace has its
+// region; the cluster draw with draw_mode 2.  Measured on B = 256, k = 8,
+// V = 151936 fp32 (222.9 against 242 us per verify) and B = 1, k = 8,
+// V = 256000 bf16 (19.3 against 21.4 us).
+static bool uses_split(const sv_tuning& tu, bool wide, int B, int V) {
+    (void)wide;
+    return tu.draw_mode != 2 && split_fits(B, V);
+}
+
 // `wide`: the draw kernel of a large batch (draw_split_wide), else seq_split.
 static sv_status launch_finish(bool sampled, const void* logits, sv_dtype dt, const float* q,
                                const int32_t* x, const float* ua, const float* ur, float T,
                                int B, int k, int V, int32_t* out, int32_t* nacc, void* ws,
                                cudaStream_t stream, int sms, bool wide, Epilogue ep,
-                               const sv_tuning& tu) {
+                               const sv_tuning& tu, bool split_zeroed = false) {
     const RowRec* rows =
         reinterpret_cast<const RowRec*>(static_cast<char*>(ws) + ws_rows_offset());
     uint32_t* seqstat = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + ws_seq_offset(B, k));
@@ -4959,11 +5010,9 @@ static sv_status launch_finish(bool sampled, const void* logits, sv_dtype dt, co
                                ep);
         return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
     }
-    // The split draw on large batches (automatic), or when asked for.
-    const bool split = tu.draw_mode == 1 || (tu.draw_mode == 0 && wide);
-    if (split && split_fits(B, V))
+    if (uses_split(tu, wide, B, V))
         return launch_split(logits, dt, q, x, ua, ur, T, B, k, V, out, nacc, ws, stream, sms, ep,
-                            tu);
+                            tu, split_zeroed);
     FinishArgs a;
     a.ep = ep;
     a.logits = logits;
@@ -5114,11 +5163,13 @@ static sv_status run_verify(bool sampled, const void* logits, sv_dtype dt, const
         return launch_fused(sampled, logits, dt, q, x, ua, ur, T, B, k, V, out, nacc, ws, stream,
                             sms, ep, tu);
     const bool skip = path == kPathSkip;
+    // the split draw's counters cleared by the row stream (one launch fewer)
+    const bool zs = sampled && full_ws && uses_split(tu, skip, B, V);
     sv_status st = launch_rows(sampled, logits, dt, q, x, ua, T, B, k, V, ws, stream, sms, skip,
-                               tu, true, full_ws);
+                               tu, true, full_ws, zs);
     if (st != SV_OK) return st;
     return launch_finish(sampled, logits, dt, q, x, ua, ur, T, B, k, V, out, nacc, ws, stream,
-                         sms, skip, ep, tu);
+                         sms, skip, ep, tu, zs);
 }
 
 // Tree verification: the row stream over all B*N rows (statistics only, no
