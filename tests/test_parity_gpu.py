@@ -48,16 +48,15 @@ SMALL = [
 ]
 
 
-@pytest.fixture(params=[(1, 0, 0), (1, 1, 0), (2, 0, 0), (3, 0, 0), (3, 1, 0), (3, 0, 4)],
-                ids=["two_kernel", "two_kernel_split_draw", "fused", "skip", "skip_split_draw",
+@pytest.fixture(params=[(1, 0, 0), (1, 2, 0), (2, 0, 0), (3, 0, 0), (3, 2, 0), (3, 0, 4)],
+                ids=["two_kernel", "two_kernel_cluster_draw", "fused", "skip", "skip_cluster_draw",
                      "skip_rows_in_4"])
 def path(request):
     """Run a test once through each one-call path: the per-call options that
     force it (passed as run_gpu's `tuning`).  The two-kernel and row-skipping
-    paths draw with one cluster per sequence, or with the split draw (slices
-    on separate CTAs) under draw_mode 1; the row-skipping stream cuts each row
-    into rows_split CTAs merged through the workspace (automatic: about 8192
-    16-byte vectors per CTA, so one CTA per row on these small shapes)."""
+    paths draw with the split draw (slices on separate CTAs; automatic), or
+    with one cluster per sequence under draw_mode 2; the row-skipping stream
+    also cuts each row into rows_split CTAs merged through the workspace."""
     from speculative_decoding_verification_18_gb300 import specverify as sv
     p, dm, rsplit = request.param
     return sv.Tuning(path=p, draw_mode=dm, rows_split=rsplit)
