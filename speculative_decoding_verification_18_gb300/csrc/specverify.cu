@@ -3964,105 +3964,101 @@ __global__ void __launch_bounds__(kThreads, 2) sv_split_precise_kernel(SplitPrec
             __syncthreads();
         } else {
             const unsigned long long M = ps.M, tau = ps.tau;
-            // the slice: each thread one slice's sums (and the listed elements in it)
-            unsigned long long sy = mine.Y, sq = mine.Q;
-            if (tid < nsl)
-                amb_in(ps, (long long)tid * slb * kFastGroup * kChunk,
-                       (long long)(tid + 1) * slb * kFastGroup * kChunk, sy, sq);
-            unsigned long long iy = sy, iq = sq;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const unsigned long long yo = __shfl_up_sync(0xffffffffu, iy, off);
-                const unsigned long long qo = __shfl_up_sync(0xffffffffu, iq, off);
-                if (lane >= off) {
-                    iy += yo;
-                    iq += qo;
+            // Warp 0 alone from here (no block-wide barrier until the token):
+            // the slice, then the block inside it, each a warp scan over
+            // contiguous ranges (one per lane) and a walk of the first range
+            // whose end passes tau; then the chunk and the element.
+            int first = -1;
+            if (warp == 0) {
+                const long long Ls = (nsl + 31) / 32;
+                const long long sb = min(nsl, (long long)lane * Ls), se = min(nsl, sb + Ls);
+                const long long eps = slb * kFastGroup * kChunk;  // elements per slice
+                unsigned long long sy = 0ull, sq = 0ull;
+                for (long long i = sb; i < se; ++i) {
+                    const ulonglong2 v = __ldcg(reinterpret_cast<const ulonglong2*>(a.items + it0 + i));
+                    sy += v.x;
+                    sq += v.y;
                 }
-            }
-            if (lane == 31) {
-                ps.ry[warp] = iy;
-                ps.rq[warp] = iq;
-            }
-            __syncthreads();
-            unsigned long long wy = 0ull, wq = 0ull;
-            for (int w = 0; w < warp; ++w) {
-                wy += ps.ry[w];
-                wq += ps.rq[w];
-            }
-            const bool past = tid < nsl && fast_cval(wy + iy, wq + iq, M) > (long long)tau;
-            const unsigned bw = __ballot_sync(0xffffffffu, past);
-            if (lane == 0) ds.red_f[warp] = bw ? (float)(__ffs(bw) - 1) : -1.0f;
-            __syncthreads();
-            int owner = -1;
-            for (int w = 0; w < kWarps && owner < 0; ++w)
-                if (ds.red_f[w] >= 0.0f) owner = w * 32 + (int)ds.red_f[w];
-            if (tid == owner) {
-                ps.Y0 = wy + iy - sy;
-                ps.Q0 = wq + iq - sq;
-            }
-            __syncthreads();
-            if (owner >= 0) {  // uniform
-                // the block: one block per thread (a slice has at most kThreads blocks?
-                // no: each thread sums a contiguous range of them)
-                const long long b0 = (long long)owner * slb;
-                const int nbs = (int)min(slb, nbr - b0);
-                const int L = (nbs + kThreads - 1) / kThreads;
-                const int cb = min(nbs, tid * L), ce = min(nbs, cb + L);
-                const unsigned long long* bs = rowblk + b0 * 2;
-                unsigned long long my = 0ull, mq = 0ull;
-                for (int i = cb; i < ce; ++i) {
-                    const ulonglong2 v = __ldcg(reinterpret_cast<const ulonglong2*>(bs) + i);
-                    my += v.x;
-                    mq += v.y;
-                }
-                if (ce > cb)
-                    amb_in(ps, (b0 + cb) * kFastGroup * kChunk, (b0 + ce) * kFastGroup * kChunk, my, mq);
-                unsigned long long jy = my, jq = mq;
+                if (se > sb) amb_in(ps, sb * eps, se * eps, sy, sq);
+                unsigned long long iy = sy, iq = sq;
 #pragma unroll
                 for (int off = 1; off < 32; off <<= 1) {
-                    const unsigned long long yo = __shfl_up_sync(0xffffffffu, jy, off);
-                    const unsigned long long qo = __shfl_up_sync(0xffffffffu, jq, off);
+                    const unsigned long long yo = __shfl_up_sync(0xffffffffu, iy, off);
+                    const unsigned long long qo = __shfl_up_sync(0xffffffffu, iq, off);
                     if (lane >= off) {
-                        jy += yo;
-                        jq += qo;
+                        iy += yo;
+                        iq += qo;
                     }
                 }
-                __syncthreads();
-                if (lane == 31) {
-                    ps.ry[warp] = jy;
-                    ps.rq[warp] = jq;
-                }
-                __syncthreads();
-                unsigned long long vy = ps.Y0, vq = ps.Q0;
-                for (int w = 0; w < warp; ++w) {
-                    vy += ps.ry[w];
-                    vq += ps.rq[w];
-                }
-                const unsigned long long ty0 = vy + jy - my, tq0 = vq + jq - mq;  // before cb
-                const bool bp = ce > cb && fast_cval(ty0 + my, tq0 + mq, M) > (long long)tau;
-                const unsigned bb = __ballot_sync(0xffffffffu, bp);
-                __syncthreads();
-                if (lane == 0) ds.red_f[warp] = bb ? (float)(__ffs(bb) - 1) : -1.0f;
-                __syncthreads();
-                int first = -1;
-                for (int w = 0; w < kWarps && first < 0; ++w)
-                    if (ds.red_f[w] >= 0.0f) first = w * 32 + (int)ds.red_f[w];
-                if (tid == first) {
-                    unsigned long long ry = ty0, rq = tq0;
-                    int i = cb;
-                    for (; i < ce - 1; ++i) {
-                        const ulonglong2 v = __ldcg(reinterpret_cast<const ulonglong2*>(bs) + i);
+                const unsigned bs1 =
+                    __ballot_sync(0xffffffffu, se > sb && fast_cval(iy, iq, M) > (long long)tau);
+                const int fl = bs1 ? __ffs(bs1) - 1 : 0;
+                long long own = -1;
+                unsigned long long y0 = 0ull, q0 = 0ull;
+                if (lane == fl && bs1) {
+                    unsigned long long ry = iy - sy, rq = iq - sq;
+                    long long i = sb;
+                    for (; i < se - 1; ++i) {
+                        const ulonglong2 v = __ldcg(reinterpret_cast<const ulonglong2*>(a.items + it0 + i));
                         unsigned long long y = v.x, q = v.y;
-                        amb_in(ps, (b0 + i) * kFastGroup * kChunk, (b0 + i + 1) * kFastGroup * kChunk, y, q);
+                        amb_in(ps, i * eps, (i + 1) * eps, y, q);
                         if (fast_cval(ry + y, rq + q, M) > (long long)tau) break;
                         ry += y;
                         rq += q;
                     }
-                    ps.blk = (int)(b0 + i);
-                    ps.bY = ry;
-                    ps.bQ = rq;
+                    own = i;
+                    y0 = ry;
+                    q0 = rq;
                 }
-                __syncthreads();
+                own = __shfl_sync(0xffffffffu, own, fl);
+                y0 = __shfl_sync(0xffffffffu, y0, fl);
+                q0 = __shfl_sync(0xffffffffu, q0, fl);
+                if (bs1) {
+                    // the block inside slice `own`
+                    const long long b0 = own * slb;
+                    const long long nbs = min(slb, nbr - b0);
+                    const long long Lb = (nbs + 31) / 32;
+                    const long long cb = min(nbs, (long long)lane * Lb), ce = min(nbs, cb + Lb);
+                    const unsigned long long* bsp = rowblk + b0 * 2;
+                    unsigned long long my = 0ull, mq = 0ull;
+                    for (long long i = cb; i < ce; ++i) {
+                        const ulonglong2 v = __ldcg(reinterpret_cast<const ulonglong2*>(bsp) + i);
+                        my += v.x;
+                        mq += v.y;
+                    }
+                    if (ce > cb) amb_in(ps, (b0 + cb) * 64, (b0 + ce) * 64, my, mq);
+                    unsigned long long jy = my, jq = mq;
+#pragma unroll
+                    for (int off = 1; off < 32; off <<= 1) {
+                        const unsigned long long yo = __shfl_up_sync(0xffffffffu, jy, off);
+                        const unsigned long long qo = __shfl_up_sync(0xffffffffu, jq, off);
+                        if (lane >= off) {
+                            jy += yo;
+                            jq += qo;
+                        }
+                    }
+                    const bool bp = ce > cb && fast_cval(y0 + jy, q0 + jq, M) > (long long)tau;
+                    const unsigned bb = __ballot_sync(0xffffffffu, bp);
+                    first = bb ? __ffs(bb) - 1 : -1;
+                    if (lane == first) {
+                        unsigned long long ry = y0 + jy - my, rq = q0 + jq - mq;
+                        long long i = cb;
+                        for (; i < ce - 1; ++i) {
+                            const ulonglong2 v = __ldcg(reinterpret_cast<const ulonglong2*>(bsp) + i);
+                            unsigned long long y = v.x, q = v.y;
+                            amb_in(ps, (b0 + i) * 64, (b0 + i + 1) * 64, y, q);
+                            if (fast_cval(ry + y, rq + q, M) > (long long)tau) break;
+                            ry += y;
+                            rq += q;
+                        }
+                        ps.blk = (int)(b0 + i);
+                        ps.bY = ry;
+                        ps.bQ = rq;
+                    }
+                    __syncwarp();
+                }
+            }
+            {
                 if (first >= 0 && warp == 0) {
                     // the chunk: lanes 0..7 recompute the block's chunks
                     DrawCtx<DT> d = slice_ctx<DT>(dyn, drow, qrow, res, V, rec.mraw, a.c2, u, 0,
@@ -4141,8 +4137,8 @@ __global__ void __launch_bounds__(kThreads, 2) sv_split_precise_kernel(SplitPrec
                     const unsigned bh = __ballot_sync(0xffffffffu, hit);
                     if (lane == 0 && bh) ps.token = (int)(c8 + __ffs(bh) - 1);
                 }
-                __syncthreads();
             }
+            __syncthreads();
         }
         if (tid == 0) {
             if (ps.token >= 0) a.out[(long long)b * (k + 1) + n] = ps.token;
