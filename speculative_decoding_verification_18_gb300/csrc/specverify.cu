@@ -231,12 +231,68 @@ __device__ __forceinline__ Partial warp_merge(Partial p, float c) {
 // With POLL: every batch also reads *poll, and once it holds a value below
 // `poll_row` the thread sets `aborted` and stops reading (its partial is then
 // meaningless; the caller discards the row).
+// Early rejection on the row-skipping stream: every batch each thread
+// publishes its running statistics as one 64-bit shared word, and every
+// second batch warp 0 merges them and, when the row's test must fail whatever
+// the rest of the row holds, lowers the stop row at once, so that rows after
+// it in its sequence stop being read sooner.
+struct EarlyRej {
+    unsigned long long* tpub;  // [nt] each thread's (max, sum) so far (shared)
+    int nt;
+    float lx, uq;              // thread 0's l(x) and u q(x)
+    uint32_t* stop;
+    uint32_t row;
+    int* fired;                // shared: the stop row was lowered
+};
+// The initial word: max -inf, sum 0 (a partial of no element).
+constexpr unsigned long long kEmptyPub = 0x00000000FF800000ull;
+
+// One batch's share of the early rejection (called by every lane of every
+// warp; the loop around it is warp-uniform, t its batch number).  Each word is
+// a valid partial of its thread's elements so far, so any mix of old and new
+// words bounds the row from below.  Sampled: warp 0 forms Z = sum over the
+// threads of s_t 2^((m_t - l(x)) c), a lower bound of sum_j 2^((l_j - l(x)) c)
+// over the whole row, so p(x) <= 1/Z; when u q(x) Z >= 1 + 2^-10 the row's own
+// test at the end (u < p/q unless p >= q, in rounded arithmetic whose errors
+// are far below that margin) rejects for sure.  Greedy: a thread's max above
+// l(x) means the argmax is not x.
+template <bool SAMPLED>
+__device__ __forceinline__ void early_check(EarlyRej& er, const Partial& p, float c, int tg,
+                                            int t) {
+    volatile unsigned long long* pub = er.tpub;
+    pub[tg] = ((unsigned long long)__float_as_uint(p.s) << 32) | __float_as_uint(p.m);
+    if ((t & 1) == 0 || tg >= 32) return;
+    // warp 0: the merge, every second batch
+    const float lx = __shfl_sync(0xffffffffu, er.lx, 0), uq = __shfl_sync(0xffffffffu, er.uq, 0);
+    float z = SAMPLED ? 0.0f : -INFINITY;
+    for (int j = tg; j < er.nt; j += 32) {
+        const unsigned long long v = pub[j];
+        const float m = __uint_as_float((uint32_t)v), sw = __uint_as_float((uint32_t)(v >> 32));
+        if (SAMPLED) {
+            if (sw > 0.0f) z = __fadd_rn(z, __fmul_rn(sw, ex2_approx(__fmul_rn(__fsub_rn(m, lx), c))));
+        } else {
+            z = fmaxf(z, m);
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float o = __shfl_xor_sync(0xffffffffu, z, off);
+        z = SAMPLED ? __fadd_rn(z, o) : fmaxf(z, o);
+    }
+    const bool rej = SAMPLED ? __fmul_rn(uq, z) >= 1.0009765625f : z > lx;
+    if (tg == 0 && rej && !*er.fired) {
+        atomicMin(er.stop, er.row);
+        *er.fired = 1;
+    }
+}
+
 template <typename DT, bool SAMPLED, int U, bool POLL = false>
 __device__ __forceinline__ Partial stream_slice(const DT* __restrict__ rowp, int V, long long vb,
                                                 long long ve, int head, long long tail0,
                                                 bool head_here, bool tail_here, int tg, int ng,
                                                 float c, const uint32_t* poll = nullptr,
-                                                uint32_t poll_row = 0, bool* aborted = nullptr) {
+                                                uint32_t poll_row = 0, bool* aborted = nullptr,
+                                                EarlyRej* er = nullptr) {
     using E = Elt<DT>;
     constexpr int VW = E::kVec;
     Partial p = empty_partial();
@@ -278,7 +334,15 @@ __device__ __forceinline__ Partial stream_slice(const DT* __restrict__ rowp, int
     // Batches of U vectors per thread, the loads of a batch issued together (the
     // last batch predicated), so a thread with up to U*n vectors waits for n
     // round trips.
-    for (long long v = vb + tg; v < ve; v += (long long)U * ng) {
+    // Polling: the batches are counted per warp (the warp's first lane's
+    // count; lanes past the end have their loads predicated off) and the
+    // abandon decision is the warp's, so every lane takes every batch's
+    // shuffles (the early rejection's warp merge) together.
+    const long long step = (long long)U * ng;
+    const long long vend = POLL ? vb + (tg & ~31) + ((ve - vb - (tg & ~31) + step - 1) / step) * step
+                                : ve;
+    int bt = 0;  // batch number
+    for (long long v = vb + tg; POLL ? (v - tg + (tg & ~31) < vend) : (v < ve); v += step, ++bt) {
         uint4 buf[U];
         uint32_t st = 0xFFFFFFFFu;
         if (POLL) st = *reinterpret_cast<const volatile uint32_t*>(poll);
@@ -288,7 +352,8 @@ __device__ __forceinline__ Partial stream_slice(const DT* __restrict__ rowp, int
 #pragma unroll
         for (int u = 0; u < U; ++u)
             if (v + (long long)u * ng < ve) vector(buf[u], head + (v + (long long)u * ng) * VW);
-        if (POLL && st < poll_row) {
+        if (POLL && er) early_check<SAMPLED>(*er, p, c, tg, bt);
+        if (POLL && __any_sync(0xffffffffu, st < poll_row)) {
             *aborted = true;
             break;
         }
@@ -2211,6 +2276,15 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sv_rows_kernel(RowsArgs a) {
         for (int i0 = tid; i0 < a.nzero; i0 += NT) a.zero[i0] = 0u;
     // Set when the row turns out to lie past the stop row while it is read.
     __shared__ int s_abort;
+    __shared__ unsigned long long s_tpub[NT];  // early rejection: threads' statistics
+    __shared__ int s_fired;
+    if (a.skip) {
+        s_tpub[tid] = kEmptyPub;
+        if (tid == 0) {
+            s_fired = 0;
+            s_abort = 0;
+        }
+    }
     if (a.skip && i > 0) {
         // One thread reads the stop row and the CTA follows its decision (the
         // value may change under concurrent CTAs, so each thread reading it
@@ -2248,12 +2322,23 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sv_rows_kernel(RowsArgs a) {
     // also re-reads stop[b]: a row that falls past the stop row while it is read
     // is abandoned (stop[b] only decreases, so one observation suffices for
     // the whole CTA, whatever the other threads saw).
-    const bool poll = a.skip && i > 0;
+    const bool poll = a.skip;
     Partial p;
     if (poll) {
+        __syncthreads();  // the early rejection's shared words are set
         bool aborted = false;
+        EarlyRej er;
+        er.tpub = s_tpub;
+        er.nt = NT;
+        er.lx = lx;
+        er.uq = __fmul_rn(ua, qx);
+        er.stop = a.stop + b;
+        er.row = (uint32_t)i;
+        er.fired = &s_fired;
+        const bool early = i < k && a.x;  // the bonus row has no test
         p = stream_slice<DT, SAMPLED, 8, true>(rowp, V, vb, ve, head, tail0, true, true, tid, NT,
-                                               a.c, a.stop + b, (uint32_t)i, &aborted);
+                                               a.c, a.stop + b, (uint32_t)i, &aborted,
+                                               early ? &er : nullptr);
         if (aborted) s_abort = 1;
     } else {
         p = stream_slice<DT, SAMPLED, 8>(rowp, V, vb, ve, head, tail0, rank == 0, rank == G - 1,
