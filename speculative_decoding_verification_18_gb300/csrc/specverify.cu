@@ -3405,18 +3405,21 @@ __global__ void __launch_bounds__(kThreads, 2) sv_precise_kernel(PreciseArgs a) 
 // entry finding the token.  No CTA waits for another: the arrival counter
 // only tells the last one that the others' sums are in memory.
 
-constexpr int kSplitTarget = 152;       // CTAs a fast split draw aims for (at least one per row)
+// CTAs a fast split draw aims for: one per SM on large batches (whose
+// pairwise pass is short), two per SM on small ones (float-float sums).
+constexpr int kSplitTargetLarge = 152, kSplitTargetSmall = 304;
 constexpr int kSplitMinChunks = 128;    // smallest slice (chunks of 8 elements)
 constexpr int kSplitMaxChunks = 1 << 18;  // largest slice (a whole row of the largest V)
 constexpr int kSplitMaxSlices = kThreads;
 
-// Slices per sequence of the fast split draw: about kSplitTarget CTAs in all
+// Slices per sequence of the fast split draw: about kSplitTarget* CTAs in all
 // (measured on B = 256, V = 151936: one slice per row 1.5 us faster than two,
 // 6 us faster than four), slices of at least kSplitMinChunks chunks, at most
 // kSplitMaxSlices.  Returns the slice length in chunks in *sc.
 __host__ __device__ inline int split_slices(int B, int V, int* sc) {
     const long long nch = ((long long)V + kChunk - 1) / kChunk;
-    long long ns = (kSplitTarget + (long long)B - 1) / (B > 0 ? B : 1);
+    const long long target = B < kSplitTargetLarge ? kSplitTargetSmall : kSplitTargetLarge;
+    long long ns = (target + (long long)B - 1) / (B > 0 ? B : 1);
     const long long lo = (nch + kSplitMaxChunks - 1) / kSplitMaxChunks;
     const long long hi = (nch + kSplitMinChunks - 1) / kSplitMinChunks;
     if (ns > hi) ns = hi;

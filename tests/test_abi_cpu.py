@@ -41,13 +41,13 @@ def test_workspace_size(lib):
     # list (a 16-byte counter and B entries); then the split draw's region:
     # five words per sequence (arrival counters, the precise entry's ambiguous
     # count, normaliser and margin), 32 ambiguous-element slots of 16 bytes,
-    # 3 slice sums of 32 bytes (V = 32000: 4000 chunks of 8, 3 slices), 512
+    # 5 slice sums of 32 bytes (V = 32000: 4000 chunks of 8, 5 slices), 512
     # precise item sums of 32 bytes, and 16 bytes of block sums per 64 elements
     # of each decision row; then per row an arrival counter, 8 partials of 16
     # bytes and a 16-byte gather record (the split row-skipping stream);
     # rounded to 256
     base = 256 + 64 * 5 * 32 + 64 * 4 * 2 + 16 + 64 * 4
-    split = 64 * 5 * 4 + 64 * 32 * 16 + 64 * 3 * 32 + 512 * 32 + 64 * 500 * 16
+    split = 64 * 5 * 4 + 64 * 32 * 16 + 64 * 5 * 32 + 512 * 32 + 64 * 500 * 16
     rows = 320 * 4 + 320 * 8 * 16 + 320 * 16
     assert sv.spec_verify_workspace_size(64, 4, 32000) == -(-(base + split + rows) // 256) * 256
     # one sequence: 368 bytes before the split region, which holds 512 precise
