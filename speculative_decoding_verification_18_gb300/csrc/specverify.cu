@@ -423,6 +423,21 @@ constexpr float kClassHi = 1.0f + 1.0f / 4096.0f, kClassLo = 1.0f - 1.0f / 4096.
 constexpr double kRowSigma = 1.0 / 8192.0;
 constexpr float kUndecided = 3.9e-4f;
 
+// The fast draw's certificate, in units of 2^-62 of p (the linear form C's
+// units).  An edge of the chosen bin with the positive mass P_b and the q mass
+// Q_b before it (P_a, Q_a after it) is kept at more than
+//   kP ((1 - u) P_b + u P_a) + kQ ((1 - u) Q_b + u Q_a)
+//   + e_S 1.004 (|u Q_tot - Q_b| + 1 + the bin's width) + max(u, 1 - u) D
+//   (+ without EXACT, 2 kQ' (P_c + Q_c) for the edge's chunk) + 2
+// from u C_tot; the derivation is at fast_bound.
+struct FastCert {
+    float kP, kQ;               // per unit of P and of Q: the elements' own errors
+    float eS;                   // the normaliser's relative error
+    float D;                    // undecided weights, float-float sums, truncations
+    long long Pt;               // P_tot (units)
+    unsigned long long Qt, uQ;  // Q_tot and floor(u Q_tot) (units)
+};
+
 template <typename DT>
 __device__ __forceinline__ void load_chunk(const DT* __restrict__ rowp, long long j0, int V,
                                            bool aligned, float* f) {
@@ -539,7 +554,7 @@ struct DrawShared {
     unsigned long long f_M, f_tau;    // floor(2^(123 - EY) / S), floor(u C_tot)
     unsigned long long f_Y, f_Q;      // this rank's starting point (sums of the ranks before)
     unsigned long long f_bY, f_bQ;    // the owner's block's starting point
-    float f_D, f_eS;                  // the error bound's parts (units of 2^-62)
+    FastCert f_c;                     // the certificate's parts
     int f_ok, f_owner;
 };
 
@@ -1142,25 +1157,30 @@ __device__ __forceinline__ void cta_fast_totals(DrawShared& sh, FastTotals t, Fa
 }
 
 // The normaliser, the check against S_row, M = floor(2^(123 - EY) / S), C_tot,
-// tau = floor(u C_tot) and the error bound's parts from a row's totals.
+// tau = floor(u C_tot) and the certificate's parts from a row's totals.
 //
 // Error bound.  Each positive element's p_fast = y/S carries its own error
 // eta_j <= kFastEy (ex2 and the correction's FMA) and the normaliser's common
 // eta_S <= e_S (kFastEy, and without EXACT the roundings of the pairwise chunk
 // sums, 3 2^-24); p_fast = p (1 + eta_j) / (1 + eta_S).  The error of
-// u C_tot - C at a bin edge is, element by element, (u - 1) times the errors
-// before the edge plus u times those after it, so the elements' own errors,
-// the undecided elements' weights (at most kUndecided q) and, without EXACT, the
-// chunk sums' three roundings contribute at most max(u, 1 - u) times their sum;
-// the normaliser's common factor contributes eta_S (u P_tot - P_edge) = eta_S
-// (u Q_tot - Q_edge + (u C_tot - C_edge)), at most e_S (max(u, 1 - u) Q_tot +
-// the bin's width).  The float-float sums (2^-44), M (2^-44) and the
-// fixed-point truncations add at most 2^20 + 2 (chunks) + 64 units.  The token
-// is kept when u C lies more than this bound (plus 2 units) inside both edges
-// of its bin.
+// u C_tot - C_b at a bin edge b is, element by element, (u - 1) times the
+// errors before the edge plus u times those after it.  So the elements' own
+// errors contribute at most kFastEy ((1 - u) P_b + u P_a), with P_b and P_a the
+// positive mass before and after the edge; without EXACT each chunk sum's
+// three roundings (3 2^-24 of its y and of its q) split the same way, except
+// in the edge's own chunk, whose prefix is not a part of the chunk's sum: its
+// roundings are counted twice in full.  The normaliser's common factor
+// contributes eta_S (u P_tot - P_b) = eta_S (u Q_tot - Q_b + (u C_tot - C_b)),
+// at most e_S (|u Q_tot - Q_b| + the bin's width).  The undecided elements'
+// weights (at most kUndecided q each, wherever they lie) contribute at most
+// max(u, 1 - u) times their sum, as do the float-float sums (2^-44), M (2^-44)
+// and the fixed-point truncations (2^20 + 2 per chunk + 64 units in all).  All
+// are bounds of sums of positive terms computed in float: inflated by 1.004
+// for their own roundings.  The token is kept when u C_tot lies more than its
+// edge's bound (plus 2 units) inside both edges of its bin.
 struct FastBound {
     unsigned long long M, tau;
-    float D, eS;
+    FastCert c;
     float S;  // the normaliser (high part)
     bool ok;
 };
@@ -1181,18 +1201,36 @@ __device__ __forceinline__ FastBound fast_bound(const FastTotals& tot, float s_r
     ok = ok && Ctot > 0;
     fb.tau = ok ? scale_floor(u, (unsigned long long)Ctot) : 0ull;
     fb.ok = ok;
-    // The bound's parts (fractions of the total mass of p; float sums of
-    // positive terms, inflated for their own roundings).
     constexpr float u24 = 5.96046448e-08f;
     const float invS = __frcp_rn(S.hi);
     const float Ppos = __fmul_rn(__fmul_rn(Yf.hi, pw), invS);
-    const float Qpos = __fmul_rn(u64_to_ff(Qall).hi, 2.16840434e-19f);  // 2^-62
-    fb.eS = kFastEy + 3.0f * u24 * (EXACT ? fmaxf(0.0f, 1.0f - Ppos) : 1.0f);
-    fb.D = (kFastEy * Ppos + fb.eS * Qpos + kUndecided * tot.Aq +
-            (EXACT ? 0.0f : 3.0f * u24 * (Ppos + Qpos))) *
-               1.004f * 4.611686018427388e18f +
-           1048576.0f + 2.0f * (float)nch + 64.0f;
+    fb.c.eS = kFastEy + 3.0f * u24 * (EXACT ? fmaxf(0.0f, 1.0f - Ppos) : 1.0f);
+    fb.c.kP = (kFastEy + (EXACT ? 0.0f : 3.0f * u24)) * 1.004f;
+    fb.c.kQ = (EXACT ? 0.0f : 3.0f * u24) * 1.004f;
+    fb.c.D = kUndecided * tot.Aq * 1.004f * 4.611686018427388e18f + 1048576.0f +
+             2.0f * (float)nch + 64.0f;
+    fb.c.Pt = ok ? fast_cval(Yall, 0ull, fb.M) : 0ll;
+    fb.c.Qt = Qall;
+    fb.c.uQ = ok ? scale_floor(u, Qall) : 0ull;
     return fb;
+}
+
+// The bound at one edge of the chosen bin (units), given the fixed-point sums
+// (Yb, Qb) through the edge, the bin's width and (without EXACT) the positive
+// and q mass of the edge's chunk (Pc + Qc, units).
+__device__ __forceinline__ long long fast_edge_bound(const FastCert& c, unsigned long long M,
+                                                     float u, unsigned long long Yb,
+                                                     unsigned long long Qb, long long width,
+                                                     float chunk_mass) {
+    const long long Pb = fast_cval(Yb, 0ull, M);
+    const float w1 = __fsub_rn(1.0f, u);
+    const float pb = (float)Pb, pa = (float)max(c.Pt - Pb, 0ll);
+    const float qb = (float)Qb, qa = (float)(c.Qt > Qb ? c.Qt - Qb : 0ull);
+    const float dq = (float)(c.uQ > Qb ? c.uQ - Qb : Qb - c.uQ);
+    float dp = c.kP * (w1 * pb + u * pa) + c.kQ * (w1 * qb + u * qa + 2.0f * chunk_mass);
+    dp += c.eS * 1.004f * (dq + 1.0f + (float)width);
+    dp += fmaxf(u, w1) * c.D + 2.0f;
+    return (long long)fminf(dp, 4.0e18f) + 1ll;
 }
 
 // Block sums {Y, Q} of a slice: from shared memory, or (GLOBAL) written to the
@@ -1212,7 +1250,7 @@ template <typename DT, bool RES, bool EXACT, bool GLOBAL>
 __device__ __forceinline__ void fast_search(DrawShared& sh, const DrawCtx<DT>& d,
                                             const FastScale& f, unsigned long long M,
                                             unsigned long long tau, unsigned long long Y0,
-                                            unsigned long long Q0, float D, float eS) {
+                                            unsigned long long Q0, const FastCert& c) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int fnb = (d.mych + kFastGroup - 1) / kFastGroup;
     // The block: each thread sums a contiguous range of block sums; a block
@@ -1331,14 +1369,23 @@ __device__ __forceinline__ void fast_search(DrawShared& sh, const DrawCtx<DT>& d
         const bool before = lane < kChunk && mine > 0.0f && h <= (long long)tau;
         const unsigned bb = __ballot_sync(0xffffffffu, before) & (be ? ((1u << (__ffs(be) - 1)) - 1u) : 0u);
         const int te = be ? __ffs(be) - 1 : -1;
-        const long long hi = __shfl_sync(0xffffffffu, h, te >= 0 ? te : 0);
-        const long long hb = __shfl_sync(0xffffffffu, h, bb ? 31 - __clz(bb) : 0);
+        const int tl = te >= 0 ? te : 0, bl0 = bb ? 31 - __clz(bb) : 0;
+        const long long hi = __shfl_sync(0xffffffffu, h, tl);
+        const long long hb = __shfl_sync(0xffffffffu, h, bl0);
+        // the sums through each edge, and the edge chunk's sums
+        const unsigned long long yhi = __shfl_sync(0xffffffffu, cly + py, tl);
+        const unsigned long long qhi = __shfl_sync(0xffffffffu, clq + pq, tl);
+        const unsigned long long ylb = __shfl_sync(0xffffffffu, cly + py, bl0);
+        const unsigned long long qlb = __shfl_sync(0xffffffffu, clq + pq, bl0);
+        const unsigned long long ccy = __shfl_sync(0xffffffffu, cy, oc);
+        const unsigned long long ccq = __shfl_sync(0xffffffffu, cq, oc);
         if (lane == 0 && te >= 0) {
             const long long lo = bb ? hb : fast_cval(cly, clq, M);
-            const float um = fmaxf(d.u, __fsub_rn(1.0f, d.u));
-            const float dp = um * D + eS * 1.004f * (float)(hi - lo) + 2.0f;
-            const long long Dp = (long long)fminf(dp, 4.0e18f) + 1ll;
-            sh.cert = ((long long)tau - lo >= Dp && hi - (long long)tau > Dp) ? 1 : 0;
+            const float cm = EXACT ? 0.0f : (float)(fast_cval(ccy, 0ull, M) + (long long)ccq);
+            const long long Dlo = fast_edge_bound(c, M, d.u, bb ? ylb : cly, bb ? qlb : clq,
+                                                  hi - lo, cm);
+            const long long Dhi = fast_edge_bound(c, M, d.u, yhi, qhi, hi - lo, cm);
+            sh.cert = ((long long)tau - lo >= Dlo && hi - (long long)tau > Dhi) ? 1 : 0;
             sh.token = (int)((d.c0 + sh.blk * kFastGroup + oc) * kChunk + te);
         }
     }
@@ -1396,8 +1443,7 @@ __device__ bool draw_fast(cg::cluster_group& cluster, DrawShared& sh, const Draw
             sh.f_tau = fb.tau;
             sh.f_Y = ybef;
             sh.f_Q = qbef;
-            sh.f_eS = fb.eS;
-            sh.f_D = fb.D;
+            sh.f_c = fb.c;
         }
     }
     __syncthreads();
@@ -1405,8 +1451,7 @@ __device__ bool draw_fast(cg::cluster_group& cluster, DrawShared& sh, const Draw
 
     int cert = 1;
     if (d.rank == sh.f_owner) {  // uniform across the CTA
-        fast_search<DT, RES, EXACT, false>(sh, d, f, sh.f_M, sh.f_tau, sh.f_Y, sh.f_Q, sh.f_D,
-                                           sh.f_eS);
+        fast_search<DT, RES, EXACT, false>(sh, d, f, sh.f_M, sh.f_tau, sh.f_Y, sh.f_Q, sh.f_c);
         cert = sh.cert;
     }
     if (d.G > 1) {
@@ -3567,7 +3612,6 @@ struct SplitShared {
     FastTotals tot;
     unsigned long long woffY[kWarps], woffQ[kWarps];
     unsigned long long M, tau, Y0, Q0;
-    float D, eS;
     int ok, owner, last;
 };
 
@@ -3671,9 +3715,9 @@ __global__ void __launch_bounds__(kThreads, 2) sv_split_draw_kernel(SplitArgs a)
             slice_ctx<DT>(reinterpret_cast<unsigned char*>(rowblk + (c0 / kFastGroup) * 2), drow,
                           qrow, res, V, m, a.c2, u, c0, (int)min((long long)a.SC, nch - c0), s_row);
         if (res)
-            fast_search<DT, true, EXACT, true>(ds, d, f, fb.M, fb.tau, ss.Y0, ss.Q0, fb.D, fb.eS);
+            fast_search<DT, true, EXACT, true>(ds, d, f, fb.M, fb.tau, ss.Y0, ss.Q0, fb.c);
         else
-            fast_search<DT, false, EXACT, true>(ds, d, f, fb.M, fb.tau, ss.Y0, ss.Q0, fb.D, fb.eS);
+            fast_search<DT, false, EXACT, true>(ds, d, f, fb.M, fb.tau, ss.Y0, ss.Q0, fb.c);
         cert = ds.cert != 0 && ds.token >= 0;
         token = ds.token;
     }
@@ -3694,7 +3738,7 @@ __global__ void __launch_bounds__(kThreads, 2) sv_split_draw_kernel(SplitArgs a)
                 // when it is a positive number, else the row stream's.
                 const bool sok = fb.S > 0.0f && fb.S < INFINITY;
                 a.pS[j] = sok ? fb.S : s_row;
-                a.pD[j] = sok ? 2.0f * fb.eS + 8.0f * 5.96046448e-08f : 1.0f / 2048.0f;
+                a.pD[j] = sok ? 2.0f * fb.c.eS + 8.0f * 5.96046448e-08f : 1.0f / 2048.0f;
                 a.plist[j] = (uint32_t)b;
             }
         }

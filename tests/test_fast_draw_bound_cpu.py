@@ -8,8 +8,9 @@ relative error is only bounded (1.75e-7, checked exhaustively on the GPU)
 and whose exponent is otherwise exact to first order (l - m by TwoSum, the
 product's rounding and log2(e)/T's low part recovered),
 sums the positive elements' y and q without rounding error that matters, and
-keeps its token only when u C lies farther than an error bound D from both
-edges of the chosen bin.  This test restates that arithmetic in Python: float32
+keeps its token only when u C lies farther from each edge of the chosen bin
+than that edge's error bound (the errors before the edge weighed by 1 - u,
+those after it by u).  This test restates that arithmetic in Python: float32
 values by rounding float64 ones, the sums exactly (integers at a fine scale),
 the normaliser with an adversarial error of the size its pairwise chunk sums
 allow, and the exponential as the exact 2^a times (1 + s E) with the sign s of
@@ -134,15 +135,34 @@ def emulate_fast_draw(l, q, T, u, s_row, signs, d_scale=1.0, s_sign=1.0, exact=T
     tok = next(j for j in range(V) if yp[j] > 0 and C[j] > tau)
     lo = C[tok - 1] if tok > 0 else 0
     hi = C[tok]
-    Ppos = float(num(Cy[-1]) // S_int) * 2.0 ** -62
-    Qpos = Cq[-1] * 2.0 ** -62
+    # the certificate: each edge's own bound, the errors before the edge
+    # weighed by 1 - u and those after it by u
+    Ptot = num(Cy[-1]) // S_int
+    Qtot = Cq[-1]
+    Ppos = Ptot * 2.0 ** -62
     eS = K_EY + 3 * U * (max(0.0, 1.0 - Ppos) if exact else 1.0)
-    D = ((K_EY * Ppos + eS * Qpos + K_UND * qv[und].sum()
-          + (0.0 if exact else 3 * U * (Ppos + Qpos))) * 1.004 * 2.0 ** 62
-         + 2.0 ** 20 + 2.0 * (V / 8) + 64.0) * d_scale
-    um = max(u, 1.0 - u)
-    Dp = int(min(um * D + eS * 1.004 * (hi - lo) + 2.0, 4.0e18)) + 1
-    return tok, (tau - lo >= Dp and hi - tau > Dp)
+    kP = (K_EY + (0.0 if exact else 3 * U)) * 1.004
+    kQ = (0.0 if exact else 3 * U) * 1.004
+    Dc = K_UND * qv[und].sum() * 1.004 * 2.0 ** 62 + 2.0 ** 20 + 2.0 * (V / 8) + 64.0
+    uQ = (int(math.ldexp(float(np.float32(u)), 40)) * Qtot) >> 40
+    if exact:
+        cm = 0.0
+    else:
+        c0 = (tok // 8) * 8
+        cm = float(num(int(math.ldexp(_sum8(ypp[c0:c0 + 8]), ey))) // S_int
+                   + int(math.ldexp(_sum8(qpp[c0:c0 + 8]), 62)))
+
+    def edge(Yb, Qb):
+        Pb = num(Yb) // S_int
+        dp = (kP * ((1 - u) * Pb + u * max(Ptot - Pb, 0))
+              + kQ * ((1 - u) * Qb + u * max(Qtot - Qb, 0) + 2 * cm)
+              + eS * 1.004 * (abs(uQ - Qb) + 1 + (hi - lo))
+              + max(u, 1.0 - u) * Dc + 2.0) * d_scale
+        return int(min(dp, 4.0e18)) + 1
+
+    Dlo = edge(Cy[tok - 1], Cq[tok - 1]) if tok > 0 else edge(0, 0)
+    Dhi = edge(Cy[tok], Cq[tok])
+    return tok, (tau - lo >= Dlo and hi - tau > Dhi)
 
 
 def exact_cdf(orc, l, q, T):
