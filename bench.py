@@ -467,9 +467,22 @@ def main():
         pass
 
     # ---- timed region
+    # nvidia-smi samples every 200 ms, far longer than a short timed region: the
+    # same steps run untimed for half a second on each side of it (whole graphs
+    # in batches of about 50 ms), so that the samples around the K timed steps
+    # see this load.
+    n_load = copies * max(1, int(0.05 / max(est, 1e-7)) // copies)
+
+    def load_for(seconds):
+        t_end = time.perf_counter() + seconds
+        while time.perf_counter() < t_end:
+            with torch.cuda.stream(stream):
+                run_steps(n_load)
+            torch.cuda.synchronize(dev)
+
     sampler = ClockSampler(uuid)
     with sampler:
-        time.sleep(0.3)
+        load_for(0.5)
         if dist:
             dist.barrier()
         torch.cuda.synchronize(dev)
@@ -483,6 +496,7 @@ def main():
         if dist:
             dist.barrier()
         ms = ev0.elapsed_time(ev1)
+        load_for(0.5)
 
         # Each kernel of the one-call path timed alone: the fused kernel is the
         # whole verify (the loop above); the two-stage paths' row stream and draw
@@ -531,6 +545,8 @@ def main():
             stage_times = {rows_kname: stage_ms(rows_stage),
                            fin_name: stage_ms(finish_stage)}
     clocks = sampler.summary()
+    clocks["window"] = (f"the {K} timed steps with 0.5 s of the same steps untimed before and "
+                        f"after them, then the per-stage replays")
 
     ms = max_over_ranks(ms, dist, dev)
     value = job_rate(rows_per_step * K * world, ms)

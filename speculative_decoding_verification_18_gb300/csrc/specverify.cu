@@ -2765,13 +2765,21 @@ __global__ void sv_finish_greedy_kernel(const int32_t* __restrict__ x, const Row
     if (b >= B) return;
     RowRec* rr = recs[wi];
     int* xx = xs[wi];
+    // The lane's first record and token are loaded before the header, so the
+    // three loads are in flight together (none depends on another).
+    RowRec rec0{};
+    int x0 = 0;
+    if (lane <= k) {
+        rec0 = rows[(long long)b * (k + 1) + lane];
+        if (lane < k) x0 = x[(long long)b * k + lane];
+    }
     const uint32_t P = hdr->flat_ctas;
     const int vpr = (int)hdr->flat_vpr, per = (int)hdr->flat_per, rem = (int)hdr->flat_rem;
     const int V = (int)hdr->V;
     for (int i = lane; i <= k; i += 32) {
         const long long r = (long long)b * (k + 1) + i;
-        const int xi = i < k ? x[(long long)b * k + i] : 0;
-        RowRec rec = rows[r];
+        const int xi = i == lane ? x0 : (i < k ? x[(long long)b * k + i] : 0);
+        RowRec rec = i == lane ? rec0 : rows[r];
         if (i < k) xx[i] = xi;
         if (P) {
             const int c0 = flat_owner((int)r * vpr, per, rem);
@@ -3879,6 +3887,9 @@ __global__ void __launch_bounds__(kThreads, 2) sv_split_precise_kernel(SplitPrec
     __shared__ PreciseShared ps;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int grp = lane / kFastGroup, gl = lane % kFastGroup;
+    float* thi = reinterpret_cast<float*>(dyn);
+    float* tlo = thi + kExpTable;
+    load_exp_table(thi, tlo);  // (a constant table: read while the draw kernel ends)
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the list is complete
     const uint32_t cnt = min(*a.plist_count, (uint32_t)a.B);
     if (cnt == 0) return;
@@ -3893,9 +3904,6 @@ __global__ void __launch_bounds__(kThreads, 2) sv_split_precise_kernel(SplitPrec
     nsl = (nbr + slb - 1) / slb;
     const long long items = (long long)cnt * nsl;
     if (blockIdx.x >= items) return;
-    float* thi = reinterpret_cast<float*>(dyn);
-    float* tlo = thi + kExpTable;
-    load_exp_table(thi, tlo);
     cg::cluster_group cluster = cg::this_cluster();
     const int k = a.k, V = a.V;
     for (long long it = blockIdx.x; it < items; it += P) {
@@ -3995,6 +4003,7 @@ __global__ void __launch_bounds__(kThreads, 2) sv_split_precise_kernel(SplitPrec
         mine.Y = 0ull;
         mine.Q = 0ull;
         mine.S = ff{0.0f, 0.0f};
+        const uint32_t na = tid == 0 ? __ldcg(a.pambn + j) : 0u;  // (read with the items)
         if (tid < nsl) {
             const ulonglong2 v0 = __ldcg(reinterpret_cast<const ulonglong2*>(a.items + it0 + tid));
             const ulonglong2 v1 = __ldcg(reinterpret_cast<const ulonglong2*>(a.items + it0 + tid) + 1);
@@ -4023,7 +4032,6 @@ __global__ void __launch_bounds__(kThreads, 2) sv_split_precise_kernel(SplitPrec
                 ps.Y = Y;
                 ps.Q = Q;
                 ps.S = ff_normalize(St);
-                const uint32_t na = __ldcg(a.pambn + j);
                 ps.nb_amb = (int)min(na, (uint32_t)kAmbCap);
                 ps.fallback = na > (uint32_t)kAmbCap ||
                               !(fabsf(__fsub_rn(ps.S.hi, Sc)) <= 0.5f * dl * ps.S.hi);
